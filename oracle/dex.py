@@ -1,0 +1,363 @@
+"""Autoregressive decoding, DEX (Algorithm 1), DECS (Algorithm 2) and brute-force EAD.
+
+Restates "Depth Exploration for LLM Decoding" (arXiv 2606.29223) section 3 and
+Appendix C.1 step by step, with the readings below where the pages leave a step open.
+TEST INFRASTRUCTURE ONLY.
+
+Lattice (section 3.2, Figure 2).  Exploration tokens ETK_i live in a binary tree in
+heap order: the root ETK_0 is the stage-0 node of the commit position p_c; node i has a
+depth child D(i) = 2i+1 (same token position, next explorer) and a position child
+P(i) = 2i+2 (its candidate becomes the next position's token, restart at explorer 0).
+This matches "ETK_1 in the same slot chain, ETK_2 the first token of a new slot" and
+"state q materializes the first 2^q - 1 tokens".  The round at state q computes the
+2^q nodes of level q; the anchor path is D^k(0) = 2^k - 1, k = 0..N-1.
+
+Node semantics.  A node is the model evaluated on its token prefix: the committed
+tokens followed by the candidates of the P-parents on its path; its stage s is the
+number of trailing depth moves, and its candidate comes from the shared exit head at
+depth d_s (Appendix C.2), decoded by DECS.
+
+Readings taken where the pages are silent:
+* q after collapse = N - k* - 1: the survivors are the subtree of the new anchor
+  m = P(b_{k*}) = 2^(k*+1), created k*+1 rounds into the cycle, re-indexed
+  i -> i - m * 2^h (h = depth of i below m); fallback k* = N-1 leaves nothing, q = 0.
+* DECS masks Prior(i) = the tokens of the shallower nodes of i's slot chain, except
+  at the final-depth reference (stage N-1, which only the anchor reaches).
+* Sampling draws the Gumbel row of the node's absolute target position (see philox).
+* Greedy argmax breaks ties toward the lowest token id.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import Dict, List, Optional, Sequence, Tuple
+
+import numpy as np
+
+from . import analysis
+from .philox import gumbel_row
+
+
+# -------------------------------------------------------------------------------------
+# lattice indexing
+# -------------------------------------------------------------------------------------
+
+def parent(i: int) -> int:
+    return (i - 1) // 2
+
+
+def depth_child(i: int) -> int:
+    return 2 * i + 1
+
+
+def position_child(i: int) -> int:
+    return 2 * i + 2
+
+
+def is_depth_child(i: int) -> bool:
+    return i > 0 and i % 2 == 1
+
+
+def level(i: int) -> int:
+    return (i + 1).bit_length() - 1
+
+
+def level_nodes(q: int) -> range:
+    """The 2^q nodes created by the round at state q."""
+    return range(2 ** q - 1, 2 ** (q + 1) - 1)
+
+
+def stage(i: int) -> int:
+    """Explorer index of node i: number of trailing depth moves on its path."""
+    s = 0
+    while is_depth_child(i):
+        s += 1
+        i = parent(i)
+    return s
+
+
+def slot_root(i: int) -> int:
+    """r(i): first node of i's slot chain (the root or a position child)."""
+    while is_depth_child(i):
+        i = parent(i)
+    return i
+
+
+def prior_nodes(i: int) -> List[int]:
+    """Prior(i): shallower nodes of the same slot chain (Appendix C.1)."""
+    out = []
+    while is_depth_child(i):
+        i = parent(i)
+        out.append(i)
+    return out
+
+
+def branch_parents(i: int) -> List[int]:
+    """Nodes whose candidates extend i's prefix (the P-parents on the root->i path), root first."""
+    out = []
+    while i > 0:
+        p = parent(i)
+        if i % 2 == 0:
+            out.append(p)
+        i = p
+    return out[::-1]
+
+
+def anchor_node(k: int) -> int:
+    """b_k = D^k(0), the anchor-path node at explorer k."""
+    return 2 ** k - 1
+
+
+def subtree_remap(m: int, max_level: int) -> Dict[int, int]:
+    """Old -> new heap index for the subtree of m restricted to levels <= max_level.
+
+    Closed form of the collapse re-indexing: i -> i - m * 2^h, h = level(i) - level(m).
+    """
+    out = {}
+    frontier = [m]
+    while frontier:
+        nxt = []
+        for i in frontier:
+            if level(i) > max_level:
+                continue
+            h = level(i) - level(m)
+            out[i] = i - m * 2 ** h
+            nxt += [depth_child(i), position_child(i)]
+        frontier = nxt
+    return out
+
+
+# -------------------------------------------------------------------------------------
+# decoding rule and DECS
+# -------------------------------------------------------------------------------------
+
+@dataclass(frozen=True)
+class Rule:
+    """Final-depth decoding rule R: greedy, or Gumbel-max sampling at temperature tau."""
+    sample: bool = False
+    tau: float = 1.0
+    seed: int = 0
+
+
+def first_argmax(score: np.ndarray) -> int:
+    """argmax with ties broken toward the lowest index."""
+    return int(np.flatnonzero(score == score.max())[0])
+
+
+def decision_scores(logits: np.ndarray, rule: Rule, seq: int, target_pos: int) -> np.ndarray:
+    """The scores whose argmax is the token: logits (greedy) or logits / tau + G (sampling)."""
+    if not rule.sample:
+        return logits
+    return logits / rule.tau + gumbel_row(rule.seed, seq, target_pos, logits.shape[-1])
+
+
+def margin(score: np.ndarray) -> float:
+    """Top-1 minus top-2 of the decision scores (ignoring masked -inf entries)."""
+    finite = np.sort(score[np.isfinite(score)])
+    return float(finite[-1] - finite[-2]) if finite.size >= 2 else float("inf")
+
+
+def decs(logits: np.ndarray, i: int, B: Dict[int, int], q: int, q_max: int, i_ref: int,
+         rule: Rule, seq: int, target_pos: int, enabled: bool = True) -> Tuple[int, float, List[int]]:
+    """Algorithm 2 (Depth-Coupled Sampling) for node i.
+
+    Returns (token, decision margin, masked token ids).  With ``enabled=False`` no token
+    is masked ("vanilla" independent decoding, section 4.1 ablation).
+    """
+    A = [B[a] for a in prior_nodes(i) if B.get(a) is not None]        # prior proposals
+    if (q == q_max and i == i_ref) or not enabled:
+        A = []                                                        # keep the reference
+    z = np.array(logits, dtype=np.float64, copy=True)
+    for v in A:
+        z[v] = -np.inf
+    score = decision_scores(z, rule, seq, target_pos)
+    y = first_argmax(score)
+    B[i] = y
+    return y, margin(score), sorted(set(A))
+
+
+# -------------------------------------------------------------------------------------
+# autoregressive decoding (the lossless target) and brute-force EAD
+# -------------------------------------------------------------------------------------
+
+@dataclass
+class ARResult:
+    tokens: List[int]
+    logits: List[np.ndarray]                       # final-depth logits per generated token
+    margins: List[float]
+    depth_candidates: Optional[List[List[int]]] = None   # [t][l-1]: candidate at depth l
+
+
+def ar_generate(model, prompt: Sequence[int], T: int, rule: Rule = Rule(), seq: int = 0,
+                record_depths: bool = False, force: Optional[Sequence[int]] = None) -> ARResult:
+    """Standard AR decoding of T tokens (section 2.1): every token through all L layers.
+
+    Prompt positions 0..P-2 are prefilled; the last prompt token at position P-1 yields the
+    first new token (position P).  With ``force`` the given tokens are appended instead of
+    the decoded ones (teacher forcing: scores a token stream produced elsewhere).  With
+    ``record_depths`` the candidate of every depth l in [L] under the same rule is kept.
+    """
+    P = len(prompt)
+    cache = model.new_cache(P + T + 1)
+    if P > 1:
+        model.forward(prompt[:-1], 0, cache)
+    last, pos = int(prompt[-1]), P - 1
+    out = ARResult([], [], [], [] if record_depths else None)
+    for t in range(T):
+        hist = model.forward([last], pos, cache, keep_depths=True)
+        z = model.exit_logits(hist[-1])[0]
+        score = decision_scores(z, rule, seq, pos + 1)
+        y = first_argmax(score)
+        out.logits.append(z)
+        out.margins.append(margin(score))
+        if record_depths:
+            cands = []
+            for l in range(model.L):
+                zl = model.exit_logits(hist[l])[0]
+                cands.append(first_argmax(decision_scores(zl, rule, seq, pos + 1)))
+            out.depth_candidates.append(cands)
+        if force is not None:
+            y = int(force[t])
+        out.tokens.append(y)
+        last, pos = y, pos + 1
+    return out
+
+
+def ead_profile(ar: ARResult):
+    """Brute-force Def. 1: Omega(t, l) = [candidate at depth l == final-depth token].
+
+    Returns (omega rows, EAD(t) list, stable EAD(t) list).
+    """
+    omegas, eads, stabs = [], [], []
+    for t, y in enumerate(ar.tokens):
+        omega = [1 if c == y else 0 for c in ar.depth_candidates[t]]
+        omegas.append(omega)
+        eads.append(analysis.ead(omega))
+        stabs.append(analysis.ead_stable(omega))
+    return omegas, eads, stabs
+
+
+# -------------------------------------------------------------------------------------
+# Algorithm 1: Depth Exploration Decoding
+# -------------------------------------------------------------------------------------
+
+@dataclass
+class NodeRecord:
+    """One lattice node's evaluation (for comparison with the GPU library)."""
+    round: int
+    q: int
+    node: int
+    stage: int
+    plen: int
+    target_pos: int
+    token: int
+    margin: float
+    masked: List[int]
+    logits: Optional[np.ndarray] = None
+
+
+@dataclass
+class CommitRecord:
+    token: int
+    kstar: int
+    rounds: int          # rounds since the previous commit (k*(t-1) + 1 after the first)
+    p_c: int             # commit position
+
+
+@dataclass
+class DEXResult:
+    tokens: List[int]
+    commits: List[CommitRecord]
+    nodes: List[NodeRecord]
+    rounds: int
+    layer_passes: int    # sum over rounds of d_{deepest live stage}: layers one GPU streams
+    node_layers: int     # sum over nodes of the layers of their stage (compute work)
+
+    def depth_charges(self, X: Sequence[int]) -> List[int]:
+        """d_{k*(t)} for every committed token: the depth-side charge (Eq. 12's W)."""
+        return [X[c.kstar] for c in self.commits]
+
+
+def dex_generate(model, prompt: Sequence[int], X: Sequence[int], T: int, rule: Rule = Rule(),
+                 use_decs: bool = True, seq: int = 0, keep_logits: bool = False) -> DEXResult:
+    """Algorithm 1 over one sequence; returns the committed tokens Y and a full trace."""
+    N = len(X)
+    assert X[-1] == model.L and list(X) == sorted(set(X))
+    P = len(prompt)
+    cache = model.new_cache(P + T + N + 1)
+    committed = [int(t) for t in prompt]
+    # init(x, {E_k}): committed KV for positions 0..P-2; the last prompt token is the root input.
+    if P > 1:
+        model.forward(committed[:-1], 0, cache)
+    anchor_hist = model.forward([committed[-1]], P - 1, cache, keep_depths=True)
+
+    Y: List[int] = []
+    B: Dict[int, int] = {}
+    q = 0
+    res = DEXResult([], [], [], 0, 0, 0)
+    rounds_since_commit = 0
+    q_max, i_ref = N - 1, anchor_node(N - 1)
+    while len(Y) < T:
+        p_c = len(committed)
+        # expand: H_q = hidden states of the level-q nodes at their stage boundaries
+        H = {}
+        for i in level_nodes(q):
+            s = stage(i)
+            path = branch_parents(i)
+            if not path:                                  # anchor path: committed prefix
+                H[i] = anchor_hist[X[s] - 1]
+            else:                                         # branch prefix: committed + candidates
+                toks = [B[a] for a in path]
+                H[i] = model.forward(toks, p_c, cache, depth=X[s])[-1:]
+            res.node_layers += X[s] - (X[s - 1] if s > 0 else 0)
+        res.layer_passes += X[q]
+        res.rounds += 1
+        rounds_since_commit += 1
+        # DECS, then insert into the explore buffer
+        Z = {}
+        for i in level_nodes(q):
+            z = model.exit_logits(H[i])[0]
+            plen = len(branch_parents(i))
+            y, mg, masked = decs(z, i, dict(B), q, q_max, i_ref, rule, seq, p_c + plen,
+                                 enabled=use_decs)
+            Z[i] = y
+            res.nodes.append(NodeRecord(res.rounds - 1, q, i, stage(i), plen, p_c + plen, y, mg,
+                                        masked, z if keep_logits else None))
+        B.update(Z)
+        if q == N - 1:                                    # ReachFinalDepth
+            y, kstar = validate_and_commit(B, N)
+            Y.append(y)
+            res.commits.append(CommitRecord(y, kstar, rounds_since_commit, p_c))
+            rounds_since_commit = 0
+            if len(Y) >= T:                               # stop(Y)
+                break
+            B, q = collapse(B, N, kstar)
+            committed.append(y)
+            anchor_hist = model.forward([y], p_c, cache, keep_depths=True)
+        else:
+            q = q + 1                                     # advance(q)
+    res.tokens = Y
+    return res
+
+
+def validate_and_commit(B: Dict[int, int], N: int) -> Tuple[int, int]:
+    """Section 3.2 commit: y = u_{N-1}; b = shallowest anchor branch with u_k = y, else b_{N-1}."""
+    u = [B[anchor_node(k)] for k in range(N)]
+    y = u[N - 1]
+    for k in range(N - 1):
+        if u[k] == y:
+            return y, k
+    return y, N - 1
+
+
+def collapse(B: Dict[int, int], N: int, kstar: int) -> Tuple[Dict[int, int], int]:
+    """Keep the nodes whose prefix is the new committed prefix; return (B', q').
+
+    The survivors are the subtree of m = P(b_{k*}); every other node's prefix contains a
+    rejected candidate.  With the fallback branch (k* = N-1) nothing survives.
+    """
+    if kstar == N - 1:
+        return {}, 0
+    m = position_child(anchor_node(kstar))
+    remap = subtree_remap(m, N - 1)
+    newB = {new: B[old] for old, new in remap.items() if old in B}
+    return newB, N - kstar - 1

@@ -1,0 +1,135 @@
+"""Pins for Algorithm 1 / Algorithm 2 in oracle/dex.py on tiny models.
+
+What the paper fixes: DEX commits exactly the AR stream (section 3.2, lossless
+invariant); the committed token is the unmasked final-depth token (section 3.3,
+Appendix C.1); commit selects the shallowest matching anchor branch (section 3.2);
+the per-token charge relates to EAD as in Def. 1-5 / Prop. 6.
+"""
+import numpy as np
+import pytest
+
+from conftest import tiny_model
+from oracle import analysis as A
+from oracle import dex
+
+import dex_inputs as di
+
+PROMPT = di.gen_prompts(di.TINY, 1, 32)[0].tolist()
+VARIANTS = [(0.1, True), (0.3, False), (1.0, False)]
+
+
+def _run(alpha, tied, X, T, rule, use_decs=True, prompt=PROMPT, n_layers=8):
+    _, _, m = tiny_model(alpha, tied, n_layers)
+    ar = dex.ar_generate(m, prompt, T, rule=rule, record_depths=True)
+    r = dex.dex_generate(m, prompt, X, T, rule=rule, use_decs=use_decs)
+    return m, ar, r
+
+
+@pytest.mark.parametrize("alpha,tied", VARIANTS)
+@pytest.mark.parametrize("X", [[2, 4, 6, 8], [4, 8], [1, 2, 3, 4, 5, 6, 7, 8], [8], [1, 8]])
+@pytest.mark.parametrize("sample", [False, True])
+def test_dex_is_lossless(alpha, tied, X, sample):
+    rule = dex.Rule(sample=sample, tau=0.7, seed=2)
+    m, ar, r = _run(alpha, tied, X, 12, rule)
+    assert r.tokens == ar.tokens
+    N = len(X)
+    for c, y in zip(r.commits, ar.tokens):
+        assert c.token == y
+    # the final-depth reference is never masked; only the anchor reaches stage N-1
+    for nd in r.nodes:
+        if nd.stage == N - 1:
+            assert nd.node == dex.anchor_node(N - 1) and nd.masked == []
+
+
+def test_dex_lossless_without_decs_and_other_prompts():
+    for seed in (3, 4):
+        prompt = di.uniform_ids(9, 4096, seed, 99).tolist()
+        for use_decs in (False, True):
+            _, ar, r = _run(1.0, False, [2, 4, 6, 8], 10, dex.Rule(), use_decs, prompt)
+            assert r.tokens == ar.tokens
+
+
+@pytest.mark.parametrize("sample", [False, True])
+def test_ead_and_charge_relations(sample):
+    """c14: (1) vanilla greedy k* is the first explored depth whose candidate is y;
+    (2) d_{k*} <= ceil(EAD^stab)_X always; (3) equality without non-stable early hits;
+    (4) 0 <= W_X - EAD^stab <= Delta(X)."""
+    rule = dex.Rule(sample=sample, tau=0.7, seed=5)
+    for alpha, tied in VARIANTS[1:]:
+        X = [2, 4, 6, 8]
+        L = 8
+        m, ar, vanilla = _run(alpha, tied, X, 16, rule, use_decs=False)
+        decs = dex.dex_generate(m, PROMPT, X, 16, rule=rule, use_decs=True)
+        omegas, eads, stabs = dex.ead_profile(ar)
+        dv, dd = vanilla.depth_charges(X), decs.depth_charges(X)
+        for t in range(16):
+            first_hit = min(d for d in X if omegas[t][d - 1])
+            assert dv[t] == first_hit                                         # (1)
+            W = A.exploration_workload(stabs[t], X)
+            assert dd[t] <= dv[t] <= W                                        # (2) and DECS never later
+            if not any(omegas[t][d - 1] for d in X if d < W):
+                assert dv[t] == W                                             # (3)
+            assert 0 <= W - stabs[t] <= A.resolution(X, L)                   # (4)
+            assert eads[t] <= stabs[t]
+
+
+def test_decs_diversifies_slot_chains():
+    _, _, m = tiny_model(1.0, False)
+    r = dex.dex_generate(m, PROMPT, [1, 2, 3, 4, 5, 6, 7, 8], 8, use_decs=True)
+    N = 8
+    by_round = {}
+    for nd in r.nodes:
+        by_round.setdefault(nd.round, {})[nd.node] = nd
+    checked = 0
+    for rnd, nodes in by_round.items():
+        for i, nd in nodes.items():
+            if nd.stage == N - 1:
+                continue
+            # masked set = tokens of the shallower members of the slot chain, and the
+            # decoded token avoids them
+            assert nd.token not in nd.masked
+            assert len(nd.masked) <= nd.stage
+            checked += len(nd.masked)
+    assert checked > 0
+
+
+def test_final_token_equals_unmasked_gumbel_max():
+    rule = dex.Rule(sample=True, tau=0.7, seed=9)
+    _, _, m = tiny_model(1.0, False)
+    r = dex.dex_generate(m, PROMPT, [2, 4, 6, 8], 6, rule=rule, keep_logits=True)
+    n_ref = 0
+    for nd in r.nodes:
+        if nd.stage == 3:
+            score = nd.logits / rule.tau + dex.gumbel_row(rule.seed, 0, nd.target_pos, nd.logits.size)
+            assert nd.token == int(np.argmax(score))
+            n_ref += 1
+    assert n_ref == 6
+
+
+def test_rounds_per_commit_and_layer_accounting():
+    X = [2, 4, 6, 8]
+    N = len(X)
+    _, _, m = tiny_model(0.3, False)
+    r = dex.dex_generate(m, PROMPT, X, 20)
+    assert r.commits[0].rounds == N                      # first cycle starts from q = 0
+    for prev, cur in zip(r.commits, r.commits[1:]):
+        assert cur.rounds == prev.kstar + 1              # q' = N - k* - 1
+    assert r.rounds == sum(c.rounds for c in r.commits)
+    per_round_nodes = {}
+    for nd in r.nodes:
+        per_round_nodes.setdefault(nd.round, []).append(nd)
+    passes, node_layers = 0, 0
+    for rnd, nodes in per_round_nodes.items():
+        q = nodes[0].q
+        assert len(nodes) == 2 ** q
+        passes += X[q]                                   # a round at state q streams layers 1..d_q
+        node_layers += sum(X[n.stage] - (X[n.stage - 1] if n.stage else 0) for n in nodes)
+    assert r.layer_passes == passes and r.node_layers == node_layers
+
+
+def test_degenerate_tiny_repeats_last_token():
+    """alpha = 0.1 with the tied head: the input token's own logit dominates, so greedy
+    repeats the last prompt token and every commit hits at the shallowest depth."""
+    _, ar, r = _run(0.1, True, [2, 4, 6, 8], 12, dex.Rule())
+    assert set(ar.tokens) == {PROMPT[-1]}
+    assert all(c.kstar == 0 for c in r.commits)
