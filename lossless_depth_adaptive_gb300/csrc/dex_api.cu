@@ -1,0 +1,998 @@
+// C ABI of the DEX library (include/dex.h): handle life cycle, prefill, DEX / AR rounds,
+// statistics, and the isolated exit-head and collapse entry points.
+//
+// A round ("Depth Exploration for LLM Decoding", Algorithm 1, one loop iteration):
+//   plan (host lattice FSM) -> upload node tables -> pending collapse copies ->
+//   stage-input assembly -> for each live stage s, layers (d_{s-1}, d_s] over the stage's
+//   nodes (QKV + RoPE + KV write, lattice attention, O + residual, gate/up + SwiGLU,
+//   down + residual) -> exit head + DECS over every node -> one device-to-host read of
+//   the tokens -> insert / validate_and_commit / collapse on the host.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <string.h>
+
+#include <algorithm>
+#include <chrono>
+#include <memory>
+#include <new>
+#include <vector>
+
+#include "../../include/dex.h"
+#include "kernels.h"
+#include "lattice.h"
+
+using bf16 = __nv_bfloat16;
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int get_encoder() {
+  if (g_encode) return DEX_OK;
+  cudaDriverEntryPointQueryResult q;
+  void* fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return DEX_ECUDA;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return DEX_OK;
+}
+
+// 2-D bf16 tensor map over a row-major [rows][cols] matrix, box {64 cols, box_rows},
+// 128-byte swizzle, zero fill out of bounds.
+int encode_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || (cols * 2) % 16) return DEX_EINVAL;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DEX_OK : DEX_EINVAL;
+}
+
+// Fixed split-K factor of a weight shape: about four CTAs per SM in total, at least
+// eight 64-wide k-blocks (128 KB of weights) per CTA.  Depends on the shape only.
+int splits_for(int n_tiles, int kblocks, int n_sm) {
+  int s = static_cast<int>(lround(4.0 * n_sm / n_tiles));
+  s = std::min(s, std::max(1, kblocks / 8));
+  return std::max(1, s);
+}
+
+int pow2_at_least(int x) {
+  int p = 32;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+}  // namespace
+
+struct dex_handle {
+  // model
+  int L = 0, d = 0, H = 0, KVH = 0, hd = 0, dff = 0, V = 0;
+  float eps = 0, theta = 0;
+  const bf16* embed = nullptr;
+  const bf16* final_norm = nullptr;
+  const bf16* lm_head = nullptr;
+  std::vector<const bf16*> w;   // [L][9]
+  std::vector<int> X;
+  int N = 0;
+  dex_decode_cfg cfg = {};
+  cudaStream_t st = nullptr;
+  int n_sm = 0;
+  std::unique_ptr<dex::Lattice> lat, lat_ar;
+  std::vector<int> mode;                 // per sequence: 0 idle, 1 DEX, 2 AR
+  std::vector<int> n_done;
+  std::vector<dex_copy_job> pending_jobs, pending_jobs_ar;
+  int rows_cap = 0, n_slots = 0, max_groups = 0, hrows = 0;
+  // device buffers
+  std::vector<void*> allocs;
+  bf16 *kv_commit = nullptr, *kv_pool = nullptr, *hb = nullptr, *exit_hb = nullptr, *attn_out = nullptr,
+       *act = nullptr;
+  float *hidden = nullptr, *ssq = nullptr, *exit_ssq = nullptr, *q = nullptr, *partial = nullptr,
+        *attn_part = nullptr, *logits_dbg = nullptr;
+  int32_t *counters = nullptr, *attn_counters = nullptr, *err = nullptr;
+  float2* rope = nullptr;
+  unsigned long long* best = nullptr;
+  const bf16** d_attn_norms = nullptr;
+  uint8_t* d_plan = nullptr;
+  size_t plan_cap = 0;
+  // pinned host
+  uint8_t* h_plan = nullptr;
+  unsigned long long* h_best = nullptr;   // rows_cap + 1 (last = error flag)
+  // tensor maps
+  std::vector<CUtensorMap> tm_q, tm_k, tm_v, tm_o, tm_g, tm_u, tm_d;
+  CUtensorMap tm_lm;
+  CUtensorMap tm_hb[17], tm_attn[17], tm_act[17], tm_exit[17];
+  int S_qkv = 1, S_o = 1, S_gu = 1, S_d = 1, S_lm = 1;
+  // bookkeeping
+  dex_stats stats = {};
+  int timing = 0;
+  std::vector<dex_plan_node> last_plan;
+  std::vector<int32_t> last_tokens;
+  std::vector<cudaEvent_t> ev_pool;
+  size_t ev_used = 0;
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> gemm_events;
+  bool broken = false;
+};
+
+namespace {
+
+int cuda_fail(dex_handle* h, cudaError_t e) {
+  if (e == cudaSuccess) return DEX_OK;
+  if (h) h->broken = true;
+  return DEX_ECUDA;
+}
+
+template <typename T>
+int dalloc(dex_handle* h, T** p, size_t bytes) {
+  void* v = nullptr;
+  if (cudaMalloc(&v, bytes ? bytes : 16) != cudaSuccess) return DEX_ENOMEM;
+  h->allocs.push_back(v);
+  *p = reinterpret_cast<T*>(v);
+  return DEX_OK;
+}
+
+cudaEvent_t next_event(dex_handle* h) {
+  if (h->ev_used == h->ev_pool.size()) {
+    cudaEvent_t e;
+    cudaEventCreate(&e);
+    h->ev_pool.push_back(e);
+  }
+  return h->ev_pool[h->ev_used++];
+}
+
+const bf16* W(const dex_handle* h, int layer, int j) { return h->w[static_cast<size_t>(layer) * 9 + j]; }
+
+// Per-round description of the node batch, built on the host and uploaded once.
+struct RoundTables {
+  std::vector<dex::DevNode> nodes;
+  std::vector<int32_t> tails, priors;
+  std::vector<dex::AttnItem> items;
+  std::vector<int> item_begin;          // per stage: first item, size N+1
+  std::vector<int> stage_off;           // per stage: first row, size N+1
+  std::vector<dex_copy_job> jobs;
+};
+
+struct Uploaded {
+  dex::DevNode* nodes;
+  int32_t *tails, *priors;
+  dex::AttnItem* items;
+  dex::CopyJob* jobs;
+};
+
+int upload(dex_handle* h, const RoundTables& t, Uploaded* u) {
+  size_t off = 0;
+  auto place = [&](size_t bytes) {
+    size_t o = (off + 255) & ~size_t(255);
+    off = o + bytes;
+    return o;
+  };
+  const size_t o_nodes = place(t.nodes.size() * sizeof(dex::DevNode));
+  const size_t o_tails = place(t.tails.size() * 4 + 4);
+  const size_t o_priors = place(t.priors.size() * 4 + 4);
+  const size_t o_items = place(t.items.size() * sizeof(dex::AttnItem));
+  const size_t o_jobs = place(t.jobs.size() * sizeof(dex::CopyJob));
+  if (off > h->plan_cap) return DEX_ECAPACITY;
+  memcpy(h->h_plan + o_nodes, t.nodes.data(), t.nodes.size() * sizeof(dex::DevNode));
+  memcpy(h->h_plan + o_tails, t.tails.data(), t.tails.size() * 4);
+  memcpy(h->h_plan + o_priors, t.priors.data(), t.priors.size() * 4);
+  memcpy(h->h_plan + o_items, t.items.data(), t.items.size() * sizeof(dex::AttnItem));
+  memcpy(h->h_plan + o_jobs, t.jobs.data(), t.jobs.size() * sizeof(dex::CopyJob));
+  if (cudaMemcpyAsync(h->d_plan, h->h_plan, off, cudaMemcpyHostToDevice, h->st) != cudaSuccess)
+    return cuda_fail(h, cudaGetLastError());
+  h->stats.h2d_bytes += static_cast<int64_t>(off);
+  u->nodes = reinterpret_cast<dex::DevNode*>(h->d_plan + o_nodes);
+  u->tails = reinterpret_cast<int32_t*>(h->d_plan + o_tails);
+  u->priors = reinterpret_cast<int32_t*>(h->d_plan + o_priors);
+  u->items = reinterpret_cast<dex::AttnItem*>(h->d_plan + o_items);
+  u->jobs = reinterpret_cast<dex::CopyJob*>(h->d_plan + o_jobs);
+  return DEX_OK;
+}
+
+dex::GemmArgs base_args(dex_handle* h) {
+  dex::GemmArgs a = {};
+  a.err = h->err;
+  a.d = h->d;
+  a.H = h->H;
+  a.KVH = h->KVH;
+  a.hd = h->hd;
+  a.L = h->L;
+  a.d_ff = h->dff;
+  a.vocab = h->V;
+  a.max_ctx = h->cfg.max_ctx;
+  a.n_slots = h->n_slots;
+  a.eps = h->eps;
+  a.partial = h->partial;
+  a.counters = h->counters;
+  a.stages = 4;
+  a.evict_first = 1;
+  return a;
+}
+
+// Launch one GEMM over rows [row0, row0 + n) in slices of at most 256 node columns.
+int gemm(dex_handle* h, int epi, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& a2,
+         const CUtensorMap* bmaps, dex::GemmArgs a, int row0, int n, int64_t weight_bytes, int64_t act_bytes_per_row) {
+  for (int r = row0; r < row0 + n; r += 256) {
+    const int nn = std::min(256, row0 + n - r);
+    a.n = nn;
+    a.nt = (nn + 15) & ~15;
+    a.b_row0 = r;
+    a.tmem_cols = pow2_at_least(a.nt);
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (h->timing >= 2) {
+      e0 = next_event(h);
+      e1 = next_event(h);
+      cudaEventRecord(e0, h->st);
+    }
+    cudaError_t e = dex::launch_gemm(epi, a0, a1, a2, bmaps[a.nt / 16], a, h->st, true);
+    if (e != cudaSuccess) return cuda_fail(h, e);
+    if (h->timing >= 2) {
+      cudaEventRecord(e1, h->st);
+      h->gemm_events.push_back({e0, e1});
+    }
+    h->stats.kernel_launches++;
+    h->stats.gemm_launches++;
+    h->stats.gemm_bytes += weight_bytes + act_bytes_per_row * nn;
+  }
+  return DEX_OK;
+}
+
+// The decoder layers of one stage batch: rows [off, off + n), layers [l0, l1).
+int run_layers(dex_handle* h, const Uploaded& u, int off, int n, int l0, int l1, int item0, int n_items,
+               int max_groups_launch, bool with_exit) {
+  const int qd = h->H * h->hd, kvd = h->KVH * h->hd;
+  const int64_t d = h->d;
+  for (int l = l0; l < l1; ++l) {
+    dex::GemmArgs a = base_args(h);
+    a.nodes = u.nodes;
+    a.layer = l;
+    // QKV + RoPE + KV write
+    a.kblocks = (h->d + 63) / 64;
+    a.splits = h->S_qkv;
+    a.src_tiles0 = qd / 128;
+    a.src_tiles1 = kvd / 128;
+    a.n_tiles = (qd + 2 * kvd) / 128;
+    a.ssq_in = h->ssq;
+    a.q_out = h->q;
+    a.kv_commit = h->kv_commit;
+    a.kv_pool = h->kv_pool;
+    a.rope = h->rope;
+    int rc = gemm(h, dex::EPI_QKV, h->tm_q[l], h->tm_k[l], h->tm_v[l], h->tm_hb, a, off, n,
+                  static_cast<int64_t>(qd + 2 * kvd) * d * 2, d * 2 + qd * 4 + 2 * kvd * 2);
+    if (rc) return rc;
+    // lattice attention
+    dex::AttnArgs at = {};
+    at.nodes = u.nodes;
+    at.items = u.items + item0;
+    at.tails = u.tails;
+    at.q = h->q;
+    at.kv_commit = h->kv_commit;
+    at.kv_pool = h->kv_pool;
+    at.out = h->attn_out;
+    at.part = h->attn_part;
+    at.counters = h->attn_counters;
+    at.err = h->err;
+    at.layer = l;
+    at.H = h->H;
+    at.KVH = h->KVH;
+    at.hd = h->hd;
+    at.L = h->L;
+    at.max_ctx = h->cfg.max_ctx;
+    at.n_slots = h->n_slots;
+    at.max_groups = h->max_groups;
+    at.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(h->hd)));
+    cudaError_t ce = dex::launch_attention(at, n_items, max_groups_launch, h->st, true);
+    if (ce != cudaSuccess) return cuda_fail(h, ce);
+    h->stats.kernel_launches++;
+    // O projection + residual
+    a = base_args(h);
+    a.nodes = u.nodes;
+    a.layer = l;
+    a.kblocks = (qd + 63) / 64;
+    a.splits = h->S_o;
+    a.n_tiles = h->d / 128;
+    a.src_tiles0 = a.n_tiles;
+    a.hidden = h->hidden;
+    a.hb_out = h->hb;
+    a.g_next = W(h, l, 5);
+    a.ssq_out = h->ssq;
+    rc = gemm(h, dex::EPI_RESID, h->tm_o[l], h->tm_o[l], h->tm_o[l], h->tm_attn, a, off, n,
+              static_cast<int64_t>(qd) * d * 2, qd * 2 + d * 8 + d * 2);
+    if (rc) return rc;
+    // gate/up + SwiGLU
+    a = base_args(h);
+    a.nodes = u.nodes;
+    a.layer = l;
+    a.kblocks = (h->d + 63) / 64;
+    a.splits = h->S_gu;
+    a.n_tiles = (h->dff + 63) / 64;
+    a.src_tiles0 = a.n_tiles;
+    a.ssq_in = h->ssq;
+    a.act_out = h->act;
+    rc = gemm(h, dex::EPI_SWIGLU, h->tm_g[l], h->tm_u[l], h->tm_u[l], h->tm_hb, a, off, n,
+              static_cast<int64_t>(2) * h->dff * d * 2, d * 2 + h->dff * 2);
+    if (rc) return rc;
+    // down + residual (+ exit-head input at the stage boundary)
+    a = base_args(h);
+    a.nodes = u.nodes;
+    a.layer = l;
+    a.kblocks = (h->dff + 63) / 64;
+    a.splits = h->S_d;
+    a.n_tiles = h->d / 128;
+    a.src_tiles0 = a.n_tiles;
+    a.hidden = h->hidden;
+    const bool last = (l == l1 - 1);
+    a.hb_out = (!last && l + 1 < h->L) ? h->hb : nullptr;
+    a.g_next = (l + 1 < h->L) ? W(h, l + 1, 0) : nullptr;
+    a.ssq_out = h->ssq;
+    a.stage_end = (last && with_exit) ? 1 : 0;
+    a.exit_hb = h->exit_hb;
+    a.g_final = h->final_norm;
+    a.exit_ssq = h->exit_ssq;
+    rc = gemm(h, dex::EPI_RESID, h->tm_d[l], h->tm_d[l], h->tm_d[l], h->tm_act, a, off, n,
+              static_cast<int64_t>(h->dff) * d * 2, h->dff * 2 + d * 8 + d * 4);
+    if (rc) return rc;
+  }
+  return DEX_OK;
+}
+
+int check_device_error(dex_handle* h, int32_t flag) {
+  if (flag == 0) return DEX_OK;
+  cudaMemsetAsync(h->err, 0, sizeof(int32_t), h->st);
+  return flag == dex::DEV_BAD_INDEX ? DEX_ECUDA : DEX_ETIMEOUT;
+}
+
+// One round on lattice `lat` (DEX or the single-stage AR lattice).
+int run_round(dex_handle* h, dex::Lattice* lat, std::vector<dex_copy_job>* pending, int32_t* out_tokens,
+              int32_t* n_committed) {
+  if (h->broken) return DEX_ECUDA;
+  auto t_host0 = std::chrono::steady_clock::now();
+  std::vector<dex_plan_node> plan;
+  const int n = lat->plan(&plan);
+  if (n < 0) return DEX_ECAPACITY;
+  if (n == 0) return DEX_ESTATE;
+  const int NS = lat->N();
+  const std::vector<int>& X = lat->X();
+  RoundTables t;
+  t.stage_off.assign(NS + 1, 0);
+  t.item_begin.assign(NS + 1, 0);
+  int max_stage = 0;
+  for (const auto& p : plan) {
+    if (p.target_pos >= h->cfg.max_ctx) return DEX_ECAPACITY;
+    t.stage_off[p.stage + 1]++;
+    max_stage = std::max(max_stage, p.stage);
+  }
+  for (int s = 0; s < NS; ++s) t.stage_off[s + 1] += t.stage_off[s];
+  for (int k = 0; k < n; ++k) {
+    const auto& p = plan[k];
+    dex::DevNode dn = {};
+    dn.seq = p.seq;
+    dn.pos = p.pos;
+    dn.c_end = p.c_end;
+    dn.slot = p.slot;
+    dn.hrow = p.seq * h->n_slots + p.slot;
+    dn.kv_commit = p.kv_commit;
+    dn.token = p.token;
+    dn.first_layer = p.stage > 0 ? X[p.stage - 1] : 0;
+    dn.tail_off = static_cast<int32_t>(t.tails.size());
+    dn.n_tail = p.n_tail;
+    for (int i = 0; i < p.n_tail; ++i) t.tails.push_back(p.tail[i]);
+    dn.target_pos = p.target_pos;
+    dn.unmasked = p.unmasked;
+    dn.prior_off = static_cast<int32_t>(t.priors.size());
+    dn.n_prior = p.n_prior;
+    for (int i = 0; i < p.n_prior; ++i) t.priors.push_back(p.prior[i]);
+    t.nodes.push_back(dn);
+  }
+  // attention items: per stage, one per sequence's contiguous rows
+  int max_groups_launch = 1;
+  for (int s = 0; s < NS; ++s) {
+    t.item_begin[s] = static_cast<int>(t.items.size());
+    for (int k = t.stage_off[s]; k < t.stage_off[s + 1];) {
+      int e = k;
+      dex::AttnItem it = {};
+      it.seq = plan[k].seq;
+      it.row_begin = k;
+      it.max_pos = 0;
+      it.max_cend = 0;
+      while (e < t.stage_off[s + 1] && plan[e].seq == it.seq) {
+        it.max_pos = std::max(it.max_pos, plan[e].pos);
+        it.max_cend = std::max(it.max_cend, plan[e].c_end);
+        ++e;
+      }
+      it.row_end = e;
+      it.n_groups = it.max_pos / 128 + 1;
+      it.counter = static_cast<int>(t.items.size());
+      max_groups_launch = std::max(max_groups_launch, it.n_groups);
+      t.items.push_back(it);
+      k = e;
+    }
+  }
+  t.item_begin[NS] = static_cast<int>(t.items.size());
+  t.jobs = *pending;
+  const double host_plan_ms =
+      std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t_host0).count();
+
+  Uploaded u;
+  int rc = upload(h, t, &u);
+  if (rc) return rc;
+  cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
+  if (h->timing >= 1)
+    for (auto& e : ev) e = next_event(h);
+  if (ev[0]) cudaEventRecord(ev[0], h->st);
+  if (!t.jobs.empty()) {
+    dex::CollapseArgs ca = {};
+    ca.jobs = u.jobs;
+    ca.n_jobs = static_cast<int>(t.jobs.size());
+    ca.kv_commit = h->kv_commit;
+    ca.kv_pool = h->kv_pool;
+    ca.L = h->L;
+    ca.KVH = h->KVH;
+    ca.hd = h->hd;
+    ca.max_ctx = h->cfg.max_ctx;
+    ca.n_slots = h->n_slots;
+    cudaError_t ce = dex::launch_collapse(ca, h->st, false);
+    if (ce != cudaSuccess) return cuda_fail(h, ce);
+    h->stats.kernel_launches++;
+  }
+  if (ev[1]) cudaEventRecord(ev[1], h->st);
+  dex::AssembleArgs aa = {};
+  aa.nodes = u.nodes;
+  aa.n_rows = n;
+  aa.d = h->d;
+  aa.embed = h->embed;
+  aa.attn_norm = h->d_attn_norms;
+  aa.hidden = h->hidden;
+  aa.hb = h->hb;
+  aa.ssq = h->ssq;
+  aa.best = h->best;
+  cudaError_t ce = dex::launch_assemble(aa, h->st, false);
+  if (ce != cudaSuccess) return cuda_fail(h, ce);
+  h->stats.kernel_launches++;
+  for (int s = 0; s <= max_stage; ++s) {
+    const int off = t.stage_off[s], ns = t.stage_off[s + 1] - off;
+    if (ns == 0) continue;
+    const int l0 = s > 0 ? X[s - 1] : 0;
+    rc = run_layers(h, u, off, ns, l0, X[s], t.item_begin[s], t.item_begin[s + 1] - t.item_begin[s],
+                    max_groups_launch, true);
+    if (rc) return rc;
+  }
+  if (ev[2]) cudaEventRecord(ev[2], h->st);
+  // exit head + DECS over every node of the round
+  {
+    dex::GemmArgs a = base_args(h);
+    a.nodes = u.nodes;
+    a.kblocks = (h->d + 63) / 64;
+    a.splits = h->S_lm;
+    a.n_tiles = (h->V + 127) / 128;
+    a.src_tiles0 = a.n_tiles;
+    a.ssq_in = h->exit_ssq;
+    a.logits_dbg = h->cfg.debug_logits ? h->logits_dbg : nullptr;
+    a.best = h->best;
+    a.priors = u.priors;
+    a.sample = h->cfg.sample;
+    a.tau = h->cfg.tau;
+    a.seed = h->cfg.seed;
+    rc = gemm(h, dex::EPI_EXIT, h->tm_lm, h->tm_lm, h->tm_lm, h->tm_exit, a, 0, n,
+              static_cast<int64_t>(h->V) * h->d * 2, static_cast<int64_t>(h->d) * 2);
+    if (rc) return rc;
+  }
+  if (ev[3]) cudaEventRecord(ev[3], h->st);
+  // tokens (and the device error flag) back to the host: the round's only sync
+  if (cudaMemcpyAsync(h->h_best, h->best, n * sizeof(unsigned long long), cudaMemcpyDeviceToHost, h->st) !=
+          cudaSuccess ||
+      cudaMemcpyAsync(h->h_best + h->rows_cap, h->err, sizeof(int32_t), cudaMemcpyDeviceToHost, h->st) !=
+          cudaSuccess)
+    return cuda_fail(h, cudaGetLastError());
+  if (cudaStreamSynchronize(h->st) != cudaSuccess) return cuda_fail(h, cudaGetLastError());
+  h->stats.d2h_bytes += n * 8 + 4;
+  const int32_t dev_err = static_cast<int32_t>(h->h_best[h->rows_cap] & 0xffffffffull);
+  if (dev_err) return check_device_error(h, dev_err);
+  auto t_host1 = std::chrono::steady_clock::now();
+  std::vector<int32_t> tokens(n);
+  for (int k = 0; k < n; ++k) tokens[k] = static_cast<int32_t>(~static_cast<uint32_t>(h->h_best[k] & 0xffffffffull));
+  std::vector<int32_t> committed(lat->batch()), kstar(lat->batch());
+  lat->update(plan, tokens.data(), committed.data(), kstar.data(), pending);
+  // statistics
+  h->stats.rounds++;
+  h->stats.nodes += n;
+  h->stats.max_round_nodes = std::max<int64_t>(h->stats.max_round_nodes, n);
+  h->stats.layer_passes += X[max_stage];
+  const int64_t layer_w = (static_cast<int64_t>(h->H + 2 * h->KVH) * h->hd * h->d + static_cast<int64_t>(h->H) *
+                           h->hd * h->d + 3ll * h->dff * h->d) * 2;
+  h->stats.weight_bytes += layer_w * X[max_stage] + static_cast<int64_t>(h->V) * h->d * 2;
+  const int64_t kv_row = 2ll * h->KVH * h->hd * 2;
+  for (int s = 0; s <= max_stage; ++s) {
+    const int nl = X[s] - (s > 0 ? X[s - 1] : 0);
+    for (int i = t.item_begin[s]; i < t.item_begin[s + 1]; ++i)
+      h->stats.kv_bytes += kv_row * nl * t.items[i].max_cend;
+    for (int k = t.stage_off[s]; k < t.stage_off[s + 1]; ++k) {
+      h->stats.node_layers += nl;
+      h->stats.kv_bytes += kv_row * nl * plan[k].n_tail;
+    }
+  }
+  for (int b = 0; b < lat->batch(); ++b) {
+    out_tokens[b] = committed[b] >= 0 ? committed[b] : -1;
+    n_committed[b] = committed[b] >= 0 ? 1 : 0;
+    if (committed[b] >= 0) {
+      h->stats.commits++;
+      h->stats.depth_charge += X[kstar[b]];
+      h->stats.kstar_hist[std::min(kstar[b], 15)]++;
+      if (++h->n_done[b] >= h->cfg.max_new) lat->stop(b);
+    }
+  }
+  h->last_plan = plan;
+  h->last_tokens = tokens;
+  const double host_upd_ms =
+      std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t_host1).count();
+  h->stats.ms_host += host_plan_ms + host_upd_ms;
+  if (h->timing >= 1) {
+    float ms;
+    cudaEventElapsedTime(&ms, ev[0], ev[1]);
+    h->stats.ms_collapse += ms;
+    cudaEventElapsedTime(&ms, ev[1], ev[2]);
+    h->stats.ms_expand += ms;
+    cudaEventElapsedTime(&ms, ev[2], ev[3]);
+    h->stats.ms_exit += ms;
+  }
+  if (h->timing >= 2) {
+    for (auto& pr : h->gemm_events) {
+      float ms;
+      cudaEventElapsedTime(&ms, pr.first, pr.second);
+      h->stats.ms_gemm += ms;
+    }
+  }
+  h->gemm_events.clear();
+  h->ev_used = 0;
+  return DEX_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dex_strerror(int code) {
+  switch (code) {
+    case DEX_OK: return "ok";
+    case DEX_EINVAL: return "invalid argument";
+    case DEX_ENOMEM: return "out of memory";
+    case DEX_ECUDA: return "CUDA error";
+    case DEX_ECAPACITY: return "capacity exceeded (max_ctx / max_new / lattice size)";
+    case DEX_ETIMEOUT: return "a bounded device wait timed out";
+    case DEX_ESTATE: return "call out of order";
+    case DEX_ENODEV: return "no sm_103 device";
+    default: return "unknown error";
+  }
+}
+
+void dex_free(dex_handle* h) {
+  if (!h) return;
+  cudaStreamSynchronize(h->st);
+  for (void* p : h->allocs) cudaFree(p);
+  if (h->h_plan) cudaFreeHost(h->h_plan);
+  if (h->h_best) cudaFreeHost(h->h_best);
+  for (auto e : h->ev_pool) cudaEventDestroy(e);
+  delete h;
+}
+
+int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode_cfg* cfg, void* stream,
+             dex_handle** out) {
+  if (!m || !X || !cfg || !out) return DEX_EINVAL;
+  *out = nullptr;
+  if (m->n_layers < 1 || m->d_model % 128 || (m->head_dim != 64 && m->head_dim != 128) || m->n_kv_heads < 1 ||
+      m->n_heads % m->n_kv_heads || (m->n_heads * m->head_dim) % 128 || (m->n_kv_heads * m->head_dim) % 128 ||
+      m->d_ff < 64 || m->d_ff % 8 || m->vocab < 2 || !m->embed || !m->final_norm || !m->lm_head || !m->layers)
+    return DEX_EINVAL;
+  if (n_X < 1 || n_X > 10 || X[n_X - 1] != m->n_layers) return DEX_EINVAL;
+  for (int i = 0; i < n_X; ++i)
+    if (X[i] < 1 || (i > 0 && X[i] <= X[i - 1])) return DEX_EINVAL;
+  if (cfg->batch < 1 || cfg->batch > 64 || cfg->max_ctx < 2 || cfg->max_new < 1 || (cfg->sample && !(cfg->tau > 0)))
+    return DEX_EINVAL;
+  int dev = 0;
+  cudaDeviceProp prop;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return DEX_ENODEV;
+  if (prop.major != 10 || prop.minor != 3) return DEX_ENODEV;
+  if (get_encoder()) return DEX_ECUDA;
+
+  std::unique_ptr<dex_handle> hp(new (std::nothrow) dex_handle());
+  if (!hp) return DEX_ENOMEM;
+  dex_handle* h = hp.get();
+  h->L = m->n_layers;
+  h->d = m->d_model;
+  h->H = m->n_heads;
+  h->KVH = m->n_kv_heads;
+  h->hd = m->head_dim;
+  h->dff = m->d_ff;
+  h->V = m->vocab;
+  h->eps = m->rms_eps;
+  h->theta = m->rope_theta;
+  h->embed = static_cast<const bf16*>(m->embed);
+  h->final_norm = static_cast<const bf16*>(m->final_norm);
+  h->lm_head = static_cast<const bf16*>(m->lm_head);
+  h->w.resize(static_cast<size_t>(h->L) * 9);
+  for (size_t i = 0; i < h->w.size(); ++i) {
+    h->w[i] = static_cast<const bf16*>(m->layers[i]);
+    if (!h->w[i]) return DEX_EINVAL;
+  }
+  h->X.assign(X, X + n_X);
+  h->N = n_X;
+  h->cfg = *cfg;
+  h->st = static_cast<cudaStream_t>(stream);
+  h->n_sm = prop.multiProcessorCount;
+  h->lat.reset(new dex::Lattice(X, n_X, cfg->batch, cfg->decs != 0));
+  const int32_t XL[1] = {h->L};
+  h->lat_ar.reset(new dex::Lattice(XL, 1, cfg->batch, false));
+  h->mode.assign(cfg->batch, 0);
+  h->n_done.assign(cfg->batch, 0);
+  h->n_slots = h->lat->n_slots();
+  h->rows_cap = std::max(h->lat->max_round_nodes(), 256);
+  h->max_groups = (cfg->max_ctx + 127) / 128;
+  h->hrows = cfg->batch * h->n_slots + 256;
+
+  const size_t B = cfg->batch, L = h->L, KVH = h->KVH, hd = h->hd, ctx = cfg->max_ctx, R = h->rows_cap;
+  const int qd = h->H * h->hd, kvd = h->KVH * h->hd;
+  int rc = 0;
+  rc |= dalloc(h, &h->kv_commit, B * L * 2 * KVH * ctx * hd * 2);
+  rc |= dalloc(h, &h->kv_pool, B * h->n_slots * L * 2 * KVH * hd * 2);
+  rc |= dalloc(h, &h->hidden, static_cast<size_t>(h->hrows) * h->d * 4);
+  rc |= dalloc(h, &h->hb, R * h->d * 2);
+  rc |= dalloc(h, &h->exit_hb, R * h->d * 2);
+  rc |= dalloc(h, &h->attn_out, R * qd * 2);
+  rc |= dalloc(h, &h->act, R * h->dff * 2);
+  rc |= dalloc(h, &h->ssq, R * (h->d / 128) * 4);
+  rc |= dalloc(h, &h->exit_ssq, R * (h->d / 128) * 4);
+  rc |= dalloc(h, &h->q, R * qd * 4);
+  rc |= dalloc(h, &h->attn_part, R * h->H * h->max_groups * (hd + 2) * 4);
+  rc |= dalloc(h, &h->attn_counters, static_cast<size_t>(B) * h->N * KVH * 4 + 256 * KVH * 4);
+  rc |= dalloc(h, &h->rope, ctx * (hd / 2) * sizeof(float2));
+  rc |= dalloc(h, &h->best, (R + 1) * 8);
+  rc |= dalloc(h, &h->err, 16);
+  rc |= dalloc(h, &h->d_attn_norms, L * sizeof(void*));
+  if (cfg->debug_logits) rc |= dalloc(h, &h->logits_dbg, R * static_cast<size_t>(h->V) * 4);
+  if (rc) return DEX_ENOMEM;
+  // split-K factors depend only on the weight shape (batch-invariant results)
+  const int kb_d = (h->d + 63) / 64, kb_q = (qd + 63) / 64, kb_f = (h->dff + 63) / 64;
+  h->S_qkv = splits_for((qd + 2 * kvd) / 128, kb_d, h->n_sm);
+  h->S_o = splits_for(h->d / 128, kb_q, h->n_sm);
+  h->S_gu = splits_for((h->dff + 63) / 64, kb_d, h->n_sm);
+  h->S_d = splits_for(h->d / 128, kb_f, h->n_sm);
+  h->S_lm = splits_for((h->V + 127) / 128, kb_d, h->n_sm);
+  size_t part = 0, ntiles_max = 0;
+  auto need = [&](int S, size_t tiles) {
+    ntiles_max = std::max(ntiles_max, tiles);
+    if (S > 1) part = std::max(part, static_cast<size_t>(S) * 256 * tiles * 128 * 4);
+  };
+  need(h->S_qkv, (qd + 2 * kvd) / 128);
+  need(h->S_o, h->d / 128);
+  need(h->S_gu, (h->dff + 63) / 64);
+  need(h->S_d, h->d / 128);
+  need(h->S_lm, (h->V + 127) / 128);
+  if (dalloc(h, &h->partial, part) || dalloc(h, &h->counters, ntiles_max * 4)) return DEX_ENOMEM;
+  h->plan_cap = (R * sizeof(dex::DevNode) + R * 16 * 8 + 1024 * sizeof(dex::AttnItem) + 64 * 16 + 8192);
+  if (dalloc(h, &h->d_plan, h->plan_cap)) return DEX_ENOMEM;
+  if (cudaMallocHost(&h->h_plan, h->plan_cap) != cudaSuccess) return DEX_ENOMEM;
+  if (cudaMallocHost(&h->h_best, (R + 1) * 8) != cudaSuccess) return DEX_ENOMEM;
+  // zero-initialised state
+  cudaMemsetAsync(h->counters, 0, ntiles_max * 4, h->st);
+  cudaMemsetAsync(h->attn_counters, 0, (static_cast<size_t>(B) * h->N * KVH + 256 * KVH) * 4, h->st);
+  cudaMemsetAsync(h->err, 0, 16, h->st);
+  cudaMemsetAsync(h->kv_commit, 0, B * L * 2 * KVH * ctx * hd * 2, h->st);
+  cudaMemsetAsync(h->kv_pool, 0, B * h->n_slots * L * 2 * KVH * hd * 2, h->st);
+  cudaMemsetAsync(h->hidden, 0, static_cast<size_t>(h->hrows) * h->d * 4, h->st);
+  cudaMemsetAsync(h->hb, 0, R * h->d * 2, h->st);
+  cudaMemsetAsync(h->exit_hb, 0, R * h->d * 2, h->st);
+  cudaMemsetAsync(h->attn_out, 0, R * qd * 2, h->st);
+  cudaMemsetAsync(h->act, 0, R * h->dff * 2, h->st);
+  // RoPE table (rotate-half, frequencies theta^(-2i/hd)), computed in double
+  {
+    std::vector<float2> tab(ctx * (hd / 2));
+    for (size_t p = 0; p < ctx; ++p)
+      for (size_t i = 0; i < hd / 2; ++i) {
+        const double inv = pow(static_cast<double>(h->theta), -2.0 * static_cast<double>(i) / static_cast<double>(hd));
+        const double ang = static_cast<double>(p) * inv;
+        tab[p * (hd / 2) + i] = make_float2(static_cast<float>(cos(ang)), static_cast<float>(sin(ang)));
+      }
+    if (cudaMemcpy(h->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess)
+      return DEX_ECUDA;
+    std::vector<const bf16*> norms(L);
+    for (size_t l = 0; l < L; ++l) norms[l] = W(h, static_cast<int>(l), 0);
+    if (cudaMemcpy(h->d_attn_norms, norms.data(), L * sizeof(void*), cudaMemcpyHostToDevice) != cudaSuccess)
+      return DEX_ECUDA;
+  }
+  // tensor maps: weights (box 128 rows; gate/up 64 rows) and activation buffers (box nt rows)
+  h->tm_q.resize(L);
+  h->tm_k.resize(L);
+  h->tm_v.resize(L);
+  h->tm_o.resize(L);
+  h->tm_g.resize(L);
+  h->tm_u.resize(L);
+  h->tm_d.resize(L);
+  for (size_t l = 0; l < L; ++l) {
+    const int li = static_cast<int>(l);
+    rc |= encode_2d(&h->tm_q[l], W(h, li, 1), qd, h->d, 128);
+    rc |= encode_2d(&h->tm_k[l], W(h, li, 2), kvd, h->d, 128);
+    rc |= encode_2d(&h->tm_v[l], W(h, li, 3), kvd, h->d, 128);
+    rc |= encode_2d(&h->tm_o[l], W(h, li, 4), h->d, qd, 128);
+    rc |= encode_2d(&h->tm_g[l], W(h, li, 6), h->dff, h->d, 64);
+    rc |= encode_2d(&h->tm_u[l], W(h, li, 7), h->dff, h->d, 64);
+    rc |= encode_2d(&h->tm_d[l], W(h, li, 8), h->d, h->dff, 128);
+  }
+  rc |= encode_2d(&h->tm_lm, h->lm_head, h->V, h->d, 128);
+  for (int i = 1; i <= 16; ++i) {
+    rc |= encode_2d(&h->tm_hb[i], h->hb, R, h->d, 16 * i);
+    rc |= encode_2d(&h->tm_attn[i], h->attn_out, R, qd, 16 * i);
+    rc |= encode_2d(&h->tm_act[i], h->act, R, h->dff, 16 * i);
+    rc |= encode_2d(&h->tm_exit[i], h->exit_hb, R, h->d, 16 * i);
+  }
+  if (rc) return DEX_EINVAL;
+  if (cudaStreamSynchronize(h->st) != cudaSuccess) return DEX_ECUDA;
+  *out = hp.release();
+  return DEX_OK;
+}
+
+int dex_prefill(dex_handle* h, int32_t seq, const int32_t* tokens, int32_t n_tokens) {
+  if (!h || !tokens || seq < 0 || seq >= h->cfg.batch || n_tokens < 1) return DEX_EINVAL;
+  if (h->broken) return DEX_ECUDA;
+  if (n_tokens + h->cfg.max_new + h->N > h->cfg.max_ctx) return DEX_ECAPACITY;
+  for (int i = 0; i < n_tokens; ++i)
+    if (tokens[i] < 0 || tokens[i] >= h->V) return DEX_EINVAL;
+  h->lat->stop(seq);
+  h->lat_ar->stop(seq);
+  h->mode[seq] = 0;
+  h->n_done[seq] = 0;
+  auto drop = [&](std::vector<dex_copy_job>& v) {
+    v.erase(std::remove_if(v.begin(), v.end(), [&](const dex_copy_job& j) { return j.seq == seq; }), v.end());
+  };
+  drop(h->pending_jobs);
+  drop(h->pending_jobs_ar);
+  const int P = n_tokens - 1;   // committed positions 0..P-1 get their KV here
+  for (int c0 = 0; c0 < P; c0 += 256) {
+    const int n = std::min(256, P - c0);
+    RoundTables t;
+    for (int i = 0; i < n; ++i) {
+      dex::DevNode dn = {};
+      dn.seq = seq;
+      dn.pos = c0 + i;
+      dn.c_end = c0 + i + 1;
+      dn.slot = 0;
+      dn.hrow = h->cfg.batch * h->n_slots + i;
+      dn.kv_commit = 1;
+      dn.token = tokens[c0 + i];
+      dn.first_layer = 0;
+      dn.unmasked = 1;
+      t.nodes.push_back(dn);
+    }
+    dex::AttnItem it = {};
+    it.seq = seq;
+    it.row_begin = 0;
+    it.row_end = n;
+    it.max_pos = c0 + n - 1;
+    it.max_cend = c0 + n;
+    it.n_groups = it.max_pos / 128 + 1;
+    it.counter = 0;
+    t.items.push_back(it);
+    Uploaded u;
+    int rc = upload(h, t, &u);
+    if (rc) return rc;
+    dex::AssembleArgs aa = {};
+    aa.nodes = u.nodes;
+    aa.n_rows = n;
+    aa.d = h->d;
+    aa.embed = h->embed;
+    aa.attn_norm = h->d_attn_norms;
+    aa.hidden = h->hidden;
+    aa.hb = h->hb;
+    aa.ssq = h->ssq;
+    aa.best = nullptr;
+    cudaError_t ce = dex::launch_assemble(aa, h->st, false);
+    if (ce != cudaSuccess) return cuda_fail(h, ce);
+    rc = run_layers(h, u, 0, n, 0, h->L, 0, 1, it.n_groups, false);
+    if (rc) return rc;
+    // the upload buffer is reused by the next chunk: wait for this chunk
+    if (cudaMemcpyAsync(h->h_best + h->rows_cap, h->err, 4, cudaMemcpyDeviceToHost, h->st) != cudaSuccess ||
+        cudaStreamSynchronize(h->st) != cudaSuccess)
+      return cuda_fail(h, cudaGetLastError());
+    const int32_t dev_err = static_cast<int32_t>(h->h_best[h->rows_cap] & 0xffffffffull);
+    if (dev_err) return check_device_error(h, dev_err);
+  }
+  h->lat->start(seq, n_tokens, tokens[n_tokens - 1]);
+  h->lat_ar->start(seq, n_tokens, tokens[n_tokens - 1]);
+  return DEX_OK;
+}
+
+static int step_common(dex_handle* h, bool ar, int32_t* out_tokens, int32_t* n_committed) {
+  if (!h || !out_tokens || !n_committed) return DEX_EINVAL;
+  dex::Lattice* lat = ar ? h->lat_ar.get() : h->lat.get();
+  dex::Lattice* other = ar ? h->lat.get() : h->lat_ar.get();
+  const int want = ar ? 2 : 1;
+  for (int b = 0; b < h->cfg.batch; ++b) {
+    if (!lat->active(b)) continue;
+    if (h->mode[b] != 0 && h->mode[b] != want) return DEX_ESTATE;
+  }
+  for (int b = 0; b < h->cfg.batch; ++b)
+    if (lat->active(b)) {
+      h->mode[b] = want;
+      other->stop(b);
+    }
+  return run_round(h, lat, ar ? &h->pending_jobs_ar : &h->pending_jobs, out_tokens, n_committed);
+}
+
+int dex_step(dex_handle* h, int32_t* out_tokens, int32_t* n_committed) {
+  return step_common(h, false, out_tokens, n_committed);
+}
+int dex_ar_step(dex_handle* h, int32_t* out_tokens, int32_t* n_committed) {
+  return step_common(h, true, out_tokens, n_committed);
+}
+
+static int generate_loop(dex_handle* h, bool ar, int32_t* out) {
+  if (!h || !out) return DEX_EINVAL;
+  std::vector<int32_t> tok(h->cfg.batch), nc(h->cfg.batch);
+  dex::Lattice* lat = ar ? h->lat_ar.get() : h->lat.get();
+  while (lat->any_active()) {
+    const int rc = step_common(h, ar, tok.data(), nc.data());
+    if (rc) return rc;
+    for (int b = 0; b < h->cfg.batch; ++b)
+      if (nc[b]) out[static_cast<size_t>(b) * h->cfg.max_new + h->n_done[b] - 1] = tok[b];
+  }
+  return DEX_OK;
+}
+
+int dex_generate(dex_handle* h, int32_t* out) { return generate_loop(h, false, out); }
+int dex_ar_generate(dex_handle* h, int32_t* out) { return generate_loop(h, true, out); }
+
+int dex_get_stats(const dex_handle* h, dex_stats* out) {
+  if (!h || !out) return DEX_EINVAL;
+  *out = h->stats;
+  return DEX_OK;
+}
+int dex_reset_stats(dex_handle* h) {
+  if (!h) return DEX_EINVAL;
+  h->stats = dex_stats{};
+  return DEX_OK;
+}
+int dex_set_timing(dex_handle* h, int32_t level) {
+  if (!h || level < 0 || level > 2) return DEX_EINVAL;
+  h->timing = level;
+  return DEX_OK;
+}
+
+int dex_last_round_nodes(const dex_handle* h, int32_t* host_out, int32_t max_rows, int32_t* rows_out) {
+  if (!h || !rows_out) return DEX_EINVAL;
+  const int n = static_cast<int>(h->last_plan.size());
+  *rows_out = n;
+  if (n > max_rows || (n && !host_out)) return DEX_ECAPACITY;
+  for (int k = 0; k < n; ++k) {
+    const auto& p = h->last_plan[k];
+    int32_t* o = host_out + 8 * k;
+    o[0] = p.seq;
+    o[1] = p.heap;
+    o[2] = p.stage;
+    o[3] = p.plen;
+    o[4] = p.target_pos;
+    o[5] = h->last_tokens[k];
+    o[6] = p.n_prior;
+    o[7] = p.pos;
+  }
+  return DEX_OK;
+}
+
+int dex_debug_logits(dex_handle* h, float* host_out, int32_t max_rows, int32_t* rows_out) {
+  if (!h || !rows_out) return DEX_EINVAL;
+  if (!h->cfg.debug_logits) return DEX_ESTATE;
+  const int n = static_cast<int>(h->last_plan.size());
+  *rows_out = n;
+  if (n > max_rows || (n && !host_out)) return DEX_ECAPACITY;
+  if (cudaMemcpyAsync(host_out, h->logits_dbg, static_cast<size_t>(n) * h->V * 4, cudaMemcpyDeviceToHost, h->st) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(h->st) != cudaSuccess)
+    return cuda_fail(h, cudaGetLastError());
+  return DEX_OK;
+}
+
+// ---- kernels in isolation ---------------------------------------------------------------
+
+__global__ void exit_nodes_kernel(const dex_exit_node* in, int n, dex::DevNode* out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  dex::DevNode d = {};
+  d.seq = in[i].seq;
+  d.target_pos = in[i].target_pos;
+  d.unmasked = in[i].unmasked;
+  d.prior_off = in[i].prior_off;
+  d.n_prior = in[i].n_prior;
+  out[i] = d;
+}
+
+int dex_exit_head_decs(const void* hidden, int32_t n, int32_t d, const void* final_norm, float rms_eps,
+                       const void* lm_head, int32_t vocab, const dex_exit_node* nodes, const int32_t* priors,
+                       int32_t sample, float tau, uint64_t seed, int32_t* tokens, float* logits, void* stream) {
+  if (!hidden || !final_norm || !lm_head || !nodes || !tokens || n < 1 || n > 256 || d < 128 || d % 128 ||
+      vocab < 2 || (sample && !(tau > 0)))
+    return DEX_EINVAL;
+  if (get_encoder()) return DEX_ECUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int dev = 0, n_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return DEX_ENODEV;
+  const int n_tiles = (vocab + 127) / 128, kb = (d + 63) / 64;
+  const int S = splits_for(n_tiles, kb, n_sm);
+  const int nt = (n + 15) & ~15;
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t o_hb = 0, o_ssq = o_hb + up(static_cast<size_t>(nt) * d * 2);
+  const size_t o_best = o_ssq + up(static_cast<size_t>(n) * (d / 128) * 4);
+  const size_t o_nodes = o_best + up(static_cast<size_t>(n) * 8);
+  const size_t o_cnt = o_nodes + up(static_cast<size_t>(n) * sizeof(dex::DevNode));
+  const size_t o_err = o_cnt + up(static_cast<size_t>(n_tiles) * 4);
+  const size_t o_part = o_err + 256;
+  const size_t total = o_part + (S > 1 ? static_cast<size_t>(S) * 256 * n_tiles * 128 * 4 : 0);
+  uint8_t* scratch = nullptr;
+  if (cudaMallocAsync(reinterpret_cast<void**>(&scratch), total, st) != cudaSuccess) return DEX_ENOMEM;
+  bf16* hb = reinterpret_cast<bf16*>(scratch + o_hb);
+  float* ssq = reinterpret_cast<float*>(scratch + o_ssq);
+  unsigned long long* best = reinterpret_cast<unsigned long long*>(scratch + o_best);
+  dex::DevNode* dn = reinterpret_cast<dex::DevNode*>(scratch + o_nodes);
+  int32_t* cnt = reinterpret_cast<int32_t*>(scratch + o_cnt);
+  int rc = DEX_OK;
+  CUtensorMap tm_w, tm_b;
+  if (encode_2d(&tm_w, lm_head, vocab, d, 128) || encode_2d(&tm_b, hb, nt, d, nt)) rc = DEX_EINVAL;
+  if (!rc) {
+    cudaMemsetAsync(hb, 0, static_cast<size_t>(nt) * d * 2, st);
+    cudaMemsetAsync(cnt, 0, o_part - o_cnt, st);   // arrival counters and the error flag
+    if (dex::launch_exit_prep(static_cast<const bf16*>(hidden), n, d, static_cast<const bf16*>(final_norm), hb, ssq,
+                              best, st) != cudaSuccess)
+      rc = DEX_ECUDA;
+    exit_nodes_kernel<<<(n + 127) / 128, 128, 0, st>>>(nodes, n, dn);
+    dex::GemmArgs a = {};
+    a.n = n;
+    a.nt = nt;
+    a.b_row0 = 0;
+    a.kblocks = kb;
+    a.splits = S;
+    a.stages = 4;
+    a.n_tiles = n_tiles;
+    a.src_tiles0 = n_tiles;
+    a.tmem_cols = pow2_at_least(nt);
+    a.partial = reinterpret_cast<float*>(scratch + o_part);
+    a.counters = cnt;
+    a.err = reinterpret_cast<int32_t*>(scratch + o_err);
+    a.nodes = dn;
+    a.evict_first = 1;
+    a.d = d;
+    a.vocab = vocab;
+    a.eps = rms_eps;
+    a.ssq_in = ssq;
+    a.logits_dbg = logits;
+    a.best = best;
+    a.priors = priors;
+    a.sample = sample;
+    a.tau = tau;
+    a.seed = seed;
+    if (!rc && dex::launch_gemm(dex::EPI_EXIT, tm_w, tm_w, tm_w, tm_b, a, st, false) != cudaSuccess) rc = DEX_ECUDA;
+    if (!rc && dex::launch_decode_best(best, n, tokens, st) != cudaSuccess) rc = DEX_ECUDA;
+  }
+  cudaFreeAsync(scratch, st);
+  return rc;
+}
+
+int dex_kv_collapse(void* committed, const void* pool, const dex_kv_geom* g, const dex_copy_job* jobs, int32_t n_jobs,
+                    void* stream) {
+  if (!committed || !pool || !g || (!jobs && n_jobs) || n_jobs < 0 || n_jobs > 65535 || g->head_dim % 8 ||
+      g->n_layers < 1 || g->n_kv_heads < 1 || g->max_ctx < 1 || g->n_slots < 1)
+    return DEX_EINVAL;
+  dex::CollapseArgs a = {};
+  a.jobs = reinterpret_cast<const dex::CopyJob*>(jobs);
+  a.n_jobs = n_jobs;
+  a.kv_commit = static_cast<bf16*>(committed);
+  a.kv_pool = static_cast<const bf16*>(pool);
+  a.L = g->n_layers;
+  a.KVH = g->n_kv_heads;
+  a.hd = g->head_dim;
+  a.max_ctx = g->max_ctx;
+  a.n_slots = g->n_slots;
+  return dex::launch_collapse(a, static_cast<cudaStream_t>(stream), false) == cudaSuccess ? DEX_OK : DEX_ECUDA;
+}
+
+}  // extern "C"

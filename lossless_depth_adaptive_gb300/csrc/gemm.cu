@@ -1,0 +1,418 @@
+// Weight-streaming GEMM on the 5th-generation tensor cores (tcgen05) with TMA-fed
+// shared-memory pipelines and fused epilogues, for the decoder slices and the shared
+// exit head of a DEX round.
+//
+//   D[row][node] = sum_k W[row][k] * X[node][k]      (W: weights, X: node activations)
+//
+// Swap-AB: the weights sit on the MMA's M = 128 side, the few lattice nodes of a stage
+// batch on the N side (16..256 columns), so each weight byte is read from HBM once per
+// round however many nodes the round holds.  One CTA owns one 128-row output tile and
+// one fixed slice of K (split-K); the split depends only on the weight shape, and the
+// partial tiles are summed in split order by the last CTA to arrive, so a node's
+// result never depends on the batch it was computed in.
+//
+// Roles: warp 0 issues TMA loads (weights first -- they do not depend on the previous
+// kernel -- then, after the grid-dependency wait, the activations); warp 1 owns TMEM
+// and issues tcgen05.mma; warps 2-5 run the epilogue from TMEM (one accumulator row per
+// thread).  Every wait is bounded and reports a stall through the error flag.
+//
+// Epilogues: EPI_QKV (RMSNorm scale, RoPE, K/V into the committed cache or the branch
+// pool), EPI_RESID (residual add into the fp32 hidden state, next layer's bf16 input,
+// RMSNorm partial sums, exit-head input at a stage boundary), EPI_SWIGLU
+// (SiLU(gate) * up), EPI_EXIT (exit logits, DECS mask, Gumbel noise, argmax).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dex {
+
+constexpr int kThreads = 192;
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr uint32_t kABytes = kBM * kBK * 2;   // 16 KB weight tile per stage
+constexpr int kNtMax = 256;
+
+struct SmemMap {
+  size_t a, b, bar, misc, xch, inv, qsum, qkey, total;
+};
+__host__ __device__ inline SmemMap smem_map(int nt, int stages) {
+  SmemMap m;
+  m.a = 0;
+  m.b = m.a + static_cast<size_t>(stages) * kABytes;
+  m.bar = m.b + static_cast<size_t>(stages) * nt * kBK * 2;
+  m.misc = m.bar + static_cast<size_t>(2 * stages + 1) * 8;
+  m.xch = (m.misc + 32 + 15) & ~static_cast<size_t>(15);        // tmem slot + flags
+  m.inv = m.xch + 16 * kBM * 4;                                    // 16 columns x 128 rows
+  m.qsum = m.inv + kNtMax * 4;
+  m.qkey = m.qsum + 4 * 16 * 4;
+  m.total = m.qkey + 4 * 16 * 8;
+  return m;
+}
+
+size_t gemm_smem_bytes(int nt, int stages) { return smem_map(nt, stages).total + 1024; }
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+                   const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB,
+                   const GemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const SmemMap sm = smem_map(a.nt, a.stages);
+  uint8_t* sA = smem + sm.a;
+  uint8_t* sB = smem + sm.b;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + sm.bar);
+  uint64_t* empty = full + a.stages;
+  uint64_t* accf = empty + a.stages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + sm.misc);
+  volatile int* sflag = reinterpret_cast<volatile int*>(smem + sm.misc + 4);   // [0] last, [1] abort
+  float* xch = reinterpret_cast<float*>(smem + sm.xch);
+  float* inv = reinterpret_cast<float*>(smem + sm.inv);
+  float* qsum = reinterpret_cast<float*>(smem + sm.qsum);
+  unsigned long long* qkey = reinterpret_cast<unsigned long long*>(smem + sm.qkey);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = a.splits, stages = a.stages;
+  const int tile = blockIdx.x / S, split = blockIdx.x % S;
+  const int kb0 = static_cast<int>(static_cast<long long>(split) * a.kblocks / S);
+  const int kb1 = static_cast<int>(static_cast<long long>(split + 1) * a.kblocks / S);
+  const int nk = kb1 - kb0;
+  const uint32_t b_bytes = static_cast<uint32_t>(a.nt) * kBK * 2;
+
+  int src = 0, lt = tile;
+  if (tile >= a.src_tiles0 + a.src_tiles1) {
+    src = 2;
+    lt = tile - a.src_tiles0 - a.src_tiles1;
+  } else if (tile >= a.src_tiles0) {
+    src = 1;
+    lt = tile - a.src_tiles0;
+  }
+  const CUtensorMap* mapA = src == 0 ? &tmA0 : (src == 1 ? &tmA1 : &tmA2);
+
+  if (tid == 0) {
+    for (int i = 0; i < stages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(accf, 1);
+    sflag[0] = 0;
+    sflag[1] = 0;
+    fence_mbar_init();
+    tma_prefetch(mapA);
+    if (EPI == EPI_SWIGLU) tma_prefetch(&tmA1);
+    tma_prefetch(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, static_cast<uint32_t>(a.tmem_cols));
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  griddep_launch_dependents();
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_first();
+      auto load_a = [&](int i, int st) {
+        const int kx = (kb0 + i) * kBK;
+        uint8_t* dst = sA + static_cast<size_t>(st) * kABytes;
+        if (EPI == EPI_SWIGLU) {
+          if (a.evict_first) {
+            tma_load_2d_hint(dst, &tmA0, &full[st], kx, lt * 64, pol);
+            tma_load_2d_hint(dst + kABytes / 2, &tmA1, &full[st], kx, lt * 64, pol);
+          } else {
+            tma_load_2d(dst, &tmA0, &full[st], kx, lt * 64);
+            tma_load_2d(dst + kABytes / 2, &tmA1, &full[st], kx, lt * 64);
+          }
+        } else {
+          if (a.evict_first) tma_load_2d_hint(dst, mapA, &full[st], kx, lt * kBM, pol);
+          else tma_load_2d(dst, mapA, &full[st], kx, lt * kBM);
+        }
+      };
+      auto load_b = [&](int i, int st) {
+        tma_load_2d(sB + static_cast<size_t>(st) * b_bytes, &tmB, &full[st], (kb0 + i) * kBK, a.b_row0);
+      };
+      const int npre = nk < stages ? nk : stages;
+      for (int i = 0; i < npre; ++i) {
+        mbar_arrive_expect_tx(&full[i], kABytes + b_bytes);
+        load_a(i, i);
+      }
+      griddep_wait();   // activations are produced by the previous kernel
+      for (int i = 0; i < npre; ++i) load_b(i, i);
+      int issued = npre;
+      bool ok = true;
+      for (int i = npre; i < nk; ++i) {
+        const int st = i % stages;
+        const uint32_t use = static_cast<uint32_t>(i / stages);
+        if (!mbar_wait(&empty[st], (use - 1) & 1u, a.err, DEV_TIMEOUT_EMPTY)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[st], kABytes + b_bytes);
+        load_a(i, st);
+        load_b(i, st);
+        issued = i + 1;
+      }
+      if (!ok) {   // drain copies still in flight before the CTA can exit
+        for (int i = (issued > stages ? issued - stages : 0); i < issued; ++i)
+          mbar_wait(&full[i % stages], static_cast<uint32_t>(i / stages) & 1u, nullptr, 0);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kBM, a.nt);
+      bool ok = true;
+      for (int i = 0; i < nk; ++i) {
+        const int st = i % stages;
+        if (!mbar_wait(&full[st], static_cast<uint32_t>(i / stages) & 1u, a.err, DEV_TIMEOUT_FULL)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t abase = smem_u32(sA + static_cast<size_t>(st) * kABytes);
+        const uint32_t bbase = smem_u32(sB + static_cast<size_t>(st) * b_bytes);
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          umma_bf16(tmem_base, sw128_kmajor_desc(abase + kk * 32), sw128_kmajor_desc(bbase + kk * 32), idesc,
+                    (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&empty[st]);
+      }
+      if (ok) umma_commit(accf);
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int wq = warp & 3;           // TMEM lane quarter this warp may access
+    const int r = wq * 32 + lane;      // accumulator row within the tile
+    const int ep = tid - 64;           // 0..127
+    const int n = a.n;
+    const int ndt = a.d / 128;
+    griddep_wait();
+    if (EPI != EPI_RESID) {
+      for (int c = ep; c < n; c += 128) {
+        const float* s = a.ssq_in + static_cast<size_t>(a.b_row0 + c) * ndt;
+        float t = s[0];
+        for (int j = 1; j < ndt; ++j) t = __fadd_rn(t, s[j]);
+        inv[c] = 1.0f / sqrtf(__fadd_rn(__fdiv_rn(t, static_cast<float>(a.d)), a.eps));
+      }
+    }
+    if (!mbar_wait(accf, 0, a.err, DEV_TIMEOUT_ACC)) sflag[1] = 1;
+    named_bar_sync(1, 128);
+    const bool abort = sflag[1] != 0;
+    tc_fence_after();
+
+    // per-chunk epilogue: v[j] = accumulator of (row r, node c0 + j)
+    auto epilogue_chunk = [&](int c0, float (&v)[16]) {
+      if (EPI == EPI_QKV) {
+        const int f = lt * kBM + r;      // feature within the source (q, k or v)
+        const int half = a.hd >> 1;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) xch[j * kBM + r] = (c0 + j < n) ? v[j] * inv[c0 + j] : 0.0f;
+        named_bar_sync(1, 128);
+        const int head = f / a.hd, dim = f - head * a.hd;
+        for (int j = 0; j < 16; ++j) {
+          const int c = c0 + j;
+          if (c >= n) break;
+          const DevNode* nd = a.nodes + a.b_row0 + c;
+          const float x = xch[j * kBM + r];
+          float out = x;
+          if (src != 2) {
+            const float y = xch[j * kBM + (r ^ half)];
+            const float2 cs = a.rope[static_cast<size_t>(nd->pos) * half + (dim & (half - 1))];
+            out = dim < half ? x * cs.x - y * cs.y : x * cs.x + y * cs.y;
+          }
+          if (src == 0) {
+            a.q_out[static_cast<size_t>(a.b_row0 + c) * (a.H * a.hd) + f] = out;
+          } else {
+            const int kv = src - 1;
+            __nv_bfloat16* dst;
+            if (nd->kv_commit) {
+              dst = a.kv_commit +
+                    ((((static_cast<size_t>(nd->seq) * a.L + a.layer) * 2 + kv) * a.KVH + head) * a.max_ctx +
+                     nd->pos) * a.hd + dim;
+            } else {
+              dst = a.kv_pool +
+                    ((((static_cast<size_t>(nd->seq) * a.n_slots + nd->slot) * a.L + a.layer) * 2 + kv) * a.KVH +
+                     head) * a.hd + dim;
+            }
+            *dst = __float2bfloat16_rn(out);
+          }
+        }
+        named_bar_sync(1, 128);
+      } else if (EPI == EPI_RESID) {
+        const int f = lt * kBM + r;
+        float sq[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int c = c0 + j;
+          sq[j] = 0.0f;
+          if (c < n) {
+            const DevNode* nd = a.nodes + a.b_row0 + c;
+            float* hp = a.hidden + static_cast<size_t>(nd->hrow) * a.d + f;
+            const float x = __fadd_rn(*hp, v[j]);
+            *hp = x;
+            const size_t o = static_cast<size_t>(a.b_row0 + c) * a.d + f;
+            if (a.hb_out) a.hb_out[o] = __float2bfloat16_rn(__fmul_rn(x, bf16_to_f32(a.g_next[f])));
+            if (a.stage_end) a.exit_hb[o] = __float2bfloat16_rn(__fmul_rn(x, bf16_to_f32(a.g_final[f])));
+            sq[j] = __fmul_rn(x, x);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float s = warp_sum(sq[j]);
+          if (lane == 0) qsum[wq * 16 + j] = s;
+        }
+        named_bar_sync(1, 128);
+        if (ep < 16 && c0 + ep < n) {
+          const float t = __fadd_rn(__fadd_rn(qsum[0 * 16 + ep], qsum[1 * 16 + ep]),
+                                    __fadd_rn(qsum[2 * 16 + ep], qsum[3 * 16 + ep]));
+          const size_t o = static_cast<size_t>(a.b_row0 + c0 + ep) * ndt + lt;
+          a.ssq_out[o] = t;
+          if (a.stage_end) a.exit_ssq[o] = t;
+        }
+        named_bar_sync(1, 128);
+      } else if (EPI == EPI_SWIGLU) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) xch[j * kBM + r] = (c0 + j < n) ? v[j] * inv[c0 + j] : 0.0f;
+        named_bar_sync(1, 128);
+        const int feat = lt * 64 + (r & 63);
+        if (r < 64 && feat < a.d_ff) {
+          for (int j = 0; j < 16; ++j) {
+            const int c = c0 + j;
+            if (c >= n) break;
+            const float g = xch[j * kBM + r], u = xch[j * kBM + r + 64];
+            const float act = g / (1.0f + expf(-g)) * u;
+            a.act_out[static_cast<size_t>(a.b_row0 + c) * a.d_ff + feat] = __float2bfloat16_rn(act);
+          }
+        }
+        named_bar_sync(1, 128);
+      } else {   // EPI_EXIT
+        const uint32_t vid = static_cast<uint32_t>(lt * kBM + r);
+#pragma unroll 1
+        for (int j = 0; j < 16; ++j) {
+          const int c = c0 + j;
+          float score = -INFINITY;
+          if (c < n && vid < static_cast<uint32_t>(a.vocab)) {
+            const float logit = v[j] * inv[c];
+            if (a.logits_dbg) a.logits_dbg[static_cast<size_t>(a.b_row0 + c) * a.vocab + vid] = logit;
+            const DevNode* nd = a.nodes + a.b_row0 + c;
+            bool masked = false;
+            if (!nd->unmasked) {
+              for (int p = 0; p < nd->n_prior; ++p) masked |= (a.priors[nd->prior_off + p] == static_cast<int>(vid));
+            }
+            if (!masked) score = a.sample ? logit / a.tau + gumbel_noise(a.seed, nd->seq, nd->target_pos, vid) : logit;
+          }
+          unsigned long long key = argmax_key(score, vid);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
+            key = other > key ? other : key;
+          }
+          if (lane == 0) qkey[wq * 16 + j] = key;
+        }
+        named_bar_sync(1, 128);
+        if (ep < 16 && c0 + ep < n) {
+          unsigned long long k = qkey[ep];
+          for (int w = 1; w < 4; ++w) k = qkey[w * 16 + ep] > k ? qkey[w * 16 + ep] : k;
+          atomicMax(a.best + a.b_row0 + c0 + ep, k);
+        }
+        named_bar_sync(1, 128);
+      }
+    };
+
+    if (!abort) {
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(wq * 32) << 16);
+      if (S > 1) {
+        const size_t rows_total = static_cast<size_t>(a.n_tiles) * kBM;
+        for (int c0 = 0; c0 < n; c0 += 16) {
+          float v[16];
+          tmem_ld16(taddr + static_cast<uint32_t>(c0), v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (c0 + j < n)
+              __stcg(a.partial + (static_cast<size_t>(split) * kNtMax + c0 + j) * rows_total + tile * kBM + r, v[j]);
+        }
+        __threadfence();
+        named_bar_sync(1, 128);
+        if (ep == 0) sflag[0] = (atomicAdd(a.counters + tile, 1) == S - 1) ? 1 : 0;
+        named_bar_sync(1, 128);
+        if (sflag[0]) {
+          __threadfence();
+          for (int c0 = 0; c0 < n; c0 += 16) {
+            float v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              v[j] = 0.0f;
+              if (c0 + j < n) {
+                const float* p = a.partial + static_cast<size_t>(c0 + j) * rows_total + tile * kBM + r;
+                float t = __ldcg(p);
+                for (int s = 1; s < S; ++s) t = __fadd_rn(t, __ldcg(p + static_cast<size_t>(s) * kNtMax * rows_total));
+                v[j] = t;
+              }
+            }
+            epilogue_chunk(c0, v);
+          }
+          if (ep == 0) a.counters[tile] = 0;
+        }
+      } else {
+        for (int c0 = 0; c0 < n; c0 += 16) {
+          float v[16];
+          tmem_ld16(taddr + static_cast<uint32_t>(c0), v);
+          epilogue_chunk(c0, v);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, static_cast<uint32_t>(a.tmem_cols));
+  }
+}
+
+template <int EPI>
+static cudaError_t launch_one(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& a2,
+                              const CUtensorMap& b, const GemmArgs& args, cudaStream_t st, bool pdl) {
+  static bool attr_set = false;
+  const size_t smem = gemm_smem_bytes(args.nt, args.stages);
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(gemm_smem_bytes(kNtMax, 4)));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(args.n_tiles * args.splits));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<EPI>, a0, a1, a2, b, args);
+}
+
+cudaError_t launch_gemm(int epi, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& a2,
+                        const CUtensorMap& b, const GemmArgs& args, cudaStream_t st, bool pdl) {
+  if (args.nt < 16 || args.nt > kNtMax || (args.nt & 15) || args.n < 1 || args.n > args.nt) return cudaErrorInvalidValue;
+  if (args.tmem_cols < args.nt || args.tmem_cols < 32 || (args.tmem_cols & (args.tmem_cols - 1)))
+    return cudaErrorInvalidValue;
+  if (args.stages < 2 || args.stages > 8 || gemm_smem_bytes(args.nt, args.stages) > gemm_smem_bytes(kNtMax, 4))
+    return cudaErrorInvalidValue;
+  switch (epi) {
+    case EPI_QKV: return launch_one<EPI_QKV>(a0, a1, a2, b, args, st, pdl);
+    case EPI_RESID: return launch_one<EPI_RESID>(a0, a1, a2, b, args, st, pdl);
+    case EPI_SWIGLU: return launch_one<EPI_SWIGLU>(a0, a1, a2, b, args, st, pdl);
+    case EPI_EXIT: return launch_one<EPI_EXIT>(a0, a1, a2, b, args, st, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace dex

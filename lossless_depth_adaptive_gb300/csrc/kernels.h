@@ -1,0 +1,148 @@
+// Shared host/device definitions: the per-node round descriptor, kernel argument
+// blocks and the launchers of the DEX kernels (sm_103a).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dex {
+
+// Error flags written by kernels (read back by the host after each round).
+enum DevErr : int { DEV_OK = 0, DEV_TIMEOUT_FULL = 1, DEV_TIMEOUT_EMPTY = 2, DEV_TIMEOUT_ACC = 3,
+                    DEV_BAD_INDEX = 4 };
+
+// One lattice node of the current round, as the kernels see it.  Node rows are ordered
+// by stage; the rows of stage s form one contiguous batch for that stage's layers, and
+// the same row index addresses the node in every activation buffer and in the exit head.
+struct DevNode {
+  int32_t seq;         // sequence
+  int32_t pos;         // absolute position of the input token
+  int32_t c_end;       // keys at positions < c_end live in the committed cache
+  int32_t slot;        // pool slot of the slot chain (branch KV)
+  int32_t hrow;        // row of the fp32 hidden-state array (slot chain or prefill scratch)
+  int32_t kv_commit;   // 1: this node's K/V are written to the committed cache at pos
+  int32_t token;       // stage-0 input token (embedding row), -1 for depth children
+  int32_t first_layer; // first layer (0-based) of the node's stage
+  int32_t tail_off;    // tail slots (positions c_end..pos) start here in the tail array
+  int32_t n_tail;
+  int32_t target_pos;  // position being predicted (Gumbel row key)
+  int32_t unmasked;    // 1: final-depth reference, no DECS mask
+  int32_t prior_off;   // DECS prior tokens start here in the prior array
+  int32_t n_prior;
+  int32_t pad0, pad1;
+};
+static_assert(sizeof(DevNode) == 64, "DevNode is 64 bytes");
+
+// Attention work item: one sequence's contiguous node rows within a stage batch.
+struct AttnItem {
+  int32_t seq, row_begin, row_end;   // absolute node rows
+  int32_t max_pos, max_cend;         // largest input position / committed extent among the rows
+  int32_t n_groups;                  // 128-position key groups covering 0..max_pos
+  int32_t counter;                   // index of this item's merge counters (x KVH)
+  int32_t pad;
+};
+
+enum Epi : int { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_EXIT = 3 };
+
+struct GemmArgs {
+  // tiling
+  int32_t n;            // valid node columns
+  int32_t nt;           // node tile (multiple of 16, <= 256)
+  int32_t b_row0;       // first B row (= first node row of the batch)
+  int32_t kblocks;      // K / 64, rounded up
+  int32_t splits;       // fixed split-K factor of this weight shape
+  int32_t stages;       // smem pipeline depth
+  int32_t n_tiles;      // output tiles
+  int32_t src_tiles0, src_tiles1;   // tiles of source 0 and 1 (source 2 takes the rest)
+  int32_t tmem_cols;
+  float* partial;       // [splits][256][n_tiles * 128] fp32 split-K partials
+  int32_t* counters;    // [n_tiles] arrival counters (left at 0)
+  int32_t* err;         // device error flag
+  const DevNode* nodes; // node rows (absolute)
+  int32_t evict_first;  // stream A with an L2 evict-first policy
+  // model geometry
+  int32_t d, H, KVH, hd, L, d_ff, vocab, max_ctx, n_slots;
+  int32_t layer;
+  float eps;
+  // RMSNorm inputs (QKV, SWIGLU, EXIT): per-row 128-feature partial sums of squares
+  const float* ssq_in;  // [rows][d/128]
+  // QKV
+  float* q_out;         // [rows][H*hd]
+  __nv_bfloat16* kv_commit;   // [B][L][2][KVH][max_ctx][hd]
+  __nv_bfloat16* kv_pool;     // [B][n_slots][L][2][KVH][hd]
+  const float2* rope;   // [max_ctx][hd/2] (cos, sin)
+  // RESID
+  float* hidden;        // [hrows][d]
+  __nv_bfloat16* hb_out;      // [rows][d]  bf16(h * g_next), next layer's input
+  const __nv_bfloat16* g_next;
+  float* ssq_out;       // [rows][d/128]
+  int32_t stage_end;    // last layer of the batch's stage: also write the exit-head input
+  __nv_bfloat16* exit_hb;     // [rows][d]
+  const __nv_bfloat16* g_final;
+  float* exit_ssq;      // [rows][d/128]
+  // SWIGLU
+  __nv_bfloat16* act_out;     // [rows][d_ff]
+  // EXIT + DECS
+  float* logits_dbg;    // [rows][vocab] or null
+  unsigned long long* best;   // [rows] packed (score, ~token), zeroed before the launch
+  const int32_t* priors;
+  int32_t sample;
+  float tau;
+  unsigned long long seed;
+};
+
+struct AttnArgs {
+  const DevNode* nodes;
+  const AttnItem* items;
+  const int32_t* tails;
+  const float* q;              // [rows][H*hd]
+  const __nv_bfloat16* kv_commit;
+  const __nv_bfloat16* kv_pool;
+  __nv_bfloat16* out;          // [rows][H*hd]
+  float* part;                 // [rows][H][max_groups][hd + 2]
+  int32_t* counters;           // [items * KVH]
+  int32_t* err;
+  int32_t layer, H, KVH, hd, L, max_ctx, n_slots, max_groups;
+  float scale_log2;            // log2(e) / sqrt(hd)
+};
+
+struct AssembleArgs {
+  const DevNode* nodes;
+  int32_t n_rows;
+  int32_t d;
+  const __nv_bfloat16* embed;          // [V][d]
+  const __nv_bfloat16* const* attn_norm;  // device array [L] of gains
+  float* hidden;
+  __nv_bfloat16* hb;
+  float* ssq;
+  unsigned long long* best;             // zeroed for rows 0..n_rows-1 (may be null)
+};
+
+struct CopyJob { int32_t seq, slot, pos, n_layers; };
+
+struct CollapseArgs {
+  const CopyJob* jobs;
+  int32_t n_jobs;
+  __nv_bfloat16* kv_commit;
+  const __nv_bfloat16* kv_pool;
+  int32_t L, KVH, hd, max_ctx, n_slots;
+};
+
+// ---- launchers (return cudaError_t of the launch) -----------------------------------------
+// A tensor maps: up to three weight sources (QKV: wq, wk, wv; SWIGLU: wg, wu with 64-row
+// boxes); B: the activation rows with a box of nt rows.
+cudaError_t launch_gemm(int epi, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& a2,
+                        const CUtensorMap& b, const GemmArgs& args, cudaStream_t st, bool pdl);
+size_t gemm_smem_bytes(int nt, int stages);
+cudaError_t launch_attention(const AttnArgs& a, int n_items, int max_groups_launch, cudaStream_t st, bool pdl);
+cudaError_t launch_assemble(const AssembleArgs& a, cudaStream_t st, bool pdl);
+cudaError_t launch_collapse(const CollapseArgs& a, cudaStream_t st, bool pdl);
+// bf16 [n][d] rows -> bf16(h * g) rows and partial sums of squares (the exit-head input
+// of an isolated exit-head call); zeroes the argmax slots.
+cudaError_t launch_exit_prep(const __nv_bfloat16* h, int n, int d, const __nv_bfloat16* g,
+                             __nv_bfloat16* hb, float* ssq, unsigned long long* best, cudaStream_t st);
+cudaError_t launch_decode_best(const unsigned long long* best, int n, int32_t* tokens, cudaStream_t st);
+
+}  // namespace dex

@@ -1,0 +1,138 @@
+// Small kernels of a DEX round: stage-input assembly (embedding gather for stage-0
+// nodes, hidden-state hand-over for depth children), the KV collapse gather/scatter
+// that moves the new anchor path's branch KV into the committed cache, and the input
+// preparation / token decode of an isolated exit-head call.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dex {
+
+// Sum of squares of one 128-feature tile held one value per thread by four warps, in
+// the canonical order shared with the residual epilogue of the GEMM: per-warp butterfly
+// (warp_sum), then (q0 + q1) + (q2 + q3).  A row's RMSNorm scale therefore does not
+// depend on which kernel produced its partial sums.
+__device__ __forceinline__ float tile_ssq_128(float x, float* qbuf) {
+  const float s = warp_sum(__fmul_rn(x, x));
+  const int warp = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) qbuf[warp] = s;
+  __syncthreads();
+  const float t = __fadd_rn(__fadd_rn(qbuf[0], qbuf[1]), __fadd_rn(qbuf[2], qbuf[3]));
+  __syncthreads();
+  return t;
+}
+
+// One CTA (128 threads) per node row.  Stage-0 nodes start a slot chain: h = E[token]
+// into the chain's hidden row.  Depth children continue the chain's hidden row left by
+// the previous stage.  Writes the first layer's bf16 input bf16(h * g) and the RMSNorm
+// partial sums, and clears the row's exit-head argmax slot.
+__global__ void __launch_bounds__(128) assemble_kernel(const AssembleArgs a) {
+  __shared__ float qbuf[4];
+  const int row = blockIdx.x;
+  griddep_wait();
+  griddep_launch_dependents();
+  const DevNode nd = a.nodes[row];
+  if (a.best && threadIdx.x == 0) a.best[row] = 0ull;
+  const __nv_bfloat16* g = a.attn_norm[nd.first_layer];
+  float* hrow = a.hidden + static_cast<size_t>(nd.hrow) * a.d;
+  const int ndt = a.d / 128;
+  for (int t = 0; t < ndt; ++t) {
+    const int f = t * 128 + threadIdx.x;
+    float h;
+    if (nd.token >= 0) {
+      h = bf16_to_f32(a.embed[static_cast<size_t>(nd.token) * a.d + f]);
+      hrow[f] = h;
+    } else {
+      h = hrow[f];
+    }
+    a.hb[static_cast<size_t>(row) * a.d + f] = __float2bfloat16_rn(__fmul_rn(h, bf16_to_f32(g[f])));
+    const float s = tile_ssq_128(h, qbuf);
+    if (threadIdx.x == 0) a.ssq[static_cast<size_t>(row) * ndt + t] = s;
+  }
+}
+
+cudaError_t launch_assemble(const AssembleArgs& a, cudaStream_t st, bool pdl) {
+  if (a.n_rows <= 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(a.n_rows));
+  cfg.blockDim = dim3(128);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, assemble_kernel, a);
+}
+
+// Collapse gather/scatter: for each job, layers 0..n_layers-1 of the slot chain's branch
+// KV (contiguous [layer][2][KVH][hd] rows in the pool) go to position pos of the
+// committed cache.  16-byte vectors; consecutive threads cover consecutive bytes of a
+// head row on both sides.
+__global__ void __launch_bounds__(256) collapse_kernel(const CollapseArgs a) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const CopyJob job = a.jobs[blockIdx.y];
+  const int vec_per_row = a.hd / 8;
+  const int total = job.n_layers * 2 * a.KVH * vec_per_row;
+  const uint4* src = reinterpret_cast<const uint4*>(
+      a.kv_pool + (static_cast<size_t>(job.seq) * a.n_slots + job.slot) * a.L * 2 * a.KVH * a.hd);
+  for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += gridDim.x * blockDim.x) {
+    const int ch = idx % vec_per_row;
+    int rest = idx / vec_per_row;
+    const int h = rest % a.KVH;
+    rest /= a.KVH;
+    const int kv = rest & 1, layer = rest >> 1;
+    __nv_bfloat16* dst = a.kv_commit +
+                         ((((static_cast<size_t>(job.seq) * a.L + layer) * 2 + kv) * a.KVH + h) * a.max_ctx +
+                          job.pos) * a.hd + ch * 8;
+    *reinterpret_cast<uint4*>(dst) = src[idx];
+  }
+}
+
+cudaError_t launch_collapse(const CollapseArgs& a, cudaStream_t st, bool pdl) {
+  if (a.n_jobs <= 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(32, static_cast<unsigned>(a.n_jobs));
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, collapse_kernel, a);
+}
+
+// Isolated exit head: bf16 hidden rows -> bf16(h * g) and the RMSNorm partial sums.
+__global__ void __launch_bounds__(128) exit_prep_kernel(const __nv_bfloat16* h, int d, const __nv_bfloat16* g,
+                                                        __nv_bfloat16* hb, float* ssq, unsigned long long* best) {
+  __shared__ float qbuf[4];
+  const int row = blockIdx.x;
+  if (threadIdx.x == 0) best[row] = 0ull;
+  const int ndt = d / 128;
+  for (int t = 0; t < ndt; ++t) {
+    const int f = t * 128 + threadIdx.x;
+    const float x = bf16_to_f32(h[static_cast<size_t>(row) * d + f]);
+    hb[static_cast<size_t>(row) * d + f] = __float2bfloat16_rn(__fmul_rn(x, bf16_to_f32(g[f])));
+    const float s = tile_ssq_128(x, qbuf);
+    if (threadIdx.x == 0) ssq[static_cast<size_t>(row) * ndt + t] = s;
+  }
+}
+
+cudaError_t launch_exit_prep(const __nv_bfloat16* h, int n, int d, const __nv_bfloat16* g, __nv_bfloat16* hb,
+                             float* ssq, unsigned long long* best, cudaStream_t st) {
+  exit_prep_kernel<<<n, 128, 0, st>>>(h, d, g, hb, ssq, best);
+  return cudaGetLastError();
+}
+
+__global__ void decode_best_kernel(const unsigned long long* best, int n, int32_t* tokens) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) tokens[i] = static_cast<int32_t>(~static_cast<uint32_t>(best[i] & 0xffffffffull));
+}
+
+cudaError_t launch_decode_best(const unsigned long long* best, int n, int32_t* tokens, cudaStream_t st) {
+  decode_best_kernel<<<(n + 127) / 128, 128, 0, st>>>(best, n, tokens);
+  return cudaGetLastError();
+}
+
+}  // namespace dex
