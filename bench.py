@@ -1,0 +1,328 @@
+#!/usr/bin/env python
+"""Benchmark: committed tokens/s and layers per committed token of DEX decoding on GB300.
+
+Workload (default): Llama-2-7B-shaped decoder (32 layers, d 4096, 32 x 128 MHA, SwiGLU
+11008, vocab 32000, seeded bf16 weights, residual scale alpha 0.05), exploration set
+X = {8, 16, 24, 32}, batch 1, prompt of 512 uniform-random ids, 256 greedy tokens.
+
+One step = one request: prefill the prompt, then DEX rounds until 256 tokens are
+committed.  ``value`` is committed tokens / device time of the decode (CUDA events on
+the library's stream around dex_generate; weights, prompt KV and lattice state resident
+in HBM; the prefill of the next step happens outside the timed windows).  ``e2e`` is the
+same request timed end to end through the C ABI with host buffers: host prompt in,
+prefill, decode, host tokens out.  The weights (13.5 GB) exceed L2 (129 MB) many times
+over, so no flush is needed between steps.
+
+Multi-GPU: replicas only (one independent request stream per rank, launched with
+torch.distributed.run); ``value`` = all ranks' tokens / the slowest rank's time.
+
+``--impl reference`` times the fp64 CPU oracle (oracle/) on the same workload: each step
+is a bounded sample (prefill of the prompt plus one committed DEX token).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import dex_inputs as di  # noqa: E402
+
+METRIC = "committed tokens/s (1 GB300, batch 1) and layers executed per committed token"
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _workload(args):
+    return di.workload(args.workload, **({"max_new": args.tokens} if args.tokens else {}))
+
+
+def run_gpu(args):
+    import torch
+    import lossless_depth_adaptive_gb300 as dexlib
+
+    rank, world, local = _dist()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    wl = _workload(args)
+    shape = wl.shape
+    w = di.gen_weights(shape, wl.alpha, seed=wl.weight_seed, device="cuda")
+    prompt_cpu = di.gen_prompts(shape, 1, wl.prompt_len, seed=wl.prompt_seed + 1000 * rank)[0]
+    prompt = prompt_cpu.tolist()
+    T = wl.max_new
+    max_ctx = wl.prompt_len + T + len(wl.X) + 8
+    dec = dexlib.Decoder(shape, w, wl.X, batch=1, max_ctx=max_ctx, max_new=T, sample=wl.sample, tau=wl.tau,
+                         seed=wl.gumbel_seed, decs=wl.decs)
+    st = torch.cuda.current_stream()
+    import ctypes as C
+    out_host = (C.c_int32 * T)()
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum_over_ranks(x):
+        if world == 1:
+            return x
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+        return float(t.item())
+
+    # warm-up requests
+    for _ in range(args.warmup):
+        dec.prefill(0, prompt)
+        dec.generate(out=out_host)
+    # ---- device-timed decode (value) ----
+    dec.reset_stats()
+    barrier()
+    ms = 0.0
+    tokens_ref = None
+    with ClockSampler(local) as clk:
+        for _ in range(args.steps):
+            dec.prefill(0, prompt)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            toks = dec.generate(out=out_host)[0]
+            e1.record(st)
+            e1.synchronize()
+            ms += e0.elapsed_time(e1)
+            if tokens_ref is None:
+                tokens_ref = toks
+            assert toks == tokens_ref, "decode is not deterministic across requests"
+    barrier()
+    stats = dec.stats()
+    launches = stats["kernel_launches"]
+    ms = max_over_ranks(ms)
+    total_tokens = sum_over_ranks(args.steps * T)
+    value = total_tokens / (ms / 1000.0)
+    ms_per_step = ms / args.steps
+    # ---- end to end through the C ABI with host buffers (e2e) ----
+    dec.reset_stats()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        dec.prefill(0, prompt)               # host prompt -> device inside
+        dec.generate(out=out_host)           # tokens -> host inside
+    barrier()
+    e2e_s = max_over_ranks(time.perf_counter() - t0)
+    st_e2e = dec.stats()
+    e2e = {"value": sum_over_ranks(args.steps * T) / e2e_s, "unit": "tokens/s",
+           "h2d_bytes_per_step": int(st_e2e["h2d_bytes"] / args.steps),
+           "d2h_bytes_per_step": int(st_e2e["d2h_bytes"] / args.steps)}
+    # ---- one instrumented request: per-GEMM events and phase split ----
+    dec.set_timing(2)
+    dec.reset_stats()
+    dec.prefill(0, prompt)
+    dec.reset_stats()
+    dec.generate(out=out_host)
+    inst = dec.stats()
+    dec.set_timing(0)
+    dec.close()
+    hbm, bf16, src = _peaks()
+    achieved = inst["gemm_bytes"] / (inst["ms_gemm"] / 1000.0) / 1e9 if inst["ms_gemm"] > 0 else None
+    commits = stats["commits"]
+    algo_bytes = stats["weight_bytes"] + stats["kv_bytes"]
+    step_roof = {"algorithmic_bytes_per_step": int(algo_bytes / args.steps),
+                 "roofline_ms_per_step": algo_bytes / args.steps / (hbm * 1e9) * 1e3,
+                 "frac": (algo_bytes / (hbm * 1e9)) / (ms / 1e3 / max(1, world)) if ms > 0 else None}
+    layers = {"depth_charge_per_token": stats["depth_charge"] / commits,
+              "layer_passes_per_token": stats["layer_passes"] / commits,
+              "node_layers_per_token": stats["node_layers"] / commits,
+              "rounds_per_token": stats["rounds"] / commits,
+              "nodes_per_round": stats["nodes"] / stats["rounds"],
+              "kstar_hist": stats["kstar_hist"][:len(wl.X)]}
+    phases = {k: inst[k] / inst["rounds"] for k in ("ms_expand", "ms_exit", "ms_collapse", "ms_host")}
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "committed tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded weights and uniform-random prompt ids)",
+        "config": {"workload": wl.name, "model": "llama2-7b-shaped", "X": wl.X, "alpha": wl.alpha,
+                   "global_batch": world, "prompt_len": wl.prompt_len, "new_tokens": T,
+                   "decode": "sample" if wl.sample else "greedy", "parallelism": f"replicas{world}",
+                   "l2": "weights 13.5 GB streamed per round >> 129 MB L2; no flush"},
+        "layers_per_token": {k: (round(v, 3) if isinstance(v, float) else v) for k, v in layers.items()},
+        "step_roofline": step_roof,
+        "phase_ms_per_round": {k: round(v, 4) for k, v in phases.items()},
+        "roofline": {"bound": "hbm", "kernel": "gemm_tc_kernel (all linear layers, one instrumented request)",
+                     "achieved": round(achieved, 1) if achieved else None, "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4) if achieved else None, "peak_source": src,
+                     "traffic": None, "launches": inst["gemm_launches"],
+                     "bytes_per_launch": int(inst["gemm_bytes"] / max(1, inst["gemm_launches"])),
+                     "ms_per_launch": inst["ms_gemm"] / max(1, inst["gemm_launches"])},
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(wl, w, prompt)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def _oracle_for(wl, w_gpu):
+    from oracle.model import OracleModel
+    bits = {k: di.bf16_bits(v) for k, v in w_gpu.items()}
+    return OracleModel(wl.shape, bits, keep_widened=True)
+
+
+def cpu_baseline(wl, w_gpu, prompt, n_tokens=1):
+    """Time the oracle on a bounded sample of the workload: prefill + n committed DEX tokens."""
+    from oracle import dex as odex
+    m = _oracle_for(wl, w_gpu)
+    rule = odex.Rule(sample=wl.sample, tau=wl.tau, seed=wl.gumbel_seed)
+    t0 = time.perf_counter()
+    r = odex.dex_generate(m, prompt, wl.X, n_tokens, rule=rule, use_decs=wl.decs)
+    dt = time.perf_counter() - t0
+    return {"value": round(len(r.tokens) / dt, 5), "unit": "committed tokens/s", "cores": os.cpu_count(),
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": f"fp64 oracle: prefill {len(prompt) - 1} positions + {n_tokens} committed DEX token(s) "
+                      f"({r.rounds} rounds) of the {wl.name} workload"}
+
+
+def run_reference(args):
+    """The oracle as the reference arm, on rank 0 only."""
+    rank, world, local = _dist()
+    if rank != 0:
+        return
+    import torch
+    wl = _workload(args)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    w = di.gen_weights(wl.shape, wl.alpha, seed=wl.weight_seed, device=dev)
+    prompt = di.gen_prompts(wl.shape, 1, wl.prompt_len, seed=wl.prompt_seed)[0].tolist()
+    from oracle import dex as odex
+    m = _oracle_for(wl, w)
+    del w
+    rule = odex.Rule(sample=wl.sample, tau=wl.tau, seed=wl.gumbel_seed)
+    for _ in range(args.warmup):
+        odex.dex_generate(m, prompt, wl.X, 1, rule=rule, use_decs=wl.decs)
+    t0 = time.perf_counter()
+    n = 0
+    for _ in range(args.steps):
+        n += len(odex.dex_generate(m, prompt, wl.X, 1, rule=rule, use_decs=wl.decs).tokens)
+    dt = time.perf_counter() - t0
+    v = n / dt
+    sample = f"fp64 oracle: per step, prefill {wl.prompt_len - 1} positions + 1 committed DEX token"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "committed tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": wl.name, "model": "llama2-7b-shaped", "X": wl.X,
+                                        "global_batch": 1, "prompt_len": wl.prompt_len},
+        "cpu_baseline": {"value": round(v, 6), "unit": "committed tokens/s", "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(v, 6), "unit": "committed tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["dex", "reference"], default="dex")
+    ap.add_argument("--workload", default="llama7b_x4", choices=sorted(di.WORKLOADS))
+    ap.add_argument("--tokens", type=int, default=0, help="override the new-token count")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "dex":
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
