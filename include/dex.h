@@ -178,6 +178,27 @@ int dex_exit_head_decs(const void* h, int32_t n, int32_t d, const void* final_no
                        const int32_t* priors, int32_t sample, float tau, uint64_t seed,
                        int32_t* tokens, float* logits, void* stream);
 
+/* Size of the fixed device scratch of dex_exit_head_decs_noalloc: 32 MiB per GPU. */
+#define DEX_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* The same exit head + DECS as dex_exit_head_decs, for callers that must not allocate
+ * device memory during the call (for example code running under another component's
+ * stream capture or allocator, or with a memory budget fixed at start-up).  The paper has
+ * no counterpart: this is a deployment convenience of this library.
+ * Scratch comes from one file-scope device array of DEX_NOALLOC_SCRATCH_BYTES that every
+ * GPU loading the library keeps until the process exits; no cudaMalloc/cudaFree or other
+ * allocating routine is called.  The array's device address is looked up on the first call
+ * made on each device (with that device current), so make that first call before any
+ * stream capture.  Calls share the array: calls that may overlap on the GPU (different
+ * streams, or several host threads) race and must be serialised by the caller.  Returns
+ * DEX_ECAPACITY, doing nothing, when the call's scratch (hidden tile, RMSNorm partials,
+ * split-K partials) would exceed DEX_NOALLOC_SCRATCH_BYTES; other arguments and errors as
+ * dex_exit_head_decs. */
+int dex_exit_head_decs_noalloc(const void* h, int32_t n, int32_t d, const void* final_norm, float rms_eps,
+                               const void* lm_head, int32_t vocab, const dex_exit_node* nodes,
+                               const int32_t* priors, int32_t sample, float tau, uint64_t seed,
+                               int32_t* tokens, float* logits, void* stream);
+
 /* Geometry of the KV caches used by dex_kv_collapse.  committed: [batch][n_layers][2]
  * [n_kv_heads][max_ctx][head_dim] bf16; pool: [batch][n_slots][n_layers][2]
  * [n_kv_heads][head_dim] bf16 (one slot per sampling-slot chain). */

@@ -104,6 +104,8 @@ SIGNATURES = {
     "dex_free": (None, [P]),
     "dex_exit_head_decs": (C.c_int, [P, C.c_int32, C.c_int32, P, C.c_float, P, C.c_int32, P, P, C.c_int32,
                                      C.c_float, C.c_uint64, P, P, P]),
+    "dex_exit_head_decs_noalloc": (C.c_int, [P, C.c_int32, C.c_int32, P, C.c_float, P, C.c_int32, P, P,
+                                             C.c_int32, C.c_float, C.c_uint64, P, P, P]),
     "dex_kv_collapse": (C.c_int, [P, P, C.POINTER(dex_kv_geom), P, C.c_int32, P]),
     "dex_lattice_new": (C.c_int, [I32P, C.c_int32, C.c_int32, C.c_int32, C.POINTER(P)]),
     "dex_lattice_start": (C.c_int, [P, C.c_int32, C.c_int32, C.c_int32]),
@@ -226,6 +228,18 @@ def dex_exit_head_decs(h_ptr: int, n: int, d: int, final_norm_ptr: int, rms_eps:
     check(lib().dex_exit_head_decs(P(h_ptr), n, d, P(final_norm_ptr), rms_eps, P(lm_head_ptr), vocab,
                                    P(nodes_ptr), P(priors_ptr), int(sample), tau, seed, P(tokens_ptr),
                                    P(logits_ptr or None), P(stream)), "dex_exit_head_decs")
+
+
+def dex_exit_head_decs_noalloc(h_ptr: int, n: int, d: int, final_norm_ptr: int, rms_eps: float,
+                               lm_head_ptr: int, vocab: int, nodes_ptr: int, priors_ptr: int, sample: bool,
+                               tau: float, seed: int, tokens_ptr: int, logits_ptr: int = 0, stream: int = 0) -> int:
+    """Allocation-free exit head + DECS; returns the status code (raises on other errors)."""
+    rc = lib().dex_exit_head_decs_noalloc(P(h_ptr), n, d, P(final_norm_ptr), rms_eps, P(lm_head_ptr), vocab,
+                                          P(nodes_ptr), P(priors_ptr), int(sample), tau, seed, P(tokens_ptr),
+                                          P(logits_ptr or None), P(stream))
+    if rc not in (DEX_OK, DEX_ECAPACITY):
+        check(rc, "dex_exit_head_decs_noalloc")
+    return rc
 
 
 def dex_kv_collapse(committed_ptr: int, pool_ptr: int, geom: dex_kv_geom, jobs_ptr: int, n_jobs: int,

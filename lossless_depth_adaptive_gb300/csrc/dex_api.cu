@@ -14,6 +14,7 @@
 #include <algorithm>
 #include <chrono>
 #include <memory>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -996,3 +997,110 @@ int dex_kv_collapse(void* committed, const void* pool, const dex_kv_geom* g, con
 }
 
 }  // extern "C"
+
+// ---- exit head + DECS without any allocation ------------------------------------------------
+//
+// For callers that cannot allocate device memory while they run: code executing inside a
+// region that is being captured into a CUDA graph on a stream whose allocator they do not
+// own, embedders whose memory budget is fixed up front, or real-time loops that must not
+// hit the driver's allocator.  The scratch of dex_exit_head_decs lives instead in one
+// file-scope device array, present on every GPU that loads this library until the process
+// exits.  Its device address is looked up once per device, on that device's first call.
+
+static __device__ __align__(256) unsigned char g_exit_scratch[DEX_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_exit_scratch_mu;
+void* g_exit_scratch_addr[256] = {};   // device ordinal -> address of g_exit_scratch there
+
+// The array's name is only a host-side handle; the kernels need its device address,
+// which cudaGetSymbolAddress returns for the device that is current.
+int exit_scratch_address(int dev, void** out) {
+  if (dev < 0 || dev >= 256) return DEX_ENODEV;
+  std::lock_guard<std::mutex> lock(g_exit_scratch_mu);
+  if (!g_exit_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_exit_scratch) != cudaSuccess || !p) return DEX_ECUDA;
+    g_exit_scratch_addr[dev] = p;
+  }
+  *out = g_exit_scratch_addr[dev];
+  return DEX_OK;
+}
+}  // namespace
+
+extern "C" int dex_exit_head_decs_noalloc(const void* hidden, int32_t n, int32_t d, const void* final_norm,
+                                          float rms_eps, const void* lm_head, int32_t vocab,
+                                          const dex_exit_node* nodes, const int32_t* priors, int32_t sample,
+                                          float tau, uint64_t seed, int32_t* tokens, float* logits, void* stream) {
+  if (!hidden || !final_norm || !lm_head || !nodes || !tokens || n < 1 || n > 256 || d < 128 || d % 128 ||
+      vocab < 2 || (sample && !(tau > 0)))
+    return DEX_EINVAL;
+  if (get_encoder()) return DEX_ECUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int dev = 0, n_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return DEX_ENODEV;
+  // same split and scratch layout as dex_exit_head_decs
+  const int n_tiles = (vocab + 127) / 128, kb = (d + 63) / 64;
+  const int S = splits_for(n_tiles, kb, n_sm);
+  const int nt = (n + 15) & ~15;
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t o_hb = 0, o_ssq = o_hb + up(static_cast<size_t>(nt) * d * 2);
+  const size_t o_best = o_ssq + up(static_cast<size_t>(n) * (d / 128) * 4);
+  const size_t o_nodes = o_best + up(static_cast<size_t>(n) * 8);
+  const size_t o_cnt = o_nodes + up(static_cast<size_t>(n) * sizeof(dex::DevNode));
+  const size_t o_err = o_cnt + up(static_cast<size_t>(n_tiles) * 4);
+  const size_t o_part = o_err + 256;
+  const size_t total = o_part + (S > 1 ? static_cast<size_t>(S) * 256 * n_tiles * 128 * 4 : 0);
+  if (total > DEX_NOALLOC_SCRATCH_BYTES) return DEX_ECAPACITY;   // does not fit the fixed scratch
+  void* base = nullptr;
+  const int rc0 = exit_scratch_address(dev, &base);
+  if (rc0) return rc0;
+  uint8_t* scratch = static_cast<uint8_t*>(base);
+  bf16* hb = reinterpret_cast<bf16*>(scratch + o_hb);
+  float* ssq = reinterpret_cast<float*>(scratch + o_ssq);
+  unsigned long long* best = reinterpret_cast<unsigned long long*>(scratch + o_best);
+  dex::DevNode* dn = reinterpret_cast<dex::DevNode*>(scratch + o_nodes);
+  int32_t* cnt = reinterpret_cast<int32_t*>(scratch + o_cnt);
+  CUtensorMap tm_w, tm_b;
+  if (encode_2d(&tm_w, lm_head, vocab, d, 128) || encode_2d(&tm_b, hb, nt, d, nt)) return DEX_EINVAL;
+  // the array keeps the previous call's contents: clear what the kernels expect at zero
+  // (padding rows of the node tile, split-K arrival counters, the stall flag)
+  if (cudaMemsetAsync(hb, 0, static_cast<size_t>(nt) * d * 2, st) != cudaSuccess ||
+      cudaMemsetAsync(cnt, 0, o_part - o_cnt, st) != cudaSuccess)
+    return DEX_ECUDA;
+  if (dex::launch_exit_prep(static_cast<const bf16*>(hidden), n, d, static_cast<const bf16*>(final_norm), hb, ssq,
+                            best, st) != cudaSuccess)
+    return DEX_ECUDA;
+  exit_nodes_kernel<<<(n + 127) / 128, 128, 0, st>>>(nodes, n, dn);
+  if (cudaGetLastError() != cudaSuccess) return DEX_ECUDA;
+  dex::GemmArgs a = {};
+  a.n = n;
+  a.nt = nt;
+  a.b_row0 = 0;
+  a.kblocks = kb;
+  a.splits = S;
+  a.stages = 4;
+  a.n_tiles = n_tiles;
+  a.src_tiles0 = n_tiles;
+  a.tmem_cols = pow2_at_least(nt);
+  a.partial = reinterpret_cast<float*>(scratch + o_part);
+  a.counters = cnt;
+  a.err = reinterpret_cast<int32_t*>(scratch + o_err);
+  a.nodes = dn;
+  a.evict_first = 1;
+  a.d = d;
+  a.vocab = vocab;
+  a.eps = rms_eps;
+  a.ssq_in = ssq;
+  a.logits_dbg = logits;
+  a.best = best;
+  a.priors = priors;
+  a.sample = sample;
+  a.tau = tau;
+  a.seed = seed;
+  if (dex::launch_gemm(dex::EPI_EXIT, tm_w, tm_w, tm_w, tm_b, a, st, false) != cudaSuccess) return DEX_ECUDA;
+  if (dex::launch_decode_best(best, n, tokens, st) != cudaSuccess) return DEX_ECUDA;
+  return DEX_OK;
+}
