@@ -1,0 +1,62 @@
+"""Run one DEX request inside a profiler window (for ncu --profile-from-start off).
+
+    python -m lossless_depth_adaptive_gb300.profile_case --workload llama7b_x4 --tokens 8
+    python -m lossless_depth_adaptive_gb300.profile_case --workload llama7b_x4 --layers 4 --tokens 2
+
+Builds the workload's seeded weights (optionally only the first ``--layers`` layers, with
+the exploration set rescaled to the same number of stages), prefills the prompt, runs
+``--warmup`` untimed requests, then opens the CUDA profiler window for exactly one
+request's decode (``--tokens`` committed tokens) and closes it.
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def main():
+    import torch
+
+    import dex_inputs as di
+    import lossless_depth_adaptive_gb300 as dexlib
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", default="llama7b_x4", choices=sorted(di.WORKLOADS))
+    ap.add_argument("--layers", type=int, default=0, help="keep only the first n layers")
+    ap.add_argument("--tokens", type=int, default=8)
+    ap.add_argument("--warmup", type=int, default=1)
+    ap.add_argument("--ar", action="store_true", help="profile plain autoregressive rounds")
+    a = ap.parse_args()
+    wl = di.workload(a.workload)
+    shape, X = wl.shape, list(wl.X)
+    if a.layers:
+        N = len(X)
+        assert a.layers % N == 0, "--layers must be a multiple of the number of stages"
+        shape = di.ModelShape(**{**shape.__dict__, "n_layers": a.layers})
+        X = [a.layers // N * (k + 1) for k in range(N)]
+    w = di.gen_weights(shape, wl.alpha, seed=wl.weight_seed, device="cuda")
+    prompt = di.gen_prompts(shape, 1, wl.prompt_len, seed=wl.prompt_seed)[0].tolist()
+    dec = dexlib.Decoder(shape, w, X, batch=1, max_ctx=wl.prompt_len + a.tokens + len(X) + 8,
+                         max_new=a.tokens, sample=wl.sample, tau=wl.tau, seed=wl.gumbel_seed, decs=wl.decs)
+    for _ in range(a.warmup):
+        dec.prefill(0, prompt)
+        dec.generate(ar=a.ar)
+    dec.prefill(0, prompt)
+    torch.cuda.synchronize()
+    torch.cuda.profiler.start()
+    toks = dec.generate(ar=a.ar)[0]
+    torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
+    st = dec.stats()
+    dec.close()
+    print(f"profiled {a.tokens} tokens ({'AR' if a.ar else 'DEX'}), layers {shape.n_layers}, X {X}: "
+          f"{toks[:8]}..., kernel launches so far {st['kernel_launches']}")
+
+
+if __name__ == "__main__":
+    main()
