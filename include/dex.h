@@ -52,7 +52,7 @@ typedef enum dex_status {
  * into wo and wd.  layers points to a HOST array of n_layers * 9 DEVICE pointers,
  * per layer in the order: attn_norm[d], wq[H*hd][d], wk[KVH*hd][d], wv[KVH*hd][d],
  * wo[d][H*hd], ffn_norm[d], wg[d_ff][d], wu[d_ff][d], wd[d][d_ff].  The array is
- * copied by dex_init().  Constraints: d_model % 128 == 0, head_dim in {64, 128},
+ * copied by dex_init().  Constraints: d_model % 128 == 0 and <= 8192, head_dim in {64, 128},
  * n_heads % n_kv_heads == 0, every row length a multiple of 8 elements, every weight
  * 16-byte aligned. */
 typedef struct dex_model {
@@ -71,7 +71,7 @@ typedef struct dex_model {
  * for dex_debug_logits() (costs vocab*4 bytes per node of device memory). */
 typedef struct dex_decode_cfg {
   int32_t batch;        /* independent sequences, 1..64 */
-  int32_t max_ctx;      /* capacity in positions per sequence (prompt + new + N) */
+  int32_t max_ctx;      /* capacity in positions per sequence (prompt + new + N), <= 4096 */
   int32_t max_new;      /* tokens to commit per sequence */
   int32_t sample;
   float tau;
@@ -171,7 +171,7 @@ typedef struct dex_exit_node {
  * score = -inf for masked priors, else z (greedy) or z / tau + G(seed, seq, pos, v).
  * h: device bf16 [n][d]; final_norm: device bf16 [d]; lm_head: device bf16
  * [vocab][d]; nodes: device [n]; priors: device int32; tokens: device int32 [n];
- * logits: device fp32 [n][vocab] or NULL.  1 <= n <= 256, d % 128 == 0.
+ * logits: device fp32 [n][vocab] or NULL.  1 <= n <= 256, d % 128 == 0, d <= 8192.
  * Allocates its scratch with the stream-ordered allocator; stream-ordered, no sync. */
 int dex_exit_head_decs(const void* h, int32_t n, int32_t d, const void* final_norm, float rms_eps,
                        const void* lm_head, int32_t vocab, const dex_exit_node* nodes,

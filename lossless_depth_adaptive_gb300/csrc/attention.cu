@@ -7,12 +7,13 @@
 // chains and its own, read from the branch pool through the node's tail table.
 //
 // Work split: CTA = (sequence item, KV head, 128-position key group).  The committed
-// keys of the group are staged once in shared memory and reused by every node and
-// every query head of the KV head (GQA).  The arithmetic for a query is fixed by
-// absolute positions only -- 64-key chunks aligned to position 0, a per-chunk
-// softmax merged in chunk order, 128-position groups merged in group order by the
-// last CTA to finish -- so a node's output is bit-identical whether its keys sit in
-// the committed cache or the branch pool and whatever batch it is computed in.
+// keys and values of the group are staged once in shared memory by two bulk copies and
+// reused by every node and every query head of the KV head (GQA).  Each warp owns a
+// 32-key slice of the group for every query.  The arithmetic for a query is fixed by
+// absolute positions only -- 32-key slices aligned to position 0, slices combined in
+// order within the group, 128-position groups combined in group order by the last CTA
+// to finish -- so a node's output is bit-identical whether its keys sit in the
+// committed cache or the branch pool and whatever batch it is computed in.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -20,37 +21,60 @@ namespace dex {
 
 constexpr int kAttnThreads = 128;
 constexpr int kGroupPos = 128;
-constexpr int kChunkPos = 64;
 
+// q . k for one key row.  The 16-byte chunks of the row are visited starting at chunk
+// `rot` (the lane's index), so the 32 lanes reading 32 different key rows of an
+// unpadded shared-memory tile hit distinct banks; four independent partial sums shorten
+// the dependency chain.  The visiting order and the summation tree are functions of the
+// key's absolute position only (lane = position mod 32), so a key's score does not depend
+// on where the key is stored or which batch it is computed in.
 template <int HD>
-__device__ __forceinline__ float dot_q_row(const float* q, const __nv_bfloat16* krow) {
-  float s = 0.0f;
+__device__ __forceinline__ float dot_q_row(const float* q, const __nv_bfloat16* krow, int rot) {
+  constexpr int NC = HD / 8;
+  float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-  for (int c = 0; c < HD / 8; ++c) {
+  for (int i = 0; i < NC; ++i) {
+    const int c = (i + rot) & (NC - 1);
     const uint4 raw = *reinterpret_cast<const uint4*>(krow + c * 8);
+    const float4 qa = *reinterpret_cast<const float4*>(q + c * 8);
+    const float4 qb = *reinterpret_cast<const float4*>(q + c * 8 + 4);
     const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 f = __bfloat1622float2(h2[e]);
-      s = fmaf(q[c * 8 + 2 * e], f.x, s);
-      s = fmaf(q[c * 8 + 2 * e + 1], f.y, s);
-    }
+    const float2 f0 = __bfloat1622float2(h2[0]), f1 = __bfloat1622float2(h2[1]);
+    const float2 f2 = __bfloat1622float2(h2[2]), f3 = __bfloat1622float2(h2[3]);
+    float& a = s[i & 3];
+    a = fmaf(qa.x, f0.x, a);
+    a = fmaf(qa.y, f0.y, a);
+    a = fmaf(qa.z, f1.x, a);
+    a = fmaf(qa.w, f1.y, a);
+    a = fmaf(qb.x, f2.x, a);
+    a = fmaf(qb.y, f2.y, a);
+    a = fmaf(qb.z, f3.x, a);
+    a = fmaf(qb.w, f3.y, a);
   }
-  return s;
+  return __fadd_rn(__fadd_rn(s[0], s[1]), __fadd_rn(s[2], s[3]));
 }
+
+constexpr int kQBatch = 8;    // queries staged per pass
 
 template <int HD>
 __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
-  constexpr int RS = HD + 8;          // padded smem row (bf16 elements)
   constexpr int DPL = HD / 32;        // output dims per lane
-  extern __shared__ uint8_t smem_raw[];
-  __nv_bfloat16* sK = reinterpret_cast<__nv_bfloat16*>(smem_raw);
-  __nv_bfloat16* sV = sK + kGroupPos * RS;
-  float* sQ = reinterpret_cast<float*>(sV + kGroupPos * RS);   // [4 warps][HD]
+  constexpr int PS = HD + 2;          // partial record: acc[HD], m, l
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  __nv_bfloat16* sK = reinterpret_cast<__nv_bfloat16*>(smem_raw);   // [128][HD], unpadded
+  __nv_bfloat16* sV = sK + kGroupPos * HD;
+  float* sQ = reinterpret_cast<float*>(sV + kGroupPos * HD);         // [kQBatch][HD]
+  float* sP = sQ + kQBatch * HD;                                     // [kQBatch][4 warps][PS]
   __shared__ int s_last;
+  __shared__ __align__(8) uint64_t s_bar;
 
   const int g = blockIdx.x, kvh = blockIdx.y, it = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    mbar_init(&s_bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
   griddep_wait();
   griddep_launch_dependents();
   const AttnItem item = a.items[it];
@@ -58,99 +82,125 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
   const int g0 = g * kGroupPos;
   const int H = a.H, G = a.H / a.KVH;
 
-  // stage committed keys/values of positions [g0, cmax) for this KV head
+  // committed keys/values of positions [g0, cmax) for this KV head: two contiguous
+  // bulk copies (head-major cache: a head's positions are consecutive HD-element rows)
   const int cmax = min(g0 + kGroupPos, item.max_cend);
-  const size_t head_base_k =
-      (((static_cast<size_t>(item.seq) * a.L + a.layer) * 2 + 0) * a.KVH + kvh) * a.max_ctx * HD;
-  const size_t head_base_v =
-      (((static_cast<size_t>(item.seq) * a.L + a.layer) * 2 + 1) * a.KVH + kvh) * a.max_ctx * HD;
-  for (int idx = tid; idx < (cmax - g0) * (HD / 8); idx += kAttnThreads) {
-    const int p = idx / (HD / 8), ch = idx % (HD / 8);
-    const size_t off = static_cast<size_t>(g0 + p) * HD + ch * 8;
-    *reinterpret_cast<uint4*>(sK + p * RS + ch * 8) = *reinterpret_cast<const uint4*>(a.kv_commit + head_base_k + off);
-    *reinterpret_cast<uint4*>(sV + p * RS + ch * 8) = *reinterpret_cast<const uint4*>(a.kv_commit + head_base_v + off);
-  }
-  __syncthreads();
-
-  const int nrows = item.row_end - item.row_begin;
-  const int nq = nrows * G;
-  float* q = sQ + warp * HD;
-  for (int qi = warp; qi < nq; qi += 4) {
-    const int row = item.row_begin + qi / G;
-    const int qh = kvh * G + qi % G;
-    const DevNode nd = a.nodes[row];
-    const int pos = nd.pos, c_end = nd.c_end;
-    for (int d = lane; d < HD; d += 32) q[d] = a.q[(static_cast<size_t>(row) * H + qh) * HD + d] * a.scale_log2;
-    __syncwarp();
-    auto branch_row = [&](int k, int kv) -> const __nv_bfloat16* {
-      int t = k - c_end;
-      if (t >= nd.n_tail) {   // cannot happen for a well-formed plan; never read out of bounds
-        atomicExch(a.err, DEV_BAD_INDEX);
-        t = nd.n_tail - 1;
-      }
-      const int slot = a.tails[nd.tail_off + t];
-      return a.kv_pool +
-             ((((static_cast<size_t>(nd.seq) * a.n_slots + slot) * a.L + a.layer) * 2 + kv) * a.KVH + kvh) * HD;
-    };
-    float m = -INFINITY, l = 0.0f, acc[DPL];
-#pragma unroll
-    for (int i = 0; i < DPL; ++i) acc[i] = 0.0f;
-    for (int c = g0; c < g0 + kGroupPos && c <= pos; c += kChunkPos) {
-      float s[2];
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const int k = c + lane + 32 * t;
-        if (k > pos) {
-          s[t] = -INFINITY;
-        } else {
-          const __nv_bfloat16* kr = k < c_end ? sK + (k - g0) * RS : branch_row(k, 0);
-          s[t] = dot_q_row<HD>(q, kr);
-        }
-      }
-      const float mc = warp_max(fmaxf(s[0], s[1]));
-      const float p0 = exp2f(s[0] - mc), p1 = exp2f(s[1] - mc);
-      const float lc = warp_sum(p0 + p1);
-      float accc[DPL];
-#pragma unroll
-      for (int i = 0; i < DPL; ++i) accc[i] = 0.0f;
-      const int kend = min(c + kChunkPos - 1, pos);
-      for (int k = c; k <= kend; ++k) {
-        const float mine = (k - c) < 32 ? p0 : p1;
-        const float pk = __shfl_sync(0xffffffffu, mine, (k - c) & 31);
-        const __nv_bfloat16* vr = k < c_end ? sV + (k - g0) * RS : branch_row(k, 1);
-        if (DPL == 4) {
-          const uint2 raw = *reinterpret_cast<const uint2*>(vr + lane * 4);
-          const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
-          const float2 f0 = __bfloat1622float2(h2[0]), f1 = __bfloat1622float2(h2[1]);
-          accc[0] = fmaf(pk, f0.x, accc[0]);
-          accc[1] = fmaf(pk, f0.y, accc[1]);
-          accc[2] = fmaf(pk, f1.x, accc[2]);
-          accc[3] = fmaf(pk, f1.y, accc[3]);
-        } else {
-          const __nv_bfloat162 h2 = *reinterpret_cast<const __nv_bfloat162*>(vr + lane * 2);
-          const float2 f0 = __bfloat1622float2(h2);
-          accc[0] = fmaf(pk, f0.x, accc[0]);
-          accc[1] = fmaf(pk, f0.y, accc[1]);
-        }
-      }
-      const float mn = fmaxf(m, mc);
-      const float sa = exp2f(m - mn), sb = exp2f(mc - mn);
-      l = l * sa + lc * sb;
-#pragma unroll
-      for (int i = 0; i < DPL; ++i) acc[i] = acc[i] * sa + accc[i] * sb;
-      m = mn;
+  if (cmax > g0) {
+    if (tid == 0) {
+      const size_t kbase =
+          ((((static_cast<size_t>(item.seq) * a.L + a.layer) * 2 + 0) * a.KVH + kvh) * a.max_ctx + g0) * HD;
+      const size_t vbase =
+          ((((static_cast<size_t>(item.seq) * a.L + a.layer) * 2 + 1) * a.KVH + kvh) * a.max_ctx + g0) * HD;
+      const uint32_t bytes = static_cast<uint32_t>(cmax - g0) * HD * 2;
+      mbar_arrive_expect_tx(&s_bar, 2 * bytes);
+      bulk_load_1d(sK, a.kv_commit + kbase, bytes, &s_bar);
+      bulk_load_1d(sV, a.kv_commit + vbase, bytes, &s_bar);
     }
-    float* pp = a.part + ((static_cast<size_t>(row) * H + qh) * a.max_groups + g) * (HD + 2);
-#pragma unroll
-    for (int i = 0; i < DPL; ++i) __stcg(pp + lane * DPL + i, acc[i]);
-    if (lane == 0) {
-      __stcg(pp + HD, m);
-      __stcg(pp + HD + 1, l);
+    if (!mbar_wait(&s_bar, 0, a.err, DEV_TIMEOUT_FULL)) {
+      mbar_wait(&s_bar, 0, nullptr, 0);   // the copies may still land: wait (bounded) before exiting
+      return;
     }
-    __syncwarp();
   }
 
-  // the last group CTA of (item, KV head) merges the groups in order
+  const int nq = (item.row_end - item.row_begin) * G;
+  const int ks = g0 + 32 * warp;       // this warp's 32-key slice
+  const int k = ks + lane;             // this lane's key
+  for (int qb = 0; qb < nq; qb += kQBatch) {
+    const int nb = min(kQBatch, nq - qb);
+    for (int idx = tid; idx < nb * HD; idx += kAttnThreads) {
+      const int qi = qb + idx / HD, d = idx % HD;
+      const int row = item.row_begin + qi / G, qh = kvh * G + qi % G;
+      sQ[idx] = a.q[(static_cast<size_t>(row) * H + qh) * HD + d] * a.scale_log2;
+    }
+    __syncthreads();
+    // each warp: its 32-key slice against every query of the batch
+    for (int j = 0; j < nb; ++j) {
+      const int qi = qb + j;
+      const DevNode nd = a.nodes[item.row_begin + qi / G];
+      const int pos = nd.pos, c_end = nd.c_end;
+      auto key_row = [&](int kk, int kv) -> const __nv_bfloat16* {
+        if (kk < c_end) return (kv ? sV : sK) + (kk - g0) * HD;
+        int t = kk - c_end;
+        if (t >= nd.n_tail) {   // cannot happen for a well-formed plan; never read out of bounds
+          atomicExch(a.err, DEV_BAD_INDEX);
+          t = nd.n_tail - 1;
+        }
+        const int slot = a.tails[nd.tail_off + t];
+        return a.kv_pool +
+               ((((static_cast<size_t>(nd.seq) * a.n_slots + slot) * a.L + a.layer) * 2 + kv) * a.KVH + kvh) * HD;
+      };
+      const float s = (k <= pos) ? dot_q_row<HD>(sQ + j * HD, key_row(k, 0), lane) : -INFINITY;
+      const float m = warp_max(s);
+      float l = 0.0f, acc[DPL];
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) acc[i] = 0.0f;
+      if (m != -INFINITY) {
+        const float p = exp2f(s - m);
+        l = warp_sum(p);
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          if (ks + jj <= pos) {   // uniform across the warp
+            const float pk = __shfl_sync(0xffffffffu, p, jj);
+            const __nv_bfloat16* vr = key_row(ks + jj, 1);
+            if constexpr (DPL == 4) {
+              const uint2 raw = *reinterpret_cast<const uint2*>(vr + lane * 4);
+              const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+              const float2 f0 = __bfloat1622float2(h2[0]), f1 = __bfloat1622float2(h2[1]);
+              acc[0] = fmaf(pk, f0.x, acc[0]);
+              acc[1] = fmaf(pk, f0.y, acc[1]);
+              acc[2] = fmaf(pk, f1.x, acc[2]);
+              acc[3] = fmaf(pk, f1.y, acc[3]);
+            } else {
+              const __nv_bfloat162 h2 = *reinterpret_cast<const __nv_bfloat162*>(vr + lane * 2);
+              const float2 f0 = __bfloat1622float2(h2);
+              acc[0] = fmaf(pk, f0.x, acc[0]);
+              acc[1] = fmaf(pk, f0.y, acc[1]);
+            }
+          }
+        }
+      }
+      float* rec = sP + (j * 4 + warp) * PS;
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) rec[lane * DPL + i] = acc[i];
+      if (lane == 0) {
+        rec[HD] = m;
+        rec[HD + 1] = l;
+      }
+    }
+    __syncthreads();
+    // combine the four slices of each query in slice order; write the group's record
+    for (int j = warp; j < nb; j += 4) {
+      const int qi = qb + j;
+      const int row = item.row_begin + qi / G, qh = kvh * G + qi % G;
+      const float* r0 = sP + (j * 4) * PS;
+      float mw[4], wgt[4];
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        mw[w] = r0[w * PS + HD];
+        M = fmaxf(M, mw[w]);
+      }
+#pragma unroll
+      for (int w = 0; w < 4; ++w) wgt[w] = (mw[w] == -INFINITY) ? 0.0f : exp2f(mw[w] - M);
+      const float Lg = __fadd_rn(__fadd_rn(r0[0 * PS + HD + 1] * wgt[0], r0[1 * PS + HD + 1] * wgt[1]),
+                                 __fadd_rn(r0[2 * PS + HD + 1] * wgt[2], r0[3 * PS + HD + 1] * wgt[3]));
+      float* pp = a.part + ((static_cast<size_t>(row) * H + qh) * a.max_groups + g) * PS;
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) {
+        const int d = lane * DPL + i;
+        const float v = __fadd_rn(__fadd_rn(r0[0 * PS + d] * wgt[0], r0[1 * PS + d] * wgt[1]),
+                                  __fadd_rn(r0[2 * PS + d] * wgt[2], r0[3 * PS + d] * wgt[3]));
+        __stcg(pp + d, v);
+      }
+      if (lane == 0) {
+        __stcg(pp + HD, M);
+        __stcg(pp + HD + 1, Lg);
+      }
+    }
+    __syncthreads();
+  }
+
+  // the last group CTA of (item, KV head) merges the groups; lane gg holds group gg
   __threadfence();
   __syncthreads();
   if (tid == 0) s_last = (atomicAdd(a.counters + item.counter * a.KVH + kvh, 1) == item.n_groups - 1) ? 1 : 0;
@@ -158,21 +208,24 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
   if (!s_last) return;
   __threadfence();
   for (int qi = warp; qi < nq; qi += 4) {
-    const int row = item.row_begin + qi / G;
-    const int qh = kvh * G + qi % G;
-    float M = -INFINITY, Lsum = 0.0f, O[DPL];
+    const int row = item.row_begin + qi / G, qh = kvh * G + qi % G;
+    const float* base = a.part + (static_cast<size_t>(row) * H + qh) * a.max_groups * PS;
+    float mg = -INFINITY, lg = 0.0f;
+    if (lane < item.n_groups) {
+      mg = __ldcg(base + lane * PS + HD);
+      lg = __ldcg(base + lane * PS + HD + 1);
+    }
+    const float M = warp_max(mg);
+    const float wg = (lg > 0.0f) ? exp2f(mg - M) : 0.0f;
+    const float Lsum = warp_sum(lg * wg);
+    float O[DPL];
 #pragma unroll
     for (int i = 0; i < DPL; ++i) O[i] = 0.0f;
     for (int gg = 0; gg < item.n_groups; ++gg) {
-      const float* pp = a.part + ((static_cast<size_t>(row) * H + qh) * a.max_groups + gg) * (HD + 2);
-      const float mg = __ldcg(pp + HD), lg = __ldcg(pp + HD + 1);
-      if (lg == 0.0f) continue;   // no visible key in this group
-      const float mn = fmaxf(M, mg);
-      const float sa = exp2f(M - mn), sb = exp2f(mg - mn);
-      Lsum = Lsum * sa + lg * sb;
+      const float w = __shfl_sync(0xffffffffu, wg, gg);
+      if (w == 0.0f) continue;
 #pragma unroll
-      for (int i = 0; i < DPL; ++i) O[i] = O[i] * sa + __ldcg(pp + lane * DPL + i) * sb;
-      M = mn;
+      for (int i = 0; i < DPL; ++i) O[i] = fmaf(w, __ldcg(base + gg * PS + lane * DPL + i), O[i]);
     }
     const float invl = 1.0f / Lsum;
 #pragma unroll
@@ -180,6 +233,10 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
       a.out[static_cast<size_t>(row) * H * HD + qh * HD + lane * DPL + i] = __float2bfloat16_rn(O[i] * invl);
   }
   if (tid == 0) a.counters[item.counter * a.KVH + kvh] = 0;
+}
+
+static size_t attn_smem_bytes(int hd) {
+  return static_cast<size_t>(2) * kGroupPos * hd * 2 + kQBatch * hd * 4 + kQBatch * 4 * (hd + 2) * 4;
 }
 
 cudaError_t launch_attention(const AttnArgs& a, int n_items, int max_groups_launch, cudaStream_t st, bool pdl) {
@@ -195,7 +252,7 @@ cudaError_t launch_attention(const AttnArgs& a, int n_items, int max_groups_laun
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   if (a.hd == 128) {
-    cfg.dynamicSmemBytes = 2 * kGroupPos * (128 + 8) * 2 + 4 * 128 * 4;
+    cfg.dynamicSmemBytes = attn_smem_bytes(128);
     static bool set = false;
     if (!set) {
       cudaError_t e = cudaFuncSetAttribute(attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -206,7 +263,7 @@ cudaError_t launch_attention(const AttnArgs& a, int n_items, int max_groups_laun
     return cudaLaunchKernelEx(&cfg, attn_kernel<128>, a);
   }
   if (a.hd == 64) {
-    cfg.dynamicSmemBytes = 2 * kGroupPos * (64 + 8) * 2 + 4 * 64 * 4;
+    cfg.dynamicSmemBytes = attn_smem_bytes(64);
     static bool set = false;
     if (!set) {
       cudaError_t e = cudaFuncSetAttribute(attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,

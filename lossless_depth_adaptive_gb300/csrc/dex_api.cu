@@ -9,6 +9,8 @@
 //   the tokens -> insert / validate_and_commit / collapse on the host.
 #include <cudaTypedefs.h>
 #include <math.h>
+#include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <algorithm>
@@ -53,14 +55,6 @@ int encode_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, 
   return r == CUDA_SUCCESS ? DEX_OK : DEX_EINVAL;
 }
 
-// Fixed split-K factor of a weight shape: about four CTAs per SM in total, at least
-// eight 64-wide k-blocks (128 KB of weights) per CTA.  Depends on the shape only.
-int splits_for(int n_tiles, int kblocks, int n_sm) {
-  int s = static_cast<int>(lround(4.0 * n_sm / n_tiles));
-  s = std::min(s, std::max(1, kblocks / 8));
-  return std::max(1, s);
-}
-
 int pow2_at_least(int x) {
   int p = 32;
   while (p < x) p <<= 1;
@@ -82,6 +76,8 @@ struct dex_handle {
   dex_decode_cfg cfg = {};
   cudaStream_t st = nullptr;
   int n_sm = 0;
+  int gemm_ctas = 0;           // persistent GEMM grid (CTAs per SM x SMs), fixed per handle
+  size_t gemm_smem = 0;        // shared-memory budget of a small-tile GEMM CTA
   std::unique_ptr<dex::Lattice> lat, lat_ar;
   std::vector<int> mode;                 // per sequence: 0 idle, 1 DEX, 2 AR
   std::vector<int> n_done;
@@ -106,7 +102,6 @@ struct dex_handle {
   std::vector<CUtensorMap> tm_q, tm_k, tm_v, tm_o, tm_g, tm_u, tm_d;
   CUtensorMap tm_lm;
   CUtensorMap tm_hb[17], tm_attn[17], tm_act[17], tm_exit[17];
-  int S_qkv = 1, S_o = 1, S_gu = 1, S_d = 1, S_lm = 1;
   // bookkeeping
   dex_stats stats = {};
   int timing = 0;
@@ -120,8 +115,14 @@ struct dex_handle {
 
 namespace {
 
+bool debug_enabled() {
+  static const bool on = getenv("DEX_DEBUG") != nullptr;
+  return on;
+}
+
 int cuda_fail(dex_handle* h, cudaError_t e) {
   if (e == cudaSuccess) return DEX_OK;
+  if (debug_enabled()) fprintf(stderr, "dex: CUDA error %s (%s)\n", cudaGetErrorName(e), cudaGetErrorString(e));
   if (h) h->broken = true;
   return DEX_ECUDA;
 }
@@ -207,7 +208,6 @@ dex::GemmArgs base_args(dex_handle* h) {
   a.eps = h->eps;
   a.partial = h->partial;
   a.counters = h->counters;
-  a.stages = 4;
   a.evict_first = 1;
   return a;
 }
@@ -221,13 +221,14 @@ int gemm(dex_handle* h, int epi, const CUtensorMap& a0, const CUtensorMap& a1, c
     a.nt = (nn + 15) & ~15;
     a.b_row0 = r;
     a.tmem_cols = pow2_at_least(a.nt);
+    a.stages = dex::gemm_stages_for(a.nt, h->gemm_smem);
     cudaEvent_t e0 = nullptr, e1 = nullptr;
     if (h->timing >= 2) {
       e0 = next_event(h);
       e1 = next_event(h);
       cudaEventRecord(e0, h->st);
     }
-    cudaError_t e = dex::launch_gemm(epi, a0, a1, a2, bmaps[a.nt / 16], a, h->st, true);
+    cudaError_t e = dex::launch_gemm(epi, a0, a1, a2, bmaps[a.nt / 16], a, h->gemm_ctas, h->st, true);
     if (e != cudaSuccess) return cuda_fail(h, e);
     if (h->timing >= 2) {
       cudaEventRecord(e1, h->st);
@@ -251,7 +252,6 @@ int run_layers(dex_handle* h, const Uploaded& u, int off, int n, int l0, int l1,
     a.layer = l;
     // QKV + RoPE + KV write
     a.kblocks = (h->d + 63) / 64;
-    a.splits = h->S_qkv;
     a.src_tiles0 = qd / 128;
     a.src_tiles1 = kvd / 128;
     a.n_tiles = (qd + 2 * kvd) / 128;
@@ -292,7 +292,6 @@ int run_layers(dex_handle* h, const Uploaded& u, int off, int n, int l0, int l1,
     a.nodes = u.nodes;
     a.layer = l;
     a.kblocks = (qd + 63) / 64;
-    a.splits = h->S_o;
     a.n_tiles = h->d / 128;
     a.src_tiles0 = a.n_tiles;
     a.hidden = h->hidden;
@@ -307,7 +306,6 @@ int run_layers(dex_handle* h, const Uploaded& u, int off, int n, int l0, int l1,
     a.nodes = u.nodes;
     a.layer = l;
     a.kblocks = (h->d + 63) / 64;
-    a.splits = h->S_gu;
     a.n_tiles = (h->dff + 63) / 64;
     a.src_tiles0 = a.n_tiles;
     a.ssq_in = h->ssq;
@@ -320,7 +318,6 @@ int run_layers(dex_handle* h, const Uploaded& u, int off, int n, int l0, int l1,
     a.nodes = u.nodes;
     a.layer = l;
     a.kblocks = (h->dff + 63) / 64;
-    a.splits = h->S_d;
     a.n_tiles = h->d / 128;
     a.src_tiles0 = a.n_tiles;
     a.hidden = h->hidden;
@@ -341,6 +338,7 @@ int run_layers(dex_handle* h, const Uploaded& u, int off, int n, int l0, int l1,
 
 int check_device_error(dex_handle* h, int32_t flag) {
   if (flag == 0) return DEX_OK;
+  if (debug_enabled()) fprintf(stderr, "dex: device error flag %d\n", flag);
   cudaMemsetAsync(h->err, 0, sizeof(int32_t), h->st);
   return flag == dex::DEV_BAD_INDEX ? DEX_ECUDA : DEX_ETIMEOUT;
 }
@@ -466,7 +464,6 @@ int run_round(dex_handle* h, dex::Lattice* lat, std::vector<dex_copy_job>* pendi
     dex::GemmArgs a = base_args(h);
     a.nodes = u.nodes;
     a.kblocks = (h->d + 63) / 64;
-    a.splits = h->S_lm;
     a.n_tiles = (h->V + 127) / 128;
     a.src_tiles0 = a.n_tiles;
     a.ssq_in = h->exit_ssq;
@@ -582,14 +579,14 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
              dex_handle** out) {
   if (!m || !X || !cfg || !out) return DEX_EINVAL;
   *out = nullptr;
-  if (m->n_layers < 1 || m->d_model % 128 || (m->head_dim != 64 && m->head_dim != 128) || m->n_kv_heads < 1 ||
+  if (m->n_layers < 1 || m->d_model % 128 || m->d_model > 8192 || (m->head_dim != 64 && m->head_dim != 128) || m->n_kv_heads < 1 ||
       m->n_heads % m->n_kv_heads || (m->n_heads * m->head_dim) % 128 || (m->n_kv_heads * m->head_dim) % 128 ||
       m->d_ff < 64 || m->d_ff % 8 || m->vocab < 2 || !m->embed || !m->final_norm || !m->lm_head || !m->layers)
     return DEX_EINVAL;
   if (n_X < 1 || n_X > 10 || X[n_X - 1] != m->n_layers) return DEX_EINVAL;
   for (int i = 0; i < n_X; ++i)
     if (X[i] < 1 || (i > 0 && X[i] <= X[i - 1])) return DEX_EINVAL;
-  if (cfg->batch < 1 || cfg->batch > 64 || cfg->max_ctx < 2 || cfg->max_new < 1 || (cfg->sample && !(cfg->tau > 0)))
+  if (cfg->batch < 1 || cfg->batch > 64 || cfg->max_ctx < 2 || cfg->max_ctx > 4096 || cfg->max_new < 1 || (cfg->sample && !(cfg->tau > 0)))
     return DEX_EINVAL;
   int dev = 0;
   cudaDeviceProp prop;
@@ -622,6 +619,17 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
   h->cfg = *cfg;
   h->st = static_cast<cudaStream_t>(stream);
   h->n_sm = prop.multiProcessorCount;
+  // GEMM launch shape (tunable for experiments; the partition, hence every result,
+  // depends on it, so it is fixed for the handle's lifetime)
+  {
+    const char* c = getenv("DEX_GEMM_CTAS_PER_SM");
+    const char* m = getenv("DEX_GEMM_SMEM_KB");
+    const int cps = c ? atoi(c) : 2;
+    const int kb = m ? atoi(m) : 104;
+    if (cps < 1 || cps > 4 || kb < 32 || kb > 227) return DEX_EINVAL;
+    h->gemm_ctas = h->n_sm * cps;
+    h->gemm_smem = static_cast<size_t>(kb) * 1024;
+  }
   h->lat.reset(new dex::Lattice(X, n_X, cfg->batch, cfg->decs != 0));
   const int32_t XL[1] = {h->L};
   h->lat_ar.reset(new dex::Lattice(XL, 1, cfg->batch, false));
@@ -653,24 +661,13 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
   rc |= dalloc(h, &h->d_attn_norms, L * sizeof(void*));
   if (cfg->debug_logits) rc |= dalloc(h, &h->logits_dbg, R * static_cast<size_t>(h->V) * 4);
   if (rc) return DEX_ENOMEM;
-  // split-K factors depend only on the weight shape (batch-invariant results)
-  const int kb_d = (h->d + 63) / 64, kb_q = (qd + 63) / 64, kb_f = (h->dff + 63) / 64;
-  h->S_qkv = splits_for((qd + 2 * kvd) / 128, kb_d, h->n_sm);
-  h->S_o = splits_for(h->d / 128, kb_q, h->n_sm);
-  h->S_gu = splits_for((h->dff + 63) / 64, kb_d, h->n_sm);
-  h->S_d = splits_for(h->d / 128, kb_f, h->n_sm);
-  h->S_lm = splits_for((h->V + 127) / 128, kb_d, h->n_sm);
-  size_t part = 0, ntiles_max = 0;
-  auto need = [&](int S, size_t tiles) {
-    ntiles_max = std::max(ntiles_max, tiles);
-    if (S > 1) part = std::max(part, static_cast<size_t>(S) * 256 * tiles * 128 * 4);
-  };
-  need(h->S_qkv, (qd + 2 * kvd) / 128);
-  need(h->S_o, h->d / 128);
-  need(h->S_gu, (h->dff + 63) / 64);
-  need(h->S_d, h->d / 128);
-  need(h->S_lm, (h->V + 127) / 128);
-  if (dalloc(h, &h->partial, part) || dalloc(h, &h->counters, ntiles_max * 4)) return DEX_ENOMEM;
+  // partial-tile workspace of the persistent GEMM (two slots per CTA) and per-tile counters
+  const size_t ntiles_max = std::max<size_t>({static_cast<size_t>((qd + 2 * kvd) / 128),
+                                              static_cast<size_t>(h->d / 128),
+                                              static_cast<size_t>((h->dff + 63) / 64),
+                                              static_cast<size_t>((h->V + 127) / 128)});
+  if (dalloc(h, &h->partial, dex::gemm_partial_bytes(256, h->gemm_ctas)) || dalloc(h, &h->counters, ntiles_max * 4))
+    return DEX_ENOMEM;
   h->plan_cap = (R * sizeof(dex::DevNode) + R * 16 * 8 + 1024 * sizeof(dex::AttnItem) + 64 * 16 + 8192);
   if (dalloc(h, &h->d_plan, h->plan_cap)) return DEX_ENOMEM;
   if (cudaMallocHost(&h->h_plan, h->plan_cap) != cudaSuccess) return DEX_ENOMEM;
@@ -909,7 +906,7 @@ __global__ void exit_nodes_kernel(const dex_exit_node* in, int n, dex::DevNode* 
 int dex_exit_head_decs(const void* hidden, int32_t n, int32_t d, const void* final_norm, float rms_eps,
                        const void* lm_head, int32_t vocab, const dex_exit_node* nodes, const int32_t* priors,
                        int32_t sample, float tau, uint64_t seed, int32_t* tokens, float* logits, void* stream) {
-  if (!hidden || !final_norm || !lm_head || !nodes || !tokens || n < 1 || n > 256 || d < 128 || d % 128 ||
+  if (!hidden || !final_norm || !lm_head || !nodes || !tokens || n < 1 || n > 256 || d < 128 || d % 128 || d > 8192 ||
       vocab < 2 || (sample && !(tau > 0)))
     return DEX_EINVAL;
   if (get_encoder()) return DEX_ECUDA;
@@ -919,7 +916,6 @@ int dex_exit_head_decs(const void* hidden, int32_t n, int32_t d, const void* fin
       cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return DEX_ENODEV;
   const int n_tiles = (vocab + 127) / 128, kb = (d + 63) / 64;
-  const int S = splits_for(n_tiles, kb, n_sm);
   const int nt = (n + 15) & ~15;
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   const size_t o_hb = 0, o_ssq = o_hb + up(static_cast<size_t>(nt) * d * 2);
@@ -928,7 +924,7 @@ int dex_exit_head_decs(const void* hidden, int32_t n, int32_t d, const void* fin
   const size_t o_cnt = o_nodes + up(static_cast<size_t>(n) * sizeof(dex::DevNode));
   const size_t o_err = o_cnt + up(static_cast<size_t>(n_tiles) * 4);
   const size_t o_part = o_err + 256;
-  const size_t total = o_part + (S > 1 ? static_cast<size_t>(S) * 256 * n_tiles * 128 * 4 : 0);
+  const size_t total = o_part + dex::gemm_partial_bytes(nt, n_sm);
   uint8_t* scratch = nullptr;
   if (cudaMallocAsync(reinterpret_cast<void**>(&scratch), total, st) != cudaSuccess) return DEX_ENOMEM;
   bf16* hb = reinterpret_cast<bf16*>(scratch + o_hb);
@@ -951,8 +947,7 @@ int dex_exit_head_decs(const void* hidden, int32_t n, int32_t d, const void* fin
     a.nt = nt;
     a.b_row0 = 0;
     a.kblocks = kb;
-    a.splits = S;
-    a.stages = 4;
+    a.stages = dex::gemm_stages_for(nt);
     a.n_tiles = n_tiles;
     a.src_tiles0 = n_tiles;
     a.tmem_cols = pow2_at_least(nt);
@@ -971,7 +966,8 @@ int dex_exit_head_decs(const void* hidden, int32_t n, int32_t d, const void* fin
     a.sample = sample;
     a.tau = tau;
     a.seed = seed;
-    if (!rc && dex::launch_gemm(dex::EPI_EXIT, tm_w, tm_w, tm_w, tm_b, a, st, false) != cudaSuccess) rc = DEX_ECUDA;
+    if (!rc && dex::launch_gemm(dex::EPI_EXIT, tm_w, tm_w, tm_w, tm_b, a, n_sm, st, false) != cudaSuccess)
+      rc = DEX_ECUDA;
     if (!rc && dex::launch_decode_best(best, n, tokens, st) != cudaSuccess) rc = DEX_ECUDA;
   }
   cudaFreeAsync(scratch, st);
@@ -1032,7 +1028,7 @@ extern "C" int dex_exit_head_decs_noalloc(const void* hidden, int32_t n, int32_t
                                           float rms_eps, const void* lm_head, int32_t vocab,
                                           const dex_exit_node* nodes, const int32_t* priors, int32_t sample,
                                           float tau, uint64_t seed, int32_t* tokens, float* logits, void* stream) {
-  if (!hidden || !final_norm || !lm_head || !nodes || !tokens || n < 1 || n > 256 || d < 128 || d % 128 ||
+  if (!hidden || !final_norm || !lm_head || !nodes || !tokens || n < 1 || n > 256 || d < 128 || d % 128 || d > 8192 ||
       vocab < 2 || (sample && !(tau > 0)))
     return DEX_EINVAL;
   if (get_encoder()) return DEX_ECUDA;
@@ -1041,9 +1037,8 @@ extern "C" int dex_exit_head_decs_noalloc(const void* hidden, int32_t n, int32_t
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return DEX_ENODEV;
-  // same split and scratch layout as dex_exit_head_decs
+  // same scratch layout as dex_exit_head_decs
   const int n_tiles = (vocab + 127) / 128, kb = (d + 63) / 64;
-  const int S = splits_for(n_tiles, kb, n_sm);
   const int nt = (n + 15) & ~15;
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   const size_t o_hb = 0, o_ssq = o_hb + up(static_cast<size_t>(nt) * d * 2);
@@ -1052,7 +1047,7 @@ extern "C" int dex_exit_head_decs_noalloc(const void* hidden, int32_t n, int32_t
   const size_t o_cnt = o_nodes + up(static_cast<size_t>(n) * sizeof(dex::DevNode));
   const size_t o_err = o_cnt + up(static_cast<size_t>(n_tiles) * 4);
   const size_t o_part = o_err + 256;
-  const size_t total = o_part + (S > 1 ? static_cast<size_t>(S) * 256 * n_tiles * 128 * 4 : 0);
+  const size_t total = o_part + dex::gemm_partial_bytes(nt, n_sm);
   if (total > DEX_NOALLOC_SCRATCH_BYTES) return DEX_ECAPACITY;   // does not fit the fixed scratch
   void* base = nullptr;
   const int rc0 = exit_scratch_address(dev, &base);
@@ -1080,8 +1075,7 @@ extern "C" int dex_exit_head_decs_noalloc(const void* hidden, int32_t n, int32_t
   a.nt = nt;
   a.b_row0 = 0;
   a.kblocks = kb;
-  a.splits = S;
-  a.stages = 4;
+  a.stages = dex::gemm_stages_for(nt);
   a.n_tiles = n_tiles;
   a.src_tiles0 = n_tiles;
   a.tmem_cols = pow2_at_least(nt);
@@ -1100,7 +1094,7 @@ extern "C" int dex_exit_head_decs_noalloc(const void* hidden, int32_t n, int32_t
   a.sample = sample;
   a.tau = tau;
   a.seed = seed;
-  if (dex::launch_gemm(dex::EPI_EXIT, tm_w, tm_w, tm_w, tm_b, a, st, false) != cudaSuccess) return DEX_ECUDA;
+  if (dex::launch_gemm(dex::EPI_EXIT, tm_w, tm_w, tm_w, tm_b, a, n_sm, st, false) != cudaSuccess) return DEX_ECUDA;
   if (dex::launch_decode_best(best, n, tokens, st) != cudaSuccess) return DEX_ECUDA;
   return DEX_OK;
 }

@@ -6,10 +6,16 @@
 //
 // Swap-AB: the weights sit on the MMA's M = 128 side, the few lattice nodes of a stage
 // batch on the N side (16..256 columns), so each weight byte is read from HBM once per
-// round however many nodes the round holds.  One CTA owns one 128-row output tile and
-// one fixed slice of K (split-K); the split depends only on the weight shape, and the
-// partial tiles are summed in split order by the last CTA to arrive, so a node's
-// result never depends on the batch it was computed in.
+// round however many nodes the round holds.
+//
+// Persistent, fixed-partition stream-K: the (128-row tile, 64-wide k-block) work items of
+// the weight matrix are laid out tile-major and cut into one contiguous range per CTA
+// (one CTA per SM).  A CTA streams its range through a deep TMA ring without pausing;
+// where its range starts or ends inside a tile, it writes a partial tile and the last of
+// that tile's CTAs sums the partials in k order.  The partition depends only on the
+// weight shape and the CTA count -- never on the number of nodes -- so a node's result is
+// bit-identical in any batch.  Two TMEM accumulators alternate between consecutive
+// segments, so the epilogue of one tile overlaps the MMAs of the next.
 //
 // Roles: warp 0 issues TMA loads (weights first -- they do not depend on the previous
 // kernel -- then, after the grid-dependency wait, the activations); warp 1 owns TMEM
@@ -39,7 +45,7 @@ __host__ __device__ inline SmemMap smem_map(int nt, int stages) {
   m.a = 0;
   m.b = m.a + static_cast<size_t>(stages) * kABytes;
   m.bar = m.b + static_cast<size_t>(stages) * nt * kBK * 2;
-  m.misc = m.bar + static_cast<size_t>(2 * stages + 1) * 8;
+  m.misc = m.bar + static_cast<size_t>(2 * stages + 4) * 8;       // full, empty, accf[2], tfree[2]
   m.xch = (m.misc + 32 + 15) & ~static_cast<size_t>(15);        // tmem slot + flags
   m.inv = m.xch + 16 * kBM * 4;                                    // 16 columns x 128 rows
   m.qsum = m.inv + kNtMax * 4;
@@ -50,11 +56,53 @@ __host__ __device__ inline SmemMap smem_map(int nt, int stages) {
 
 size_t gemm_smem_bytes(int nt, int stages) { return smem_map(nt, stages).total + 1024; }
 
+constexpr size_t kSmemOptin = 227 * 1024;   // largest dynamic shared memory a CTA may opt into
+
+// Pipeline depth: the most stages (2..8) whose whole footprint fits the given budget for
+// small node tiles, or the opt-in limit for the wide tiles of prefill.
+int gemm_stages_for(int nt, size_t small_budget) {
+  const size_t budget = nt <= 64 ? small_budget : kSmemOptin;
+  int s = 8;
+  while (s > 2 && gemm_smem_bytes(nt, s) > budget) --s;
+  return s;
+}
+
+// Work range of CTA c: [c W / G, (c+1) W / G) over tile-major (tile, k-block) items.
+__device__ __forceinline__ long long work_start(int c, long long W, int G) {
+  return static_cast<long long>(c) * W / G;
+}
+// CTAs whose ranges may intersect tile t (work [t kb, (t+1) kb)): c_lo..c_hi.
+__device__ __forceinline__ void tile_cta_span(int t, int kb, long long W, int G, int& c_lo, int& c_hi) {
+  const long long x = static_cast<long long>(t) * kb, y = x + kb;
+  c_lo = static_cast<int>(((x + 1) * G + W - 1) / W) - 1;   // first c with end(c) > x
+  c_hi = static_cast<int>((y * G + W - 1) / W) - 1;         // last c with start(c) < y
+  c_lo = c_lo < 0 ? 0 : c_lo;
+  c_hi = c_hi > G - 1 ? G - 1 : c_hi;
+}
+__device__ __forceinline__ bool cta_touches_tile(int c, int t, int kb, long long W, int G) {
+  const long long x = static_cast<long long>(t) * kb, y = x + kb;
+  const long long s = work_start(c, W, G), e = work_start(c + 1, W, G);
+  return (s > x ? s : x) < (e < y ? e : y);
+}
+// Partial slot of CTA c for tile t: slot 2c for the tile its range starts in, else 2c+1.
+__device__ __forceinline__ int partial_slot(int c, int t, int kb, long long W, int G) {
+  return (work_start(c, W, G) / kb == t) ? 2 * c : 2 * c + 1;
+}
+
 template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB,
                    const GemmArgs a) {
+  const int G = gridDim.x, cta = blockIdx.x;
+  const int kb = a.kblocks;
+  const long long W = static_cast<long long>(a.n_tiles) * kb;
+  const long long w0 = work_start(cta, W, G), w1 = work_start(cta + 1, W, G);
+  if (w0 >= w1) return;   // no work (more CTAs than work items)
+  const int nwork = static_cast<int>(w1 - w0);
+  const int t_first = static_cast<int>(w0 / kb), t_last = static_cast<int>((w1 - 1) / kb);
+  const int nseg = t_last - t_first + 1;
+
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const SmemMap sm = smem_map(a.nt, a.stages);
@@ -62,7 +110,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sB = smem + sm.b;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + sm.bar);
   uint64_t* empty = full + a.stages;
-  uint64_t* accf = empty + a.stages;
+  uint64_t* accf = empty + a.stages;   // [2] accumulator ready
+  uint64_t* tfree = accf + 2;          // [2] accumulator drained by the epilogue
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + sm.misc);
   volatile int* sflag = reinterpret_cast<volatile int*>(smem + sm.misc + 4);   // [0] last, [1] abort
   float* xch = reinterpret_cast<float*>(smem + sm.xch);
@@ -71,38 +120,41 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned long long* qkey = reinterpret_cast<unsigned long long*>(smem + sm.qkey);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int S = a.splits, stages = a.stages;
-  const int tile = blockIdx.x / S, split = blockIdx.x % S;
-  const int kb0 = static_cast<int>(static_cast<long long>(split) * a.kblocks / S);
-  const int kb1 = static_cast<int>(static_cast<long long>(split + 1) * a.kblocks / S);
-  const int nk = kb1 - kb0;
+  const int stages = a.stages;
   const uint32_t b_bytes = static_cast<uint32_t>(a.nt) * kBK * 2;
+  const uint32_t cols = static_cast<uint32_t>(a.tmem_cols);
 
-  int src = 0, lt = tile;
-  if (tile >= a.src_tiles0 + a.src_tiles1) {
-    src = 2;
-    lt = tile - a.src_tiles0 - a.src_tiles1;
-  } else if (tile >= a.src_tiles0) {
-    src = 1;
-    lt = tile - a.src_tiles0;
-  }
-  const CUtensorMap* mapA = src == 0 ? &tmA0 : (src == 1 ? &tmA1 : &tmA2);
+  auto tile_src = [&](int t, int& src, int& lt) {
+    src = 0;
+    lt = t;
+    if (t >= a.src_tiles0 + a.src_tiles1) {
+      src = 2;
+      lt = t - a.src_tiles0 - a.src_tiles1;
+    } else if (t >= a.src_tiles0) {
+      src = 1;
+      lt = t - a.src_tiles0;
+    }
+  };
 
   if (tid == 0) {
     for (int i = 0; i < stages; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
-    mbar_init(accf, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accf[b], 1);
+      mbar_init(&tfree[b], 128);
+    }
     sflag[0] = 0;
     sflag[1] = 0;
     fence_mbar_init();
-    tma_prefetch(mapA);
-    if (EPI == EPI_SWIGLU) tma_prefetch(&tmA1);
+    tma_prefetch(&tmA0);
+    if (a.src_tiles0 < a.n_tiles || EPI == EPI_SWIGLU) tma_prefetch(&tmA1);
+    if (a.src_tiles0 + a.src_tiles1 < a.n_tiles) tma_prefetch(&tmA2);
     tma_prefetch(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, static_cast<uint32_t>(a.tmem_cols));
+    tmem_alloc(tmem_slot, 2 * cols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -115,8 +167,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
-      auto load_a = [&](int i, int st) {
-        const int kx = (kb0 + i) * kBK;
+      auto load_a = [&](long long w, int st) {
+        const int t = static_cast<int>(w / kb), kx = static_cast<int>(w % kb) * kBK;
+        int src, lt;
+        tile_src(t, src, lt);
         uint8_t* dst = sA + static_cast<size_t>(st) * kABytes;
         if (EPI == EPI_SWIGLU) {
           if (a.evict_first) {
@@ -127,23 +181,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(dst + kABytes / 2, &tmA1, &full[st], kx, lt * 64);
           }
         } else {
+          const CUtensorMap* mapA = src == 0 ? &tmA0 : (src == 1 ? &tmA1 : &tmA2);
           if (a.evict_first) tma_load_2d_hint(dst, mapA, &full[st], kx, lt * kBM, pol);
           else tma_load_2d(dst, mapA, &full[st], kx, lt * kBM);
         }
       };
-      auto load_b = [&](int i, int st) {
-        tma_load_2d(sB + static_cast<size_t>(st) * b_bytes, &tmB, &full[st], (kb0 + i) * kBK, a.b_row0);
+      auto load_b = [&](long long w, int st) {
+        tma_load_2d(sB + static_cast<size_t>(st) * b_bytes, &tmB, &full[st], static_cast<int>(w % kb) * kBK,
+                    a.b_row0);
       };
-      const int npre = nk < stages ? nk : stages;
+      const int npre = nwork < stages ? nwork : stages;
       for (int i = 0; i < npre; ++i) {
         mbar_arrive_expect_tx(&full[i], kABytes + b_bytes);
-        load_a(i, i);
+        load_a(w0 + i, i);
       }
       griddep_wait();   // activations are produced by the previous kernel
-      for (int i = 0; i < npre; ++i) load_b(i, i);
+      for (int i = 0; i < npre; ++i) load_b(w0 + i, i);
       int issued = npre;
       bool ok = true;
-      for (int i = npre; i < nk; ++i) {
+      for (int i = npre; i < nwork; ++i) {
         const int st = i % stages;
         const uint32_t use = static_cast<uint32_t>(i / stages);
         if (!mbar_wait(&empty[st], (use - 1) & 1u, a.err, DEV_TIMEOUT_EMPTY)) {
@@ -151,8 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         mbar_arrive_expect_tx(&full[st], kABytes + b_bytes);
-        load_a(i, st);
-        load_b(i, st);
+        load_a(w0 + i, st);
+        load_b(w0 + i, st);
         issued = i + 1;
       }
       if (!ok) {   // drain copies still in flight before the CTA can exit
@@ -164,24 +220,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(kBM, a.nt);
-      bool ok = true;
-      for (int i = 0; i < nk; ++i) {
-        const int st = i % stages;
-        if (!mbar_wait(&full[st], static_cast<uint32_t>(i / stages) & 1u, a.err, DEV_TIMEOUT_FULL)) {
-          ok = false;
-          break;
+      int seg = 0;
+      for (int i = 0; i < nwork; ++i) {
+        const long long w = w0 + i;
+        const int k = static_cast<int>(w % kb);
+        const bool seg_first = (i == 0) || (k == 0);
+        const bool seg_last = (i == nwork - 1) || (k == kb - 1);
+        const int buf = seg & 1;
+        if (seg_first && seg >= 2) {   // reuse of an accumulator: wait until the epilogue drained it
+          if (!mbar_wait(&tfree[buf], static_cast<uint32_t>((seg >> 1) - 1) & 1u, a.err, DEV_TIMEOUT_ACC)) break;
+          tc_fence_after();
         }
+        const int st = i % stages;
+        if (!mbar_wait(&full[st], static_cast<uint32_t>(i / stages) & 1u, a.err, DEV_TIMEOUT_FULL)) break;
         tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(buf) * cols;
         const uint32_t abase = smem_u32(sA + static_cast<size_t>(st) * kABytes);
         const uint32_t bbase = smem_u32(sB + static_cast<size_t>(st) * b_bytes);
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk) {
-          umma_bf16(tmem_base, sw128_kmajor_desc(abase + kk * 32), sw128_kmajor_desc(bbase + kk * 32), idesc,
-                    (i > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16(d, sw128_kmajor_desc(abase + kk * 32), sw128_kmajor_desc(bbase + kk * 32), idesc,
+                    (!seg_first || kk > 0) ? 1u : 0u);
         }
         umma_commit(&empty[st]);
+        if (seg_last) {
+          umma_commit(&accf[buf]);
+          ++seg;
+        }
       }
-      if (ok) umma_commit(accf);
     }
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
@@ -199,13 +265,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         inv[c] = 1.0f / sqrtf(__fadd_rn(__fdiv_rn(t, static_cast<float>(a.d)), a.eps));
       }
     }
-    if (!mbar_wait(accf, 0, a.err, DEV_TIMEOUT_ACC)) sflag[1] = 1;
-    named_bar_sync(1, 128);
-    const bool abort = sflag[1] != 0;
-    tc_fence_after();
 
-    // per-chunk epilogue: v[j] = accumulator of (row r, node c0 + j)
-    auto epilogue_chunk = [&](int c0, float (&v)[16]) {
+    // per-chunk epilogue of tile (src, lt): v[j] = accumulator of (row r, node c0 + j)
+    auto epilogue_chunk = [&](int src, int lt, int c0, float (&v)[16]) {
       if (EPI == EPI_QKV) {
         const int f = lt * kBM + r;      // feature within the source (q, k or v)
         const int half = a.hd >> 1;
@@ -323,46 +385,63 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
 
-    if (!abort) {
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(wq * 32) << 16);
-      if (S > 1) {
-        const size_t rows_total = static_cast<size_t>(a.n_tiles) * kBM;
+    for (int sg = 0; sg < nseg; ++sg) {
+      const int t = t_first + sg, buf = sg & 1;
+      int src, lt;
+      tile_src(t, src, lt);
+      if (!mbar_wait(&accf[buf], static_cast<uint32_t>(sg >> 1) & 1u, a.err, DEV_TIMEOUT_ACC)) sflag[1] = 1;
+      named_bar_sync(1, 128);
+      if (sflag[1]) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + static_cast<uint32_t>(buf) * cols + (static_cast<uint32_t>(wq * 32) << 16);
+      int c_lo, c_hi;
+      tile_cta_span(t, kb, W, G, c_lo, c_hi);
+      int parts = 0;
+      for (int c = c_lo; c <= c_hi; ++c) parts += cta_touches_tile(c, t, kb, W, G) ? 1 : 0;
+      if (parts == 1) {   // the whole tile is in this CTA's range
+        for (int c0 = 0; c0 < n; c0 += 16) {
+          float v[16];
+          tmem_ld16(taddr + static_cast<uint32_t>(c0), v);
+          epilogue_chunk(src, lt, c0, v);
+        }
+        tc_fence_before();
+        mbar_arrive(&tfree[buf]);
+      } else {
+        float* part = a.partial + static_cast<size_t>(partial_slot(cta, t, kb, W, G)) * a.nt * kBM;
         for (int c0 = 0; c0 < n; c0 += 16) {
           float v[16];
           tmem_ld16(taddr + static_cast<uint32_t>(c0), v);
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            if (c0 + j < n)
-              __stcg(a.partial + (static_cast<size_t>(split) * kNtMax + c0 + j) * rows_total + tile * kBM + r, v[j]);
+            if (c0 + j < n) __stcg(part + static_cast<size_t>(c0 + j) * kBM + r, v[j]);
         }
+        tc_fence_before();
+        mbar_arrive(&tfree[buf]);
         __threadfence();
         named_bar_sync(1, 128);
-        if (ep == 0) sflag[0] = (atomicAdd(a.counters + tile, 1) == S - 1) ? 1 : 0;
+        if (ep == 0) sflag[0] = (atomicAdd(a.counters + t, 1) == parts - 1) ? 1 : 0;
         named_bar_sync(1, 128);
-        if (sflag[0]) {
+        if (sflag[0]) {   // last of the tile's CTAs: sum the partial tiles in k order
           __threadfence();
           for (int c0 = 0; c0 < n; c0 += 16) {
             float v[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              v[j] = 0.0f;
-              if (c0 + j < n) {
-                const float* p = a.partial + static_cast<size_t>(c0 + j) * rows_total + tile * kBM + r;
-                float t = __ldcg(p);
-                for (int s = 1; s < S; ++s) t = __fadd_rn(t, __ldcg(p + static_cast<size_t>(s) * kNtMax * rows_total));
-                v[j] = t;
-              }
+            for (int j = 0; j < 16; ++j) v[j] = 0.0f;
+            bool first = true;
+            for (int c = c_lo; c <= c_hi; ++c) {
+              if (!cta_touches_tile(c, t, kb, W, G)) continue;
+              const float* p = a.partial + static_cast<size_t>(partial_slot(c, t, kb, W, G)) * a.nt * kBM +
+                               static_cast<size_t>(c0) * kBM + r;
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (c0 + j < n) v[j] = first ? __ldcg(p + j * kBM) : __fadd_rn(v[j], __ldcg(p + j * kBM));
+              first = false;
             }
-            epilogue_chunk(c0, v);
+            epilogue_chunk(src, lt, c0, v);
           }
-          if (ep == 0) a.counters[tile] = 0;
+          if (ep == 0) a.counters[t] = 0;
         }
-      } else {
-        for (int c0 = 0; c0 < n; c0 += 16) {
-          float v[16];
-          tmem_ld16(taddr + static_cast<uint32_t>(c0), v);
-          epilogue_chunk(c0, v);
-        }
+        named_bar_sync(1, 128);
       }
     }
   }
@@ -371,23 +450,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, static_cast<uint32_t>(a.tmem_cols));
+    tmem_dealloc(tmem_base, 2 * cols);
   }
 }
 
 template <int EPI>
 static cudaError_t launch_one(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& a2,
-                              const CUtensorMap& b, const GemmArgs& args, cudaStream_t st, bool pdl) {
+                              const CUtensorMap& b, const GemmArgs& args, int n_ctas, cudaStream_t st, bool pdl) {
   static bool attr_set = false;
   const size_t smem = gemm_smem_bytes(args.nt, args.stages);
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(gemm_smem_bytes(kNtMax, 4)));
+                                         static_cast<int>(kSmemOptin));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(args.n_tiles * args.splits));
+  cfg.gridDim = dim3(static_cast<unsigned>(n_ctas));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
@@ -400,17 +479,19 @@ static cudaError_t launch_one(const CUtensorMap& a0, const CUtensorMap& a1, cons
 }
 
 cudaError_t launch_gemm(int epi, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& a2,
-                        const CUtensorMap& b, const GemmArgs& args, cudaStream_t st, bool pdl) {
-  if (args.nt < 16 || args.nt > kNtMax || (args.nt & 15) || args.n < 1 || args.n > args.nt) return cudaErrorInvalidValue;
-  if (args.tmem_cols < args.nt || args.tmem_cols < 32 || (args.tmem_cols & (args.tmem_cols - 1)))
+                        const CUtensorMap& b, const GemmArgs& args, int n_ctas, cudaStream_t st, bool pdl) {
+  if (args.nt < 16 || args.nt > kNtMax || (args.nt & 15) || args.n < 1 || args.n > args.nt || n_ctas < 1)
     return cudaErrorInvalidValue;
-  if (args.stages < 2 || args.stages > 8 || gemm_smem_bytes(args.nt, args.stages) > gemm_smem_bytes(kNtMax, 4))
+  if (args.tmem_cols < args.nt || args.tmem_cols < 32 || args.tmem_cols > 256 ||
+      (args.tmem_cols & (args.tmem_cols - 1)))
+    return cudaErrorInvalidValue;
+  if (args.stages < 2 || args.stages > 8 || gemm_smem_bytes(args.nt, args.stages) > kSmemOptin)
     return cudaErrorInvalidValue;
   switch (epi) {
-    case EPI_QKV: return launch_one<EPI_QKV>(a0, a1, a2, b, args, st, pdl);
-    case EPI_RESID: return launch_one<EPI_RESID>(a0, a1, a2, b, args, st, pdl);
-    case EPI_SWIGLU: return launch_one<EPI_SWIGLU>(a0, a1, a2, b, args, st, pdl);
-    case EPI_EXIT: return launch_one<EPI_EXIT>(a0, a1, a2, b, args, st, pdl);
+    case EPI_QKV: return launch_one<EPI_QKV>(a0, a1, a2, b, args, n_ctas, st, pdl);
+    case EPI_RESID: return launch_one<EPI_RESID>(a0, a1, a2, b, args, n_ctas, st, pdl);
+    case EPI_SWIGLU: return launch_one<EPI_SWIGLU>(a0, a1, a2, b, args, n_ctas, st, pdl);
+    case EPI_EXIT: return launch_one<EPI_EXIT>(a0, a1, a2, b, args, n_ctas, st, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -52,12 +52,11 @@ struct GemmArgs {
   int32_t nt;           // node tile (multiple of 16, <= 256)
   int32_t b_row0;       // first B row (= first node row of the batch)
   int32_t kblocks;      // K / 64, rounded up
-  int32_t splits;       // fixed split-K factor of this weight shape
   int32_t stages;       // smem pipeline depth
   int32_t n_tiles;      // output tiles
   int32_t src_tiles0, src_tiles1;   // tiles of source 0 and 1 (source 2 takes the rest)
   int32_t tmem_cols;
-  float* partial;       // [splits][256][n_tiles * 128] fp32 split-K partials
+  float* partial;       // [2 * gridDim.x][nt][128] fp32 partial tiles (two slots per CTA)
   int32_t* counters;    // [n_tiles] arrival counters (left at 0)
   int32_t* err;         // device error flag
   const DevNode* nodes; // node rows (absolute)
@@ -133,9 +132,14 @@ struct CollapseArgs {
 // ---- launchers (return cudaError_t of the launch) -----------------------------------------
 // A tensor maps: up to three weight sources (QKV: wq, wk, wv; SWIGLU: wg, wu with 64-row
 // boxes); B: the activation rows with a box of nt rows.
+// Persistent launch: grid = n_ctas (the SM count), each CTA streams a fixed contiguous
+// range of the (tile, k-block) work; stages chosen from the node tile.
 cudaError_t launch_gemm(int epi, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& a2,
-                        const CUtensorMap& b, const GemmArgs& args, cudaStream_t st, bool pdl);
+                        const CUtensorMap& b, const GemmArgs& args, int n_ctas, cudaStream_t st, bool pdl);
 size_t gemm_smem_bytes(int nt, int stages);
+int gemm_stages_for(int nt, size_t small_budget = 104 * 1024);
+// Bytes of the partial-tile workspace a launch over n_ctas CTAs with node tile nt needs.
+inline size_t gemm_partial_bytes(int nt, int n_ctas) { return static_cast<size_t>(2) * n_ctas * nt * 128 * 4; }
 cudaError_t launch_attention(const AttnArgs& a, int n_items, int max_groups_launch, cudaStream_t st, bool pdl);
 cudaError_t launch_assemble(const AssembleArgs& a, cudaStream_t st, bool pdl);
 cudaError_t launch_collapse(const CollapseArgs& a, cudaStream_t st, bool pdl);

@@ -7,26 +7,37 @@
 
 namespace dex {
 
-// Sum of squares of one 128-feature tile held one value per thread by four warps, in
-// the canonical order shared with the residual epilogue of the GEMM: per-warp butterfly
-// (warp_sum), then (q0 + q1) + (q2 + q3).  A row's RMSNorm scale therefore does not
-// depend on which kernel produced its partial sums.
-__device__ __forceinline__ float tile_ssq_128(float x, float* qbuf) {
-  const float s = warp_sum(__fmul_rn(x, x));
+// Sums of squares of the d/128 feature tiles of one row, one value per thread per tile
+// (thread t holds feature 128 i + t of tile i), in the canonical order shared with the
+// residual epilogue of the GEMM: per-warp butterfly (warp_sum), then (q0 + q1) + (q2 + q3)
+// over the four warps.  A row's RMSNorm scale therefore does not depend on which kernel
+// produced its partial sums.  ssq_out: [ndt] (written by threads 0..ndt-1).
+template <int MAXT>
+__device__ __forceinline__ void row_tile_ssq(const float (&x)[MAXT], int ndt, float* qbuf, float* ssq_out) {
   const int warp = threadIdx.x >> 5;
-  if ((threadIdx.x & 31) == 0) qbuf[warp] = s;
+#pragma unroll
+  for (int t = 0; t < MAXT; ++t) {
+    if (t < ndt) {
+      const float s = warp_sum(__fmul_rn(x[t], x[t]));
+      if ((threadIdx.x & 31) == 0) qbuf[t * 4 + warp] = s;
+    }
+  }
   __syncthreads();
-  const float t = __fadd_rn(__fadd_rn(qbuf[0], qbuf[1]), __fadd_rn(qbuf[2], qbuf[3]));
-  __syncthreads();
-  return t;
+  if (static_cast<int>(threadIdx.x) < ndt) {
+    const float* q = qbuf + threadIdx.x * 4;
+    ssq_out[threadIdx.x] = __fadd_rn(__fadd_rn(q[0], q[1]), __fadd_rn(q[2], q[3]));
+  }
 }
+
+constexpr int kMaxTiles = 64;   // d_model up to 8192
 
 // One CTA (128 threads) per node row.  Stage-0 nodes start a slot chain: h = E[token]
 // into the chain's hidden row.  Depth children continue the chain's hidden row left by
 // the previous stage.  Writes the first layer's bf16 input bf16(h * g) and the RMSNorm
-// partial sums, and clears the row's exit-head argmax slot.
+// partial sums, and clears the row's exit-head argmax slot.  The whole row is loaded
+// before any reduction so the loads overlap.
 __global__ void __launch_bounds__(128) assemble_kernel(const AssembleArgs a) {
-  __shared__ float qbuf[4];
+  __shared__ float qbuf[kMaxTiles * 4];
   const int row = blockIdx.x;
   griddep_wait();
   griddep_launch_dependents();
@@ -35,19 +46,23 @@ __global__ void __launch_bounds__(128) assemble_kernel(const AssembleArgs a) {
   const __nv_bfloat16* g = a.attn_norm[nd.first_layer];
   float* hrow = a.hidden + static_cast<size_t>(nd.hrow) * a.d;
   const int ndt = a.d / 128;
-  for (int t = 0; t < ndt; ++t) {
-    const int f = t * 128 + threadIdx.x;
-    float h;
-    if (nd.token >= 0) {
-      h = bf16_to_f32(a.embed[static_cast<size_t>(nd.token) * a.d + f]);
-      hrow[f] = h;
-    } else {
-      h = hrow[f];
+  float x[kMaxTiles];
+#pragma unroll
+  for (int t = 0; t < kMaxTiles; ++t) {
+    if (t < ndt) {
+      const int f = t * 128 + threadIdx.x;
+      x[t] = nd.token >= 0 ? bf16_to_f32(a.embed[static_cast<size_t>(nd.token) * a.d + f]) : hrow[f];
     }
-    a.hb[static_cast<size_t>(row) * a.d + f] = __float2bfloat16_rn(__fmul_rn(h, bf16_to_f32(g[f])));
-    const float s = tile_ssq_128(h, qbuf);
-    if (threadIdx.x == 0) a.ssq[static_cast<size_t>(row) * ndt + t] = s;
   }
+#pragma unroll
+  for (int t = 0; t < kMaxTiles; ++t) {
+    if (t < ndt) {
+      const int f = t * 128 + threadIdx.x;
+      if (nd.token >= 0) hrow[f] = x[t];
+      a.hb[static_cast<size_t>(row) * a.d + f] = __float2bfloat16_rn(__fmul_rn(x[t], bf16_to_f32(g[f])));
+    }
+  }
+  row_tile_ssq<kMaxTiles>(x, ndt, qbuf, a.ssq + static_cast<size_t>(row) * ndt);
 }
 
 cudaError_t launch_assemble(const AssembleArgs& a, cudaStream_t st, bool pdl) {
@@ -106,17 +121,22 @@ cudaError_t launch_collapse(const CollapseArgs& a, cudaStream_t st, bool pdl) {
 // Isolated exit head: bf16 hidden rows -> bf16(h * g) and the RMSNorm partial sums.
 __global__ void __launch_bounds__(128) exit_prep_kernel(const __nv_bfloat16* h, int d, const __nv_bfloat16* g,
                                                         __nv_bfloat16* hb, float* ssq, unsigned long long* best) {
-  __shared__ float qbuf[4];
+  __shared__ float qbuf[kMaxTiles * 4];
   const int row = blockIdx.x;
   if (threadIdx.x == 0) best[row] = 0ull;
   const int ndt = d / 128;
-  for (int t = 0; t < ndt; ++t) {
-    const int f = t * 128 + threadIdx.x;
-    const float x = bf16_to_f32(h[static_cast<size_t>(row) * d + f]);
-    hb[static_cast<size_t>(row) * d + f] = __float2bfloat16_rn(__fmul_rn(x, bf16_to_f32(g[f])));
-    const float s = tile_ssq_128(x, qbuf);
-    if (threadIdx.x == 0) ssq[static_cast<size_t>(row) * ndt + t] = s;
+  float x[kMaxTiles];
+#pragma unroll
+  for (int t = 0; t < kMaxTiles; ++t)
+    if (t < ndt) x[t] = bf16_to_f32(h[static_cast<size_t>(row) * d + t * 128 + threadIdx.x]);
+#pragma unroll
+  for (int t = 0; t < kMaxTiles; ++t) {
+    if (t < ndt) {
+      const int f = t * 128 + threadIdx.x;
+      hb[static_cast<size_t>(row) * d + f] = __float2bfloat16_rn(__fmul_rn(x[t], bf16_to_f32(g[f])));
+    }
   }
+  row_tile_ssq<kMaxTiles>(x, ndt, qbuf, ssq + static_cast<size_t>(row) * ndt);
 }
 
 cudaError_t launch_exit_prep(const __nv_bfloat16* h, int n, int d, const __nv_bfloat16* g, __nv_bfloat16* hb,
