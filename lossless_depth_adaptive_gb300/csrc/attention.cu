@@ -88,9 +88,9 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
   if (cmax > g0) {
     if (tid == 0) {
       const size_t kbase =
-          ((((static_cast<size_t>(item.seq) * a.L + a.layer) * 2 + 0) * a.KVH + kvh) * a.max_ctx + g0) * HD;
+          ((((static_cast<size_t>(item.seq) * a.L + item.layer) * 2 + 0) * a.KVH + kvh) * a.max_ctx + g0) * HD;
       const size_t vbase =
-          ((((static_cast<size_t>(item.seq) * a.L + a.layer) * 2 + 1) * a.KVH + kvh) * a.max_ctx + g0) * HD;
+          ((((static_cast<size_t>(item.seq) * a.L + item.layer) * 2 + 1) * a.KVH + kvh) * a.max_ctx + g0) * HD;
       const uint32_t bytes = static_cast<uint32_t>(cmax - g0) * HD * 2;
       mbar_arrive_expect_tx(&s_bar, 2 * bytes);
       bulk_load_1d(sK, a.kv_commit + kbase, bytes, &s_bar);
@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
         }
         const int slot = a.tails[nd.tail_off + t];
         return a.kv_pool +
-               ((((static_cast<size_t>(nd.seq) * a.n_slots + slot) * a.L + a.layer) * 2 + kv) * a.KVH + kvh) * HD;
+               ((((static_cast<size_t>(nd.seq) * a.n_slots + slot) * a.L + item.layer) * 2 + kv) * a.KVH + kvh) * HD;
       };
       const float s = (k <= pos) ? dot_q_row<HD>(sQ + j * HD, key_row(k, 0), lane) : -INFINITY;
       const float m = warp_max(s);
@@ -241,6 +241,9 @@ static size_t attn_smem_bytes(int hd) {
 
 cudaError_t launch_attention(const AttnArgs& a, int n_items, int max_groups_launch, cudaStream_t st, bool pdl) {
   if (n_items <= 0) return cudaSuccess;
+  if (!a.nodes || !a.items || !a.tails || !a.q || !a.kv_commit || !a.kv_pool || !a.out || !a.part || !a.counters ||
+      !a.err || max_groups_launch < 1 || max_groups_launch > a.max_groups || max_groups_launch > 32)
+    return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(max_groups_launch), static_cast<unsigned>(a.KVH),
                      static_cast<unsigned>(n_items));

@@ -98,6 +98,10 @@ struct dex_handle {
   // pinned host
   uint8_t* h_plan = nullptr;
   unsigned long long* h_best = nullptr;   // rows_cap + 1 (last = error flag)
+  // packed GEMM weights (one swizzled 16 KB box per (tile, k-block), tile-major)
+  std::vector<const uint8_t*> pk_qkv, pk_o, pk_gu, pk_d;
+  const uint8_t* pk_lm = nullptr;
+  size_t packed_total = 0;
   // tensor maps
   std::vector<CUtensorMap> tm_q, tm_k, tm_v, tm_o, tm_g, tm_u, tm_d;
   CUtensorMap tm_lm;
@@ -151,11 +155,46 @@ const bf16* W(const dex_handle* h, int layer, int j) { return h->w[static_cast<s
 struct RoundTables {
   std::vector<dex::DevNode> nodes;
   std::vector<int32_t> tails, priors;
-  std::vector<dex::AttnItem> items;
-  std::vector<int> item_begin;          // per stage: first item, size N+1
-  std::vector<int> stage_off;           // per stage: first row, size N+1
+  std::vector<dex::AttnItem> items;     // attention items of every layer slot, slot after slot
   std::vector<dex_copy_job> jobs;
 };
+
+// A batch of node rows that runs a contiguous range of layers: one stage of a DEX round,
+// or a prefill chunk.  `items` are its attention items (layer filled in per slot).
+struct Batch {
+  int off, n, l0, l1;
+  std::vector<dex::AttnItem> items;
+};
+
+// Layer slot j of a round: layer l0 + j of every batch that has it, run as one grouped
+// launch per operator.  Batches of a round are independent (their inputs come from the
+// previous round), so their layers may share launches.
+struct Slot {
+  std::vector<int> batch;   // batch indices
+  int item0 = 0, n_items = 0, max_groups = 1;
+};
+
+std::vector<Slot> build_slots(const std::vector<Batch>& batches, RoundTables* t) {
+  int max_len = 0;
+  for (const auto& b : batches) max_len = std::max(max_len, b.l1 - b.l0);
+  std::vector<Slot> slots(max_len);
+  for (int j = 0; j < max_len; ++j) {
+    Slot& sl = slots[j];
+    sl.item0 = static_cast<int>(t->items.size());
+    for (size_t bi = 0; bi < batches.size(); ++bi) {
+      const Batch& b = batches[bi];
+      if (b.l0 + j >= b.l1 || b.n == 0) continue;
+      sl.batch.push_back(static_cast<int>(bi));
+      for (dex::AttnItem it : b.items) {
+        it.layer = b.l0 + j;
+        it.counter = sl.n_items++;
+        sl.max_groups = std::max(sl.max_groups, it.n_groups);
+        t->items.push_back(it);
+      }
+    }
+  }
+  return slots;
+}
 
 struct Uploaded {
   dex::DevNode* nodes;
@@ -212,45 +251,77 @@ dex::GemmArgs base_args(dex_handle* h) {
   return a;
 }
 
-// Launch one GEMM over rows [row0, row0 + n) in slices of at most 256 node columns.
+// Launch one grouped GEMM.  Every group has at most 256 node rows; nmax is the largest.
 int gemm(dex_handle* h, int epi, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& a2,
-         const CUtensorMap* bmaps, dex::GemmArgs a, int row0, int n, int64_t weight_bytes, int64_t act_bytes_per_row) {
-  for (int r = row0; r < row0 + n; r += 256) {
-    const int nn = std::min(256, row0 + n - r);
-    a.n = nn;
-    a.nt = (nn + 15) & ~15;
-    a.b_row0 = r;
-    a.tmem_cols = pow2_at_least(a.nt);
-    a.stages = dex::gemm_stages_for(a.nt, h->gemm_smem);
-    cudaEvent_t e0 = nullptr, e1 = nullptr;
-    if (h->timing >= 2) {
-      e0 = next_event(h);
-      e1 = next_event(h);
-      cudaEventRecord(e0, h->st);
-    }
-    cudaError_t e = dex::launch_gemm(epi, a0, a1, a2, bmaps[a.nt / 16], a, h->gemm_ctas, h->st, true);
-    if (e != cudaSuccess) return cuda_fail(h, e);
-    if (h->timing >= 2) {
-      cudaEventRecord(e1, h->st);
-      h->gemm_events.push_back({e0, e1});
-    }
-    h->stats.kernel_launches++;
-    h->stats.gemm_launches++;
-    h->stats.gemm_bytes += weight_bytes + act_bytes_per_row * nn;
+         const CUtensorMap* bmaps, dex::GemmArgs a, int nmax, int64_t weight_bytes, int64_t act_bytes_per_row) {
+  if (nmax < 1 || nmax > 256) return DEX_ECAPACITY;
+  a.nt = (nmax + 15) & ~15;
+  a.ctas_per_group = h->gemm_ctas;
+  a.tmem_cols = pow2_at_least(a.nt);
+  a.stages = dex::gemm_stages_for(a.nt, h->gemm_smem);
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  if (h->timing >= 2) {
+    e0 = next_event(h);
+    e1 = next_event(h);
+    cudaEventRecord(e0, h->st);
   }
+  cudaError_t e = dex::launch_gemm(epi, a0, a1, a2, bmaps[a.nt / 16], a, h->st, true);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  if (h->timing >= 2) {
+    cudaEventRecord(e1, h->st);
+    h->gemm_events.push_back({e0, e1});
+  }
+  int rows = 0;
+  for (int g = 0; g < a.n_groups; ++g) rows += a.groups[g].n;
+  h->stats.kernel_launches++;
+  h->stats.gemm_launches++;
+  h->stats.gemm_bytes += weight_bytes * a.n_groups + act_bytes_per_row * rows;
   return DEX_OK;
 }
 
-// The decoder layers of one stage batch: rows [off, off + n), layers [l0, l1).
-int run_layers(dex_handle* h, const Uploaded& u, int off, int n, int l0, int l1, int item0, int n_items,
-               int max_groups_launch, bool with_exit) {
+// The decoder layers of every slot: per slot, grouped QKV+RoPE+KV write, lattice
+// attention, O + residual, gate/up + SwiGLU, down + residual over the slot's batches.
+int run_layers(dex_handle* h, const Uploaded& u, const std::vector<Batch>& batches, const std::vector<Slot>& slots,
+               bool with_exit) {
   const int qd = h->H * h->hd, kvd = h->KVH * h->hd;
   const int64_t d = h->d;
-  for (int l = l0; l < l1; ++l) {
-    dex::GemmArgs a = base_args(h);
-    a.nodes = u.nodes;
-    a.layer = l;
+  for (size_t j = 0; j < slots.size(); ++j) {
+    const Slot& sl = slots[j];
+    const int ng = static_cast<int>(sl.batch.size());
+    if (ng == 0) continue;
+    int nmax = 0;
+    for (int bi : sl.batch) nmax = std::max(nmax, batches[bi].n);
+    auto fill_groups = [&](dex::GemmArgs& a, int op) {
+      a.nodes = u.nodes;
+      a.n_groups = ng;
+      for (int g = 0; g < ng; ++g) {
+        const Batch& b = batches[sl.batch[g]];
+        const int l = b.l0 + static_cast<int>(j);
+        dex::GemmGroup& gr = a.groups[g];
+        gr = dex::GemmGroup{};
+        gr.b_row0 = b.off;
+        gr.n = b.n;
+        gr.layer = l;
+        if (op == 0) gr.a_packed = h->pk_qkv[l];
+        if (op == 1) {
+          gr.a_packed = h->pk_o[l];
+          gr.has_next = 1;
+          gr.g_next = W(h, l, 5);
+        }
+        if (op == 2) gr.a_packed = h->pk_gu[l];
+        if (op == 3) {
+          const bool last = (l == b.l1 - 1);
+          gr.a_packed = h->pk_d[l];
+          gr.has_next = (!last && l + 1 < h->L) ? 1 : 0;
+          gr.g_next = (l + 1 < h->L) ? W(h, l + 1, 0) : nullptr;
+          gr.stage_end = (last && with_exit) ? 1 : 0;
+        }
+      }
+    };
+    const int l_first = batches[sl.batch[0]].l0 + static_cast<int>(j);   // tensor maps of one member (unused when packed)
     // QKV + RoPE + KV write
+    dex::GemmArgs a = base_args(h);
+    fill_groups(a, 0);
     a.kblocks = (h->d + 63) / 64;
     a.src_tiles0 = qd / 128;
     a.src_tiles1 = kvd / 128;
@@ -260,13 +331,13 @@ int run_layers(dex_handle* h, const Uploaded& u, int off, int n, int l0, int l1,
     a.kv_commit = h->kv_commit;
     a.kv_pool = h->kv_pool;
     a.rope = h->rope;
-    int rc = gemm(h, dex::EPI_QKV, h->tm_q[l], h->tm_k[l], h->tm_v[l], h->tm_hb, a, off, n,
+    int rc = gemm(h, dex::EPI_QKV, h->tm_q[l_first], h->tm_k[l_first], h->tm_v[l_first], h->tm_hb, a, nmax,
                   static_cast<int64_t>(qd + 2 * kvd) * d * 2, d * 2 + qd * 4 + 2 * kvd * 2);
     if (rc) return rc;
-    // lattice attention
+    // lattice attention over every batch of the slot
     dex::AttnArgs at = {};
     at.nodes = u.nodes;
-    at.items = u.items + item0;
+    at.items = u.items + sl.item0;
     at.tails = u.tails;
     at.q = h->q;
     at.kv_commit = h->kv_commit;
@@ -275,7 +346,6 @@ int run_layers(dex_handle* h, const Uploaded& u, int off, int n, int l0, int l1,
     at.part = h->attn_part;
     at.counters = h->attn_counters;
     at.err = h->err;
-    at.layer = l;
     at.H = h->H;
     at.KVH = h->KVH;
     at.hd = h->hd;
@@ -284,52 +354,45 @@ int run_layers(dex_handle* h, const Uploaded& u, int off, int n, int l0, int l1,
     at.n_slots = h->n_slots;
     at.max_groups = h->max_groups;
     at.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(h->hd)));
-    cudaError_t ce = dex::launch_attention(at, n_items, max_groups_launch, h->st, true);
+    cudaError_t ce = dex::launch_attention(at, sl.n_items, sl.max_groups, h->st, true);
     if (ce != cudaSuccess) return cuda_fail(h, ce);
     h->stats.kernel_launches++;
     // O projection + residual
     a = base_args(h);
-    a.nodes = u.nodes;
-    a.layer = l;
+    fill_groups(a, 1);
     a.kblocks = (qd + 63) / 64;
     a.n_tiles = h->d / 128;
     a.src_tiles0 = a.n_tiles;
     a.hidden = h->hidden;
     a.hb_out = h->hb;
-    a.g_next = W(h, l, 5);
     a.ssq_out = h->ssq;
-    rc = gemm(h, dex::EPI_RESID, h->tm_o[l], h->tm_o[l], h->tm_o[l], h->tm_attn, a, off, n,
+    rc = gemm(h, dex::EPI_RESID, h->tm_o[l_first], h->tm_o[l_first], h->tm_o[l_first], h->tm_attn, a, nmax,
               static_cast<int64_t>(qd) * d * 2, qd * 2 + d * 8 + d * 2);
     if (rc) return rc;
     // gate/up + SwiGLU
     a = base_args(h);
-    a.nodes = u.nodes;
-    a.layer = l;
+    fill_groups(a, 2);
     a.kblocks = (h->d + 63) / 64;
     a.n_tiles = (h->dff + 63) / 64;
     a.src_tiles0 = a.n_tiles;
     a.ssq_in = h->ssq;
     a.act_out = h->act;
-    rc = gemm(h, dex::EPI_SWIGLU, h->tm_g[l], h->tm_u[l], h->tm_u[l], h->tm_hb, a, off, n,
+    rc = gemm(h, dex::EPI_SWIGLU, h->tm_g[l_first], h->tm_u[l_first], h->tm_u[l_first], h->tm_hb, a, nmax,
               static_cast<int64_t>(2) * h->dff * d * 2, d * 2 + h->dff * 2);
     if (rc) return rc;
     // down + residual (+ exit-head input at the stage boundary)
     a = base_args(h);
-    a.nodes = u.nodes;
-    a.layer = l;
+    fill_groups(a, 3);
     a.kblocks = (h->dff + 63) / 64;
     a.n_tiles = h->d / 128;
     a.src_tiles0 = a.n_tiles;
     a.hidden = h->hidden;
-    const bool last = (l == l1 - 1);
-    a.hb_out = (!last && l + 1 < h->L) ? h->hb : nullptr;
-    a.g_next = (l + 1 < h->L) ? W(h, l + 1, 0) : nullptr;
+    a.hb_out = h->hb;
     a.ssq_out = h->ssq;
-    a.stage_end = (last && with_exit) ? 1 : 0;
     a.exit_hb = h->exit_hb;
     a.g_final = h->final_norm;
     a.exit_ssq = h->exit_ssq;
-    rc = gemm(h, dex::EPI_RESID, h->tm_d[l], h->tm_d[l], h->tm_d[l], h->tm_act, a, off, n,
+    rc = gemm(h, dex::EPI_RESID, h->tm_d[l_first], h->tm_d[l_first], h->tm_d[l_first], h->tm_act, a, nmax,
               static_cast<int64_t>(h->dff) * d * 2, h->dff * 2 + d * 8 + d * 4);
     if (rc) return rc;
   }
@@ -355,15 +418,14 @@ int run_round(dex_handle* h, dex::Lattice* lat, std::vector<dex_copy_job>* pendi
   const int NS = lat->N();
   const std::vector<int>& X = lat->X();
   RoundTables t;
-  t.stage_off.assign(NS + 1, 0);
-  t.item_begin.assign(NS + 1, 0);
+  std::vector<int> stage_off(NS + 1, 0);
   int max_stage = 0;
   for (const auto& p : plan) {
     if (p.target_pos >= h->cfg.max_ctx) return DEX_ECAPACITY;
-    t.stage_off[p.stage + 1]++;
+    stage_off[p.stage + 1]++;
     max_stage = std::max(max_stage, p.stage);
   }
-  for (int s = 0; s < NS; ++s) t.stage_off[s + 1] += t.stage_off[s];
+  for (int s = 0; s < NS; ++s) stage_off[s + 1] += stage_off[s];
   for (int k = 0; k < n; ++k) {
     const auto& p = plan[k];
     dex::DevNode dn = {};
@@ -385,31 +447,34 @@ int run_round(dex_handle* h, dex::Lattice* lat, std::vector<dex_copy_job>* pendi
     for (int i = 0; i < p.n_prior; ++i) t.priors.push_back(p.prior[i]);
     t.nodes.push_back(dn);
   }
-  // attention items: per stage, one per sequence's contiguous rows
-  int max_groups_launch = 1;
-  for (int s = 0; s < NS; ++s) {
-    t.item_begin[s] = static_cast<int>(t.items.size());
-    for (int k = t.stage_off[s]; k < t.stage_off[s + 1];) {
+  // one batch per live stage: its layers (d_{s-1}, d_s] and one attention item per
+  // sequence's contiguous rows
+  std::vector<Batch> batches;
+  for (int s = 0; s <= max_stage; ++s) {
+    Batch b;
+    b.off = stage_off[s];
+    b.n = stage_off[s + 1] - stage_off[s];
+    b.l0 = s > 0 ? X[s - 1] : 0;
+    b.l1 = X[s];
+    for (int k = b.off; k < b.off + b.n;) {
       int e = k;
       dex::AttnItem it = {};
       it.seq = plan[k].seq;
       it.row_begin = k;
-      it.max_pos = 0;
-      it.max_cend = 0;
-      while (e < t.stage_off[s + 1] && plan[e].seq == it.seq) {
+      while (e < b.off + b.n && plan[e].seq == it.seq) {
         it.max_pos = std::max(it.max_pos, plan[e].pos);
         it.max_cend = std::max(it.max_cend, plan[e].c_end);
         ++e;
       }
       it.row_end = e;
       it.n_groups = it.max_pos / 128 + 1;
-      it.counter = static_cast<int>(t.items.size());
-      max_groups_launch = std::max(max_groups_launch, it.n_groups);
-      t.items.push_back(it);
+      b.items.push_back(it);
       k = e;
     }
+    if (b.n > 256) return DEX_ECAPACITY;
+    batches.push_back(b);
   }
-  t.item_begin[NS] = static_cast<int>(t.items.size());
+  const std::vector<Slot> slots = build_slots(batches, &t);
   t.jobs = *pending;
   const double host_plan_ms =
       std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t_host0).count();
@@ -450,14 +515,8 @@ int run_round(dex_handle* h, dex::Lattice* lat, std::vector<dex_copy_job>* pendi
   cudaError_t ce = dex::launch_assemble(aa, h->st, false);
   if (ce != cudaSuccess) return cuda_fail(h, ce);
   h->stats.kernel_launches++;
-  for (int s = 0; s <= max_stage; ++s) {
-    const int off = t.stage_off[s], ns = t.stage_off[s + 1] - off;
-    if (ns == 0) continue;
-    const int l0 = s > 0 ? X[s - 1] : 0;
-    rc = run_layers(h, u, off, ns, l0, X[s], t.item_begin[s], t.item_begin[s + 1] - t.item_begin[s],
-                    max_groups_launch, true);
-    if (rc) return rc;
-  }
+  rc = run_layers(h, u, batches, slots, true);
+  if (rc) return rc;
   if (ev[2]) cudaEventRecord(ev[2], h->st);
   // exit head + DECS over every node of the round
   {
@@ -473,8 +532,15 @@ int run_round(dex_handle* h, dex::Lattice* lat, std::vector<dex_copy_job>* pendi
     a.sample = h->cfg.sample;
     a.tau = h->cfg.tau;
     a.seed = h->cfg.seed;
-    rc = gemm(h, dex::EPI_EXIT, h->tm_lm, h->tm_lm, h->tm_lm, h->tm_exit, a, 0, n,
-              static_cast<int64_t>(h->V) * h->d * 2, static_cast<int64_t>(h->d) * 2);
+    for (int r0 = 0; r0 < n && !rc; r0 += 256) {
+      a.n_groups = 1;
+      a.groups[0] = dex::GemmGroup{};
+      a.groups[0].a_packed = h->pk_lm;
+      a.groups[0].b_row0 = r0;
+      a.groups[0].n = std::min(256, n - r0);
+      rc = gemm(h, dex::EPI_EXIT, h->tm_lm, h->tm_lm, h->tm_lm, h->tm_exit, a, a.groups[0].n,
+                static_cast<int64_t>(h->V) * h->d * 2, static_cast<int64_t>(h->d) * 2);
+    }
     if (rc) return rc;
   }
   if (ev[3]) cudaEventRecord(ev[3], h->st);
@@ -502,11 +568,10 @@ int run_round(dex_handle* h, dex::Lattice* lat, std::vector<dex_copy_job>* pendi
                            h->hd * h->d + 3ll * h->dff * h->d) * 2;
   h->stats.weight_bytes += layer_w * X[max_stage] + static_cast<int64_t>(h->V) * h->d * 2;
   const int64_t kv_row = 2ll * h->KVH * h->hd * 2;
-  for (int s = 0; s <= max_stage; ++s) {
-    const int nl = X[s] - (s > 0 ? X[s - 1] : 0);
-    for (int i = t.item_begin[s]; i < t.item_begin[s + 1]; ++i)
-      h->stats.kv_bytes += kv_row * nl * t.items[i].max_cend;
-    for (int k = t.stage_off[s]; k < t.stage_off[s + 1]; ++k) {
+  for (const Batch& b : batches) {
+    const int nl = b.l1 - b.l0;
+    for (const auto& it : b.items) h->stats.kv_bytes += kv_row * nl * it.max_cend;
+    for (int k = b.off; k < b.off + b.n; ++k) {
       h->stats.node_layers += nl;
       h->stats.kv_bytes += kv_row * nl * plan[k].n_tail;
     }
@@ -666,14 +731,16 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
                                               static_cast<size_t>(h->d / 128),
                                               static_cast<size_t>((h->dff + 63) / 64),
                                               static_cast<size_t>((h->V + 127) / 128)});
-  if (dalloc(h, &h->partial, dex::gemm_partial_bytes(256, h->gemm_ctas)) || dalloc(h, &h->counters, ntiles_max * 4))
+  if (dalloc(h, &h->partial, dex::gemm_partial_bytes(256, h->gemm_ctas) * std::max(1, h->N)) ||
+      dalloc(h, &h->counters, ntiles_max * 4 * std::max(1, h->N)))
     return DEX_ENOMEM;
-  h->plan_cap = (R * sizeof(dex::DevNode) + R * 16 * 8 + 1024 * sizeof(dex::AttnItem) + 64 * 16 + 8192);
+  h->plan_cap = (R * sizeof(dex::DevNode) + R * 16 * 8 +
+                 static_cast<size_t>(L) * (B * h->N + 8) * sizeof(dex::AttnItem) + 64 * 16 + 8192);
   if (dalloc(h, &h->d_plan, h->plan_cap)) return DEX_ENOMEM;
   if (cudaMallocHost(&h->h_plan, h->plan_cap) != cudaSuccess) return DEX_ENOMEM;
   if (cudaMallocHost(&h->h_best, (R + 1) * 8) != cudaSuccess) return DEX_ENOMEM;
   // zero-initialised state
-  cudaMemsetAsync(h->counters, 0, ntiles_max * 4, h->st);
+  cudaMemsetAsync(h->counters, 0, ntiles_max * 4 * std::max(1, h->N), h->st);
   cudaMemsetAsync(h->attn_counters, 0, (static_cast<size_t>(B) * h->N * KVH + 256 * KVH) * 4, h->st);
   cudaMemsetAsync(h->err, 0, 16, h->st);
   cudaMemsetAsync(h->kv_commit, 0, B * L * 2 * KVH * ctx * hd * 2, h->st);
@@ -725,6 +792,46 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
     rc |= encode_2d(&h->tm_exit[i], h->exit_hb, R, h->d, 16 * i);
   }
   if (rc) return DEX_EINVAL;
+  // pack every GEMM weight once: contiguous, pre-swizzled 16 KB boxes in streaming order
+  {
+    const int kb_d = (h->d + 63) / 64, kb_q = (qd + 63) / 64, kb_f = (h->dff + 63) / 64;
+    const int t_qkv = (qd + 2 * kvd) / 128, t_o = h->d / 128, t_gu = (h->dff + 63) / 64, t_lm = (h->V + 127) / 128;
+    const size_t b_qkv = dex::packed_bytes(t_qkv, kb_d), b_o = dex::packed_bytes(t_o, kb_q);
+    const size_t b_gu = dex::packed_bytes(t_gu, kb_d), b_d = dex::packed_bytes(t_o, kb_f);
+    const size_t b_lm = dex::packed_bytes(t_lm, kb_d);
+    h->packed_total = L * (b_qkv + b_o + b_gu + b_d) + b_lm;
+    uint8_t* base = nullptr;
+    if (dalloc(h, &base, h->packed_total)) return DEX_ENOMEM;
+    using PS = dex::PackSrc;
+    const PS none = {nullptr, 0};
+    cudaError_t ce = cudaSuccess;
+    for (size_t l = 0; l < L; ++l) {
+      const int li = static_cast<int>(l);
+      uint8_t* pq = base + l * (b_qkv + b_o + b_gu + b_d);
+      uint8_t* po = pq + b_qkv;
+      uint8_t* pg = po + b_o;
+      uint8_t* pd = pg + b_gu;
+      h->pk_qkv.push_back(pq);
+      h->pk_o.push_back(po);
+      h->pk_gu.push_back(pg);
+      h->pk_d.push_back(pd);
+      if (ce == cudaSuccess)
+        ce = dex::launch_pack(dex::PACK_ROWS, PS{W(h, li, 1), qd}, PS{W(h, li, 2), kvd}, PS{W(h, li, 3), kvd}, h->d,
+                              t_qkv, pq, h->st);
+      if (ce == cudaSuccess)
+        ce = dex::launch_pack(dex::PACK_ROWS, PS{W(h, li, 4), h->d}, none, none, qd, t_o, po, h->st);
+      if (ce == cudaSuccess)
+        ce = dex::launch_pack(dex::PACK_SWIGLU, PS{W(h, li, 6), h->dff}, PS{W(h, li, 7), h->dff}, none, h->d, t_gu,
+                              pg, h->st);
+      if (ce == cudaSuccess)
+        ce = dex::launch_pack(dex::PACK_ROWS, PS{W(h, li, 8), h->d}, none, none, h->dff, t_o, pd, h->st);
+    }
+    uint8_t* plm = base + L * (b_qkv + b_o + b_gu + b_d);
+    h->pk_lm = plm;
+    if (ce == cudaSuccess)
+      ce = dex::launch_pack(dex::PACK_ROWS, PS{h->lm_head, h->V}, none, none, h->d, t_lm, plm, h->st);
+    if (ce != cudaSuccess) return DEX_ECUDA;
+  }
   if (cudaStreamSynchronize(h->st) != cudaSuccess) return DEX_ECUDA;
   *out = hp.release();
   return DEX_OK;
@@ -762,6 +869,11 @@ int dex_prefill(dex_handle* h, int32_t seq, const int32_t* tokens, int32_t n_tok
       dn.unmasked = 1;
       t.nodes.push_back(dn);
     }
+    std::vector<Batch> batches(1);
+    batches[0].off = 0;
+    batches[0].n = n;
+    batches[0].l0 = 0;
+    batches[0].l1 = h->L;
     dex::AttnItem it = {};
     it.seq = seq;
     it.row_begin = 0;
@@ -769,8 +881,8 @@ int dex_prefill(dex_handle* h, int32_t seq, const int32_t* tokens, int32_t n_tok
     it.max_pos = c0 + n - 1;
     it.max_cend = c0 + n;
     it.n_groups = it.max_pos / 128 + 1;
-    it.counter = 0;
-    t.items.push_back(it);
+    batches[0].items.push_back(it);
+    const std::vector<Slot> slots = build_slots(batches, &t);
     Uploaded u;
     int rc = upload(h, t, &u);
     if (rc) return rc;
@@ -786,7 +898,7 @@ int dex_prefill(dex_handle* h, int32_t seq, const int32_t* tokens, int32_t n_tok
     aa.best = nullptr;
     cudaError_t ce = dex::launch_assemble(aa, h->st, false);
     if (ce != cudaSuccess) return cuda_fail(h, ce);
-    rc = run_layers(h, u, 0, n, 0, h->L, 0, 1, it.n_groups, false);
+    rc = run_layers(h, u, batches, slots, false);
     if (rc) return rc;
     // the upload buffer is reused by the next chunk: wait for this chunk
     if (cudaMemcpyAsync(h->h_best + h->rows_cap, h->err, 4, cudaMemcpyDeviceToHost, h->st) != cudaSuccess ||
@@ -943,9 +1055,11 @@ int dex_exit_head_decs(const void* hidden, int32_t n, int32_t d, const void* fin
       rc = DEX_ECUDA;
     exit_nodes_kernel<<<(n + 127) / 128, 128, 0, st>>>(nodes, n, dn);
     dex::GemmArgs a = {};
-    a.n = n;
+    a.n_groups = 1;
+    a.ctas_per_group = n_sm;
+    a.groups[0].n = n;
+    a.groups[0].b_row0 = 0;
     a.nt = nt;
-    a.b_row0 = 0;
     a.kblocks = kb;
     a.stages = dex::gemm_stages_for(nt);
     a.n_tiles = n_tiles;
@@ -966,8 +1080,7 @@ int dex_exit_head_decs(const void* hidden, int32_t n, int32_t d, const void* fin
     a.sample = sample;
     a.tau = tau;
     a.seed = seed;
-    if (!rc && dex::launch_gemm(dex::EPI_EXIT, tm_w, tm_w, tm_w, tm_b, a, n_sm, st, false) != cudaSuccess)
-      rc = DEX_ECUDA;
+    if (!rc && dex::launch_gemm(dex::EPI_EXIT, tm_w, tm_w, tm_w, tm_b, a, st, false) != cudaSuccess) rc = DEX_ECUDA;
     if (!rc && dex::launch_decode_best(best, n, tokens, st) != cudaSuccess) rc = DEX_ECUDA;
   }
   cudaFreeAsync(scratch, st);
@@ -1071,9 +1184,11 @@ extern "C" int dex_exit_head_decs_noalloc(const void* hidden, int32_t n, int32_t
   exit_nodes_kernel<<<(n + 127) / 128, 128, 0, st>>>(nodes, n, dn);
   if (cudaGetLastError() != cudaSuccess) return DEX_ECUDA;
   dex::GemmArgs a = {};
-  a.n = n;
+  a.n_groups = 1;
+  a.ctas_per_group = n_sm;
+  a.groups[0].n = n;
+  a.groups[0].b_row0 = 0;
   a.nt = nt;
-  a.b_row0 = 0;
   a.kblocks = kb;
   a.stages = dex::gemm_stages_for(nt);
   a.n_tiles = n_tiles;
@@ -1094,7 +1209,7 @@ extern "C" int dex_exit_head_decs_noalloc(const void* hidden, int32_t n, int32_t
   a.sample = sample;
   a.tau = tau;
   a.seed = seed;
-  if (dex::launch_gemm(dex::EPI_EXIT, tm_w, tm_w, tm_w, tm_b, a, n_sm, st, false) != cudaSuccess) return DEX_ECUDA;
+  if (dex::launch_gemm(dex::EPI_EXIT, tm_w, tm_w, tm_w, tm_b, a, st, false) != cudaSuccess) return DEX_ECUDA;
   if (dex::launch_decode_best(best, n, tokens, st) != cudaSuccess) return DEX_ECUDA;
   return DEX_OK;
 }

@@ -93,8 +93,11 @@ template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB,
-                   const GemmArgs a) {
-  const int G = gridDim.x, cta = blockIdx.x;
+                   const __grid_constant__ GemmArgs a) {
+  const int G = a.ctas_per_group;
+  const int gi = blockIdx.x / G, cta = blockIdx.x % G;   // group, CTA within the group
+  const GemmGroup& grp = a.groups[gi];
+  const int b_row0 = grp.b_row0;
   const int kb = a.kblocks;
   const long long W = static_cast<long long>(a.n_tiles) * kb;
   const long long w0 = work_start(cta, W, G), w1 = work_start(cta + 1, W, G);
@@ -148,9 +151,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     sflag[0] = 0;
     sflag[1] = 0;
     fence_mbar_init();
-    tma_prefetch(&tmA0);
-    if (a.src_tiles0 < a.n_tiles || EPI == EPI_SWIGLU) tma_prefetch(&tmA1);
-    if (a.src_tiles0 + a.src_tiles1 < a.n_tiles) tma_prefetch(&tmA2);
+    if (!grp.a_packed) {
+      tma_prefetch(&tmA0);
+      if (a.src_tiles0 < a.n_tiles || EPI == EPI_SWIGLU) tma_prefetch(&tmA1);
+      if (a.src_tiles0 + a.src_tiles1 < a.n_tiles) tma_prefetch(&tmA2);
+    }
     tma_prefetch(&tmB);
   }
   if (warp == 1) {
@@ -168,10 +173,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
       auto load_a = [&](long long w, int st) {
+        uint8_t* dst = sA + static_cast<size_t>(st) * kABytes;
+        if (grp.a_packed) {   // packed weights: the work item's 16 KB box is contiguous
+          const uint8_t* src = grp.a_packed + static_cast<size_t>(w) * kABytes;
+          if (a.evict_first) bulk_load_1d_hint(dst, src, kABytes, &full[st], pol);
+          else bulk_load_1d(dst, src, kABytes, &full[st]);
+          return;
+        }
         const int t = static_cast<int>(w / kb), kx = static_cast<int>(w % kb) * kBK;
         int src, lt;
         tile_src(t, src, lt);
-        uint8_t* dst = sA + static_cast<size_t>(st) * kABytes;
         if (EPI == EPI_SWIGLU) {
           if (a.evict_first) {
             tma_load_2d_hint(dst, &tmA0, &full[st], kx, lt * 64, pol);
@@ -188,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto load_b = [&](long long w, int st) {
         tma_load_2d(sB + static_cast<size_t>(st) * b_bytes, &tmB, &full[st], static_cast<int>(w % kb) * kBK,
-                    a.b_row0);
+                    b_row0);
       };
       const int npre = nwork < stages ? nwork : stages;
       for (int i = 0; i < npre; ++i) {
@@ -254,12 +265,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wq = warp & 3;           // TMEM lane quarter this warp may access
     const int r = wq * 32 + lane;      // accumulator row within the tile
     const int ep = tid - 64;           // 0..127
-    const int n = a.n;
+    const int n = grp.n;
     const int ndt = a.d / 128;
     griddep_wait();
     if (EPI != EPI_RESID) {
       for (int c = ep; c < n; c += 128) {
-        const float* s = a.ssq_in + static_cast<size_t>(a.b_row0 + c) * ndt;
+        const float* s = a.ssq_in + static_cast<size_t>(b_row0 + c) * ndt;
         float t = s[0];
         for (int j = 1; j < ndt; ++j) t = __fadd_rn(t, s[j]);
         inv[c] = 1.0f / sqrtf(__fadd_rn(__fdiv_rn(t, static_cast<float>(a.d)), a.eps));
@@ -278,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 16; ++j) {
           const int c = c0 + j;
           if (c >= n) break;
-          const DevNode* nd = a.nodes + a.b_row0 + c;
+          const DevNode* nd = a.nodes + b_row0 + c;
           const float x = xch[j * kBM + r];
           float out = x;
           if (src != 2) {
@@ -287,17 +298,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             out = dim < half ? x * cs.x - y * cs.y : x * cs.x + y * cs.y;
           }
           if (src == 0) {
-            a.q_out[static_cast<size_t>(a.b_row0 + c) * (a.H * a.hd) + f] = out;
+            a.q_out[static_cast<size_t>(b_row0 + c) * (a.H * a.hd) + f] = out;
           } else {
             const int kv = src - 1;
             __nv_bfloat16* dst;
             if (nd->kv_commit) {
               dst = a.kv_commit +
-                    ((((static_cast<size_t>(nd->seq) * a.L + a.layer) * 2 + kv) * a.KVH + head) * a.max_ctx +
+                    ((((static_cast<size_t>(nd->seq) * a.L + grp.layer) * 2 + kv) * a.KVH + head) * a.max_ctx +
                      nd->pos) * a.hd + dim;
             } else {
               dst = a.kv_pool +
-                    ((((static_cast<size_t>(nd->seq) * a.n_slots + nd->slot) * a.L + a.layer) * 2 + kv) * a.KVH +
+                    ((((static_cast<size_t>(nd->seq) * a.n_slots + nd->slot) * a.L + grp.layer) * 2 + kv) * a.KVH +
                      head) * a.hd + dim;
             }
             *dst = __float2bfloat16_rn(out);
@@ -312,13 +323,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int c = c0 + j;
           sq[j] = 0.0f;
           if (c < n) {
-            const DevNode* nd = a.nodes + a.b_row0 + c;
+            const DevNode* nd = a.nodes + b_row0 + c;
             float* hp = a.hidden + static_cast<size_t>(nd->hrow) * a.d + f;
             const float x = __fadd_rn(*hp, v[j]);
             *hp = x;
-            const size_t o = static_cast<size_t>(a.b_row0 + c) * a.d + f;
-            if (a.hb_out) a.hb_out[o] = __float2bfloat16_rn(__fmul_rn(x, bf16_to_f32(a.g_next[f])));
-            if (a.stage_end) a.exit_hb[o] = __float2bfloat16_rn(__fmul_rn(x, bf16_to_f32(a.g_final[f])));
+            const size_t o = static_cast<size_t>(b_row0 + c) * a.d + f;
+            if (grp.has_next) a.hb_out[o] = __float2bfloat16_rn(__fmul_rn(x, bf16_to_f32(grp.g_next[f])));
+            if (grp.stage_end) a.exit_hb[o] = __float2bfloat16_rn(__fmul_rn(x, bf16_to_f32(a.g_final[f])));
             sq[j] = __fmul_rn(x, x);
           }
         }
@@ -331,9 +342,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ep < 16 && c0 + ep < n) {
           const float t = __fadd_rn(__fadd_rn(qsum[0 * 16 + ep], qsum[1 * 16 + ep]),
                                     __fadd_rn(qsum[2 * 16 + ep], qsum[3 * 16 + ep]));
-          const size_t o = static_cast<size_t>(a.b_row0 + c0 + ep) * ndt + lt;
+          const size_t o = static_cast<size_t>(b_row0 + c0 + ep) * ndt + lt;
           a.ssq_out[o] = t;
-          if (a.stage_end) a.exit_ssq[o] = t;
+          if (grp.stage_end) a.exit_ssq[o] = t;
         }
         named_bar_sync(1, 128);
       } else if (EPI == EPI_SWIGLU) {
@@ -347,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (c >= n) break;
             const float g = xch[j * kBM + r], u = xch[j * kBM + r + 64];
             const float act = g / (1.0f + expf(-g)) * u;
-            a.act_out[static_cast<size_t>(a.b_row0 + c) * a.d_ff + feat] = __float2bfloat16_rn(act);
+            a.act_out[static_cast<size_t>(b_row0 + c) * a.d_ff + feat] = __float2bfloat16_rn(act);
           }
         }
         named_bar_sync(1, 128);
@@ -359,8 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           float score = -INFINITY;
           if (c < n && vid < static_cast<uint32_t>(a.vocab)) {
             const float logit = v[j] * inv[c];
-            if (a.logits_dbg) a.logits_dbg[static_cast<size_t>(a.b_row0 + c) * a.vocab + vid] = logit;
-            const DevNode* nd = a.nodes + a.b_row0 + c;
+            if (a.logits_dbg) a.logits_dbg[static_cast<size_t>(b_row0 + c) * a.vocab + vid] = logit;
+            const DevNode* nd = a.nodes + b_row0 + c;
             bool masked = false;
             if (!nd->unmasked) {
               for (int p = 0; p < nd->n_prior; ++p) masked |= (a.priors[nd->prior_off + p] == static_cast<int>(vid));
@@ -379,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ep < 16 && c0 + ep < n) {
           unsigned long long k = qkey[ep];
           for (int w = 1; w < 4; ++w) k = qkey[w * 16 + ep] > k ? qkey[w * 16 + ep] : k;
-          atomicMax(a.best + a.b_row0 + c0 + ep, k);
+          atomicMax(a.best + b_row0 + c0 + ep, k);
         }
         named_bar_sync(1, 128);
       }
@@ -407,7 +418,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(&tfree[buf]);
       } else {
-        float* part = a.partial + static_cast<size_t>(partial_slot(cta, t, kb, W, G)) * a.nt * kBM;
+        float* gpart = a.partial + static_cast<size_t>(gi) * 2 * G * a.nt * kBM;
+        float* part = gpart + static_cast<size_t>(partial_slot(cta, t, kb, W, G)) * a.nt * kBM;
         for (int c0 = 0; c0 < n; c0 += 16) {
           float v[16];
           tmem_ld16(taddr + static_cast<uint32_t>(c0), v);
@@ -419,7 +431,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&tfree[buf]);
         __threadfence();
         named_bar_sync(1, 128);
-        if (ep == 0) sflag[0] = (atomicAdd(a.counters + t, 1) == parts - 1) ? 1 : 0;
+        int32_t* counter = a.counters + static_cast<size_t>(gi) * a.n_tiles + t;
+        if (ep == 0) sflag[0] = (atomicAdd(counter, 1) == parts - 1) ? 1 : 0;
         named_bar_sync(1, 128);
         if (sflag[0]) {   // last of the tile's CTAs: sum the partial tiles in k order
           __threadfence();
@@ -430,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool first = true;
             for (int c = c_lo; c <= c_hi; ++c) {
               if (!cta_touches_tile(c, t, kb, W, G)) continue;
-              const float* p = a.partial + static_cast<size_t>(partial_slot(c, t, kb, W, G)) * a.nt * kBM +
+              const float* p = gpart + static_cast<size_t>(partial_slot(c, t, kb, W, G)) * a.nt * kBM +
                                static_cast<size_t>(c0) * kBM + r;
 #pragma unroll
               for (int j = 0; j < 16; ++j)
@@ -439,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             epilogue_chunk(src, lt, c0, v);
           }
-          if (ep == 0) a.counters[t] = 0;
+          if (ep == 0) *counter = 0;
         }
         named_bar_sync(1, 128);
       }
@@ -456,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int EPI>
 static cudaError_t launch_one(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& a2,
-                              const CUtensorMap& b, const GemmArgs& args, int n_ctas, cudaStream_t st, bool pdl) {
+                              const CUtensorMap& b, const GemmArgs& args, cudaStream_t st, bool pdl) {
   static bool attr_set = false;
   const size_t smem = gemm_smem_bytes(args.nt, args.stages);
   if (!attr_set) {
@@ -466,7 +479,7 @@ static cudaError_t launch_one(const CUtensorMap& a0, const CUtensorMap& a1, cons
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(n_ctas));
+  cfg.gridDim = dim3(static_cast<unsigned>(args.n_groups * args.ctas_per_group));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
@@ -479,19 +492,38 @@ static cudaError_t launch_one(const CUtensorMap& a0, const CUtensorMap& a1, cons
 }
 
 cudaError_t launch_gemm(int epi, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& a2,
-                        const CUtensorMap& b, const GemmArgs& args, int n_ctas, cudaStream_t st, bool pdl) {
-  if (args.nt < 16 || args.nt > kNtMax || (args.nt & 15) || args.n < 1 || args.n > args.nt || n_ctas < 1)
+                        const CUtensorMap& b, const GemmArgs& args, cudaStream_t st, bool pdl) {
+  if (args.nt < 16 || args.nt > kNtMax || (args.nt & 15) || args.n_groups < 1 || args.n_groups > kMaxGroups ||
+      args.ctas_per_group < 1)
     return cudaErrorInvalidValue;
+  // every pointer the chosen epilogue dereferences must be set (checked here, on the host)
+  bool any_next = false, any_end = false;
+  for (int g = 0; g < args.n_groups; ++g) {
+    const GemmGroup& gr = args.groups[g];
+    if (gr.n < 1 || gr.n > args.nt || gr.b_row0 < 0) return cudaErrorInvalidValue;
+    if (gr.has_next && !gr.g_next) return cudaErrorInvalidValue;
+    any_next |= gr.has_next != 0;
+    any_end |= gr.stage_end != 0;
+  }
+  if (!args.err || !args.counters || !args.partial) return cudaErrorInvalidValue;
+  if (epi != EPI_RESID && !args.ssq_in) return cudaErrorInvalidValue;
+  if (epi != EPI_SWIGLU && !args.nodes) return cudaErrorInvalidValue;
+  if (epi == EPI_QKV && (!args.q_out || !args.kv_commit || !args.kv_pool || !args.rope)) return cudaErrorInvalidValue;
+  if (epi == EPI_RESID && (!args.hidden || !args.ssq_out || (any_next && !args.hb_out) ||
+                           (any_end && (!args.exit_hb || !args.exit_ssq || !args.g_final))))
+    return cudaErrorInvalidValue;
+  if (epi == EPI_SWIGLU && !args.act_out) return cudaErrorInvalidValue;
+  if (epi == EPI_EXIT && !args.best) return cudaErrorInvalidValue;
   if (args.tmem_cols < args.nt || args.tmem_cols < 32 || args.tmem_cols > 256 ||
       (args.tmem_cols & (args.tmem_cols - 1)))
     return cudaErrorInvalidValue;
   if (args.stages < 2 || args.stages > 8 || gemm_smem_bytes(args.nt, args.stages) > kSmemOptin)
     return cudaErrorInvalidValue;
   switch (epi) {
-    case EPI_QKV: return launch_one<EPI_QKV>(a0, a1, a2, b, args, n_ctas, st, pdl);
-    case EPI_RESID: return launch_one<EPI_RESID>(a0, a1, a2, b, args, n_ctas, st, pdl);
-    case EPI_SWIGLU: return launch_one<EPI_SWIGLU>(a0, a1, a2, b, args, n_ctas, st, pdl);
-    case EPI_EXIT: return launch_one<EPI_EXIT>(a0, a1, a2, b, args, n_ctas, st, pdl);
+    case EPI_QKV: return launch_one<EPI_QKV>(a0, a1, a2, b, args, st, pdl);
+    case EPI_RESID: return launch_one<EPI_RESID>(a0, a1, a2, b, args, st, pdl);
+    case EPI_SWIGLU: return launch_one<EPI_SWIGLU>(a0, a1, a2, b, args, st, pdl);
+    case EPI_EXIT: return launch_one<EPI_EXIT>(a0, a1, a2, b, args, st, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -41,29 +41,42 @@ struct AttnItem {
   int32_t max_pos, max_cend;         // largest input position / committed extent among the rows
   int32_t n_groups;                  // 128-position key groups covering 0..max_pos
   int32_t counter;                   // index of this item's merge counters (x KVH)
-  int32_t pad;
+  int32_t layer;                     // decoder layer of this item (items of several stages share a launch)
 };
 
 enum Epi : int { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_EXIT = 3 };
 
+// One weight matrix of a grouped launch: a stage's layer and that stage's node rows.  The
+// groups of a launch share the weight shape; each keeps its own fixed work partition.
+constexpr int kMaxGroups = 10;
+struct GemmGroup {
+  const uint8_t* a_packed;    // packed weights of this group's layer (null: TMA from tmA*)
+  const __nv_bfloat16* g_next;// RESID: gain of the next norm (null at the model's end)
+  int32_t b_row0;       // first node row (= first B row)
+  int32_t n;            // node rows
+  int32_t layer;        // decoder layer (QKV: KV cache addressing)
+  int32_t stage_end;    // RESID: last layer of the stage -> also write the exit-head input
+  int32_t has_next;     // RESID: write the next layer's bf16 input
+  int32_t pad;
+};
+
 struct GemmArgs {
   // tiling
-  int32_t n;            // valid node columns
-  int32_t nt;           // node tile (multiple of 16, <= 256)
-  int32_t b_row0;       // first B row (= first node row of the batch)
+  int32_t n_groups;     // weight matrices in this launch
+  int32_t ctas_per_group;     // fixed partition size of every group
+  int32_t nt;           // node tile (multiple of 16, <= 256) >= every group's n
   int32_t kblocks;      // K / 64, rounded up
   int32_t stages;       // smem pipeline depth
   int32_t n_tiles;      // output tiles
   int32_t src_tiles0, src_tiles1;   // tiles of source 0 and 1 (source 2 takes the rest)
   int32_t tmem_cols;
-  float* partial;       // [2 * gridDim.x][nt][128] fp32 partial tiles (two slots per CTA)
-  int32_t* counters;    // [n_tiles] arrival counters (left at 0)
+  float* partial;       // [n_groups][2 * ctas_per_group][nt][128] fp32 partial tiles
+  int32_t* counters;    // [n_groups][n_tiles] arrival counters (left at 0)
   int32_t* err;         // device error flag
   const DevNode* nodes; // node rows (absolute)
   int32_t evict_first;  // stream A with an L2 evict-first policy
   // model geometry
   int32_t d, H, KVH, hd, L, d_ff, vocab, max_ctx, n_slots;
-  int32_t layer;
   float eps;
   // RMSNorm inputs (QKV, SWIGLU, EXIT): per-row 128-feature partial sums of squares
   const float* ssq_in;  // [rows][d/128]
@@ -75,9 +88,7 @@ struct GemmArgs {
   // RESID
   float* hidden;        // [hrows][d]
   __nv_bfloat16* hb_out;      // [rows][d]  bf16(h * g_next), next layer's input
-  const __nv_bfloat16* g_next;
   float* ssq_out;       // [rows][d/128]
-  int32_t stage_end;    // last layer of the batch's stage: also write the exit-head input
   __nv_bfloat16* exit_hb;     // [rows][d]
   const __nv_bfloat16* g_final;
   float* exit_ssq;      // [rows][d/128]
@@ -90,6 +101,7 @@ struct GemmArgs {
   int32_t sample;
   float tau;
   unsigned long long seed;
+  GemmGroup groups[kMaxGroups];
 };
 
 struct AttnArgs {
@@ -103,7 +115,7 @@ struct AttnArgs {
   float* part;                 // [rows][H][max_groups][hd + 2]
   int32_t* counters;           // [items * KVH]
   int32_t* err;
-  int32_t layer, H, KVH, hd, L, max_ctx, n_slots, max_groups;
+  int32_t H, KVH, hd, L, max_ctx, n_slots, max_groups;
   float scale_log2;            // log2(e) / sqrt(hd)
 };
 
@@ -132,10 +144,10 @@ struct CollapseArgs {
 // ---- launchers (return cudaError_t of the launch) -----------------------------------------
 // A tensor maps: up to three weight sources (QKV: wq, wk, wv; SWIGLU: wg, wu with 64-row
 // boxes); B: the activation rows with a box of nt rows.
-// Persistent launch: grid = n_ctas (the SM count), each CTA streams a fixed contiguous
-// range of the (tile, k-block) work; stages chosen from the node tile.
+// Persistent launch: grid = n_groups x ctas_per_group; each CTA streams a fixed contiguous
+// range of its group's (tile, k-block) work; stages chosen from the node tile.
 cudaError_t launch_gemm(int epi, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& a2,
-                        const CUtensorMap& b, const GemmArgs& args, int n_ctas, cudaStream_t st, bool pdl);
+                        const CUtensorMap& b, const GemmArgs& args, cudaStream_t st, bool pdl);
 size_t gemm_smem_bytes(int nt, int stages);
 int gemm_stages_for(int nt, size_t small_budget = 104 * 1024);
 // Bytes of the partial-tile workspace a launch over n_ctas CTAs with node tile nt needs.
@@ -147,6 +159,17 @@ cudaError_t launch_collapse(const CollapseArgs& a, cudaStream_t st, bool pdl);
 // of an isolated exit-head call); zeroes the argmax slots.
 cudaError_t launch_exit_prep(const __nv_bfloat16* h, int n, int d, const __nv_bfloat16* g,
                              __nv_bfloat16* hb, float* ssq, unsigned long long* best, cudaStream_t st);
+// Packed GEMM weights: box (t, k) = rows 128t..128t+127 x columns 64k..64k+63 of the
+// (virtual) weight matrix, stored at byte offset (t * kblocks + k) * 16384 in the 128-byte
+// swizzled K-major shared-memory image (chunk c of row r at r*128 + (c ^ (r & 7))*16).
+// Modes: PACK_ROWS stacks up to three row-major sources (QKV: wq, wk, wv); PACK_SWIGLU
+// puts 64 rows of src0 (gate) over the same 64 rows of src1 (up) in each tile.  Rows and
+// columns outside the sources are zero.
+enum PackMode : int { PACK_ROWS = 0, PACK_SWIGLU = 1 };
+struct PackSrc { const __nv_bfloat16* ptr; int32_t rows; };
+size_t packed_bytes(int n_tiles, int kblocks);
+cudaError_t launch_pack(int mode, PackSrc s0, PackSrc s1, PackSrc s2, int K, int n_tiles, uint8_t* out,
+                        cudaStream_t st);
 cudaError_t launch_decode_best(const unsigned long long* best, int n, int32_t* tokens, cudaStream_t st);
 
 }  // namespace dex

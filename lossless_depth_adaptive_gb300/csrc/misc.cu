@@ -67,6 +67,8 @@ __global__ void __launch_bounds__(128) assemble_kernel(const AssembleArgs a) {
 
 cudaError_t launch_assemble(const AssembleArgs& a, cudaStream_t st, bool pdl) {
   if (a.n_rows <= 0) return cudaSuccess;
+  if (!a.nodes || !a.embed || !a.attn_norm || !a.hidden || !a.hb || !a.ssq || a.d % 128 || a.d > 128 * 64)
+    return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(a.n_rows));
   cfg.blockDim = dim3(128);
@@ -106,6 +108,7 @@ __global__ void __launch_bounds__(256) collapse_kernel(const CollapseArgs a) {
 
 cudaError_t launch_collapse(const CollapseArgs& a, cudaStream_t st, bool pdl) {
   if (a.n_jobs <= 0) return cudaSuccess;
+  if (!a.jobs || !a.kv_commit || !a.kv_pool) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(32, static_cast<unsigned>(a.n_jobs));
   cfg.blockDim = dim3(256);
@@ -142,6 +145,53 @@ __global__ void __launch_bounds__(128) exit_prep_kernel(const __nv_bfloat16* h, 
 cudaError_t launch_exit_prep(const __nv_bfloat16* h, int n, int d, const __nv_bfloat16* g, __nv_bfloat16* hb,
                              float* ssq, unsigned long long* best, cudaStream_t st) {
   exit_prep_kernel<<<n, 128, 0, st>>>(h, d, g, hb, ssq, best);
+  return cudaGetLastError();
+}
+
+// Weight packing (once per handle): one thread per 16-byte chunk of the packed image.
+__global__ void __launch_bounds__(256) pack_kernel(int mode, PackSrc s0, PackSrc s1, PackSrc s2, int K, int kblocks,
+                                                   long long n_chunks, uint8_t* out) {
+  for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < n_chunks;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(idx & 7), r = static_cast<int>((idx >> 3) & 127);
+    const long long box = idx >> 10;
+    const int t = static_cast<int>(box / kblocks), k = static_cast<int>(box % kblocks);
+    const __nv_bfloat16* src = nullptr;
+    int srow = 0;
+    if (mode == PACK_SWIGLU) {
+      const PackSrc& ps = r < 64 ? s0 : s1;
+      srow = t * 64 + (r & 63);
+      if (srow < ps.rows) src = ps.ptr;
+    } else {
+      int grow = t * 128 + r;
+      if (grow < s0.rows) {
+        src = s0.ptr;
+        srow = grow;
+      } else if ((grow -= s0.rows) < s1.rows) {
+        src = s1.ptr;
+        srow = grow;
+      } else if ((grow -= s1.rows) < s2.rows) {
+        src = s2.ptr;
+        srow = grow;
+      }
+    }
+    const int col = k * 64 + ((c ^ (r & 7)) * 8);   // the chunk stored at position c
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (src && col < K) v = *reinterpret_cast<const uint4*>(src + static_cast<size_t>(srow) * K + col);
+    *reinterpret_cast<uint4*>(out + box * 16384 + r * 128 + c * 16) = v;
+  }
+}
+
+size_t packed_bytes(int n_tiles, int kblocks) { return static_cast<size_t>(n_tiles) * kblocks * 16384; }
+
+cudaError_t launch_pack(int mode, PackSrc s0, PackSrc s1, PackSrc s2, int K, int n_tiles, uint8_t* out,
+                        cudaStream_t st) {
+  if (K % 8) return cudaErrorInvalidValue;
+  const int kblocks = (K + 63) / 64;
+  const long long n_chunks = static_cast<long long>(n_tiles) * kblocks * 1024;
+  const long long blocks = (n_chunks + 255) / 256;
+  pack_kernel<<<static_cast<unsigned>(blocks < 65535 * 16 ? blocks : 65535 * 16), 256, 0, st>>>(
+      mode, s0, s1, s2, K, kblocks, n_chunks, out);
   return cudaGetLastError();
 }
 
