@@ -36,6 +36,7 @@ constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr uint32_t kABytes = kBM * kBK * 2;   // 16 KB weight tile per stage
 constexpr int kNtMax = 256;
+constexpr int kMaxContrib = 32;   // partial tiles listed in shared memory per reduction
 
 struct SmemMap {
   size_t a, b, bar, misc, xch, inv, qsum, qkey, total;
@@ -50,7 +51,7 @@ __host__ __device__ inline SmemMap smem_map(int nt, int stages) {
   m.inv = m.xch + 16 * kBM * 4;                                    // 16 columns x 128 rows
   m.qsum = m.inv + kNtMax * 4;
   m.qkey = m.qsum + 4 * 16 * 4;
-  m.total = m.qkey + 4 * 16 * 8;
+  m.total = m.qkey + 4 * 16 * 8 + (kMaxContrib + 4) * 4;
   return m;
 }
 
@@ -68,27 +69,25 @@ int gemm_stages_for(int nt, size_t small_budget) {
 }
 
 // Work range of CTA c: [c W / G, (c+1) W / G) over tile-major (tile, k-block) items.
-__device__ __forceinline__ long long work_start(int c, long long W, int G) {
-  return static_cast<long long>(c) * W / G;
-}
+// (W * G < 2^31 for every shape here, so 32-bit arithmetic is exact.)
+__device__ __forceinline__ int work_start(int c, int W, int G) { return static_cast<int>((static_cast<unsigned>(c) * W) / G); }
 // CTAs whose ranges may intersect tile t (work [t kb, (t+1) kb)): c_lo..c_hi.
-__device__ __forceinline__ void tile_cta_span(int t, int kb, long long W, int G, int& c_lo, int& c_hi) {
-  const long long x = static_cast<long long>(t) * kb, y = x + kb;
+__device__ __forceinline__ void tile_cta_span(int t, int kb, int W, int G, int& c_lo, int& c_hi) {
+  const unsigned x = static_cast<unsigned>(t) * kb, y = x + kb;
   c_lo = static_cast<int>(((x + 1) * G + W - 1) / W) - 1;   // first c with end(c) > x
   c_hi = static_cast<int>((y * G + W - 1) / W) - 1;         // last c with start(c) < y
   c_lo = c_lo < 0 ? 0 : c_lo;
   c_hi = c_hi > G - 1 ? G - 1 : c_hi;
 }
-__device__ __forceinline__ bool cta_touches_tile(int c, int t, int kb, long long W, int G) {
-  const long long x = static_cast<long long>(t) * kb, y = x + kb;
-  const long long s = work_start(c, W, G), e = work_start(c + 1, W, G);
+__device__ __forceinline__ bool cta_touches_tile(int c, int t, int kb, int W, int G) {
+  const int x = t * kb, y = x + kb;
+  const int s = work_start(c, W, G), e = work_start(c + 1, W, G);
   return (s > x ? s : x) < (e < y ? e : y);
 }
 // Partial slot of CTA c for tile t: slot 2c for the tile its range starts in, else 2c+1.
-__device__ __forceinline__ int partial_slot(int c, int t, int kb, long long W, int G) {
+__device__ __forceinline__ int partial_slot(int c, int t, int kb, int W, int G) {
   return (work_start(c, W, G) / kb == t) ? 2 * c : 2 * c + 1;
 }
-
 template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
@@ -99,8 +98,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const GemmGroup& grp = a.groups[gi];
   const int b_row0 = grp.b_row0;
   const int kb = a.kblocks;
-  const long long W = static_cast<long long>(a.n_tiles) * kb;
-  const long long w0 = work_start(cta, W, G), w1 = work_start(cta + 1, W, G);
+  const int W = a.n_tiles * kb;
+  const int w0 = work_start(cta, W, G), w1 = work_start(cta + 1, W, G);
   if (w0 >= w1) return;   // no work (more CTAs than work items)
   const int nwork = static_cast<int>(w1 - w0);
   const int t_first = static_cast<int>(w0 / kb), t_last = static_cast<int>((w1 - 1) / kb);
@@ -121,6 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* inv = reinterpret_cast<float*>(smem + sm.inv);
   float* qsum = reinterpret_cast<float*>(smem + sm.qsum);
   unsigned long long* qkey = reinterpret_cast<unsigned long long*>(smem + sm.qkey);
+  volatile int* s_contrib = reinterpret_cast<volatile int*>(smem + sm.qkey + 4 * 16 * 8);   // [0] count, [1..] slots
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int stages = a.stages;
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
-      auto load_a = [&](long long w, int st) {
+      auto load_a = [&](int w, int st) {
         uint8_t* dst = sA + static_cast<size_t>(st) * kABytes;
         if (grp.a_packed) {   // packed weights: the work item's 16 KB box is contiguous
           const uint8_t* src = grp.a_packed + static_cast<size_t>(w) * kABytes;
@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           else tma_load_2d(dst, mapA, &full[st], kx, lt * kBM);
         }
       };
-      auto load_b = [&](long long w, int st) {
+      auto load_b = [&](int w, int st) {
         tma_load_2d(sB + static_cast<size_t>(st) * b_bytes, &tmB, &full[st], static_cast<int>(w % kb) * kBK,
                     b_row0);
       };
@@ -233,8 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = idesc_bf16_f32(kBM, a.nt);
       int seg = 0;
       for (int i = 0; i < nwork; ++i) {
-        const long long w = w0 + i;
-        const int k = static_cast<int>(w % kb);
+        const int w = w0 + i;
+        const int k = w % kb;
         const bool seg_first = (i == 0) || (k == 0);
         const bool seg_last = (i == nwork - 1) || (k == kb - 1);
         const int buf = seg & 1;
@@ -405,10 +405,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (sflag[1]) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + static_cast<uint32_t>(buf) * cols + (static_cast<uint32_t>(wq * 32) << 16);
-      int c_lo, c_hi;
-      tile_cta_span(t, kb, W, G, c_lo, c_hi);
-      int parts = 0;
-      for (int c = c_lo; c <= c_hi; ++c) parts += cta_touches_tile(c, t, kb, W, G) ? 1 : 0;
+      // the tile's contributing CTAs, in k order (= CTA order), listed once
+      if (ep == 0) {
+        int c_lo, c_hi;
+        tile_cta_span(t, kb, W, G, c_lo, c_hi);
+        int cnt = 0;
+        for (int c = c_lo; c <= c_hi; ++c) {
+          if (!cta_touches_tile(c, t, kb, W, G)) continue;
+          if (cnt < kMaxContrib) s_contrib[1 + cnt] = partial_slot(c, t, kb, W, G);
+          ++cnt;
+        }
+        s_contrib[0] = cnt;
+      }
+      named_bar_sync(1, 128);
+      const int parts = s_contrib[0];
       if (parts == 1) {   // the whole tile is in this CTA's range
         for (int c0 = 0; c0 < n; c0 += 16) {
           float v[16];
@@ -418,14 +428,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(&tfree[buf]);
       } else {
+        // partial tiles: [slot][row][nt] fp32, a thread's 16 columns are 64 contiguous bytes
         float* gpart = a.partial + static_cast<size_t>(gi) * 2 * G * a.nt * kBM;
-        float* part = gpart + static_cast<size_t>(partial_slot(cta, t, kb, W, G)) * a.nt * kBM;
+        float* part = gpart + static_cast<size_t>(partial_slot(cta, t, kb, W, G)) * a.nt * kBM +
+                      static_cast<size_t>(r) * a.nt;
         for (int c0 = 0; c0 < n; c0 += 16) {
           float v[16];
           tmem_ld16(taddr + static_cast<uint32_t>(c0), v);
+          float4* dst = reinterpret_cast<float4*>(part + c0);
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (c0 + j < n) __stcg(part + static_cast<size_t>(c0 + j) * kBM + r, v[j]);
+          for (int q4 = 0; q4 < 4; ++q4) __stcg(dst + q4, make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]));
         }
         tc_fence_before();
         mbar_arrive(&tfree[buf]);
@@ -436,19 +448,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_sync(1, 128);
         if (sflag[0]) {   // last of the tile's CTAs: sum the partial tiles in k order
           __threadfence();
+          const bool listed = parts <= kMaxContrib;   // else walk the contributors in CTA order
+          int c_lo = 0, c_hi = -1;
+          if (!listed) tile_cta_span(t, kb, W, G, c_lo, c_hi);
           for (int c0 = 0; c0 < n; c0 += 16) {
             float v[16];
+            int cnext = c_lo;
+            for (int i = 0; i < parts; ++i) {
+              int slot;
+              if (listed) {
+                slot = s_contrib[1 + i];
+              } else {
+                while (!cta_touches_tile(cnext, t, kb, W, G)) ++cnext;
+                slot = partial_slot(cnext, t, kb, W, G);
+                ++cnext;
+              }
+              const float4* p = reinterpret_cast<const float4*>(gpart + static_cast<size_t>(slot) * a.nt * kBM +
+                                                                 static_cast<size_t>(r) * a.nt + c0);
+              float4 q[4];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = 0.0f;
-            bool first = true;
-            for (int c = c_lo; c <= c_hi; ++c) {
-              if (!cta_touches_tile(c, t, kb, W, G)) continue;
-              const float* p = gpart + static_cast<size_t>(partial_slot(c, t, kb, W, G)) * a.nt * kBM +
-                               static_cast<size_t>(c0) * kBM + r;
+              for (int q4 = 0; q4 < 4; ++q4) q[q4] = __ldcg(p + q4);
+              const float* qf = reinterpret_cast<const float*>(q);
 #pragma unroll
-              for (int j = 0; j < 16; ++j)
-                if (c0 + j < n) v[j] = first ? __ldcg(p + j * kBM) : __fadd_rn(v[j], __ldcg(p + j * kBM));
-              first = false;
+              for (int j = 0; j < 16; ++j) v[j] = (i == 0) ? qf[j] : __fadd_rn(v[j], qf[j]);
             }
             epilogue_chunk(src, lt, c0, v);
           }
