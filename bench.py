@@ -108,6 +108,22 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def _gemm_traffic_ratio():
+    """DRAM bytes per algorithmic byte of gemm_tc_kernel from the committed ncu summary, if
+    that summary was taken on the current gemm.cu (else None: the counters are stale)."""
+    import hashlib
+    prof = os.path.join(ROOT, "profiles", "gemm_tc_kernel_grouped_l4.md")
+    src = os.path.join(ROOT, "lossless_depth_adaptive_gb300", "csrc", "gemm.cu")
+    try:
+        text = open(prof).read()
+        ratio = float(text.split("dram_over_algorithmic:")[1].split()[0])
+        sha = text.split("gemm_cu_sha256_16:")[1].split()[0]
+    except (OSError, IndexError, ValueError):
+        return None
+    with open(src, "rb") as f:
+        return ratio if hashlib.sha256(f.read()).hexdigest()[:16] == sha else None
+
+
 def _workload(args):
     return di.workload(args.workload, **({"max_new": args.tokens} if args.tokens else {}))
 
@@ -208,6 +224,8 @@ def run_gpu(args):
     dec.close()
     hbm, bf16, src = _peaks()
     achieved = inst["gemm_bytes"] / (inst["ms_gemm"] / 1000.0) / 1e9 if inst["ms_gemm"] > 0 else None
+    ratio = _gemm_traffic_ratio()
+    bytes_per_launch = inst["gemm_bytes"] / max(1, inst["gemm_launches"])
     commits = stats["commits"]
     algo_bytes = stats["weight_bytes"] + stats["kv_bytes"]
     step_roof = {"algorithmic_bytes_per_step": int(algo_bytes / args.steps),
@@ -235,8 +253,10 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "kernel": "gemm_tc_kernel (all linear layers, one instrumented request)",
                      "achieved": round(achieved, 1) if achieved else None, "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4) if achieved else None, "peak_source": src,
-                     "traffic": None, "launches": inst["gemm_launches"],
-                     "bytes_per_launch": int(inst["gemm_bytes"] / max(1, inst["gemm_launches"])),
+                     "traffic": int(ratio * bytes_per_launch) if ratio else None,
+                     "traffic_source": "ncu dram bytes / algorithmic bytes (profiles/gemm_tc_kernel_grouped_l4.md)"
+                                       " x this run's algorithmic bytes per launch" if ratio else None,
+                     "launches": inst["gemm_launches"], "bytes_per_launch": int(bytes_per_launch),
                      "ms_per_launch": inst["ms_gemm"] / max(1, inst["gemm_launches"])},
         "e2e": e2e,
         "gpu_launches": launches,
