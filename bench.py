@@ -108,6 +108,30 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def rank_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_over_ranks(x, op, world, device):
+    """max or sum of a per-rank float over the process group (identity at world 1)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def replica_throughput(tokens_per_rank, seconds_per_rank, world, device):
+    """Whole-job committed tokens/s of independent replicas: all ranks' tokens over the
+    slowest rank's time."""
+    return (reduce_over_ranks(tokens_per_rank, "sum", world, device) /
+            reduce_over_ranks(seconds_per_rank, "max", world, device))
+
+
 def _gemm_traffic_ratio():
     """DRAM bytes per algorithmic byte of gemm_tc_kernel from the committed ncu summary, if
     that summary was taken on the current gemm.cu (else None: the counters are stale)."""
@@ -150,27 +174,14 @@ def run_gpu(args):
     import ctypes as C
     out_host = (C.c_int32 * T)()
 
+    dev = torch.device("cuda", local)
+
     def barrier():
         torch.cuda.synchronize()
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
+        rank_barrier(world)
 
     def max_over_ranks(x):
-        if world == 1:
-            return x
-        import torch.distributed as dist
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
-    def sum_over_ranks(x):
-        if world == 1:
-            return x
-        import torch.distributed as dist
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.SUM)
-        return float(t.item())
+        return reduce_over_ranks(x, "max", world, dev)
 
     # warm-up requests
     for _ in range(args.warmup):
@@ -196,9 +207,8 @@ def run_gpu(args):
     barrier()
     stats = dec.stats()
     launches = stats["kernel_launches"]
+    value = replica_throughput(args.steps * T, ms / 1000.0, world, dev)
     ms = max_over_ranks(ms)
-    total_tokens = sum_over_ranks(args.steps * T)
-    value = total_tokens / (ms / 1000.0)
     ms_per_step = ms / args.steps
     # ---- end to end through the C ABI with host buffers (e2e) ----
     dec.reset_stats()
@@ -208,9 +218,9 @@ def run_gpu(args):
         dec.prefill(0, prompt)               # host prompt -> device inside
         dec.generate(out=out_host)           # tokens -> host inside
     barrier()
-    e2e_s = max_over_ranks(time.perf_counter() - t0)
+    e2e_value = replica_throughput(args.steps * T, time.perf_counter() - t0, world, dev)
     st_e2e = dec.stats()
-    e2e = {"value": sum_over_ranks(args.steps * T) / e2e_s, "unit": "tokens/s",
+    e2e = {"value": e2e_value, "unit": "tokens/s",
            "h2d_bytes_per_step": int(st_e2e["h2d_bytes"] / args.steps),
            "d2h_bytes_per_step": int(st_e2e["d2h_bytes"] / args.steps)}
     # ---- one instrumented request: per-GEMM events and phase split ----
@@ -230,7 +240,7 @@ def run_gpu(args):
     algo_bytes = stats["weight_bytes"] + stats["kv_bytes"]
     step_roof = {"algorithmic_bytes_per_step": int(algo_bytes / args.steps),
                  "roofline_ms_per_step": algo_bytes / args.steps / (hbm * 1e9) * 1e3,
-                 "frac": (algo_bytes / (hbm * 1e9)) / (ms / 1e3 / max(1, world)) if ms > 0 else None}
+                 "frac": (algo_bytes / (hbm * 1e9)) / (ms / 1e3) if ms > 0 else None}
     layers = {"depth_charge_per_token": stats["depth_charge"] / commits,
               "layer_passes_per_token": stats["layer_passes"] / commits,
               "node_layers_per_token": stats["node_layers"] / commits,

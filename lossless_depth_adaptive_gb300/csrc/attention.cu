@@ -22,34 +22,26 @@ namespace dex {
 constexpr int kAttnThreads = 128;
 constexpr int kGroupPos = 128;
 
-// q . k for one key row.  The 16-byte chunks of the row are visited starting at chunk
-// `rot` (the lane's index), so the 32 lanes reading 32 different key rows of an
-// unpadded shared-memory tile hit distinct banks; four independent partial sums shorten
-// the dependency chain.  The visiting order and the summation tree are functions of the
-// key's absolute position only (lane = position mod 32), so a key's score does not depend
-// on where the key is stored or which batch it is computed in.
+// q . k for one fp32 key row.  The 16-byte chunks of the row are visited starting at
+// chunk `rot` (the lane's index), so the lanes of a quarter-warp reading different key
+// rows of an unpadded shared-memory tile hit distinct banks; four independent partial
+// sums shorten the dependency chain.  The visiting order and the summation tree are
+// functions of the key's absolute position only (lane = position mod 32), so a key's
+// score does not depend on where the key is stored or which batch it is computed in.
 template <int HD>
-__device__ __forceinline__ float dot_q_row(const float* q, const __nv_bfloat16* krow, int rot) {
-  constexpr int NC = HD / 8;
+__device__ __forceinline__ float dot_q_row(const float* q, const float* krow, int rot) {
+  constexpr int NC = HD / 4;
   float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
   for (int i = 0; i < NC; ++i) {
     const int c = (i + rot) & (NC - 1);
-    const uint4 raw = *reinterpret_cast<const uint4*>(krow + c * 8);
-    const float4 qa = *reinterpret_cast<const float4*>(q + c * 8);
-    const float4 qb = *reinterpret_cast<const float4*>(q + c * 8 + 4);
-    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
-    const float2 f0 = __bfloat1622float2(h2[0]), f1 = __bfloat1622float2(h2[1]);
-    const float2 f2 = __bfloat1622float2(h2[2]), f3 = __bfloat1622float2(h2[3]);
+    const float4 k4 = *reinterpret_cast<const float4*>(krow + c * 4);
+    const float4 q4 = *reinterpret_cast<const float4*>(q + c * 4);
     float& a = s[i & 3];
-    a = fmaf(qa.x, f0.x, a);
-    a = fmaf(qa.y, f0.y, a);
-    a = fmaf(qa.z, f1.x, a);
-    a = fmaf(qa.w, f1.y, a);
-    a = fmaf(qb.x, f2.x, a);
-    a = fmaf(qb.y, f2.y, a);
-    a = fmaf(qb.z, f3.x, a);
-    a = fmaf(qb.w, f3.y, a);
+    a = fmaf(q4.x, k4.x, a);
+    a = fmaf(q4.y, k4.y, a);
+    a = fmaf(q4.z, k4.z, a);
+    a = fmaf(q4.w, k4.w, a);
   }
   return __fadd_rn(__fadd_rn(s[0], s[1]), __fadd_rn(s[2], s[3]));
 }
@@ -61,8 +53,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
   constexpr int DPL = HD / 32;        // output dims per lane
   constexpr int PS = HD + 2;          // partial record: acc[HD], m, l
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  __nv_bfloat16* sK = reinterpret_cast<__nv_bfloat16*>(smem_raw);   // [128][HD], unpadded
-  __nv_bfloat16* sV = sK + kGroupPos * HD;
+  float* sK = reinterpret_cast<float*>(smem_raw);   // [128][HD] fp32, unpadded
+  float* sV = sK + kGroupPos * HD;
   float* sQ = reinterpret_cast<float*>(sV + kGroupPos * HD);         // [kQBatch][HD]
   float* sP = sQ + kQBatch * HD;                                     // [kQBatch][4 warps][PS]
   __shared__ int s_last;
@@ -91,7 +83,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
           ((((static_cast<size_t>(item.seq) * a.L + item.layer) * 2 + 0) * a.KVH + kvh) * a.max_ctx + g0) * HD;
       const size_t vbase =
           ((((static_cast<size_t>(item.seq) * a.L + item.layer) * 2 + 1) * a.KVH + kvh) * a.max_ctx + g0) * HD;
-      const uint32_t bytes = static_cast<uint32_t>(cmax - g0) * HD * 2;
+      const uint32_t bytes = static_cast<uint32_t>(cmax - g0) * HD * 4;
       mbar_arrive_expect_tx(&s_bar, 2 * bytes);
       bulk_load_1d(sK, a.kv_commit + kbase, bytes, &s_bar);
       bulk_load_1d(sV, a.kv_commit + vbase, bytes, &s_bar);
@@ -118,7 +110,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
       const int qi = qb + j;
       const DevNode nd = a.nodes[item.row_begin + qi / G];
       const int pos = nd.pos, c_end = nd.c_end;
-      auto key_row = [&](int kk, int kv) -> const __nv_bfloat16* {
+      auto key_row = [&](int kk, int kv) -> const float* {
         if (kk < c_end) return (kv ? sV : sK) + (kk - g0) * HD;
         int t = kk - c_end;
         if (t >= nd.n_tail) {   // cannot happen for a well-formed plan; never read out of bounds
@@ -141,20 +133,17 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
         for (int jj = 0; jj < 32; ++jj) {
           if (ks + jj <= pos) {   // uniform across the warp
             const float pk = __shfl_sync(0xffffffffu, p, jj);
-            const __nv_bfloat16* vr = key_row(ks + jj, 1);
+            const float* vr = key_row(ks + jj, 1);
             if constexpr (DPL == 4) {
-              const uint2 raw = *reinterpret_cast<const uint2*>(vr + lane * 4);
-              const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
-              const float2 f0 = __bfloat1622float2(h2[0]), f1 = __bfloat1622float2(h2[1]);
-              acc[0] = fmaf(pk, f0.x, acc[0]);
-              acc[1] = fmaf(pk, f0.y, acc[1]);
-              acc[2] = fmaf(pk, f1.x, acc[2]);
-              acc[3] = fmaf(pk, f1.y, acc[3]);
+              const float4 f = *reinterpret_cast<const float4*>(vr + lane * 4);
+              acc[0] = fmaf(pk, f.x, acc[0]);
+              acc[1] = fmaf(pk, f.y, acc[1]);
+              acc[2] = fmaf(pk, f.z, acc[2]);
+              acc[3] = fmaf(pk, f.w, acc[3]);
             } else {
-              const __nv_bfloat162 h2 = *reinterpret_cast<const __nv_bfloat162*>(vr + lane * 2);
-              const float2 f0 = __bfloat1622float2(h2);
-              acc[0] = fmaf(pk, f0.x, acc[0]);
-              acc[1] = fmaf(pk, f0.y, acc[1]);
+              const float2 f = *reinterpret_cast<const float2*>(vr + lane * 2);
+              acc[0] = fmaf(pk, f.x, acc[0]);
+              acc[1] = fmaf(pk, f.y, acc[1]);
             }
           }
         }
@@ -228,21 +217,24 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
       for (int i = 0; i < DPL; ++i) O[i] = fmaf(w, __ldcg(base + gg * PS + lane * DPL + i), O[i]);
     }
     const float invl = 1.0f / Lsum;
+    const size_t lo = static_cast<size_t>(a.plane_rows) * H * HD;
 #pragma unroll
-    for (int i = 0; i < DPL; ++i)
-      a.out[static_cast<size_t>(row) * H * HD + qh * HD + lane * DPL + i] = __float2bfloat16_rn(O[i] * invl);
+    for (int i = 0; i < DPL; ++i) {
+      const size_t o = static_cast<size_t>(row) * H * HD + qh * HD + lane * DPL + i;
+      store_pair(a.out + o, a.out + lo + o, O[i] * invl);
+    }
   }
   if (tid == 0) a.counters[item.counter * a.KVH + kvh] = 0;
 }
 
 static size_t attn_smem_bytes(int hd) {
-  return static_cast<size_t>(2) * kGroupPos * hd * 2 + kQBatch * hd * 4 + kQBatch * 4 * (hd + 2) * 4;
+  return static_cast<size_t>(2) * kGroupPos * hd * 4 + kQBatch * hd * 4 + kQBatch * 4 * (hd + 2) * 4;
 }
 
 cudaError_t launch_attention(const AttnArgs& a, int n_items, int max_groups_launch, cudaStream_t st, bool pdl) {
   if (n_items <= 0) return cudaSuccess;
   if (!a.nodes || !a.items || !a.tails || !a.q || !a.kv_commit || !a.kv_pool || !a.out || !a.part || !a.counters ||
-      !a.err || max_groups_launch < 1 || max_groups_launch > a.max_groups || max_groups_launch > 32)
+      !a.err || a.plane_rows < 1 || max_groups_launch < 1 || max_groups_launch > a.max_groups || max_groups_launch > 32)
     return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(max_groups_launch), static_cast<unsigned>(a.KVH),

@@ -207,6 +207,17 @@ __device__ __forceinline__ unsigned long long argmax_key(float score, uint32_t i
 
 __device__ __forceinline__ float bf16_to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 
+// Activations enter the tensor cores as a pair of bf16 operands, x ~= hi + lo:
+// hi = bf16(x), lo = bf16(x - hi).  x - hi is exact in fp32, so the pair carries x to a
+// relative 2^-17 (the MMA sums W*hi + W*lo into one fp32 accumulator).  Plain bf16
+// activations (2^-9) are amplified through 30+ random-weight layers into logits errors
+// well above the 5e-2 parity bound; the pair keeps them near fp32 arithmetic.
+__device__ __forceinline__ void store_pair(__nv_bfloat16* hi, __nv_bfloat16* lo, float x) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(x);
+  *hi = h;
+  *lo = __float2bfloat16_rn(__fsub_rn(x, __bfloat162float(h)));
+}
+
 // ---- Philox4x32-10 (Salmon et al., SC'11) for the Gumbel rows -----------------------------------------
 struct U4 { uint32_t x, y, z, w; };
 __device__ __forceinline__ U4 philox4x32_10(U4 c, uint32_t k0, uint32_t k1) {

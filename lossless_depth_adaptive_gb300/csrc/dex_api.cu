@@ -85,8 +85,9 @@ struct dex_handle {
   int rows_cap = 0, n_slots = 0, max_groups = 0, hrows = 0;
   // device buffers
   std::vector<void*> allocs;
-  bf16 *kv_commit = nullptr, *kv_pool = nullptr, *hb = nullptr, *exit_hb = nullptr, *attn_out = nullptr,
-       *act = nullptr;
+  float *kv_commit = nullptr, *kv_pool = nullptr;   // fp32 KV
+  // activation buffers: two planes of rows_cap rows each, hi then lo (x ~= hi + lo)
+  bf16 *hb = nullptr, *exit_hb = nullptr, *attn_out = nullptr, *act = nullptr;
   float *hidden = nullptr, *ssq = nullptr, *exit_ssq = nullptr, *q = nullptr, *partial = nullptr,
         *attn_part = nullptr, *logits_dbg = nullptr;
   int32_t *counters = nullptr, *attn_counters = nullptr, *err = nullptr;
@@ -248,6 +249,7 @@ dex::GemmArgs base_args(dex_handle* h) {
   a.partial = h->partial;
   a.counters = h->counters;
   a.evict_first = 1;
+  a.plane_rows = h->rows_cap;
   return a;
 }
 
@@ -332,7 +334,7 @@ int run_layers(dex_handle* h, const Uploaded& u, const std::vector<Batch>& batch
     a.kv_pool = h->kv_pool;
     a.rope = h->rope;
     int rc = gemm(h, dex::EPI_QKV, h->tm_q[l_first], h->tm_k[l_first], h->tm_v[l_first], h->tm_hb, a, nmax,
-                  static_cast<int64_t>(qd + 2 * kvd) * d * 2, d * 2 + qd * 4 + 2 * kvd * 2);
+                  static_cast<int64_t>(qd + 2 * kvd) * d * 2, d * 4 + qd * 4 + 2 * kvd * 4);
     if (rc) return rc;
     // lattice attention over every batch of the slot
     dex::AttnArgs at = {};
@@ -353,6 +355,7 @@ int run_layers(dex_handle* h, const Uploaded& u, const std::vector<Batch>& batch
     at.max_ctx = h->cfg.max_ctx;
     at.n_slots = h->n_slots;
     at.max_groups = h->max_groups;
+    at.plane_rows = h->rows_cap;
     at.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(h->hd)));
     cudaError_t ce = dex::launch_attention(at, sl.n_items, sl.max_groups, h->st, true);
     if (ce != cudaSuccess) return cuda_fail(h, ce);
@@ -367,7 +370,7 @@ int run_layers(dex_handle* h, const Uploaded& u, const std::vector<Batch>& batch
     a.hb_out = h->hb;
     a.ssq_out = h->ssq;
     rc = gemm(h, dex::EPI_RESID, h->tm_o[l_first], h->tm_o[l_first], h->tm_o[l_first], h->tm_attn, a, nmax,
-              static_cast<int64_t>(qd) * d * 2, qd * 2 + d * 8 + d * 2);
+              static_cast<int64_t>(qd) * d * 2, qd * 4 + d * 8 + d * 4);
     if (rc) return rc;
     // gate/up + SwiGLU
     a = base_args(h);
@@ -378,7 +381,7 @@ int run_layers(dex_handle* h, const Uploaded& u, const std::vector<Batch>& batch
     a.ssq_in = h->ssq;
     a.act_out = h->act;
     rc = gemm(h, dex::EPI_SWIGLU, h->tm_g[l_first], h->tm_u[l_first], h->tm_u[l_first], h->tm_hb, a, nmax,
-              static_cast<int64_t>(2) * h->dff * d * 2, d * 2 + h->dff * 2);
+              static_cast<int64_t>(2) * h->dff * d * 2, d * 4 + h->dff * 4);
     if (rc) return rc;
     // down + residual (+ exit-head input at the stage boundary)
     a = base_args(h);
@@ -393,7 +396,7 @@ int run_layers(dex_handle* h, const Uploaded& u, const std::vector<Batch>& batch
     a.g_final = h->final_norm;
     a.exit_ssq = h->exit_ssq;
     rc = gemm(h, dex::EPI_RESID, h->tm_d[l_first], h->tm_d[l_first], h->tm_d[l_first], h->tm_act, a, nmax,
-              static_cast<int64_t>(h->dff) * d * 2, h->dff * 2 + d * 8 + d * 4);
+              static_cast<int64_t>(h->dff) * d * 2, h->dff * 4 + d * 8 + d * 8);
     if (rc) return rc;
   }
   return DEX_OK;
@@ -494,7 +497,7 @@ int run_round(dex_handle* h, dex::Lattice* lat, std::vector<dex_copy_job>* pendi
     ca.kv_pool = h->kv_pool;
     ca.L = h->L;
     ca.KVH = h->KVH;
-    ca.hd = h->hd;
+    ca.row_bytes = h->hd * 4;
     ca.max_ctx = h->cfg.max_ctx;
     ca.n_slots = h->n_slots;
     cudaError_t ce = dex::launch_collapse(ca, h->st, false);
@@ -510,6 +513,7 @@ int run_round(dex_handle* h, dex::Lattice* lat, std::vector<dex_copy_job>* pendi
   aa.attn_norm = h->d_attn_norms;
   aa.hidden = h->hidden;
   aa.hb = h->hb;
+  aa.plane_rows = h->rows_cap;
   aa.ssq = h->ssq;
   aa.best = h->best;
   cudaError_t ce = dex::launch_assemble(aa, h->st, false);
@@ -539,7 +543,7 @@ int run_round(dex_handle* h, dex::Lattice* lat, std::vector<dex_copy_job>* pendi
       a.groups[0].b_row0 = r0;
       a.groups[0].n = std::min(256, n - r0);
       rc = gemm(h, dex::EPI_EXIT, h->tm_lm, h->tm_lm, h->tm_lm, h->tm_exit, a, a.groups[0].n,
-                static_cast<int64_t>(h->V) * h->d * 2, static_cast<int64_t>(h->d) * 2);
+                static_cast<int64_t>(h->V) * h->d * 2, static_cast<int64_t>(h->d) * 4);
     }
     if (rc) return rc;
   }
@@ -567,7 +571,7 @@ int run_round(dex_handle* h, dex::Lattice* lat, std::vector<dex_copy_job>* pendi
   const int64_t layer_w = (static_cast<int64_t>(h->H + 2 * h->KVH) * h->hd * h->d + static_cast<int64_t>(h->H) *
                            h->hd * h->d + 3ll * h->dff * h->d) * 2;
   h->stats.weight_bytes += layer_w * X[max_stage] + static_cast<int64_t>(h->V) * h->d * 2;
-  const int64_t kv_row = 2ll * h->KVH * h->hd * 2;
+  const int64_t kv_row = 2ll * h->KVH * h->hd * 4;
   for (const Batch& b : batches) {
     const int nl = b.l1 - b.l0;
     for (const auto& it : b.items) h->stats.kv_bytes += kv_row * nl * it.max_cend;
@@ -708,13 +712,13 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
   const size_t B = cfg->batch, L = h->L, KVH = h->KVH, hd = h->hd, ctx = cfg->max_ctx, R = h->rows_cap;
   const int qd = h->H * h->hd, kvd = h->KVH * h->hd;
   int rc = 0;
-  rc |= dalloc(h, &h->kv_commit, B * L * 2 * KVH * ctx * hd * 2);
-  rc |= dalloc(h, &h->kv_pool, B * h->n_slots * L * 2 * KVH * hd * 2);
+  rc |= dalloc(h, &h->kv_commit, B * L * 2 * KVH * ctx * hd * 4);
+  rc |= dalloc(h, &h->kv_pool, B * h->n_slots * L * 2 * KVH * hd * 4);
   rc |= dalloc(h, &h->hidden, static_cast<size_t>(h->hrows) * h->d * 4);
-  rc |= dalloc(h, &h->hb, R * h->d * 2);
-  rc |= dalloc(h, &h->exit_hb, R * h->d * 2);
-  rc |= dalloc(h, &h->attn_out, R * qd * 2);
-  rc |= dalloc(h, &h->act, R * h->dff * 2);
+  rc |= dalloc(h, &h->hb, 2 * R * h->d * 2);
+  rc |= dalloc(h, &h->exit_hb, 2 * R * h->d * 2);
+  rc |= dalloc(h, &h->attn_out, 2 * R * qd * 2);
+  rc |= dalloc(h, &h->act, 2 * R * h->dff * 2);
   rc |= dalloc(h, &h->ssq, R * (h->d / 128) * 4);
   rc |= dalloc(h, &h->exit_ssq, R * (h->d / 128) * 4);
   rc |= dalloc(h, &h->q, R * qd * 4);
@@ -743,13 +747,13 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
   cudaMemsetAsync(h->counters, 0, ntiles_max * 4 * std::max(1, h->N), h->st);
   cudaMemsetAsync(h->attn_counters, 0, (static_cast<size_t>(B) * h->N * KVH + 256 * KVH) * 4, h->st);
   cudaMemsetAsync(h->err, 0, 16, h->st);
-  cudaMemsetAsync(h->kv_commit, 0, B * L * 2 * KVH * ctx * hd * 2, h->st);
-  cudaMemsetAsync(h->kv_pool, 0, B * h->n_slots * L * 2 * KVH * hd * 2, h->st);
+  cudaMemsetAsync(h->kv_commit, 0, B * L * 2 * KVH * ctx * hd * 4, h->st);
+  cudaMemsetAsync(h->kv_pool, 0, B * h->n_slots * L * 2 * KVH * hd * 4, h->st);
   cudaMemsetAsync(h->hidden, 0, static_cast<size_t>(h->hrows) * h->d * 4, h->st);
-  cudaMemsetAsync(h->hb, 0, R * h->d * 2, h->st);
-  cudaMemsetAsync(h->exit_hb, 0, R * h->d * 2, h->st);
-  cudaMemsetAsync(h->attn_out, 0, R * qd * 2, h->st);
-  cudaMemsetAsync(h->act, 0, R * h->dff * 2, h->st);
+  cudaMemsetAsync(h->hb, 0, 2 * R * h->d * 2, h->st);
+  cudaMemsetAsync(h->exit_hb, 0, 2 * R * h->d * 2, h->st);
+  cudaMemsetAsync(h->attn_out, 0, 2 * R * qd * 2, h->st);
+  cudaMemsetAsync(h->act, 0, 2 * R * h->dff * 2, h->st);
   // RoPE table (rotate-half, frequencies theta^(-2i/hd)), computed in double
   {
     std::vector<float2> tab(ctx * (hd / 2));
@@ -766,7 +770,8 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
     if (cudaMemcpy(h->d_attn_norms, norms.data(), L * sizeof(void*), cudaMemcpyHostToDevice) != cudaSuccess)
       return DEX_ECUDA;
   }
-  // tensor maps: weights (box 128 rows; gate/up 64 rows) and activation buffers (box nt rows)
+  // tensor maps: weights (box 128 rows; gate/up 64 rows) and activation buffers over both
+  // planes (2 R rows, box nt rows; the lo box is read plane_rows = R rows below the hi box)
   h->tm_q.resize(L);
   h->tm_k.resize(L);
   h->tm_v.resize(L);
@@ -786,10 +791,10 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
   }
   rc |= encode_2d(&h->tm_lm, h->lm_head, h->V, h->d, 128);
   for (int i = 1; i <= 16; ++i) {
-    rc |= encode_2d(&h->tm_hb[i], h->hb, R, h->d, 16 * i);
-    rc |= encode_2d(&h->tm_attn[i], h->attn_out, R, qd, 16 * i);
-    rc |= encode_2d(&h->tm_act[i], h->act, R, h->dff, 16 * i);
-    rc |= encode_2d(&h->tm_exit[i], h->exit_hb, R, h->d, 16 * i);
+    rc |= encode_2d(&h->tm_hb[i], h->hb, 2 * R, h->d, 16 * i);
+    rc |= encode_2d(&h->tm_attn[i], h->attn_out, 2 * R, qd, 16 * i);
+    rc |= encode_2d(&h->tm_act[i], h->act, 2 * R, h->dff, 16 * i);
+    rc |= encode_2d(&h->tm_exit[i], h->exit_hb, 2 * R, h->d, 16 * i);
   }
   if (rc) return DEX_EINVAL;
   // pack every GEMM weight once: contiguous, pre-swizzled 16 KB boxes in streaming order
@@ -894,6 +899,7 @@ int dex_prefill(dex_handle* h, int32_t seq, const int32_t* tokens, int32_t n_tok
     aa.attn_norm = h->d_attn_norms;
     aa.hidden = h->hidden;
     aa.hb = h->hb;
+    aa.plane_rows = h->rows_cap;
     aa.ssq = h->ssq;
     aa.best = nullptr;
     cudaError_t ce = dex::launch_assemble(aa, h->st, false);
@@ -1030,7 +1036,7 @@ int dex_exit_head_decs(const void* hidden, int32_t n, int32_t d, const void* fin
   const int n_tiles = (vocab + 127) / 128, kb = (d + 63) / 64;
   const int nt = (n + 15) & ~15;
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
-  const size_t o_hb = 0, o_ssq = o_hb + up(static_cast<size_t>(nt) * d * 2);
+  const size_t o_hb = 0, o_ssq = o_hb + up(static_cast<size_t>(2) * nt * d * 2);   // hi/lo planes of nt rows
   const size_t o_best = o_ssq + up(static_cast<size_t>(n) * (d / 128) * 4);
   const size_t o_nodes = o_best + up(static_cast<size_t>(n) * 8);
   const size_t o_cnt = o_nodes + up(static_cast<size_t>(n) * sizeof(dex::DevNode));
@@ -1046,11 +1052,11 @@ int dex_exit_head_decs(const void* hidden, int32_t n, int32_t d, const void* fin
   int32_t* cnt = reinterpret_cast<int32_t*>(scratch + o_cnt);
   int rc = DEX_OK;
   CUtensorMap tm_w, tm_b;
-  if (encode_2d(&tm_w, lm_head, vocab, d, 128) || encode_2d(&tm_b, hb, nt, d, nt)) rc = DEX_EINVAL;
+  if (encode_2d(&tm_w, lm_head, vocab, d, 128) || encode_2d(&tm_b, hb, 2 * nt, d, nt)) rc = DEX_EINVAL;
   if (!rc) {
-    cudaMemsetAsync(hb, 0, static_cast<size_t>(nt) * d * 2, st);
+    cudaMemsetAsync(hb, 0, static_cast<size_t>(2) * nt * d * 2, st);
     cudaMemsetAsync(cnt, 0, o_part - o_cnt, st);   // arrival counters and the error flag
-    if (dex::launch_exit_prep(static_cast<const bf16*>(hidden), n, d, static_cast<const bf16*>(final_norm), hb, ssq,
+    if (dex::launch_exit_prep(static_cast<const bf16*>(hidden), n, d, static_cast<const bf16*>(final_norm), hb, nt, ssq,
                               best, st) != cudaSuccess)
       rc = DEX_ECUDA;
     exit_nodes_kernel<<<(n + 127) / 128, 128, 0, st>>>(nodes, n, dn);
@@ -1061,7 +1067,7 @@ int dex_exit_head_decs(const void* hidden, int32_t n, int32_t d, const void* fin
     a.groups[0].b_row0 = 0;
     a.nt = nt;
     a.kblocks = kb;
-    a.stages = dex::gemm_stages_for(nt);
+    a.stages = dex::gemm_stages_for(nt, 200 * 1024);   // one CTA per SM: a deeper ring
     a.n_tiles = n_tiles;
     a.src_tiles0 = n_tiles;
     a.tmem_cols = pow2_at_least(nt);
@@ -1070,6 +1076,7 @@ int dex_exit_head_decs(const void* hidden, int32_t n, int32_t d, const void* fin
     a.err = reinterpret_cast<int32_t*>(scratch + o_err);
     a.nodes = dn;
     a.evict_first = 1;
+    a.plane_rows = nt;
     a.d = d;
     a.vocab = vocab;
     a.eps = rms_eps;
@@ -1095,11 +1102,11 @@ int dex_kv_collapse(void* committed, const void* pool, const dex_kv_geom* g, con
   dex::CollapseArgs a = {};
   a.jobs = reinterpret_cast<const dex::CopyJob*>(jobs);
   a.n_jobs = n_jobs;
-  a.kv_commit = static_cast<bf16*>(committed);
-  a.kv_pool = static_cast<const bf16*>(pool);
+  a.kv_commit = committed;
+  a.kv_pool = pool;
   a.L = g->n_layers;
   a.KVH = g->n_kv_heads;
-  a.hd = g->head_dim;
+  a.row_bytes = g->head_dim * 2;   // bf16 caches
   a.max_ctx = g->max_ctx;
   a.n_slots = g->n_slots;
   return dex::launch_collapse(a, static_cast<cudaStream_t>(stream), false) == cudaSuccess ? DEX_OK : DEX_ECUDA;
@@ -1154,7 +1161,7 @@ extern "C" int dex_exit_head_decs_noalloc(const void* hidden, int32_t n, int32_t
   const int n_tiles = (vocab + 127) / 128, kb = (d + 63) / 64;
   const int nt = (n + 15) & ~15;
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
-  const size_t o_hb = 0, o_ssq = o_hb + up(static_cast<size_t>(nt) * d * 2);
+  const size_t o_hb = 0, o_ssq = o_hb + up(static_cast<size_t>(2) * nt * d * 2);   // hi/lo planes of nt rows
   const size_t o_best = o_ssq + up(static_cast<size_t>(n) * (d / 128) * 4);
   const size_t o_nodes = o_best + up(static_cast<size_t>(n) * 8);
   const size_t o_cnt = o_nodes + up(static_cast<size_t>(n) * sizeof(dex::DevNode));
@@ -1172,13 +1179,13 @@ extern "C" int dex_exit_head_decs_noalloc(const void* hidden, int32_t n, int32_t
   dex::DevNode* dn = reinterpret_cast<dex::DevNode*>(scratch + o_nodes);
   int32_t* cnt = reinterpret_cast<int32_t*>(scratch + o_cnt);
   CUtensorMap tm_w, tm_b;
-  if (encode_2d(&tm_w, lm_head, vocab, d, 128) || encode_2d(&tm_b, hb, nt, d, nt)) return DEX_EINVAL;
+  if (encode_2d(&tm_w, lm_head, vocab, d, 128) || encode_2d(&tm_b, hb, 2 * nt, d, nt)) return DEX_EINVAL;
   // the array keeps the previous call's contents: clear what the kernels expect at zero
   // (padding rows of the node tile, split-K arrival counters, the stall flag)
-  if (cudaMemsetAsync(hb, 0, static_cast<size_t>(nt) * d * 2, st) != cudaSuccess ||
+  if (cudaMemsetAsync(hb, 0, static_cast<size_t>(2) * nt * d * 2, st) != cudaSuccess ||
       cudaMemsetAsync(cnt, 0, o_part - o_cnt, st) != cudaSuccess)
     return DEX_ECUDA;
-  if (dex::launch_exit_prep(static_cast<const bf16*>(hidden), n, d, static_cast<const bf16*>(final_norm), hb, ssq,
+  if (dex::launch_exit_prep(static_cast<const bf16*>(hidden), n, d, static_cast<const bf16*>(final_norm), hb, nt, ssq,
                             best, st) != cudaSuccess)
     return DEX_ECUDA;
   exit_nodes_kernel<<<(n + 127) / 128, 128, 0, st>>>(nodes, n, dn);
@@ -1190,7 +1197,7 @@ extern "C" int dex_exit_head_decs_noalloc(const void* hidden, int32_t n, int32_t
   a.groups[0].b_row0 = 0;
   a.nt = nt;
   a.kblocks = kb;
-  a.stages = dex::gemm_stages_for(nt);
+  a.stages = dex::gemm_stages_for(nt, 200 * 1024);   // one CTA per SM: a deeper ring
   a.n_tiles = n_tiles;
   a.src_tiles0 = n_tiles;
   a.tmem_cols = pow2_at_least(nt);
@@ -1199,6 +1206,7 @@ extern "C" int dex_exit_head_decs_noalloc(const void* hidden, int32_t n, int32_t
   a.err = reinterpret_cast<int32_t*>(scratch + o_err);
   a.nodes = dn;
   a.evict_first = 1;
+  a.plane_rows = nt;
   a.d = d;
   a.vocab = vocab;
   a.eps = rms_eps;

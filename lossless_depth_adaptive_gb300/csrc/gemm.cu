@@ -8,6 +8,11 @@
 // batch on the N side (16..256 columns), so each weight byte is read from HBM once per
 // round however many nodes the round holds.
 //
+// Activations arrive as hi/lo bf16 pairs (x ~= hi + lo, two planes of one buffer): each
+// 16-wide k step issues W*hi and W*lo into the same fp32 accumulator.  The tensor pipe is
+// nearly idle in these weight-streaming GEMMs, so the second MMA costs no time, and the
+// activations keep ~17 significant bits instead of bf16's 8.
+//
 // Persistent, fixed-partition stream-K: the (128-row tile, 64-wide k-block) work items of
 // the weight matrix are laid out tile-major and cut into one contiguous range per CTA
 // (one CTA per SM).  A CTA streams its range through a deep TMA ring without pausing;
@@ -45,7 +50,7 @@ __host__ __device__ inline SmemMap smem_map(int nt, int stages) {
   SmemMap m;
   m.a = 0;
   m.b = m.a + static_cast<size_t>(stages) * kABytes;
-  m.bar = m.b + static_cast<size_t>(stages) * nt * kBK * 2;
+  m.bar = m.b + static_cast<size_t>(stages) * 2 * nt * kBK * 2;   // hi and lo boxes per stage
   m.misc = m.bar + static_cast<size_t>(2 * stages + 4) * 8;       // full, empty, accf[2], tfree[2]
   m.xch = (m.misc + 32 + 15) & ~static_cast<size_t>(15);        // tmem slot + flags
   m.inv = m.xch + 16 * kBM * 4;                                    // 16 columns x 128 rows
@@ -197,13 +202,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           else tma_load_2d(dst, mapA, &full[st], kx, lt * kBM);
         }
       };
-      auto load_b = [&](int w, int st) {
-        tma_load_2d(sB + static_cast<size_t>(st) * b_bytes, &tmB, &full[st], static_cast<int>(w % kb) * kBK,
-                    b_row0);
+      auto load_b = [&](int w, int st) {   // hi box, then the lo box plane_rows rows further
+        uint8_t* dst = sB + static_cast<size_t>(st) * 2 * b_bytes;
+        const int kx = static_cast<int>(w % kb) * kBK;
+        tma_load_2d(dst, &tmB, &full[st], kx, b_row0);
+        tma_load_2d(dst + b_bytes, &tmB, &full[st], kx, b_row0 + a.plane_rows);
       };
       const int npre = nwork < stages ? nwork : stages;
       for (int i = 0; i < npre; ++i) {
-        mbar_arrive_expect_tx(&full[i], kABytes + b_bytes);
+        mbar_arrive_expect_tx(&full[i], kABytes + 2 * b_bytes);
         load_a(w0 + i, i);
       }
       griddep_wait();   // activations are produced by the previous kernel
@@ -217,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&full[st], kABytes + b_bytes);
+        mbar_arrive_expect_tx(&full[st], kABytes + 2 * b_bytes);
         load_a(w0 + i, st);
         load_b(w0 + i, st);
         issued = i + 1;
@@ -247,11 +254,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(buf) * cols;
         const uint32_t abase = smem_u32(sA + static_cast<size_t>(st) * kABytes);
-        const uint32_t bbase = smem_u32(sB + static_cast<size_t>(st) * b_bytes);
+        const uint32_t bbase = smem_u32(sB + static_cast<size_t>(st) * 2 * b_bytes);
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk) {
-          umma_bf16(d, sw128_kmajor_desc(abase + kk * 32), sw128_kmajor_desc(bbase + kk * 32), idesc,
-                    (!seg_first || kk > 0) ? 1u : 0u);
+          const uint64_t adesc = sw128_kmajor_desc(abase + kk * 32);
+          umma_bf16(d, adesc, sw128_kmajor_desc(bbase + kk * 32), idesc, (!seg_first || kk > 0) ? 1u : 0u);
+          umma_bf16(d, adesc, sw128_kmajor_desc(bbase + b_bytes + kk * 32), idesc, 1u);
         }
         umma_commit(&empty[st]);
         if (seg_last) {
@@ -301,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             a.q_out[static_cast<size_t>(b_row0 + c) * (a.H * a.hd) + f] = out;
           } else {
             const int kv = src - 1;
-            __nv_bfloat16* dst;
+            float* dst;
             if (nd->kv_commit) {
               dst = a.kv_commit +
                     ((((static_cast<size_t>(nd->seq) * a.L + grp.layer) * 2 + kv) * a.KVH + head) * a.max_ctx +
@@ -311,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ((((static_cast<size_t>(nd->seq) * a.n_slots + nd->slot) * a.L + grp.layer) * 2 + kv) * a.KVH +
                      head) * a.hd + dim;
             }
-            *dst = __float2bfloat16_rn(out);
+            *dst = out;
           }
         }
         named_bar_sync(1, 128);
@@ -328,8 +336,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float x = __fadd_rn(*hp, v[j]);
             *hp = x;
             const size_t o = static_cast<size_t>(b_row0 + c) * a.d + f;
-            if (grp.has_next) a.hb_out[o] = __float2bfloat16_rn(__fmul_rn(x, bf16_to_f32(grp.g_next[f])));
-            if (grp.stage_end) a.exit_hb[o] = __float2bfloat16_rn(__fmul_rn(x, bf16_to_f32(a.g_final[f])));
+            const size_t lo = static_cast<size_t>(a.plane_rows) * a.d;
+            if (grp.has_next) store_pair(a.hb_out + o, a.hb_out + lo + o, __fmul_rn(x, bf16_to_f32(grp.g_next[f])));
+            if (grp.stage_end) store_pair(a.exit_hb + o, a.exit_hb + lo + o, __fmul_rn(x, bf16_to_f32(a.g_final[f])));
             sq[j] = __fmul_rn(x, x);
           }
         }
@@ -358,7 +367,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (c >= n) break;
             const float g = xch[j * kBM + r], u = xch[j * kBM + r + 64];
             const float act = g / (1.0f + expf(-g)) * u;
-            a.act_out[static_cast<size_t>(b_row0 + c) * a.d_ff + feat] = __float2bfloat16_rn(act);
+            const size_t o = static_cast<size_t>(b_row0 + c) * a.d_ff + feat;
+            store_pair(a.act_out + o, a.act_out + static_cast<size_t>(a.plane_rows) * a.d_ff + o, act);
           }
         }
         named_bar_sync(1, 128);
@@ -522,7 +532,8 @@ cudaError_t launch_gemm(int epi, const CUtensorMap& a0, const CUtensorMap& a1, c
   bool any_next = false, any_end = false;
   for (int g = 0; g < args.n_groups; ++g) {
     const GemmGroup& gr = args.groups[g];
-    if (gr.n < 1 || gr.n > args.nt || gr.b_row0 < 0) return cudaErrorInvalidValue;
+    if (gr.n < 1 || gr.n > args.nt || gr.b_row0 < 0 || gr.b_row0 + gr.n > args.plane_rows)
+      return cudaErrorInvalidValue;
     if (gr.has_next && !gr.g_next) return cudaErrorInvalidValue;
     any_next |= gr.has_next != 0;
     any_end |= gr.stage_end != 0;

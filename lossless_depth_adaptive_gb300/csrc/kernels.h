@@ -75,6 +75,10 @@ struct GemmArgs {
   int32_t* err;         // device error flag
   const DevNode* nodes; // node rows (absolute)
   int32_t evict_first;  // stream A with an L2 evict-first policy
+  // Activation buffers hold two bf16 planes, hi then lo (x ~= hi + lo): the lo plane of a
+  // [rows][K] buffer starts plane_rows rows after the hi plane, for the B operand (tensor
+  // map over 2 * plane_rows rows) and for every activation the epilogue writes.
+  int32_t plane_rows;
   // model geometry
   int32_t d, H, KVH, hd, L, d_ff, vocab, max_ctx, n_slots;
   float eps;
@@ -82,18 +86,18 @@ struct GemmArgs {
   const float* ssq_in;  // [rows][d/128]
   // QKV
   float* q_out;         // [rows][H*hd]
-  __nv_bfloat16* kv_commit;   // [B][L][2][KVH][max_ctx][hd]
-  __nv_bfloat16* kv_pool;     // [B][n_slots][L][2][KVH][hd]
+  float* kv_commit;     // [B][L][2][KVH][max_ctx][hd] fp32
+  float* kv_pool;       // [B][n_slots][L][2][KVH][hd] fp32
   const float2* rope;   // [max_ctx][hd/2] (cos, sin)
   // RESID
   float* hidden;        // [hrows][d]
-  __nv_bfloat16* hb_out;      // [rows][d]  bf16(h * g_next), next layer's input
+  __nv_bfloat16* hb_out;      // [2][rows][d]  pair of h * g_next, next layer's input
   float* ssq_out;       // [rows][d/128]
-  __nv_bfloat16* exit_hb;     // [rows][d]
+  __nv_bfloat16* exit_hb;     // [2][rows][d]  pair of h * g_final
   const __nv_bfloat16* g_final;
   float* exit_ssq;      // [rows][d/128]
   // SWIGLU
-  __nv_bfloat16* act_out;     // [rows][d_ff]
+  __nv_bfloat16* act_out;     // [2][rows][d_ff]  pair of SiLU(gate) * up
   // EXIT + DECS
   float* logits_dbg;    // [rows][vocab] or null
   unsigned long long* best;   // [rows] packed (score, ~token), zeroed before the launch
@@ -109,9 +113,10 @@ struct AttnArgs {
   const AttnItem* items;
   const int32_t* tails;
   const float* q;              // [rows][H*hd]
-  const __nv_bfloat16* kv_commit;
-  const __nv_bfloat16* kv_pool;
-  __nv_bfloat16* out;          // [rows][H*hd]
+  const float* kv_commit;      // fp32 caches (layouts as in GemmArgs)
+  const float* kv_pool;
+  __nv_bfloat16* out;          // [2][plane_rows][H*hd] hi/lo pair
+  int32_t plane_rows;
   float* part;                 // [rows][H][max_groups][hd + 2]
   int32_t* counters;           // [items * KVH]
   int32_t* err;
@@ -126,19 +131,22 @@ struct AssembleArgs {
   const __nv_bfloat16* embed;          // [V][d]
   const __nv_bfloat16* const* attn_norm;  // device array [L] of gains
   float* hidden;
-  __nv_bfloat16* hb;
+  __nv_bfloat16* hb;                    // [2][plane_rows][d] hi/lo pair
+  int32_t plane_rows;
   float* ssq;
   unsigned long long* best;             // zeroed for rows 0..n_rows-1 (may be null)
 };
 
 struct CopyJob { int32_t seq, slot, pos, n_layers; };
 
+// KV rows are copied as raw bytes: row_bytes = head_dim x element size (fp32 caches of the
+// decoder, bf16 caches of the isolated entry point), a multiple of 16.
 struct CollapseArgs {
   const CopyJob* jobs;
   int32_t n_jobs;
-  __nv_bfloat16* kv_commit;
-  const __nv_bfloat16* kv_pool;
-  int32_t L, KVH, hd, max_ctx, n_slots;
+  void* kv_commit;
+  const void* kv_pool;
+  int32_t L, KVH, row_bytes, max_ctx, n_slots;
 };
 
 // ---- launchers (return cudaError_t of the launch) -----------------------------------------
@@ -155,10 +163,11 @@ inline size_t gemm_partial_bytes(int nt, int n_ctas) { return static_cast<size_t
 cudaError_t launch_attention(const AttnArgs& a, int n_items, int max_groups_launch, cudaStream_t st, bool pdl);
 cudaError_t launch_assemble(const AssembleArgs& a, cudaStream_t st, bool pdl);
 cudaError_t launch_collapse(const CollapseArgs& a, cudaStream_t st, bool pdl);
-// bf16 [n][d] rows -> bf16(h * g) rows and partial sums of squares (the exit-head input
-// of an isolated exit-head call); zeroes the argmax slots.
+// bf16 [n][d] rows -> hi/lo pair of h * g ([2][plane_rows][d]) and partial sums of squares
+// (the exit-head input of an isolated exit-head call); zeroes the argmax slots.
 cudaError_t launch_exit_prep(const __nv_bfloat16* h, int n, int d, const __nv_bfloat16* g,
-                             __nv_bfloat16* hb, float* ssq, unsigned long long* best, cudaStream_t st);
+                             __nv_bfloat16* hb, int plane_rows, float* ssq, unsigned long long* best,
+                             cudaStream_t st);
 // Packed GEMM weights: box (t, k) = rows 128t..128t+127 x columns 64k..64k+63 of the
 // (virtual) weight matrix, stored at byte offset (t * kblocks + k) * 16384 in the 128-byte
 // swizzled K-major shared-memory image (chunk c of row r at r*128 + (c ^ (r & 7))*16).

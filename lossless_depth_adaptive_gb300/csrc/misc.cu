@@ -33,8 +33,8 @@ constexpr int kMaxTiles = 64;   // d_model up to 8192
 
 // One CTA (128 threads) per node row.  Stage-0 nodes start a slot chain: h = E[token]
 // into the chain's hidden row.  Depth children continue the chain's hidden row left by
-// the previous stage.  Writes the first layer's bf16 input bf16(h * g) and the RMSNorm
-// partial sums, and clears the row's exit-head argmax slot.  The whole row is loaded
+// the previous stage.  Writes the first layer's input h * g as a hi/lo bf16 pair and the
+// RMSNorm partial sums, and clears the row's exit-head argmax slot.  The whole row is loaded
 // before any reduction so the loads overlap.
 __global__ void __launch_bounds__(128) assemble_kernel(const AssembleArgs a) {
   __shared__ float qbuf[kMaxTiles * 4];
@@ -59,7 +59,8 @@ __global__ void __launch_bounds__(128) assemble_kernel(const AssembleArgs a) {
     if (t < ndt) {
       const int f = t * 128 + threadIdx.x;
       if (nd.token >= 0) hrow[f] = x[t];
-      a.hb[static_cast<size_t>(row) * a.d + f] = __float2bfloat16_rn(__fmul_rn(x[t], bf16_to_f32(g[f])));
+      const size_t o = static_cast<size_t>(row) * a.d + f;
+      store_pair(a.hb + o, a.hb + static_cast<size_t>(a.plane_rows) * a.d + o, __fmul_rn(x[t], bf16_to_f32(g[f])));
     }
   }
   row_tile_ssq<kMaxTiles>(x, ndt, qbuf, a.ssq + static_cast<size_t>(row) * ndt);
@@ -67,7 +68,8 @@ __global__ void __launch_bounds__(128) assemble_kernel(const AssembleArgs a) {
 
 cudaError_t launch_assemble(const AssembleArgs& a, cudaStream_t st, bool pdl) {
   if (a.n_rows <= 0) return cudaSuccess;
-  if (!a.nodes || !a.embed || !a.attn_norm || !a.hidden || !a.hb || !a.ssq || a.d % 128 || a.d > 128 * 64)
+  if (!a.nodes || !a.embed || !a.attn_norm || !a.hidden || !a.hb || !a.ssq || a.d % 128 || a.d > 128 * 64 ||
+      a.plane_rows < a.n_rows)
     return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(a.n_rows));
@@ -82,33 +84,34 @@ cudaError_t launch_assemble(const AssembleArgs& a, cudaStream_t st, bool pdl) {
 }
 
 // Collapse gather/scatter: for each job, layers 0..n_layers-1 of the slot chain's branch
-// KV (contiguous [layer][2][KVH][hd] rows in the pool) go to position pos of the
+// KV (contiguous [layer][2][KVH] head rows in the pool) go to position pos of the
 // committed cache.  16-byte vectors; consecutive threads cover consecutive bytes of a
 // head row on both sides.
 __global__ void __launch_bounds__(256) collapse_kernel(const CollapseArgs a) {
   griddep_wait();
   griddep_launch_dependents();
   const CopyJob job = a.jobs[blockIdx.y];
-  const int vec_per_row = a.hd / 8;
+  const int vec_per_row = a.row_bytes / 16;
   const int total = job.n_layers * 2 * a.KVH * vec_per_row;
-  const uint4* src = reinterpret_cast<const uint4*>(
-      a.kv_pool + (static_cast<size_t>(job.seq) * a.n_slots + job.slot) * a.L * 2 * a.KVH * a.hd);
+  const uint4* src = reinterpret_cast<const uint4*>(a.kv_pool) +
+                     (static_cast<size_t>(job.seq) * a.n_slots + job.slot) * a.L * 2 * a.KVH * vec_per_row;
+  uint4* commit = reinterpret_cast<uint4*>(a.kv_commit);
   for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += gridDim.x * blockDim.x) {
     const int ch = idx % vec_per_row;
     int rest = idx / vec_per_row;
     const int h = rest % a.KVH;
     rest /= a.KVH;
     const int kv = rest & 1, layer = rest >> 1;
-    __nv_bfloat16* dst = a.kv_commit +
-                         ((((static_cast<size_t>(job.seq) * a.L + layer) * 2 + kv) * a.KVH + h) * a.max_ctx +
-                          job.pos) * a.hd + ch * 8;
-    *reinterpret_cast<uint4*>(dst) = src[idx];
+    commit[((((static_cast<size_t>(job.seq) * a.L + layer) * 2 + kv) * a.KVH + h) * a.max_ctx + job.pos) *
+               vec_per_row + ch] = src[idx];
   }
 }
 
 cudaError_t launch_collapse(const CollapseArgs& a, cudaStream_t st, bool pdl) {
   if (a.n_jobs <= 0) return cudaSuccess;
-  if (!a.jobs || !a.kv_commit || !a.kv_pool) return cudaErrorInvalidValue;
+  if (!a.jobs || !a.kv_commit || !a.kv_pool || a.row_bytes < 16 || a.row_bytes % 16 ||
+      (reinterpret_cast<uintptr_t>(a.kv_commit) & 15) || (reinterpret_cast<uintptr_t>(a.kv_pool) & 15))
+    return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(32, static_cast<unsigned>(a.n_jobs));
   cfg.blockDim = dim3(256);
@@ -121,9 +124,11 @@ cudaError_t launch_collapse(const CollapseArgs& a, cudaStream_t st, bool pdl) {
   return cudaLaunchKernelEx(&cfg, collapse_kernel, a);
 }
 
-// Isolated exit head: bf16 hidden rows -> bf16(h * g) and the RMSNorm partial sums.
+// Isolated exit head: bf16 hidden rows -> the hi/lo pair of h * g and the RMSNorm
+// partial sums.
 __global__ void __launch_bounds__(128) exit_prep_kernel(const __nv_bfloat16* h, int d, const __nv_bfloat16* g,
-                                                        __nv_bfloat16* hb, float* ssq, unsigned long long* best) {
+                                                        __nv_bfloat16* hb, int plane_rows, float* ssq,
+                                                        unsigned long long* best) {
   __shared__ float qbuf[kMaxTiles * 4];
   const int row = blockIdx.x;
   if (threadIdx.x == 0) best[row] = 0ull;
@@ -136,15 +141,18 @@ __global__ void __launch_bounds__(128) exit_prep_kernel(const __nv_bfloat16* h, 
   for (int t = 0; t < kMaxTiles; ++t) {
     if (t < ndt) {
       const int f = t * 128 + threadIdx.x;
-      hb[static_cast<size_t>(row) * d + f] = __float2bfloat16_rn(__fmul_rn(x[t], bf16_to_f32(g[f])));
+      const size_t o = static_cast<size_t>(row) * d + f;
+      store_pair(hb + o, hb + static_cast<size_t>(plane_rows) * d + o, __fmul_rn(x[t], bf16_to_f32(g[f])));
     }
   }
   row_tile_ssq<kMaxTiles>(x, ndt, qbuf, ssq + static_cast<size_t>(row) * ndt);
 }
 
 cudaError_t launch_exit_prep(const __nv_bfloat16* h, int n, int d, const __nv_bfloat16* g, __nv_bfloat16* hb,
-                             float* ssq, unsigned long long* best, cudaStream_t st) {
-  exit_prep_kernel<<<n, 128, 0, st>>>(h, d, g, hb, ssq, best);
+                             int plane_rows, float* ssq, unsigned long long* best, cudaStream_t st) {
+  if (n < 1 || plane_rows < n || d % 128 || d > 128 * kMaxTiles || !h || !g || !hb || !ssq || !best)
+    return cudaErrorInvalidValue;
+  exit_prep_kernel<<<n, 128, 0, st>>>(h, d, g, hb, plane_rows, ssq, best);
   return cudaGetLastError();
 }
 
