@@ -77,6 +77,9 @@ struct dex_handle {
   cudaStream_t st = nullptr;
   int n_sm = 0;
   int gemm_ctas = 0;           // persistent GEMM grid (CTAs per SM x SMs), fixed per handle
+  // k segments per tile of each weight shape (fixed per handle: results depend on them)
+  int seg_qkv = 1, seg_o = 1, seg_gu = 1, seg_d = 1, seg_lm = 1;
+  size_t partial_bytes = 0;    // segment-partial workspace
   size_t gemm_smem = 0;        // shared-memory budget of a small-tile GEMM CTA
   std::unique_ptr<dex::Lattice> lat, lat_ar;
   std::vector<int> mode;                 // per sequence: 0 idle, 1 DEX, 2 AR
@@ -258,7 +261,10 @@ int gemm(dex_handle* h, int epi, const CUtensorMap& a0, const CUtensorMap& a1, c
          const CUtensorMap* bmaps, dex::GemmArgs a, int nmax, int64_t weight_bytes, int64_t act_bytes_per_row) {
   if (nmax < 1 || nmax > 256) return DEX_ECAPACITY;
   a.nt = (nmax + 15) & ~15;
-  a.ctas_per_group = h->gemm_ctas;
+  a.n_ctas = h->gemm_ctas;
+  if (a.n_segs > 1 &&
+      dex::gemm_partial_bytes(a.nt, static_cast<size_t>(a.n_groups) * a.n_tiles * a.n_segs) > h->partial_bytes)
+    return DEX_ECAPACITY;
   a.tmem_cols = pow2_at_least(a.nt);
   a.stages = dex::gemm_stages_for(a.nt, h->gemm_smem);
   cudaEvent_t e0 = nullptr, e1 = nullptr;
@@ -328,6 +334,7 @@ int run_layers(dex_handle* h, const Uploaded& u, const std::vector<Batch>& batch
     a.src_tiles0 = qd / 128;
     a.src_tiles1 = kvd / 128;
     a.n_tiles = (qd + 2 * kvd) / 128;
+    a.n_segs = h->seg_qkv;
     a.ssq_in = h->ssq;
     a.q_out = h->q;
     a.kv_commit = h->kv_commit;
@@ -365,6 +372,7 @@ int run_layers(dex_handle* h, const Uploaded& u, const std::vector<Batch>& batch
     fill_groups(a, 1);
     a.kblocks = (qd + 63) / 64;
     a.n_tiles = h->d / 128;
+    a.n_segs = h->seg_o;
     a.src_tiles0 = a.n_tiles;
     a.hidden = h->hidden;
     a.hb_out = h->hb;
@@ -377,6 +385,7 @@ int run_layers(dex_handle* h, const Uploaded& u, const std::vector<Batch>& batch
     fill_groups(a, 2);
     a.kblocks = (h->d + 63) / 64;
     a.n_tiles = (h->dff + 63) / 64;
+    a.n_segs = h->seg_gu;
     a.src_tiles0 = a.n_tiles;
     a.ssq_in = h->ssq;
     a.act_out = h->act;
@@ -388,6 +397,7 @@ int run_layers(dex_handle* h, const Uploaded& u, const std::vector<Batch>& batch
     fill_groups(a, 3);
     a.kblocks = (h->dff + 63) / 64;
     a.n_tiles = h->d / 128;
+    a.n_segs = h->seg_d;
     a.src_tiles0 = a.n_tiles;
     a.hidden = h->hidden;
     a.hb_out = h->hb;
@@ -528,6 +538,7 @@ int run_round(dex_handle* h, dex::Lattice* lat, std::vector<dex_copy_job>* pendi
     a.nodes = u.nodes;
     a.kblocks = (h->d + 63) / 64;
     a.n_tiles = (h->V + 127) / 128;
+    a.n_segs = h->seg_lm;
     a.src_tiles0 = a.n_tiles;
     a.ssq_in = h->exit_ssq;
     a.logits_dbg = h->cfg.debug_logits ? h->logits_dbg : nullptr;
@@ -735,8 +746,29 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
                                               static_cast<size_t>(h->d / 128),
                                               static_cast<size_t>((h->dff + 63) / 64),
                                               static_cast<size_t>((h->V + 127) / 128)});
-  if (dalloc(h, &h->partial, dex::gemm_partial_bytes(256, h->gemm_ctas) * std::max(1, h->N)) ||
-      dalloc(h, &h->counters, ntiles_max * 4 * std::max(1, h->N)))
+  // fixed k segments per weight shape, and a partial workspace for the largest launch:
+  // a prefill chunk (one group, node tile 256) or a round (N groups, node tile <= rows)
+  {
+    const int kb_d = (h->d + 63) / 64, kb_q = (qd + 63) / 64, kb_f = (h->dff + 63) / 64;
+    const int t_qkv = (qd + 2 * kvd) / 128, t_o = h->d / 128, t_gu = (h->dff + 63) / 64, t_lm = (h->V + 127) / 128;
+    h->seg_qkv = dex::gemm_segments(t_qkv, kb_d, h->gemm_ctas);
+    h->seg_o = dex::gemm_segments(t_o, kb_q, h->gemm_ctas);
+    h->seg_gu = dex::gemm_segments(t_gu, kb_d, h->gemm_ctas);
+    h->seg_d = dex::gemm_segments(t_o, kb_f, h->gemm_ctas);
+    h->seg_lm = dex::gemm_segments(t_lm, kb_d, h->gemm_ctas);
+    const size_t u_layer = std::max<size_t>({static_cast<size_t>(t_qkv) * h->seg_qkv,
+                                            static_cast<size_t>(t_o) * h->seg_o,
+                                            static_cast<size_t>(t_gu) * h->seg_gu,
+                                            static_cast<size_t>(t_o) * h->seg_d});
+    const int nt_round = std::min(256, (std::max(1, h->lat->max_round_nodes()) + 15) & ~15);
+    h->partial_bytes = std::max({dex::gemm_partial_bytes(256, u_layer),
+                                 dex::gemm_partial_bytes(nt_round, u_layer * std::max(1, h->N)),
+                                 dex::gemm_partial_bytes(256, static_cast<size_t>(t_lm) * h->seg_lm)});
+    if (debug_enabled())
+      fprintf(stderr, "dex: segments qkv %d o %d gu %d down %d lm %d, partial workspace %.1f MB\n", h->seg_qkv,
+              h->seg_o, h->seg_gu, h->seg_d, h->seg_lm, h->partial_bytes / 1e6);
+  }
+  if (dalloc(h, &h->partial, h->partial_bytes) || dalloc(h, &h->counters, ntiles_max * 4 * std::max(1, h->N)))
     return DEX_ENOMEM;
   h->plan_cap = (R * sizeof(dex::DevNode) + R * 16 * 8 +
                  static_cast<size_t>(L) * (B * h->N + 8) * sizeof(dex::AttnItem) + 64 * 16 + 8192);
@@ -1042,7 +1074,8 @@ int dex_exit_head_decs(const void* hidden, int32_t n, int32_t d, const void* fin
   const size_t o_cnt = o_nodes + up(static_cast<size_t>(n) * sizeof(dex::DevNode));
   const size_t o_err = o_cnt + up(static_cast<size_t>(n_tiles) * 4);
   const size_t o_part = o_err + 256;
-  const size_t total = o_part + dex::gemm_partial_bytes(nt, n_sm);
+  const int segs = dex::gemm_segments(n_tiles, kb, n_sm);
+  const size_t total = o_part + (segs > 1 ? dex::gemm_partial_bytes(nt, static_cast<size_t>(n_tiles) * segs) : 256);
   uint8_t* scratch = nullptr;
   if (cudaMallocAsync(reinterpret_cast<void**>(&scratch), total, st) != cudaSuccess) return DEX_ENOMEM;
   bf16* hb = reinterpret_cast<bf16*>(scratch + o_hb);
@@ -1062,7 +1095,8 @@ int dex_exit_head_decs(const void* hidden, int32_t n, int32_t d, const void* fin
     exit_nodes_kernel<<<(n + 127) / 128, 128, 0, st>>>(nodes, n, dn);
     dex::GemmArgs a = {};
     a.n_groups = 1;
-    a.ctas_per_group = n_sm;
+    a.n_ctas = n_sm;
+    a.n_segs = segs;
     a.groups[0].n = n;
     a.groups[0].b_row0 = 0;
     a.nt = nt;
@@ -1167,7 +1201,8 @@ extern "C" int dex_exit_head_decs_noalloc(const void* hidden, int32_t n, int32_t
   const size_t o_cnt = o_nodes + up(static_cast<size_t>(n) * sizeof(dex::DevNode));
   const size_t o_err = o_cnt + up(static_cast<size_t>(n_tiles) * 4);
   const size_t o_part = o_err + 256;
-  const size_t total = o_part + dex::gemm_partial_bytes(nt, n_sm);
+  const int segs = dex::gemm_segments(n_tiles, kb, n_sm);
+  const size_t total = o_part + (segs > 1 ? dex::gemm_partial_bytes(nt, static_cast<size_t>(n_tiles) * segs) : 256);
   if (total > DEX_NOALLOC_SCRATCH_BYTES) return DEX_ECAPACITY;   // does not fit the fixed scratch
   void* base = nullptr;
   const int rc0 = exit_scratch_address(dev, &base);
@@ -1192,7 +1227,8 @@ extern "C" int dex_exit_head_decs_noalloc(const void* hidden, int32_t n, int32_t
   if (cudaGetLastError() != cudaSuccess) return DEX_ECUDA;
   dex::GemmArgs a = {};
   a.n_groups = 1;
-  a.ctas_per_group = n_sm;
+  a.n_ctas = n_sm;
+  a.n_segs = segs;
   a.groups[0].n = n;
   a.groups[0].b_row0 = 0;
   a.nt = nt;

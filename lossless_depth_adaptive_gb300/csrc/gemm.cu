@@ -13,14 +13,16 @@
 // nearly idle in these weight-streaming GEMMs, so the second MMA costs no time, and the
 // activations keep ~17 significant bits instead of bf16's 8.
 //
-// Persistent, fixed-partition stream-K: the (128-row tile, 64-wide k-block) work items of
-// the weight matrix are laid out tile-major and cut into one contiguous range per CTA
-// (one CTA per SM).  A CTA streams its range through a deep TMA ring without pausing;
-// where its range starts or ends inside a tile, it writes a partial tile and the last of
-// that tile's CTAs sums the partials in k order.  The partition depends only on the
-// weight shape and the CTA count -- never on the number of nodes -- so a node's result is
-// bit-identical in any batch.  Two TMEM accumulators alternate between consecutive
-// segments, so the epilogue of one tile overlaps the MMAs of the next.
+// Persistent, fixed-segment split-K: every 128-row output tile's k range is cut into a
+// fixed number of segments S that depends only on the weight shape (and the handle's
+// grid), never on the nodes or on how many weight matrices share the launch.  Each
+// segment is accumulated from zero; a tile's segments are summed in segment order by
+// the last CTA to finish one of them.  A node's result is therefore bit-identical in any
+// batch and in any grouped launch.  The (group, tile, segment) units of a launch are
+// dealt out as contiguous ranges over a fixed grid of resident CTAs, so a launch with
+// several weight matrices still runs in one wave; each CTA streams its units' k-blocks
+// through a deep TMA ring without pausing.  Two TMEM accumulators alternate between
+// consecutive units, so the epilogue of one unit overlaps the MMAs of the next.
 //
 // Roles: warp 0 issues TMA loads (weights first -- they do not depend on the previous
 // kernel -- then, after the grid-dependency wait, the activations); warp 1 owns TMEM
@@ -31,6 +33,8 @@
 // pool), EPI_RESID (residual add into the fp32 hidden state, next layer's bf16 input,
 // RMSNorm partial sums, exit-head input at a stage boundary), EPI_SWIGLU
 // (SiLU(gate) * up), EPI_EXIT (exit logits, DECS mask, Gumbel noise, argmax).
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -41,7 +45,6 @@ constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr uint32_t kABytes = kBM * kBK * 2;   // 16 KB weight tile per stage
 constexpr int kNtMax = 256;
-constexpr int kMaxContrib = 32;   // partial tiles listed in shared memory per reduction
 
 struct SmemMap {
   size_t a, b, bar, misc, xch, inv, qsum, qkey, total;
@@ -56,7 +59,7 @@ __host__ __device__ inline SmemMap smem_map(int nt, int stages) {
   m.inv = m.xch + 16 * kBM * 4;                                    // 16 columns x 128 rows
   m.qsum = m.inv + kNtMax * 4;
   m.qkey = m.qsum + 4 * 16 * 4;
-  m.total = m.qkey + 4 * 16 * 8 + (kMaxContrib + 4) * 4;
+  m.total = m.qkey + 4 * 16 * 8;
   return m;
 }
 
@@ -73,42 +76,73 @@ int gemm_stages_for(int nt, size_t small_budget) {
   return s;
 }
 
-// Work range of CTA c: [c W / G, (c+1) W / G) over tile-major (tile, k-block) items.
-// (W * G < 2^31 for every shape here, so 32-bit arithmetic is exact.)
-__device__ __forceinline__ int work_start(int c, int W, int G) { return static_cast<int>((static_cast<unsigned>(c) * W) / G); }
-// CTAs whose ranges may intersect tile t (work [t kb, (t+1) kb)): c_lo..c_hi.
-__device__ __forceinline__ void tile_cta_span(int t, int kb, int W, int G, int& c_lo, int& c_hi) {
-  const unsigned x = static_cast<unsigned>(t) * kb, y = x + kb;
-  c_lo = static_cast<int>(((x + 1) * G + W - 1) / W) - 1;   // first c with end(c) > x
-  c_hi = static_cast<int>((y * G + W - 1) / W) - 1;         // last c with start(c) < y
-  c_lo = c_lo < 0 ? 0 : c_lo;
-  c_hi = c_hi > G - 1 ? G - 1 : c_hi;
+// Units of a launch, group-major: u = (g * n_tiles + t) * S + s.  CTA c owns units
+// [c U / C, (c+1) U / C).  Segment s of a tile covers k-blocks [s kb / S, (s+1) kb / S).
+struct Unit {
+  int g, t, s, k0, k1;
+};
+__device__ __forceinline__ Unit unit_at(int u, int n_tiles, int S, int kb) {
+  Unit x;
+  const int per_group = n_tiles * S;
+  x.g = u / per_group;
+  const int r = u - x.g * per_group;
+  x.t = r / S;
+  x.s = r - x.t * S;
+  x.k0 = (x.s * kb) / S;
+  x.k1 = ((x.s + 1) * kb) / S;
+  return x;
 }
-__device__ __forceinline__ bool cta_touches_tile(int c, int t, int kb, int W, int G) {
-  const int x = t * kb, y = x + kb;
-  const int s = work_start(c, W, G), e = work_start(c + 1, W, G);
-  return (s > x ? s : x) < (e < y ? e : y);
+__device__ __forceinline__ int unit_begin(int c, int U, int C) {
+  return static_cast<int>((static_cast<long long>(c) * U) / C);
 }
-// Partial slot of CTA c for tile t: slot 2c for the tile its range starts in, else 2c+1.
-__device__ __forceinline__ int partial_slot(int c, int t, int kb, int W, int G) {
-  return (work_start(c, W, G) / kb == t) ? 2 * c : 2 * c + 1;
+
+// Segments per tile for a weight shape on a grid of C CTAs: the smallest S for which the
+// busiest CTA of a one-matrix launch streams at most 1/0.9 of the average k-blocks (fewer
+// segments mean fewer partial tiles to write and sum), else the best balance among
+// S <= 8 C / n_tiles.  Host-side, once per handle.
+int gemm_segments(int n_tiles, int kblocks, int C) {
+  int best = 1;
+  double best_eff = -1.0;
+  const int s_max = std::max(1, std::min(kblocks, (8 * C + n_tiles - 1) / n_tiles));
+  const double avg = static_cast<double>(n_tiles) * kblocks / C;
+  for (int S = 1; S <= s_max; ++S) {
+    const long long U = static_cast<long long>(n_tiles) * S;
+    long long most = 0;
+    for (int c = 0; c < C; ++c) {
+      const long long u0 = c * U / C, u1 = (c + 1) * U / C;
+      long long w = 0;
+      for (long long u = u0; u < u1; ++u) {
+        const long long sg = u % S;
+        w += ((sg + 1) * kblocks) / S - (sg * kblocks) / S;
+      }
+      most = std::max(most, w);
+    }
+    const double eff = most > 0 ? avg / static_cast<double>(most) : 0.0;
+    if (eff >= 0.9) return S;
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = S;
+    }
+  }
+  return best;
 }
+
 template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ GemmArgs a) {
-  const int G = a.ctas_per_group;
-  const int gi = blockIdx.x / G, cta = blockIdx.x % G;   // group, CTA within the group
-  const GemmGroup& grp = a.groups[gi];
-  const int b_row0 = grp.b_row0;
-  const int kb = a.kblocks;
-  const int W = a.n_tiles * kb;
-  const int w0 = work_start(cta, W, G), w1 = work_start(cta + 1, W, G);
-  if (w0 >= w1) return;   // no work (more CTAs than work items)
-  const int nwork = static_cast<int>(w1 - w0);
-  const int t_first = static_cast<int>(w0 / kb), t_last = static_cast<int>((w1 - 1) / kb);
-  const int nseg = t_last - t_first + 1;
+  const int C = gridDim.x, cta = blockIdx.x;
+  const int kb = a.kblocks, S = a.n_segs, nT = a.n_tiles;
+  const int U = a.n_groups * nT * S;
+  const int u0 = unit_begin(cta, U, C), u1 = unit_begin(cta + 1, U, C);
+  if (u0 >= u1) return;   // no work (more CTAs than units)
+  const int n_units = u1 - u0;
+  int nwork = 0;   // k-blocks this CTA streams
+  for (int u = u0; u < u1; ++u) {
+    const Unit x = unit_at(u, nT, S, kb);
+    nwork += x.k1 - x.k0;
+  }
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -125,7 +159,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* inv = reinterpret_cast<float*>(smem + sm.inv);
   float* qsum = reinterpret_cast<float*>(smem + sm.qsum);
   unsigned long long* qkey = reinterpret_cast<unsigned long long*>(smem + sm.qkey);
-  volatile int* s_contrib = reinterpret_cast<volatile int*>(smem + sm.qkey + 4 * 16 * 8);   // [0] count, [1..] slots
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int stages = a.stages;
@@ -156,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     sflag[0] = 0;
     sflag[1] = 0;
     fence_mbar_init();
-    if (!grp.a_packed) {
+    if (!a.groups[0].a_packed) {
       tma_prefetch(&tmA0);
       if (a.src_tiles0 < a.n_tiles || EPI == EPI_SWIGLU) tma_prefetch(&tmA1);
       if (a.src_tiles0 + a.src_tiles1 < a.n_tiles) tma_prefetch(&tmA2);
@@ -177,17 +210,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
-      auto load_a = [&](int w, int st) {
+      auto load_a = [&](const Unit& x, int k, int st) {
         uint8_t* dst = sA + static_cast<size_t>(st) * kABytes;
-        if (grp.a_packed) {   // packed weights: the work item's 16 KB box is contiguous
-          const uint8_t* src = grp.a_packed + static_cast<size_t>(w) * kABytes;
+        const uint8_t* packed = a.groups[x.g].a_packed;
+        if (packed) {   // packed weights: the (tile, k-block) 16 KB box is contiguous
+          const uint8_t* src = packed + (static_cast<size_t>(x.t) * kb + k) * kABytes;
           if (a.evict_first) bulk_load_1d_hint(dst, src, kABytes, &full[st], pol);
           else bulk_load_1d(dst, src, kABytes, &full[st]);
           return;
         }
-        const int t = static_cast<int>(w / kb), kx = static_cast<int>(w % kb) * kBK;
+        const int kx = k * kBK;
         int src, lt;
-        tile_src(t, src, lt);
+        tile_src(x.t, src, lt);
         if (EPI == EPI_SWIGLU) {
           if (a.evict_first) {
             tma_load_2d_hint(dst, &tmA0, &full[st], kx, lt * 64, pol);
@@ -202,32 +236,50 @@ __global__ void __launch_bounds__(kThreads, 1)
           else tma_load_2d(dst, mapA, &full[st], kx, lt * kBM);
         }
       };
-      auto load_b = [&](int w, int st) {   // hi box, then the lo box plane_rows rows further
+      auto load_b = [&](const Unit& x, int k, int st) {   // hi box, then the lo box plane_rows rows further
         uint8_t* dst = sB + static_cast<size_t>(st) * 2 * b_bytes;
-        const int kx = static_cast<int>(w % kb) * kBK;
-        tma_load_2d(dst, &tmB, &full[st], kx, b_row0);
-        tma_load_2d(dst + b_bytes, &tmB, &full[st], kx, b_row0 + a.plane_rows);
+        const int row0 = a.groups[x.g].b_row0;
+        tma_load_2d(dst, &tmB, &full[st], k * kBK, row0);
+        tma_load_2d(dst + b_bytes, &tmB, &full[st], k * kBK, row0 + a.plane_rows);
       };
+      // weights of the first ring slots before the grid-dependency wait
       const int npre = nwork < stages ? nwork : stages;
-      for (int i = 0; i < npre; ++i) {
-        mbar_arrive_expect_tx(&full[i], kABytes + 2 * b_bytes);
-        load_a(w0 + i, i);
+      {
+        int u = u0, i = 0;
+        Unit x = unit_at(u, nT, S, kb);
+        int k = x.k0;
+        for (; i < npre; ++i) {
+          mbar_arrive_expect_tx(&full[i], kABytes + 2 * b_bytes);
+          load_a(x, k, i);
+          if (++k == x.k1 && ++u < u1) {
+            x = unit_at(u, nT, S, kb);
+            k = x.k0;
+          }
+        }
       }
       griddep_wait();   // activations are produced by the previous kernel
-      for (int i = 0; i < npre; ++i) load_b(w0 + i, i);
+      int u = u0;
+      Unit x = unit_at(u, nT, S, kb);
+      int k = x.k0;
       int issued = npre;
       bool ok = true;
-      for (int i = npre; i < nwork; ++i) {
+      for (int i = 0; i < nwork; ++i) {
         const int st = i % stages;
-        const uint32_t use = static_cast<uint32_t>(i / stages);
-        if (!mbar_wait(&empty[st], (use - 1) & 1u, a.err, DEV_TIMEOUT_EMPTY)) {
-          ok = false;
-          break;
+        if (i >= npre) {
+          const uint32_t use = static_cast<uint32_t>(i / stages);
+          if (!mbar_wait(&empty[st], (use - 1) & 1u, a.err, DEV_TIMEOUT_EMPTY)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[st], kABytes + 2 * b_bytes);
+          load_a(x, k, st);
+          issued = i + 1;
         }
-        mbar_arrive_expect_tx(&full[st], kABytes + 2 * b_bytes);
-        load_a(w0 + i, st);
-        load_b(w0 + i, st);
-        issued = i + 1;
+        load_b(x, k, st);
+        if (++k == x.k1 && ++u < u1) {
+          x = unit_at(u, nT, S, kb);
+          k = x.k0;
+        }
       }
       if (!ok) {   // drain copies still in flight before the CTA can exit
         for (int i = (issued > stages ? issued - stages : 0); i < issued; ++i)
@@ -238,15 +290,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(kBM, a.nt);
-      int seg = 0;
+      int ui = 0;   // unit index within this CTA
+      int u = u0;
+      Unit x = unit_at(u, nT, S, kb);
+      int k = x.k0;
       for (int i = 0; i < nwork; ++i) {
-        const int w = w0 + i;
-        const int k = w % kb;
-        const bool seg_first = (i == 0) || (k == 0);
-        const bool seg_last = (i == nwork - 1) || (k == kb - 1);
-        const int buf = seg & 1;
-        if (seg_first && seg >= 2) {   // reuse of an accumulator: wait until the epilogue drained it
-          if (!mbar_wait(&tfree[buf], static_cast<uint32_t>((seg >> 1) - 1) & 1u, a.err, DEV_TIMEOUT_ACC)) break;
+        const bool seg_first = (k == x.k0);
+        const bool seg_last = (k == x.k1 - 1);
+        const int buf = ui & 1;
+        if (seg_first && ui >= 2) {   // reuse of an accumulator: wait until the epilogue drained it
+          if (!mbar_wait(&tfree[buf], static_cast<uint32_t>((ui >> 1) - 1) & 1u, a.err, DEV_TIMEOUT_ACC)) break;
           tc_fence_after();
         }
         const int st = i % stages;
@@ -264,7 +317,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(&empty[st]);
         if (seg_last) {
           umma_commit(&accf[buf]);
-          ++seg;
+          ++ui;
+        }
+        if (++k == x.k1 && ++u < u1) {
+          x = unit_at(u, nT, S, kb);
+          k = x.k0;
         }
       }
     }
@@ -273,20 +330,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wq = warp & 3;           // TMEM lane quarter this warp may access
     const int r = wq * 32 + lane;      // accumulator row within the tile
     const int ep = tid - 64;           // 0..127
-    const int n = grp.n;
     const int ndt = a.d / 128;
     griddep_wait();
-    if (EPI != EPI_RESID) {
-      for (int c = ep; c < n; c += 128) {
-        const float* s = a.ssq_in + static_cast<size_t>(b_row0 + c) * ndt;
-        float t = s[0];
-        for (int j = 1; j < ndt; ++j) t = __fadd_rn(t, s[j]);
-        inv[c] = 1.0f / sqrtf(__fadd_rn(__fdiv_rn(t, static_cast<float>(a.d)), a.eps));
-      }
-    }
+    int g_inv = -1;                    // group whose RMSNorm scales are in inv[]
 
-    // per-chunk epilogue of tile (src, lt): v[j] = accumulator of (row r, node c0 + j)
-    auto epilogue_chunk = [&](int src, int lt, int c0, float (&v)[16]) {
+    // per-chunk epilogue of tile (src, lt) of group g: v[j] = accumulator of (row r, node c0 + j)
+    auto epilogue_chunk = [&](const GemmGroup& grp, int src, int lt, int c0, float (&v)[16]) {
+      const int n = grp.n;
+      const int b_row0 = grp.b_row0;
       if (EPI == EPI_QKV) {
         const int f = lt * kBM + r;      // feature within the source (q, k or v)
         const int half = a.hd >> 1;
@@ -406,42 +457,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
 
-    for (int sg = 0; sg < nseg; ++sg) {
-      const int t = t_first + sg, buf = sg & 1;
+    for (int ui = 0; ui < n_units; ++ui) {
+      const Unit x = unit_at(u0 + ui, nT, S, kb);
+      const GemmGroup& grp = a.groups[x.g];
+      const int n = grp.n;
+      const int buf = ui & 1;
       int src, lt;
-      tile_src(t, src, lt);
-      if (!mbar_wait(&accf[buf], static_cast<uint32_t>(sg >> 1) & 1u, a.err, DEV_TIMEOUT_ACC)) sflag[1] = 1;
+      tile_src(x.t, src, lt);
+      if (EPI != EPI_RESID && x.g != g_inv) {   // RMSNorm scales of this group's node rows
+        named_bar_sync(1, 128);                 // previous readers of inv[] are done
+        for (int c = ep; c < n; c += 128) {
+          const float* sp = a.ssq_in + static_cast<size_t>(grp.b_row0 + c) * ndt;
+          float t = sp[0];
+          for (int j = 1; j < ndt; ++j) t = __fadd_rn(t, sp[j]);
+          inv[c] = 1.0f / sqrtf(__fadd_rn(__fdiv_rn(t, static_cast<float>(a.d)), a.eps));
+        }
+        g_inv = x.g;
+      }
+      if (!mbar_wait(&accf[buf], static_cast<uint32_t>(ui >> 1) & 1u, a.err, DEV_TIMEOUT_ACC)) sflag[1] = 1;
       named_bar_sync(1, 128);
       if (sflag[1]) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + static_cast<uint32_t>(buf) * cols + (static_cast<uint32_t>(wq * 32) << 16);
-      // the tile's contributing CTAs, in k order (= CTA order), listed once
-      if (ep == 0) {
-        int c_lo, c_hi;
-        tile_cta_span(t, kb, W, G, c_lo, c_hi);
-        int cnt = 0;
-        for (int c = c_lo; c <= c_hi; ++c) {
-          if (!cta_touches_tile(c, t, kb, W, G)) continue;
-          if (cnt < kMaxContrib) s_contrib[1 + cnt] = partial_slot(c, t, kb, W, G);
-          ++cnt;
-        }
-        s_contrib[0] = cnt;
-      }
-      named_bar_sync(1, 128);
-      const int parts = s_contrib[0];
-      if (parts == 1) {   // the whole tile is in this CTA's range
+      if (S == 1) {   // the whole tile is this unit
         for (int c0 = 0; c0 < n; c0 += 16) {
           float v[16];
           tmem_ld16(taddr + static_cast<uint32_t>(c0), v);
-          epilogue_chunk(src, lt, c0, v);
+          epilogue_chunk(grp, src, lt, c0, v);
         }
         tc_fence_before();
         mbar_arrive(&tfree[buf]);
       } else {
-        // partial tiles: [slot][row][nt] fp32, a thread's 16 columns are 64 contiguous bytes
-        float* gpart = a.partial + static_cast<size_t>(gi) * 2 * G * a.nt * kBM;
-        float* part = gpart + static_cast<size_t>(partial_slot(cta, t, kb, W, G)) * a.nt * kBM +
-                      static_cast<size_t>(r) * a.nt;
+        // segment partial: [unit][row][nt] fp32, a thread's 16 columns are 64 contiguous bytes
+        const size_t tile_unit0 = (static_cast<size_t>(x.g) * nT + x.t) * S;   // unit of segment 0
+        float* part = a.partial + ((tile_unit0 + x.s) * kBM + r) * a.nt;
         for (int c0 = 0; c0 < n; c0 += 16) {
           float v[16];
           tmem_ld16(taddr + static_cast<uint32_t>(c0), v);
@@ -453,36 +502,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&tfree[buf]);
         __threadfence();
         named_bar_sync(1, 128);
-        int32_t* counter = a.counters + static_cast<size_t>(gi) * a.n_tiles + t;
-        if (ep == 0) sflag[0] = (atomicAdd(counter, 1) == parts - 1) ? 1 : 0;
+        int32_t* counter = a.counters + static_cast<size_t>(x.g) * nT + x.t;
+        if (ep == 0) sflag[0] = (atomicAdd(counter, 1) == S - 1) ? 1 : 0;
         named_bar_sync(1, 128);
-        if (sflag[0]) {   // last of the tile's CTAs: sum the partial tiles in k order
+        if (sflag[0]) {   // last of the tile's segments: sum the partials in segment order
           __threadfence();
-          const bool listed = parts <= kMaxContrib;   // else walk the contributors in CTA order
-          int c_lo = 0, c_hi = -1;
-          if (!listed) tile_cta_span(t, kb, W, G, c_lo, c_hi);
           for (int c0 = 0; c0 < n; c0 += 16) {
             float v[16];
-            int cnext = c_lo;
-            for (int i = 0; i < parts; ++i) {
-              int slot;
-              if (listed) {
-                slot = s_contrib[1 + i];
-              } else {
-                while (!cta_touches_tile(cnext, t, kb, W, G)) ++cnext;
-                slot = partial_slot(cnext, t, kb, W, G);
-                ++cnext;
-              }
-              const float4* p = reinterpret_cast<const float4*>(gpart + static_cast<size_t>(slot) * a.nt * kBM +
-                                                                 static_cast<size_t>(r) * a.nt + c0);
+            for (int s2 = 0; s2 < S; ++s2) {
+              const float4* p =
+                  reinterpret_cast<const float4*>(a.partial + ((tile_unit0 + s2) * kBM + r) * a.nt + c0);
               float4 q[4];
 #pragma unroll
               for (int q4 = 0; q4 < 4; ++q4) q[q4] = __ldcg(p + q4);
               const float* qf = reinterpret_cast<const float*>(q);
 #pragma unroll
-              for (int j = 0; j < 16; ++j) v[j] = (i == 0) ? qf[j] : __fadd_rn(v[j], qf[j]);
+              for (int j = 0; j < 16; ++j) v[j] = (s2 == 0) ? qf[j] : __fadd_rn(v[j], qf[j]);
             }
-            epilogue_chunk(src, lt, c0, v);
+            epilogue_chunk(grp, src, lt, c0, v);
           }
           if (ep == 0) *counter = 0;
         }
@@ -511,7 +548,7 @@ static cudaError_t launch_one(const CUtensorMap& a0, const CUtensorMap& a1, cons
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(args.n_groups * args.ctas_per_group));
+  cfg.gridDim = dim3(static_cast<unsigned>(args.n_ctas));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
@@ -526,8 +563,12 @@ static cudaError_t launch_one(const CUtensorMap& a0, const CUtensorMap& a1, cons
 cudaError_t launch_gemm(int epi, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& a2,
                         const CUtensorMap& b, const GemmArgs& args, cudaStream_t st, bool pdl) {
   if (args.nt < 16 || args.nt > kNtMax || (args.nt & 15) || args.n_groups < 1 || args.n_groups > kMaxGroups ||
-      args.ctas_per_group < 1)
+      args.n_ctas < 1 || args.n_segs < 1 || args.n_segs > args.kblocks || args.n_tiles < 1 || args.kblocks < 1 ||
+      static_cast<long long>(args.n_groups) * args.n_tiles * args.n_segs > (1ll << 30))
     return cudaErrorInvalidValue;
+  // a launch mixes packed groups with tensor-map weights never: the prefetch decision is per launch
+  for (int g = 1; g < args.n_groups; ++g)
+    if ((args.groups[g].a_packed != nullptr) != (args.groups[0].a_packed != nullptr)) return cudaErrorInvalidValue;
   // every pointer the chosen epilogue dereferences must be set (checked here, on the host)
   bool any_next = false, any_end = false;
   for (int g = 0; g < args.n_groups; ++g) {

@@ -63,14 +63,15 @@ struct GemmGroup {
 struct GemmArgs {
   // tiling
   int32_t n_groups;     // weight matrices in this launch
-  int32_t ctas_per_group;     // fixed partition size of every group
+  int32_t n_ctas;       // grid size (resident CTAs); units are dealt out over it
+  int32_t n_segs;       // k segments per output tile (fixed per weight shape)
   int32_t nt;           // node tile (multiple of 16, <= 256) >= every group's n
   int32_t kblocks;      // K / 64, rounded up
   int32_t stages;       // smem pipeline depth
   int32_t n_tiles;      // output tiles
   int32_t src_tiles0, src_tiles1;   // tiles of source 0 and 1 (source 2 takes the rest)
   int32_t tmem_cols;
-  float* partial;       // [n_groups][2 * ctas_per_group][nt][128] fp32 partial tiles
+  float* partial;       // [n_groups][n_tiles][n_segs][128][nt] fp32 segment partials
   int32_t* counters;    // [n_groups][n_tiles] arrival counters (left at 0)
   int32_t* err;         // device error flag
   const DevNode* nodes; // node rows (absolute)
@@ -152,14 +153,18 @@ struct CollapseArgs {
 // ---- launchers (return cudaError_t of the launch) -----------------------------------------
 // A tensor maps: up to three weight sources (QKV: wq, wk, wv; SWIGLU: wg, wu with 64-row
 // boxes); B: the activation rows with a box of nt rows.
-// Persistent launch: grid = n_groups x ctas_per_group; each CTA streams a fixed contiguous
-// range of its group's (tile, k-block) work; stages chosen from the node tile.
+// Persistent launch over n_ctas CTAs: the launch's (group, tile, k-segment) units are cut
+// into one contiguous range per CTA; stages chosen from the node tile.
 cudaError_t launch_gemm(int epi, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& a2,
                         const CUtensorMap& b, const GemmArgs& args, cudaStream_t st, bool pdl);
 size_t gemm_smem_bytes(int nt, int stages);
 int gemm_stages_for(int nt, size_t small_budget = 104 * 1024);
-// Bytes of the partial-tile workspace a launch over n_ctas CTAs with node tile nt needs.
-inline size_t gemm_partial_bytes(int nt, int n_ctas) { return static_cast<size_t>(2) * n_ctas * nt * 128 * 4; }
+// k segments per 128-row tile for a weight of n_tiles tiles and kblocks k-blocks on a grid
+// of n_ctas CTAs (depends on nothing else, so results never depend on the batch).
+int gemm_segments(int n_tiles, int kblocks, int n_ctas);
+// Bytes of the segment-partial workspace of a launch with `units` (group, tile, segment)
+// units and node tile nt (none is needed when every tile has one segment).
+inline size_t gemm_partial_bytes(int nt, size_t units) { return units * nt * 128 * 4; }
 cudaError_t launch_attention(const AttnArgs& a, int n_items, int max_groups_launch, cudaStream_t st, bool pdl);
 cudaError_t launch_assemble(const AssembleArgs& a, cudaStream_t st, bool pdl);
 cudaError_t launch_collapse(const CollapseArgs& a, cudaStream_t st, bool pdl);
