@@ -6,14 +6,15 @@
 // sequence); keys at c_end..p are the branch entries of the node's P-ancestors' slot
 // chains and its own, read from the branch pool through the node's tail table.
 //
-// Work split: CTA = (sequence item, KV head, 128-position key group).  The committed
-// keys and values of the group are staged once in shared memory by two bulk copies and
-// reused by every node and every query head of the KV head (GQA).  Each warp owns a
-// 32-key slice of the group for every query.  The arithmetic for a query is fixed by
-// absolute positions only -- 32-key slices aligned to position 0, slices combined in
-// order within the group, 128-position groups combined in group order by the last CTA
-// to finish -- so a node's output is bit-identical whether its keys sit in the
-// committed cache or the branch pool and whatever batch it is computed in.
+// Work split: CTA = (sequence item, KV head, 128-position key group); each warp owns a
+// 32-key slice of the group, lane = key.  Keys and values are fp32 rows read straight
+// from global memory (no shared-memory staging, so several CTAs share an SM and hide
+// each other's latency): a lane walks its key's row in 16-byte chunks, and a key that is
+// committed for every query of a batch is read once and scored against all of them.
+// The arithmetic for a query is fixed by absolute positions only -- 32-key slices aligned
+// to position 0, slices combined in order within the group, 128-position groups combined
+// in group order by the last CTA to finish -- so a node's output is bit-identical whether
+// its keys sit in the committed cache or the branch pool and whatever batch it is in.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -22,12 +23,9 @@ namespace dex {
 constexpr int kAttnThreads = 128;
 constexpr int kGroupPos = 128;
 
-// q . k for one fp32 key row.  The 16-byte chunks of the row are visited starting at
-// chunk `rot` (the lane's index), so the lanes of a quarter-warp reading different key
-// rows of an unpadded shared-memory tile hit distinct banks; four independent partial
-// sums shorten the dependency chain.  The visiting order and the summation tree are
-// functions of the key's absolute position only (lane = position mod 32), so a key's
-// score does not depend on where the key is stored or which batch it is computed in.
+// q . k for one fp32 key row.  The lane walks the row's 16-byte chunks starting at chunk
+// `rot` (its index = key position mod 32) with four interleaved partial sums; the order is
+// a function of the key's absolute position only.
 template <int HD>
 __device__ __forceinline__ float dot_q_row(const float* q, const float* krow, int rot) {
   constexpr int NC = HD / 4;
@@ -35,7 +33,7 @@ __device__ __forceinline__ float dot_q_row(const float* q, const float* krow, in
 #pragma unroll
   for (int i = 0; i < NC; ++i) {
     const int c = (i + rot) & (NC - 1);
-    const float4 k4 = *reinterpret_cast<const float4*>(krow + c * 4);
+    const float4 k4 = __ldg(reinterpret_cast<const float4*>(krow) + c);
     const float4 q4 = *reinterpret_cast<const float4*>(q + c * 4);
     float& a = s[i & 3];
     a = fmaf(q4.x, k4.x, a);
@@ -46,53 +44,35 @@ __device__ __forceinline__ float dot_q_row(const float* q, const float* krow, in
   return __fadd_rn(__fadd_rn(s[0], s[1]), __fadd_rn(s[2], s[3]));
 }
 
-constexpr int kQBatch = 8;    // queries staged per pass
+constexpr int kQBatchMax = 8;  // largest query batch of a pass (QB is a template parameter: 1, 2, 4, 8)
+constexpr int kVB = 8;         // value rows loaded ahead
 
-template <int HD>
+// QB: queries per pass, chosen per launch from its largest item (the unused slots of a
+// batch would otherwise still issue their predicated instructions).  A query's arithmetic
+// is the same in every instantiation.
+template <int HD, int QB>
 __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
+  constexpr int kQBatch = QB;
   constexpr int DPL = HD / 32;        // output dims per lane
+  constexpr int NC = HD / 4;          // 16-byte chunks per row
   constexpr int PS = HD + 2;          // partial record: acc[HD], m, l
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  float* sK = reinterpret_cast<float*>(smem_raw);   // [128][HD] fp32, unpadded
-  float* sV = sK + kGroupPos * HD;
-  float* sQ = reinterpret_cast<float*>(sV + kGroupPos * HD);         // [kQBatch][HD]
-  float* sP = sQ + kQBatch * HD;                                     // [kQBatch][4 warps][PS]
+  extern __shared__ __align__(16) float smem_f[];
+  float* sQ = smem_f;                 // [kQBatch][HD]
+  float* sP = sQ + kQBatch * HD;      // [kQBatch][4 warps][PS]
   __shared__ int s_last;
-  __shared__ __align__(8) uint64_t s_bar;
 
   const int g = blockIdx.x, kvh = blockIdx.y, it = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (tid == 0) {
-    mbar_init(&s_bar, 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
   griddep_wait();
   griddep_launch_dependents();
   const AttnItem item = a.items[it];
   if (g >= item.n_groups) return;
   const int g0 = g * kGroupPos;
   const int H = a.H, G = a.H / a.KVH;
-
-  // committed keys/values of positions [g0, cmax) for this KV head: two contiguous
-  // bulk copies (head-major cache: a head's positions are consecutive HD-element rows)
-  const int cmax = min(g0 + kGroupPos, item.max_cend);
-  if (cmax > g0) {
-    if (tid == 0) {
-      const size_t kbase =
-          ((((static_cast<size_t>(item.seq) * a.L + item.layer) * 2 + 0) * a.KVH + kvh) * a.max_ctx + g0) * HD;
-      const size_t vbase =
-          ((((static_cast<size_t>(item.seq) * a.L + item.layer) * 2 + 1) * a.KVH + kvh) * a.max_ctx + g0) * HD;
-      const uint32_t bytes = static_cast<uint32_t>(cmax - g0) * HD * 4;
-      mbar_arrive_expect_tx(&s_bar, 2 * bytes);
-      bulk_load_1d(sK, a.kv_commit + kbase, bytes, &s_bar);
-      bulk_load_1d(sV, a.kv_commit + vbase, bytes, &s_bar);
-    }
-    if (!mbar_wait(&s_bar, 0, a.err, DEV_TIMEOUT_FULL)) {
-      mbar_wait(&s_bar, 0, nullptr, 0);   // the copies may still land: wait (bounded) before exiting
-      return;
-    }
-  }
+  // committed K and V rows of (sequence, layer, KV head): [max_ctx][HD] each
+  const float* kcom =
+      a.kv_commit + ((((static_cast<size_t>(item.seq) * a.L + item.layer) * 2 + 0) * a.KVH + kvh) * a.max_ctx) * HD;
+  const float* vcom = kcom + static_cast<size_t>(a.KVH) * a.max_ctx * HD;
 
   const int nq = (item.row_end - item.row_begin) * G;
   const int ks = g0 + 32 * warp;       // this warp's 32-key slice
@@ -104,56 +84,138 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
       const int row = item.row_begin + qi / G, qh = kvh * G + qi % G;
       sQ[idx] = a.q[(static_cast<size_t>(row) * H + qh) * HD + d] * a.scale_log2;
     }
+    int pos[kQBatch], cend[kQBatch], nrow[kQBatch];
+    int cend_min = 0x7fffffff, pos_max = -1;
+#pragma unroll
+    for (int j = 0; j < kQBatch; ++j) {
+      pos[j] = -1;
+      cend[j] = 0;
+      nrow[j] = item.row_begin;
+      if (j < nb) {
+        nrow[j] = item.row_begin + (qb + j) / G;
+        const DevNode* nd = a.nodes + nrow[j];
+        pos[j] = nd->pos;
+        cend[j] = nd->c_end;
+        cend_min = min(cend_min, cend[j]);
+        pos_max = max(pos_max, pos[j]);
+      }
+    }
     __syncthreads();
-    // each warp: its 32-key slice against every query of the batch
-    for (int j = 0; j < nb; ++j) {
-      const int qi = qb + j;
-      const DevNode nd = a.nodes[item.row_begin + qi / G];
-      const int pos = nd.pos, c_end = nd.c_end;
-      auto key_row = [&](int kk, int kv) -> const float* {
-        if (kk < c_end) return (kv ? sV : sK) + (kk - g0) * HD;
-        int t = kk - c_end;
-        if (t >= nd.n_tail) {   // cannot happen for a well-formed plan; never read out of bounds
-          atomicExch(a.err, DEV_BAD_INDEX);
-          t = nd.n_tail - 1;
+    // key (or value) row kk of query j: committed cache below its c_end, else the branch
+    // entry of its P-ancestry from the pool through the node's tail table
+    auto key_row = [&](int j, int kk, int kv) -> const float* {
+      if (kk < cend[j]) return (kv ? vcom : kcom) + static_cast<size_t>(kk) * HD;
+      const DevNode* nd = a.nodes + nrow[j];
+      int t = kk - cend[j];
+      if (t >= nd->n_tail) {   // cannot happen for a well-formed plan; never read out of bounds
+        atomicExch(a.err, DEV_BAD_INDEX);
+        t = nd->n_tail - 1;
+      }
+      const int slot = a.tails[nd->tail_off + t];
+      return a.kv_pool +
+             ((((static_cast<size_t>(item.seq) * a.n_slots + slot) * a.L + item.layer) * 2 + kv) * a.KVH + kvh) * HD;
+    };
+    // scores of this lane's key against every query of the batch
+    float sc[kQBatch];
+    if (k < cend_min && k <= pos_max) {   // committed for every query: read the row once
+      float part[kQBatch][4];
+#pragma unroll
+      for (int j = 0; j < kQBatch; ++j) part[j][0] = part[j][1] = part[j][2] = part[j][3] = 0.0f;
+      const float4* kr = reinterpret_cast<const float4*>(kcom + static_cast<size_t>(k) * HD);
+#pragma unroll 16
+      for (int i = 0; i < NC; ++i) {
+        const int c = (i + lane) & (NC - 1);
+        const float4 k4 = __ldg(kr + c);
+#pragma unroll
+        for (int j = 0; j < kQBatch; ++j) {
+          if (j < nb) {
+            const float4 q4 = *reinterpret_cast<const float4*>(sQ + j * HD + c * 4);
+            float& acc = part[j][i & 3];
+            acc = fmaf(q4.x, k4.x, acc);
+            acc = fmaf(q4.y, k4.y, acc);
+            acc = fmaf(q4.z, k4.z, acc);
+            acc = fmaf(q4.w, k4.w, acc);
+          }
         }
-        const int slot = a.tails[nd.tail_off + t];
-        return a.kv_pool +
-               ((((static_cast<size_t>(nd.seq) * a.n_slots + slot) * a.L + item.layer) * 2 + kv) * a.KVH + kvh) * HD;
-      };
-      const float s = (k <= pos) ? dot_q_row<HD>(sQ + j * HD, key_row(k, 0), lane) : -INFINITY;
-      const float m = warp_max(s);
-      float l = 0.0f, acc[DPL];
+      }
 #pragma unroll
-      for (int i = 0; i < DPL; ++i) acc[i] = 0.0f;
-      if (m != -INFINITY) {
-        const float p = exp2f(s - m);
-        l = warp_sum(p);
+      for (int j = 0; j < kQBatch; ++j)
+        sc[j] = (j < nb && k <= pos[j]) ? __fadd_rn(__fadd_rn(part[j][0], part[j][1]), __fadd_rn(part[j][2], part[j][3]))
+                                        : -INFINITY;
+    } else {
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          if (ks + jj <= pos) {   // uniform across the warp
-            const float pk = __shfl_sync(0xffffffffu, p, jj);
-            const float* vr = key_row(ks + jj, 1);
-            if constexpr (DPL == 4) {
-              const float4 f = *reinterpret_cast<const float4*>(vr + lane * 4);
-              acc[0] = fmaf(pk, f.x, acc[0]);
-              acc[1] = fmaf(pk, f.y, acc[1]);
-              acc[2] = fmaf(pk, f.z, acc[2]);
-              acc[3] = fmaf(pk, f.w, acc[3]);
-            } else {
-              const float2 f = *reinterpret_cast<const float2*>(vr + lane * 2);
-              acc[0] = fmaf(pk, f.x, acc[0]);
-              acc[1] = fmaf(pk, f.y, acc[1]);
+      for (int j = 0; j < kQBatch; ++j)
+        sc[j] = (j < nb && k <= pos[j]) ? dot_q_row<HD>(sQ + j * HD, key_row(j, k, 0), lane) : -INFINITY;
+    }
+    // per query: slice softmax statistics and the value accumulation, keys in order
+    float mx[kQBatch], lsum[kQBatch], pr[kQBatch], acc[kQBatch][DPL];
+#pragma unroll
+    for (int j = 0; j < kQBatch; ++j) {
+      mx[j] = warp_max(sc[j]);
+      pr[j] = 0.0f;
+      lsum[j] = 0.0f;
+      if (mx[j] != -INFINITY) {
+        pr[j] = exp2f(sc[j] - mx[j]);
+        lsum[j] = warp_sum(pr[j]);
+      }
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) acc[j][i] = 0.0f;
+    }
+    // value rows in batches of kVB keys: a batch's loads are all issued before any is used
+    for (int jb = 0; jb < 32; jb += kVB) {
+      if (ks + jb > pos_max) break;   // uniform across the warp
+      float vv[kVB][DPL];
+#pragma unroll
+      for (int u = 0; u < kVB; ++u) {
+        const int key = ks + jb + u;
+        const bool shared = key <= pos_max && key < cend_min;
+        if constexpr (DPL == 4) {
+          const float4 f = shared ? __ldg(reinterpret_cast<const float4*>(vcom + static_cast<size_t>(key) * HD) + lane)
+                                  : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          vv[u][0] = f.x; vv[u][1] = f.y; vv[u][2] = f.z; vv[u][3] = f.w;
+        } else {
+          const float2 f = shared ? __ldg(reinterpret_cast<const float2*>(vcom + static_cast<size_t>(key) * HD) + lane)
+                                  : make_float2(0.0f, 0.0f);
+          vv[u][0] = f.x; vv[u][1] = f.y;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kVB; ++u) {
+        const int key = ks + jb + u, jj = jb + u;
+        if (key <= pos_max) {       // uniform across the warp
+          if (key < cend_min) {     // committed for every query: the row loaded above
+#pragma unroll
+            for (int j = 0; j < kQBatch; ++j) {
+              if (j < nb && key <= pos[j]) {
+                const float pk = __shfl_sync(0xffffffffu, pr[j], jj);
+#pragma unroll
+                for (int i = 0; i < DPL; ++i) acc[j][i] = fmaf(pk, vv[u][i], acc[j][i]);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < kQBatch; ++j) {
+              if (j < nb && key <= pos[j]) {
+                const float pk = __shfl_sync(0xffffffffu, pr[j], jj);
+                const float* vr = key_row(j, key, 1) + lane * DPL;
+#pragma unroll
+                for (int i = 0; i < DPL; ++i) acc[j][i] = fmaf(pk, __ldg(vr + i), acc[j][i]);
+              }
             }
           }
         }
       }
-      float* rec = sP + (j * 4 + warp) * PS;
+    }
 #pragma unroll
-      for (int i = 0; i < DPL; ++i) rec[lane * DPL + i] = acc[i];
-      if (lane == 0) {
-        rec[HD] = m;
-        rec[HD + 1] = l;
+    for (int j = 0; j < kQBatch; ++j) {
+      if (j < nb) {
+        float* rec = sP + (j * 4 + warp) * PS;
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) rec[lane * DPL + i] = acc[j][i];
+        if (lane == 0) {
+          rec[HD] = mx[j];
+          rec[HD + 1] = lsum[j];
+        }
       }
     }
     __syncthreads();
@@ -227,14 +289,35 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
   if (tid == 0) a.counters[item.counter * a.KVH + kvh] = 0;
 }
 
-static size_t attn_smem_bytes(int hd) {
-  return static_cast<size_t>(2) * kGroupPos * hd * 4 + kQBatch * hd * 4 + kQBatch * 4 * (hd + 2) * 4;
+static size_t attn_smem_bytes(int hd, int qb) { return static_cast<size_t>(qb) * hd * 4 + qb * 4 * (hd + 2) * 4; }
+
+template <int HD, int QB>
+static cudaError_t launch_attn_variant(cudaLaunchConfig_t cfg, const AttnArgs& a) {
+  static bool set = false;
+  cfg.dynamicSmemBytes = attn_smem_bytes(HD, QB);
+  if (!set) {
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel<HD, QB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(cfg.dynamicSmemBytes));
+    if (e != cudaSuccess) return e;
+    set = true;
+  }
+  return cudaLaunchKernelEx(&cfg, attn_kernel<HD, QB>, a);
 }
 
-cudaError_t launch_attention(const AttnArgs& a, int n_items, int max_groups_launch, cudaStream_t st, bool pdl) {
+template <int HD>
+static cudaError_t launch_attn_hd(const cudaLaunchConfig_t& cfg, const AttnArgs& a, int max_nq) {
+  if (max_nq <= 1) return launch_attn_variant<HD, 1>(cfg, a);
+  if (max_nq <= 2) return launch_attn_variant<HD, 2>(cfg, a);
+  if (max_nq <= 4) return launch_attn_variant<HD, 4>(cfg, a);
+  return launch_attn_variant<HD, 8>(cfg, a);
+}
+
+cudaError_t launch_attention(const AttnArgs& a, int n_items, int max_groups_launch, int max_nq, cudaStream_t st,
+                             bool pdl) {
   if (n_items <= 0) return cudaSuccess;
   if (!a.nodes || !a.items || !a.tails || !a.q || !a.kv_commit || !a.kv_pool || !a.out || !a.part || !a.counters ||
-      !a.err || a.plane_rows < 1 || max_groups_launch < 1 || max_groups_launch > a.max_groups || max_groups_launch > 32)
+      !a.err || a.plane_rows < 1 || max_groups_launch < 1 || max_groups_launch > a.max_groups ||
+      max_groups_launch > 32 || max_nq < 1)
     return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(max_groups_launch), static_cast<unsigned>(a.KVH),
@@ -246,28 +329,8 @@ cudaError_t launch_attention(const AttnArgs& a, int n_items, int max_groups_laun
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  if (a.hd == 128) {
-    cfg.dynamicSmemBytes = attn_smem_bytes(128);
-    static bool set = false;
-    if (!set) {
-      cudaError_t e = cudaFuncSetAttribute(attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(cfg.dynamicSmemBytes));
-      if (e != cudaSuccess) return e;
-      set = true;
-    }
-    return cudaLaunchKernelEx(&cfg, attn_kernel<128>, a);
-  }
-  if (a.hd == 64) {
-    cfg.dynamicSmemBytes = attn_smem_bytes(64);
-    static bool set = false;
-    if (!set) {
-      cudaError_t e = cudaFuncSetAttribute(attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(cfg.dynamicSmemBytes));
-      if (e != cudaSuccess) return e;
-      set = true;
-    }
-    return cudaLaunchKernelEx(&cfg, attn_kernel<64>, a);
-  }
+  if (a.hd == 128) return launch_attn_hd<128>(cfg, a, max_nq);
+  if (a.hd == 64) return launch_attn_hd<64>(cfg, a, max_nq);
   return cudaErrorInvalidValue;
 }
 

@@ -175,7 +175,7 @@ struct Batch {
 // previous round), so their layers may share launches.
 struct Slot {
   std::vector<int> batch;   // batch indices
-  int item0 = 0, n_items = 0, max_groups = 1;
+  int item0 = 0, n_items = 0, max_groups = 1, max_rows = 1;
 };
 
 std::vector<Slot> build_slots(const std::vector<Batch>& batches, RoundTables* t) {
@@ -193,6 +193,7 @@ std::vector<Slot> build_slots(const std::vector<Batch>& batches, RoundTables* t)
         it.layer = b.l0 + j;
         it.counter = sl.n_items++;
         sl.max_groups = std::max(sl.max_groups, it.n_groups);
+        sl.max_rows = std::max(sl.max_rows, it.row_end - it.row_begin);
         t->items.push_back(it);
       }
     }
@@ -364,7 +365,7 @@ int run_layers(dex_handle* h, const Uploaded& u, const std::vector<Batch>& batch
     at.max_groups = h->max_groups;
     at.plane_rows = h->rows_cap;
     at.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(h->hd)));
-    cudaError_t ce = dex::launch_attention(at, sl.n_items, sl.max_groups, h->st, true);
+    cudaError_t ce = dex::launch_attention(at, sl.n_items, sl.max_groups, sl.max_rows * (h->H / h->KVH), h->st, true);
     if (ce != cudaSuccess) return cuda_fail(h, ce);
     h->stats.kernel_launches++;
     // O projection + residual

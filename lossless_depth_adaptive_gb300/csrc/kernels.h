@@ -165,7 +165,9 @@ int gemm_segments(int n_tiles, int kblocks, int n_ctas);
 // Bytes of the segment-partial workspace of a launch with `units` (group, tile, segment)
 // units and node tile nt (none is needed when every tile has one segment).
 inline size_t gemm_partial_bytes(int nt, size_t units) { return units * nt * 128 * 4; }
-cudaError_t launch_attention(const AttnArgs& a, int n_items, int max_groups_launch, cudaStream_t st, bool pdl);
+// max_nq: the largest number of queries (node rows x query heads per KV head) of an item.
+cudaError_t launch_attention(const AttnArgs& a, int n_items, int max_groups_launch, int max_nq, cudaStream_t st,
+                             bool pdl);
 cudaError_t launch_assemble(const AssembleArgs& a, cudaStream_t st, bool pdl);
 cudaError_t launch_collapse(const CollapseArgs& a, cudaStream_t st, bool pdl);
 // bf16 [n][d] rows -> hi/lo pair of h * g ([2][plane_rows][d]) and partial sums of squares
