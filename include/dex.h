@@ -143,7 +143,10 @@ int dex_get_stats(const dex_handle* h, dex_stats* out);
 int dex_reset_stats(dex_handle* h);
 
 /* timing: 0 off; 1 = CUDA events around the expansion / exit+DECS / collapse phases of
- * each round; 2 = also around every linear-layer GEMM launch (adds events). */
+ * each round; 2 = also around every linear-layer GEMM launch (adds events); 3 = level 1
+ * plus per-CTA clock records of the GEMM launches that follow (diagnostics: only when the
+ * environment variable DEX_TIMELINE names a file, which dex_free() writes; the first
+ * DEX_TIMELINE_LAUNCHES launches, default 512, are kept). */
 int dex_set_timing(dex_handle* h, int32_t level);
 
 /* Lattice nodes of the most recent round, in evaluation order: HOST int32

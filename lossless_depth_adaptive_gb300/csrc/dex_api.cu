@@ -119,6 +119,10 @@ struct dex_handle {
   size_t ev_used = 0;
   std::vector<std::pair<cudaEvent_t, cudaEvent_t>> gemm_events;
   bool broken = false;
+  // GEMM timeline diagnostics (timing level 3 with DEX_TIMELINE set)
+  unsigned long long* timeline = nullptr;
+  int tl_cap = 0, tl_used = 0;
+  std::vector<int32_t> tl_meta;   // per launch: epi, n_groups, nt, n_tiles, n_segs, kblocks, n_ctas, rows
 };
 
 namespace {
@@ -269,14 +273,21 @@ int gemm(dex_handle* h, int epi, const CUtensorMap& a0, const CUtensorMap& a1, c
   a.tmem_cols = pow2_at_least(a.nt);
   a.stages = dex::gemm_stages_for(a.nt, h->gemm_smem);
   cudaEvent_t e0 = nullptr, e1 = nullptr;
-  if (h->timing >= 2) {
+  if (h->timing == 2) {
     e0 = next_event(h);
     e1 = next_event(h);
     cudaEventRecord(e0, h->st);
   }
+  if (h->timing == 3 && h->timeline && h->tl_used < h->tl_cap) {
+    a.timeline = h->timeline + static_cast<size_t>(h->tl_used++) * h->gemm_ctas * dex::kTimelineSlots;
+    int rows_all = 0;
+    for (int g = 0; g < a.n_groups; ++g) rows_all += a.groups[g].n;
+    const int32_t meta[8] = {epi, a.n_groups, a.nt, a.n_tiles, a.n_segs, a.kblocks, a.n_ctas, rows_all};
+    h->tl_meta.insert(h->tl_meta.end(), meta, meta + 8);
+  }
   cudaError_t e = dex::launch_gemm(epi, a0, a1, a2, bmaps[a.nt / 16], a, h->st, true);
   if (e != cudaSuccess) return cuda_fail(h, e);
-  if (h->timing >= 2) {
+  if (h->timing == 2) {
     cudaEventRecord(e1, h->st);
     h->gemm_events.push_back({e0, e1});
   }
@@ -616,7 +627,7 @@ int run_round(dex_handle* h, dex::Lattice* lat, std::vector<dex_copy_job>* pendi
     cudaEventElapsedTime(&ms, ev[2], ev[3]);
     h->stats.ms_exit += ms;
   }
-  if (h->timing >= 2) {
+  if (h->timing == 2) {
     for (auto& pr : h->gemm_events) {
       float ms;
       cudaEventElapsedTime(&ms, pr.first, pr.second);
@@ -646,9 +657,27 @@ const char* dex_strerror(int code) {
   }
 }
 
+// Diagnostics file of timing level 3: int64 header {launches, n_ctas, slots}, then int32
+// metadata [launches][8], then the uint64 records [launches][n_ctas][slots].
+static void write_timeline(dex_handle* h) {
+  const char* path = getenv("DEX_TIMELINE");
+  if (!path || !h->timeline || h->tl_used == 0) return;
+  const size_t words = static_cast<size_t>(h->tl_used) * h->gemm_ctas * dex::kTimelineSlots;
+  std::vector<unsigned long long> buf(words);
+  if (cudaMemcpy(buf.data(), h->timeline, words * 8, cudaMemcpyDeviceToHost) != cudaSuccess) return;
+  FILE* f = fopen(path, "wb");
+  if (!f) return;
+  const int64_t hdr[3] = {h->tl_used, h->gemm_ctas, dex::kTimelineSlots};
+  fwrite(hdr, sizeof(hdr), 1, f);
+  fwrite(h->tl_meta.data(), 4, h->tl_meta.size(), f);
+  fwrite(buf.data(), 8, words, f);
+  fclose(f);
+}
+
 void dex_free(dex_handle* h) {
   if (!h) return;
   cudaStreamSynchronize(h->st);
+  write_timeline(h);
   for (void* p : h->allocs) cudaFree(p);
   if (h->h_plan) cudaFreeHost(h->h_plan);
   if (h->h_best) cudaFreeHost(h->h_best);
@@ -1002,7 +1031,13 @@ int dex_reset_stats(dex_handle* h) {
   return DEX_OK;
 }
 int dex_set_timing(dex_handle* h, int32_t level) {
-  if (!h || level < 0 || level > 2) return DEX_EINVAL;
+  if (!h || level < 0 || level > 3) return DEX_EINVAL;
+  if (level == 3 && !h->timeline && getenv("DEX_TIMELINE")) {
+    const char* n = getenv("DEX_TIMELINE_LAUNCHES");
+    h->tl_cap = n ? std::max(1, atoi(n)) : 512;
+    const size_t bytes = static_cast<size_t>(h->tl_cap) * h->gemm_ctas * dex::kTimelineSlots * 8;
+    if (dalloc(h, &h->timeline, bytes) || cudaMemset(h->timeline, 0, bytes) != cudaSuccess) return DEX_ENOMEM;
+  }
   h->timing = level;
   return DEX_OK;
 }

@@ -29,6 +29,13 @@
 // and issues tcgen05.mma; warps 2-5 run the epilogue from TMEM (one accumulator row per
 // thread).  Every wait is bounded and reports a stall through the error flag.
 //
+// Diagnostics: with a.timeline set, epilogue thread 0 of each CTA records its start
+// (globaltimer ns, then clock64), the clock64 at which each unit's accumulator was ready
+// and at which the unit's epilogue finished, a per-unit tag (bit 0: whole tile, bit 1:
+// last arriver that summed the tile, bits 8..15: group, bits 16..31: tile, bits 32..:
+// cycles from accumulator-ready to the arrival count), and at the end the clock64 and
+// the unit count.
+//
 // Epilogues: EPI_QKV (RMSNorm scale, RoPE, K/V into the committed cache or the branch
 // pool), EPI_RESID (residual add into the fp32 hidden state, next layer's bf16 input,
 // RMSNorm partial sums, exit-head input at a stage boundary), EPI_SWIGLU
@@ -331,6 +338,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = wq * 32 + lane;      // accumulator row within the tile
     const int ep = tid - 64;           // 0..127
     const int ndt = a.d / 128;
+    unsigned long long* tl = (a.timeline && ep == 0) ? a.timeline + static_cast<size_t>(cta) * kTimelineSlots : nullptr;
+    if (tl) {
+      tl[0] = global_timer_ns();
+      tl[1] = clock64();
+    }
     griddep_wait();
     int g_inv = -1;                    // group whose RMSNorm scales are in inv[]
 
@@ -475,6 +487,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         g_inv = x.g;
       }
       if (!mbar_wait(&accf[buf], static_cast<uint32_t>(ui >> 1) & 1u, a.err, DEV_TIMEOUT_ACC)) sflag[1] = 1;
+      const bool rec = tl && ui < kTimelineUnits;
+      if (rec) tl[4 + 3 * ui] = clock64();
       named_bar_sync(1, 128);
       if (sflag[1]) break;
       tc_fence_after();
@@ -487,6 +501,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         mbar_arrive(&tfree[buf]);
+        if (rec) {
+          tl[5 + 3 * ui] = clock64();
+          tl[6 + 3 * ui] = 1ull | (static_cast<unsigned long long>(x.g) << 8) |
+                           (static_cast<unsigned long long>(x.t & 0xffff) << 16);
+        }
       } else {
         // segment partial: [unit][row][nt] fp32, a thread's 16 columns are 64 contiguous bytes
         const size_t tile_unit0 = (static_cast<size_t>(x.g) * nT + x.t) * S;   // unit of segment 0
@@ -505,6 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int32_t* counter = a.counters + static_cast<size_t>(x.g) * nT + x.t;
         if (ep == 0) sflag[0] = (atomicAdd(counter, 1) == S - 1) ? 1 : 0;
         named_bar_sync(1, 128);
+        const unsigned long long t_arrived = rec ? clock64() : 0ull;
         if (sflag[0]) {   // last of the tile's segments: sum the partials in segment order
           __threadfence();
           for (int c0 = 0; c0 < n; c0 += 16) {
@@ -524,7 +544,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ep == 0) *counter = 0;
         }
         named_bar_sync(1, 128);
+        if (rec) {
+          tl[5 + 3 * ui] = clock64();
+          tl[6 + 3 * ui] = (sflag[0] ? 2ull : 0ull) | (static_cast<unsigned long long>(x.g) << 8) |
+                           (static_cast<unsigned long long>(x.t & 0xffff) << 16) |
+                           ((t_arrived - tl[4 + 3 * ui]) << 32);
+        }
       }
+    }
+    if (tl) {
+      tl[2] = clock64();
+      tl[3] = static_cast<unsigned long long>(n_units);
     }
   }
 

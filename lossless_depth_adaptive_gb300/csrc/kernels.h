@@ -106,8 +106,12 @@ struct GemmArgs {
   int32_t sample;
   float tau;
   unsigned long long seed;
+  // diagnostics: per-CTA records of kTimelineSlots words, or null (see gemm.cu)
+  unsigned long long* timeline;
   GemmGroup groups[kMaxGroups];
 };
+constexpr int kTimelineUnits = 48;
+constexpr int kTimelineSlots = 4 + 3 * kTimelineUnits;
 
 struct AttnArgs {
   const DevNode* nodes;

@@ -31,6 +31,8 @@ def main():
     ap.add_argument("--tokens", type=int, default=8)
     ap.add_argument("--warmup", type=int, default=1)
     ap.add_argument("--ar", action="store_true", help="profile plain autoregressive rounds")
+    ap.add_argument("--timeline", action="store_true",
+                    help="record per-CTA GEMM clock records of the profiled request (needs DEX_TIMELINE=<file>)")
     a = ap.parse_args()
     wl = di.workload(a.workload)
     shape, X = wl.shape, list(wl.X)
@@ -48,10 +50,13 @@ def main():
         dec.generate(ar=a.ar)
     dec.prefill(0, prompt)
     torch.cuda.synchronize()
+    if a.timeline:
+        dec.set_timing(3)
     torch.cuda.profiler.start()
     toks = dec.generate(ar=a.ar)[0]
     torch.cuda.synchronize()
     torch.cuda.profiler.stop()
+    dec.set_timing(0)
     st = dec.stats()
     dec.close()
     print(f"profiled {a.tokens} tokens ({'AR' if a.ar else 'DEX'}), layers {shape.n_layers}, X {X}: "
