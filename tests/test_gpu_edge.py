@@ -158,3 +158,67 @@ def test_argument_and_state_errors():
         dexlib.Decoder(shape, w, [2, 4, 6], batch=1, max_ctx=64, max_new=8)   # X must end at L
     with pytest.raises(dexlib.DexError):
         dexlib.Decoder(shape, w, X, batch=1, max_ctx=4097, max_new=8)          # above the context cap
+
+
+@pytest.mark.parametrize("sample", [False, True])
+def test_vanilla_lattice_without_decs_matches_oracle(sample):
+    """decs = 0 (every node decoded on its own, section 4's vanilla ablation): still lossless,
+    and every round's nodes, tokens and the round count equal the oracle's Algorithm 1
+    run without DECS."""
+    dexlib = require_gpu()
+    shape, X, T = TINY_UNTIED, [2, 4, 6, 8], 12
+    w = di.gen_weights(shape, 0.3, seed=0, device="cuda")
+    prompt = di.gen_prompts(shape, 1, 24)[0].tolist()
+    dec = dexlib.Decoder(shape, w, X, batch=1, max_ctx=64, max_new=T, sample=sample, tau=0.7, seed=5, decs=False,
+                         debug_logits=True)
+    m = oracle_model(shape, w)
+    rule = odex.Rule(sample=sample, tau=0.7, seed=5)
+    ref = odex.dex_generate(m, prompt, X, T, rule=rule, use_decs=False, keep_logits=True)
+    rounds = {}
+    for nd in ref.nodes:
+        rounds.setdefault(nd.round, {})[nd.node] = nd
+    try:
+        dec.prefill(0, prompt)
+        toks, checked = [], 0
+        for r in range(ref.rounds):
+            tok, nc = dec.step()
+            if nc[0]:
+                toks.append(tok[0])
+            nodes = dec.last_round_nodes()
+            assert sorted(nd["heap"] for nd in nodes) == sorted(rounds[r])
+            for nd in nodes:
+                o = rounds[r][nd["heap"]]
+                if o.margin > 0.1:
+                    assert nd["token"] == o.token
+                    checked += 1
+        assert toks == ref.tokens and checked > 0
+        assert dec.stats()["rounds"] == ref.rounds
+    finally:
+        dec.close()
+
+
+def test_single_exit_variant_and_ten_stages():
+    """X = {d_0, L} (one intermediate exit: the single-exit variant) and |X| = 10 (the
+    largest exploration set) on a 10-layer model: lossless against the library's AR path
+    and the oracle's Algorithm 1 token stream."""
+    dexlib = require_gpu()
+    shape = di.ModelShape(**{**TINY_UNTIED.__dict__, "n_layers": 10})
+    w = di.gen_weights(shape, 0.3, seed=0, device="cuda")
+    prompt = di.gen_prompts(shape, 1, 20)[0].tolist()
+    m = oracle_model(shape, w)
+    for X in ([3, 10], list(range(1, 11))):
+        T = 8
+        out = _run(dexlib, shape, w, X, [prompt], T, 64)
+        ref = odex.dex_generate(m, prompt, X, T)
+        assert out["dex"][0][0] == ref.tokens
+        assert out["dex"][2]["rounds"] == ref.rounds
+
+
+def test_batch_of_sixteen_sequences():
+    """16 independent sequences with different prompt lengths in one handle: each equals
+    its own AR stream bit for bit (greedy)."""
+    dexlib = require_gpu()
+    shape, X, T = TINY_UNTIED, [2, 4, 6, 8], 6
+    w = di.gen_weights(shape, 0.3, seed=0, device="cuda")
+    prompts = [di.gen_prompts(shape, 1, 5 + 3 * b, seed=100 + b)[0].tolist() for b in range(16)]
+    _run(dexlib, shape, w, X, prompts, T, 64)
