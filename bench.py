@@ -148,6 +148,15 @@ def _gemm_traffic_ratio():
         return ratio if hashlib.sha256(f.read()).hexdigest()[:16] == sha else None
 
 
+MODEL_NAMES = {di.LLAMA7B: "llama2-7b-shaped", di.QWEN8B: "qwen3-8b-shaped", di.TINY: "tiny"}
+
+
+def _weight_gb(shape):
+    qd, kvd = shape.n_heads * shape.head_dim, shape.n_kv_heads * shape.head_dim
+    per_layer = (qd + 2 * kvd) * shape.d_model + qd * shape.d_model + 3 * shape.d_ff * shape.d_model
+    return (shape.n_layers * per_layer + shape.vocab * shape.d_model) * 2 / 1e9
+
+
 def _workload(args):
     return di.workload(args.workload, **({"max_new": args.tokens} if args.tokens else {}))
 
@@ -164,15 +173,20 @@ def run_gpu(args):
     wl = _workload(args)
     shape = wl.shape
     w = di.gen_weights(shape, wl.alpha, seed=wl.weight_seed, device="cuda")
-    prompt_cpu = di.gen_prompts(shape, 1, wl.prompt_len, seed=wl.prompt_seed + 1000 * rank)[0]
-    prompt = prompt_cpu.tolist()
+    B = wl.batch   # independent sequences decoded together (one request each)
+    prompts = di.gen_prompts(shape, B, wl.prompt_len, seed=wl.prompt_seed + 1000 * rank).tolist()
+    prompt = prompts[0]
     T = wl.max_new
     max_ctx = wl.prompt_len + T + len(wl.X) + 8
-    dec = dexlib.Decoder(shape, w, wl.X, batch=1, max_ctx=max_ctx, max_new=T, sample=wl.sample, tau=wl.tau,
+    dec = dexlib.Decoder(shape, w, wl.X, batch=B, max_ctx=max_ctx, max_new=T, sample=wl.sample, tau=wl.tau,
                          seed=wl.gumbel_seed, decs=wl.decs)
     st = torch.cuda.current_stream()
     import ctypes as C
-    out_host = (C.c_int32 * T)()
+    out_host = (C.c_int32 * (B * T))()
+
+    def prefill_all():
+        for b in range(B):
+            dec.prefill(b, prompts[b])
 
     dev = torch.device("cuda", local)
 
@@ -185,7 +199,7 @@ def run_gpu(args):
 
     # warm-up requests
     for _ in range(args.warmup):
-        dec.prefill(0, prompt)
+        prefill_all()
         dec.generate(out=out_host)
     # ---- device-timed decode (value) ----
     dec.reset_stats()
@@ -194,10 +208,10 @@ def run_gpu(args):
     tokens_ref = None
     with ClockSampler(local) as clk:
         for _ in range(args.steps):
-            dec.prefill(0, prompt)
+            prefill_all()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(st)
-            toks = dec.generate(out=out_host)[0]
+            toks = dec.generate(out=out_host)
             e1.record(st)
             e1.synchronize()
             ms += e0.elapsed_time(e1)
@@ -207,7 +221,7 @@ def run_gpu(args):
     barrier()
     stats = dec.stats()
     launches = stats["kernel_launches"]
-    value = replica_throughput(args.steps * T, ms / 1000.0, world, dev)
+    value = replica_throughput(args.steps * B * T, ms / 1000.0, world, dev)
     ms = max_over_ranks(ms)
     ms_per_step = ms / args.steps
     # ---- end to end through the C ABI with host buffers (e2e) ----
@@ -215,10 +229,10 @@ def run_gpu(args):
     barrier()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        dec.prefill(0, prompt)               # host prompt -> device inside
+        prefill_all()                        # host prompts -> device inside
         dec.generate(out=out_host)           # tokens -> host inside
     barrier()
-    e2e_value = replica_throughput(args.steps * T, time.perf_counter() - t0, world, dev)
+    e2e_value = replica_throughput(args.steps * B * T, time.perf_counter() - t0, world, dev)
     st_e2e = dec.stats()
     e2e = {"value": e2e_value, "unit": "tokens/s",
            "h2d_bytes_per_step": int(st_e2e["h2d_bytes"] / args.steps),
@@ -226,7 +240,7 @@ def run_gpu(args):
     # ---- one instrumented request: per-GEMM events and phase split ----
     dec.set_timing(2)
     dec.reset_stats()
-    dec.prefill(0, prompt)
+    prefill_all()
     dec.reset_stats()
     dec.generate(out=out_host)
     inst = dec.stats()
@@ -253,10 +267,10 @@ def run_gpu(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded weights and uniform-random prompt ids)",
-        "config": {"workload": wl.name, "model": "llama2-7b-shaped", "X": wl.X, "alpha": wl.alpha,
-                   "global_batch": world, "prompt_len": wl.prompt_len, "new_tokens": T,
+        "config": {"workload": wl.name, "model": MODEL_NAMES.get(wl.shape, "decoder"), "X": wl.X, "alpha": wl.alpha,
+                   "global_batch": world * B, "prompt_len": wl.prompt_len, "new_tokens": T,
                    "decode": "sample" if wl.sample else "greedy", "parallelism": f"replicas{world}",
-                   "l2": "weights 13.5 GB streamed per round >> 129 MB L2; no flush"},
+                   "l2": f"weights {_weight_gb(wl.shape):.1f} GB streamed per round >> 129 MB L2; no flush"},
         "layers_per_token": {k: (round(v, 3) if isinstance(v, float) else v) for k, v in layers.items()},
         "step_roofline": step_roof,
         "phase_ms_per_round": {k: round(v, 4) for k, v in phases.items()},
@@ -279,6 +293,90 @@ def run_gpu(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def run_micro(args):
+    """Exit head + DECS and the KV collapse in isolation (the kernel micro-benchmark shapes):
+    64 lattice nodes (8 slot chains x 8 depths, 0-7 masked priors each, sampled with shared
+    Gumbel rows) against a 128256 x 4096 bf16 LM head; 6 surviving branch positions copied
+    into a 32-layer x 8-KV-head x 128 bf16 cache at context 4096."""
+    import torch
+    import lossless_depth_adaptive_gb300 as dexlib
+    torch.cuda.set_device(_dist()[2])
+    m = di.ExitMicro()
+    h, w = di.gen_exit_micro(m, device="cuda")
+    n, d, V = m.n_slots * m.depth, m.d_model, m.vocab
+    g = torch.ones(d, dtype=torch.bfloat16, device="cuda")
+    ids = di.uniform_ids(n * m.depth, V, m.seed, 7).tolist()
+    nodes, priors = [], []
+    for sl in range(m.n_slots):
+        for k in range(m.depth):
+            unmasked = 1 if k == m.depth - 1 else 0
+            pr = [] if unmasked else ids[(sl * m.depth + k) * m.depth:][:k]
+            nodes.append((sl, 1000 + sl, unmasked, len(priors), len(pr)))
+            priors += pr
+    nodes_t = torch.tensor(nodes, dtype=torch.int32, device="cuda")
+    priors_t = torch.tensor(priors + [0], dtype=torch.int32, device="cuda")
+    tokens = torch.empty(n, dtype=torch.int32, device="cuda")
+    st = torch.cuda.current_stream()
+
+    def exit_call():
+        dexlib.dex_exit_head_decs(h.data_ptr(), n, d, g.data_ptr(), 1e-5, w.data_ptr(), V, nodes_t.data_ptr(),
+                                  priors_t.data_ptr(), 1, 0.7, 2, tokens.data_ptr(), 0, st.cuda_stream)
+
+    def exit_call_noalloc():
+        dexlib.dex_exit_head_decs_noalloc(h.data_ptr(), n, d, g.data_ptr(), 1e-5, w.data_ptr(), V,
+                                          nodes_t.data_ptr(), priors_t.data_ptr(), 1, 0.7, 2, tokens.data_ptr(),
+                                          0, st.cuda_stream)
+
+    cm = di.CollapseMicro()
+    S = 8
+    committed = torch.zeros((1, cm.n_layers, 2, cm.n_kv_heads, cm.ctx, cm.head_dim), dtype=torch.bfloat16,
+                            device="cuda")
+    pool = torch.ones((1, S, cm.n_layers, 2, cm.n_kv_heads, cm.head_dim), dtype=torch.bfloat16, device="cuda")
+    jobs = torch.tensor([(0, j, cm.ctx - 1 - 7 * j, cm.n_layers) for j in range(cm.n_positions)], dtype=torch.int32,
+                        device="cuda")
+    geom = dexlib.dex_kv_geom(1, cm.n_layers, cm.n_kv_heads, cm.head_dim, cm.ctx, S)
+
+    def collapse_call():
+        dexlib.dex_kv_collapse(committed.data_ptr(), pool.data_ptr(), geom, jobs.data_ptr(), cm.n_positions,
+                               st.cuda_stream)
+
+    def timed(fn, reps):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(reps):
+            fn()
+        e1.record(st)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / reps * 1e3   # us
+
+    hbm, _, src = _peaks()
+    with ClockSampler(_dist()[2]) as clk:
+        t_exit = timed(exit_call, max(10, args.steps * 10))
+        t_exit_na = timed(exit_call_noalloc, max(10, args.steps * 10))
+        t_col = timed(collapse_call, max(10, args.steps * 10))
+    exit_bytes = V * d * 2 + n * d * 2 + len(priors) * 4
+    col_bytes = 2 * cm.n_positions * cm.n_layers * 2 * cm.n_kv_heads * cm.head_dim * 2
+    line = {"metric": "exit head + DECS (64 nodes, LM head 128256 x 4096 bf16) and KV collapse "
+                      "(6 positions, 32 layers x 8 KV heads x 128, context 4096), isolated",
+            "value": round(exit_bytes / (t_exit * 1e-6) / 1e9, 1), "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "dtype": "bf16",
+            "data": "synthetic", "config": {"workload": "micro", "nodes": n, "vocab": V, "d_model": d,
+                                            "sample": True, "collapse_positions": cm.n_positions},
+            "exit_head": {"us_per_call": round(t_exit, 2), "bytes": exit_bytes,
+                          "frac_of_hbm": round(exit_bytes / (t_exit * 1e-6) / 1e9 / hbm, 4), "peak_source": src,
+                          "grid": "2 CTAs per SM"},
+            "exit_head_noalloc": {"us_per_call": round(t_exit_na, 2),
+                                  "frac_of_hbm": round(exit_bytes / (t_exit_na * 1e-6) / 1e9 / hbm, 4),
+                                  "grid": "1 CTA per SM (fixed 32 MiB scratch)"},
+            "collapse": {"us_per_call": round(t_col, 2), "bytes_moved": col_bytes,
+                         "gbs": round(col_bytes / (t_col * 1e-6) / 1e9, 2)},
+            "clocks": clk.summary()}
+    print(json.dumps(line))
 
 
 def _oracle_for(wl, w_gpu):
@@ -342,7 +440,8 @@ def main():
     ap.add_argument("--steps", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["dex", "reference"], default="dex")
-    ap.add_argument("--workload", default="llama7b_x4", choices=sorted(di.WORKLOADS))
+    ap.add_argument("--workload", default="llama7b_x4", choices=sorted(di.WORKLOADS) + ["micro"],
+                    help="micro: exit head + DECS and KV collapse in isolation")
     ap.add_argument("--tokens", type=int, default=0, help="override the new-token count")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -350,6 +449,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "micro":
+        run_micro(args)
     else:
         run_gpu(args)
 

@@ -1110,7 +1110,8 @@ int dex_exit_head_decs(const void* hidden, int32_t n, int32_t d, const void* fin
   const size_t o_cnt = o_nodes + up(static_cast<size_t>(n) * sizeof(dex::DevNode));
   const size_t o_err = o_cnt + up(static_cast<size_t>(n_tiles) * 4);
   const size_t o_part = o_err + 256;
-  const int segs = dex::gemm_segments(n_tiles, kb, n_sm);
+  const int ctas = 2 * n_sm;   // two CTAs per SM, as in the decoder (104 KB shared memory each)
+  const int segs = dex::gemm_segments(n_tiles, kb, ctas);
   const size_t total = o_part + (segs > 1 ? dex::gemm_partial_bytes(nt, static_cast<size_t>(n_tiles) * segs) : 256);
   uint8_t* scratch = nullptr;
   if (cudaMallocAsync(reinterpret_cast<void**>(&scratch), total, st) != cudaSuccess) return DEX_ENOMEM;
@@ -1131,13 +1132,13 @@ int dex_exit_head_decs(const void* hidden, int32_t n, int32_t d, const void* fin
     exit_nodes_kernel<<<(n + 127) / 128, 128, 0, st>>>(nodes, n, dn);
     dex::GemmArgs a = {};
     a.n_groups = 1;
-    a.n_ctas = n_sm;
+    a.n_ctas = ctas;
     a.n_segs = segs;
     a.groups[0].n = n;
     a.groups[0].b_row0 = 0;
     a.nt = nt;
     a.kblocks = kb;
-    a.stages = dex::gemm_stages_for(nt, 200 * 1024);   // one CTA per SM: a deeper ring
+    a.stages = dex::gemm_stages_for(nt);
     a.n_tiles = n_tiles;
     a.src_tiles0 = n_tiles;
     a.tmem_cols = pow2_at_least(nt);

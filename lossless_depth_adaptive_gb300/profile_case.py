@@ -42,13 +42,18 @@ def main():
         shape = di.ModelShape(**{**shape.__dict__, "n_layers": a.layers})
         X = [a.layers // N * (k + 1) for k in range(N)]
     w = di.gen_weights(shape, wl.alpha, seed=wl.weight_seed, device="cuda")
-    prompt = di.gen_prompts(shape, 1, wl.prompt_len, seed=wl.prompt_seed)[0].tolist()
-    dec = dexlib.Decoder(shape, w, X, batch=1, max_ctx=wl.prompt_len + a.tokens + len(X) + 8,
+    prompts = di.gen_prompts(shape, wl.batch, wl.prompt_len, seed=wl.prompt_seed).tolist()
+    dec = dexlib.Decoder(shape, w, X, batch=wl.batch, max_ctx=wl.prompt_len + a.tokens + len(X) + 8,
                          max_new=a.tokens, sample=wl.sample, tau=wl.tau, seed=wl.gumbel_seed, decs=wl.decs)
+
+    def prefill_all():
+        for b, p in enumerate(prompts):
+            dec.prefill(b, p)
+
     for _ in range(a.warmup):
-        dec.prefill(0, prompt)
+        prefill_all()
         dec.generate(ar=a.ar)
-    dec.prefill(0, prompt)
+    prefill_all()
     torch.cuda.synchronize()
     if a.timeline:
         dec.set_timing(3)
