@@ -278,8 +278,16 @@ class DEXResult:
 
 
 def dex_generate(model, prompt: Sequence[int], X: Sequence[int], T: int, rule: Rule = Rule(),
-                 use_decs: bool = True, seq: int = 0, keep_logits: bool = False) -> DEXResult:
-    """Algorithm 1 over one sequence; returns the committed tokens Y and a full trace."""
+                 use_decs: bool = True, seq: int = 0, keep_logits: bool = False,
+                 max_branch: int = 0) -> DEXResult:
+    """Algorithm 1 over one sequence; returns the committed tokens Y and a full trace.
+
+    max_branch > 0 builds a sparse lattice (the pruning of low-value branches that the
+    paper's discussion of expansion growth proposes, with the final-depth commit kept): a
+    node exists only if its parent does and its path holds at most max_branch position
+    moves, i.e. it speculates at most that many tokens ahead of the commit.  The anchor
+    chain has none and always exists, so the committed stream is unchanged.
+    """
     N = len(X)
     assert X[-1] == model.L and list(X) == sorted(set(X))
     P = len(prompt)
@@ -300,7 +308,12 @@ def dex_generate(model, prompt: Sequence[int], X: Sequence[int], T: int, rule: R
         p_c = len(committed)
         # expand: H_q = hidden states of the level-q nodes at their stage boundaries
         H = {}
-        for i in level_nodes(q):
+        # a node exists when its parent does (after a collapse the re-rooted subtree may
+        # lack branches pruned in the old frame) and, with a cap, its path speculates at
+        # most max_branch tokens ahead
+        live = [i for i in level_nodes(q)
+                if (i == 0 or parent(i) in B) and (max_branch <= 0 or len(branch_parents(i)) <= max_branch)]
+        for i in live:
             s = stage(i)
             path = branch_parents(i)
             if not path:                                  # anchor path: committed prefix
@@ -314,7 +327,7 @@ def dex_generate(model, prompt: Sequence[int], X: Sequence[int], T: int, rule: R
         rounds_since_commit += 1
         # DECS, then insert into the explore buffer
         Z = {}
-        for i in level_nodes(q):
+        for i in live:
             z = model.exit_logits(H[i])[0]
             plen = len(branch_parents(i))
             y, mg, masked = decs(z, i, dict(B), q, q_max, i_ref, rule, seq, p_c + plen,

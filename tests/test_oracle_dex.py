@@ -133,3 +133,47 @@ def test_degenerate_tiny_repeats_last_token():
     _, ar, r = _run(0.1, True, [2, 4, 6, 8], 12, dex.Rule())
     assert set(ar.tokens) == {PROMPT[-1]}
     assert all(c.kstar == 0 for c in r.commits)
+
+
+# ---- sparse lattice (speculation cap) -------------------------------------------------------
+
+@pytest.mark.parametrize("X", [[2, 4, 6, 8], [1, 2, 3, 4, 5, 6, 7, 8]])
+@pytest.mark.parametrize("cap", [1, 2, 3])
+def test_sparse_lattice_is_lossless(X, cap):
+    """Pruned branches never carry the commit: the stream equals plain AR for any cap."""
+    shape, w, m = tiny_model(alpha=1.0, tied=False)
+    prompt = di.gen_prompts(shape, 1, 16)[0].tolist()
+    ar = dex.ar_generate(m, prompt, 12)
+    r = dex.dex_generate(m, prompt, X, 12, max_branch=cap)
+    assert r.tokens == ar.tokens
+    for nd in r.nodes:   # every node respects the cap
+        assert nd.plen <= cap
+
+
+def test_sparse_lattice_with_cap_at_least_n_minus_1_is_the_full_lattice():
+    """plen <= q <= N-1 always, so a cap of N-1 prunes nothing: same nodes, same rounds."""
+    shape, w, m = tiny_model(alpha=0.3, tied=False)
+    prompt = di.gen_prompts(shape, 1, 16)[0].tolist()
+    X = [2, 4, 6, 8]
+    full = dex.dex_generate(m, prompt, X, 10)
+    capped = dex.dex_generate(m, prompt, X, 10, max_branch=len(X) - 1)
+    assert full.tokens == capped.tokens and full.rounds == capped.rounds
+    assert [(n.round, n.node, n.token) for n in full.nodes] == [(n.round, n.node, n.token) for n in capped.nodes]
+
+
+@pytest.mark.parametrize("cap", [1, 2])
+def test_sparse_lattice_first_cycle_counts(cap):
+    """Before the first commit the lattice is fresh: the level-q round holds the paths of q
+    moves with at most `cap` position moves, sum_{p <= cap} C(q, p) nodes (counted here by
+    brute force over move strings)."""
+    from itertools import product
+    shape, w, m = tiny_model(alpha=0.3, tied=False)
+    prompt = di.gen_prompts(shape, 1, 16)[0].tolist()
+    X = [1, 2, 3, 4, 5, 6, 7, 8]
+    r = dex.dex_generate(m, prompt, X, 1, max_branch=cap)
+    per_round = {}
+    for nd in r.nodes:
+        per_round[nd.round] = per_round.get(nd.round, 0) + 1
+    for q in range(len(X)):
+        brute = sum(1 for moves in product("DP", repeat=q) if moves.count("P") <= cap)
+        assert per_round[q] == brute, (q, per_round[q], brute)
