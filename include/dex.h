@@ -82,6 +82,9 @@ typedef struct dex_decode_cfg {
   uint64_t seed;
   int32_t decs;
   int32_t debug_logits;
+  int32_t max_branch;   /* 0: the full lattice; k > 0: a sparse lattice whose nodes speculate at
+                           most k tokens ahead of the commit (k position moves on their path;
+                           the final-depth commit, hence the token stream, is unchanged) */
 } dex_decode_cfg;
 
 typedef struct dex_handle dex_handle;
@@ -242,7 +245,8 @@ typedef struct dex_plan_node {
 
 typedef struct dex_lattice dex_lattice;
 
-int dex_lattice_new(const int32_t* X, int32_t n_X, int32_t batch, int32_t decs, dex_lattice** out);
+int dex_lattice_new(const int32_t* X, int32_t n_X, int32_t batch, int32_t decs, int32_t max_branch,
+                    dex_lattice** out);
 /* Start sequence seq with p_c committed tokens, last_token at position p_c - 1. */
 int dex_lattice_start(dex_lattice* lat, int32_t seq, int32_t p_c, int32_t last_token);
 /* Nodes of the next round (level q of each active sequence), grouped by stage. */

@@ -44,7 +44,7 @@ class dex_model(C.Structure):
 class dex_decode_cfg(C.Structure):
     _fields_ = [("batch", C.c_int32), ("max_ctx", C.c_int32), ("max_new", C.c_int32),
                 ("sample", C.c_int32), ("tau", C.c_float), ("seed", C.c_uint64),
-                ("decs", C.c_int32), ("debug_logits", C.c_int32)]
+                ("decs", C.c_int32), ("debug_logits", C.c_int32), ("max_branch", C.c_int32)]
 
 
 class dex_stats(C.Structure):
@@ -107,7 +107,7 @@ SIGNATURES = {
     "dex_exit_head_decs_noalloc": (C.c_int, [P, C.c_int32, C.c_int32, P, C.c_float, P, C.c_int32, P, P,
                                              C.c_int32, C.c_float, C.c_uint64, P, P, P]),
     "dex_kv_collapse": (C.c_int, [P, P, C.POINTER(dex_kv_geom), P, C.c_int32, P]),
-    "dex_lattice_new": (C.c_int, [I32P, C.c_int32, C.c_int32, C.c_int32, C.POINTER(P)]),
+    "dex_lattice_new": (C.c_int, [I32P, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.POINTER(P)]),
     "dex_lattice_start": (C.c_int, [P, C.c_int32, C.c_int32, C.c_int32]),
     "dex_lattice_plan": (C.c_int, [P, C.POINTER(dex_plan_node), C.c_int32, I32P]),
     "dex_lattice_update": (C.c_int, [P, I32P, I32P, I32P, C.POINTER(dex_copy_job), C.c_int32, I32P]),
@@ -274,11 +274,12 @@ class Decoder:
 
     def __init__(self, shape, weights: Dict, X: Sequence[int], batch: int, max_ctx: int, max_new: int,
                  sample: bool = False, tau: float = 1.0, seed: int = 0, decs: bool = True,
-                 debug_logits: bool = False, stream: Optional[int] = None):
+                 debug_logits: bool = False, stream: Optional[int] = None, max_branch: int = 0):
         import torch
         self.shape, self.X, self.batch, self.max_new = shape, list(X), batch, max_new
         self.ref = ModelRef(shape, weights)
-        cfg = dex_decode_cfg(batch, max_ctx, max_new, int(sample), tau, seed, int(decs), int(debug_logits))
+        cfg = dex_decode_cfg(batch, max_ctx, max_new, int(sample), tau, seed, int(decs), int(debug_logits),
+                             int(max_branch))
         self.stream = torch.cuda.current_stream().cuda_stream if stream is None else stream
         self.h = dex_init(self.ref.model, self.X, cfg, self.stream)
 
@@ -321,10 +322,11 @@ class Decoder:
 class Lattice:
     """Host-only lattice scheduler (the library's FSM), usable without a GPU."""
 
-    def __init__(self, X: Sequence[int], batch: int, decs: bool = True):
+    def __init__(self, X: Sequence[int], batch: int, decs: bool = True, max_branch: int = 0):
         self.h = C.c_void_p()
         self.batch = batch
-        check(lib().dex_lattice_new(i32(X), len(X), batch, int(decs), C.byref(self.h)), "dex_lattice_new")
+        check(lib().dex_lattice_new(i32(X), len(X), batch, int(decs), int(max_branch), C.byref(self.h)),
+              "dex_lattice_new")
         self.cap = batch << (len(X) - 1)
 
     def start(self, seq: int, p_c: int, last_token: int) -> None:

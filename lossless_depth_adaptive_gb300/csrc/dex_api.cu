@@ -696,7 +696,8 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
   if (n_X < 1 || n_X > 10 || X[n_X - 1] != m->n_layers) return DEX_EINVAL;
   for (int i = 0; i < n_X; ++i)
     if (X[i] < 1 || (i > 0 && X[i] <= X[i - 1])) return DEX_EINVAL;
-  if (cfg->batch < 1 || cfg->batch > 64 || cfg->max_ctx < 2 || cfg->max_ctx > 4096 || cfg->max_new < 1 || (cfg->sample && !(cfg->tau > 0)))
+  if (cfg->batch < 1 || cfg->batch > 64 || cfg->max_ctx < 2 || cfg->max_ctx > 4096 || cfg->max_new < 1 ||
+      (cfg->sample && !(cfg->tau > 0)) || cfg->max_branch < 0)
     return DEX_EINVAL;
   int dev = 0;
   cudaDeviceProp prop;
@@ -740,7 +741,7 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
     h->gemm_ctas = h->n_sm * cps;
     h->gemm_smem = static_cast<size_t>(kb) * 1024;
   }
-  h->lat.reset(new dex::Lattice(X, n_X, cfg->batch, cfg->decs != 0));
+  h->lat.reset(new dex::Lattice(X, n_X, cfg->batch, cfg->decs != 0, cfg->max_branch));
   const int32_t XL[1] = {h->L};
   h->lat_ar.reset(new dex::Lattice(XL, 1, cfg->batch, false));
   h->mode.assign(cfg->batch, 0);

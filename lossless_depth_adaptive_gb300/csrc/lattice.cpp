@@ -6,8 +6,8 @@
 
 namespace dex {
 
-Lattice::Lattice(const int32_t* X, int n_X, int batch, bool decs)
-    : N_(n_X), n_slots_(1 << (n_X - 1)), X_(X, X + n_X), decs_(decs), seqs_(batch) {
+Lattice::Lattice(const int32_t* X, int n_X, int batch, bool decs, int max_branch)
+    : N_(n_X), n_slots_(1 << (n_X - 1)), X_(X, X + n_X), decs_(decs), max_branch_(max_branch), seqs_(batch) {
   for (auto& s : seqs_) {
     s.B.assign((1 << N_) - 1, -1);
     s.slot.assign((1 << N_) - 1, -1);
@@ -51,16 +51,18 @@ int Lattice::plan(std::vector<dex_plan_node>* out) {
       const int lo = (1 << s.q) - 1, hi = (1 << (s.q + 1)) - 1;
       for (int i = lo; i < hi; ++i) {
         if (node_stage(i) != st) continue;
-        dex_plan_node nd = {};
-        nd.seq = b;
-        nd.heap = i;
-        nd.stage = st;
+        if (i > 0 && s.B[heap_parent(i)] < 0) continue;   // parent pruned (or never planned)
         // P-children on the path root -> i, root first (each adds one branch position)
         int pc[32];
         int npc = 0;
         for (int j = i; j > 0; j = heap_parent(j))
           if ((j & 1) == 0) pc[npc++] = j;
         std::reverse(pc, pc + npc);
+        if (max_branch_ > 0 && npc > max_branch_) continue;   // sparse lattice: speculates too far ahead
+        dex_plan_node nd = {};
+        nd.seq = b;
+        nd.heap = i;
+        nd.stage = st;
         nd.plen = npc;
         nd.pos = s.p_c - 1 + npc;
         nd.c_end = s.p_c;
@@ -122,7 +124,7 @@ int Lattice::update(const std::vector<dex_plan_node>& plan, const int32_t* token
     std::vector<int32_t> nB(s.B.size(), -1), nslot(s.slot.size(), -1);
     std::vector<char> keep(n_slots_, 0);
     int new_q = 0;
-    if (ks < N_ - 1) {
+    if (ks < N_ - 1 && s.B[1 << (ks + 1)] >= 0) {   // (a sparse lattice may lack m: then nothing survives)
       const int m = 1 << (ks + 1);
       const int lm = heap_level(m);
       for (int i = 0; i < static_cast<int>(s.B.size()); ++i) {
@@ -166,16 +168,17 @@ int Lattice::update(const std::vector<dex_plan_node>& plan, const int32_t* token
 struct dex_lattice {
   dex::Lattice lat;
   std::vector<dex_plan_node> plan;
-  dex_lattice(const int32_t* X, int n, int b, bool d) : lat(X, n, b, d) {}
+  dex_lattice(const int32_t* X, int n, int b, bool d, int mb) : lat(X, n, b, d, mb) {}
 };
 
 extern "C" {
 
-int dex_lattice_new(const int32_t* X, int32_t n_X, int32_t batch, int32_t decs, dex_lattice** out) {
-  if (!X || !out || n_X < 1 || n_X > 10 || batch < 1 || batch > 64) return DEX_EINVAL;
+int dex_lattice_new(const int32_t* X, int32_t n_X, int32_t batch, int32_t decs, int32_t max_branch,
+                    dex_lattice** out) {
+  if (!X || !out || n_X < 1 || n_X > 10 || batch < 1 || batch > 64 || max_branch < 0) return DEX_EINVAL;
   for (int i = 0; i < n_X; ++i)
     if (X[i] < 1 || (i > 0 && X[i] <= X[i - 1])) return DEX_EINVAL;
-  dex_lattice* l = new (std::nothrow) dex_lattice(X, n_X, batch, decs != 0);
+  dex_lattice* l = new (std::nothrow) dex_lattice(X, n_X, batch, decs != 0, max_branch);
   if (!l) return DEX_ENOMEM;
   *out = l;
   return DEX_OK;

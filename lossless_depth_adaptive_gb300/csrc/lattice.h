@@ -54,7 +54,9 @@ struct LatticeSeq {
 
 class Lattice {
  public:
-  Lattice(const int32_t* X, int n_X, int batch, bool decs);
+  // max_branch > 0: sparse lattice -- a node is planned only when its parent exists and its
+  // path holds at most max_branch position moves (the anchor chain always qualifies).
+  Lattice(const int32_t* X, int n_X, int batch, bool decs, int max_branch = 0);
   int N() const { return N_; }
   int n_slots() const { return n_slots_; }
   int batch() const { return static_cast<int>(seqs_.size()); }
@@ -80,6 +82,7 @@ class Lattice {
   int N_, n_slots_;
   std::vector<int> X_;
   bool decs_;
+  int max_branch_;
   std::vector<LatticeSeq> seqs_;
 };
 

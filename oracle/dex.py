@@ -366,11 +366,14 @@ def collapse(B: Dict[int, int], N: int, kstar: int) -> Tuple[Dict[int, int], int
     """Keep the nodes whose prefix is the new committed prefix; return (B', q').
 
     The survivors are the subtree of m = P(b_{k*}); every other node's prefix contains a
-    rejected candidate.  With the fallback branch (k* = N-1) nothing survives.
+    rejected candidate.  With the fallback branch (k* = N-1) nothing survives, and neither
+    when a sparse lattice never materialised m.
     """
     if kstar == N - 1:
         return {}, 0
     m = position_child(anchor_node(kstar))
+    if m not in B:   # sparse lattice: the new root was pruned, nothing to reuse
+        return {}, 0
     remap = subtree_remap(m, N - 1)
     newB = {new: B[old] for old, new in remap.items() if old in B}
     return newB, N - kstar - 1

@@ -44,20 +44,21 @@ def test_strerror_and_bad_arguments():
     h = C.c_void_p()
     assert L.dex_init(None, None, 0, None, None, C.byref(h)) == dexlib.DEX_EINVAL
     lat = C.c_void_p()
-    assert L.dex_lattice_new(dexlib.i32([4, 2]), 2, 1, 1, C.byref(lat)) == dexlib.DEX_EINVAL   # not increasing
-    assert L.dex_lattice_new(dexlib.i32([4]), 1, 0, 1, C.byref(lat)) == dexlib.DEX_EINVAL      # batch 0
+    assert L.dex_lattice_new(dexlib.i32([4, 2]), 2, 1, 1, 0, C.byref(lat)) == dexlib.DEX_EINVAL   # not increasing
+    assert L.dex_lattice_new(dexlib.i32([4]), 1, 0, 1, 0, C.byref(lat)) == dexlib.DEX_EINVAL      # batch 0
+    assert L.dex_lattice_new(dexlib.i32([4]), 1, 1, 1, -1, C.byref(lat)) == dexlib.DEX_EINVAL     # negative cap
     assert L.dex_exit_head_decs(None, 1, 128, None, 1e-5, None, 10, None, None, 0, 1.0, 0, None, None,
                                 None) == dexlib.DEX_EINVAL
 
 
-def _drive_lattice_with_oracle(X, alpha, tied, sample, use_decs, T=12):
+def _drive_lattice_with_oracle(X, alpha, tied, sample, use_decs, T=12, max_branch=0):
     _lib()
     _, _, m = tiny_model(alpha, tied)
     prompt = di.gen_prompts(di.TINY, 1, 32)[0].tolist()
     rule = odex.Rule(sample=sample, tau=0.7, seed=3)
-    ref = odex.dex_generate(m, prompt, X, T, rule=rule, use_decs=use_decs)
+    ref = odex.dex_generate(m, prompt, X, T, rule=rule, use_decs=use_decs, max_branch=max_branch)
     N = len(X)
-    lat = dexlib.Lattice(X, 1, use_decs)
+    lat = dexlib.Lattice(X, 1, use_decs, max_branch)
     lat.start(0, len(prompt), prompt[-1])
     rounds = {}
     by_heap_prev = {}
@@ -99,11 +100,12 @@ def _drive_lattice_with_oracle(X, alpha, tied, sample, use_decs, T=12):
             c = next(commits)
             last = c.token
             assert (committed[0], kstar[0]) == (c.token, c.kstar)
-            if c.kstar < N - 1:       # survivors re-indexed: i -> i - m 2^h
-                remap = odex.subtree_remap(odex.position_child(odex.anchor_node(c.kstar)), N - 1)
+            m_root = odex.position_child(odex.anchor_node(c.kstar)) if c.kstar < N - 1 else None
+            if m_root is not None and m_root in by_heap_prev:   # survivors re-indexed: i -> i - m 2^h
+                remap = odex.subtree_remap(m_root, N - 1)
                 by_heap_prev = {remap[o]: t for o, t in by_heap_prev.items() if o in remap}
                 assert jobs == [(0, jobs[0][1], p_c, X[N - c.kstar - 2])]
-            else:
+            else:   # fallback, or a sparse lattice that never materialised m: nothing survives
                 by_heap_prev = {}
                 assert jobs == []
             p_c += 1
@@ -116,6 +118,14 @@ def _drive_lattice_with_oracle(X, alpha, tied, sample, use_decs, T=12):
 @pytest.mark.parametrize("alpha,tied", [(0.3, False), (1.0, False)])
 def test_lattice_scheduler_matches_oracle(X, alpha, tied):
     _drive_lattice_with_oracle(X, alpha, tied, sample=False, use_decs=True)
+
+
+@pytest.mark.parametrize("X", [[2, 4, 6, 8], [1, 2, 3, 4, 5, 6, 7, 8]])
+@pytest.mark.parametrize("cap", [1, 2])
+def test_sparse_lattice_scheduler_matches_oracle(X, cap):
+    """The speculation-capped lattice plans exactly the oracle's nodes, commits and collapses."""
+    _drive_lattice_with_oracle(X, 1.0, False, sample=False, use_decs=True, max_branch=cap)
+    _drive_lattice_with_oracle(X, 0.3, False, sample=True, use_decs=True, max_branch=cap)
 
 
 def test_lattice_scheduler_sampled_and_vanilla():
