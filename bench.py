@@ -179,7 +179,7 @@ def run_gpu(args):
     T = wl.max_new
     max_ctx = wl.prompt_len + T + len(wl.X) + 8
     dec = dexlib.Decoder(shape, w, wl.X, batch=B, max_ctx=max_ctx, max_new=T, sample=wl.sample, tau=wl.tau,
-                         seed=wl.gumbel_seed, decs=wl.decs)
+                         seed=wl.gumbel_seed, decs=wl.decs, max_branch=args.max_branch)
     st = torch.cuda.current_stream()
     import ctypes as C
     out_host = (C.c_int32 * (B * T))()
@@ -270,6 +270,7 @@ def run_gpu(args):
         "config": {"workload": wl.name, "model": MODEL_NAMES.get(wl.shape, "decoder"), "X": wl.X, "alpha": wl.alpha,
                    "global_batch": world * B, "prompt_len": wl.prompt_len, "new_tokens": T,
                    "decode": "sample" if wl.sample else "greedy", "parallelism": f"replicas{world}",
+                   "max_branch": args.max_branch,
                    "l2": f"weights {_weight_gb(wl.shape):.1f} GB streamed per round >> 129 MB L2; no flush"},
         "layers_per_token": {k: (round(v, 3) if isinstance(v, float) else v) for k, v in layers.items()},
         "step_roofline": step_roof,
@@ -444,6 +445,8 @@ def main():
                     help="micro: exit head + DECS and KV collapse in isolation")
     ap.add_argument("--tokens", type=int, default=0, help="override the new-token count")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--max-branch", type=int, default=0,
+                    help="sparse lattice: nodes speculate at most this many tokens ahead (0: full lattice)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "dex":
         ap.error("--warmup must be >= 3")

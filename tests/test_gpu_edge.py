@@ -222,3 +222,39 @@ def test_batch_of_sixteen_sequences():
     w = di.gen_weights(shape, 0.3, seed=0, device="cuda")
     prompts = [di.gen_prompts(shape, 1, 5 + 3 * b, seed=100 + b)[0].tolist() for b in range(16)]
     _run(dexlib, shape, w, X, prompts, T, 64)
+
+
+@pytest.mark.parametrize("cap", [1, 2])
+def test_sparse_lattice_on_gpu(cap):
+    """max_branch caps the speculation depth: DEX is still bit-identical to AR, and every
+    round's nodes and tokens equal the oracle's capped Algorithm 1."""
+    dexlib = require_gpu()
+    shape, X, T = TINY_UNTIED, [1, 2, 3, 4, 5, 6, 7, 8], 10
+    w = di.gen_weights(shape, 0.3, seed=0, device="cuda")
+    prompt = di.gen_prompts(shape, 1, 24)[0].tolist()
+    dec = dexlib.Decoder(shape, w, X, batch=1, max_ctx=64, max_new=T, debug_logits=True, max_branch=cap)
+    m = oracle_model(shape, w)
+    ref = odex.dex_generate(m, prompt, X, T, max_branch=cap)
+    rounds = {}
+    for nd in ref.nodes:
+        rounds.setdefault(nd.round, {})[nd.node] = nd
+    try:
+        dec.prefill(0, prompt)
+        toks, checked = [], 0
+        for r in range(ref.rounds):
+            tok, nc = dec.step()
+            if nc[0]:
+                toks.append(tok[0])
+            nodes = dec.last_round_nodes()
+            assert sorted(nd["heap"] for nd in nodes) == sorted(rounds[r])
+            for nd in nodes:
+                o = rounds[r][nd["heap"]]
+                if o.margin > 0.1:
+                    assert nd["token"] == o.token
+                    checked += 1
+        assert toks == ref.tokens and checked > 0
+        dec.prefill(0, prompt)
+        y_ar = dec.generate(ar=True)[0]
+        assert y_ar == toks
+    finally:
+        dec.close()
