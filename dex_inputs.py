@@ -213,6 +213,29 @@ def gen_weights(shape: ModelShape, alpha: float, seed: int = 0, std: float = 0.0
     return w
 
 
+ADAPTER_TENSORS = ["g", "w1", "b1", "w2", "b2"]   # RMSNorm gain, W1 [2d][d], b1 [2d], W2 [d][2d], b2 [d]
+
+
+def gen_adapters(shape: ModelShape, X: List[int], seed: int = 5, std: float = 0.02, gate: float = 0.3,
+                 device="cpu") -> List[Dict[str, torch.Tensor]]:
+    """Synthetic inducing adapters for the non-final depths X[0..N-2] (hidden width 2d).
+
+    Per adapter: ``g`` RMSNorm gain (ones), ``w1`` [2d][d], ``b1`` [2d], ``w2`` [d][2d],
+    ``b2`` [d] (bf16, N(0, std)) and ``alpha`` (a Python float, the scalar gate).
+    """
+    d = shape.d_model
+    out = []
+    for k in range(len(X) - 1):
+        base = 4096 + 16 * k   # tensor ids of adapter k
+        out.append({"g": torch.ones(d, dtype=torch.bfloat16, device=device),
+                    "w1": normal_bf16((2 * d, d), seed, base + 1, std, device=device),
+                    "b1": normal_bf16((2 * d,), seed, base + 2, std, device=device),
+                    "w2": normal_bf16((d, 2 * d), seed, base + 3, std, device=device),
+                    "b2": normal_bf16((d,), seed, base + 4, std, device=device),
+                    "alpha": float(gate)})
+    return out
+
+
 def gen_prompts(shape: ModelShape, batch: int, prompt_len: int, seed: int = 1,
                 device="cpu") -> torch.Tensor:
     """[batch][prompt_len] int32 prompt ids, uniform in [0, vocab); row b uses stream seed+b."""

@@ -279,7 +279,7 @@ class DEXResult:
 
 def dex_generate(model, prompt: Sequence[int], X: Sequence[int], T: int, rule: Rule = Rule(),
                  use_decs: bool = True, seq: int = 0, keep_logits: bool = False,
-                 max_branch: int = 0) -> DEXResult:
+                 max_branch: int = 0, adapters: Optional[Sequence[Dict]] = None) -> DEXResult:
     """Algorithm 1 over one sequence; returns the committed tokens Y and a full trace.
 
     max_branch > 0 builds a sparse lattice (the pruning of low-value branches that the
@@ -287,6 +287,10 @@ def dex_generate(model, prompt: Sequence[int], X: Sequence[int], T: int, rule: R
     node exists only if its parent does and its path holds at most max_branch position
     moves, i.e. it speculates at most that many tokens ahead of the commit.  The anchor
     chain has none and always exists, so the committed stream is unchanged.
+
+    adapters: one inducing adapter per non-final depth X[0..N-2] (Appendix C.2; fp64 arrays
+    as oracle.model.apply_adapter takes them) applied before the shared exit head of the
+    nodes at those stages; the final depth keeps the plain exit, so commits are unchanged.
     """
     N = len(X)
     assert X[-1] == model.L and list(X) == sorted(set(X))
@@ -328,7 +332,8 @@ def dex_generate(model, prompt: Sequence[int], X: Sequence[int], T: int, rule: R
         # DECS, then insert into the explore buffer
         Z = {}
         for i in live:
-            z = model.exit_logits(H[i])[0]
+            ad = adapters[stage(i)] if adapters is not None and stage(i) < N - 1 else None
+            z = model.exit_logits(H[i], ad)[0]
             plen = len(branch_parents(i))
             y, mg, masked = decs(z, i, dict(B), q, q_max, i_ref, rule, seq, p_c + plen,
                                  enabled=use_decs)

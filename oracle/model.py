@@ -164,6 +164,26 @@ class OracleModel:
                 hist.append(h)
         return hist if keep_depths else h
 
-    def exit_logits(self, h: np.ndarray) -> np.ndarray:
-        """Shared exit head: RMSNorm(h; g_final) W_lm^T (Appendix C.2)."""
+    def exit_logits(self, h: np.ndarray, adapter: Optional[Dict] = None) -> np.ndarray:
+        """Shared exit head: RMSNorm(h; g_final) W_lm^T (Appendix C.2), after the inducing
+        adapter of the depth when one is given."""
+        if adapter is not None:
+            h = apply_adapter(h, adapter, self.eps)
         return rmsnorm(h, self.final_norm, self.eps) @ self._lm_head().T
+
+
+def silu_act(x: np.ndarray) -> np.ndarray:
+    return x / (1.0 + np.exp(-x))
+
+
+def apply_adapter(h: np.ndarray, ad: Dict, eps: float) -> np.ndarray:
+    """Inducing adapter of Appendix C.2 at a non-final depth:
+
+        delta = alpha (W2 sigma(W1 RMSNorm(h; g) + b1) + b2),   h~ = h + delta,
+
+    two linear layers with biases (hidden width m = 2h), the backbone activation sigma
+    (SiLU for these SwiGLU decoders) and the scalar gate alpha.  ``ad`` holds widened fp64
+    arrays g, w1 [m][h], b1 [m], w2 [h][m], b2 [h] and the float alpha."""
+    n = rmsnorm(h, ad["g"], eps)
+    u = n @ ad["w1"].T + ad["b1"]
+    return h + ad["alpha"] * (silu_act(u) @ ad["w2"].T + ad["b2"])

@@ -177,3 +177,79 @@ def test_sparse_lattice_first_cycle_counts(cap):
     for q in range(len(X)):
         brute = sum(1 for moves in product("DP", repeat=q) if moves.count("P") <= cap)
         assert per_round[q] == brute, (q, per_round[q], brute)
+
+
+# ---- inducing adapters (Appendix C.2) --------------------------------------------------------
+
+def _adapter(rng, d, alpha, zero_w2=False):
+    ad = {"g": 1.0 + 0.1 * rng.standard_normal(d), "w1": 0.1 * rng.standard_normal((2 * d, d)),
+          "b1": 0.1 * rng.standard_normal(2 * d), "w2": 0.1 * rng.standard_normal((d, 2 * d)),
+          "b2": 0.1 * rng.standard_normal(d), "alpha": alpha}
+    if zero_w2:
+        ad["w2"] = np.zeros((d, 2 * d))
+    return ad
+
+
+def test_adapter_special_cases():
+    from oracle.model import apply_adapter
+    from scipy.special import expit
+    rng = np.random.default_rng(0)
+    d = 16
+    h = rng.standard_normal((3, d))
+    # alpha = 0: the plain hidden state
+    assert np.array_equal(apply_adapter(h, _adapter(rng, d, 0.0), 1e-5), h)
+    # W2 = 0: h + alpha b2 whatever W1, b1, g
+    ad = _adapter(rng, d, 0.7, zero_w2=True)
+    assert np.allclose(apply_adapter(h, ad, 1e-5), h + 0.7 * ad["b2"], rtol=0, atol=1e-15)
+    # W1 = [I; 0], b1 = 0, W2 = [I, 0]: h + alpha (SiLU(RMSNorm(h; g)) + b2), SiLU = x expit(x)
+    ad = _adapter(rng, d, 0.5)
+    ad["w1"] = np.vstack([np.eye(d), np.zeros((d, d))])
+    ad["b1"] = np.zeros(2 * d)
+    ad["w2"] = np.hstack([np.eye(d), np.zeros((d, d))])
+    n = h / np.sqrt(np.mean(h * h, axis=-1, keepdims=True) + 1e-5) * ad["g"]
+    assert np.allclose(apply_adapter(h, ad, 1e-5), h + 0.5 * (n * expit(n) + ad["b2"]), rtol=1e-13, atol=1e-13)
+
+
+def test_adapter_correction_is_scale_invariant():
+    """The correction depends on h only through RMSNorm(h): with eps = 0, scaling h by a
+    positive factor leaves h~ - h unchanged."""
+    from oracle.model import apply_adapter
+    rng = np.random.default_rng(1)
+    d = 32
+    h = rng.standard_normal((2, d))
+    ad = _adapter(rng, d, 0.4)
+    d1 = apply_adapter(h, ad, 0.0) - h
+    d2 = apply_adapter(7.5 * h, ad, 0.0) - 7.5 * h
+    assert np.allclose(d1, d2, rtol=1e-12, atol=1e-12)
+
+
+def _widened_adapters(shape, X, gate):
+    from oracle.model import widen_bf16
+    ads = di.gen_adapters(shape, X, gate=gate)
+    return [{k: (v if k == "alpha" else widen_bf16(di.bf16_bits(v))) for k, v in a.items()} for a in ads]
+
+
+@pytest.mark.parametrize("sample", [False, True])
+def test_adapters_keep_dex_lossless_and_change_proposals(sample):
+    shape, w, m = tiny_model(alpha=0.3, tied=False)
+    prompt = di.gen_prompts(shape, 1, 16)[0].tolist()
+    X = [2, 4, 6, 8]
+    rule = dex.Rule(sample=sample, tau=0.7, seed=3)
+    ads = _widened_adapters(shape, X, gate=2.0)
+    ar = dex.ar_generate(m, prompt, 12, rule=rule)
+    plain = dex.dex_generate(m, prompt, X, 12, rule=rule)
+    adapted = dex.dex_generate(m, prompt, X, 12, rule=rule, adapters=ads)
+    assert adapted.tokens == ar.tokens == plain.tokens
+    # in the first cycle (before any commit) both lattices hold the same prefixes: the
+    # final-depth node is never adapted, intermediate proposals are
+    first = {(n.round, n.node): n for n in plain.nodes if n.round < len(X)}
+    changed = 0
+    for n in adapted.nodes:
+        if n.round >= len(X):
+            continue
+        o = first[(n.round, n.node)]
+        if n.stage == len(X) - 1:
+            assert n.token == o.token
+        elif n.token != o.token:
+            changed += 1
+    assert changed > 0
