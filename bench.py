@@ -178,8 +178,9 @@ def run_gpu(args):
     prompt = prompts[0]
     T = wl.max_new
     max_ctx = wl.prompt_len + T + len(wl.X) + 8
+    ads = _adapters(args, wl, "cuda")
     dec = dexlib.Decoder(shape, w, wl.X, batch=B, max_ctx=max_ctx, max_new=T, sample=wl.sample, tau=wl.tau,
-                         seed=wl.gumbel_seed, decs=wl.decs, max_branch=args.max_branch)
+                         seed=wl.gumbel_seed, decs=wl.decs, max_branch=args.max_branch, adapters=ads)
     st = torch.cuda.current_stream()
     import ctypes as C
     out_host = (C.c_int32 * (B * T))()
@@ -270,7 +271,7 @@ def run_gpu(args):
         "config": {"workload": wl.name, "model": MODEL_NAMES.get(wl.shape, "decoder"), "X": wl.X, "alpha": wl.alpha,
                    "global_batch": world * B, "prompt_len": wl.prompt_len, "new_tokens": T,
                    "decode": "sample" if wl.sample else "greedy", "parallelism": f"replicas{world}",
-                   "max_branch": args.max_branch,
+                   "max_branch": args.max_branch, "adapters": _adapter_cfg(args, wl),
                    "l2": f"weights {_weight_gb(wl.shape):.1f} GB streamed per round >> 129 MB L2; no flush"},
         "layers_per_token": {k: (round(v, 3) if isinstance(v, float) else v) for k, v in layers.items()},
         "step_roofline": step_roof,
@@ -288,7 +289,7 @@ def run_gpu(args):
         "clocks": clk.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(wl, w, prompt)
+        line["cpu_baseline"] = cpu_baseline(wl, w, prompt, args.max_branch, ads)
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
@@ -386,13 +387,35 @@ def _oracle_for(wl, w_gpu):
     return OracleModel(wl.shape, bits, keep_widened=True)
 
 
-def cpu_baseline(wl, w_gpu, prompt, n_tokens=1):
+def _adapters(args, wl, device):
+    """Seeded inducing adapters at the non-final exits when --adapters GATE is given."""
+    if args.adapters is None:
+        return None
+    return di.gen_adapters(wl.shape, wl.X, gate=args.adapters, device=device)
+
+
+def _adapter_cfg(args, wl):
+    if args.adapters is None:
+        return None
+    return {"gate": args.adapters, "hidden": 2 * wl.shape.d_model, "count": len(wl.X) - 1, "weights": "seeded"}
+
+
+def _oracle_adapters(ads):
+    if ads is None:
+        return None
+    from oracle.model import widen_bf16
+    return [{k: (v if k == "alpha" else widen_bf16(di.bf16_bits(v))) for k, v in a.items()} for a in ads]
+
+
+def cpu_baseline(wl, w_gpu, prompt, max_branch=0, ads=None, n_tokens=1):
     """Time the oracle on a bounded sample of the workload: prefill + n committed DEX tokens."""
     from oracle import dex as odex
     m = _oracle_for(wl, w_gpu)
     rule = odex.Rule(sample=wl.sample, tau=wl.tau, seed=wl.gumbel_seed)
+    wide = _oracle_adapters(ads)
     t0 = time.perf_counter()
-    r = odex.dex_generate(m, prompt, wl.X, n_tokens, rule=rule, use_decs=wl.decs)
+    r = odex.dex_generate(m, prompt, wl.X, n_tokens, rule=rule, use_decs=wl.decs, max_branch=max_branch,
+                          adapters=wide)
     dt = time.perf_counter() - t0
     return {"value": round(len(r.tokens) / dt, 5), "unit": "committed tokens/s", "cores": os.cpu_count(),
             "kind": "oracle", "seconds": round(dt, 2),
@@ -414,12 +437,14 @@ def run_reference(args):
     m = _oracle_for(wl, w)
     del w
     rule = odex.Rule(sample=wl.sample, tau=wl.tau, seed=wl.gumbel_seed)
+    kw = dict(rule=rule, use_decs=wl.decs, max_branch=args.max_branch,
+              adapters=_oracle_adapters(_adapters(args, wl, "cpu")))
     for _ in range(args.warmup):
-        odex.dex_generate(m, prompt, wl.X, 1, rule=rule, use_decs=wl.decs)
+        odex.dex_generate(m, prompt, wl.X, 1, **kw)
     t0 = time.perf_counter()
     n = 0
     for _ in range(args.steps):
-        n += len(odex.dex_generate(m, prompt, wl.X, 1, rule=rule, use_decs=wl.decs).tokens)
+        n += len(odex.dex_generate(m, prompt, wl.X, 1, **kw).tokens)
     dt = time.perf_counter() - t0
     v = n / dt
     sample = f"fp64 oracle: per step, prefill {wl.prompt_len - 1} positions + 1 committed DEX token"
@@ -427,8 +452,9 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "committed tokens/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": wl.name, "model": "llama2-7b-shaped", "X": wl.X,
-                                        "global_batch": 1, "prompt_len": wl.prompt_len},
+        "data": "synthetic", "config": {"workload": wl.name, "model": MODEL_NAMES.get(wl.shape, "decoder"),
+                                        "X": wl.X, "global_batch": 1, "prompt_len": wl.prompt_len,
+                                        "max_branch": args.max_branch, "adapters": _adapter_cfg(args, wl)},
         "cpu_baseline": {"value": round(v, 6), "unit": "committed tokens/s", "cores": os.cpu_count(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(v, 6), "unit": "committed tokens/s", "h2d_bytes_per_step": 0,
@@ -447,6 +473,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--max-branch", type=int, default=0,
                     help="sparse lattice: nodes speculate at most this many tokens ahead (0: full lattice)")
+    ap.add_argument("--adapters", type=float, default=None, metavar="GATE",
+                    help="seeded inducing adapters (hidden width 2d) at the non-final exits, scalar gate GATE")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "dex":
         ap.error("--warmup must be >= 3")

@@ -66,6 +66,13 @@ typedef struct dex_model {
   const void* final_norm;   /* device, [d_model] bf16 */
   const void* lm_head;      /* device, [vocab][d_model] bf16 (== embed for a tied head) */
   const void* const* layers;/* host array of n_layers*9 device pointers (see above) */
+  /* Inducing adapters (Appendix C.2), or NULL: a host array of (n_X - 1) * 5 device pointers,
+   * one adapter per non-final depth X[k], k < n_X - 1, of the X given to dex_init, in the
+   * order g[d] (RMSNorm gain), w1[2d][d], b1[2d], w2[d][2d], b2[d] (bf16), with
+   * adapter_alpha a host array of the n_X - 1 scalar gates.  The node of a non-final stage
+   * is decoded from h + alpha (w2 SiLU(w1 RMSNorm(h; g) + b1) + b2); the final depth never is. */
+  const void* const* adapters;
+  const float* adapter_alpha;
 } dex_model;
 
 /* Decode setup.  sample=0: greedy (ties -> lowest id); sample=1: Gumbel-max at

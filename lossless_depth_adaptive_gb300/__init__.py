@@ -38,7 +38,8 @@ class dex_model(C.Structure):
                 ("n_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("d_ff", C.c_int32),
                 ("vocab", C.c_int32), ("rms_eps", C.c_float), ("rope_theta", C.c_float),
                 ("embed", C.c_void_p), ("final_norm", C.c_void_p), ("lm_head", C.c_void_p),
-                ("layers", C.POINTER(C.c_void_p))]
+                ("layers", C.POINTER(C.c_void_p)), ("adapters", C.POINTER(C.c_void_p)),
+                ("adapter_alpha", C.POINTER(C.c_float))]
 
 
 class dex_decode_cfg(C.Structure):
@@ -253,7 +254,7 @@ def dex_kv_collapse(committed_ptr: int, pool_ptr: int, geom: dex_kv_geom, jobs_p
 class ModelRef:
     """Keeps the ctypes model description and the layer-pointer array alive."""
 
-    def __init__(self, shape, weights: Dict):
+    def __init__(self, shape, weights: Dict, adapters: Optional[Sequence[Dict]] = None):
         ptrs = []
         for l in range(shape.n_layers):
             for name in LAYER_TENSORS:
@@ -267,6 +268,18 @@ class ModelRef:
                                weights["embed"].data_ptr(), weights["final_norm"].data_ptr(), head.data_ptr(),
                                C.cast(self._layers, C.POINTER(C.c_void_p)))
         self.weights = weights
+        self.adapters = adapters
+        if adapters:
+            aptrs = []
+            for ad in adapters:
+                for name in ("g", "w1", "b1", "w2", "b2"):
+                    t = ad[name]
+                    assert t.is_cuda and t.is_contiguous()
+                    aptrs.append(t.data_ptr())
+            self._adapters = (C.c_void_p * len(aptrs))(*aptrs)
+            self._alpha = (C.c_float * len(adapters))(*[float(ad["alpha"]) for ad in adapters])
+            self.model.adapters = C.cast(self._adapters, C.POINTER(C.c_void_p))
+            self.model.adapter_alpha = C.cast(self._alpha, C.POINTER(C.c_float))
 
 
 class Decoder:
@@ -274,10 +287,11 @@ class Decoder:
 
     def __init__(self, shape, weights: Dict, X: Sequence[int], batch: int, max_ctx: int, max_new: int,
                  sample: bool = False, tau: float = 1.0, seed: int = 0, decs: bool = True,
-                 debug_logits: bool = False, stream: Optional[int] = None, max_branch: int = 0):
+                 debug_logits: bool = False, stream: Optional[int] = None, max_branch: int = 0,
+                 adapters: Optional[Sequence[Dict]] = None):
         import torch
         self.shape, self.X, self.batch, self.max_new = shape, list(X), batch, max_new
-        self.ref = ModelRef(shape, weights)
+        self.ref = ModelRef(shape, weights, adapters)
         cfg = dex_decode_cfg(batch, max_ctx, max_new, int(sample), tau, seed, int(decs), int(debug_logits),
                              int(max_branch))
         self.stream = torch.cuda.current_stream().cuda_stream if stream is None else stream

@@ -80,6 +80,13 @@ struct dex_handle {
   // k segments per tile of each weight shape (fixed per handle: results depend on them)
   int seg_qkv = 1, seg_o = 1, seg_gu = 1, seg_d = 1, seg_lm = 1;
   size_t partial_bytes = 0;    // segment-partial workspace
+  // inducing adapters of the non-final depths (Appendix C.2), n_adapters = N - 1 or 0
+  int n_adapters = 0, seg_ad1 = 1, seg_ad2 = 1;
+  std::vector<const bf16*> ad_g, ad_b1, ad_b2;
+  std::vector<float> ad_alpha;
+  std::vector<const uint8_t*> pk_ad1, pk_ad2;   // packed W1 [2d][d], W2 [d][2d]
+  bf16* ad_act = nullptr;                        // [2][rows_cap][2d] hidden activations
+  CUtensorMap tm_adact[17];
   size_t gemm_smem = 0;        // shared-memory budget of a small-tile GEMM CTA
   std::unique_ptr<dex::Lattice> lat, lat_ar;
   std::vector<int> mode;                 // per sequence: 0 idle, 1 DEX, 2 AR
@@ -171,6 +178,7 @@ struct RoundTables {
 // or a prefill chunk.  `items` are its attention items (layer filled in per slot).
 struct Batch {
   int off, n, l0, l1;
+  int stage = -1;   // lattice stage of a DEX round's batch (-1: prefill)
   std::vector<dex::AttnItem> items;
 };
 
@@ -335,6 +343,7 @@ int run_layers(dex_handle* h, const Uploaded& u, const std::vector<Batch>& batch
           gr.has_next = (!last && l + 1 < h->L) ? 1 : 0;
           gr.g_next = (l + 1 < h->L) ? W(h, l + 1, 0) : nullptr;
           gr.stage_end = (last && with_exit) ? 1 : 0;
+          if (gr.stage_end && b.stage >= 0 && b.stage < h->n_adapters) gr.g_exit = h->ad_g[b.stage];
         }
       }
     };
@@ -481,6 +490,7 @@ int run_round(dex_handle* h, dex::Lattice* lat, std::vector<dex_copy_job>* pendi
     b.n = stage_off[s + 1] - stage_off[s];
     b.l0 = s > 0 ? X[s - 1] : 0;
     b.l1 = X[s];
+    b.stage = (NS == h->N) ? s : -1;   // adapters belong to the DEX lattice's stages only
     for (int k = b.off; k < b.off + b.n;) {
       int e = k;
       dex::AttnItem it = {};
@@ -543,6 +553,52 @@ int run_round(dex_handle* h, dex::Lattice* lat, std::vector<dex_copy_job>* pendi
   h->stats.kernel_launches++;
   rc = run_layers(h, u, batches, slots, true);
   if (rc) return rc;
+  // inducing adapters of the non-final stages: exit input h -> h + alpha (W2 SiLU(W1 n + b1) + b2)
+  if (h->n_adapters > 0) {
+    dex::GemmArgs up = base_args(h), dn = base_args(h);
+    int ng = 0, nmax_ad = 0;
+    for (const Batch& b : batches) {
+      if (b.stage < 0 || b.stage >= h->n_adapters || b.n == 0) continue;
+      dex::GemmGroup gu = {}, gd = {};
+      gu.a_packed = h->pk_ad1[b.stage];
+      gu.bias = h->ad_b1[b.stage];
+      gd.a_packed = h->pk_ad2[b.stage];
+      gd.bias = h->ad_b2[b.stage];
+      gd.alpha = h->ad_alpha[b.stage];
+      gu.b_row0 = gd.b_row0 = b.off;
+      gu.n = gd.n = b.n;
+      up.groups[ng] = gu;
+      dn.groups[ng] = gd;
+      ++ng;
+      nmax_ad = std::max(nmax_ad, b.n);
+    }
+    if (ng > 0) {
+      up.nodes = dn.nodes = u.nodes;
+      up.n_groups = dn.n_groups = ng;
+      up.kblocks = (h->d + 63) / 64;
+      up.n_tiles = 2 * h->d / 128;
+      up.n_segs = h->seg_ad1;
+      up.src_tiles0 = up.n_tiles;
+      up.ssq_in = h->exit_ssq;
+      up.act_out = h->ad_act;
+      up.d_ff = 2 * h->d;
+      rc = gemm(h, dex::EPI_ADUP, h->tm_lm, h->tm_lm, h->tm_lm, h->tm_exit, up, nmax_ad,
+                static_cast<int64_t>(2) * h->d * h->d * 2, static_cast<int64_t>(h->d) * 4 + 2 * h->d * 4);
+      if (rc) return rc;
+      dn.kblocks = (2 * h->d + 63) / 64;
+      dn.n_tiles = h->d / 128;
+      dn.n_segs = h->seg_ad2;
+      dn.src_tiles0 = dn.n_tiles;
+      dn.hidden = h->hidden;
+      dn.exit_hb = h->exit_hb;
+      dn.exit_ssq = h->exit_ssq;
+      dn.g_final = h->final_norm;
+      rc = gemm(h, dex::EPI_ADDOWN, h->tm_lm, h->tm_lm, h->tm_lm, h->tm_adact, dn, nmax_ad,
+                static_cast<int64_t>(2) * h->d * h->d * 2, static_cast<int64_t>(2) * h->d * 4 + h->d * 8);
+      if (rc) return rc;
+      h->stats.weight_bytes += static_cast<int64_t>(ng) * 8 * h->d * h->d;
+    }
+  }
   if (ev[2]) cudaEventRecord(ev[2], h->st);
   // exit head + DECS over every node of the round
   {
@@ -727,6 +783,19 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
   }
   h->X.assign(X, X + n_X);
   h->N = n_X;
+  if (m->adapters && n_X > 1) {   // one adapter per non-final depth
+    if (!m->adapter_alpha) return DEX_EINVAL;
+    h->n_adapters = n_X - 1;
+    for (int k = 0; k < h->n_adapters; ++k) {
+      const void* const* ap = m->adapters + static_cast<size_t>(k) * 5;
+      for (int j = 0; j < 5; ++j)
+        if (!ap[j] || (reinterpret_cast<uintptr_t>(ap[j]) & 15)) return DEX_EINVAL;
+      h->ad_g.push_back(static_cast<const bf16*>(ap[0]));
+      h->ad_b1.push_back(static_cast<const bf16*>(ap[2]));
+      h->ad_b2.push_back(static_cast<const bf16*>(ap[4]));
+      h->ad_alpha.push_back(m->adapter_alpha[k]);
+    }
+  }
   h->cfg = *cfg;
   h->st = static_cast<cudaStream_t>(stream);
   h->n_sm = prop.multiProcessorCount;
@@ -761,6 +830,7 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
   rc |= dalloc(h, &h->exit_hb, 2 * R * h->d * 2);
   rc |= dalloc(h, &h->attn_out, 2 * R * qd * 2);
   rc |= dalloc(h, &h->act, 2 * R * h->dff * 2);
+  if (h->n_adapters) rc |= dalloc(h, &h->ad_act, 2 * R * 2 * static_cast<size_t>(h->d) * 2);
   rc |= dalloc(h, &h->ssq, R * (h->d / 128) * 4);
   rc |= dalloc(h, &h->exit_ssq, R * (h->d / 128) * 4);
   rc |= dalloc(h, &h->q, R * qd * 4);
@@ -787,10 +857,14 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
     h->seg_gu = dex::gemm_segments(t_gu, kb_d, h->gemm_ctas);
     h->seg_d = dex::gemm_segments(t_o, kb_f, h->gemm_ctas);
     h->seg_lm = dex::gemm_segments(t_lm, kb_d, h->gemm_ctas);
+    h->seg_ad1 = dex::gemm_segments(2 * h->d / 128, kb_d, h->gemm_ctas);
+    h->seg_ad2 = dex::gemm_segments(t_o, (2 * h->d + 63) / 64, h->gemm_ctas);
     const size_t u_layer = std::max<size_t>({static_cast<size_t>(t_qkv) * h->seg_qkv,
                                             static_cast<size_t>(t_o) * h->seg_o,
                                             static_cast<size_t>(t_gu) * h->seg_gu,
-                                            static_cast<size_t>(t_o) * h->seg_d});
+                                            static_cast<size_t>(t_o) * h->seg_d,
+                                            static_cast<size_t>(2 * h->d / 128) * h->seg_ad1,
+                                            static_cast<size_t>(t_o) * h->seg_ad2});
     const int nt_round = std::min(256, (std::max(1, h->lat->max_round_nodes()) + 15) & ~15);
     h->partial_bytes = std::max({dex::gemm_partial_bytes(256, u_layer),
                                  dex::gemm_partial_bytes(nt_round, u_layer * std::max(1, h->N)),
@@ -817,6 +891,7 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
   cudaMemsetAsync(h->exit_hb, 0, 2 * R * h->d * 2, h->st);
   cudaMemsetAsync(h->attn_out, 0, 2 * R * qd * 2, h->st);
   cudaMemsetAsync(h->act, 0, 2 * R * h->dff * 2, h->st);
+  if (h->ad_act) cudaMemsetAsync(h->ad_act, 0, 2 * R * 2 * static_cast<size_t>(h->d) * 2, h->st);
   // RoPE table (rotate-half, frequencies theta^(-2i/hd)), computed in double
   {
     std::vector<float2> tab(ctx * (hd / 2));
@@ -858,6 +933,7 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
     rc |= encode_2d(&h->tm_attn[i], h->attn_out, 2 * R, qd, 16 * i);
     rc |= encode_2d(&h->tm_act[i], h->act, 2 * R, h->dff, 16 * i);
     rc |= encode_2d(&h->tm_exit[i], h->exit_hb, 2 * R, h->d, 16 * i);
+    if (h->ad_act) rc |= encode_2d(&h->tm_adact[i], h->ad_act, 2 * R, 2 * h->d, 16 * i);
   }
   if (rc) return DEX_EINVAL;
   // pack every GEMM weight once: contiguous, pre-swizzled 16 KB boxes in streaming order
@@ -899,6 +975,26 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
     if (ce == cudaSuccess)
       ce = dex::launch_pack(dex::PACK_ROWS, PS{h->lm_head, h->V}, none, none, h->d, t_lm, plm, h->st);
     if (ce != cudaSuccess) return DEX_ECUDA;
+    // adapters: W1 [2d][d] (2d/128 tiles over d), W2 [d][2d] (d/128 tiles over 2d)
+    if (h->n_adapters) {
+      const size_t b_a1 = dex::packed_bytes(2 * h->d / 128, kb_d);
+      const size_t b_a2 = dex::packed_bytes(t_o, (2 * h->d + 63) / 64);
+      uint8_t* abase = nullptr;
+      if (dalloc(h, &abase, h->n_adapters * (b_a1 + b_a2))) return DEX_ENOMEM;
+      for (int k = 0; k < h->n_adapters && ce == cudaSuccess; ++k) {
+        const void* const* ap = m->adapters + static_cast<size_t>(k) * 5;
+        uint8_t* p1 = abase + k * (b_a1 + b_a2);
+        uint8_t* p2 = p1 + b_a1;
+        h->pk_ad1.push_back(p1);
+        h->pk_ad2.push_back(p2);
+        ce = dex::launch_pack(dex::PACK_ROWS, PS{static_cast<const bf16*>(ap[1]), 2 * h->d}, none, none, h->d,
+                              2 * h->d / 128, p1, h->st);
+        if (ce == cudaSuccess)
+          ce = dex::launch_pack(dex::PACK_ROWS, PS{static_cast<const bf16*>(ap[3]), h->d}, none, none, 2 * h->d,
+                                t_o, p2, h->st);
+      }
+      if (ce != cudaSuccess) return DEX_ECUDA;
+    }
   }
   if (cudaStreamSynchronize(h->st) != cudaSuccess) return DEX_ECUDA;
   *out = hp.release();

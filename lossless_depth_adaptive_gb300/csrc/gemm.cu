@@ -401,7 +401,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const size_t o = static_cast<size_t>(b_row0 + c) * a.d + f;
             const size_t lo = static_cast<size_t>(a.plane_rows) * a.d;
             if (grp.has_next) store_pair(a.hb_out + o, a.hb_out + lo + o, __fmul_rn(x, bf16_to_f32(grp.g_next[f])));
-            if (grp.stage_end) store_pair(a.exit_hb + o, a.exit_hb + lo + o, __fmul_rn(x, bf16_to_f32(a.g_final[f])));
+            if (grp.stage_end) {
+              const __nv_bfloat16* gx = grp.g_exit ? grp.g_exit : a.g_final;
+              store_pair(a.exit_hb + o, a.exit_hb + lo + o, __fmul_rn(x, bf16_to_f32(gx[f])));
+            }
             sq[j] = __fmul_rn(x, x);
           }
         }
@@ -434,6 +437,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             store_pair(a.act_out + o, a.act_out + static_cast<size_t>(a.plane_rows) * a.d_ff + o, act);
           }
         }
+        named_bar_sync(1, 128);
+      } else if (EPI == EPI_ADUP) {   // adapter layer 1: SiLU(W1 RMSNorm(h; g) + b1)
+        const int f = lt * kBM + r;      // hidden unit of the adapter (0 .. 2d-1)
+        const float b1 = bf16_to_f32(grp.bias[f]);
+        for (int j = 0; j < 16; ++j) {
+          const int c = c0 + j;
+          if (c >= n) break;
+          const float u = __fadd_rn(v[j] * inv[c], b1);
+          const float act = u / (1.0f + expf(-u));
+          const size_t o = static_cast<size_t>(b_row0 + c) * a.d_ff + f;
+          store_pair(a.act_out + o, a.act_out + static_cast<size_t>(a.plane_rows) * a.d_ff + o, act);
+        }
+      } else if (EPI == EPI_ADDOWN) {   // adapter layer 2: h~ = h + alpha (W2 a + b2) -> exit input
+        const int f = lt * kBM + r;
+        const float b2 = bf16_to_f32(grp.bias[f]);
+        const float gf = bf16_to_f32(a.g_final[f]);
+        float sq[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int c = c0 + j;
+          sq[j] = 0.0f;
+          if (c < n) {
+            const DevNode* nd = a.nodes + b_row0 + c;
+            const float x = __fadd_rn(a.hidden[static_cast<size_t>(nd->hrow) * a.d + f],
+                                      __fmul_rn(grp.alpha, __fadd_rn(v[j], b2)));
+            const size_t o = static_cast<size_t>(b_row0 + c) * a.d + f;
+            store_pair(a.exit_hb + o, a.exit_hb + static_cast<size_t>(a.plane_rows) * a.d + o, __fmul_rn(x, gf));
+            sq[j] = __fmul_rn(x, x);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float s = warp_sum(sq[j]);
+          if (lane == 0) qsum[wq * 16 + j] = s;
+        }
+        named_bar_sync(1, 128);
+        if (ep < 16 && c0 + ep < n)
+          a.exit_ssq[static_cast<size_t>(b_row0 + c0 + ep) * ndt + lt] =
+              __fadd_rn(__fadd_rn(qsum[0 * 16 + ep], qsum[1 * 16 + ep]), __fadd_rn(qsum[2 * 16 + ep], qsum[3 * 16 + ep]));
         named_bar_sync(1, 128);
       } else {   // EPI_EXIT
         const uint32_t vid = static_cast<uint32_t>(lt * kBM + r);
@@ -476,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int buf = ui & 1;
       int src, lt;
       tile_src(x.t, src, lt);
-      if (EPI != EPI_RESID && x.g != g_inv) {   // RMSNorm scales of this group's node rows
+      if (EPI != EPI_RESID && EPI != EPI_ADDOWN && x.g != g_inv) {   // RMSNorm scales of this group's node rows
         named_bar_sync(1, 128);                 // previous readers of inv[] are done
         for (int c = ep; c < n; c += 128) {
           const float* sp = a.ssq_in + static_cast<size_t>(grp.b_row0 + c) * ndt;
@@ -610,8 +652,14 @@ cudaError_t launch_gemm(int epi, const CUtensorMap& a0, const CUtensorMap& a1, c
     any_end |= gr.stage_end != 0;
   }
   if (!args.err || !args.counters || !args.partial) return cudaErrorInvalidValue;
-  if (epi != EPI_RESID && !args.ssq_in) return cudaErrorInvalidValue;
-  if (epi != EPI_SWIGLU && !args.nodes) return cudaErrorInvalidValue;
+  if (epi != EPI_RESID && epi != EPI_ADDOWN && !args.ssq_in) return cudaErrorInvalidValue;
+  if (epi != EPI_SWIGLU && epi != EPI_ADUP && !args.nodes) return cudaErrorInvalidValue;
+  if (epi == EPI_ADUP || epi == EPI_ADDOWN)
+    for (int g = 0; g < args.n_groups; ++g)
+      if (!args.groups[g].bias) return cudaErrorInvalidValue;
+  if (epi == EPI_ADUP && !args.act_out) return cudaErrorInvalidValue;
+  if (epi == EPI_ADDOWN && (!args.hidden || !args.exit_hb || !args.exit_ssq || !args.g_final))
+    return cudaErrorInvalidValue;
   if (epi == EPI_QKV && (!args.q_out || !args.kv_commit || !args.kv_pool || !args.rope)) return cudaErrorInvalidValue;
   if (epi == EPI_RESID && (!args.hidden || !args.ssq_out || (any_next && !args.hb_out) ||
                            (any_end && (!args.exit_hb || !args.exit_ssq || !args.g_final))))
@@ -628,6 +676,8 @@ cudaError_t launch_gemm(int epi, const CUtensorMap& a0, const CUtensorMap& a1, c
     case EPI_RESID: return launch_one<EPI_RESID>(a0, a1, a2, b, args, st, pdl);
     case EPI_SWIGLU: return launch_one<EPI_SWIGLU>(a0, a1, a2, b, args, st, pdl);
     case EPI_EXIT: return launch_one<EPI_EXIT>(a0, a1, a2, b, args, st, pdl);
+    case EPI_ADUP: return launch_one<EPI_ADUP>(a0, a1, a2, b, args, st, pdl);
+    case EPI_ADDOWN: return launch_one<EPI_ADDOWN>(a0, a1, a2, b, args, st, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

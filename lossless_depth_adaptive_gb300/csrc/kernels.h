@@ -44,7 +44,8 @@ struct AttnItem {
   int32_t layer;                     // decoder layer of this item (items of several stages share a launch)
 };
 
-enum Epi : int { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_EXIT = 3 };
+// EPI_ADUP / EPI_ADDOWN: the two layers of an inducing adapter at a non-final exit.
+enum Epi : int { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_EXIT = 3, EPI_ADUP = 4, EPI_ADDOWN = 5 };
 
 // One weight matrix of a grouped launch: a stage's layer and that stage's node rows.  The
 // groups of a launch share the weight shape; each keeps its own fixed work partition.
@@ -52,12 +53,15 @@ constexpr int kMaxGroups = 10;
 struct GemmGroup {
   const uint8_t* a_packed;    // packed weights of this group's layer (null: TMA from tmA*)
   const __nv_bfloat16* g_next;// RESID: gain of the next norm (null at the model's end)
+  const __nv_bfloat16* g_exit;// RESID at a stage end: gain of the exit input (null: g_final;
+                              // an adapter's RMSNorm gain when the stage's exit is adapted)
+  const __nv_bfloat16* bias;  // ADUP: b1, ADDOWN: b2
   int32_t b_row0;       // first node row (= first B row)
   int32_t n;            // node rows
   int32_t layer;        // decoder layer (QKV: KV cache addressing)
   int32_t stage_end;    // RESID: last layer of the stage -> also write the exit-head input
   int32_t has_next;     // RESID: write the next layer's bf16 input
-  int32_t pad;
+  float alpha;          // ADDOWN: the adapter's scalar gate
 };
 
 struct GemmArgs {
@@ -97,7 +101,7 @@ struct GemmArgs {
   __nv_bfloat16* exit_hb;     // [2][rows][d]  pair of h * g_final
   const __nv_bfloat16* g_final;
   float* exit_ssq;      // [rows][d/128]
-  // SWIGLU
+  // SWIGLU (and ADUP: [2][rows][2d], d_ff = 2d)
   __nv_bfloat16* act_out;     // [2][rows][d_ff]  pair of SiLU(gate) * up
   // EXIT + DECS
   float* logits_dbg;    // [rows][vocab] or null

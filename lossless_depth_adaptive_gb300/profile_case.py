@@ -2,6 +2,7 @@
 
     python -m lossless_depth_adaptive_gb300.profile_case --workload llama7b_x4 --tokens 8
     python -m lossless_depth_adaptive_gb300.profile_case --workload llama7b_x4 --layers 4 --tokens 2
+    python -m lossless_depth_adaptive_gb300.profile_case --tokens 8 --adapters 0.001
 
 Builds the workload's seeded weights (optionally only the first ``--layers`` layers, with
 the exploration set rescaled to the same number of stages), prefills the prompt, runs
@@ -31,6 +32,9 @@ def main():
     ap.add_argument("--tokens", type=int, default=8)
     ap.add_argument("--warmup", type=int, default=1)
     ap.add_argument("--ar", action="store_true", help="profile plain autoregressive rounds")
+    ap.add_argument("--max-branch", type=int, default=0, help="sparse lattice speculation cap (0: full lattice)")
+    ap.add_argument("--adapters", type=float, default=None, metavar="GATE",
+                    help="seeded inducing adapters at the non-final exits with scalar gate GATE")
     ap.add_argument("--timeline", action="store_true",
                     help="record per-CTA GEMM clock records of the profiled request (needs DEX_TIMELINE=<file>)")
     a = ap.parse_args()
@@ -43,8 +47,10 @@ def main():
         X = [a.layers // N * (k + 1) for k in range(N)]
     w = di.gen_weights(shape, wl.alpha, seed=wl.weight_seed, device="cuda")
     prompts = di.gen_prompts(shape, wl.batch, wl.prompt_len, seed=wl.prompt_seed).tolist()
+    ads = None if a.adapters is None else di.gen_adapters(shape, X, gate=a.adapters, device="cuda")
     dec = dexlib.Decoder(shape, w, X, batch=wl.batch, max_ctx=wl.prompt_len + a.tokens + len(X) + 8,
-                         max_new=a.tokens, sample=wl.sample, tau=wl.tau, seed=wl.gumbel_seed, decs=wl.decs)
+                         max_new=a.tokens, sample=wl.sample, tau=wl.tau, seed=wl.gumbel_seed, decs=wl.decs,
+                         max_branch=a.max_branch, adapters=ads)
 
     def prefill_all():
         for b, p in enumerate(prompts):

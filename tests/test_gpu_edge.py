@@ -258,3 +258,53 @@ def test_sparse_lattice_on_gpu(cap):
         assert y_ar == toks
     finally:
         dec.close()
+
+
+@pytest.mark.parametrize("which,sample", [("tiny", False), ("tiny", True), ("small", False)])
+def test_inducing_adapters_on_gpu(which, sample):
+    """Inducing adapters at the non-final exits (Appendix C.2, gate 2.0): every round's nodes
+    and exit logits equal the oracle's adapted Algorithm 1, the committed stream is still
+    bit-identical to AR, and the adapters move the intermediate logits by far more than the
+    tolerance (so the comparison could tell adapted from plain exits apart)."""
+    from oracle.model import widen_bf16
+    dexlib = require_gpu()
+    shape, X, T = (TINY_UNTIED, [2, 4, 6, 8], 10) if which == "tiny" else (SMALL, [1, 2, 3, 4], 8)
+    w = di.gen_weights(shape, 0.3, seed=0, device="cuda")
+    prompt = di.gen_prompts(shape, 1, 24)[0].tolist()
+    ads = di.gen_adapters(shape, X, gate=2.0, device="cuda")
+    wide = [{k: (v if k == "alpha" else widen_bf16(di.bf16_bits(v))) for k, v in a.items()} for a in ads]
+    m = oracle_model(shape, w)
+    rule = odex.Rule(sample=sample, tau=0.7, seed=5)
+    ref = odex.dex_generate(m, prompt, X, T, rule=rule, adapters=wide, keep_logits=True)
+    plain = odex.dex_generate(m, prompt, X, T, rule=rule, keep_logits=True)
+    first_plain = {(nd.round, nd.node): nd for nd in plain.nodes if nd.round < len(X)}
+    moved = max(float(np.max(np.abs(nd.logits - first_plain[(nd.round, nd.node)].logits)))
+                for nd in ref.nodes if nd.round < len(X) and nd.stage < len(X) - 1)
+    assert moved > 0.25
+    rounds = {}
+    for nd in ref.nodes:
+        rounds.setdefault(nd.round, {})[nd.node] = nd
+    dec = dexlib.Decoder(shape, w, X, batch=1, max_ctx=64, max_new=T, sample=sample, tau=0.7, seed=5,
+                         debug_logits=True, adapters=ads)
+    try:
+        dec.prefill(0, prompt)
+        toks, checked, worst = [], 0, 0.0
+        for r in range(ref.rounds):
+            tok, nc = dec.step()
+            if nc[0]:
+                toks.append(tok[0])
+            nodes = dec.last_round_nodes()
+            lg = dec.debug_logits()
+            assert sorted(nd["heap"] for nd in nodes) == sorted(rounds[r])
+            for i, nd in enumerate(nodes):
+                o = rounds[r][nd["heap"]]
+                worst = max(worst, float(np.max(np.abs(lg[i] - o.logits))))
+                if o.margin > 0.1:
+                    assert nd["token"] == o.token, (r, nd, o.token)
+                    checked += 1
+        assert worst < 5e-2 and checked > 0
+        assert toks == ref.tokens
+        dec.prefill(0, prompt)
+        assert dec.generate(ar=True)[0] == toks
+    finally:
+        dec.close()
