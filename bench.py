@@ -276,6 +276,11 @@ def run_gpu(args):
         "layers_per_token": {k: (round(v, 3) if isinstance(v, float) else v) for k, v in layers.items()},
         "step_roofline": step_roof,
         "phase_ms_per_round": {k: round(v, 4) for k, v in phases.items()},
+        "attention": {"launches": inst["attn_launches"],
+                      "us_per_launch": round(inst["ms_attn"] * 1e3 / max(1, inst["attn_launches"]), 2),
+                      "kv_gbs": round(inst["kv_bytes"] / (inst["ms_attn"] / 1e3) / 1e9, 1) if inst["ms_attn"] else None,
+                      "share_of_request": round(inst["ms_attn"] / ms_per_step, 4) if ms_per_step else None,
+                      "note": "CUDA events around each launch in one instrumented request (no launch overlap)"},
         "roofline": {"bound": "hbm", "kernel": "gemm_tc_kernel (all linear layers, one instrumented request)",
                      "achieved": round(achieved, 1) if achieved else None, "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4) if achieved else None, "peak_source": src,

@@ -147,13 +147,16 @@ typedef struct dex_stats {
   int64_t gemm_bytes;       /* their algorithmic bytes (weights + activations in/out) */
   double ms_gemm;           /* summed CUDA-event duration of those launches (timing >= 2) */
   double ms_expand, ms_exit, ms_collapse, ms_host;  /* phase split (timing >= 1) */
+  int64_t attn_launches;    /* lattice-attention launches */
+  double ms_attn;           /* summed CUDA-event duration of those launches (timing >= 2) */
 } dex_stats;
 
 int dex_get_stats(const dex_handle* h, dex_stats* out);
 int dex_reset_stats(dex_handle* h);
 
 /* timing: 0 off; 1 = CUDA events around the expansion / exit+DECS / collapse phases of
- * each round; 2 = also around every linear-layer GEMM launch (adds events); 3 = level 1
+ * each round; 2 = also around every linear-layer GEMM and attention launch (adds events,
+ * which also stop programmatic-dependent-launch overlap across them); 3 = level 1
  * plus per-CTA clock records of the GEMM launches that follow (diagnostics: only when the
  * environment variable DEX_TIMELINE names a file, which dex_free() writes; the first
  * DEX_TIMELINE_LAUNCHES launches, default 512, are kept). */

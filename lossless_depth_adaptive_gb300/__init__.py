@@ -56,7 +56,7 @@ class dex_stats(C.Structure):
                 ("h2d_bytes", C.c_int64), ("d2h_bytes", C.c_int64), ("kernel_launches", C.c_int64),
                 ("gemm_launches", C.c_int64), ("gemm_bytes", C.c_int64), ("ms_gemm", C.c_double),
                 ("ms_expand", C.c_double), ("ms_exit", C.c_double), ("ms_collapse", C.c_double),
-                ("ms_host", C.c_double)]
+                ("ms_host", C.c_double), ("attn_launches", C.c_int64), ("ms_attn", C.c_double)]
 
     def as_dict(self) -> Dict:
         d = {k: getattr(self, k) for k, _ in self._fields_}

@@ -125,6 +125,7 @@ struct dex_handle {
   std::vector<cudaEvent_t> ev_pool;
   size_t ev_used = 0;
   std::vector<std::pair<cudaEvent_t, cudaEvent_t>> gemm_events;
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> attn_events;
   bool broken = false;
   // GEMM timeline diagnostics (timing level 3 with DEX_TIMELINE set)
   unsigned long long* timeline = nullptr;
@@ -385,9 +386,20 @@ int run_layers(dex_handle* h, const Uploaded& u, const std::vector<Batch>& batch
     at.max_groups = h->max_groups;
     at.plane_rows = h->rows_cap;
     at.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(h->hd)));
+    cudaEvent_t ae0 = nullptr, ae1 = nullptr;
+    if (h->timing == 2) {
+      ae0 = next_event(h);
+      ae1 = next_event(h);
+      cudaEventRecord(ae0, h->st);
+    }
     cudaError_t ce = dex::launch_attention(at, sl.n_items, sl.max_groups, sl.max_rows * (h->H / h->KVH), h->st, true);
     if (ce != cudaSuccess) return cuda_fail(h, ce);
+    if (h->timing == 2) {
+      cudaEventRecord(ae1, h->st);
+      h->attn_events.push_back({ae0, ae1});
+    }
     h->stats.kernel_launches++;
+    h->stats.attn_launches++;
     // O projection + residual
     a = base_args(h);
     fill_groups(a, 1);
@@ -690,7 +702,15 @@ int run_round(dex_handle* h, dex::Lattice* lat, std::vector<dex_copy_job>* pendi
       h->stats.ms_gemm += ms;
     }
   }
+  if (h->timing == 2) {
+    for (auto& pr : h->attn_events) {
+      float ms;
+      cudaEventElapsedTime(&ms, pr.first, pr.second);
+      h->stats.ms_attn += ms;
+    }
+  }
   h->gemm_events.clear();
+  h->attn_events.clear();
   h->ev_used = 0;
   return DEX_OK;
 }
