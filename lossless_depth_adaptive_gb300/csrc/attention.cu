@@ -6,26 +6,37 @@
 // sequence); keys at c_end..p are the branch entries of the node's P-ancestors' slot
 // chains and its own, read from the branch pool through the node's tail table.
 //
-// Work split: CTA = (sequence item, KV head, 128-position key group); each warp owns a
-// 32-key slice of the group, lane = key.  Keys and values are fp32 rows read straight
-// from global memory (no shared-memory staging, so several CTAs share an SM and hide
-// each other's latency): a lane walks its key's row in 16-byte chunks, and a key that is
-// committed for every query of a batch is read once and scored against all of them.
+// Work split: CTA = (sequence item, KV head, 128-position key group), four warps, each
+// owning a 32-key slice of the group.  Scores take lane = key: the group's committed key
+// rows are contiguous fp32 in the cache, so one thread brings them into shared memory
+// with a single bulk copy (completion on an mbarrier) -- nothing is held in registers
+// while the bytes are in flight and nothing goes through L1 -- and each lane walks its
+// row's 16-byte chunks from chunk (key mod 32) onwards, so consecutive lanes touch
+// consecutive chunks and the shared-memory reads are conflict-free.  Values take lane = a
+// run of output dimensions, so a warp reads one whole value row per load (coalesced).
+// When the CTA's queries fit one pass (decode), the committed value rows
+// follow the keys into the same shared buffer with a second bulk copy once the scores are
+// taken; otherwise (prefill) the key rows stay in shared memory across query batches and
+// values are read from global memory eight rows ahead.  Branch keys (few per node) are
+// read from the pool.  A committed key is read once and used for every query of the batch.
+//
 // The arithmetic for a query is fixed by absolute positions only -- 32-key slices aligned
-// to position 0, slices combined in order within the group, 128-position groups combined
-// in group order by the last CTA to finish -- so a node's output is bit-identical whether
-// its keys sit in the committed cache or the branch pool and whatever batch it is in.
+// to position 0, each score summed over the same chunk order wherever the key row lives,
+// slices combined in order within a group, groups combined in group order by the last
+// CTA to finish -- so a node's output is bit-identical whether its keys sit in the
+// committed cache or the branch pool and whatever batch it is in.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace dex {
 
-constexpr int kAttnThreads = 128;
-constexpr int kGroupPos = 128;
+constexpr int kAttnWarps = kAttnGroupPos / 32;
+constexpr int kAttnThreads = 32 * kAttnWarps;
+static_assert(kAttnGroupPos == 32 * kAttnWarps && kAttnWarps == 4, "four 32-key warp slices per group");
+constexpr int kVB = 8;   // value rows loaded ahead
 
-// q . k for one fp32 key row.  The lane walks the row's 16-byte chunks starting at chunk
-// `rot` (its index = key position mod 32) with four interleaved partial sums; the order is
-// a function of the key's absolute position only.
+// Four interleaved partial sums of q . k over the row's chunks, starting at chunk `rot`;
+// the same order for a row in shared or global memory.
 template <int HD>
 __device__ __forceinline__ float dot_q_row(const float* q, const float* krow, int rot) {
   constexpr int NC = HD / 4;
@@ -33,7 +44,7 @@ __device__ __forceinline__ float dot_q_row(const float* q, const float* krow, in
 #pragma unroll
   for (int i = 0; i < NC; ++i) {
     const int c = (i + rot) & (NC - 1);
-    const float4 k4 = __ldg(reinterpret_cast<const float4*>(krow) + c);
+    const float4 k4 = *(reinterpret_cast<const float4*>(krow) + c);
     const float4 q4 = *reinterpret_cast<const float4*>(q + c * 4);
     float& a = s[i & 3];
     a = fmaf(q4.x, k4.x, a);
@@ -44,50 +55,72 @@ __device__ __forceinline__ float dot_q_row(const float* q, const float* krow, in
   return __fadd_rn(__fadd_rn(s[0], s[1]), __fadd_rn(s[2], s[3]));
 }
 
-constexpr int kQBatchMax = 8;  // largest query batch of a pass (QB is a template parameter: 1, 2, 4, 8)
-constexpr int kVB = 8;         // value rows loaded ahead
+__host__ __device__ constexpr size_t attn_smem_floats(int hd, int qb) {
+  return static_cast<size_t>(kAttnGroupPos) * hd + static_cast<size_t>(qb) * hd +
+         static_cast<size_t>(qb) * kAttnWarps * (hd + 2);
+}
 
 // QB: queries per pass, chosen per launch from its largest item (the unused slots of a
 // batch would otherwise still issue their predicated instructions).  A query's arithmetic
 // is the same in every instantiation.
 template <int HD, int QB>
 __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
-  constexpr int kQBatch = QB;
   constexpr int DPL = HD / 32;        // output dims per lane
   constexpr int NC = HD / 4;          // 16-byte chunks per row
   constexpr int PS = HD + 2;          // partial record: acc[HD], m, l
-  extern __shared__ __align__(16) float smem_f[];
-  float* sQ = smem_f;                 // [kQBatch][HD]
-  float* sP = sQ + kQBatch * HD;      // [kQBatch][4 warps][PS]
+  extern __shared__ __align__(128) float smem_f[];
+  float* sK = smem_f;                             // [kAttnGroupPos][HD] committed keys of the group
+  float* sQ = sK + kAttnGroupPos * HD;            // [QB][HD]
+  float* sP = sQ + QB * HD;                       // [QB][warps][PS]
+  __shared__ __align__(8) uint64_t bars[2];       // key rows landed, value rows landed
   __shared__ int s_last;
 
   const int g = blockIdx.x, kvh = blockIdx.y, it = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  griddep_wait();
+  griddep_wait();   // q and this round's K/V come from the preceding launch
   griddep_launch_dependents();
   const AttnItem item = a.items[it];
+  // the groups must cover every position up to max_pos (a malformed plan is reported)
+  if (g == 0 && kvh == 0 && tid == 0 && item.n_groups * kAttnGroupPos <= item.max_pos) atomicExch(a.err, DEV_BAD_INDEX);
   if (g >= item.n_groups) return;
-  const int g0 = g * kGroupPos;
+  const int g0 = g * kAttnGroupPos;
   const int H = a.H, G = a.H / a.KVH;
   // committed K and V rows of (sequence, layer, KV head): [max_ctx][HD] each
   const float* kcom =
       a.kv_commit + ((((static_cast<size_t>(item.seq) * a.L + item.layer) * 2 + 0) * a.KVH + kvh) * a.max_ctx) * HD;
   const float* vcom = kcom + static_cast<size_t>(a.KVH) * a.max_ctx * HD;
+  // committed rows some query of the item reads: [g0, g0 + n_com)
+  const int n_com = max(0, min(kAttnGroupPos, min(item.max_cend, item.max_pos + 1) - g0));
+  if (tid == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_mbar_init();
+    if (n_com > 0) {
+      const uint32_t bytes = static_cast<uint32_t>(n_com) * HD * 4;
+      mbar_arrive_expect_tx(&bars[0], bytes);
+      bulk_load_1d(sK, kcom + static_cast<size_t>(g0) * HD, bytes, &bars[0]);
+    }
+  }
+  bool have_k = n_com == 0, failed = false;
 
   const int nq = (item.row_end - item.row_begin) * G;
+  // one query pass (decode): once scored, the key buffer takes the group's committed value
+  // rows in one more bulk copy; several passes (prefill) keep the keys and read values from
+  // global memory
+  const bool v_smem = nq <= QB && n_com > 0;
   const int ks = g0 + 32 * warp;       // this warp's 32-key slice
   const int k = ks + lane;             // this lane's key
-  for (int qb = 0; qb < nq; qb += kQBatch) {
-    const int nb = min(kQBatch, nq - qb);
+  for (int qb = 0; qb < nq; qb += QB) {
+    const int nb = min(QB, nq - qb);
     for (int idx = tid; idx < nb * HD; idx += kAttnThreads) {
       const int qi = qb + idx / HD, d = idx % HD;
       const int row = item.row_begin + qi / G, qh = kvh * G + qi % G;
       sQ[idx] = a.q[(static_cast<size_t>(row) * H + qh) * HD + d] * a.scale_log2;
     }
-    int pos[kQBatch], cend[kQBatch], nrow[kQBatch];
+    int pos[QB], cend[QB], nrow[QB];
     int cend_min = 0x7fffffff, pos_max = -1;
 #pragma unroll
-    for (int j = 0; j < kQBatch; ++j) {
+    for (int j = 0; j < QB; ++j) {
       pos[j] = -1;
       cend[j] = 0;
       nrow[j] = item.row_begin;
@@ -100,11 +133,17 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
         pos_max = max(pos_max, pos[j]);
       }
     }
-    __syncthreads();
-    // key (or value) row kk of query j: committed cache below its c_end, else the branch
-    // entry of its P-ancestry from the pool through the node's tail table
-    auto key_row = [&](int j, int kk, int kv) -> const float* {
-      if (kk < cend[j]) return (kv ? vcom : kcom) + static_cast<size_t>(kk) * HD;
+    __syncthreads();   // sQ written; the barriers' initialisation is visible
+    if (!have_k) {
+      failed |= !mbar_wait(&bars[0], 0, a.err, DEV_TIMEOUT_FULL);
+      have_k = true;
+    }
+    if (__syncthreads_or(failed)) {   // a stalled copy ends the CTA on every thread alike
+      failed = true;
+      break;
+    }
+    // the branch-pool row of query j's key kk (kk >= c_end of that query)
+    auto pool_row = [&](int j, int kk, int kv) -> const float* {
       const DevNode* nd = a.nodes + nrow[j];
       int t = kk - cend[j];
       if (t >= nd->n_tail) {   // cannot happen for a well-formed plan; never read out of bounds
@@ -116,18 +155,18 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
              ((((static_cast<size_t>(item.seq) * a.n_slots + slot) * a.L + item.layer) * 2 + kv) * a.KVH + kvh) * HD;
     };
     // scores of this lane's key against every query of the batch
-    float sc[kQBatch];
-    if (k < cend_min && k <= pos_max) {   // committed for every query: read the row once
-      float part[kQBatch][4];
+    float sc[QB];
+    if (k < cend_min && k <= pos_max) {   // committed for every query: one pass over the row
+      float part[QB][4];
 #pragma unroll
-      for (int j = 0; j < kQBatch; ++j) part[j][0] = part[j][1] = part[j][2] = part[j][3] = 0.0f;
-      const float4* kr = reinterpret_cast<const float4*>(kcom + static_cast<size_t>(k) * HD);
-#pragma unroll 16
+      for (int j = 0; j < QB; ++j) part[j][0] = part[j][1] = part[j][2] = part[j][3] = 0.0f;
+      const float4* kr = reinterpret_cast<const float4*>(sK + (k - g0) * HD);
+#pragma unroll 8
       for (int i = 0; i < NC; ++i) {
         const int c = (i + lane) & (NC - 1);
-        const float4 k4 = __ldg(kr + c);
+        const float4 k4 = kr[c];
 #pragma unroll
-        for (int j = 0; j < kQBatch; ++j) {
+        for (int j = 0; j < QB; ++j) {
           if (j < nb) {
             const float4 q4 = *reinterpret_cast<const float4*>(sQ + j * HD + c * 4);
             float& acc = part[j][i & 3];
@@ -139,18 +178,30 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
         }
       }
 #pragma unroll
-      for (int j = 0; j < kQBatch; ++j)
+      for (int j = 0; j < QB; ++j)
         sc[j] = (j < nb && k <= pos[j]) ? __fadd_rn(__fadd_rn(part[j][0], part[j][1]), __fadd_rn(part[j][2], part[j][3]))
                                         : -INFINITY;
     } else {
 #pragma unroll
-      for (int j = 0; j < kQBatch; ++j)
-        sc[j] = (j < nb && k <= pos[j]) ? dot_q_row<HD>(sQ + j * HD, key_row(j, k, 0), lane) : -INFINITY;
+      for (int j = 0; j < QB; ++j) {
+        sc[j] = -INFINITY;
+        if (j < nb && k <= pos[j])
+          sc[j] = dot_q_row<HD>(sQ + j * HD, k < cend[j] ? sK + (k - g0) * HD : pool_row(j, k, 0), lane);
+      }
+    }
+    if (v_smem) {
+      __syncthreads();   // every score read of the key rows is done
+      if (tid == 0) {
+        const uint32_t bytes = static_cast<uint32_t>(n_com) * HD * 4;
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&bars[1], bytes);
+        bulk_load_1d(sK, vcom + static_cast<size_t>(g0) * HD, bytes, &bars[1]);
+      }
     }
     // per query: slice softmax statistics and the value accumulation, keys in order
-    float mx[kQBatch], lsum[kQBatch], pr[kQBatch], acc[kQBatch][DPL];
+    float mx[QB], lsum[QB], pr[QB], acc[QB][DPL];
 #pragma unroll
-    for (int j = 0; j < kQBatch; ++j) {
+    for (int j = 0; j < QB; ++j) {
       mx[j] = warp_max(sc[j]);
       pr[j] = 0.0f;
       lsum[j] = 0.0f;
@@ -161,6 +212,47 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
 #pragma unroll
       for (int i = 0; i < DPL; ++i) acc[j][i] = 0.0f;
     }
+    if (v_smem) {
+      failed |= !mbar_wait(&bars[1], 0, a.err, DEV_TIMEOUT_FULL);
+      if (__syncthreads_or(failed)) {
+        failed = true;
+        break;
+      }
+      const int n_keys = min(32, pos_max - ks + 1);   // keys of the slice any query attends
+#pragma unroll 4
+      for (int u = 0; u < n_keys; ++u) {
+        const int key = ks + u;
+        const float* vs = sK + (key - g0) * HD + lane * DPL;
+        if (key < cend_min) {   // committed for every query
+          float vv[DPL];
+          if constexpr (DPL == 4) {
+            const float4 f = *reinterpret_cast<const float4*>(vs);
+            vv[0] = f.x; vv[1] = f.y; vv[2] = f.z; vv[3] = f.w;
+          } else {
+            const float2 f = *reinterpret_cast<const float2*>(vs);
+            vv[0] = f.x; vv[1] = f.y;
+          }
+#pragma unroll
+          for (int j = 0; j < QB; ++j) {
+            if (j < nb && key <= pos[j]) {
+              const float pk = __shfl_sync(0xffffffffu, pr[j], u);
+#pragma unroll
+              for (int i = 0; i < DPL; ++i) acc[j][i] = fmaf(pk, vv[i], acc[j][i]);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < QB; ++j) {
+            if (j < nb && key <= pos[j]) {
+              const float pk = __shfl_sync(0xffffffffu, pr[j], u);
+              const float* vr = key < cend[j] ? vs : pool_row(j, key, 1) + lane * DPL;
+#pragma unroll
+              for (int i = 0; i < DPL; ++i) acc[j][i] = fmaf(pk, vr[i], acc[j][i]);
+            }
+          }
+        }
+      }
+    } else {
     // value rows in batches of kVB keys: a batch's loads are all issued before any is used
     for (int jb = 0; jb < 32; jb += kVB) {
       if (ks + jb > pos_max) break;   // uniform across the warp
@@ -185,7 +277,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
         if (key <= pos_max) {       // uniform across the warp
           if (key < cend_min) {     // committed for every query: the row loaded above
 #pragma unroll
-            for (int j = 0; j < kQBatch; ++j) {
+            for (int j = 0; j < QB; ++j) {
               if (j < nb && key <= pos[j]) {
                 const float pk = __shfl_sync(0xffffffffu, pr[j], jj);
 #pragma unroll
@@ -194,10 +286,11 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
             }
           } else {
 #pragma unroll
-            for (int j = 0; j < kQBatch; ++j) {
+            for (int j = 0; j < QB; ++j) {
               if (j < nb && key <= pos[j]) {
                 const float pk = __shfl_sync(0xffffffffu, pr[j], jj);
-                const float* vr = key_row(j, key, 1) + lane * DPL;
+                const float* vr =
+                    (key < cend[j] ? vcom + static_cast<size_t>(key) * HD : pool_row(j, key, 1)) + lane * DPL;
 #pragma unroll
                 for (int i = 0; i < DPL; ++i) acc[j][i] = fmaf(pk, __ldg(vr + i), acc[j][i]);
               }
@@ -206,10 +299,11 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
         }
       }
     }
+    }
 #pragma unroll
-    for (int j = 0; j < kQBatch; ++j) {
+    for (int j = 0; j < QB; ++j) {
       if (j < nb) {
-        float* rec = sP + (j * 4 + warp) * PS;
+        float* rec = sP + (j * kAttnWarps + warp) * PS;
 #pragma unroll
         for (int i = 0; i < DPL; ++i) rec[lane * DPL + i] = acc[j][i];
         if (lane == 0) {
@@ -220,10 +314,10 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
     }
     __syncthreads();
     // combine the four slices of each query in slice order; write the group's record
-    for (int j = warp; j < nb; j += 4) {
+    for (int j = warp; j < nb; j += kAttnWarps) {
       const int qi = qb + j;
       const int row = item.row_begin + qi / G, qh = kvh * G + qi % G;
-      const float* r0 = sP + (j * 4) * PS;
+      const float* r0 = sP + (j * kAttnWarps) * PS;
       float mw[4], wgt[4];
       float M = -INFINITY;
 #pragma unroll
@@ -250,30 +344,37 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
     }
     __syncthreads();
   }
+  if (failed) return;   // error flag set; the host reports the stall
 
-  // the last group CTA of (item, KV head) merges the groups; lane gg holds group gg
+  // the last group CTA of (item, KV head) merges the groups; lane gg holds groups gg, gg + 32
   __threadfence();
   __syncthreads();
   if (tid == 0) s_last = (atomicAdd(a.counters + item.counter * a.KVH + kvh, 1) == item.n_groups - 1) ? 1 : 0;
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  for (int qi = warp; qi < nq; qi += 4) {
+  for (int qi = warp; qi < nq; qi += kAttnWarps) {
     const int row = item.row_begin + qi / G, qh = kvh * G + qi % G;
     const float* base = a.part + (static_cast<size_t>(row) * H + qh) * a.max_groups * PS;
-    float mg = -INFINITY, lg = 0.0f;
-    if (lane < item.n_groups) {
-      mg = __ldcg(base + lane * PS + HD);
-      lg = __ldcg(base + lane * PS + HD + 1);
+    float mg[2] = {-INFINITY, -INFINITY}, lg[2] = {0.0f, 0.0f};
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      const int gg = lane + 32 * h2;
+      if (gg < item.n_groups) {
+        mg[h2] = __ldcg(base + gg * PS + HD);
+        lg[h2] = __ldcg(base + gg * PS + HD + 1);
+      }
     }
-    const float M = warp_max(mg);
-    const float wg = (lg > 0.0f) ? exp2f(mg - M) : 0.0f;
-    const float Lsum = warp_sum(lg * wg);
+    const float M = warp_max(fmaxf(mg[0], mg[1]));
+    float wg[2];
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) wg[h2] = (lg[h2] > 0.0f) ? exp2f(mg[h2] - M) : 0.0f;
+    const float Lsum = warp_sum(__fadd_rn(lg[0] * wg[0], lg[1] * wg[1]));
     float O[DPL];
 #pragma unroll
     for (int i = 0; i < DPL; ++i) O[i] = 0.0f;
     for (int gg = 0; gg < item.n_groups; ++gg) {
-      const float w = __shfl_sync(0xffffffffu, wg, gg);
+      const float w = __shfl_sync(0xffffffffu, gg < 32 ? wg[0] : wg[1], gg & 31);
       if (w == 0.0f) continue;
 #pragma unroll
       for (int i = 0; i < DPL; ++i) O[i] = fmaf(w, __ldcg(base + gg * PS + lane * DPL + i), O[i]);
@@ -289,15 +390,14 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
   if (tid == 0) a.counters[item.counter * a.KVH + kvh] = 0;
 }
 
-static size_t attn_smem_bytes(int hd, int qb) { return static_cast<size_t>(qb) * hd * 4 + qb * 4 * (hd + 2) * 4; }
-
 template <int HD, int QB>
 static cudaError_t launch_attn_variant(cudaLaunchConfig_t cfg, const AttnArgs& a) {
   static bool set = false;
-  cfg.dynamicSmemBytes = attn_smem_bytes(HD, QB);
+  cfg.dynamicSmemBytes = attn_smem_floats(HD, QB) * 4;
   if (!set) {
     cudaError_t e = cudaFuncSetAttribute(attn_kernel<HD, QB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(cfg.dynamicSmemBytes));
+    if (e == cudaSuccess) e = apply_carveout(attn_kernel<HD, QB>);
     if (e != cudaSuccess) return e;
     set = true;
   }
@@ -317,7 +417,7 @@ cudaError_t launch_attention(const AttnArgs& a, int n_items, int max_groups_laun
   if (n_items <= 0) return cudaSuccess;
   if (!a.nodes || !a.items || !a.tails || !a.q || !a.kv_commit || !a.kv_pool || !a.out || !a.part || !a.counters ||
       !a.err || a.plane_rows < 1 || max_groups_launch < 1 || max_groups_launch > a.max_groups ||
-      max_groups_launch > 32 || max_nq < 1)
+      max_groups_launch > kAttnMaxGroups || max_nq < 1 || (reinterpret_cast<uintptr_t>(a.kv_commit) & 15))
     return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(max_groups_launch), static_cast<unsigned>(a.KVH),

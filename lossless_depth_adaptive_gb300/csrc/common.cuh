@@ -109,6 +109,12 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
 }
 
 // ---- programmatic dependent launch ---------------------------------------------------------
+// Orders this thread's earlier generic-proxy shared-memory accesses before its later
+// async-proxy (bulk copy) accesses to the same bytes.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

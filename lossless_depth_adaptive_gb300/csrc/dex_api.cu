@@ -514,7 +514,7 @@ int run_round(dex_handle* h, dex::Lattice* lat, std::vector<dex_copy_job>* pendi
         ++e;
       }
       it.row_end = e;
-      it.n_groups = it.max_pos / 128 + 1;
+      it.n_groups = it.max_pos / dex::kAttnGroupPos + 1;
       b.items.push_back(it);
       k = e;
     }
@@ -837,7 +837,7 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
   h->n_done.assign(cfg->batch, 0);
   h->n_slots = h->lat->n_slots();
   h->rows_cap = std::max(h->lat->max_round_nodes(), 256);
-  h->max_groups = (cfg->max_ctx + 127) / 128;
+  h->max_groups = (cfg->max_ctx + dex::kAttnGroupPos - 1) / dex::kAttnGroupPos;
   h->hrows = cfg->batch * h->n_slots + 256;
 
   const size_t B = cfg->batch, L = h->L, KVH = h->KVH, hd = h->hd, ctx = cfg->max_ctx, R = h->rows_cap;
@@ -1064,7 +1064,7 @@ int dex_prefill(dex_handle* h, int32_t seq, const int32_t* tokens, int32_t n_tok
     it.row_end = n;
     it.max_pos = c0 + n - 1;
     it.max_cend = c0 + n;
-    it.n_groups = it.max_pos / 128 + 1;
+    it.n_groups = it.max_pos / dex::kAttnGroupPos + 1;
     batches[0].items.push_back(it);
     const std::vector<Slot> slots = build_slots(batches, &t);
     Uploaded u;
@@ -1091,6 +1091,10 @@ int dex_prefill(dex_handle* h, int32_t seq, const int32_t* tokens, int32_t n_tok
       return cuda_fail(h, cudaGetLastError());
     const int32_t dev_err = static_cast<int32_t>(h->h_best[h->rows_cap] & 0xffffffffull);
     if (dev_err) return check_device_error(h, dev_err);
+    // per-launch timings cover decode rounds only: drop the prefill's events
+    h->gemm_events.clear();
+    h->attn_events.clear();
+    h->ev_used = 0;
   }
   h->lat->start(seq, n_tokens, tokens[n_tokens - 1]);
   h->lat_ar->start(seq, n_tokens, tokens[n_tokens - 1]);
@@ -1145,6 +1149,8 @@ int dex_get_stats(const dex_handle* h, dex_stats* out) {
 int dex_reset_stats(dex_handle* h) {
   if (!h) return DEX_EINVAL;
   h->stats = dex_stats{};
+  h->gemm_events.clear();
+  h->attn_events.clear();
   return DEX_OK;
 }
 int dex_set_timing(dex_handle* h, int32_t level) {

@@ -616,6 +616,7 @@ static cudaError_t launch_one(const CUtensorMap& a0, const CUtensorMap& a1, cons
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemOptin));
+    if (e == cudaSuccess) e = apply_carveout(gemm_tc_kernel<EPI>);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }

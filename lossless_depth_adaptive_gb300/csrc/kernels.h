@@ -35,11 +35,15 @@ struct DevNode {
 };
 static_assert(sizeof(DevNode) == 64, "DevNode is 64 bytes");
 
+// Key positions per attention CTA (four 32-key warp slices); groups are aligned to position 0.
+constexpr int kAttnGroupPos = 128;
+constexpr int kAttnMaxGroups = 32;   // max_ctx <= 4096
+
 // Attention work item: one sequence's contiguous node rows within a stage batch.
 struct AttnItem {
   int32_t seq, row_begin, row_end;   // absolute node rows
   int32_t max_pos, max_cend;         // largest input position / committed extent among the rows
-  int32_t n_groups;                  // 128-position key groups covering 0..max_pos
+  int32_t n_groups;                  // kAttnGroupPos-position key groups covering 0..max_pos
   int32_t counter;                   // index of this item's merge counters (x KVH)
   int32_t layer;                     // decoder layer of this item (items of several stages share a launch)
 };
@@ -174,6 +178,16 @@ int gemm_segments(int n_tiles, int kblocks, int n_ctas);
 // units and node tile nt (none is needed when every tile has one segment).
 inline size_t gemm_partial_bytes(int nt, size_t units) { return units * nt * 128 * 4; }
 // max_nq: the largest number of queries (node rows x query heads per KV head) of an item.
+// Preferred shared-memory carveout (percent) applied to every kernel of the library, or -1
+// for the driver's choice: DEX_SMEM_CARVEOUT, read once (diagnostics / tuning).
+int smem_carveout_pref();
+template <typename F>
+inline cudaError_t apply_carveout(F* func) {
+  const int c = smem_carveout_pref();
+  if (c < 0) return cudaSuccess;
+  return cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, c);
+}
+
 cudaError_t launch_attention(const AttnArgs& a, int n_items, int max_groups_launch, int max_nq, cudaStream_t st,
                              bool pdl);
 cudaError_t launch_assemble(const AssembleArgs& a, cudaStream_t st, bool pdl);

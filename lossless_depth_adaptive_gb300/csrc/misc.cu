@@ -5,6 +5,8 @@
 #include "common.cuh"
 #include "kernels.h"
 
+#include <stdlib.h>
+
 namespace dex {
 
 // Sums of squares of the d/128 feature tiles of one row, one value per thread per tile
@@ -66,8 +68,24 @@ __global__ void __launch_bounds__(128) assemble_kernel(const AssembleArgs a) {
   row_tile_ssq<kMaxTiles>(x, ndt, qbuf, a.ssq + static_cast<size_t>(row) * ndt);
 }
 
+int smem_carveout_pref() {
+  static const int pref = [] {
+    const char* e = getenv("DEX_SMEM_CARVEOUT");
+    if (!e) return -1;
+    const int v = atoi(e);
+    return (v >= 0 && v <= 100) ? v : -1;
+  }();
+  return pref;
+}
+
 cudaError_t launch_assemble(const AssembleArgs& a, cudaStream_t st, bool pdl) {
   if (a.n_rows <= 0) return cudaSuccess;
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e = apply_carveout(assemble_kernel);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
   if (!a.nodes || !a.embed || !a.attn_norm || !a.hidden || !a.hb || !a.ssq || a.d % 128 || a.d > 128 * 64 ||
       a.plane_rows < a.n_rows)
     return cudaErrorInvalidValue;
@@ -109,6 +127,12 @@ __global__ void __launch_bounds__(256) collapse_kernel(const CollapseArgs a) {
 
 cudaError_t launch_collapse(const CollapseArgs& a, cudaStream_t st, bool pdl) {
   if (a.n_jobs <= 0) return cudaSuccess;
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e = apply_carveout(collapse_kernel);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
   if (!a.jobs || !a.kv_commit || !a.kv_pool || a.row_bytes < 16 || a.row_bytes % 16 ||
       (reinterpret_cast<uintptr_t>(a.kv_commit) & 15) || (reinterpret_cast<uintptr_t>(a.kv_pool) & 15))
     return cudaErrorInvalidValue;
