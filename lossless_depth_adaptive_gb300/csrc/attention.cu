@@ -8,20 +8,19 @@
 //
 // Work split: CTA = (sequence item, KV head, 128-position key group), four warps, each
 // owning a 32-key slice of the group.  Scores take lane = key: the group's committed key
-// rows are contiguous fp32 in the cache, so one thread brings them into shared memory
-// with a single bulk copy (completion on an mbarrier) -- nothing is held in registers
-// while the bytes are in flight and nothing goes through L1 -- and each lane walks its
-// row's 16-byte chunks from chunk (key mod 32) onwards, so consecutive lanes touch
-// consecutive chunks and the shared-memory reads are conflict-free.  Values take lane = a
-// run of output dimensions, so a warp reads one whole value row per load (coalesced).
-// When the CTA's queries fit one pass (decode), the committed value rows
-// follow the keys into the same shared buffer with a second bulk copy once the scores are
-// taken; otherwise (prefill) the key rows stay in shared memory across query batches and
-// values are read from global memory eight rows ahead.  Branch keys (few per node) are
-// read from the pool.  A committed key is read once and used for every query of the batch.
+// rows go to shared memory with asynchronous 16-byte copies (nothing held in registers,
+// nothing through L1), chunk c of row r stored at chunk c ^ (r mod 32), so when every lane
+// reads chunk c of its own row the 32 reads hit distinct banks while the query's chunk c
+// is one broadcast read.  Values take lane = a run of output dimensions, so a warp reads
+// one whole value row per load.  When the CTA's queries fit one pass (decode), the
+// committed value rows follow the keys into the same shared buffer with a bulk copy once
+// the scores are taken; otherwise (prefill) the key rows stay in shared memory across
+// query batches and values are read from global memory eight rows ahead.  Branch keys
+// (few per node) are read from the pool.  A committed key is read once and used for every
+// query of the batch.
 //
 // The arithmetic for a query is fixed by absolute positions only -- 32-key slices aligned
-// to position 0, each score summed over the same chunk order wherever the key row lives,
+// to position 0, each score summed in chunk order wherever the key row lives,
 // slices combined in order within a group, groups combined in group order by the last
 // CTA to finish -- so a node's output is bit-identical whether its keys sit in the
 // committed cache or the branch pool and whatever batch it is in.
@@ -35,18 +34,17 @@ constexpr int kAttnThreads = 32 * kAttnWarps;
 static_assert(kAttnGroupPos == 32 * kAttnWarps && kAttnWarps == 4, "four 32-key warp slices per group");
 constexpr int kVB = 8;   // value rows loaded ahead
 
-// Four interleaved partial sums of q . k over the row's chunks, starting at chunk `rot`;
-// the same order for a row in shared or global memory.
+// Four interleaved partial sums of q . k over the row's chunks in chunk order; chunk c of
+// the row sits at c ^ swz (shared-memory key rows are swizzled by row, pool rows are not).
 template <int HD>
-__device__ __forceinline__ float dot_q_row(const float* q, const float* krow, int rot) {
+__device__ __forceinline__ float dot_q_row(const float* q, const float* krow, int swz) {
   constexpr int NC = HD / 4;
   float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-  for (int i = 0; i < NC; ++i) {
-    const int c = (i + rot) & (NC - 1);
-    const float4 k4 = *(reinterpret_cast<const float4*>(krow) + c);
+  for (int c = 0; c < NC; ++c) {
+    const float4 k4 = *(reinterpret_cast<const float4*>(krow) + (c ^ swz));
     const float4 q4 = *reinterpret_cast<const float4*>(q + c * 4);
-    float& a = s[i & 3];
+    float& a = s[c & 3];
     a = fmaf(q4.x, k4.x, a);
     a = fmaf(q4.y, k4.y, a);
     a = fmaf(q4.z, k4.z, a);
@@ -55,15 +53,19 @@ __device__ __forceinline__ float dot_q_row(const float* q, const float* krow, in
   return __fadd_rn(__fadd_rn(s[0], s[1]), __fadd_rn(s[2], s[3]));
 }
 
-__host__ __device__ constexpr size_t attn_smem_floats(int hd, int qb) {
+// Shared floats of a CTA: key/value rows, queries and (unless SP) the slice records.
+__host__ __device__ constexpr size_t attn_smem_floats(int hd, int qb, bool sp) {
   return static_cast<size_t>(kAttnGroupPos) * hd + static_cast<size_t>(qb) * hd +
-         static_cast<size_t>(qb) * kAttnWarps * (hd + 2);
+         (sp ? 0 : static_cast<size_t>(qb) * kAttnWarps * (hd + 2));
 }
+static_assert(kAttnGroupPos * 64 >= 8 * kAttnWarps * (64 + 2), "slice records fit the key buffer");
 
 // QB: queries per pass, chosen per launch from its largest item (the unused slots of a
-// batch would otherwise still issue their predicated instructions).  A query's arithmetic
-// is the same in every instantiation.
-template <int HD, int QB>
+// batch would otherwise still issue their predicated instructions).  SP: every item of the
+// launch fits one pass, so the slice records reuse the key/value buffer once the values
+// are consumed (a smaller CTA: three per SM instead of two).  A query's arithmetic is the
+// same in every instantiation.
+template <int HD, int QB, bool SP>
 __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
   constexpr int DPL = HD / 32;        // output dims per lane
   constexpr int NC = HD / 4;          // 16-byte chunks per row
@@ -71,8 +73,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
   extern __shared__ __align__(128) float smem_f[];
   float* sK = smem_f;                             // [kAttnGroupPos][HD] committed keys of the group
   float* sQ = sK + kAttnGroupPos * HD;            // [QB][HD]
-  float* sP = sQ + QB * HD;                       // [QB][warps][PS]
-  __shared__ __align__(8) uint64_t bars[2];       // key rows landed, value rows landed
+  float* sP = SP ? sK : sQ + QB * HD;             // [QB][warps][PS]
+  __shared__ __align__(8) uint64_t vbar;          // value rows landed (single-pass CTAs)
   __shared__ int s_last;
 
   const int g = blockIdx.x, kvh = blockIdx.y, it = blockIdx.z;
@@ -92,18 +94,27 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
   // committed rows some query of the item reads: [g0, g0 + n_com)
   const int n_com = max(0, min(kAttnGroupPos, min(item.max_cend, item.max_pos + 1) - g0));
   if (tid == 0) {
-    mbar_init(&bars[0], 1);
-    mbar_init(&bars[1], 1);
+    mbar_init(&vbar, 1);
     fence_mbar_init();
-    if (n_com > 0) {
-      const uint32_t bytes = static_cast<uint32_t>(n_com) * HD * 4;
-      mbar_arrive_expect_tx(&bars[0], bytes);
-      bulk_load_1d(sK, kcom + static_cast<size_t>(g0) * HD, bytes, &bars[0]);
-    }
   }
-  bool have_k = n_com == 0, failed = false;
+  // committed key rows -> shared memory, chunk c of row r at c ^ (r mod NC): lanes reading
+  // the same chunk of 32 consecutive rows hit distinct banks
+  {
+    const uint32_t base = smem_u32(sK);
+    const float* src = kcom + static_cast<size_t>(g0) * HD;
+    for (int idx = tid; idx < n_com * NC; idx += kAttnThreads) {
+      const int r = idx / NC, c = idx % NC;
+      cp_async_16(base + static_cast<uint32_t>(r * HD + ((c ^ (r & (NC - 1))) << 2)) * 4u, src + r * HD + c * 4);
+    }
+    cp_async_commit();
+  }
+  bool have_k = false, failed = false;
 
   const int nq = (item.row_end - item.row_begin) * G;
+  if (SP && nq > QB) {   // the launch promised one pass per item
+    if (tid == 0) atomicExch(a.err, DEV_BAD_INDEX);
+    return;
+  }
   // one query pass (decode): once scored, the key buffer takes the group's committed value
   // rows in one more bulk copy; several passes (prefill) keep the keys and read values from
   // global memory
@@ -135,12 +146,9 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
     }
     __syncthreads();   // sQ written; the barriers' initialisation is visible
     if (!have_k) {
-      failed |= !mbar_wait(&bars[0], 0, a.err, DEV_TIMEOUT_FULL);
+      cp_async_wait_all();
+      __syncthreads();   // every thread's key chunks have landed
       have_k = true;
-    }
-    if (__syncthreads_or(failed)) {   // a stalled copy ends the CTA on every thread alike
-      failed = true;
-      break;
     }
     // the branch-pool row of query j's key kk (kk >= c_end of that query)
     auto pool_row = [&](int j, int kk, int kv) -> const float* {
@@ -161,15 +169,15 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
 #pragma unroll
       for (int j = 0; j < QB; ++j) part[j][0] = part[j][1] = part[j][2] = part[j][3] = 0.0f;
       const float4* kr = reinterpret_cast<const float4*>(sK + (k - g0) * HD);
+      const int swz = (k - g0) & (NC - 1);
 #pragma unroll 8
-      for (int i = 0; i < NC; ++i) {
-        const int c = (i + lane) & (NC - 1);
-        const float4 k4 = kr[c];
+      for (int c = 0; c < NC; ++c) {
+        const float4 k4 = kr[c ^ swz];
 #pragma unroll
         for (int j = 0; j < QB; ++j) {
           if (j < nb) {
-            const float4 q4 = *reinterpret_cast<const float4*>(sQ + j * HD + c * 4);
-            float& acc = part[j][i & 3];
+            const float4 q4 = *reinterpret_cast<const float4*>(sQ + j * HD + c * 4);   // same address: broadcast
+            float& acc = part[j][c & 3];
             acc = fmaf(q4.x, k4.x, acc);
             acc = fmaf(q4.y, k4.y, acc);
             acc = fmaf(q4.z, k4.z, acc);
@@ -186,7 +194,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
       for (int j = 0; j < QB; ++j) {
         sc[j] = -INFINITY;
         if (j < nb && k <= pos[j])
-          sc[j] = dot_q_row<HD>(sQ + j * HD, k < cend[j] ? sK + (k - g0) * HD : pool_row(j, k, 0), lane);
+          sc[j] = k < cend[j] ? dot_q_row<HD>(sQ + j * HD, sK + (k - g0) * HD, (k - g0) & (NC - 1))
+                              : dot_q_row<HD>(sQ + j * HD, pool_row(j, k, 0), 0);
       }
     }
     if (v_smem) {
@@ -194,8 +203,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
       if (tid == 0) {
         const uint32_t bytes = static_cast<uint32_t>(n_com) * HD * 4;
         fence_proxy_async_smem();
-        mbar_arrive_expect_tx(&bars[1], bytes);
-        bulk_load_1d(sK, vcom + static_cast<size_t>(g0) * HD, bytes, &bars[1]);
+        mbar_arrive_expect_tx(&vbar, bytes);
+        bulk_load_1d(sK, vcom + static_cast<size_t>(g0) * HD, bytes, &vbar);
       }
     }
     // per query: slice softmax statistics and the value accumulation, keys in order
@@ -213,7 +222,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
       for (int i = 0; i < DPL; ++i) acc[j][i] = 0.0f;
     }
     if (v_smem) {
-      failed |= !mbar_wait(&bars[1], 0, a.err, DEV_TIMEOUT_FULL);
+      failed |= !mbar_wait(&vbar, 0, a.err, DEV_TIMEOUT_FULL);
       if (__syncthreads_or(failed)) {
         failed = true;
         break;
@@ -300,6 +309,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
       }
     }
     }
+    if constexpr (SP) __syncthreads();   // every warp is done with the value rows under sP
 #pragma unroll
     for (int j = 0; j < QB; ++j) {
       if (j < nb) {
@@ -390,26 +400,33 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
   if (tid == 0) a.counters[item.counter * a.KVH + kvh] = 0;
 }
 
-template <int HD, int QB>
+template <int HD, int QB, bool SP>
 static cudaError_t launch_attn_variant(cudaLaunchConfig_t cfg, const AttnArgs& a) {
   static bool set = false;
-  cfg.dynamicSmemBytes = attn_smem_floats(HD, QB) * 4;
+  cfg.dynamicSmemBytes = attn_smem_floats(HD, QB, SP) * 4;
   if (!set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<HD, QB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel<HD, QB, SP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(cfg.dynamicSmemBytes));
-    if (e == cudaSuccess) e = apply_carveout(attn_kernel<HD, QB>);
+    // three single-pass CTAs (about 69 KB each) fit only the largest shared-memory
+    // configuration, which the driver does not choose by itself for these sizes
+    if (e == cudaSuccess)
+      e = (SP && smem_carveout_pref() < 0)
+              ? cudaFuncSetAttribute(attn_kernel<HD, QB, SP>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     static_cast<int>(cudaSharedmemCarveoutMaxShared))
+              : apply_carveout(attn_kernel<HD, QB, SP>);
     if (e != cudaSuccess) return e;
     set = true;
   }
-  return cudaLaunchKernelEx(&cfg, attn_kernel<HD, QB>, a);
+  return cudaLaunchKernelEx(&cfg, attn_kernel<HD, QB, SP>, a);
 }
 
 template <int HD>
 static cudaError_t launch_attn_hd(const cudaLaunchConfig_t& cfg, const AttnArgs& a, int max_nq) {
-  if (max_nq <= 1) return launch_attn_variant<HD, 1>(cfg, a);
-  if (max_nq <= 2) return launch_attn_variant<HD, 2>(cfg, a);
-  if (max_nq <= 4) return launch_attn_variant<HD, 4>(cfg, a);
-  return launch_attn_variant<HD, 8>(cfg, a);
+  if (max_nq <= 1) return launch_attn_variant<HD, 1, true>(cfg, a);
+  if (max_nq <= 2) return launch_attn_variant<HD, 2, true>(cfg, a);
+  if (max_nq <= 4) return launch_attn_variant<HD, 4, true>(cfg, a);
+  if (max_nq <= 8) return launch_attn_variant<HD, 8, true>(cfg, a);
+  return launch_attn_variant<HD, 8, false>(cfg, a);
 }
 
 cudaError_t launch_attention(const AttnArgs& a, int n_items, int max_groups_launch, int max_nq, cudaStream_t st,

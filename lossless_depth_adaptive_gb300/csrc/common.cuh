@@ -109,6 +109,13 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
 }
 
 // ---- programmatic dependent launch ---------------------------------------------------------
+// Ampere-style asynchronous 16-byte copy global -> shared, cached in L2 only.
+__device__ __forceinline__ void cp_async_16(uint32_t dst_smem, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 // Orders this thread's earlier generic-proxy shared-memory accesses before its later
 // async-proxy (bulk copy) accesses to the same bytes.
 __device__ __forceinline__ void fence_proxy_async_smem() {

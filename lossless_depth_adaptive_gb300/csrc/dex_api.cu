@@ -493,8 +493,11 @@ int run_round(dex_handle* h, dex::Lattice* lat, std::vector<dex_copy_job>* pendi
     for (int i = 0; i < p.n_prior; ++i) t.priors.push_back(p.prior[i]);
     t.nodes.push_back(dn);
   }
-  // one batch per live stage: its layers (d_{s-1}, d_s] and one attention item per
-  // sequence's contiguous rows
+  // one batch per live stage: its layers (d_{s-1}, d_s] and attention items over each
+  // sequence's contiguous rows, at most one pass of queries per item (an item that fits one
+  // pass takes the smaller single-pass attention CTA; the committed keys the items of a
+  // sequence share are re-read from L2)
+  const int rows_per_item = std::max(1, dex::kAttnPassQueries / (h->H / h->KVH));
   std::vector<Batch> batches;
   for (int s = 0; s <= max_stage; ++s) {
     Batch b;
@@ -508,7 +511,7 @@ int run_round(dex_handle* h, dex::Lattice* lat, std::vector<dex_copy_job>* pendi
       dex::AttnItem it = {};
       it.seq = plan[k].seq;
       it.row_begin = k;
-      while (e < b.off + b.n && plan[e].seq == it.seq) {
+      while (e < b.off + b.n && plan[e].seq == it.seq && e - k < rows_per_item) {
         it.max_pos = std::max(it.max_pos, plan[e].pos);
         it.max_cend = std::max(it.max_cend, plan[e].c_end);
         ++e;
@@ -665,7 +668,12 @@ int run_round(dex_handle* h, dex::Lattice* lat, std::vector<dex_copy_job>* pendi
   const int64_t kv_row = 2ll * h->KVH * h->hd * 4;
   for (const Batch& b : batches) {
     const int nl = b.l1 - b.l0;
-    for (const auto& it : b.items) h->stats.kv_bytes += kv_row * nl * it.max_cend;
+    // committed keys and values once per (sequence, layer), however many items read them
+    for (size_t i = 0; i < b.items.size(); ++i) {
+      int cend = b.items[i].max_cend;
+      while (i + 1 < b.items.size() && b.items[i + 1].seq == b.items[i].seq) cend = std::max(cend, b.items[++i].max_cend);
+      h->stats.kv_bytes += kv_row * nl * cend;
+    }
     for (int k = b.off; k < b.off + b.n; ++k) {
       h->stats.node_layers += nl;
       h->stats.kv_bytes += kv_row * nl * plan[k].n_tail;
@@ -855,7 +863,7 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
   rc |= dalloc(h, &h->exit_ssq, R * (h->d / 128) * 4);
   rc |= dalloc(h, &h->q, R * qd * 4);
   rc |= dalloc(h, &h->attn_part, R * h->H * h->max_groups * (hd + 2) * 4);
-  rc |= dalloc(h, &h->attn_counters, static_cast<size_t>(B) * h->N * KVH * 4 + 256 * KVH * 4);
+  rc |= dalloc(h, &h->attn_counters, (static_cast<size_t>(B) * h->N + R) * KVH * 4);
   rc |= dalloc(h, &h->rope, ctx * (hd / 2) * sizeof(float2));
   rc |= dalloc(h, &h->best, (R + 1) * 8);
   rc |= dalloc(h, &h->err, 16);
@@ -896,13 +904,13 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
   if (dalloc(h, &h->partial, h->partial_bytes) || dalloc(h, &h->counters, ntiles_max * 4 * std::max(1, h->N)))
     return DEX_ENOMEM;
   h->plan_cap = (R * sizeof(dex::DevNode) + R * 16 * 8 +
-                 static_cast<size_t>(L) * (B * h->N + 8) * sizeof(dex::AttnItem) + 64 * 16 + 8192);
+                 static_cast<size_t>(L) * (B * h->N + R + 8) * sizeof(dex::AttnItem) + 64 * 16 + 8192);
   if (dalloc(h, &h->d_plan, h->plan_cap)) return DEX_ENOMEM;
   if (cudaMallocHost(&h->h_plan, h->plan_cap) != cudaSuccess) return DEX_ENOMEM;
   if (cudaMallocHost(&h->h_best, (R + 1) * 8) != cudaSuccess) return DEX_ENOMEM;
   // zero-initialised state
   cudaMemsetAsync(h->counters, 0, ntiles_max * 4 * std::max(1, h->N), h->st);
-  cudaMemsetAsync(h->attn_counters, 0, (static_cast<size_t>(B) * h->N * KVH + 256 * KVH) * 4, h->st);
+  cudaMemsetAsync(h->attn_counters, 0, (static_cast<size_t>(B) * h->N + R) * KVH * 4, h->st);
   cudaMemsetAsync(h->err, 0, 16, h->st);
   cudaMemsetAsync(h->kv_commit, 0, B * L * 2 * KVH * ctx * hd * 4, h->st);
   cudaMemsetAsync(h->kv_pool, 0, B * h->n_slots * L * 2 * KVH * hd * 4, h->st);

@@ -38,6 +38,7 @@ static_assert(sizeof(DevNode) == 64, "DevNode is 64 bytes");
 // Key positions per attention CTA (four 32-key warp slices); groups are aligned to position 0.
 constexpr int kAttnGroupPos = 128;
 constexpr int kAttnMaxGroups = 32;   // max_ctx <= 4096
+constexpr int kAttnPassQueries = 8;  // queries of one attention pass (the largest query batch)
 
 // Attention work item: one sequence's contiguous node rows within a stage batch.
 struct AttnItem {
