@@ -34,23 +34,40 @@ constexpr int kAttnThreads = 32 * kAttnWarps;
 static_assert(kAttnGroupPos == 32 * kAttnWarps && kAttnWarps == 4, "four 32-key warp slices per group");
 constexpr int kVB = 8;   // value rows loaded ahead
 
-// Four interleaved partial sums of q . k over the row's chunks in chunk order; chunk c of
-// the row sits at c ^ swz (shared-memory key rows are swizzled by row, pool rows are not).
+// q . k as four partial sums, one per feature residue mod 4 (features 4c + r go to sum r),
+// accumulated over the chunks in order, two sums per packed FMA (each element rounded as
+// fmaf), then (s0 + s1) + (s2 + s3).  The committed-key loop below follows the same order.
+__device__ __forceinline__ void dot_chunk(float2& s01, float2& s23, const float4& q4, const float4& k4) {
+  s01 = __ffma2_rn(make_float2(q4.x, q4.y), make_float2(k4.x, k4.y), s01);
+  s23 = __ffma2_rn(make_float2(q4.z, q4.w), make_float2(k4.z, k4.w), s23);
+}
+__device__ __forceinline__ float dot_finish(const float2& s01, const float2& s23) {
+  return __fadd_rn(__fadd_rn(s01.x, s01.y), __fadd_rn(s23.x, s23.y));
+}
+
+// Chunk c of the row sits at c ^ swz (shared-memory key rows are swizzled by row, pool rows
+// are not).
 template <int HD>
 __device__ __forceinline__ float dot_q_row(const float* q, const float* krow, int swz) {
   constexpr int NC = HD / 4;
-  float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  float2 s01 = make_float2(0.0f, 0.0f), s23 = make_float2(0.0f, 0.0f);
 #pragma unroll
-  for (int c = 0; c < NC; ++c) {
-    const float4 k4 = *(reinterpret_cast<const float4*>(krow) + (c ^ swz));
-    const float4 q4 = *reinterpret_cast<const float4*>(q + c * 4);
-    float& a = s[c & 3];
-    a = fmaf(q4.x, k4.x, a);
-    a = fmaf(q4.y, k4.y, a);
-    a = fmaf(q4.z, k4.z, a);
-    a = fmaf(q4.w, k4.w, a);
+  for (int c = 0; c < NC; ++c)
+    dot_chunk(s01, s23, *reinterpret_cast<const float4*>(q + c * 4), *(reinterpret_cast<const float4*>(krow) + (c ^ swz)));
+  return dot_finish(s01, s23);
+}
+
+// acc[i] += p * v[i] over the lane's output dims, two dims per packed FMA (each element
+// rounded as fmaf, so the order per element is that of a scalar loop).
+template <int DPL>
+__device__ __forceinline__ void axpy_dims(float (&acc)[DPL], float p, const float (&v)[DPL]) {
+  const float2 pp = make_float2(p, p);
+#pragma unroll
+  for (int i = 0; i < DPL; i += 2) {
+    const float2 r = __ffma2_rn(pp, make_float2(v[i], v[i + 1]), make_float2(acc[i], acc[i + 1]));
+    acc[i] = r.x;
+    acc[i + 1] = r.y;
   }
-  return __fadd_rn(__fadd_rn(s[0], s[1]), __fadd_rn(s[2], s[3]));
 }
 
 // Shared floats of a CTA: key/value rows, queries and (unless SP) the slice records.
@@ -165,9 +182,9 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
     // scores of this lane's key against every query of the batch
     float sc[QB];
     if (k < cend_min && k <= pos_max) {   // committed for every query: one pass over the row
-      float part[QB][4];
+      float2 s01[QB], s23[QB];
 #pragma unroll
-      for (int j = 0; j < QB; ++j) part[j][0] = part[j][1] = part[j][2] = part[j][3] = 0.0f;
+      for (int j = 0; j < QB; ++j) s01[j] = s23[j] = make_float2(0.0f, 0.0f);
       const float4* kr = reinterpret_cast<const float4*>(sK + (k - g0) * HD);
       const int swz = (k - g0) & (NC - 1);
 #pragma unroll 8
@@ -175,20 +192,12 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
         const float4 k4 = kr[c ^ swz];
 #pragma unroll
         for (int j = 0; j < QB; ++j) {
-          if (j < nb) {
-            const float4 q4 = *reinterpret_cast<const float4*>(sQ + j * HD + c * 4);   // same address: broadcast
-            float& acc = part[j][c & 3];
-            acc = fmaf(q4.x, k4.x, acc);
-            acc = fmaf(q4.y, k4.y, acc);
-            acc = fmaf(q4.z, k4.z, acc);
-            acc = fmaf(q4.w, k4.w, acc);
-          }
+          // same address in every lane: broadcast
+          if (j < nb) dot_chunk(s01[j], s23[j], *reinterpret_cast<const float4*>(sQ + j * HD + c * 4), k4);
         }
       }
 #pragma unroll
-      for (int j = 0; j < QB; ++j)
-        sc[j] = (j < nb && k <= pos[j]) ? __fadd_rn(__fadd_rn(part[j][0], part[j][1]), __fadd_rn(part[j][2], part[j][3]))
-                                        : -INFINITY;
+      for (int j = 0; j < QB; ++j) sc[j] = (j < nb && k <= pos[j]) ? dot_finish(s01[j], s23[j]) : -INFINITY;
     } else {
 #pragma unroll
       for (int j = 0; j < QB; ++j) {
@@ -245,8 +254,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
           for (int j = 0; j < QB; ++j) {
             if (j < nb && key <= pos[j]) {
               const float pk = __shfl_sync(0xffffffffu, pr[j], u);
-#pragma unroll
-              for (int i = 0; i < DPL; ++i) acc[j][i] = fmaf(pk, vv[i], acc[j][i]);
+              axpy_dims<DPL>(acc[j], pk, vv);
             }
           }
         } else {
@@ -255,8 +263,10 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
             if (j < nb && key <= pos[j]) {
               const float pk = __shfl_sync(0xffffffffu, pr[j], u);
               const float* vr = key < cend[j] ? vs : pool_row(j, key, 1) + lane * DPL;
+              float vt[DPL];
 #pragma unroll
-              for (int i = 0; i < DPL; ++i) acc[j][i] = fmaf(pk, vr[i], acc[j][i]);
+              for (int i = 0; i < DPL; ++i) vt[i] = vr[i];
+              axpy_dims<DPL>(acc[j], pk, vt);
             }
           }
         }
@@ -289,8 +299,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
             for (int j = 0; j < QB; ++j) {
               if (j < nb && key <= pos[j]) {
                 const float pk = __shfl_sync(0xffffffffu, pr[j], jj);
-#pragma unroll
-                for (int i = 0; i < DPL; ++i) acc[j][i] = fmaf(pk, vv[u][i], acc[j][i]);
+                axpy_dims<DPL>(acc[j], pk, vv[u]);
               }
             }
           } else {
@@ -300,8 +309,10 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
                 const float pk = __shfl_sync(0xffffffffu, pr[j], jj);
                 const float* vr =
                     (key < cend[j] ? vcom + static_cast<size_t>(key) * HD : pool_row(j, key, 1)) + lane * DPL;
+                float vt[DPL];
 #pragma unroll
-                for (int i = 0; i < DPL; ++i) acc[j][i] = fmaf(pk, __ldg(vr + i), acc[j][i]);
+                for (int i = 0; i < DPL; ++i) vt[i] = __ldg(vr + i);
+                axpy_dims<DPL>(acc[j], pk, vt);
               }
             }
           }
