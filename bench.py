@@ -158,7 +158,12 @@ def _weight_gb(shape):
 
 
 def _workload(args):
-    return di.workload(args.workload, **({"max_new": args.tokens} if args.tokens else {}))
+    over = {}
+    if args.tokens:
+        over["max_new"] = args.tokens
+    if getattr(args, "alpha", None) is not None:
+        over["alpha"] = args.alpha
+    return di.workload(args.workload, **over)
 
 
 def run_gpu(args):
@@ -475,6 +480,8 @@ def main():
     ap.add_argument("--workload", default="llama7b_x4", choices=sorted(di.WORKLOADS) + ["micro"],
                     help="micro: exit head + DECS and KV collapse in isolation")
     ap.add_argument("--tokens", type=int, default=0, help="override the new-token count")
+    ap.add_argument("--alpha", type=float, default=None,
+                    help="override the residual-branch scale (sets how often shallow exits agree)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--max-branch", type=int, default=0,
                     help="sparse lattice: nodes speculate at most this many tokens ahead (0: full lattice)")
