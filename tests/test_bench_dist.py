@@ -60,3 +60,15 @@ def test_single_rank_is_identity():
     import bench
     assert bench.reduce_over_ranks(3.5, "max", 1, None) == 3.5
     assert bench.replica_throughput(100.0, 2.0, 1, None) == 50.0
+
+
+def test_workload_overrides():
+    """--tokens and --alpha replace only their own fields of the named workload."""
+    sys.path.insert(0, ROOT)
+    import argparse
+    import bench
+    base = bench._workload(argparse.Namespace(workload="llama7b_x8_sample", tokens=0, alpha=None))
+    wl = bench._workload(argparse.Namespace(workload="llama7b_x8_sample", tokens=32, alpha=0.1))
+    assert (wl.max_new, wl.alpha) == (32, 0.1)
+    assert (base.max_new, base.alpha) == (256, 0.05)
+    assert (wl.X, wl.tau, wl.sample, wl.shape) == (base.X, base.tau, base.sample, base.shape)
