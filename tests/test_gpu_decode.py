@@ -21,6 +21,10 @@ SMALL = di.ModelShape(n_layers=4, d_model=1024, n_heads=8, n_kv_heads=8, head_di
                       vocab=8192, tied_head=False)
 SMALL_GQA = di.ModelShape(n_layers=4, d_model=1024, n_heads=16, n_kv_heads=4, head_dim=64, d_ff=2816,
                           vocab=8192, tied_head=False, rope_theta=1e6)
+# sixteen query heads per KV head: a node row alone exceeds one attention pass (8 queries),
+# so decode items take the multi-pass attention variant
+SMALL_GQA16 = di.ModelShape(n_layers=4, d_model=2048, n_heads=16, n_kv_heads=1, head_dim=128, d_ff=5632,
+                            vocab=8192, tied_head=False, rope_theta=1e6)
 TINY_UNTIED = di.ModelShape(**{**di.TINY.__dict__, "tied_head": False})
 
 
@@ -55,6 +59,7 @@ CASES = [
     ("tiny_untied_a1_x8", TINY_UNTIED, 1.0, [1, 2, 3, 4, 5, 6, 7, 8], 16),
     ("small_split_k", SMALL, 0.3, [1, 2, 3, 4], 16),
     ("small_gqa_hd64", SMALL_GQA, 0.3, [2, 4], 16),
+    ("small_gqa16", SMALL_GQA16, 0.3, [2, 4], 16),
 ]
 
 
