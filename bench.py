@@ -266,7 +266,9 @@ def run_gpu(args):
               "node_layers_per_token": stats["node_layers"] / commits,
               "rounds_per_token": stats["rounds"] / commits,
               "nodes_per_round": stats["nodes"] / stats["rounds"],
-              "kstar_hist": stats["kstar_hist"][:len(wl.X)]}
+              "kstar_hist": stats["kstar_hist"][:len(wl.X)],
+              # depth-side speedup (Eq. 12): L T / sum_t W(t), W(t) the depth charged to token t
+              "depth_side_speedup": shape.n_layers * commits / stats["depth_charge"] if stats["depth_charge"] else None}
     phases = {k: inst[k] / inst["rounds"] for k in ("ms_expand", "ms_exit", "ms_collapse", "ms_host")}
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "committed tokens/s", "n_gpus": world,
