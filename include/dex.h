@@ -57,8 +57,8 @@ typedef enum dex_status {
  * per layer in the order: attn_norm[d], wq[H*hd][d], wk[KVH*hd][d], wv[KVH*hd][d],
  * wo[d][H*hd], ffn_norm[d], wg[d_ff][d], wu[d_ff][d], wd[d][d_ff].  The array is
  * copied by dex_init().  Constraints: d_model % 128 == 0 and <= 8192, head_dim in {64, 128},
- * n_heads % n_kv_heads == 0, every row length a multiple of 8 elements, every weight
- * 16-byte aligned. */
+ * n_heads % n_kv_heads == 0, n_heads*head_dim and n_kv_heads*head_dim multiples of 128,
+ * d_ff a multiple of 8 (>= 64), every weight 16-byte aligned (DEX_EINVAL otherwise). */
 typedef struct dex_model {
   int32_t n_layers, d_model, n_heads, n_kv_heads, head_dim, d_ff, vocab;
   float rms_eps, rope_theta;
