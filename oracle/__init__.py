@@ -9,9 +9,10 @@ A plain, slow, fp64 restatement of what the GPU library computes, written from
                    that the sampling rule and DECS draw from;
 * ``model``     -- the Llama-style pre-norm decoder (RMSNorm, RoPE, causal softmax
                    attention with GQA, SwiGLU FFN) and the shared exit head;
-* ``dex``       -- autoregressive decoding, Algorithm 1 (expand / DECS / insert /
-                   validate_and_commit / collapse / advance), Algorithm 2 (DECS) and
-                   the brute-force EAD measurement.
+* ``dex``       -- autoregressive decoding, depth exploration decoding as the
+                   section 3.2 prose describes it (exploration cycles, commit,
+                   collapse), depth-coupled sampling (section 3.3) and the
+                   brute-force EAD measurement.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg may
 import this package.  It shares no code with ``lossless_depth_adaptive_gb300`` and

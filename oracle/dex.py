@@ -1,8 +1,10 @@
-"""Autoregressive decoding, DEX (Algorithm 1), DECS (Algorithm 2) and brute-force EAD.
+"""Autoregressive decoding, depth exploration decoding (DEX), depth-coupled sampling
+(DECS) and brute-force EAD -- oracle side.
 
-Restates "Depth Exploration for LLM Decoding" (arXiv 2606.29223) section 3 and
-Appendix C.1 step by step, with the readings below where the pages leave a step open.
-TEST INFRASTRUCTURE ONLY.
+Written from the prose of "Depth Exploration for LLM Decoding" (arXiv 2606.29223),
+section 3.2 (lattice expansion, commit, finite-state control and collapse) and
+section 3.3 / Appendix C.1 (depth-coupled sampling), with the readings below where
+the pages leave a step open.  TEST INFRASTRUCTURE ONLY.
 
 Lattice (section 3.2, Figure 2).  Exploration tokens ETK_i live in a binary tree in
 heap order: the root ETK_0 is the stage-0 node of the commit position p_c; node i has a
@@ -156,23 +158,25 @@ def margin(score: np.ndarray) -> float:
     return float(finite[-1] - finite[-2]) if finite.size >= 2 else float("inf")
 
 
-def decs(logits: np.ndarray, i: int, B: Dict[int, int], q: int, q_max: int, i_ref: int,
-         rule: Rule, seq: int, target_pos: int, enabled: bool = True) -> Tuple[int, float, List[int]]:
-    """Algorithm 2 (Depth-Coupled Sampling) for node i.
+def depth_coupled_token(logits: np.ndarray, shallower: Sequence[int], final_depth: bool, rule: Rule,
+                        seq: int, target_pos: int, enabled: bool = True) -> Tuple[int, float, List[int]]:
+    """One exploration token of a slot chain under depth-coupled sampling (section 3.3;
+    Appendix C.1).
 
-    Returns (token, decision margin, masked token ids).  With ``enabled=False`` no token
-    is masked ("vanilla" independent decoding, section 4.1 ablation).
+    ``shallower`` holds the tokens the chain already proposed at shallower depths.  They
+    are excluded from this depth's choice -- a repeat could never add a new match -- except
+    for the final-depth reference, which always sees the unmasked logits so the committed
+    token is exactly the decoding rule's token.  With ``enabled=False`` nothing is excluded
+    (the independent "vanilla" decoding of the section 4.1 ablation).
+
+    Returns (token, margin of the decision scores, excluded token ids).
     """
-    A = [B[a] for a in prior_nodes(i) if B.get(a) is not None]        # prior proposals
-    if (q == q_max and i == i_ref) or not enabled:
-        A = []                                                        # keep the reference
+    excluded = sorted(set(int(v) for v in shallower)) if (enabled and not final_depth) else []
     z = np.array(logits, dtype=np.float64, copy=True)
-    for v in A:
-        z[v] = -np.inf
+    if excluded:
+        z[excluded] = -np.inf
     score = decision_scores(z, rule, seq, target_pos)
-    y = first_argmax(score)
-    B[i] = y
-    return y, margin(score), sorted(set(A))
+    return first_argmax(score), margin(score), excluded
 
 
 # -------------------------------------------------------------------------------------
@@ -237,7 +241,7 @@ def ead_profile(ar: ARResult):
 
 
 # -------------------------------------------------------------------------------------
-# Algorithm 1: Depth Exploration Decoding
+# depth exploration over one sequence (section 3.2)
 # -------------------------------------------------------------------------------------
 
 @dataclass
@@ -280,7 +284,12 @@ class DEXResult:
 def dex_generate(model, prompt: Sequence[int], X: Sequence[int], T: int, rule: Rule = Rule(),
                  use_decs: bool = True, seq: int = 0, keep_logits: bool = False,
                  max_branch: int = 0, adapters: Optional[Sequence[Dict]] = None) -> DEXResult:
-    """Algorithm 1 over one sequence; returns the committed tokens Y and a full trace.
+    """Depth exploration decoding of T tokens for one sequence (section 3.2), with a trace.
+
+    The decode is a series of exploration cycles, one per committed token.  A cycle is
+    centred on the commit position p_c and runs explorer rounds until the anchor path
+    reaches the final depth; the final-depth anchor token is committed, and the lattice
+    is cut down to the part whose prefix is still valid (see ``_exploration_cycle``).
 
     max_branch > 0 builds a sparse lattice (the pruning of low-value branches that the
     paper's discussion of expansion growth proposes, with the final-depth commit kept): a
@@ -294,91 +303,107 @@ def dex_generate(model, prompt: Sequence[int], X: Sequence[int], T: int, rule: R
     """
     N = len(X)
     assert X[-1] == model.L and list(X) == sorted(set(X))
-    P = len(prompt)
-    cache = model.new_cache(P + T + N + 1)
     committed = [int(t) for t in prompt]
-    # init(x, {E_k}): committed KV for positions 0..P-2; the last prompt token is the root input.
-    if P > 1:
+    cache = model.new_cache(len(committed) + T + N + 1)
+    # the committed context: every prompt position but the last has its KV state; the last
+    # prompt token is the input of the first anchor (the root of the first lattice)
+    if len(committed) > 1:
         model.forward(committed[:-1], 0, cache)
-    anchor_hist = model.forward([committed[-1]], P - 1, cache, keep_depths=True)
-
-    Y: List[int] = []
-    B: Dict[int, int] = {}
-    q = 0
     res = DEXResult([], [], [], 0, 0, 0)
-    rounds_since_commit = 0
-    q_max, i_ref = N - 1, anchor_node(N - 1)
-    while len(Y) < T:
-        p_c = len(committed)
-        # expand: H_q = hidden states of the level-q nodes at their stage boundaries
-        H = {}
-        # a node exists when its parent does (after a collapse the re-rooted subtree may
-        # lack branches pruned in the old frame) and, with a cap, its path speculates at
-        # most max_branch tokens ahead
-        live = [i for i in level_nodes(q)
-                if (i == 0 or parent(i) in B) and (max_branch <= 0 or len(branch_parents(i)) <= max_branch)]
-        for i in live:
-            s = stage(i)
-            path = branch_parents(i)
-            if not path:                                  # anchor path: committed prefix
-                H[i] = anchor_hist[X[s] - 1]
-            else:                                         # branch prefix: committed + candidates
-                toks = [B[a] for a in path]
-                H[i] = model.forward(toks, p_c, cache, depth=X[s])[-1:]
-            res.node_layers += X[s] - (X[s - 1] if s > 0 else 0)
-        res.layer_passes += X[q]
-        res.rounds += 1
-        rounds_since_commit += 1
-        # DECS, then insert into the explore buffer
-        Z = {}
-        for i in live:
-            ad = adapters[stage(i)] if adapters is not None and stage(i) < N - 1 else None
-            z = model.exit_logits(H[i], ad)[0]
-            plen = len(branch_parents(i))
-            y, mg, masked = decs(z, i, dict(B), q, q_max, i_ref, rule, seq, p_c + plen,
-                                 enabled=use_decs)
-            Z[i] = y
-            res.nodes.append(NodeRecord(res.rounds - 1, q, i, stage(i), plen, p_c + plen, y, mg,
-                                        masked, z if keep_logits else None))
-        B.update(Z)
-        if q == N - 1:                                    # ReachFinalDepth
-            y, kstar = validate_and_commit(B, N)
-            Y.append(y)
-            res.commits.append(CommitRecord(y, kstar, rounds_since_commit, p_c))
-            rounds_since_commit = 0
-            if len(Y) >= T:                               # stop(Y)
-                break
-            B, q = collapse(B, N, kstar)
-            committed.append(y)
-            anchor_hist = model.forward([y], p_c, cache, keep_depths=True)
-        else:
-            q = q + 1                                     # advance(q)
-    res.tokens = Y
+    lattice: Dict[int, int] = {}      # explore buffer: heap index -> candidate token
+    rounds_done = 0                   # explorer rounds completed since the last commit
+    while len(res.tokens) < T:
+        y, kstar, lattice, rounds_done = _exploration_cycle(
+            model, committed, cache, X, lattice, rounds_done, rule, use_decs, seq, keep_logits, max_branch,
+            adapters, res)
+        res.tokens.append(y)
+        committed.append(y)
     return res
 
 
-def validate_and_commit(B: Dict[int, int], N: int) -> Tuple[int, int]:
-    """Section 3.2 commit: y = u_{N-1}; b = shallowest anchor branch with u_k = y, else b_{N-1}."""
-    u = [B[anchor_node(k)] for k in range(N)]
-    y = u[N - 1]
-    for k in range(N - 1):
-        if u[k] == y:
-            return y, k
-    return y, N - 1
+def _exploration_cycle(model, committed: List[int], cache, X: Sequence[int], lattice: Dict[int, int],
+                       rounds_done: int, rule: Rule, use_decs: bool, seq: int, keep_logits: bool,
+                       max_branch: int, adapters, res: DEXResult):
+    """One cycle around the commit position p_c = len(committed) (section 3.2).
+
+    Rounds continue from ``rounds_done`` (what survived the previous collapse).  In the
+    round after r completed rounds, every existing node of level r of the binary lattice
+    is evaluated: a node continues its slot chain one explorer deeper (a depth child) or
+    opens a new slot at the next position with its parent's candidate as prefix (a
+    position child).  Its hidden state is the model run on its prefix -- the committed
+    tokens plus the candidates of the position moves on its path -- to the boundary d_s of
+    its explorer s; its candidate comes from the shared exit head under depth-coupled
+    sampling.  After N rounds the anchor path (the slot chain of p_c itself) has reached
+    the final depth: its final-depth token is committed, the shallowest anchor depth that
+    already proposed it is the accepted branch k*, and the lattice collapses onto it.
+
+    Returns (committed token, k*, collapsed lattice, rounds it has already completed).
+    """
+    N = len(X)
+    p_c = len(committed)
+    # the anchor path at every depth: the committed prefix through the model, as AR computes it
+    anchor_states = model.forward([committed[-1]], p_c - 1, cache, keep_depths=True)
+    rounds_in_cycle = 0
+    while True:
+        level_q = rounds_done
+        evaluated: Dict[int, int] = {}
+        for i in level_nodes(level_q):
+            if i > 0 and parent(i) not in lattice:
+                continue                  # its branch was discarded (or never materialised)
+            prefix = [lattice[a] for a in branch_parents(i)]
+            if max_branch > 0 and len(prefix) > max_branch:
+                continue
+            s = stage(i)
+            if prefix:
+                h = model.forward(prefix, p_c, cache, depth=X[s])[-1:]
+            else:
+                h = anchor_states[X[s] - 1]
+            res.node_layers += X[s] - (X[s - 1] if s > 0 else 0)
+            ad = adapters[s] if adapters is not None and s < N - 1 else None
+            z = model.exit_logits(h, ad)[0]
+            shallower = [lattice[a] for a in prior_nodes(i) if a in lattice]
+            tok, mg, excluded = depth_coupled_token(z, shallower, s == N - 1, rule, seq, p_c + len(prefix),
+                                                    enabled=use_decs)
+            evaluated[i] = tok
+            res.nodes.append(NodeRecord(res.rounds, level_q, i, s, len(prefix), p_c + len(prefix), tok, mg,
+                                        excluded, z if keep_logits else None))
+        lattice.update(evaluated)
+        res.layer_passes += X[level_q]
+        res.rounds += 1
+        rounds_in_cycle += 1
+        if level_q < N - 1:
+            rounds_done += 1
+            continue
+        y, kstar = select_commit([lattice[anchor_node(k)] for k in range(N)])
+        res.commits.append(CommitRecord(y, kstar, rounds_in_cycle, p_c))
+        lattice, rounds_done = collapse(lattice, N, kstar)
+        return y, kstar, lattice, rounds_done
 
 
-def collapse(B: Dict[int, int], N: int, kstar: int) -> Tuple[Dict[int, int], int]:
-    """Keep the nodes whose prefix is the new committed prefix; return (B', q').
+def select_commit(anchor_tokens: Sequence[int]) -> Tuple[int, int]:
+    """Section 3.2, commit: the final-depth anchor token u_{N-1} is committed; the accepted
+    branch is the shallowest anchor depth k whose candidate u_k equals it (k = N-1 when
+    no shallower depth did)."""
+    y = int(anchor_tokens[-1])
+    kstar = next(k for k, u in enumerate(anchor_tokens) if u == y)
+    return y, kstar
 
-    The survivors are the subtree of m = P(b_{k*}); every other node's prefix contains a
-    rejected candidate.  With the fallback branch (k* = N-1) nothing survives, and neither
-    when a sparse lattice never materialised m.
+
+def collapse(lattice: Dict[int, int], N: int, kstar: int) -> Tuple[Dict[int, int], int]:
+    """Keep only the nodes whose prefix is the new committed prefix; return them
+    re-indexed from the new root, and the rounds the new lattice has already completed.
+
+    The valid nodes are the subtree of m = P(b_{k*}), the position child of the accepted
+    branch: every other node's prefix holds a token that was not committed.  m was created
+    k*+1 rounds into the cycle, so its subtree covers N - k* - 1 completed rounds.  With the
+    fallback branch (k* = N-1) nothing survives, and neither when a sparse lattice never
+    materialised m.
     """
     if kstar == N - 1:
         return {}, 0
     m = position_child(anchor_node(kstar))
-    if m not in B:   # sparse lattice: the new root was pruned, nothing to reuse
+    if m not in lattice:
         return {}, 0
     remap = subtree_remap(m, N - 1)
-    newB = {new: B[old] for old, new in remap.items() if old in B}
-    return newB, N - kstar - 1
+    kept = {new: lattice[old] for old, new in remap.items() if old in lattice}
+    return kept, N - kstar - 1

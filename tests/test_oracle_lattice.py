@@ -91,7 +91,7 @@ def test_collapse_state_and_commit():
     B[dex.anchor_node(3)] = 7
     B[dex.anchor_node(1)] = 7
     B[dex.anchor_node(2)] = 7
-    y, k = dex.validate_and_commit(B, N)
+    y, k = dex.select_commit([B[dex.anchor_node(j)] for j in range(N)])
     assert (y, k) == (7, 1)
     newB, q = dex.collapse(B, N, k)
     assert q == N - k - 1 == 2
@@ -99,6 +99,6 @@ def test_collapse_state_and_commit():
     # fallback
     B[dex.anchor_node(1)] = 8
     B[dex.anchor_node(2)] = 9
-    y, k = dex.validate_and_commit(B, N)
+    y, k = dex.select_commit([B[dex.anchor_node(j)] for j in range(N)])
     assert (y, k) == (7, 3)
     assert dex.collapse(B, N, k) == ({}, 0)
