@@ -16,8 +16,14 @@ over, so no flush is needed between steps.
 Multi-GPU: replicas only (one independent request stream per rank, launched with
 torch.distributed.run); ``value`` = all ranks' tokens / the slowest rank's time.
 
-``--impl reference`` times the fp64 CPU oracle (oracle/) on the same workload: each step
-is a bounded sample (prefill of the prompt plus one committed DEX token).
+``--impl reference`` times the fp64 CPU oracle (oracle/) on the same workload and the same
+decode-only unit: the prompt is prefilled once outside the timed region, and each step
+decodes a bounded sample of committed tokens from that prefilled state.
+
+Ablations (section 4.1 of the paper): ``--X 4,32`` replaces the exploration set (the
+single-exit variant explores only d_0 and L), ``--no-decs`` decodes every lattice node
+independently (vanilla), ``--ar`` times the library's plain autoregressive path on the same
+kernels (the lossless reference every DEX stream equals).
 """
 from __future__ import annotations
 
@@ -36,6 +42,7 @@ sys.path.insert(0, ROOT)
 import dex_inputs as di  # noqa: E402
 
 METRIC = "committed tokens/s (1 GB300, batch 1) and layers executed per committed token"
+KV_ELEM_BYTES = 4   # bytes per element of the library's K/V caches
 
 
 def _dist():
@@ -163,7 +170,21 @@ def _workload(args):
         over["max_new"] = args.tokens
     if getattr(args, "alpha", None) is not None:
         over["alpha"] = args.alpha
+    if getattr(args, "X", None):
+        over["X"] = [int(x) for x in args.X.split(",")]
+    if getattr(args, "no_decs", False):
+        over["decs"] = False
     return di.workload(args.workload, **over)
+
+
+def _config(args, wl, world, B):
+    """The workload description both arms print (same keys, so the lines compare)."""
+    return {"workload": wl.name, "model": MODEL_NAMES.get(wl.shape, "decoder"), "X": wl.X, "alpha": wl.alpha,
+            "global_batch": world * B, "prompt_len": wl.prompt_len, "new_tokens": wl.max_new,
+            "decode": "sample" if wl.sample else "greedy", "decs": bool(wl.decs),
+            "path": "ar" if getattr(args, "ar", False) else "dex", "parallelism": f"replicas{world}",
+            "max_branch": args.max_branch, "adapters": _adapter_cfg(args, wl),
+            "l2": f"weights {_weight_gb(wl.shape):.1f} GB streamed per round >> 129 MB L2; no flush"}
 
 
 def run_gpu(args):
@@ -204,9 +225,10 @@ def run_gpu(args):
         return reduce_over_ranks(x, "max", world, dev)
 
     # warm-up requests
+    AR = bool(args.ar)
     for _ in range(args.warmup):
         prefill_all()
-        dec.generate(out=out_host)
+        dec.generate(ar=AR, out=out_host)
     # ---- device-timed decode (value) ----
     dec.reset_stats()
     barrier()
@@ -217,7 +239,7 @@ def run_gpu(args):
             prefill_all()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(st)
-            toks = dec.generate(out=out_host)
+            toks = dec.generate(ar=AR, out=out_host)
             e1.record(st)
             e1.synchronize()
             ms += e0.elapsed_time(e1)
@@ -236,11 +258,11 @@ def run_gpu(args):
     t0 = time.perf_counter()
     for _ in range(args.steps):
         prefill_all()                        # host prompts -> device inside
-        dec.generate(out=out_host)           # tokens -> host inside
+        dec.generate(ar=AR, out=out_host)    # tokens -> host inside
     barrier()
     e2e_value = replica_throughput(args.steps * B * T, time.perf_counter() - t0, world, dev)
     st_e2e = dec.stats()
-    e2e = {"value": e2e_value, "unit": "tokens/s",
+    e2e = {"value": e2e_value, "unit": "committed tokens/s",
            "h2d_bytes_per_step": int(st_e2e["h2d_bytes"] / args.steps),
            "d2h_bytes_per_step": int(st_e2e["d2h_bytes"] / args.steps)}
     # ---- one instrumented request: per-GEMM events and phase split ----
@@ -248,7 +270,7 @@ def run_gpu(args):
     dec.reset_stats()
     prefill_all()
     dec.reset_stats()
-    dec.generate(out=out_host)
+    dec.generate(ar=AR, out=out_host)
     inst = dec.stats()
     dec.set_timing(0)
     dec.close()
@@ -257,10 +279,17 @@ def run_gpu(args):
     ratio = _gemm_traffic_ratio()
     bytes_per_launch = inst["gemm_bytes"] / max(1, inst["gemm_launches"])
     commits = stats["commits"]
-    algo_bytes = stats["weight_bytes"] + stats["kv_bytes"]
+    # algorithmic bytes: every live layer's weights once per round, the LM head once per
+    # round, the KV entries attention must read counted at 2 bytes per element (the cache's
+    # own element size is reported beside it)
+    kv_algo = stats["kv_bytes"] * 2 // KV_ELEM_BYTES
+    algo_bytes = stats["weight_bytes"] + kv_algo
     step_roof = {"algorithmic_bytes_per_step": int(algo_bytes / args.steps),
+                 "kv_bytes_per_step": int(kv_algo / args.steps), "kv_cache_elem_bytes": KV_ELEM_BYTES,
                  "roofline_ms_per_step": algo_bytes / args.steps / (hbm * 1e9) * 1e3,
-                 "frac": (algo_bytes / (hbm * 1e9)) / (ms / 1e3) if ms > 0 else None}
+                 "frac": (algo_bytes / (hbm * 1e9)) / (ms / 1e3) if ms > 0 else None,
+                 "frac_of": f"measured {hbm:.0f} GB/s ({src})",
+                 "frac_8tbs": (algo_bytes / 8e12) / (ms / 1e3) if ms > 0 else None}
     layers = {"depth_charge_per_token": stats["depth_charge"] / commits,
               "layer_passes_per_token": stats["layer_passes"] / commits,
               "node_layers_per_token": stats["node_layers"] / commits,
@@ -275,11 +304,7 @@ def run_gpu(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded weights and uniform-random prompt ids)",
-        "config": {"workload": wl.name, "model": MODEL_NAMES.get(wl.shape, "decoder"), "X": wl.X, "alpha": wl.alpha,
-                   "global_batch": world * B, "prompt_len": wl.prompt_len, "new_tokens": T,
-                   "decode": "sample" if wl.sample else "greedy", "parallelism": f"replicas{world}",
-                   "max_branch": args.max_branch, "adapters": _adapter_cfg(args, wl),
-                   "l2": f"weights {_weight_gb(wl.shape):.1f} GB streamed per round >> 129 MB L2; no flush"},
+        "config": _config(args, wl, world, B),
         "layers_per_token": {k: (round(v, 3) if isinstance(v, float) else v) for k, v in layers.items()},
         "step_roofline": step_roof,
         "phase_ms_per_round": {k: round(v, 4) for k, v in phases.items()},
@@ -291,6 +316,7 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "kernel": "gemm_tc_kernel (all linear layers, one instrumented request)",
                      "achieved": round(achieved, 1) if achieved else None, "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4) if achieved else None, "peak_source": src,
+                     "frac_8tbs": round(achieved / 8000.0, 4) if achieved else None,
                      "traffic": int(ratio * bytes_per_launch) if ratio else None,
                      "traffic_source": "ncu dram bytes / algorithmic bytes (profiles/gemm_tc_kernel_grouped_l4.md)"
                                        " x this run's algorithmic bytes per launch" if ratio else None,
@@ -301,7 +327,7 @@ def run_gpu(args):
         "clocks": clk.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(wl, w, prompt, args.max_branch, ads)
+        line["cpu_baseline"] = cpu_baseline(args, wl, w, prompt, ads)
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
@@ -419,24 +445,116 @@ def _oracle_adapters(ads):
     return [{k: (v if k == "alpha" else widen_bf16(di.bf16_bits(v))) for k, v in a.items()} for a in ads]
 
 
-def cpu_baseline(wl, w_gpu, prompt, max_branch=0, ads=None, n_tokens=1):
-    """Time the oracle on a bounded sample of the workload: prefill + n committed DEX tokens."""
+def _cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.split(":")[0].strip() in ("Model name", "Model"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith(("model name", "cpu part")):
+                return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
+
+
+class _OneCore:
+    """Run numpy's BLAS on one thread and the process on one core for the block (the
+    OpenBLAS thread count is set through its own C entry point, found among the loaded
+    libraries); ``ok`` is False when no BLAS control was found."""
+
+    def __enter__(self):
+        import ctypes
+        self.ok, self.restore, self.set_fn = False, None, None
+        try:
+            maps = open("/proc/self/maps").read().split("\n")
+        except OSError:
+            maps = []
+        libs = sorted({ln.split()[-1] for ln in maps if "openblas" in ln.lower() and ln.split()[-1].startswith("/")})
+        for path in libs:
+            try:
+                h = ctypes.CDLL(path, mode=getattr(os, "RTLD_NOLOAD", 4) | ctypes.RTLD_GLOBAL)
+            except OSError:
+                continue
+            for stem in ("scipy_openblas", "openblas"):
+                for suf in ("64_", ""):
+                    get = getattr(h, f"{stem}_get_num_threads{suf}", None)
+                    put = getattr(h, f"{stem}_set_num_threads{suf}", None)
+                    if get is not None and put is not None:
+                        self.restore, self.set_fn = get(), put
+                        put(1)
+                        self.ok = True
+                        break
+                if self.ok:
+                    break
+            if self.ok:
+                break
+        self.aff = os.sched_getaffinity(0)
+        os.sched_setaffinity(0, {min(self.aff)})
+        return self
+
+    def __exit__(self, *exc):
+        os.sched_setaffinity(0, self.aff)
+        if self.set_fn is not None:
+            self.set_fn(self.restore)
+
+
+CPU_SAMPLE_TOKENS = {"tiny": 16, "llama7b_x4": 2, "llama7b_x8_sample": 1, "qwen8b_x4_b8": 1}
+
+
+def _oracle_decode(args, wl, m, prompt, n_tokens, cache, ads_wide):
+    """Decode n_tokens committed tokens of the workload's path with the oracle, from a
+    prefilled cache; returns (tokens, rounds)."""
+    from oracle import dex as odex
+    rule = odex.Rule(sample=wl.sample, tau=wl.tau, seed=wl.gumbel_seed)
+    if getattr(args, "ar", False):
+        r = odex.ar_generate(m, prompt, n_tokens, rule=rule, cache=cache)
+        return len(r.tokens), len(r.tokens)
+    r = odex.dex_generate(m, prompt, wl.X, n_tokens, rule=rule, use_decs=wl.decs, max_branch=args.max_branch,
+                          adapters=ads_wide, cache=cache)
+    return len(r.tokens), r.rounds
+
+
+def cpu_baseline(args, wl, w_gpu, prompt, ads=None):
+    """Time the oracle on a bounded sample of the same decode the GPU line measures: the
+    prompt is prefilled once (timed on its own), then committed tokens are decoded from that
+    state on all host cores and, for one token, on one core."""
     from oracle import dex as odex
     m = _oracle_for(wl, w_gpu)
-    rule = odex.Rule(sample=wl.sample, tau=wl.tau, seed=wl.gumbel_seed)
     wide = _oracle_adapters(ads)
+    n = CPU_SAMPLE_TOKENS.get(wl.name, 1)
+    cap = len(prompt) + n + len(wl.X) + 2
     t0 = time.perf_counter()
-    r = odex.dex_generate(m, prompt, wl.X, n_tokens, rule=rule, use_decs=wl.decs, max_branch=max_branch,
-                          adapters=wide)
+    cache = odex.prefill(m, prompt, cap)
+    prefill_s = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    toks, rounds = _oracle_decode(args, wl, m, prompt, n, cache, wide)
     dt = time.perf_counter() - t0
-    return {"value": round(len(r.tokens) / dt, 5), "unit": "committed tokens/s", "cores": os.cpu_count(),
-            "kind": "oracle", "seconds": round(dt, 2),
-            "sample": f"fp64 oracle: prefill {len(prompt) - 1} positions + {n_tokens} committed DEX token(s) "
-                      f"({r.rounds} rounds) of the {wl.name} workload"}
+    one = None
+    with _OneCore() as oc:
+        t1 = time.perf_counter()
+        toks1, rounds1 = _oracle_decode(args, wl, m, prompt, 1, cache, wide)
+        dt1 = time.perf_counter() - t1
+        if oc.ok:
+            one = {"value": round(toks1 / dt1, 6), "cores": 1, "seconds": round(dt1, 2),
+                   "ms_per_round": round(dt1 / rounds1 * 1e3, 1)}
+    return {"value": round(toks / dt, 6), "unit": "committed tokens/s", "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle", "seconds": round(dt, 2), "ms_per_round": round(dt / rounds * 1e3, 1),
+            "prefill_s": round(prefill_s, 2), "prefill_positions": len(prompt) - 1, "one_core": one,
+            "cpu_model": _cpu_model(),
+            "sample": f"fp64 oracle: {toks} committed token(s) ({rounds} rounds) of the {wl.name} workload, "
+                      f"decoded from the prefilled prompt (prefill timed separately); one sequence"}
 
 
 def run_reference(args):
-    """The oracle as the reference arm, on rank 0 only."""
+    """The oracle as the reference arm, on rank 0 only: the same workload, unit and config
+    keys as the library's line.  Setup (weights, the fp64 model, the prompt's prefill) is
+    outside the timed region; each step decodes a bounded sample of committed tokens from
+    the prefilled state, like the library's decode-only ``value``."""
     rank, world, local = _dist()
     if rank != 0:
         return
@@ -444,31 +562,36 @@ def run_reference(args):
     wl = _workload(args)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     w = di.gen_weights(wl.shape, wl.alpha, seed=wl.weight_seed, device=dev)
-    prompt = di.gen_prompts(wl.shape, 1, wl.prompt_len, seed=wl.prompt_seed)[0].tolist()
+    prompt = di.gen_prompts(wl.shape, wl.batch, wl.prompt_len, seed=wl.prompt_seed)[0].tolist()
     from oracle import dex as odex
     m = _oracle_for(wl, w)
     del w
-    rule = odex.Rule(sample=wl.sample, tau=wl.tau, seed=wl.gumbel_seed)
-    kw = dict(rule=rule, use_decs=wl.decs, max_branch=args.max_branch,
-              adapters=_oracle_adapters(_adapters(args, wl, "cpu")))
-    for _ in range(args.warmup):
-        odex.dex_generate(m, prompt, wl.X, 1, **kw)
+    wide = _oracle_adapters(_adapters(args, wl, "cpu"))
+    n = CPU_SAMPLE_TOKENS.get(wl.name, 1)
     t0 = time.perf_counter()
-    n = 0
+    cache = odex.prefill(m, prompt, len(prompt) + n + len(wl.X) + 2)
+    prefill_s = time.perf_counter() - t0
+    for _ in range(args.warmup):
+        _oracle_decode(args, wl, m, prompt, n, cache, wide)
+    t0 = time.perf_counter()
+    toks = rounds = 0
     for _ in range(args.steps):
-        n += len(odex.dex_generate(m, prompt, wl.X, 1, **kw).tokens)
+        a, b = _oracle_decode(args, wl, m, prompt, n, cache, wide)
+        toks += a
+        rounds += b
     dt = time.perf_counter() - t0
-    v = n / dt
-    sample = f"fp64 oracle: per step, prefill {wl.prompt_len - 1} positions + 1 committed DEX token"
+    v = toks / dt
+    cores = len(os.sched_getaffinity(0))
+    sample = (f"fp64 oracle: per step, {n} committed token(s) of one sequence decoded from the prefilled "
+              f"{wl.prompt_len}-token prompt ({rounds / args.steps:.1f} rounds); prefill {prefill_s:.1f} s, untimed")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "committed tokens/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": wl.name, "model": MODEL_NAMES.get(wl.shape, "decoder"),
-                                        "X": wl.X, "global_batch": 1, "prompt_len": wl.prompt_len,
-                                        "max_branch": args.max_branch, "adapters": _adapter_cfg(args, wl)},
-        "cpu_baseline": {"value": round(v, 6), "unit": "committed tokens/s", "cores": os.cpu_count(),
-                         "kind": "oracle", "sample": sample},
+        "data": "synthetic (seeded weights and uniform-random prompt ids)",
+        "config": _config(args, wl, world, wl.batch),
+        "cpu_baseline": {"value": round(v, 6), "unit": "committed tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample, "cpu_model": _cpu_model(), "prefill_s": round(prefill_s, 2)},
         "e2e": {"value": round(v, 6), "unit": "committed tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0}}))
 
@@ -489,6 +612,9 @@ def main():
                     help="sparse lattice: nodes speculate at most this many tokens ahead (0: full lattice)")
     ap.add_argument("--adapters", type=float, default=None, metavar="GATE",
                     help="seeded inducing adapters (hidden width 2d) at the non-final exits, scalar gate GATE")
+    ap.add_argument("--X", default=None, help="exploration set override, e.g. 4,32 (single-exit variant)")
+    ap.add_argument("--no-decs", action="store_true", help="vanilla lattice: no depth-coupled masking")
+    ap.add_argument("--ar", action="store_true", help="time the plain autoregressive path on the same kernels")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "dex":
         ap.error("--warmup must be >= 3")

@@ -175,6 +175,18 @@ int dex_debug_logits(dex_handle* h, float* host_out, int32_t max_rows, int32_t* 
 const char* dex_strerror(int code);
 void dex_free(dex_handle* h);
 
+/* Failure-path self-test (diagnostics; the paper has no counterpart).  Runs the bounded
+ * mbarrier wait that every pipeline of the library uses against a barrier that nothing
+ * completes, with a limit of limit_us microseconds (1..1000000), on the handle's stream,
+ * and reads the device error flag back exactly as a decode round does.  Returns
+ * DEX_ETIMEOUT when the wait gave up as designed (the flag is then cleared and the handle
+ * stays usable), DEX_OK if it did not, DEX_EINVAL for a bad argument.  Synchronises the
+ * stream.  Allocation failures of dex_init can likewise be injected on the host: with the
+ * environment variable DEX_FAIL_ALLOC_AT=k set, the k-th device or pinned-host allocation
+ * of dex_init reports failure, and dex_init returns DEX_ENOMEM after releasing everything
+ * it had allocated. */
+int dex_selftest_stall(dex_handle* h, int32_t limit_us);
+
 /* ---- kernels in isolation ------------------------------------------------------ */
 
 /* One node of an isolated exit-head + DECS call. */
@@ -192,7 +204,9 @@ typedef struct dex_exit_node {
  * h: device bf16 [n][d]; final_norm: device bf16 [d]; lm_head: device bf16
  * [vocab][d]; nodes: device [n]; priors: device int32; tokens: device int32 [n];
  * logits: device fp32 [n][vocab] or NULL.  1 <= n <= 256, d % 128 == 0, d <= 8192.
- * Allocates its scratch with the stream-ordered allocator; stream-ordered, no sync. */
+ * Allocates its scratch with the stream-ordered allocator; stream-ordered, no sync, so
+ * device-side failures cannot be returned: if a bounded wait inside the GEMM gives up
+ * (the decoder would report DEX_ETIMEOUT), every token of the call is written as -1. */
 int dex_exit_head_decs(const void* h, int32_t n, int32_t d, const void* final_norm, float rms_eps,
                        const void* lm_head, int32_t vocab, const dex_exit_node* nodes,
                        const int32_t* priors, int32_t sample, float tau, uint64_t seed,
@@ -201,10 +215,16 @@ int dex_exit_head_decs(const void* h, int32_t n, int32_t d, const void* final_no
 /* Size of the fixed device scratch of dex_exit_head_decs_noalloc: 32 MiB per GPU. */
 #define DEX_NOALLOC_SCRATCH_BYTES (32u << 20)
 
-/* The same exit head + DECS as dex_exit_head_decs, for callers that must not allocate
- * device memory during the call (for example code running under another component's
- * stream capture or allocator, or with a memory budget fixed at start-up).  The paper has
- * no counterpart: this is a deployment convenience of this library.
+/* The exit head + DECS of dex_exit_head_decs, for callers that must not allocate device
+ * memory during the call (for example code running under another component's stream
+ * capture or allocator, or with a memory budget fixed at start-up).  The paper has no
+ * counterpart: this is a deployment convenience of this library.
+ * It runs the GEMM on one CTA per SM (a deeper weight ring; its split-K partials then fit
+ * the fixed scratch) where dex_exit_head_decs uses two, so the k-segment split and hence
+ * the last bits of the logits may differ between the two entry points; each is within the
+ * same tolerance of the fp64 exit head, and tokens agree wherever the decision margin is
+ * not within rounding of zero.  A stalled bounded wait writes every token as -1, as in
+ * dex_exit_head_decs (the stall flag lives in the scratch and is cleared by the next call).
  * Scratch comes from one file-scope device array of DEX_NOALLOC_SCRATCH_BYTES that every
  * GPU loading the library keeps until the process exits; no cudaMalloc/cudaFree or other
  * allocating routine is called.  The array's device address is looked up on the first call
@@ -232,9 +252,14 @@ typedef struct dex_copy_job {
   int32_t seq, slot, pos, n_layers;   /* layers 0..n_layers-1 of slot -> position pos */
 } dex_copy_job;
 
-/* Vectorised gather/scatter of n_jobs copy jobs (device array).  Stream-ordered. */
+/* Vectorised gather/scatter of n_jobs copy jobs (device array, 0 <= n_jobs <= 65535).
+ * committed / pool: device, 16-byte aligned, with geom's layouts; head_dim a multiple of 8.
+ * A job with seq outside [0, batch), slot outside [0, n_slots), pos outside [0, max_ctx) or
+ * n_layers outside [1, n_layers] is skipped without any memory access.  rejected: device
+ * int32 or NULL; when given, the call zeroes it (stream-ordered) and adds one per skipped
+ * job.  Stream-ordered, no sync.  DEX_EINVAL for a bad geometry or pointer. */
 int dex_kv_collapse(void* committed, const void* pool, const dex_kv_geom* geom,
-                    const dex_copy_job* jobs, int32_t n_jobs, void* stream);
+                    const dex_copy_job* jobs, int32_t n_jobs, int32_t* rejected, void* stream);
 
 /* ---- host-only lattice scheduler (no GPU needed) ---------------------------------- */
 

@@ -103,11 +103,12 @@ SIGNATURES = {
     "dex_debug_logits": (C.c_int, [P, C.POINTER(C.c_float), C.c_int32, I32P]),
     "dex_strerror": (C.c_char_p, [C.c_int]),
     "dex_free": (None, [P]),
+    "dex_selftest_stall": (C.c_int, [P, C.c_int32]),
     "dex_exit_head_decs": (C.c_int, [P, C.c_int32, C.c_int32, P, C.c_float, P, C.c_int32, P, P, C.c_int32,
                                      C.c_float, C.c_uint64, P, P, P]),
     "dex_exit_head_decs_noalloc": (C.c_int, [P, C.c_int32, C.c_int32, P, C.c_float, P, C.c_int32, P, P,
                                              C.c_int32, C.c_float, C.c_uint64, P, P, P]),
-    "dex_kv_collapse": (C.c_int, [P, P, C.POINTER(dex_kv_geom), P, C.c_int32, P]),
+    "dex_kv_collapse": (C.c_int, [P, P, C.POINTER(dex_kv_geom), P, C.c_int32, P, P]),
     "dex_lattice_new": (C.c_int, [I32P, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.POINTER(P)]),
     "dex_lattice_start": (C.c_int, [P, C.c_int32, C.c_int32, C.c_int32]),
     "dex_lattice_plan": (C.c_int, [P, C.POINTER(dex_plan_node), C.c_int32, I32P]),
@@ -244,9 +245,10 @@ def dex_exit_head_decs_noalloc(h_ptr: int, n: int, d: int, final_norm_ptr: int, 
 
 
 def dex_kv_collapse(committed_ptr: int, pool_ptr: int, geom: dex_kv_geom, jobs_ptr: int, n_jobs: int,
-                    stream: int = 0) -> None:
-    check(lib().dex_kv_collapse(P(committed_ptr), P(pool_ptr), C.byref(geom), P(jobs_ptr), n_jobs, P(stream)),
-          "dex_kv_collapse")
+                    stream: int = 0, rejected_ptr: int = 0) -> None:
+    """rejected_ptr: device int32 that receives the number of out-of-range jobs skipped (or 0)."""
+    check(lib().dex_kv_collapse(P(committed_ptr), P(pool_ptr), C.byref(geom), P(jobs_ptr), n_jobs,
+                                P(rejected_ptr or None), P(stream)), "dex_kv_collapse")
 
 
 # ---- model marshalling (PyTorch tensors -> dex_model) -------------------------------------------
@@ -320,6 +322,10 @@ class Decoder:
 
     def debug_logits(self):
         return dex_debug_logits(self.h, self.shape.vocab)
+
+    def selftest_stall(self, limit_us: int) -> int:
+        """Return code of dex_selftest_stall (DEX_ETIMEOUT when the bounded wait gave up)."""
+        return lib().dex_selftest_stall(self.h, int(limit_us))
 
     def close(self) -> None:
         if self.h:

@@ -21,6 +21,7 @@
 #include <vector>
 
 #include "../../include/dex.h"
+#include "common.cuh"
 #include "kernels.h"
 #include "lattice.h"
 
@@ -131,6 +132,18 @@ struct dex_handle {
   unsigned long long* timeline = nullptr;
   int tl_cap = 0, tl_used = 0;
   std::vector<int32_t> tl_meta;   // per launch: epi, n_groups, nt, n_tiles, n_segs, kblocks, n_ctas, rows
+  // host-side allocation-failure injection (DEX_FAIL_ALLOC_AT=k: the k-th allocation of
+  // dex_init fails), for tests of the DEX_ENOMEM path
+  int alloc_fail_at = 0, alloc_count = 0;
+
+  // Releases everything the handle owns; runs on dex_free and on every failing dex_init.
+  ~dex_handle() {
+    cudaStreamSynchronize(st);
+    for (void* p : allocs) cudaFree(p);
+    if (h_plan) cudaFreeHost(h_plan);
+    if (h_best) cudaFreeHost(h_best);
+    for (auto e : ev_pool) cudaEventDestroy(e);
+  }
 };
 
 namespace {
@@ -147,11 +160,23 @@ int cuda_fail(dex_handle* h, cudaError_t e) {
   return DEX_ECUDA;
 }
 
+bool injected_alloc_failure(dex_handle* h) {
+  return h->alloc_fail_at > 0 && ++h->alloc_count == h->alloc_fail_at;
+}
+
 template <typename T>
 int dalloc(dex_handle* h, T** p, size_t bytes) {
   void* v = nullptr;
-  if (cudaMalloc(&v, bytes ? bytes : 16) != cudaSuccess) return DEX_ENOMEM;
+  if (injected_alloc_failure(h) || cudaMalloc(&v, bytes ? bytes : 16) != cudaSuccess) return DEX_ENOMEM;
   h->allocs.push_back(v);
+  *p = reinterpret_cast<T*>(v);
+  return DEX_OK;
+}
+
+template <typename T>
+int halloc(dex_handle* h, T** p, size_t bytes) {   // pinned host memory, freed by the handle
+  void* v = nullptr;
+  if (injected_alloc_failure(h) || cudaMallocHost(&v, bytes ? bytes : 16) != cudaSuccess) return DEX_ENOMEM;
   *p = reinterpret_cast<T*>(v);
   return DEX_OK;
 }
@@ -542,6 +567,8 @@ int run_round(dex_handle* h, dex::Lattice* lat, std::vector<dex_copy_job>* pendi
     ca.n_jobs = static_cast<int>(t.jobs.size());
     ca.kv_commit = h->kv_commit;
     ca.kv_pool = h->kv_pool;
+    ca.batch = h->cfg.batch;
+    ca.err = h->err;
     ca.L = h->L;
     ca.KVH = h->KVH;
     ca.row_bytes = h->hd * 4;
@@ -762,11 +789,7 @@ void dex_free(dex_handle* h) {
   if (!h) return;
   cudaStreamSynchronize(h->st);
   write_timeline(h);
-  for (void* p : h->allocs) cudaFree(p);
-  if (h->h_plan) cudaFreeHost(h->h_plan);
-  if (h->h_best) cudaFreeHost(h->h_best);
-  for (auto e : h->ev_pool) cudaEventDestroy(e);
-  delete h;
+  delete h;   // the destructor releases device, pinned and event resources
 }
 
 int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode_cfg* cfg, void* stream,
@@ -826,6 +849,7 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
   }
   h->cfg = *cfg;
   h->st = static_cast<cudaStream_t>(stream);
+  if (const char* f = getenv("DEX_FAIL_ALLOC_AT")) h->alloc_fail_at = atoi(f);
   h->n_sm = prop.multiProcessorCount;
   // GEMM launch shape (tunable for experiments; the partition, hence every result,
   // depends on it, so it is fixed for the handle's lifetime)
@@ -906,8 +930,7 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
   h->plan_cap = (R * sizeof(dex::DevNode) + R * 16 * 8 +
                  static_cast<size_t>(L) * (B * h->N + R + 8) * sizeof(dex::AttnItem) + 64 * 16 + 8192);
   if (dalloc(h, &h->d_plan, h->plan_cap)) return DEX_ENOMEM;
-  if (cudaMallocHost(&h->h_plan, h->plan_cap) != cudaSuccess) return DEX_ENOMEM;
-  if (cudaMallocHost(&h->h_best, (R + 1) * 8) != cudaSuccess) return DEX_ENOMEM;
+  if (halloc(h, &h->h_plan, h->plan_cap) || halloc(h, &h->h_best, (R + 1) * 8)) return DEX_ENOMEM;
   // zero-initialised state
   cudaMemsetAsync(h->counters, 0, ntiles_max * 4 * std::max(1, h->N), h->st);
   cudaMemsetAsync(h->attn_counters, 0, (static_cast<size_t>(B) * h->N + R) * KVH * 4, h->st);
@@ -1206,19 +1229,46 @@ int dex_debug_logits(dex_handle* h, float* host_out, int32_t max_rows, int32_t* 
   return DEX_OK;
 }
 
+// ---- failure-path self-test --------------------------------------------------------------
+
+// The bounded mbarrier wait every pipeline of the library uses, against a barrier that
+// nothing arrives on: it gives up after limit_ns and raises the device error flag exactly
+// as a stalled GEMM or attention pipeline would.  No copy or MMA is issued against the
+// barrier, so nothing is in flight when the kernel returns.
+__global__ void stall_probe_kernel(int32_t* err, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    dex::mbar_init(&bar, 1);
+    dex::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) dex::mbar_wait(&bar, 0, err, dex::DEV_TIMEOUT_FULL, limit_ns);
+}
+
+int dex_selftest_stall(dex_handle* h, int32_t limit_us) {
+  if (!h || limit_us < 1 || limit_us > 1000000) return DEX_EINVAL;
+  if (h->broken) return DEX_ECUDA;
+  const unsigned long long limit_ns = static_cast<unsigned long long>(limit_us) * 1000ull;
+  int32_t* err = h->err;
+  void* args[] = {&err, const_cast<unsigned long long*>(&limit_ns)};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(32);
+  cfg.stream = h->st;
+  if (cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(stall_probe_kernel), args) != cudaSuccess)
+    return cuda_fail(h, cudaGetLastError());
+  // the same read-back and check as the end of a decode round
+  if (cudaMemcpyAsync(h->h_best + h->rows_cap, h->err, sizeof(int32_t), cudaMemcpyDeviceToHost, h->st) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(h->st) != cudaSuccess)
+    return cuda_fail(h, cudaGetLastError());
+  const int32_t flag = static_cast<int32_t>(h->h_best[h->rows_cap] & 0xffffffffull);
+  return check_device_error(h, flag);
+}
+
 // ---- kernels in isolation ---------------------------------------------------------------
 
-__global__ void exit_nodes_kernel(const dex_exit_node* in, int n, dex::DevNode* out) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n) return;
-  dex::DevNode d = {};
-  d.seq = in[i].seq;
-  d.target_pos = in[i].target_pos;
-  d.unmasked = in[i].unmasked;
-  d.prior_off = in[i].prior_off;
-  d.n_prior = in[i].n_prior;
-  out[i] = d;
-}
+static_assert(sizeof(dex_exit_node) == 5 * sizeof(int32_t), "dex_exit_node is five int32 fields");
 
 int dex_exit_head_decs(const void* hidden, int32_t n, int32_t d, const void* final_norm, float rms_eps,
                        const void* lm_head, int32_t vocab, const dex_exit_node* nodes, const int32_t* priors,
@@ -1260,7 +1310,7 @@ int dex_exit_head_decs(const void* hidden, int32_t n, int32_t d, const void* fin
     if (dex::launch_exit_prep(static_cast<const bf16*>(hidden), n, d, static_cast<const bf16*>(final_norm), hb, nt, ssq,
                               best, st) != cudaSuccess)
       rc = DEX_ECUDA;
-    exit_nodes_kernel<<<(n + 127) / 128, 128, 0, st>>>(nodes, n, dn);
+    if (!rc && dex::launch_exit_nodes(nodes, n, dn, st) != cudaSuccess) rc = DEX_ECUDA;
     dex::GemmArgs a = {};
     a.n_groups = 1;
     a.n_ctas = ctas;
@@ -1290,28 +1340,34 @@ int dex_exit_head_decs(const void* hidden, int32_t n, int32_t d, const void* fin
     a.tau = tau;
     a.seed = seed;
     if (!rc && dex::launch_gemm(dex::EPI_EXIT, tm_w, tm_w, tm_w, tm_b, a, st, false) != cudaSuccess) rc = DEX_ECUDA;
-    if (!rc && dex::launch_decode_best(best, n, tokens, st) != cudaSuccess) rc = DEX_ECUDA;
+    if (!rc && dex::launch_decode_best(best, n, a.err, tokens, st) != cudaSuccess) rc = DEX_ECUDA;
   }
   cudaFreeAsync(scratch, st);
   return rc;
 }
 
 int dex_kv_collapse(void* committed, const void* pool, const dex_kv_geom* g, const dex_copy_job* jobs, int32_t n_jobs,
-                    void* stream) {
-  if (!committed || !pool || !g || (!jobs && n_jobs) || n_jobs < 0 || n_jobs > 65535 || g->head_dim % 8 ||
-      g->n_layers < 1 || g->n_kv_heads < 1 || g->max_ctx < 1 || g->n_slots < 1)
+                    int32_t* rejected, void* stream) {
+  if (!committed || !pool || !g || (!jobs && n_jobs) || n_jobs < 0 || n_jobs > 65535 || g->head_dim < 8 ||
+      g->head_dim % 8 || g->batch < 1 || g->n_layers < 1 || g->n_kv_heads < 1 || g->max_ctx < 1 || g->n_slots < 1)
     return DEX_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (rejected && cudaMemsetAsync(rejected, 0, sizeof(int32_t), st) != cudaSuccess) return DEX_ECUDA;
   dex::CollapseArgs a = {};
   a.jobs = reinterpret_cast<const dex::CopyJob*>(jobs);
   a.n_jobs = n_jobs;
   a.kv_commit = committed;
   a.kv_pool = pool;
+  a.batch = g->batch;
   a.L = g->n_layers;
   a.KVH = g->n_kv_heads;
   a.row_bytes = g->head_dim * 2;   // bf16 caches
   a.max_ctx = g->max_ctx;
   a.n_slots = g->n_slots;
-  return dex::launch_collapse(a, static_cast<cudaStream_t>(stream), false) == cudaSuccess ? DEX_OK : DEX_ECUDA;
+  a.rejected = rejected;
+  const cudaError_t e = dex::launch_collapse(a, st, false);
+  if (e == cudaErrorInvalidValue) return DEX_EINVAL;
+  return e == cudaSuccess ? DEX_OK : DEX_ECUDA;
 }
 
 }  // extern "C"
@@ -1391,8 +1447,7 @@ extern "C" int dex_exit_head_decs_noalloc(const void* hidden, int32_t n, int32_t
   if (dex::launch_exit_prep(static_cast<const bf16*>(hidden), n, d, static_cast<const bf16*>(final_norm), hb, nt, ssq,
                             best, st) != cudaSuccess)
     return DEX_ECUDA;
-  exit_nodes_kernel<<<(n + 127) / 128, 128, 0, st>>>(nodes, n, dn);
-  if (cudaGetLastError() != cudaSuccess) return DEX_ECUDA;
+  if (dex::launch_exit_nodes(nodes, n, dn, st) != cudaSuccess) return DEX_ECUDA;
   dex::GemmArgs a = {};
   a.n_groups = 1;
   a.n_ctas = n_sm;
@@ -1422,6 +1477,6 @@ extern "C" int dex_exit_head_decs_noalloc(const void* hidden, int32_t n, int32_t
   a.tau = tau;
   a.seed = seed;
   if (dex::launch_gemm(dex::EPI_EXIT, tm_w, tm_w, tm_w, tm_b, a, st, false) != cudaSuccess) return DEX_ECUDA;
-  if (dex::launch_decode_best(best, n, tokens, st) != cudaSuccess) return DEX_ECUDA;
+  if (dex::launch_decode_best(best, n, a.err, tokens, st) != cudaSuccess) return DEX_ECUDA;
   return DEX_OK;
 }

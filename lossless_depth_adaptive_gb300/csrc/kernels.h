@@ -155,12 +155,17 @@ struct CopyJob { int32_t seq, slot, pos, n_layers; };
 
 // KV rows are copied as raw bytes: row_bytes = head_dim x element size (fp32 caches of the
 // decoder, bf16 caches of the isolated entry point), a multiple of 16.
+// A job whose sequence, slot, position or layer count is out of range is skipped (nothing
+// is read or written for it): it sets *err to DEV_BAD_INDEX and adds one to *rejected
+// (either may be null).
 struct CollapseArgs {
   const CopyJob* jobs;
   int32_t n_jobs;
   void* kv_commit;
   const void* kv_pool;
-  int32_t L, KVH, row_bytes, max_ctx, n_slots;
+  int32_t batch, L, KVH, row_bytes, max_ctx, n_slots;
+  int32_t* err;
+  int32_t* rejected;
 };
 
 // ---- launchers (return cudaError_t of the launch) -----------------------------------------
@@ -209,6 +214,12 @@ struct PackSrc { const __nv_bfloat16* ptr; int32_t rows; };
 size_t packed_bytes(int n_tiles, int kblocks);
 cudaError_t launch_pack(int mode, PackSrc s0, PackSrc s1, PackSrc s2, int K, int n_tiles, uint8_t* out,
                         cudaStream_t st);
-cudaError_t launch_decode_best(const unsigned long long* best, int n, int32_t* tokens, cudaStream_t st);
+// tokens[i] = the token packed in best[i]; every token is -1 when *err is set (a bounded
+// wait of the exit-head GEMM gave up, so the argmax slots are incomplete).
+cudaError_t launch_decode_best(const unsigned long long* best, int n, const int32_t* err, int32_t* tokens,
+                               cudaStream_t st);
+// Node table of an isolated exit-head call (host struct dex_exit_node, device array) ->
+// the kernels' DevNode rows.
+cudaError_t launch_exit_nodes(const void* exit_nodes, int n, DevNode* out, cudaStream_t st);
 
 }  // namespace dex

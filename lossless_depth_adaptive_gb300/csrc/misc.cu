@@ -109,6 +109,14 @@ __global__ void __launch_bounds__(256) collapse_kernel(const CollapseArgs a) {
   griddep_wait();
   griddep_launch_dependents();
   const CopyJob job = a.jobs[blockIdx.y];
+  if (job.seq < 0 || job.seq >= a.batch || job.slot < 0 || job.slot >= a.n_slots || job.pos < 0 ||
+      job.pos >= a.max_ctx || job.n_layers < 1 || job.n_layers > a.L) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+      if (a.err) atomicExch(a.err, DEV_BAD_INDEX);
+      if (a.rejected) atomicAdd(a.rejected, 1);
+    }
+    return;
+  }
   const int vec_per_row = a.row_bytes / 16;
   const int total = job.n_layers * 2 * a.KVH * vec_per_row;
   const uint4* src = reinterpret_cast<const uint4*>(a.kv_pool) +
@@ -133,7 +141,8 @@ cudaError_t launch_collapse(const CollapseArgs& a, cudaStream_t st, bool pdl) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  if (!a.jobs || !a.kv_commit || !a.kv_pool || a.row_bytes < 16 || a.row_bytes % 16 ||
+  if (!a.jobs || !a.kv_commit || !a.kv_pool || a.row_bytes < 16 || a.row_bytes % 16 || a.batch < 1 || a.L < 1 ||
+      a.KVH < 1 || a.max_ctx < 1 || a.n_slots < 1 ||
       (reinterpret_cast<uintptr_t>(a.kv_commit) & 15) || (reinterpret_cast<uintptr_t>(a.kv_pool) & 15))
     return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
@@ -227,14 +236,46 @@ cudaError_t launch_pack(int mode, PackSrc s0, PackSrc s1, PackSrc s2, int K, int
   return cudaGetLastError();
 }
 
-__global__ void decode_best_kernel(const unsigned long long* best, int n, int32_t* tokens) {
+__global__ void decode_best_kernel(const unsigned long long* best, int n, const int32_t* err, int32_t* tokens) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < n) tokens[i] = static_cast<int32_t>(~static_cast<uint32_t>(best[i] & 0xffffffffull));
+  if (i >= n) return;
+  tokens[i] = (err && *err) ? -1 : static_cast<int32_t>(~static_cast<uint32_t>(best[i] & 0xffffffffull));
 }
 
-cudaError_t launch_decode_best(const unsigned long long* best, int n, int32_t* tokens, cudaStream_t st) {
-  decode_best_kernel<<<(n + 127) / 128, 128, 0, st>>>(best, n, tokens);
-  return cudaGetLastError();
+static cudaError_t launch_plain(const void* func, int grid, int block, void** args, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(block));
+  cfg.stream = st;
+  return cudaLaunchKernelExC(&cfg, func, args);
+}
+
+cudaError_t launch_decode_best(const unsigned long long* best, int n, const int32_t* err, int32_t* tokens,
+                               cudaStream_t st) {
+  if (n < 1 || !best || !tokens) return cudaErrorInvalidValue;
+  void* args[] = {&best, &n, &err, &tokens};
+  return launch_plain(reinterpret_cast<const void*>(decode_best_kernel), (n + 127) / 128, 128, args, st);
+}
+
+// The public node struct of an isolated exit-head call: five int32 fields
+// (seq, target_pos, unmasked, prior_off, n_prior).
+__global__ void exit_nodes_kernel(const int32_t* in, int n, DevNode* out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  DevNode d = {};
+  d.seq = in[5 * i + 0];
+  d.target_pos = in[5 * i + 1];
+  d.unmasked = in[5 * i + 2];
+  d.prior_off = in[5 * i + 3];
+  d.n_prior = in[5 * i + 4];
+  out[i] = d;
+}
+
+cudaError_t launch_exit_nodes(const void* exit_nodes, int n, DevNode* out, cudaStream_t st) {
+  if (n < 1 || !exit_nodes || !out) return cudaErrorInvalidValue;
+  const int32_t* in = static_cast<const int32_t*>(exit_nodes);
+  void* args[] = {&in, &n, &out};
+  return launch_plain(reinterpret_cast<const void*>(exit_nodes_kernel), (n + 127) / 128, 128, args, st);
 }
 
 }  // namespace dex

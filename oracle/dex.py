@@ -191,19 +191,32 @@ class ARResult:
     depth_candidates: Optional[List[List[int]]] = None   # [t][l-1]: candidate at depth l
 
 
+def prefill(model, prompt: Sequence[int], capacity: int):
+    """The committed context of a prompt: a cache of ``capacity`` positions holding the KV
+    state of positions 0..P-2.  The last prompt token is the first decode step's input, so
+    its position is computed by the decode itself (section 2.1 / 3.2 alike).
+
+    A decode started from this cache writes only positions >= P-1, so the same prefilled
+    cache serves any number of decodes of the same prompt."""
+    cache = model.new_cache(capacity)
+    if len(prompt) > 1:
+        model.forward([int(t) for t in prompt[:-1]], 0, cache)
+    return cache
+
+
 def ar_generate(model, prompt: Sequence[int], T: int, rule: Rule = Rule(), seq: int = 0,
-                record_depths: bool = False, force: Optional[Sequence[int]] = None) -> ARResult:
+                record_depths: bool = False, force: Optional[Sequence[int]] = None, cache=None) -> ARResult:
     """Standard AR decoding of T tokens (section 2.1): every token through all L layers.
 
-    Prompt positions 0..P-2 are prefilled; the last prompt token at position P-1 yields the
-    first new token (position P).  With ``force`` the given tokens are appended instead of
+    Prompt positions 0..P-2 are prefilled (or taken from ``cache``, a ``prefill`` of the same
+    prompt with room for P + T + 1 positions); the last prompt token at position P-1 yields
+    the first new token (position P).  With ``force`` the given tokens are appended instead of
     the decoded ones (teacher forcing: scores a token stream produced elsewhere).  With
     ``record_depths`` the candidate of every depth l in [L] under the same rule is kept.
     """
     P = len(prompt)
-    cache = model.new_cache(P + T + 1)
-    if P > 1:
-        model.forward(prompt[:-1], 0, cache)
+    if cache is None:
+        cache = prefill(model, prompt, P + T + 1)
     last, pos = int(prompt[-1]), P - 1
     out = ARResult([], [], [], [] if record_depths else None)
     for t in range(T):
@@ -283,7 +296,7 @@ class DEXResult:
 
 def dex_generate(model, prompt: Sequence[int], X: Sequence[int], T: int, rule: Rule = Rule(),
                  use_decs: bool = True, seq: int = 0, keep_logits: bool = False,
-                 max_branch: int = 0, adapters: Optional[Sequence[Dict]] = None) -> DEXResult:
+                 max_branch: int = 0, adapters: Optional[Sequence[Dict]] = None, cache=None) -> DEXResult:
     """Depth exploration decoding of T tokens for one sequence (section 3.2), with a trace.
 
     The decode is a series of exploration cycles, one per committed token.  A cycle is
@@ -300,15 +313,17 @@ def dex_generate(model, prompt: Sequence[int], X: Sequence[int], T: int, rule: R
     adapters: one inducing adapter per non-final depth X[0..N-2] (Appendix C.2; fp64 arrays
     as oracle.model.apply_adapter takes them) applied before the shared exit head of the
     nodes at those stages; the final depth keeps the plain exit, so commits are unchanged.
+
+    cache: a ``prefill`` of the same prompt with room for P + T + N + 1 positions, or None to
+    prefill here.
     """
     N = len(X)
     assert X[-1] == model.L and list(X) == sorted(set(X))
     committed = [int(t) for t in prompt]
-    cache = model.new_cache(len(committed) + T + N + 1)
     # the committed context: every prompt position but the last has its KV state; the last
     # prompt token is the input of the first anchor (the root of the first lattice)
-    if len(committed) > 1:
-        model.forward(committed[:-1], 0, cache)
+    if cache is None:
+        cache = prefill(model, committed, len(committed) + T + N + 1)
     res = DEXResult([], [], [], 0, 0, 0)
     lattice: Dict[int, int] = {}      # explore buffer: heap index -> candidate token
     rounds_done = 0                   # explorer rounds completed since the last commit

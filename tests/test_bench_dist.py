@@ -72,3 +72,37 @@ def test_workload_overrides():
     assert (wl.max_new, wl.alpha) == (32, 0.1)
     assert (base.max_new, base.alpha) == (256, 0.05)
     assert (wl.X, wl.tau, wl.sample, wl.shape) == (base.X, base.tau, base.sample, base.shape)
+
+
+def test_ablation_overrides():
+    import argparse
+    import bench
+    ns = argparse.Namespace(workload="llama7b_x8_sample", tokens=0, alpha=None, X="4,32", no_decs=True)
+    wl = bench._workload(ns)
+    assert wl.X == [4, 32] and wl.decs is False
+
+
+def test_reference_arm_line_matches_the_library_line(capsys):
+    """The oracle arm decodes the same unit from a prefilled prompt and prints the library
+    line's config keys and e2e unit (so the two lines compare)."""
+    import argparse
+    import json
+    import bench
+    args = argparse.Namespace(workload="tiny", tokens=4, alpha=None, X=None, no_decs=False, ar=False,
+                              max_branch=0, adapters=None, steps=1, warmup=0)
+    bench.run_reference(args)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "committed tokens/s"
+    assert line["e2e"]["unit"] == line["unit"] and line["value"] > 0
+    wl = bench._workload(args)
+    assert line["config"] == json.loads(json.dumps(bench._config(args, wl, 1, wl.batch)))
+    assert "prefill" in line["cpu_baseline"]["sample"]
+
+
+def test_one_core_block_restores_affinity():
+    import os
+    import bench
+    before = os.sched_getaffinity(0)
+    with bench._OneCore():
+        assert len(os.sched_getaffinity(0)) == 1
+    assert os.sched_getaffinity(0) == before

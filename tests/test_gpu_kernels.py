@@ -99,13 +99,23 @@ def test_kv_collapse_bit_exact():
     committed = torch.randn((B, L, 2, KVH, ctx, hd), generator=gen, device="cuda").to(torch.bfloat16)
     pool = torch.randn((B, S, L, 2, KVH, hd), generator=gen, device="cuda").to(torch.bfloat16)
     jobs = [(0, 3, 4000, 32), (1, 5, 17, 12), (1, 0, 4095, 1), (0, 7, 0, 7), (1, 2, 2048, 32), (0, 1, 1, 20)]
+    # out-of-range jobs (sequence, slot, position, layer count) are skipped and counted;
+    # the kernel checks every field before any access
+    bad = [(B, 0, 0, 1), (-1, 0, 0, 1), (0, S, 0, 1), (0, 0, ctx, 1), (0, 0, -3, 1), (0, 0, 5, L + 1),
+           (0, 0, 5, 0)]
     before = committed.clone()
-    jt = torch.tensor(jobs, dtype=torch.int32, device="cuda")
+    jt = torch.tensor(jobs[:3] + bad + jobs[3:], dtype=torch.int32, device="cuda")
+    rejected = torch.full((1,), 99, dtype=torch.int32, device="cuda")
     geom = dexlib.dex_kv_geom(B, L, KVH, hd, ctx, S)
-    dexlib.dex_kv_collapse(committed.data_ptr(), pool.data_ptr(), geom, jt.data_ptr(), len(jobs),
-                           torch.cuda.current_stream().cuda_stream)
+    dexlib.dex_kv_collapse(committed.data_ptr(), pool.data_ptr(), geom, jt.data_ptr(), jt.shape[0],
+                           torch.cuda.current_stream().cuda_stream, rejected.data_ptr())
     torch.cuda.synchronize()
     want = before.clone()
     for seq, slot, pos, nl in jobs:
         want[seq, :nl, :, :, pos, :] = pool[seq, slot, :nl]
     assert torch.equal(committed.view(torch.int16), want.view(torch.int16))
+    assert int(rejected.item()) == len(bad)
+    # a bad geometry is refused on the host
+    with pytest.raises(dexlib.DexError):
+        dexlib.dex_kv_collapse(committed.data_ptr(), pool.data_ptr(), dexlib.dex_kv_geom(0, L, KVH, hd, ctx, S),
+                               jt.data_ptr(), 1, torch.cuda.current_stream().cuda_stream)

@@ -253,3 +253,21 @@ def test_adapters_keep_dex_lossless_and_change_proposals(sample):
         elif n.token != o.token:
             changed += 1
     assert changed > 0
+
+
+def test_decoding_from_a_prefilled_cache_is_the_same_decode():
+    """A prefilled cache reused across decodes (the benchmark's CPU leg) gives the same
+    tokens, logits and nodes as prefilling inside each call, any number of times."""
+    shape, w, m = tiny_model(alpha=0.3, tied=False)
+    prompt = di.gen_prompts(shape, 1, 16)[0].tolist()
+    X = [2, 4, 6, 8]
+    T = 6
+    plain = dex.dex_generate(m, prompt, X, T, keep_logits=True)
+    cache = dex.prefill(m, prompt, len(prompt) + T + len(X) + 1)
+    for _ in range(2):
+        again = dex.dex_generate(m, prompt, X, T, keep_logits=True, cache=cache)
+        assert again.tokens == plain.tokens and again.rounds == plain.rounds
+        for a, b in zip(again.nodes, plain.nodes):
+            assert (a.node, a.token) == (b.node, b.token) and np.array_equal(a.logits, b.logits)
+    ar = dex.ar_generate(m, prompt, T, cache=cache)
+    assert ar.tokens == dex.ar_generate(m, prompt, T).tokens == plain.tokens
