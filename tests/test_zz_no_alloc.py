@@ -89,10 +89,10 @@ def test_noalloc_calls_leave_device_memory_unchanged():
                                                  tokens.data_ptr(), 0, st)
 
     assert call() == dexlib.DEX_OK
+    first = tokens.clone()
     torch.cuda.synchronize()
     free0, _ = torch.cuda.mem_get_info()
     torch_alloc0 = torch.cuda.memory_allocated()
-    first = tokens.clone()
     for _ in range(4):
         assert call() == dexlib.DEX_OK
     torch.cuda.synchronize()
