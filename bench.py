@@ -42,7 +42,7 @@ sys.path.insert(0, ROOT)
 import dex_inputs as di  # noqa: E402
 
 METRIC = "committed tokens/s (1 GB300, batch 1) and layers executed per committed token"
-KV_ELEM_BYTES = 4   # bytes per element of the library's K/V caches
+KV_ELEM_BYTES = 2   # bytes per element of the library's K/V caches (fp16)
 
 
 def _dist():

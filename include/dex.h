@@ -24,8 +24,8 @@
  *    dex_init() and released by dex_free().
  *  - Arithmetic: bf16 weights on the tensor cores with fp32 accumulation; activations
  *    enter every GEMM as a pair of bf16 operands (x ~= hi + lo, about 17 significant
- *    bits) and the KV caches and hidden states are fp32, so the decoder tracks fp32
- *    arithmetic over the same bf16 weights.
+ *    bits), hidden states are fp32, and the K/V caches hold fp16 (11 significant bits,
+ *    8x finer than bf16 at the same two bytes) read into fp32 attention arithmetic.
  *  - All work is issued on the stream given to dex_init().  Calls returning host data
  *    synchronise that stream.  A handle is not thread-safe.
  *  - Positions are absolute token indices starting at 0; the commit position p_c is

@@ -1,4 +1,4 @@
-// Lattice-masked decode attention for a stage batch of DEX nodes.
+// Lattice-masked attention for the node batches of a DEX round (and prefill chunks).
 //
 // A node at input position p attends keys 0..p of its own token prefix (section 3.2:
 // "ancestry, KV entries, and attention masks" follow the binary lattice).  Keys at
@@ -6,59 +6,107 @@
 // sequence); keys at c_end..p are the branch entries of the node's P-ancestors' slot
 // chains and its own, read from the branch pool through the node's tail table.
 //
-// Work split: CTA = (sequence item, KV head, 128-position key group), four warps, each
-// owning a 32-key slice of the group.  Scores take lane = key: the group's committed key
-// rows go to shared memory with asynchronous 16-byte copies (nothing held in registers,
-// nothing through L1), chunk c of row r stored at chunk c ^ (r mod 32), so when every lane
-// reads chunk c of its own row the 32 reads hit distinct banks while the query's chunk c
-// is one broadcast read.  Values take lane = a run of output dimensions, so a warp reads
-// one whole value row per load.  When the CTA's queries fit one pass (decode), the
-// committed value rows follow the keys into the same shared buffer with a bulk copy once
-// the scores are taken; otherwise (prefill) the key rows stay in shared memory across
-// query batches and values are read from global memory eight rows ahead.  Branch keys
-// (few per node) are read from the pool.  A committed key is read once and used for every
-// query of the batch.
+// Work: a unit is (item, KV head, 128-position key group); an item is one sequence's
+// contiguous node rows of one layer.  Persistent CTAs (one per SM) take contiguous ranges
+// of units.  Warp 0 streams each unit's committed key and value tiles (fp16, up to 128
+// rows) into a ring of shared-memory stages with TMA (128-byte swizzle, 32-row boxes, so
+// a ragged last group moves only the rows it has); eight consumer warps work on the
+// oldest landed stage while the next stages load.  The consumers form two quads; each
+// quad takes half of the unit's queries, and within a quad warp w owns keys 32w..32w+31
+// of the group.  Scores take lane = key (the swizzle puts the 16-byte chunk c of the
+// eight rows a quarter-warp reads in eight distinct bank groups; the query chunk is one
+// broadcast read); values take lane = four (or two) output dims, so a warp reads one
+// whole value row per load.  A committed key is read from HBM once per (item, KV head).
 //
 // The arithmetic for a query is fixed by absolute positions only -- 32-key slices aligned
-// to position 0, each score summed in chunk order wherever the key row lives,
-// slices combined in order within a group, groups combined in group order by the last
-// CTA to finish -- so a node's output is bit-identical whether its keys sit in the
-// committed cache or the branch pool and whatever batch it is in.
+// to position 0, each score summed in chunk order wherever the key row lives (tile or
+// pool), slices combined in order within a group, groups combined in group order by the
+// unit that finishes an (item, KV head) last -- so a node's output is bit-identical
+// whether its keys sit in the committed cache or the branch pool and whatever batch,
+// launch or CTA it is computed in.
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
 namespace dex {
 
-constexpr int kAttnWarps = kAttnGroupPos / 32;
-constexpr int kAttnThreads = 32 * kAttnWarps;
-static_assert(kAttnGroupPos == 32 * kAttnWarps && kAttnWarps == 4, "four 32-key warp slices per group");
-constexpr int kVB = 8;   // value rows loaded ahead
+constexpr int kSlices = kAttnGroupPos / 32;           // 32-key slices per group
+constexpr int kTeamWarps = 2 * kSlices;               // two quads of consumer warps
+constexpr int kAttnThreads = 32 * (1 + kTeamWarps);   // + the producer warp
+constexpr int kBoxRows = 32;                          // TMA box height
+constexpr int kTeamBar = 1, kQuadBar0 = 2;            // named barriers (ids)
+static_assert(kAttnGroupPos == 128 && kSlices == 4, "four 32-key slices per 128-position group");
 
-// q . k as four partial sums, one per feature residue mod 4 (features 4c + r go to sum r),
-// accumulated over the chunks in order, two sums per packed FMA (each element rounded as
-// fmaf), then (s0 + s1) + (s2 + s3).  The committed-key loop below follows the same order.
-__device__ __forceinline__ void dot_chunk(float2& s01, float2& s23, const float4& q4, const float4& k4) {
-  s01 = __ffma2_rn(make_float2(q4.x, q4.y), make_float2(k4.x, k4.y), s01);
-  s23 = __ffma2_rn(make_float2(q4.z, q4.w), make_float2(k4.z, k4.w), s23);
+// Shared-memory plan of a CTA: ring stages (K tile, V tile), two query buffers, the slice
+// records of one pass, barriers.
+template <int HD, int QB>
+struct AttnSmem {
+  static constexpr uint32_t kTile = kAttnGroupPos * HD * 2;     // fp16 tile, 1024-aligned
+  static constexpr uint32_t kStage = 2 * kTile;
+  static constexpr int kStages = (HD == 128) ? 3 : 6;
+  static constexpr uint32_t kRing = kStages * kStage;
+  static constexpr uint32_t kQ = 2u * QB * HD * 4;              // double-buffered fp32 queries
+  static constexpr uint32_t kRec = static_cast<uint32_t>(QB) * kSlices * (HD + 2) * 4;
+  static constexpr uint32_t kBars = 2 * kStages * 8 + 16;
+  static constexpr uint32_t kTotal = kRing + kQ + kRec + kBars + 1024;   // + alignment slack
+};
+
+// q . k over 8-dim chunks in order: four partial sums by feature residue mod 4 (features
+// 4c + r go to sum r), two per packed FMA (each element rounded as fmaf), then
+// (s0 + s1) + (s2 + s3).
+__device__ __forceinline__ void dot8(float2& s01, float2& s23, const float* q, const uint4& kraw) {
+  const float4 qa = *reinterpret_cast<const float4*>(q);
+  const float4 qb = *reinterpret_cast<const float4*>(q + 4);
+  const float2 k0 = __half22float2(*reinterpret_cast<const __half2*>(&kraw.x));
+  const float2 k1 = __half22float2(*reinterpret_cast<const __half2*>(&kraw.y));
+  const float2 k2 = __half22float2(*reinterpret_cast<const __half2*>(&kraw.z));
+  const float2 k3 = __half22float2(*reinterpret_cast<const __half2*>(&kraw.w));
+  s01 = __ffma2_rn(make_float2(qa.x, qa.y), k0, s01);
+  s23 = __ffma2_rn(make_float2(qa.z, qa.w), k1, s23);
+  s01 = __ffma2_rn(make_float2(qb.x, qb.y), k2, s01);
+  s23 = __ffma2_rn(make_float2(qb.z, qb.w), k3, s23);
 }
 __device__ __forceinline__ float dot_finish(const float2& s01, const float2& s23) {
   return __fadd_rn(__fadd_rn(s01.x, s01.y), __fadd_rn(s23.x, s23.y));
 }
 
-// Chunk c of the row sits at c ^ swz (shared-memory key rows are swizzled by row, pool rows
-// are not).
-template <int HD>
-__device__ __forceinline__ float dot_q_row(const float* q, const float* krow, int swz) {
-  constexpr int NC = HD / 4;
-  float2 s01 = make_float2(0.0f, 0.0f), s23 = make_float2(0.0f, 0.0f);
-#pragma unroll
-  for (int c = 0; c < NC; ++c)
-    dot_chunk(s01, s23, *reinterpret_cast<const float4*>(q + c * 4), *(reinterpret_cast<const float4*>(krow) + (c ^ swz)));
-  return dot_finish(s01, s23);
+// 16-byte chunk c (dims 8c..8c+7) of row r of a swizzled fp16 tile: 64-dim halves of
+// kAttnGroupPos rows x 128 bytes; chunk cc of row r sits at (cc ^ (r & 7)) * 16.
+__device__ __forceinline__ uint32_t tile_chunk_off(int r, int c) {
+  return static_cast<uint32_t>((c >> 3) * (kAttnGroupPos * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
-// acc[i] += p * v[i] over the lane's output dims, two dims per packed FMA (each element
-// rounded as fmaf, so the order per element is that of a scalar loop).
+// Dims [lane * DPL, lane * DPL + DPL) of row r of a value tile (or a pool row) as floats.
+template <int HD>
+__device__ __forceinline__ void value_dims_tile(const uint8_t* tile, int r, int lane, float (&v)[HD / 32]) {
+  if constexpr (HD == 128) {   // four dims = 8 bytes: chunk lane / 2, half (lane & 1)
+    const uint2 raw =
+        *reinterpret_cast<const uint2*>(tile + tile_chunk_off(r, lane >> 1) + ((lane & 1) << 3));
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+    v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+  } else {                     // two dims = 4 bytes: chunk lane / 4, quarter (lane & 3)
+    const uint32_t raw = *reinterpret_cast<const uint32_t*>(tile + tile_chunk_off(r, lane >> 2) + ((lane & 3) << 2));
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw));
+    v[0] = a.x; v[1] = a.y;
+  }
+}
+template <int HD>
+__device__ __forceinline__ void value_dims_row(const __half* row, int lane, float (&v)[HD / 32]) {
+  if constexpr (HD == 128) {
+    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(row) + lane);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+    v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+  } else {
+    const uint32_t raw = __ldg(reinterpret_cast<const uint32_t*>(row) + lane);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw));
+    v[0] = a.x; v[1] = a.y;
+  }
+}
+
+// acc[i] += p * v[i] over the lane's output dims, two dims per packed FMA.
 template <int DPL>
 __device__ __forceinline__ void axpy_dims(float (&acc)[DPL], float p, const float (&v)[DPL]) {
   const float2 pp = make_float2(p, p);
@@ -70,386 +118,405 @@ __device__ __forceinline__ void axpy_dims(float (&acc)[DPL], float p, const floa
   }
 }
 
-// Shared floats of a CTA: key/value rows, queries and (unless SP) the slice records.
-__host__ __device__ constexpr size_t attn_smem_floats(int hd, int qb, bool sp) {
-  return static_cast<size_t>(kAttnGroupPos) * hd + static_cast<size_t>(qb) * hd +
-         (sp ? 0 : static_cast<size_t>(qb) * kAttnWarps * (hd + 2));
+struct UnitRef {
+  int item, kvh, g;
+};
+// Unit u of the launch: items are laid out back to back, KVH x n_groups units each.
+__device__ __forceinline__ UnitRef unit_ref(const AttnArgs& a, int u) {
+  int lo = 0, hi = a.n_items - 1;
+  while (lo < hi) {   // last item with unit0 <= u
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(&a.items[mid].unit0) <= u) lo = mid;
+    else hi = mid - 1;
+  }
+  UnitRef r;
+  r.item = lo;
+  const int rem = u - __ldg(&a.items[lo].unit0);
+  const int ng = __ldg(&a.items[lo].n_groups);
+  r.kvh = rem / ng;
+  r.g = rem - r.kvh * ng;
+  return r;
 }
-static_assert(kAttnGroupPos * 64 >= 8 * kAttnWarps * (64 + 2), "slice records fit the key buffer");
+// Committed rows of group g that some query of the item reads: [g0, g0 + n).
+__device__ __forceinline__ int committed_rows(const AttnItem& it, int g) {
+  return max(0, min(kAttnGroupPos, min(it.max_cend, it.max_pos + 1) - g * kAttnGroupPos));
+}
 
-// QB: queries per pass, chosen per launch from its largest item (the unused slots of a
-// batch would otherwise still issue their predicated instructions).  SP: every item of the
-// launch fits one pass, so the slice records reuse the key/value buffer once the values
-// are consumed (a smaller CTA: three per SM instead of two).  A query's arithmetic is the
-// same in every instantiation.
-template <int HD, int QB, bool SP>
-__global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
-  constexpr int DPL = HD / 32;        // output dims per lane
-  constexpr int NC = HD / 4;          // 16-byte chunks per row
-  constexpr int PS = HD + 2;          // partial record: acc[HD], m, l
-  extern __shared__ __align__(128) float smem_f[];
-  float* sK = smem_f;                             // [kAttnGroupPos][HD] committed keys of the group
-  float* sQ = sK + kAttnGroupPos * HD;            // [QB][HD]
-  float* sP = SP ? sK : sQ + QB * HD;             // [QB][warps][PS]
-  __shared__ __align__(8) uint64_t vbar;          // value rows landed (single-pass CTAs)
-  __shared__ int s_last;
+template <int HD, int QB>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_kernel(const __grid_constant__ CUtensorMap tmKV, const __grid_constant__ AttnArgs a) {
+  using SM = AttnSmem<HD, QB>;
+  constexpr int S = SM::kStages;
+  constexpr int DPL = HD / 32;                  // output dims per lane
+  constexpr int NCH = HD / 8;                   // 16-byte chunks per fp16 row
+  constexpr int QH = QB >= 2 ? QB / 2 : 1;      // queries per quad per pass
+  constexpr int PS = HD + 2;                    // slice record: acc[HD], m, l
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  float* sQ = reinterpret_cast<float*>(smem + SM::kRing);           // [2][QB][HD]
+  float* sRec = sQ + 2 * QB * HD;                                   // [QB][kSlices][PS]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::kRing + SM::kQ + SM::kRec);
+  uint64_t* empty = full + S;
+  volatile int* sflag = reinterpret_cast<volatile int*>(empty + S);   // [0] last arriver, [1] abort
 
-  const int g = blockIdx.x, kvh = blockIdx.y, it = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int C = gridDim.x, cta = blockIdx.x;
+  const int u0 = static_cast<int>((static_cast<long long>(cta) * a.n_units) / C);
+  const int u1 = static_cast<int>((static_cast<long long>(cta + 1) * a.n_units) / C);
+  const int n_my = u1 - u0;
+  const int G = a.H / a.KVH;
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kTeamWarps);
+    }
+    sflag[0] = 0;
+    sflag[1] = 0;
+    fence_mbar_init();
+    tma_prefetch(&tmKV);
+  }
+  __syncthreads();
   griddep_wait();   // q and this round's K/V come from the preceding launch
   griddep_launch_dependents();
-  const AttnItem item = a.items[it];
-  // the groups must cover every position up to max_pos (a malformed plan is reported)
-  if (g == 0 && kvh == 0 && tid == 0 && item.n_groups * kAttnGroupPos <= item.max_pos) atomicExch(a.err, DEV_BAD_INDEX);
-  if (g >= item.n_groups) return;
-  const int g0 = g * kAttnGroupPos;
-  const int H = a.H, G = a.H / a.KVH;
-  // committed K and V rows of (sequence, layer, KV head): [max_ctx][HD] each
-  const float* kcom =
-      a.kv_commit + ((((static_cast<size_t>(item.seq) * a.L + item.layer) * 2 + 0) * a.KVH + kvh) * a.max_ctx) * HD;
-  const float* vcom = kcom + static_cast<size_t>(a.KVH) * a.max_ctx * HD;
-  // committed rows some query of the item reads: [g0, g0 + n_com)
-  const int n_com = max(0, min(kAttnGroupPos, min(item.max_cend, item.max_pos + 1) - g0));
-  if (tid == 0) {
-    mbar_init(&vbar, 1);
-    fence_mbar_init();
-  }
-  // committed key rows -> shared memory, chunk c of row r at c ^ (r mod NC): lanes reading
-  // the same chunk of 32 consecutive rows hit distinct banks
-  {
-    const uint32_t base = smem_u32(sK);
-    const float* src = kcom + static_cast<size_t>(g0) * HD;
-    for (int idx = tid; idx < n_com * NC; idx += kAttnThreads) {
-      const int r = idx / NC, c = idx % NC;
-      cp_async_16(base + static_cast<uint32_t>(r * HD + ((c ^ (r & (NC - 1))) << 2)) * 4u, src + r * HD + c * 4);
-    }
-    cp_async_commit();
-  }
-  bool have_k = false, failed = false;
+  if (n_my <= 0) return;
 
-  const int nq = (item.row_end - item.row_begin) * G;
-  if (SP && nq > QB) {   // the launch promised one pass per item
-    if (tid == 0) atomicExch(a.err, DEV_BAD_INDEX);
+  if (warp == 0) {
+    // ---------------- producer: committed K and V tiles of each unit ----------------
+    if (lane == 0) {
+      int issued = 0;
+      bool ok = true;
+      for (int i = 0; i < n_my; ++i) {
+        const int st = i % S;
+        if (i >= S && !mbar_wait(&empty[st], static_cast<uint32_t>((i / S) - 1) & 1u, a.err, DEV_TIMEOUT_EMPTY)) {
+          ok = false;
+          break;
+        }
+        const UnitRef ur = unit_ref(a, u0 + i);
+        const AttnItem it = a.items[ur.item];
+        const int n_com = committed_rows(it, ur.g);
+        const int nbox = (n_com + kBoxRows - 1) / kBoxRows;
+        constexpr int halves = HD / 64;
+        mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(2 * nbox * halves * kBoxRows * 128));
+        const int row_k = ((((it.seq * a.L + it.layer) * 2 + 0) * a.KVH + ur.kvh) * a.max_ctx) +
+                          ur.g * kAttnGroupPos;
+        const int row_v = row_k + a.KVH * a.max_ctx;
+        uint8_t* sk = ring + static_cast<size_t>(st) * SM::kStage;
+        uint8_t* sv = sk + SM::kTile;
+        for (int b = 0; b < nbox; ++b) {
+#pragma unroll
+          for (int h = 0; h < halves; ++h) {
+            const uint32_t off = static_cast<uint32_t>(h * kAttnGroupPos * 128 + b * kBoxRows * 128);
+            tma_load_2d(sk + off, &tmKV, &full[st], h * 64, row_k + b * kBoxRows);
+            tma_load_2d(sv + off, &tmKV, &full[st], h * 64, row_v + b * kBoxRows);
+          }
+        }
+        issued = i + 1;
+      }
+      if (!ok) {   // drain the copies still in flight before the CTA exits
+        for (int i = (issued > S ? issued - S : 0); i < issued; ++i)
+          mbar_wait(&full[i % S], static_cast<uint32_t>(i / S) & 1u, nullptr, 0);
+      }
+    }
     return;
   }
-  // one query pass (decode): once scored, the key buffer takes the group's committed value
-  // rows in one more bulk copy; several passes (prefill) keep the keys and read values from
-  // global memory
-  const bool v_smem = nq <= QB && n_com > 0;
-  const int ks = g0 + 32 * warp;       // this warp's 32-key slice
-  const int k = ks + lane;             // this lane's key
-  for (int qb = 0; qb < nq; qb += QB) {
-    const int nb = min(QB, nq - qb);
-    for (int idx = tid; idx < nb * HD; idx += kAttnThreads) {
-      const int qi = qb + idx / HD, d = idx % HD;
-      const int row = item.row_begin + qi / G, qh = kvh * G + qi % G;
-      sQ[idx] = a.q[(static_cast<size_t>(row) * H + qh) * HD + d] * a.scale_log2;
-    }
-    int pos[QB], cend[QB], nrow[QB];
-    int cend_min = 0x7fffffff, pos_max = -1;
-#pragma unroll
-    for (int j = 0; j < QB; ++j) {
-      pos[j] = -1;
-      cend[j] = 0;
-      nrow[j] = item.row_begin;
-      if (j < nb) {
-        nrow[j] = item.row_begin + (qb + j) / G;
-        const DevNode* nd = a.nodes + nrow[j];
-        pos[j] = nd->pos;
-        cend[j] = nd->c_end;
-        cend_min = min(cend_min, cend[j]);
-        pos_max = max(pos_max, pos[j]);
-      }
-    }
-    __syncthreads();   // sQ written; the barriers' initialisation is visible
-    if (!have_k) {
-      cp_async_wait_all();
-      __syncthreads();   // every thread's key chunks have landed
-      have_k = true;
-    }
-    // the branch-pool row of query j's key kk (kk >= c_end of that query)
-    auto pool_row = [&](int j, int kk, int kv) -> const float* {
-      const DevNode* nd = a.nodes + nrow[j];
-      int t = kk - cend[j];
-      if (t >= nd->n_tail) {   // cannot happen for a well-formed plan; never read out of bounds
-        atomicExch(a.err, DEV_BAD_INDEX);
-        t = nd->n_tail - 1;
-      }
-      const int slot = a.tails[nd->tail_off + t];
-      return a.kv_pool +
-             ((((static_cast<size_t>(item.seq) * a.n_slots + slot) * a.L + item.layer) * 2 + kv) * a.KVH + kvh) * HD;
-    };
-    // scores of this lane's key against every query of the batch
-    float sc[QB];
-    if (k < cend_min && k <= pos_max) {   // committed for every query: one pass over the row
-      float2 s01[QB], s23[QB];
-#pragma unroll
-      for (int j = 0; j < QB; ++j) s01[j] = s23[j] = make_float2(0.0f, 0.0f);
-      const float4* kr = reinterpret_cast<const float4*>(sK + (k - g0) * HD);
-      const int swz = (k - g0) & (NC - 1);
-#pragma unroll 8
-      for (int c = 0; c < NC; ++c) {
-        const float4 k4 = kr[c ^ swz];
-#pragma unroll
-        for (int j = 0; j < QB; ++j) {
-          // same address in every lane: broadcast
-          if (j < nb) dot_chunk(s01[j], s23[j], *reinterpret_cast<const float4*>(sQ + j * HD + c * 4), k4);
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < QB; ++j) sc[j] = (j < nb && k <= pos[j]) ? dot_finish(s01[j], s23[j]) : -INFINITY;
-    } else {
-#pragma unroll
-      for (int j = 0; j < QB; ++j) {
-        sc[j] = -INFINITY;
-        if (j < nb && k <= pos[j])
-          sc[j] = k < cend[j] ? dot_q_row<HD>(sQ + j * HD, sK + (k - g0) * HD, (k - g0) & (NC - 1))
-                              : dot_q_row<HD>(sQ + j * HD, pool_row(j, k, 0), 0);
-      }
-    }
-    if (v_smem) {
-      __syncthreads();   // every score read of the key rows is done
-      if (tid == 0) {
-        const uint32_t bytes = static_cast<uint32_t>(n_com) * HD * 4;
-        fence_proxy_async_smem();
-        mbar_arrive_expect_tx(&vbar, bytes);
-        bulk_load_1d(sK, vcom + static_cast<size_t>(g0) * HD, bytes, &vbar);
-      }
-    }
-    // per query: slice softmax statistics and the value accumulation, keys in order
-    float mx[QB], lsum[QB], pr[QB], acc[QB][DPL];
-#pragma unroll
-    for (int j = 0; j < QB; ++j) {
-      mx[j] = warp_max(sc[j]);
-      pr[j] = 0.0f;
-      lsum[j] = 0.0f;
-      if (mx[j] != -INFINITY) {
-        pr[j] = exp2f(sc[j] - mx[j]);
-        lsum[j] = warp_sum(pr[j]);
-      }
-#pragma unroll
-      for (int i = 0; i < DPL; ++i) acc[j][i] = 0.0f;
-    }
-    if (v_smem) {
-      failed |= !mbar_wait(&vbar, 0, a.err, DEV_TIMEOUT_FULL);
-      if (__syncthreads_or(failed)) {
-        failed = true;
-        break;
-      }
-      const int n_keys = min(32, pos_max - ks + 1);   // keys of the slice any query attends
-#pragma unroll 4
-      for (int u = 0; u < n_keys; ++u) {
-        const int key = ks + u;
-        const float* vs = sK + (key - g0) * HD + lane * DPL;
-        if (key < cend_min) {   // committed for every query
-          float vv[DPL];
-          if constexpr (DPL == 4) {
-            const float4 f = *reinterpret_cast<const float4*>(vs);
-            vv[0] = f.x; vv[1] = f.y; vv[2] = f.z; vv[3] = f.w;
-          } else {
-            const float2 f = *reinterpret_cast<const float2*>(vs);
-            vv[0] = f.x; vv[1] = f.y;
-          }
-#pragma unroll
-          for (int j = 0; j < QB; ++j) {
-            if (j < nb && key <= pos[j]) {
-              const float pk = __shfl_sync(0xffffffffu, pr[j], u);
-              axpy_dims<DPL>(acc[j], pk, vv);
-            }
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < QB; ++j) {
-            if (j < nb && key <= pos[j]) {
-              const float pk = __shfl_sync(0xffffffffu, pr[j], u);
-              const float* vr = key < cend[j] ? vs : pool_row(j, key, 1) + lane * DPL;
-              float vt[DPL];
-#pragma unroll
-              for (int i = 0; i < DPL; ++i) vt[i] = vr[i];
-              axpy_dims<DPL>(acc[j], pk, vt);
-            }
-          }
-        }
-      }
-    } else {
-    // value rows in batches of kVB keys: a batch's loads are all issued before any is used
-    for (int jb = 0; jb < 32; jb += kVB) {
-      if (ks + jb > pos_max) break;   // uniform across the warp
-      float vv[kVB][DPL];
-#pragma unroll
-      for (int u = 0; u < kVB; ++u) {
-        const int key = ks + jb + u;
-        const bool shared = key <= pos_max && key < cend_min;
-        if constexpr (DPL == 4) {
-          const float4 f = shared ? __ldg(reinterpret_cast<const float4*>(vcom + static_cast<size_t>(key) * HD) + lane)
-                                  : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-          vv[u][0] = f.x; vv[u][1] = f.y; vv[u][2] = f.z; vv[u][3] = f.w;
-        } else {
-          const float2 f = shared ? __ldg(reinterpret_cast<const float2*>(vcom + static_cast<size_t>(key) * HD) + lane)
-                                  : make_float2(0.0f, 0.0f);
-          vv[u][0] = f.x; vv[u][1] = f.y;
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kVB; ++u) {
-        const int key = ks + jb + u, jj = jb + u;
-        if (key <= pos_max) {       // uniform across the warp
-          if (key < cend_min) {     // committed for every query: the row loaded above
-#pragma unroll
-            for (int j = 0; j < QB; ++j) {
-              if (j < nb && key <= pos[j]) {
-                const float pk = __shfl_sync(0xffffffffu, pr[j], jj);
-                axpy_dims<DPL>(acc[j], pk, vv[u]);
-              }
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < QB; ++j) {
-              if (j < nb && key <= pos[j]) {
-                const float pk = __shfl_sync(0xffffffffu, pr[j], jj);
-                const float* vr =
-                    (key < cend[j] ? vcom + static_cast<size_t>(key) * HD : pool_row(j, key, 1)) + lane * DPL;
-                float vt[DPL];
-#pragma unroll
-                for (int i = 0; i < DPL; ++i) vt[i] = __ldg(vr + i);
-                axpy_dims<DPL>(acc[j], pk, vt);
-              }
-            }
-          }
-        }
-      }
-    }
-    }
-    if constexpr (SP) __syncthreads();   // every warp is done with the value rows under sP
-#pragma unroll
-    for (int j = 0; j < QB; ++j) {
-      if (j < nb) {
-        float* rec = sP + (j * kAttnWarps + warp) * PS;
-#pragma unroll
-        for (int i = 0; i < DPL; ++i) rec[lane * DPL + i] = acc[j][i];
-        if (lane == 0) {
-          rec[HD] = mx[j];
-          rec[HD + 1] = lsum[j];
-        }
-      }
-    }
-    __syncthreads();
-    // combine the four slices of each query in slice order; write the group's record
-    for (int j = warp; j < nb; j += kAttnWarps) {
-      const int qi = qb + j;
-      const int row = item.row_begin + qi / G, qh = kvh * G + qi % G;
-      const float* r0 = sP + (j * kAttnWarps) * PS;
-      float mw[4], wgt[4];
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        mw[w] = r0[w * PS + HD];
-        M = fmaxf(M, mw[w]);
-      }
-#pragma unroll
-      for (int w = 0; w < 4; ++w) wgt[w] = (mw[w] == -INFINITY) ? 0.0f : exp2f(mw[w] - M);
-      const float Lg = __fadd_rn(__fadd_rn(r0[0 * PS + HD + 1] * wgt[0], r0[1 * PS + HD + 1] * wgt[1]),
-                                 __fadd_rn(r0[2 * PS + HD + 1] * wgt[2], r0[3 * PS + HD + 1] * wgt[3]));
-      float* pp = a.part + ((static_cast<size_t>(row) * H + qh) * a.max_groups + g) * PS;
-#pragma unroll
-      for (int i = 0; i < DPL; ++i) {
-        const int d = lane * DPL + i;
-        const float v = __fadd_rn(__fadd_rn(r0[0 * PS + d] * wgt[0], r0[1 * PS + d] * wgt[1]),
-                                  __fadd_rn(r0[2 * PS + d] * wgt[2], r0[3 * PS + d] * wgt[3]));
-        __stcg(pp + d, v);
-      }
-      if (lane == 0) {
-        __stcg(pp + HD, M);
-        __stcg(pp + HD + 1, Lg);
-      }
-    }
-    __syncthreads();
-  }
-  if (failed) return;   // error flag set; the host reports the stall
 
-  // the last group CTA of (item, KV head) merges the groups; lane gg holds groups gg, gg + 32
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = (atomicAdd(a.counters + item.counter * a.KVH + kvh, 1) == item.n_groups - 1) ? 1 : 0;
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  for (int qi = warp; qi < nq; qi += kAttnWarps) {
-    const int row = item.row_begin + qi / G, qh = kvh * G + qi % G;
-    const float* base = a.part + (static_cast<size_t>(row) * H + qh) * a.max_groups * PS;
-    float mg[2] = {-INFINITY, -INFINITY}, lg[2] = {0.0f, 0.0f};
-#pragma unroll
-    for (int h2 = 0; h2 < 2; ++h2) {
-      const int gg = lane + 32 * h2;
-      if (gg < item.n_groups) {
-        mg[h2] = __ldcg(base + gg * PS + HD);
-        lg[h2] = __ldcg(base + gg * PS + HD + 1);
+  // ---------------- consumers: warps 1..8, quads of four key slices ----------------
+  const int cw = warp - 1, quad = cw >> 2, w = cw & 3;
+  const int tt = tid - 32;                      // team thread 0..255
+  const int qbar = kQuadBar0 + quad;
+  auto team_sync = [] { named_bar_sync(kTeamBar, 32 * kTeamWarps); };
+  auto quad_sync = [&] { named_bar_sync(qbar, 32 * kSlices); };
+
+  // query pass sequence of this CTA: (unit i, pass p); the next pass's queries are copied
+  // into the other buffer while the current one is computed
+  auto issue_q = [&](int i, int p, int buf) {
+    const UnitRef ur = unit_ref(a, u0 + i);
+    const AttnItem it = a.items[ur.item];
+    const int nq = (it.row_end - it.row_begin) * G;
+    const int q0 = p * QB;
+    float* dst = sQ + buf * QB * HD;
+    for (int idx = tt * 4; idx < QB * HD; idx += 32 * kTeamWarps * 4) {
+      const int j = idx / HD, d = idx - j * HD;
+      const int qi = q0 + j;
+      if (qi < nq) {
+        const int row = it.row_begin + qi / G, qh = ur.kvh * G + qi % G;
+        cp_async_16(smem_u32(dst + idx), a.q + (static_cast<size_t>(row) * a.H + qh) * HD + d);
+      } else {
+        *reinterpret_cast<float4*>(dst + idx) = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
-    const float M = warp_max(fmaxf(mg[0], mg[1]));
-    float wg[2];
+    cp_async_commit();
+  };
+  int buf = 0;
+  issue_q(0, 0, 0);
+  for (int i = 0; i < n_my; ++i) {
+    const UnitRef ur = unit_ref(a, u0 + i);
+    const AttnItem it = a.items[ur.item];
+    const int st = i % S;
+    const int g0 = ur.g * kAttnGroupPos;
+    const int nq = (it.row_end - it.row_begin) * G;
+    const int n_pass = (nq + QB - 1) / QB;
+    const uint8_t* sk = ring + static_cast<size_t>(st) * SM::kStage;
+    const uint8_t* sv = sk + SM::kTile;
+    const bool landed = mbar_wait(&full[st], static_cast<uint32_t>(i / S) & 1u, a.err, DEV_TIMEOUT_FULL);
+    if (!landed) sflag[1] = 1;
+    const __half* kcom_pool = reinterpret_cast<const __half*>(a.kv_pool);
+    // the branch-pool row of key kk (kk >= c_end) of node row nrow
+    auto pool_row = [&](int nrow, int kk, int kv) -> const __half* {
+      const DevNode* nd = a.nodes + nrow;
+      const int t = kk - nd->c_end;
+      int slot = 0;
+      if (t >= 0 && t < nd->n_tail) {
+        slot = a.tails[nd->tail_off + t];
+      } else {   // cannot happen for a well-formed plan; reported, and slot 0 is read instead
+        atomicExch(a.err, DEV_BAD_INDEX);
+      }
+      return kcom_pool +
+             ((((static_cast<size_t>(it.seq) * a.n_slots + slot) * a.L + it.layer) * 2 + kv) * a.KVH + ur.kvh) * HD;
+    };
+    for (int p = 0; p < n_pass; ++p) {
+      cp_async_wait_all();   // this pass's queries (copied while the previous pass ran)
+      team_sync();           // ... visible to all; every thread is done with the other buffer
+      if (sflag[1]) break;
+      // the next pass's queries into the other buffer, overlapping this pass
+      if (p + 1 < n_pass) issue_q(i, p + 1, buf ^ 1);
+      else if (i + 1 < n_my) issue_q(i + 1, 0, buf ^ 1);
+      const float* qbuf = sQ + buf * QB * HD;
+      const int q0 = p * QB;
+      const int nb = min(QB, nq - q0);
+      // this quad's queries: pass-local slots jb .. jb + QH - 1
+      const int jb = quad * QH;
+      int pos[QH], cend[QH], nrow[QH];
+      int cmin = 0x7fffffff, pmax = -1;
 #pragma unroll
-    for (int h2 = 0; h2 < 2; ++h2) wg[h2] = (lg[h2] > 0.0f) ? exp2f(mg[h2] - M) : 0.0f;
-    const float Lsum = warp_sum(__fadd_rn(lg[0] * wg[0], lg[1] * wg[1]));
-    float O[DPL];
+      for (int j = 0; j < QH; ++j) {
+        pos[j] = -1;
+        cend[j] = 0;
+        nrow[j] = it.row_begin;
+        if (jb + j < nb) {
+          nrow[j] = it.row_begin + (q0 + jb + j) / G;
+          pos[j] = __ldg(&a.nodes[nrow[j]].pos);
+          cend[j] = __ldg(&a.nodes[nrow[j]].c_end);
+          cmin = min(cmin, cend[j]);
+          pmax = max(pmax, pos[j]);
+        }
+      }
+      const bool quad_live = jb < nb;
+      const int kr = 32 * w + lane;             // this lane's key row within the group
+      const int k = g0 + kr;
+      float sc[QH];
+      if (quad_live && k < cmin && k <= pmax) {   // committed for every query of the quad
+        float2 s01[QH], s23[QH];
 #pragma unroll
-    for (int i = 0; i < DPL; ++i) O[i] = 0.0f;
-    for (int gg = 0; gg < item.n_groups; ++gg) {
-      const float w = __shfl_sync(0xffffffffu, gg < 32 ? wg[0] : wg[1], gg & 31);
-      if (w == 0.0f) continue;
+        for (int j = 0; j < QH; ++j) s01[j] = s23[j] = make_float2(0.0f, 0.0f);
+#pragma unroll 4
+        for (int c = 0; c < NCH; ++c) {
+          const uint4 kraw = *reinterpret_cast<const uint4*>(sk + tile_chunk_off(kr, c));
 #pragma unroll
-      for (int i = 0; i < DPL; ++i) O[i] = fmaf(w, __ldcg(base + gg * PS + lane * DPL + i), O[i]);
+          for (int j = 0; j < QH; ++j)
+            if (jb + j < nb) dot8(s01[j], s23[j], qbuf + (jb + j) * HD + 8 * c, kraw);
+        }
+#pragma unroll
+        for (int j = 0; j < QH; ++j)
+          sc[j] = (jb + j < nb && k <= pos[j]) ? dot_finish(s01[j], s23[j]) * a.scale_log2 : -INFINITY;
+      } else {
+#pragma unroll
+        for (int j = 0; j < QH; ++j) {
+          sc[j] = -INFINITY;
+          if (jb + j < nb && k <= pos[j]) {
+            float2 s01 = make_float2(0.0f, 0.0f), s23 = make_float2(0.0f, 0.0f);
+            if (k < cend[j]) {
+              for (int c = 0; c < NCH; ++c)
+                dot8(s01, s23, qbuf + (jb + j) * HD + 8 * c, *reinterpret_cast<const uint4*>(sk + tile_chunk_off(kr, c)));
+            } else {
+              const uint4* prow = reinterpret_cast<const uint4*>(pool_row(nrow[j], k, 0));
+              for (int c = 0; c < NCH; ++c) dot8(s01, s23, qbuf + (jb + j) * HD + 8 * c, __ldg(prow + c));
+            }
+            sc[j] = dot_finish(s01, s23) * a.scale_log2;
+          }
+        }
+      }
+      // slice softmax statistics and the value accumulation, keys in order
+      float mx[QH], lsum[QH], pr[QH], acc[QH][DPL];
+#pragma unroll
+      for (int j = 0; j < QH; ++j) {
+        mx[j] = warp_max(sc[j]);
+        pr[j] = 0.0f;
+        lsum[j] = 0.0f;
+        if (mx[j] != -INFINITY) {
+          pr[j] = exp2f(sc[j] - mx[j]);
+          lsum[j] = warp_sum(pr[j]);
+        }
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) acc[j][d] = 0.0f;
+      }
+      if (quad_live) {
+        const int ks = g0 + 32 * w;
+        const int n_keys = min(32, pmax - ks + 1);   // keys of the slice some query attends
+#pragma unroll 2
+        for (int u = 0; u < n_keys; ++u) {
+          const int key = ks + u;
+          if (key < cmin) {   // committed for every query: one row read
+            float vv[DPL];
+            value_dims_tile<HD>(sv, 32 * w + u, lane, vv);
+#pragma unroll
+            for (int j = 0; j < QH; ++j) {
+              if (jb + j < nb && key <= pos[j]) axpy_dims<DPL>(acc[j], __shfl_sync(0xffffffffu, pr[j], u), vv);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < QH; ++j) {
+              if (jb + j < nb && key <= pos[j]) {
+                float vv[DPL];
+                if (key < cend[j]) value_dims_tile<HD>(sv, 32 * w + u, lane, vv);
+                else value_dims_row<HD>(pool_row(nrow[j], key, 1), lane, vv);
+                axpy_dims<DPL>(acc[j], __shfl_sync(0xffffffffu, pr[j], u), vv);
+              }
+            }
+          }
+        }
+      }
+      // the stage is free once the last pass has read its values
+      if (p == n_pass - 1) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+      }
+      // slice records of the quad's queries, then the in-order combination of the slices
+#pragma unroll
+      for (int j = 0; j < QH; ++j) {
+        if (jb + j < nb) {
+          float* rec = sRec + ((jb + j) * kSlices + w) * PS;
+#pragma unroll
+          for (int d = 0; d < DPL; ++d) rec[lane * DPL + d] = acc[j][d];
+          if (lane == 0) {
+            rec[HD] = mx[j];
+            rec[HD + 1] = lsum[j];
+          }
+        }
+      }
+      quad_sync();
+      for (int j = jb + w; j < min(nb, jb + QH); j += kSlices) {
+        const int qi = q0 + j;
+        const int row = it.row_begin + qi / G, qh = ur.kvh * G + qi % G;
+        const float* r0 = sRec + (j * kSlices) * PS;
+        float mw[kSlices], wgt[kSlices];
+        float M = -INFINITY;
+#pragma unroll
+        for (int s2 = 0; s2 < kSlices; ++s2) {
+          mw[s2] = r0[s2 * PS + HD];
+          M = fmaxf(M, mw[s2]);
+        }
+#pragma unroll
+        for (int s2 = 0; s2 < kSlices; ++s2) wgt[s2] = (mw[s2] == -INFINITY) ? 0.0f : exp2f(mw[s2] - M);
+        const float Lg = __fadd_rn(__fadd_rn(r0[0 * PS + HD + 1] * wgt[0], r0[1 * PS + HD + 1] * wgt[1]),
+                                   __fadd_rn(r0[2 * PS + HD + 1] * wgt[2], r0[3 * PS + HD + 1] * wgt[3]));
+        float* pp = a.part + ((static_cast<size_t>(row) * a.H + qh) * a.max_groups + ur.g) * PS;
+#pragma unroll
+        for (int d2 = 0; d2 < DPL; ++d2) {
+          const int d = lane * DPL + d2;
+          const float v = __fadd_rn(__fadd_rn(r0[0 * PS + d] * wgt[0], r0[1 * PS + d] * wgt[1]),
+                                    __fadd_rn(r0[2 * PS + d] * wgt[2], r0[3 * PS + d] * wgt[3]));
+          __stcg(pp + d, v);
+        }
+        if (lane == 0) {
+          __stcg(pp + HD, M);
+          __stcg(pp + HD + 1, Lg);
+        }
+      }
+      quad_sync();   // records consumed before the next pass writes them
+      buf ^= 1;
     }
-    const float invl = 1.0f / Lsum;
-    const size_t lo = static_cast<size_t>(a.plane_rows) * H * HD;
+    if (sflag[1]) break;
+    // the unit that completes an (item, KV head) merges its groups in group order
+    __threadfence();
+    team_sync();
+    if (tt == 0)
+      sflag[0] = (atomicAdd(a.counters + it.counter * a.KVH + ur.kvh, 1) == it.n_groups - 1) ? 1 : 0;
+    team_sync();
+    if (sflag[0]) {
+      __threadfence();
+      for (int qi = cw; qi < nq; qi += kTeamWarps) {
+        const int row = it.row_begin + qi / G, qh = ur.kvh * G + qi % G;
+        const float* base = a.part + (static_cast<size_t>(row) * a.H + qh) * a.max_groups * PS;
+        float mg[2] = {-INFINITY, -INFINITY}, lg[2] = {0.0f, 0.0f};
 #pragma unroll
-    for (int i = 0; i < DPL; ++i) {
-      const size_t o = static_cast<size_t>(row) * H * HD + qh * HD + lane * DPL + i;
-      store_pair(a.out + o, a.out + lo + o, O[i] * invl);
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int gg = lane + 32 * h2;
+          if (gg < it.n_groups) {
+            mg[h2] = __ldcg(base + gg * PS + HD);
+            lg[h2] = __ldcg(base + gg * PS + HD + 1);
+          }
+        }
+        const float M = warp_max(fmaxf(mg[0], mg[1]));
+        float wg[2];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) wg[h2] = (lg[h2] > 0.0f) ? exp2f(mg[h2] - M) : 0.0f;
+        const float Lsum = warp_sum(__fadd_rn(lg[0] * wg[0], lg[1] * wg[1]));
+        float O[DPL];
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) O[d] = 0.0f;
+        for (int gg = 0; gg < it.n_groups; ++gg) {
+          const float wv = __shfl_sync(0xffffffffu, gg < 32 ? wg[0] : wg[1], gg & 31);
+          if (wv == 0.0f) continue;
+#pragma unroll
+          for (int d = 0; d < DPL; ++d) O[d] = fmaf(wv, __ldcg(base + gg * PS + lane * DPL + d), O[d]);
+        }
+        const float invl = 1.0f / Lsum;
+        const size_t lo = static_cast<size_t>(a.plane_rows) * a.H * HD;
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) {
+          const size_t o = static_cast<size_t>(row) * a.H * HD + qh * HD + lane * DPL + d;
+          store_pair(a.out + o, a.out + lo + o, O[d] * invl);
+        }
+      }
+      if (tt == 0) a.counters[it.counter * a.KVH + ur.kvh] = 0;
     }
   }
-  if (tid == 0) a.counters[item.counter * a.KVH + kvh] = 0;
+  cp_async_wait_all();   // no copy of a skipped pass outlives the CTA
 }
 
-template <int HD, int QB, bool SP>
-static cudaError_t launch_attn_variant(cudaLaunchConfig_t cfg, const AttnArgs& a) {
+template <int HD, int QB>
+static cudaError_t launch_attn_variant(cudaLaunchConfig_t cfg, const CUtensorMap& tm, const AttnArgs& a) {
   static bool set = false;
-  cfg.dynamicSmemBytes = attn_smem_floats(HD, QB, SP) * 4;
+  cfg.dynamicSmemBytes = AttnSmem<HD, QB>::kTotal;
   if (!set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<HD, QB, SP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel<HD, QB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(cfg.dynamicSmemBytes));
-    // three single-pass CTAs (about 69 KB each) fit only the largest shared-memory
-    // configuration, which the driver does not choose by itself for these sizes
-    if (e == cudaSuccess)
-      e = (SP && smem_carveout_pref() < 0)
-              ? cudaFuncSetAttribute(attn_kernel<HD, QB, SP>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     static_cast<int>(cudaSharedmemCarveoutMaxShared))
-              : apply_carveout(attn_kernel<HD, QB, SP>);
+    if (e == cudaSuccess) e = apply_carveout(attn_kernel<HD, QB>);
     if (e != cudaSuccess) return e;
     set = true;
   }
-  return cudaLaunchKernelEx(&cfg, attn_kernel<HD, QB, SP>, a);
+  return cudaLaunchKernelEx(&cfg, attn_kernel<HD, QB>, tm, a);
 }
 
 template <int HD>
-static cudaError_t launch_attn_hd(const cudaLaunchConfig_t& cfg, const AttnArgs& a, int max_nq) {
-  if (max_nq <= 1) return launch_attn_variant<HD, 1, true>(cfg, a);
-  if (max_nq <= 2) return launch_attn_variant<HD, 2, true>(cfg, a);
-  if (max_nq <= 4) return launch_attn_variant<HD, 4, true>(cfg, a);
-  if (max_nq <= 8) return launch_attn_variant<HD, 8, true>(cfg, a);
-  return launch_attn_variant<HD, 8, false>(cfg, a);
+static cudaError_t launch_attn_hd(const cudaLaunchConfig_t& cfg, const CUtensorMap& tm, const AttnArgs& a,
+                                  int max_nq) {
+  if (max_nq <= 1) return launch_attn_variant<HD, 1>(cfg, tm, a);
+  if (max_nq <= 2) return launch_attn_variant<HD, 2>(cfg, tm, a);
+  if (max_nq <= 4) return launch_attn_variant<HD, 4>(cfg, tm, a);
+  return launch_attn_variant<HD, 8>(cfg, tm, a);
 }
 
-cudaError_t launch_attention(const AttnArgs& a, int n_items, int max_groups_launch, int max_nq, cudaStream_t st,
+size_t attention_smem_bytes(int hd, int max_nq) {
+  const int qb = max_nq <= 1 ? 1 : max_nq <= 2 ? 2 : max_nq <= 4 ? 4 : 8;
+  if (hd == 128)
+    return qb == 1 ? AttnSmem<128, 1>::kTotal : qb == 2 ? AttnSmem<128, 2>::kTotal
+                                                          : qb == 4 ? AttnSmem<128, 4>::kTotal : AttnSmem<128, 8>::kTotal;
+  return qb == 1 ? AttnSmem<64, 1>::kTotal : qb == 2 ? AttnSmem<64, 2>::kTotal
+                                                      : qb == 4 ? AttnSmem<64, 4>::kTotal : AttnSmem<64, 8>::kTotal;
+}
+
+cudaError_t launch_attention(const CUtensorMap& tm, const AttnArgs& a, int max_nq, int n_ctas, cudaStream_t st,
                              bool pdl) {
-  if (n_items <= 0) return cudaSuccess;
-  if (!a.nodes || !a.items || !a.tails || !a.q || !a.kv_commit || !a.kv_pool || !a.out || !a.part || !a.counters ||
-      !a.err || a.plane_rows < 1 || max_groups_launch < 1 || max_groups_launch > a.max_groups ||
-      max_groups_launch > kAttnMaxGroups || max_nq < 1 || (reinterpret_cast<uintptr_t>(a.kv_commit) & 15))
+  if (a.n_items <= 0 || a.n_units <= 0) return cudaSuccess;
+  if (!a.nodes || !a.items || !a.tails || !a.q || !a.kv_pool || !a.out || !a.part || !a.counters || !a.err ||
+      a.plane_rows < 1 || a.max_groups < 1 || a.max_groups > kAttnMaxGroups || max_nq < 1 || n_ctas < 1 ||
+      (a.hd != 64 && a.hd != 128))
     return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(max_groups_launch), static_cast<unsigned>(a.KVH),
-                     static_cast<unsigned>(n_items));
+  cfg.gridDim = dim3(static_cast<unsigned>(n_ctas < a.n_units ? n_ctas : a.n_units));
   cfg.blockDim = dim3(kAttnThreads);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -457,9 +524,8 @@ cudaError_t launch_attention(const AttnArgs& a, int n_items, int max_groups_laun
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  if (a.hd == 128) return launch_attn_hd<128>(cfg, a, max_nq);
-  if (a.hd == 64) return launch_attn_hd<64>(cfg, a, max_nq);
-  return cudaErrorInvalidValue;
+  if (a.hd == 128) return launch_attn_hd<128>(cfg, tm, a, max_nq);
+  return launch_attn_hd<64>(cfg, tm, a, max_nq);
 }
 
 }  // namespace dex

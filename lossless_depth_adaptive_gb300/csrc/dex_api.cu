@@ -44,13 +44,14 @@ int get_encoder() {
 
 // 2-D bf16 tensor map over a row-major [rows][cols] matrix, box {64 cols, box_rows},
 // 128-byte swizzle, zero fill out of bounds.
-int encode_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+int encode_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+              CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   if ((reinterpret_cast<uintptr_t>(base) & 15) || (cols * 2) % 16) return DEX_EINVAL;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
   cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  CUresult r = g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DEX_OK : DEX_EINVAL;
@@ -96,7 +97,8 @@ struct dex_handle {
   int rows_cap = 0, n_slots = 0, max_groups = 0, hrows = 0;
   // device buffers
   std::vector<void*> allocs;
-  float *kv_commit = nullptr, *kv_pool = nullptr;   // fp32 KV
+  __half *kv_commit = nullptr, *kv_pool = nullptr;   // fp16 K/V caches
+  CUtensorMap tm_kv;                                 // committed cache rows for the attention
   // activation buffers: two planes of rows_cap rows each, hi then lo (x ~= hi + lo)
   bf16 *hb = nullptr, *exit_hb = nullptr, *attn_out = nullptr, *act = nullptr;
   float *hidden = nullptr, *ssq = nullptr, *exit_ssq = nullptr, *q = nullptr, *partial = nullptr,
@@ -213,10 +215,10 @@ struct Batch {
 // previous round), so their layers may share launches.
 struct Slot {
   std::vector<int> batch;   // batch indices
-  int item0 = 0, n_items = 0, max_groups = 1, max_rows = 1;
+  int item0 = 0, n_items = 0, n_units = 0, max_groups = 1, max_rows = 1;
 };
 
-std::vector<Slot> build_slots(const std::vector<Batch>& batches, RoundTables* t) {
+std::vector<Slot> build_slots(const std::vector<Batch>& batches, int kvh, RoundTables* t) {
   int max_len = 0;
   for (const auto& b : batches) max_len = std::max(max_len, b.l1 - b.l0);
   std::vector<Slot> slots(max_len);
@@ -230,6 +232,8 @@ std::vector<Slot> build_slots(const std::vector<Batch>& batches, RoundTables* t)
       for (dex::AttnItem it : b.items) {
         it.layer = b.l0 + j;
         it.counter = sl.n_items++;
+        it.unit0 = sl.n_units;
+        sl.n_units += kvh * it.n_groups;
         sl.max_groups = std::max(sl.max_groups, it.n_groups);
         sl.max_rows = std::max(sl.max_rows, it.row_end - it.row_begin);
         t->items.push_back(it);
@@ -394,9 +398,10 @@ int run_layers(dex_handle* h, const Uploaded& u, const std::vector<Batch>& batch
     dex::AttnArgs at = {};
     at.nodes = u.nodes;
     at.items = u.items + sl.item0;
+    at.n_items = sl.n_items;
+    at.n_units = sl.n_units;
     at.tails = u.tails;
     at.q = h->q;
-    at.kv_commit = h->kv_commit;
     at.kv_pool = h->kv_pool;
     at.out = h->attn_out;
     at.part = h->attn_part;
@@ -417,7 +422,7 @@ int run_layers(dex_handle* h, const Uploaded& u, const std::vector<Batch>& batch
       ae1 = next_event(h);
       cudaEventRecord(ae0, h->st);
     }
-    cudaError_t ce = dex::launch_attention(at, sl.n_items, sl.max_groups, sl.max_rows * (h->H / h->KVH), h->st, true);
+    cudaError_t ce = dex::launch_attention(h->tm_kv, at, sl.max_rows * (h->H / h->KVH), h->n_sm, h->st, true);
     if (ce != cudaSuccess) return cuda_fail(h, ce);
     if (h->timing == 2) {
       cudaEventRecord(ae1, h->st);
@@ -549,7 +554,7 @@ int run_round(dex_handle* h, dex::Lattice* lat, std::vector<dex_copy_job>* pendi
     if (b.n > 256) return DEX_ECAPACITY;
     batches.push_back(b);
   }
-  const std::vector<Slot> slots = build_slots(batches, &t);
+  const std::vector<Slot> slots = build_slots(batches, h->KVH, &t);
   t.jobs = *pending;
   const double host_plan_ms =
       std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t_host0).count();
@@ -571,7 +576,7 @@ int run_round(dex_handle* h, dex::Lattice* lat, std::vector<dex_copy_job>* pendi
     ca.err = h->err;
     ca.L = h->L;
     ca.KVH = h->KVH;
-    ca.row_bytes = h->hd * 4;
+    ca.row_bytes = h->hd * 2;
     ca.max_ctx = h->cfg.max_ctx;
     ca.n_slots = h->n_slots;
     cudaError_t ce = dex::launch_collapse(ca, h->st, false);
@@ -692,7 +697,7 @@ int run_round(dex_handle* h, dex::Lattice* lat, std::vector<dex_copy_job>* pendi
   const int64_t layer_w = (static_cast<int64_t>(h->H + 2 * h->KVH) * h->hd * h->d + static_cast<int64_t>(h->H) *
                            h->hd * h->d + 3ll * h->dff * h->d) * 2;
   h->stats.weight_bytes += layer_w * X[max_stage] + static_cast<int64_t>(h->V) * h->d * 2;
-  const int64_t kv_row = 2ll * h->KVH * h->hd * 4;
+  const int64_t kv_row = 2ll * h->KVH * h->hd * 2;   // fp16 K and V of one position and layer
   for (const Batch& b : batches) {
     const int nl = b.l1 - b.l0;
     // committed keys and values once per (sequence, layer), however many items read them
@@ -873,10 +878,11 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
   h->hrows = cfg->batch * h->n_slots + 256;
 
   const size_t B = cfg->batch, L = h->L, KVH = h->KVH, hd = h->hd, ctx = cfg->max_ctx, R = h->rows_cap;
+  if (B * L * 2 * KVH * ctx >= (size_t(1) << 31)) return DEX_ECAPACITY;   // committed rows: 32-bit TMA rows
   const int qd = h->H * h->hd, kvd = h->KVH * h->hd;
   int rc = 0;
-  rc |= dalloc(h, &h->kv_commit, B * L * 2 * KVH * ctx * hd * 4);
-  rc |= dalloc(h, &h->kv_pool, B * h->n_slots * L * 2 * KVH * hd * 4);
+  rc |= dalloc(h, &h->kv_commit, B * L * 2 * KVH * ctx * hd * 2);
+  rc |= dalloc(h, &h->kv_pool, B * h->n_slots * L * 2 * KVH * hd * 2);
   rc |= dalloc(h, &h->hidden, static_cast<size_t>(h->hrows) * h->d * 4);
   rc |= dalloc(h, &h->hb, 2 * R * h->d * 2);
   rc |= dalloc(h, &h->exit_hb, 2 * R * h->d * 2);
@@ -935,8 +941,8 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
   cudaMemsetAsync(h->counters, 0, ntiles_max * 4 * std::max(1, h->N), h->st);
   cudaMemsetAsync(h->attn_counters, 0, (static_cast<size_t>(B) * h->N + R) * KVH * 4, h->st);
   cudaMemsetAsync(h->err, 0, 16, h->st);
-  cudaMemsetAsync(h->kv_commit, 0, B * L * 2 * KVH * ctx * hd * 4, h->st);
-  cudaMemsetAsync(h->kv_pool, 0, B * h->n_slots * L * 2 * KVH * hd * 4, h->st);
+  cudaMemsetAsync(h->kv_commit, 0, B * L * 2 * KVH * ctx * hd * 2, h->st);
+  cudaMemsetAsync(h->kv_pool, 0, B * h->n_slots * L * 2 * KVH * hd * 2, h->st);
   cudaMemsetAsync(h->hidden, 0, static_cast<size_t>(h->hrows) * h->d * 4, h->st);
   cudaMemsetAsync(h->hb, 0, 2 * R * h->d * 2, h->st);
   cudaMemsetAsync(h->exit_hb, 0, 2 * R * h->d * 2, h->st);
@@ -979,6 +985,8 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
     rc |= encode_2d(&h->tm_d[l], W(h, li, 8), h->d, h->dff, 128);
   }
   rc |= encode_2d(&h->tm_lm, h->lm_head, h->V, h->d, 128);
+  // committed K/V rows of hd fp16 elements: [B][L][2][KVH][max_ctx] rows (32-row boxes)
+  rc |= encode_2d(&h->tm_kv, h->kv_commit, B * L * 2 * KVH * ctx, hd, 32, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
   for (int i = 1; i <= 16; ++i) {
     rc |= encode_2d(&h->tm_hb[i], h->hb, 2 * R, h->d, 16 * i);
     rc |= encode_2d(&h->tm_attn[i], h->attn_out, 2 * R, qd, 16 * i);
@@ -1097,7 +1105,7 @@ int dex_prefill(dex_handle* h, int32_t seq, const int32_t* tokens, int32_t n_tok
     it.max_cend = c0 + n;
     it.n_groups = it.max_pos / dex::kAttnGroupPos + 1;
     batches[0].items.push_back(it);
-    const std::vector<Slot> slots = build_slots(batches, &t);
+    const std::vector<Slot> slots = build_slots(batches, h->KVH, &t);
     Uploaded u;
     int rc = upload(h, t, &u);
     if (rc) return rc;

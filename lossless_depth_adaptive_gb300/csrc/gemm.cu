@@ -36,8 +36,8 @@
 // cycles from accumulator-ready to the arrival count), and at the end the clock64 and
 // the unit count.
 //
-// Epilogues: EPI_QKV (RMSNorm scale, RoPE, K/V into the committed cache or the branch
-// pool), EPI_RESID (residual add into the fp32 hidden state, next layer's bf16 input,
+// Epilogues: EPI_QKV (RMSNorm scale, RoPE, fp16 K/V into the committed cache or the
+// branch pool), EPI_RESID (residual add into the fp32 hidden state, next layer's bf16 input,
 // RMSNorm partial sums, exit-head input at a stage boundary), EPI_SWIGLU
 // (SiLU(gate) * up), EPI_EXIT (exit logits, DECS mask, Gumbel noise, argmax).
 #include <algorithm>
@@ -372,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             a.q_out[static_cast<size_t>(b_row0 + c) * (a.H * a.hd) + f] = out;
           } else {
             const int kv = src - 1;
-            float* dst;
+            __half* dst;
             if (nd->kv_commit) {
               dst = a.kv_commit +
                     ((((static_cast<size_t>(nd->seq) * a.L + grp.layer) * 2 + kv) * a.KVH + head) * a.max_ctx +
@@ -382,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ((((static_cast<size_t>(nd->seq) * a.n_slots + nd->slot) * a.L + grp.layer) * 2 + kv) * a.KVH +
                      head) * a.hd + dim;
             }
-            *dst = out;
+            *dst = __float2half_rn(out);   // the caches hold fp16 K/V
           }
         }
         named_bar_sync(1, 128);

@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -47,6 +48,8 @@ struct AttnItem {
   int32_t n_groups;                  // kAttnGroupPos-position key groups covering 0..max_pos
   int32_t counter;                   // index of this item's merge counters (x KVH)
   int32_t layer;                     // decoder layer of this item (items of several stages share a launch)
+  int32_t unit0;                     // first (item, KV head, group) unit of the item in its launch
+  int32_t pad0;
 };
 
 // EPI_ADUP / EPI_ADDOWN: the two layers of an inducing adapter at a non-final exit.
@@ -96,8 +99,8 @@ struct GemmArgs {
   const float* ssq_in;  // [rows][d/128]
   // QKV
   float* q_out;         // [rows][H*hd]
-  float* kv_commit;     // [B][L][2][KVH][max_ctx][hd] fp32
-  float* kv_pool;       // [B][n_slots][L][2][KVH][hd] fp32
+  __half* kv_commit;    // [B][L][2][KVH][max_ctx][hd] fp16
+  __half* kv_pool;      // [B][n_slots][L][2][KVH][hd] fp16
   const float2* rope;   // [max_ctx][hd/2] (cos, sin)
   // RESID
   float* hidden;        // [hrows][d]
@@ -122,13 +125,15 @@ struct GemmArgs {
 constexpr int kTimelineUnits = 48;
 constexpr int kTimelineSlots = 4 + 3 * kTimelineUnits;
 
+// The committed cache is read through a TMA tensor map (fp16 rows of hd elements, box
+// 64 x 32 rows, 128-byte swizzle); the branch pool through kv_pool.
 struct AttnArgs {
   const DevNode* nodes;
   const AttnItem* items;
+  int32_t n_items, n_units;    // items of the launch; units = sum over items of KVH x n_groups
   const int32_t* tails;
   const float* q;              // [rows][H*hd]
-  const float* kv_commit;      // fp32 caches (layouts as in GemmArgs)
-  const float* kv_pool;
+  const __half* kv_pool;       // fp16 pool (layout as in GemmArgs)
   __nv_bfloat16* out;          // [2][plane_rows][H*hd] hi/lo pair
   int32_t plane_rows;
   float* part;                 // [rows][H][max_groups][hd + 2]
@@ -153,7 +158,7 @@ struct AssembleArgs {
 
 struct CopyJob { int32_t seq, slot, pos, n_layers; };
 
-// KV rows are copied as raw bytes: row_bytes = head_dim x element size (fp32 caches of the
+// KV rows are copied as raw bytes: row_bytes = head_dim x element size (fp16 caches of the
 // decoder, bf16 caches of the isolated entry point), a multiple of 16.
 // A job whose sequence, slot, position or layer count is out of range is skipped (nothing
 // is read or written for it): it sets *err to DEV_BAD_INDEX and adds one to *rejected
@@ -194,8 +199,11 @@ inline cudaError_t apply_carveout(F* func) {
   return cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, c);
 }
 
-cudaError_t launch_attention(const AttnArgs& a, int n_items, int max_groups_launch, int max_nq, cudaStream_t st,
+// Persistent launch over min(n_units, n_ctas) CTAs (one per SM); max_nq picks the query
+// batch of a pass (1, 2, 4 or 8; items with more queries take several passes).
+cudaError_t launch_attention(const CUtensorMap& tm_kv, const AttnArgs& a, int max_nq, int n_ctas, cudaStream_t st,
                              bool pdl);
+size_t attention_smem_bytes(int hd, int max_nq);
 cudaError_t launch_assemble(const AssembleArgs& a, cudaStream_t st, bool pdl);
 cudaError_t launch_collapse(const CollapseArgs& a, cudaStream_t st, bool pdl);
 // bf16 [n][d] rows -> hi/lo pair of h * g ([2][plane_rows][d]) and partial sums of squares
