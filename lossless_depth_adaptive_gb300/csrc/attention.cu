@@ -428,14 +428,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       buf ^= 1;
     }
     if (sflag[1]) break;
-    // the unit that completes an (item, KV head) merges its groups in group order
-    __threadfence();
+    // the unit that completes an (item, KV head) merges its groups in group order: the
+    // barrier orders the team's partial writes before one thread's gpu-scope release
+    // increment; the last arriver's acquire makes every unit's partials visible
     team_sync();
-    if (tt == 0)
-      sflag[0] = (atomicAdd(a.counters + it.counter * a.KVH + ur.kvh, 1) == it.n_groups - 1) ? 1 : 0;
+    if (tt == 0) {
+      int prev;
+      asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;"
+                   : "=r"(prev)
+                   : "l"(a.counters + it.counter * a.KVH + ur.kvh)
+                   : "memory");
+      sflag[0] = (prev == it.n_groups - 1) ? 1 : 0;
+    }
     team_sync();
     if (sflag[0]) {
-      __threadfence();
       for (int qi = cw; qi < nq; qi += kTeamWarps) {
         const int row = it.row_begin + qi / G, qh = ur.kvh * G + qi % G;
         const float* base = a.part + (static_cast<size_t>(row) * a.H + qh) * a.max_groups * PS;
@@ -456,11 +462,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         float O[DPL];
 #pragma unroll
         for (int d = 0; d < DPL; ++d) O[d] = 0.0f;
-        for (int gg = 0; gg < it.n_groups; ++gg) {
-          const float wv = __shfl_sync(0xffffffffu, gg < 32 ? wg[0] : wg[1], gg & 31);
-          if (wv == 0.0f) continue;
+        // groups in order; the loads of four groups are issued before their FMAs
+        for (int g4 = 0; g4 < it.n_groups; g4 += 4) {
+          float pv[4][DPL], wv[4];
 #pragma unroll
-          for (int d = 0; d < DPL; ++d) O[d] = fmaf(wv, __ldcg(base + gg * PS + lane * DPL + d), O[d]);
+          for (int e = 0; e < 4; ++e) {
+            const int gg = g4 + e;
+            wv[e] = __shfl_sync(0xffffffffu, gg < 32 ? wg[0] : wg[1], gg & 31);
+            if (gg >= it.n_groups) wv[e] = 0.0f;
+#pragma unroll
+            for (int d = 0; d < DPL; ++d) pv[e][d] = wv[e] != 0.0f ? __ldcg(base + gg * PS + lane * DPL + d) : 0.0f;
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (wv[e] == 0.0f) continue;
+#pragma unroll
+            for (int d = 0; d < DPL; ++d) O[d] = fmaf(wv[e], pv[e][d], O[d]);
+          }
         }
         const float invl = 1.0f / Lsum;
         const size_t lo = static_cast<size_t>(a.plane_rows) * a.H * HD;
