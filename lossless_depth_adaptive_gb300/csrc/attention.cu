@@ -1,4 +1,5 @@
-// Lattice-masked attention for the node batches of a DEX round (and prefill chunks).
+// Lattice-masked attention for the node batches of a DEX round (and prefill chunks), with
+// the bulk of every query's keys on the 5th-generation tensor cores.
 //
 // A node at input position p attends keys 0..p of its own token prefix (section 3.2:
 // "ancestry, KV entries, and attention masks" follow the binary lattice).  Keys at
@@ -6,24 +7,28 @@
 // sequence); keys at c_end..p are the branch entries of the node's P-ancestors' slot
 // chains and its own, read from the branch pool through the node's tail table.
 //
-// Work: a unit is (item, KV head, 128-position key group); an item is one sequence's
-// contiguous node rows of one layer.  Persistent CTAs (one per SM) take contiguous ranges
-// of units.  Warp 0 streams each unit's committed key and value tiles (fp16, up to 128
-// rows) into a ring of shared-memory stages with TMA (128-byte swizzle, 32-row boxes, so
-// a ragged last group moves only the rows it has); eight consumer warps work on the
-// oldest landed stage while the next stages load.  The consumers form two quads; each
-// quad takes half of the unit's queries, and within a quad warp w owns keys 32w..32w+31
-// of the group.  Scores take lane = key (the swizzle puts the 16-byte chunk c of the
-// eight rows a quarter-warp reads in eight distinct bank groups; the query chunk is one
-// broadcast read); values take lane = four (or two) output dims, so a warp reads one
-// whole value row per load.  A committed key is read from HBM once per (item, KV head).
+// Split of a query's keys (fixed by its position p alone):
+//  * bulk keys [0, b), b = max(0, p - kAttnWindow + 1): always committed (a node's branch
+//    keys are its last <= |X| positions and kAttnWindow > |X|).  Per 128-position group,
+//    scores S = K Q^T and the group output O = V^T P^T run as tcgen05 MMAs (M = 128 keys or
+//    128 value dims, N = 16 queries) from shared-memory tiles: K and V fp16 tiles exactly as
+//    cached, Q and P as fp16 hi/lo pairs (x ~= hi + lo, two MMAs into one fp32 accumulator),
+//    so every product is carried to about fp32 precision.  A masked key gets p = 0, which
+//    adds exact zeros.
+//  * window keys [b, p] (at most kAttnWindow): fp32 dot products on CUDA cores, reading
+//    the committed cache or the branch pool, in one fixed order wherever the row lives.
+// The group partials (max, sum, output) are combined in group order and then with the
+// window part by the unit that completes an (item, KV head).  A tensor-core element's
+// value depends only on its own row and column operands, so a query's result is the same
+// bits whatever else shares its MMA, whichever buffer holds its window keys, and whatever
+// batch or launch it is in: GPU-DEX equals GPU-AR bit for bit.
 //
-// The arithmetic for a query is fixed by absolute positions only -- 32-key slices aligned
-// to position 0, each score summed in chunk order wherever the key row lives (tile or
-// pool), slices combined in order within a group, groups combined in group order by the
-// unit that finishes an (item, KV head) last -- so a node's output is bit-identical
-// whether its keys sit in the committed cache or the branch pool and whatever batch,
-// launch or CTA it is computed in.
+// Work: a unit is (item, KV head, group); an item is one sequence's contiguous node rows of
+// one layer (at most 16 queries per pass; prefill items take several passes).  Persistent
+// CTAs (one per SM) take contiguous ranges of units.  Warp 0 streams the committed K and V
+// tiles of each unit through a ring of shared-memory stages with TMA (128-byte swizzle,
+// 32-row boxes); warp 1 owns TMEM and issues the MMAs; warps 2-5 build the query tiles,
+// run the softmax between the two MMAs and write the group partials.
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -31,91 +36,60 @@
 
 namespace dex {
 
-constexpr int kSlices = kAttnGroupPos / 32;           // 32-key slices per group
-constexpr int kTeamWarps = 2 * kSlices;               // two quads of consumer warps
-constexpr int kAttnThreads = 32 * (1 + kTeamWarps);   // + the producer warp
+constexpr int kQT = kAttnPassQueries;                 // queries per pass (MMA N)
+constexpr int kAttnThreads = 192;                     // producer, MMA, four epilogue warps
 constexpr int kBoxRows = 32;                          // TMA box height
-constexpr int kTeamBar = 1, kQuadBar0 = 2;            // named barriers (ids)
-static_assert(kAttnGroupPos == 128 && kSlices == 4, "four 32-key slices per 128-position group");
+constexpr int kEpiBar = 1;                            // named barrier of the epilogue warps
+static_assert(kAttnGroupPos == 128 && kQT == 16, "128-key groups, 16-query MMA columns");
 
-// Shared-memory plan of a CTA: ring stages (K tile, V tile), two query buffers, the slice
-// records of one pass, barriers.
-template <int HD, int QB>
+// Shared-memory plan: K/V ring, query and probability tiles (hi, lo), a zero atom that pads
+// the 64-dim value tiles of head_dim 64 to the MMA's 128 rows, reduction scratch, barriers.
+template <int HD>
 struct AttnSmem {
-  static constexpr uint32_t kTile = kAttnGroupPos * HD * 2;     // fp16 tile, 1024-aligned
+  static constexpr uint32_t kTile = kAttnGroupPos * HD * 2;   // [128 rows][HD] fp16, HD/64 halves of 16 KB
   static constexpr uint32_t kStage = 2 * kTile;
-  static constexpr int kStages = (HD == 128) ? 3 : 6;
+  static constexpr int kStages = (HD == 128) ? 3 : 5;
   static constexpr uint32_t kRing = kStages * kStage;
-  static constexpr uint32_t kQ = 2u * QB * HD * 4;              // double-buffered fp32 queries
-  static constexpr uint32_t kRec = static_cast<uint32_t>(QB) * kSlices * (HD + 2) * 4;
-  static constexpr uint32_t kBars = 2 * kStages * 8 + 16;
-  static constexpr uint32_t kTotal = kRing + kQ + kRec + kBars + 1024;   // + alignment slack
+  static constexpr uint32_t kQTile = kQT * HD * 2;            // [16][HD] fp16, HD/64 halves of 2 KB
+  static constexpr uint32_t kPTile = kQT * kAttnGroupPos * 2; // [16][128 keys] fp16, two halves of 2 KB
+  static constexpr uint32_t kZero = (HD == 128) ? 0 : kAttnGroupPos * 128;
+  static constexpr uint32_t oQhi = kRing, oQlo = oQhi + kQTile, oPhi = oQlo + kQTile, oPlo = oPhi + kPTile;
+  static constexpr uint32_t oZero = oPlo + kPTile;
+  static constexpr uint32_t oRed = oZero + kZero;                  // float [2][4][16] max / sum
+  static constexpr uint32_t oMeta = oRed + 2 * 4 * kQT * 4;        // int [16] bulk bounds
+  static constexpr uint32_t oBar = oMeta + kQT * 4 + 16;
+  static constexpr uint32_t kTotal = oBar + (2 * kStages + 4) * 8 + 16 + 1024;   // + alignment slack
 };
 
-// q . k over 8-dim chunks in order: four partial sums by feature residue mod 4 (features
-// 4c + r go to sum r), two per packed FMA (each element rounded as fmaf), then
-// (s0 + s1) + (s2 + s3).
-__device__ __forceinline__ void dot8(float2& s01, float2& s23, const float* q, const uint4& kraw) {
-  const float4 qa = *reinterpret_cast<const float4*>(q);
-  const float4 qb = *reinterpret_cast<const float4*>(q + 4);
-  const float2 k0 = __half22float2(*reinterpret_cast<const __half2*>(&kraw.x));
-  const float2 k1 = __half22float2(*reinterpret_cast<const __half2*>(&kraw.y));
-  const float2 k2 = __half22float2(*reinterpret_cast<const __half2*>(&kraw.z));
-  const float2 k3 = __half22float2(*reinterpret_cast<const __half2*>(&kraw.w));
-  s01 = __ffma2_rn(make_float2(qa.x, qa.y), k0, s01);
-  s23 = __ffma2_rn(make_float2(qa.z, qa.w), k1, s23);
-  s01 = __ffma2_rn(make_float2(qb.x, qb.y), k2, s01);
-  s23 = __ffma2_rn(make_float2(qb.z, qb.w), k3, s23);
+// MN-major operand descriptor, 128-byte swizzle: 64 contiguous 16-bit elements of M (or N)
+// per 128-byte row, rows along K 128 bytes apart in 1024-byte 8-row atoms; lbo = bytes
+// between 64-element atoms along M, sbo = bytes between 8-row groups along K.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
 }
-__device__ __forceinline__ float dot_finish(const float2& s01, const float2& s23) {
-  return __fadd_rn(__fadd_rn(s01.x, s01.y), __fadd_rn(s23.x, s23.y));
-}
-
-// 16-byte chunk c (dims 8c..8c+7) of row r of a swizzled fp16 tile: 64-dim halves of
-// kAttnGroupPos rows x 128 bytes; chunk cc of row r sits at (cc ^ (r & 7)) * 16.
-__device__ __forceinline__ uint32_t tile_chunk_off(int r, int c) {
-  return static_cast<uint32_t>((c >> 3) * (kAttnGroupPos * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+// kind::f16 instruction descriptor with fp16 A and B, fp32 D; a_mn: A is MN-major.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn) {
+  return (1u << 4) | (a_mn ? (1u << 15) : 0u) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// Dims [lane * DPL, lane * DPL + DPL) of row r of a value tile (or a pool row) as floats.
-template <int HD>
-__device__ __forceinline__ void value_dims_tile(const uint8_t* tile, int r, int lane, float (&v)[HD / 32]) {
-  if constexpr (HD == 128) {   // four dims = 8 bytes: chunk lane / 2, half (lane & 1)
-    const uint2 raw =
-        *reinterpret_cast<const uint2*>(tile + tile_chunk_off(r, lane >> 1) + ((lane & 1) << 3));
-    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
-    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
-    v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
-  } else {                     // two dims = 4 bytes: chunk lane / 4, quarter (lane & 3)
-    const uint32_t raw = *reinterpret_cast<const uint32_t*>(tile + tile_chunk_off(r, lane >> 2) + ((lane & 3) << 2));
-    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw));
-    v[0] = a.x; v[1] = a.y;
-  }
-}
-template <int HD>
-__device__ __forceinline__ void value_dims_row(const __half* row, int lane, float (&v)[HD / 32]) {
-  if constexpr (HD == 128) {
-    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(row) + lane);
-    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
-    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
-    v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
-  } else {
-    const uint32_t raw = __ldg(reinterpret_cast<const uint32_t*>(row) + lane);
-    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw));
-    v[0] = a.x; v[1] = a.y;
-  }
+// fp32 -> (hi, lo) fp16 pair: hi = fp16(x), lo = fp16(x - hi).
+__device__ __forceinline__ void split_f16(float x, __half& hi, __half& lo) {
+  hi = __float2half_rn(x);
+  lo = __float2half_rn(__fsub_rn(x, __half2float(hi)));
 }
 
-// acc[i] += p * v[i] over the lane's output dims, two dims per packed FMA.
-template <int DPL>
-__device__ __forceinline__ void axpy_dims(float (&acc)[DPL], float p, const float (&v)[DPL]) {
-  const float2 pp = make_float2(p, p);
-#pragma unroll
-  for (int i = 0; i < DPL; i += 2) {
-    const float2 r = __ffma2_rn(pp, make_float2(v[i], v[i + 1]), make_float2(acc[i], acc[i + 1]));
-    acc[i] = r.x;
-    acc[i + 1] = r.y;
-  }
+// Byte offset of element (row, col) in a 128-byte-swizzled fp16 tile whose 64-column halves
+// hold `rows` rows each.
+__device__ __forceinline__ uint32_t sw_elem_off(int row, int col, int rows) {
+  return static_cast<uint32_t>((col >> 6) * rows * 128 + row * 128 + ((((col >> 3) & 7) ^ (row & 7)) << 4) +
+                               ((col & 7) << 1));
 }
 
 struct UnitRef {
@@ -137,28 +111,30 @@ __device__ __forceinline__ UnitRef unit_ref(const AttnArgs& a, int u) {
   r.g = rem - r.kvh * ng;
   return r;
 }
-// Committed rows of group g that some query of the item reads: [g0, g0 + n).
-__device__ __forceinline__ int committed_rows(const AttnItem& it, int g) {
-  return max(0, min(kAttnGroupPos, min(it.max_cend, it.max_pos + 1) - g * kAttnGroupPos));
-}
+__device__ __forceinline__ int bulk_end(int pos) { return max(0, pos - kAttnWindow + 1); }
 
-template <int HD, int QB>
+template <int HD>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tmKV, const __grid_constant__ AttnArgs a) {
-  using SM = AttnSmem<HD, QB>;
+  using SM = AttnSmem<HD>;
   constexpr int S = SM::kStages;
-  constexpr int DPL = HD / 32;                  // output dims per lane
-  constexpr int NCH = HD / 8;                   // 16-byte chunks per fp16 row
-  constexpr int QH = QB >= 2 ? QB / 2 : 1;      // queries per quad per pass
-  constexpr int PS = HD + 2;                    // slice record: acc[HD], m, l
+  constexpr int KSTEPS = HD / 16;                // QK k-steps (dims)
+  constexpr int PSTEPS = kAttnGroupPos / 16;     // PV k-steps (keys)
+  constexpr int PS = HD + 2;                     // partial record: O[HD], m, l
+  constexpr int DPL = HD / 32;                   // window dims per lane
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
-  float* sQ = reinterpret_cast<float*>(smem + SM::kRing);           // [2][QB][HD]
-  float* sRec = sQ + 2 * QB * HD;                                   // [QB][kSlices][PS]
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::kRing + SM::kQ + SM::kRec);
+  float* red = reinterpret_cast<float*>(smem + SM::oRed);     // [0]: max [4][16], [1]: sum [4][16]
+  int* meta = reinterpret_cast<int*>(smem + SM::oMeta);       // bulk bound per pass-local query
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::oBar);
   uint64_t* empty = full + S;
-  volatile int* sflag = reinterpret_cast<volatile int*>(empty + S);   // [0] last arriver, [1] abort
+  uint64_t* q_full = empty + S;   // query tile written (epilogue -> MMA)
+  uint64_t* s_full = q_full + 1;  // scores in TMEM (MMA -> epilogue)
+  uint64_t* p_full = s_full + 1;  // probability tile written (epilogue -> MMA)
+  uint64_t* o_full = p_full + 1;  // group output in TMEM (MMA -> epilogue)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_full + 1);
+  volatile int* sflag = reinterpret_cast<volatile int*>(tmem_slot + 1);   // [0] last arriver, [1] abort
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int C = gridDim.x, cta = blockIdx.x;
@@ -169,17 +145,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kTeamWarps);
+      mbar_init(&empty[s], 1);
     }
+    mbar_init(q_full, 128);
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 128);
+    mbar_init(o_full, 1);
     sflag[0] = 0;
     sflag[1] = 0;
     fence_mbar_init();
     tma_prefetch(&tmKV);
   }
+  // rows of a tile beyond what TMA writes keep finite values: zero the ring (and the zero
+  // atom) once, so a masked key (p = 0) never meets a non-finite value in the MMA
+  for (uint32_t o = tid * 16; o < SM::oRed; o += kAttnThreads * 16)
+    *reinterpret_cast<uint4*>(smem + o) = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 32);
+    tmem_relinquish();
+  }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
   griddep_wait();   // q and this round's K/V come from the preceding launch
   griddep_launch_dependents();
-  if (n_my <= 0) return;
 
   if (warp == 0) {
     // ---------------- producer: committed K and V tiles of each unit ----------------
@@ -194,12 +185,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         const UnitRef ur = unit_ref(a, u0 + i);
         const AttnItem it = a.items[ur.item];
-        const int n_com = committed_rows(it, ur.g);
+        const int g0 = ur.g * kAttnGroupPos;
+        const int n_com = max(0, min(kAttnGroupPos, bulk_end(it.max_pos) - g0));
         const int nbox = (n_com + kBoxRows - 1) / kBoxRows;
         constexpr int halves = HD / 64;
         mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(2 * nbox * halves * kBoxRows * 128));
-        const int row_k = ((((it.seq * a.L + it.layer) * 2 + 0) * a.KVH + ur.kvh) * a.max_ctx) +
-                          ur.g * kAttnGroupPos;
+        const int row_k = ((((it.seq * a.L + it.layer) * 2 + 0) * a.KVH + ur.kvh) * a.max_ctx) + g0;
         const int row_v = row_k + a.KVH * a.max_ctx;
         uint8_t* sk = ring + static_cast<size_t>(st) * SM::kStage;
         uint8_t* sv = sk + SM::kTile;
@@ -218,319 +209,332 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           mbar_wait(&full[i % S], static_cast<uint32_t>(i / S) & 1u, nullptr, 0);
       }
     }
-    return;
-  }
-
-  // ---------------- consumers: warps 1..8, quads of four key slices ----------------
-  const int cw = warp - 1, quad = cw >> 2, w = cw & 3;
-  const int tt = tid - 32;                      // team thread 0..255
-  const int qbar = kQuadBar0 + quad;
-  auto team_sync = [] { named_bar_sync(kTeamBar, 32 * kTeamWarps); };
-  auto quad_sync = [&] { named_bar_sync(qbar, 32 * kSlices); };
-
-  // query pass sequence of this CTA: (unit i, pass p); the next pass's queries are copied
-  // into the other buffer while the current one is computed
-  auto issue_q = [&](int i, int p, int buf) {
-    const UnitRef ur = unit_ref(a, u0 + i);
-    const AttnItem it = a.items[ur.item];
-    const int nq = (it.row_end - it.row_begin) * G;
-    const int q0 = p * QB;
-    float* dst = sQ + buf * QB * HD;
-    for (int idx = tt * 4; idx < QB * HD; idx += 32 * kTeamWarps * 4) {
-      const int j = idx / HD, d = idx - j * HD;
-      const int qi = q0 + j;
-      if (qi < nq) {
-        const int row = it.row_begin + qi / G, qh = ur.kvh * G + qi % G;
-        cp_async_16(smem_u32(dst + idx), a.q + (static_cast<size_t>(row) * a.H + qh) * HD + d);
-      } else {
-        *reinterpret_cast<float4*>(dst + idx) = make_float4(0.f, 0.f, 0.f, 0.f);
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      const uint32_t id_qk = idesc_f16_f32(128, kQT, false);
+      const uint32_t id_pv = idesc_f16_f32(128, kQT, true);
+      const uint32_t d_s = tmem_base, d_o = tmem_base + kQT;
+      const uint32_t qhi = smem_u32(smem + SM::oQhi), qlo = smem_u32(smem + SM::oQlo);
+      const uint32_t phi = smem_u32(smem + SM::oPhi), plo = smem_u32(smem + SM::oPlo);
+      uint32_t np = 0;   // passes so far (barrier phases)
+      bool ok = true;
+      for (int i = 0; i < n_my && ok; ++i) {
+        const UnitRef ur = unit_ref(a, u0 + i);
+        const AttnItem it = a.items[ur.item];
+        const int st = i % S;
+        const int n_pass = ((it.row_end - it.row_begin) * G + kQT - 1) / kQT;
+        const uint32_t kt = smem_u32(ring + static_cast<size_t>(st) * SM::kStage);
+        const uint32_t vt = kt + SM::kTile;
+        const uint32_t lbo_v = (HD == 128) ? 64u * 256u : smem_u32(smem + SM::oZero) - vt;
+        if (!mbar_wait(&full[st], static_cast<uint32_t>(i / S) & 1u, a.err, DEV_TIMEOUT_FULL)) break;
+        for (int p = 0; p < n_pass; ++p, ++np) {
+          if (!mbar_wait(q_full, np & 1u, a.err, DEV_TIMEOUT_FULL)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < KSTEPS; ++ks) {   // S = K Q^T over 16-dim steps, hi then lo
+            const uint32_t off_a = static_cast<uint32_t>((ks >> 2) * kAttnGroupPos * 128 + (ks & 3) * 32);
+            const uint32_t off_b = static_cast<uint32_t>((ks >> 2) * kQT * 128 + (ks & 3) * 32);
+            const uint64_t ad = sw128_kmajor_desc(kt + off_a);
+            umma_bf16(d_s, ad, sw128_kmajor_desc(qhi + off_b), id_qk, ks > 0 ? 1u : 0u);
+            umma_bf16(d_s, ad, sw128_kmajor_desc(qlo + off_b), id_qk, 1u);
+          }
+          umma_commit(s_full);
+          if (!mbar_wait(p_full, np & 1u, a.err, DEV_TIMEOUT_FULL)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < PSTEPS; ++ks) {   // O^T = V^T P^T over 16-key steps, hi then lo
+            const uint64_t ad = sw128_mnmajor_desc(vt + ks * 16 * 128, lbo_v, 1024);
+            const uint32_t off_b = static_cast<uint32_t>((ks >> 2) * kQT * 128 + (ks & 3) * 32);
+            umma_bf16(d_o, ad, sw128_kmajor_desc(phi + off_b), id_pv, ks > 0 ? 1u : 0u);
+            umma_bf16(d_o, ad, sw128_kmajor_desc(plo + off_b), id_pv, 1u);
+          }
+          umma_commit(o_full);
+          if (p == n_pass - 1) umma_commit(&empty[st]);   // the stage is free once these MMAs complete
+        }
       }
     }
-    cp_async_commit();
-  };
-  int buf = 0;
-  issue_q(0, 0, 0);
-  for (int i = 0; i < n_my; ++i) {
-    const UnitRef ur = unit_ref(a, u0 + i);
-    const AttnItem it = a.items[ur.item];
-    const int st = i % S;
-    const int g0 = ur.g * kAttnGroupPos;
-    const int nq = (it.row_end - it.row_begin) * G;
-    const int n_pass = (nq + QB - 1) / QB;
-    const uint8_t* sk = ring + static_cast<size_t>(st) * SM::kStage;
-    const uint8_t* sv = sk + SM::kTile;
-    const bool landed = mbar_wait(&full[st], static_cast<uint32_t>(i / S) & 1u, a.err, DEV_TIMEOUT_FULL);
-    if (!landed) sflag[1] = 1;
-    const __half* kcom_pool = reinterpret_cast<const __half*>(a.kv_pool);
-    // the branch-pool row of key kk (kk >= c_end) of node row nrow
-    auto pool_row = [&](int nrow, int kk, int kv) -> const __half* {
-      const DevNode* nd = a.nodes + nrow;
-      const int t = kk - nd->c_end;
-      int slot = 0;
-      if (t >= 0 && t < nd->n_tail) {
-        slot = a.tails[nd->tail_off + t];
-      } else {   // cannot happen for a well-formed plan; reported, and slot 0 is read instead
-        atomicExch(a.err, DEV_BAD_INDEX);
+  } else {
+    // ---------------- epilogue: query tiles, softmax, partials, merge ----------------
+    const int et = tid - 64;                   // 0..127
+    const int lq = warp & 3;                   // TMEM lane quarter of this warp
+    const int r = lq * 32 + lane;              // TMEM row: key (scores) or value dim (output)
+    const uint32_t t_row = static_cast<uint32_t>(lq * 32) << 16;
+    uint8_t* qhi = smem + SM::oQhi;
+    uint8_t* qlo = smem + SM::oQlo;
+    uint8_t* phi = smem + SM::oPhi;
+    uint8_t* plo = smem + SM::oPlo;
+    auto epi_sync = [] { named_bar_sync(kEpiBar, 128); };
+    constexpr int QD = HD / 8;                 // query dims per thread (8 threads per query)
+    const int qj = et >> 3, qd0 = (et & 7) * QD;
+    uint32_t np = 0;
+    // this thread's slice of pass (i, p)'s queries, fp32 (prefetched one pass ahead)
+    float qv[QD];
+    auto load_q = [&](int i, int p) {
+      const UnitRef ur = unit_ref(a, u0 + i);
+      const AttnItem it = a.items[ur.item];
+      const int nq = (it.row_end - it.row_begin) * G;
+      const int qi = p * kQT + qj;
+#pragma unroll
+      for (int e = 0; e < QD; ++e) qv[e] = 0.0f;
+      if (qi < nq) {
+        const int row = it.row_begin + qi / G, qh = ur.kvh * G + qi % G;
+        const float4* src = reinterpret_cast<const float4*>(a.q + (static_cast<size_t>(row) * a.H + qh) * HD + qd0);
+#pragma unroll
+        for (int e = 0; e < QD / 4; ++e) {
+          const float4 v = __ldcg(src + e);
+          qv[4 * e] = v.x; qv[4 * e + 1] = v.y; qv[4 * e + 2] = v.z; qv[4 * e + 3] = v.w;
+        }
       }
-      return kcom_pool +
-             ((((static_cast<size_t>(it.seq) * a.n_slots + slot) * a.L + it.layer) * 2 + kv) * a.KVH + ur.kvh) * HD;
     };
-    for (int p = 0; p < n_pass; ++p) {
-      cp_async_wait_all();   // this pass's queries (copied while the previous pass ran)
-      team_sync();           // ... visible to all; every thread is done with the other buffer
-      if (sflag[1]) break;
-      // the next pass's queries into the other buffer, overlapping this pass
-      if (p + 1 < n_pass) issue_q(i, p + 1, buf ^ 1);
-      else if (i + 1 < n_my) issue_q(i + 1, 0, buf ^ 1);
-      const float* qbuf = sQ + buf * QB * HD;
-      const int q0 = p * QB;
-      const int nb = min(QB, nq - q0);
-      // this quad's queries: pass-local slots jb .. jb + QH - 1
-      const int jb = quad * QH;
-      int pos[QH], cend[QH], nrow[QH];
-      int cmin = 0x7fffffff, pmax = -1;
+    if (n_my > 0) load_q(0, 0);
+    bool aborted = false;
+    for (int i = 0; i < n_my && !aborted; ++i) {
+      const UnitRef ur = unit_ref(a, u0 + i);
+      const AttnItem it = a.items[ur.item];
+      const int g0 = ur.g * kAttnGroupPos;
+      const int nq = (it.row_end - it.row_begin) * G;
+      const int n_pass = (nq + kQT - 1) / kQT;
+      for (int p = 0; p < n_pass; ++p, ++np) {
+        const int q0 = p * kQT;
+        const int nb = min(kQT, nq - q0);
+        // (1) query tile: hi/lo fp16 in the MMA's K-major swizzled layout; bulk bounds
 #pragma unroll
-      for (int j = 0; j < QH; ++j) {
-        pos[j] = -1;
-        cend[j] = 0;
-        nrow[j] = it.row_begin;
-        if (jb + j < nb) {
-          nrow[j] = it.row_begin + (q0 + jb + j) / G;
-          pos[j] = __ldg(&a.nodes[nrow[j]].pos);
-          cend[j] = __ldg(&a.nodes[nrow[j]].c_end);
-          cmin = min(cmin, cend[j]);
-          pmax = max(pmax, pos[j]);
+        for (int e = 0; e < QD; e += 8) {
+          __align__(16) __half h8[8], l8[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) split_f16(qv[e + k], h8[k], l8[k]);
+          const uint32_t off = sw_elem_off(qj, qd0 + e, kQT);
+          *reinterpret_cast<uint4*>(qhi + off) = *reinterpret_cast<const uint4*>(h8);
+          *reinterpret_cast<uint4*>(qlo + off) = *reinterpret_cast<const uint4*>(l8);
         }
-      }
-      const bool quad_live = jb < nb;
-      const int kr = 32 * w + lane;             // this lane's key row within the group
-      const int k = g0 + kr;
-      float sc[QH];
-      if (quad_live && k < cmin && k <= pmax) {   // committed for every query of the quad
-        float2 s01[QH], s23[QH];
-#pragma unroll
-        for (int j = 0; j < QH; ++j) s01[j] = s23[j] = make_float2(0.0f, 0.0f);
-#pragma unroll 4
-        for (int c = 0; c < NCH; ++c) {
-          const uint4 kraw = *reinterpret_cast<const uint4*>(sk + tile_chunk_off(kr, c));
-#pragma unroll
-          for (int j = 0; j < QH; ++j)
-            if (jb + j < nb) dot8(s01[j], s23[j], qbuf + (jb + j) * HD + 8 * c, kraw);
+        if (et < kQT) {
+          int bnd = 0;
+          if (et < nb) {
+            const int row = it.row_begin + (q0 + et) / G;
+            const int pos = __ldg(&a.nodes[row].pos), cend = __ldg(&a.nodes[row].c_end);
+            bnd = bulk_end(pos);
+            if (bnd > cend) atomicExch(a.err, DEV_BAD_INDEX);   // a branch key would be in the bulk
+          }
+          meta[et] = bnd;
         }
+        fence_proxy_async_smem();
+        mbar_arrive(q_full);
+        // the next pass's queries, while this one runs
+        if (p + 1 < n_pass) load_q(i, p + 1);
+        else if (i + 1 < n_my) load_q(i + 1, 0);
+        // (2) scores -> masked exp2 -> probability tile; group max and sum per query
+        if (!mbar_wait(s_full, np & 1u, a.err, DEV_TIMEOUT_ACC)) sflag[1] = 1;
+        epi_sync();   // meta visible; abort visible
+        if (sflag[1]) { aborted = true; break; }
+        tc_fence_after();
+        float s[kQT];
+        tmem_ld16(tmem_base + t_row, s);
+        const int key = g0 + r;
+        float* rmax = red;
+        float* rsum = red + 4 * kQT;
 #pragma unroll
-        for (int j = 0; j < QH; ++j)
-          sc[j] = (jb + j < nb && k <= pos[j]) ? dot_finish(s01[j], s23[j]) * a.scale_log2 : -INFINITY;
-      } else {
+        for (int j = 0; j < kQT; ++j) {
+          s[j] = (j < nb && key < meta[j]) ? s[j] * a.scale_log2 : -INFINITY;
+          const float m = warp_max(s[j]);
+          if (lane == 0) rmax[lq * kQT + j] = m;
+        }
+        epi_sync();
+        float gm[kQT];
 #pragma unroll
-        for (int j = 0; j < QH; ++j) {
-          sc[j] = -INFINITY;
-          if (jb + j < nb && k <= pos[j]) {
-            float2 s01 = make_float2(0.0f, 0.0f), s23 = make_float2(0.0f, 0.0f);
-            if (k < cend[j]) {
-              for (int c = 0; c < NCH; ++c)
-                dot8(s01, s23, qbuf + (jb + j) * HD + 8 * c, *reinterpret_cast<const uint4*>(sk + tile_chunk_off(kr, c)));
-            } else {
-              const uint4* prow = reinterpret_cast<const uint4*>(pool_row(nrow[j], k, 0));
-              for (int c = 0; c < NCH; ++c) dot8(s01, s23, qbuf + (jb + j) * HD + 8 * c, __ldg(prow + c));
-            }
-            sc[j] = dot_finish(s01, s23) * a.scale_log2;
+        for (int j = 0; j < kQT; ++j) {
+          gm[j] = fmaxf(fmaxf(rmax[0 * kQT + j], rmax[1 * kQT + j]), fmaxf(rmax[2 * kQT + j], rmax[3 * kQT + j]));
+          const float pj = (s[j] == -INFINITY) ? 0.0f : exp2f(s[j] - gm[j]);
+          __half h, l;
+          split_f16(pj, h, l);
+          const uint32_t off = sw_elem_off(j, r, kQT);
+          *reinterpret_cast<__half*>(phi + off) = h;
+          *reinterpret_cast<__half*>(plo + off) = l;
+          const float ps = warp_sum(pj);
+          if (lane == 0) rsum[lq * kQT + j] = ps;
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(p_full);
+        // (3) group output -> partial records (O, m, l) of the pass's queries
+        if (!mbar_wait(o_full, np & 1u, a.err, DEV_TIMEOUT_ACC)) sflag[1] = 1;
+        epi_sync();   // sums visible; abort visible
+        if (sflag[1]) { aborted = true; break; }
+        tc_fence_after();
+        float o[kQT];
+        tmem_ld16(tmem_base + kQT + t_row, o);
+        tc_fence_before();
+        for (int j = 0; j < nb; ++j) {
+          const int qi = q0 + j;
+          const int row = it.row_begin + qi / G, qh = ur.kvh * G + qi % G;
+          float* pp = a.part + ((static_cast<size_t>(row) * a.H + qh) * a.max_groups + ur.g) * PS;
+          if (r < HD) __stcg(pp + r, o[j]);
+          if (r == HD - 1) {   // the sum in key-quarter order
+            __stcg(pp + HD, gm[j]);
+            __stcg(pp + HD + 1, __fadd_rn(__fadd_rn(rsum[0 * kQT + j], rsum[1 * kQT + j]),
+                                          __fadd_rn(rsum[2 * kQT + j], rsum[3 * kQT + j])));
           }
         }
+        epi_sync();   // red / meta / tiles free for the next pass
       }
-      // slice softmax statistics and the value accumulation, keys in order
-      float mx[QH], lsum[QH], pr[QH], acc[QH][DPL];
-#pragma unroll
-      for (int j = 0; j < QH; ++j) {
-        mx[j] = warp_max(sc[j]);
-        pr[j] = 0.0f;
-        lsum[j] = 0.0f;
-        if (mx[j] != -INFINITY) {
-          pr[j] = exp2f(sc[j] - mx[j]);
-          lsum[j] = warp_sum(pr[j]);
-        }
-#pragma unroll
-        for (int d = 0; d < DPL; ++d) acc[j][d] = 0.0f;
+      if (aborted) break;
+      // the unit that completes an (item, KV head) merges: the barrier orders the team's
+      // partial writes before one thread's gpu-scope release increment; the last arriver's
+      // acquire makes every unit's partials visible
+      if (et == 0) {
+        int prev;
+        asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;"
+                     : "=r"(prev)
+                     : "l"(a.counters + it.counter * a.KVH + ur.kvh)
+                     : "memory");
+        sflag[0] = (prev == it.n_groups - 1) ? 1 : 0;
       }
-      if (quad_live) {
-        const int ks = g0 + 32 * w;
-        const int n_keys = min(32, pmax - ks + 1);   // keys of the slice some query attends
-#pragma unroll 2
-        for (int u = 0; u < n_keys; ++u) {
-          const int key = ks + u;
-          if (key < cmin) {   // committed for every query: one row read
-            float vv[DPL];
-            value_dims_tile<HD>(sv, 32 * w + u, lane, vv);
+      epi_sync();
+      if (sflag[0]) {
+        const int ew = warp - 2;
+        for (int qi = ew; qi < nq; qi += 4) {
+          const int row = it.row_begin + qi / G, qh = ur.kvh * G + qi % G;
+          const DevNode nd = a.nodes[row];
+          const int bnd = bulk_end(nd.pos);
+          // window keys [bnd, pos] on CUDA cores: lane owns dims lane*DPL .. +DPL-1
+          float qw[DPL];
+          const float* qsrc = a.q + (static_cast<size_t>(row) * a.H + qh) * HD + lane * DPL;
 #pragma unroll
-            for (int j = 0; j < QH; ++j) {
-              if (jb + j < nb && key <= pos[j]) axpy_dims<DPL>(acc[j], __shfl_sync(0xffffffffu, pr[j], u), vv);
+          for (int d = 0; d < DPL; ++d) qw[d] = __ldcg(qsrc + d);
+          const int nw = nd.pos - bnd + 1;   // 1 .. kAttnWindow
+          float sw[kAttnWindow];
+          const __half* rows[kAttnWindow];
+#pragma unroll
+          for (int t = 0; t < kAttnWindow; ++t) {
+            sw[t] = -INFINITY;
+            rows[t] = nullptr;
+            if (t < nw) {
+              const int kk = bnd + t;
+              if (kk < nd.c_end) {
+                rows[t] = a.kv_commit +
+                          ((((static_cast<size_t>(it.seq) * a.L + it.layer) * 2) * a.KVH + ur.kvh) * a.max_ctx + kk) * HD;
+              } else {
+                const int tt = kk - nd.c_end;
+                int slot = 0;
+                if (tt < nd.n_tail) slot = a.tails[nd.tail_off + tt];
+                else atomicExch(a.err, DEV_BAD_INDEX);
+                rows[t] = a.kv_pool +
+                          ((((static_cast<size_t>(it.seq) * a.n_slots + slot) * a.L + it.layer) * 2) * a.KVH + ur.kvh) * HD;
+              }
+              float kv[DPL];
+              const __half* kr = rows[t] + lane * DPL;
+#pragma unroll
+              for (int d = 0; d < DPL; d += 2) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(kr + d));
+                kv[d] = f.x;
+                kv[d + 1] = f.y;
+              }
+              float dp = 0.0f;
+#pragma unroll
+              for (int d = 0; d < DPL; ++d) dp = fmaf(qw[d], kv[d], dp);
+              sw[t] = warp_sum(dp) * a.scale_log2;
             }
-          } else {
+          }
+          float mw = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < QH; ++j) {
-              if (jb + j < nb && key <= pos[j]) {
-                float vv[DPL];
-                if (key < cend[j]) value_dims_tile<HD>(sv, 32 * w + u, lane, vv);
-                else value_dims_row<HD>(pool_row(nrow[j], key, 1), lane, vv);
-                axpy_dims<DPL>(acc[j], __shfl_sync(0xffffffffu, pr[j], u), vv);
+          for (int t = 0; t < kAttnWindow; ++t) mw = fmaxf(mw, sw[t]);
+          float lw = 0.0f, ow[DPL];
+#pragma unroll
+          for (int d = 0; d < DPL; ++d) ow[d] = 0.0f;
+          const size_t voff = static_cast<size_t>(a.KVH) * a.max_ctx * HD;   // V rows of the cache
+          const size_t voff_pool = static_cast<size_t>(a.KVH) * HD;          // V rows of the pool
+#pragma unroll
+          for (int t = 0; t < kAttnWindow; ++t) {
+            if (t < nw) {
+              const float pt = exp2f(sw[t] - mw);
+              lw = __fadd_rn(lw, pt);
+              const int kk = bnd + t;
+              const __half* vr = rows[t] + (kk < nd.c_end ? voff : voff_pool) + lane * DPL;
+#pragma unroll
+              for (int d = 0; d < DPL; d += 2) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(vr + d));
+                ow[d] = fmaf(pt, f.x, ow[d]);
+                ow[d + 1] = fmaf(pt, f.y, ow[d + 1]);
               }
             }
           }
-        }
-      }
-      // the stage is free once the last pass has read its values
-      if (p == n_pass - 1) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
-      }
-      // slice records of the quad's queries, then the in-order combination of the slices
+          // bulk groups in group order, then the window
+          const float* base = a.part + (static_cast<size_t>(row) * a.H + qh) * a.max_groups * PS;
+          float mg[2] = {-INFINITY, -INFINITY}, lg[2] = {0.0f, 0.0f};
 #pragma unroll
-      for (int j = 0; j < QH; ++j) {
-        if (jb + j < nb) {
-          float* rec = sRec + ((jb + j) * kSlices + w) * PS;
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int gg = lane + 32 * h2;
+            if (gg < it.n_groups) {
+              mg[h2] = __ldcg(base + gg * PS + HD);
+              lg[h2] = __ldcg(base + gg * PS + HD + 1);
+            }
+          }
+          const float M = fmaxf(warp_max(fmaxf(mg[0], mg[1])), mw);
+          float wg[2];
 #pragma unroll
-          for (int d = 0; d < DPL; ++d) rec[lane * DPL + d] = acc[j][d];
-          if (lane == 0) {
-            rec[HD] = mx[j];
-            rec[HD + 1] = lsum[j];
+          for (int h2 = 0; h2 < 2; ++h2) wg[h2] = (lg[h2] > 0.0f) ? exp2f(mg[h2] - M) : 0.0f;
+          const float ww = exp2f(mw - M);
+          const float L = __fadd_rn(warp_sum(__fadd_rn(lg[0] * wg[0], lg[1] * wg[1])), lw * ww);
+          float O[DPL];
+#pragma unroll
+          for (int d = 0; d < DPL; ++d) O[d] = 0.0f;
+          for (int g4 = 0; g4 < it.n_groups; g4 += 4) {   // four groups' loads ahead of their FMAs
+            float pv[4][DPL], wv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int gg = g4 + e;
+              wv[e] = __shfl_sync(0xffffffffu, gg < 32 ? wg[0] : wg[1], gg & 31);
+              if (gg >= it.n_groups) wv[e] = 0.0f;
+#pragma unroll
+              for (int d = 0; d < DPL; ++d) pv[e][d] = wv[e] != 0.0f ? __ldcg(base + gg * PS + lane * DPL + d) : 0.0f;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              if (wv[e] == 0.0f) continue;
+#pragma unroll
+              for (int d = 0; d < DPL; ++d) O[d] = fmaf(wv[e], pv[e][d], O[d]);
+            }
+          }
+          const float invl = 1.0f / L;
+          const size_t lo = static_cast<size_t>(a.plane_rows) * a.H * HD;
+#pragma unroll
+          for (int d = 0; d < DPL; ++d) {
+            const float v = fmaf(ww, ow[d], O[d]) * invl;
+            const size_t oo = static_cast<size_t>(row) * a.H * HD + qh * HD + lane * DPL + d;
+            store_pair(a.out + oo, a.out + lo + oo, v);
           }
         }
+        if (et == 0) a.counters[it.counter * a.KVH + ur.kvh] = 0;
       }
-      quad_sync();
-      for (int j = jb + w; j < min(nb, jb + QH); j += kSlices) {
-        const int qi = q0 + j;
-        const int row = it.row_begin + qi / G, qh = ur.kvh * G + qi % G;
-        const float* r0 = sRec + (j * kSlices) * PS;
-        float mw[kSlices], wgt[kSlices];
-        float M = -INFINITY;
-#pragma unroll
-        for (int s2 = 0; s2 < kSlices; ++s2) {
-          mw[s2] = r0[s2 * PS + HD];
-          M = fmaxf(M, mw[s2]);
-        }
-#pragma unroll
-        for (int s2 = 0; s2 < kSlices; ++s2) wgt[s2] = (mw[s2] == -INFINITY) ? 0.0f : exp2f(mw[s2] - M);
-        const float Lg = __fadd_rn(__fadd_rn(r0[0 * PS + HD + 1] * wgt[0], r0[1 * PS + HD + 1] * wgt[1]),
-                                   __fadd_rn(r0[2 * PS + HD + 1] * wgt[2], r0[3 * PS + HD + 1] * wgt[3]));
-        float* pp = a.part + ((static_cast<size_t>(row) * a.H + qh) * a.max_groups + ur.g) * PS;
-#pragma unroll
-        for (int d2 = 0; d2 < DPL; ++d2) {
-          const int d = lane * DPL + d2;
-          const float v = __fadd_rn(__fadd_rn(r0[0 * PS + d] * wgt[0], r0[1 * PS + d] * wgt[1]),
-                                    __fadd_rn(r0[2 * PS + d] * wgt[2], r0[3 * PS + d] * wgt[3]));
-          __stcg(pp + d, v);
-        }
-        if (lane == 0) {
-          __stcg(pp + HD, M);
-          __stcg(pp + HD + 1, Lg);
-        }
-      }
-      quad_sync();   // records consumed before the next pass writes them
-      buf ^= 1;
-    }
-    if (sflag[1]) break;
-    // the unit that completes an (item, KV head) merges its groups in group order: the
-    // barrier orders the team's partial writes before one thread's gpu-scope release
-    // increment; the last arriver's acquire makes every unit's partials visible
-    team_sync();
-    if (tt == 0) {
-      int prev;
-      asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;"
-                   : "=r"(prev)
-                   : "l"(a.counters + it.counter * a.KVH + ur.kvh)
-                   : "memory");
-      sflag[0] = (prev == it.n_groups - 1) ? 1 : 0;
-    }
-    team_sync();
-    if (sflag[0]) {
-      for (int qi = cw; qi < nq; qi += kTeamWarps) {
-        const int row = it.row_begin + qi / G, qh = ur.kvh * G + qi % G;
-        const float* base = a.part + (static_cast<size_t>(row) * a.H + qh) * a.max_groups * PS;
-        float mg[2] = {-INFINITY, -INFINITY}, lg[2] = {0.0f, 0.0f};
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const int gg = lane + 32 * h2;
-          if (gg < it.n_groups) {
-            mg[h2] = __ldcg(base + gg * PS + HD);
-            lg[h2] = __ldcg(base + gg * PS + HD + 1);
-          }
-        }
-        const float M = warp_max(fmaxf(mg[0], mg[1]));
-        float wg[2];
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) wg[h2] = (lg[h2] > 0.0f) ? exp2f(mg[h2] - M) : 0.0f;
-        const float Lsum = warp_sum(__fadd_rn(lg[0] * wg[0], lg[1] * wg[1]));
-        float O[DPL];
-#pragma unroll
-        for (int d = 0; d < DPL; ++d) O[d] = 0.0f;
-        // groups in order; the loads of four groups are issued before their FMAs
-        for (int g4 = 0; g4 < it.n_groups; g4 += 4) {
-          float pv[4][DPL], wv[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int gg = g4 + e;
-            wv[e] = __shfl_sync(0xffffffffu, gg < 32 ? wg[0] : wg[1], gg & 31);
-            if (gg >= it.n_groups) wv[e] = 0.0f;
-#pragma unroll
-            for (int d = 0; d < DPL; ++d) pv[e][d] = wv[e] != 0.0f ? __ldcg(base + gg * PS + lane * DPL + d) : 0.0f;
-          }
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            if (wv[e] == 0.0f) continue;
-#pragma unroll
-            for (int d = 0; d < DPL; ++d) O[d] = fmaf(wv[e], pv[e][d], O[d]);
-          }
-        }
-        const float invl = 1.0f / Lsum;
-        const size_t lo = static_cast<size_t>(a.plane_rows) * a.H * HD;
-#pragma unroll
-        for (int d = 0; d < DPL; ++d) {
-          const size_t o = static_cast<size_t>(row) * a.H * HD + qh * HD + lane * DPL + d;
-          store_pair(a.out + o, a.out + lo + o, O[d] * invl);
-        }
-      }
-      if (tt == 0) a.counters[it.counter * a.KVH + ur.kvh] = 0;
+      epi_sync();   // sflag[0] consumed
     }
   }
-  cp_async_wait_all();   // no copy of a skipped pass outlives the CTA
-}
-
-template <int HD, int QB>
-static cudaError_t launch_attn_variant(cudaLaunchConfig_t cfg, const CUtensorMap& tm, const AttnArgs& a) {
-  static bool set = false;
-  cfg.dynamicSmemBytes = AttnSmem<HD, QB>::kTotal;
-  if (!set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<HD, QB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(cfg.dynamicSmemBytes));
-    if (e == cudaSuccess) e = apply_carveout(attn_kernel<HD, QB>);
-    if (e != cudaSuccess) return e;
-    set = true;
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 32);
   }
-  return cudaLaunchKernelEx(&cfg, attn_kernel<HD, QB>, tm, a);
 }
 
 template <int HD>
-static cudaError_t launch_attn_hd(const cudaLaunchConfig_t& cfg, const CUtensorMap& tm, const AttnArgs& a,
-                                  int max_nq) {
-  if (max_nq <= 1) return launch_attn_variant<HD, 1>(cfg, tm, a);
-  if (max_nq <= 2) return launch_attn_variant<HD, 2>(cfg, tm, a);
-  if (max_nq <= 4) return launch_attn_variant<HD, 4>(cfg, tm, a);
-  return launch_attn_variant<HD, 8>(cfg, tm, a);
+static cudaError_t launch_attn_hd(cudaLaunchConfig_t cfg, const CUtensorMap& tm, const AttnArgs& a) {
+  static bool set = false;
+  cfg.dynamicSmemBytes = AttnSmem<HD>::kTotal;
+  if (!set) {
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(cfg.dynamicSmemBytes));
+    if (e == cudaSuccess) e = apply_carveout(attn_kernel<HD>);
+    if (e != cudaSuccess) return e;
+    set = true;
+  }
+  return cudaLaunchKernelEx(&cfg, attn_kernel<HD>, tm, a);
 }
 
-size_t attention_smem_bytes(int hd, int max_nq) {
-  const int qb = max_nq <= 1 ? 1 : max_nq <= 2 ? 2 : max_nq <= 4 ? 4 : 8;
-  if (hd == 128)
-    return qb == 1 ? AttnSmem<128, 1>::kTotal : qb == 2 ? AttnSmem<128, 2>::kTotal
-                                                          : qb == 4 ? AttnSmem<128, 4>::kTotal : AttnSmem<128, 8>::kTotal;
-  return qb == 1 ? AttnSmem<64, 1>::kTotal : qb == 2 ? AttnSmem<64, 2>::kTotal
-                                                      : qb == 4 ? AttnSmem<64, 4>::kTotal : AttnSmem<64, 8>::kTotal;
-}
-
-cudaError_t launch_attention(const CUtensorMap& tm, const AttnArgs& a, int max_nq, int n_ctas, cudaStream_t st,
-                             bool pdl) {
+cudaError_t launch_attention(const CUtensorMap& tm, const AttnArgs& a, int n_ctas, cudaStream_t st, bool pdl) {
   if (a.n_items <= 0 || a.n_units <= 0) return cudaSuccess;
-  if (!a.nodes || !a.items || !a.tails || !a.q || !a.kv_pool || !a.out || !a.part || !a.counters || !a.err ||
-      a.plane_rows < 1 || a.max_groups < 1 || a.max_groups > kAttnMaxGroups || max_nq < 1 || n_ctas < 1 ||
+  if (!a.nodes || !a.items || !a.tails || !a.q || !a.kv_commit || !a.kv_pool || !a.out || !a.part || !a.counters ||
+      !a.err || a.plane_rows < 1 || a.max_groups < 1 || a.max_groups > kAttnMaxGroups || n_ctas < 1 ||
       (a.hd != 64 && a.hd != 128))
     return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
@@ -542,8 +546,8 @@ cudaError_t launch_attention(const CUtensorMap& tm, const AttnArgs& a, int max_n
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  if (a.hd == 128) return launch_attn_hd<128>(cfg, tm, a, max_nq);
-  return launch_attn_hd<64>(cfg, tm, a, max_nq);
+  if (a.hd == 128) return launch_attn_hd<128>(cfg, tm, a);
+  return launch_attn_hd<64>(cfg, tm, a);
 }
 
 }  // namespace dex

@@ -402,6 +402,7 @@ int run_layers(dex_handle* h, const Uploaded& u, const std::vector<Batch>& batch
     at.n_units = sl.n_units;
     at.tails = u.tails;
     at.q = h->q;
+    at.kv_commit = h->kv_commit;
     at.kv_pool = h->kv_pool;
     at.out = h->attn_out;
     at.part = h->attn_part;
@@ -422,7 +423,7 @@ int run_layers(dex_handle* h, const Uploaded& u, const std::vector<Batch>& batch
       ae1 = next_event(h);
       cudaEventRecord(ae0, h->st);
     }
-    cudaError_t ce = dex::launch_attention(h->tm_kv, at, sl.max_rows * (h->H / h->KVH), h->n_sm, h->st, true);
+    cudaError_t ce = dex::launch_attention(h->tm_kv, at, h->n_sm, h->st, true);
     if (ce != cudaSuccess) return cuda_fail(h, ce);
     if (h->timing == 2) {
       cudaEventRecord(ae1, h->st);
@@ -547,7 +548,7 @@ int run_round(dex_handle* h, dex::Lattice* lat, std::vector<dex_copy_job>* pendi
         ++e;
       }
       it.row_end = e;
-      it.n_groups = it.max_pos / dex::kAttnGroupPos + 1;
+      it.n_groups = std::max(1, (dex::attn_bulk_end(it.max_pos) + dex::kAttnGroupPos - 1) / dex::kAttnGroupPos);
       b.items.push_back(it);
       k = e;
     }
@@ -805,6 +806,7 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
       m->n_heads % m->n_kv_heads || (m->n_heads * m->head_dim) % 128 || (m->n_kv_heads * m->head_dim) % 128 ||
       m->d_ff < 64 || m->d_ff % 8 || m->vocab < 2 || !m->embed || !m->final_norm || !m->lm_head || !m->layers)
     return DEX_EINVAL;
+  static_assert(dex::kAttnWindow > 10, "the attention window must cover every node's branch keys (|X| <= 10)");
   if (n_X < 1 || n_X > 10 || X[n_X - 1] != m->n_layers) return DEX_EINVAL;
   for (int i = 0; i < n_X; ++i)
     if (X[i] < 1 || (i > 0 && X[i] <= X[i - 1])) return DEX_EINVAL;
@@ -1103,7 +1105,7 @@ int dex_prefill(dex_handle* h, int32_t seq, const int32_t* tokens, int32_t n_tok
     it.row_end = n;
     it.max_pos = c0 + n - 1;
     it.max_cend = c0 + n;
-    it.n_groups = it.max_pos / dex::kAttnGroupPos + 1;
+    it.n_groups = std::max(1, (dex::attn_bulk_end(it.max_pos) + dex::kAttnGroupPos - 1) / dex::kAttnGroupPos);
     batches[0].items.push_back(it);
     const std::vector<Slot> slots = build_slots(batches, h->KVH, &t);
     Uploaded u;

@@ -39,13 +39,18 @@ static_assert(sizeof(DevNode) == 64, "DevNode is 64 bytes");
 // Key positions per attention CTA (four 32-key warp slices); groups are aligned to position 0.
 constexpr int kAttnGroupPos = 128;
 constexpr int kAttnMaxGroups = 32;   // max_ctx <= 4096
-constexpr int kAttnPassQueries = 8;  // queries of one attention pass (the largest query batch)
+constexpr int kAttnPassQueries = 16; // queries of one attention pass (the MMA's N)
+// A query at position p takes keys [max(0, p - kAttnWindow + 1), p] on CUDA cores and the
+// older ones on the tensor cores; the window exceeds every node's branch depth (|X| <= 10),
+// so the tensor-core keys are always committed ones.
+constexpr int kAttnWindow = 16;
+inline int attn_bulk_end(int pos) { return pos - kAttnWindow + 1 > 0 ? pos - kAttnWindow + 1 : 0; }
 
 // Attention work item: one sequence's contiguous node rows within a stage batch.
 struct AttnItem {
   int32_t seq, row_begin, row_end;   // absolute node rows
   int32_t max_pos, max_cend;         // largest input position / committed extent among the rows
-  int32_t n_groups;                  // kAttnGroupPos-position key groups covering 0..max_pos
+  int32_t n_groups;                  // kAttnGroupPos-position key groups covering the bulk keys (>= 1)
   int32_t counter;                   // index of this item's merge counters (x KVH)
   int32_t layer;                     // decoder layer of this item (items of several stages share a launch)
   int32_t unit0;                     // first (item, KV head, group) unit of the item in its launch
@@ -133,6 +138,7 @@ struct AttnArgs {
   int32_t n_items, n_units;    // items of the launch; units = sum over items of KVH x n_groups
   const int32_t* tails;
   const float* q;              // [rows][H*hd]
+  const __half* kv_commit;     // fp16 committed cache (window keys; layout as in GemmArgs)
   const __half* kv_pool;       // fp16 pool (layout as in GemmArgs)
   __nv_bfloat16* out;          // [2][plane_rows][H*hd] hi/lo pair
   int32_t plane_rows;
@@ -199,11 +205,9 @@ inline cudaError_t apply_carveout(F* func) {
   return cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, c);
 }
 
-// Persistent launch over min(n_units, n_ctas) CTAs (one per SM); max_nq picks the query
-// batch of a pass (1, 2, 4 or 8; items with more queries take several passes).
-cudaError_t launch_attention(const CUtensorMap& tm_kv, const AttnArgs& a, int max_nq, int n_ctas, cudaStream_t st,
-                             bool pdl);
-size_t attention_smem_bytes(int hd, int max_nq);
+// Persistent launch over min(n_units, n_ctas) CTAs (one per SM); items with more than
+// kAttnPassQueries queries take several passes.
+cudaError_t launch_attention(const CUtensorMap& tm_kv, const AttnArgs& a, int n_ctas, cudaStream_t st, bool pdl);
 cudaError_t launch_assemble(const AssembleArgs& a, cudaStream_t st, bool pdl);
 cudaError_t launch_collapse(const CollapseArgs& a, cudaStream_t st, bool pdl);
 // bf16 [n][d] rows -> hi/lo pair of h * g ([2][plane_rows][d]) and partial sums of squares
