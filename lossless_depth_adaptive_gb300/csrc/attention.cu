@@ -28,8 +28,12 @@
 // CTAs (one per SM) take contiguous ranges of units.  Warp 0 streams the committed K and V
 // tiles of each unit through a ring of shared-memory stages with TMA (128-byte swizzle,
 // 32-row boxes); warp 1 owns TMEM and issues the MMAs; warps 2-5 build the query tiles,
-// run the softmax between the two MMAs and write the group partials.
+// run the softmax between the two MMAs and write the group partials; warps 6-9 take the
+// final combinations (window keys + group merge) of completed (item, KV head)s off the
+// critical path.
 #include <cuda_fp16.h>
+
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -37,9 +41,10 @@
 namespace dex {
 
 constexpr int kQT = kAttnPassQueries;                 // queries per pass (MMA N)
-constexpr int kAttnThreads = 192;                     // producer, MMA, four epilogue warps
+constexpr int kAttnThreads = 320;                     // producer, MMA, four epilogue, four merge warps
 constexpr int kBoxRows = 32;                          // TMA box height
-constexpr int kEpiBar = 1;                            // named barrier of the epilogue warps
+constexpr int kEpiBar = 1, kMergeBar = 2;             // named barriers of the epilogue / merge warps
+constexpr int kMergeSlots = 4;                        // merge requests in flight
 static_assert(kAttnGroupPos == 128 && kQT == 16, "128-key groups, 16-query MMA columns");
 
 // Shared-memory plan: K/V ring, query and probability tiles (hi, lo), a zero atom that pads
@@ -58,7 +63,7 @@ struct AttnSmem {
   static constexpr uint32_t oRed = oZero + kZero;                  // float [2][4][16] max / sum
   static constexpr uint32_t oMeta = oRed + 2 * 4 * kQT * 4;        // int [16] bulk bounds
   static constexpr uint32_t oBar = oMeta + kQT * 4 + 16;
-  static constexpr uint32_t kTotal = oBar + (2 * kStages + 4) * 8 + 16 + 1024;   // + alignment slack
+  static constexpr uint32_t kTotal = oBar + (2 * kStages + 4 + 2 * 4) * 8 + 4 * 8 + 16 + 1024;   // + alignment slack
 };
 
 // MN-major operand descriptor, 128-byte swizzle: 64 contiguous 16-bit elements of M (or N)
@@ -113,6 +118,137 @@ __device__ __forceinline__ UnitRef unit_ref(const AttnArgs& a, int u) {
 }
 __device__ __forceinline__ int bulk_end(int pos) { return max(0, pos - kAttnWindow + 1); }
 
+// Final combination of one query of an (item, KV head): its window keys on CUDA cores,
+// then the bulk groups' partials in group order, then the window part; the output is
+// written as a hi/lo bf16 pair.  One warp per query; every global load of the query is
+// issued before the arithmetic that needs it.
+template <int HD>
+__device__ __forceinline__ void merge_query(const AttnArgs& a, const AttnItem& it, int kvh, int qi, int lane) {
+  constexpr int DPL = HD / 32;                   // dims per lane
+  constexpr int PS = HD + 2;
+  using Raw = typename std::conditional<HD == 128, uint2, uint32_t>::type;   // DPL fp16 values
+  const int G = a.H / a.KVH;
+  const int row = it.row_begin + qi / G, qh = kvh * G + qi % G;
+  const DevNode* nd = a.nodes + row;
+  const int pos = __ldg(&nd->pos), cend = __ldg(&nd->c_end);
+  const int toff = __ldg(&nd->tail_off), ntail = __ldg(&nd->n_tail);
+  const int bnd = bulk_end(pos);
+  const int nw = pos - bnd + 1;                  // window keys, 1 .. kAttnWindow
+  // lane t resolves window key bnd + t: committed cache row, or the branch pool row
+  const __half* krow = a.kv_commit;
+  const __half* vrow = a.kv_commit;
+  if (lane < nw) {
+    const int kk = bnd + lane;
+    if (kk < cend) {
+      krow = a.kv_commit + ((((static_cast<size_t>(it.seq) * a.L + it.layer) * 2) * a.KVH + kvh) * a.max_ctx + kk) * HD;
+      vrow = krow + static_cast<size_t>(a.KVH) * a.max_ctx * HD;
+    } else {
+      const int t = kk - cend;
+      int slot = 0;
+      if (t < ntail) slot = __ldg(a.tails + toff + t);
+      else atomicExch(a.err, DEV_BAD_INDEX);   // cannot happen for a well-formed plan; slot 0 is read
+      krow = a.kv_pool + ((((static_cast<size_t>(it.seq) * a.n_slots + slot) * a.L + it.layer) * 2) * a.KVH + kvh) * HD;
+      vrow = krow + static_cast<size_t>(a.KVH) * HD;
+    }
+  }
+  float qw[DPL];
+  const float* qsrc = a.q + (static_cast<size_t>(row) * a.H + qh) * HD + lane * DPL;
+#pragma unroll
+  for (int d = 0; d < DPL; ++d) qw[d] = __ldcg(qsrc + d);
+  Raw kr[kAttnWindow], vr[kAttnWindow];
+#pragma unroll
+  for (int t = 0; t < kAttnWindow; ++t) {
+    const __half* kp = reinterpret_cast<const __half*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(krow), t));
+    const __half* vp = reinterpret_cast<const __half*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(vrow), t));
+    if (t < nw) {
+      kr[t] = *reinterpret_cast<const Raw*>(kp + lane * DPL);
+      vr[t] = *reinterpret_cast<const Raw*>(vp + lane * DPL);
+    }
+  }
+  // the bulk groups' statistics (lane gg holds groups gg and gg + 32)
+  const float* base = a.part + (static_cast<size_t>(row) * a.H + qh) * a.max_groups * PS;
+  float mg[2] = {-INFINITY, -INFINITY}, lg[2] = {0.0f, 0.0f};
+#pragma unroll
+  for (int h2 = 0; h2 < 2; ++h2) {
+    const int gg = lane + 32 * h2;
+    if (gg < it.n_groups) {
+      mg[h2] = __ldcg(base + gg * PS + HD);
+      lg[h2] = __ldcg(base + gg * PS + HD + 1);
+    }
+  }
+  // window scores: per key the lane's products in dim order, then the warp butterfly
+  float sw[kAttnWindow];
+  float mw = -INFINITY;
+#pragma unroll
+  for (int t = 0; t < kAttnWindow; ++t) {
+    sw[t] = -INFINITY;
+    if (t < nw) {
+      const __half2* h2p = reinterpret_cast<const __half2*>(&kr[t]);
+      float dp = 0.0f;
+#pragma unroll
+      for (int d = 0; d < DPL; d += 2) {
+        const float2 f = __half22float2(h2p[d / 2]);
+        dp = fmaf(qw[d], f.x, dp);
+        dp = fmaf(qw[d + 1], f.y, dp);
+      }
+      sw[t] = warp_sum(dp) * a.scale_log2;
+      mw = fmaxf(mw, sw[t]);
+    }
+  }
+  float lw = 0.0f, ow[DPL];
+#pragma unroll
+  for (int d = 0; d < DPL; ++d) ow[d] = 0.0f;
+#pragma unroll
+  for (int t = 0; t < kAttnWindow; ++t) {
+    if (t < nw) {
+      const float pt = exp2f(sw[t] - mw);
+      lw = __fadd_rn(lw, pt);
+      const __half2* h2p = reinterpret_cast<const __half2*>(&vr[t]);
+#pragma unroll
+      for (int d = 0; d < DPL; d += 2) {
+        const float2 f = __half22float2(h2p[d / 2]);
+        ow[d] = fmaf(pt, f.x, ow[d]);
+        ow[d + 1] = fmaf(pt, f.y, ow[d + 1]);
+      }
+    }
+  }
+  // bulk groups in group order, then the window
+  const float M = fmaxf(warp_max(fmaxf(mg[0], mg[1])), mw);
+  float wg[2];
+#pragma unroll
+  for (int h2 = 0; h2 < 2; ++h2) wg[h2] = (lg[h2] > 0.0f) ? exp2f(mg[h2] - M) : 0.0f;
+  const float ww = exp2f(mw - M);
+  const float L = __fadd_rn(warp_sum(__fadd_rn(lg[0] * wg[0], lg[1] * wg[1])), lw * ww);
+  float O[DPL];
+#pragma unroll
+  for (int d = 0; d < DPL; ++d) O[d] = 0.0f;
+  for (int g8 = 0; g8 < it.n_groups; g8 += 8) {   // eight groups' loads ahead of their FMAs
+    float pv[8][DPL], wv[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int gg = g8 + e;
+      wv[e] = __shfl_sync(0xffffffffu, gg < 32 ? wg[0] : wg[1], gg & 31);
+      if (gg >= it.n_groups) wv[e] = 0.0f;
+#pragma unroll
+      for (int d = 0; d < DPL; ++d) pv[e][d] = wv[e] != 0.0f ? __ldcg(base + gg * PS + lane * DPL + d) : 0.0f;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      if (wv[e] == 0.0f) continue;
+#pragma unroll
+      for (int d = 0; d < DPL; ++d) O[d] = fmaf(wv[e], pv[e][d], O[d]);
+    }
+  }
+  const float invl = 1.0f / L;
+  const size_t lo = static_cast<size_t>(a.plane_rows) * a.H * HD;
+#pragma unroll
+  for (int d = 0; d < DPL; ++d) {
+    const float v = fmaf(ww, ow[d], O[d]) * invl;
+    const size_t oo = static_cast<size_t>(row) * a.H * HD + qh * HD + lane * DPL + d;
+    store_pair(a.out + oo, a.out + lo + oo, v);
+  }
+}
+
 template <int HD>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tmKV, const __grid_constant__ AttnArgs a) {
@@ -121,7 +257,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   constexpr int KSTEPS = HD / 16;                // QK k-steps (dims)
   constexpr int PSTEPS = kAttnGroupPos / 16;     // PV k-steps (keys)
   constexpr int PS = HD + 2;                     // partial record: O[HD], m, l
-  constexpr int DPL = HD / 32;                   // window dims per lane
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
@@ -133,8 +268,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* s_full = q_full + 1;  // scores in TMEM (MMA -> epilogue)
   uint64_t* p_full = s_full + 1;  // probability tile written (epilogue -> MMA)
   uint64_t* o_full = p_full + 1;  // group output in TMEM (MMA -> epilogue)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_full + 1);
-  volatile int* sflag = reinterpret_cast<volatile int*>(tmem_slot + 1);   // [0] last arriver, [1] abort
+  uint64_t* m_full = o_full + 1;  // [kMergeSlots] merge request posted (epilogue -> merge warps)
+  uint64_t* m_empty = m_full + kMergeSlots;   // [kMergeSlots] merge request done
+  int* mreq = reinterpret_cast<int*>(m_empty + kMergeSlots);   // [kMergeSlots][2] item, KV head
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mreq + 2 * kMergeSlots);
+  volatile int* sflag = reinterpret_cast<volatile int*>(tmem_slot + 1);   // [1] abort
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int C = gridDim.x, cta = blockIdx.x;
@@ -151,7 +289,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     mbar_init(s_full, 1);
     mbar_init(p_full, 128);
     mbar_init(o_full, 1);
-    sflag[0] = 0;
+    for (int k = 0; k < kMergeSlots; ++k) {
+      mbar_init(&m_full[k], 1);
+      mbar_init(&m_empty[k], 1);
+    }
     sflag[1] = 0;
     fence_mbar_init();
     tma_prefetch(&tmKV);
@@ -254,8 +395,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
       }
     }
-  } else {
-    // ---------------- epilogue: query tiles, softmax, partials, merge ----------------
+  } else if (warp < 6) {
+    // ---------------- epilogue: query tiles, softmax, partials ----------------
     const int et = tid - 64;                   // 0..127
     const int lq = warp & 3;                   // TMEM lane quarter of this warp
     const int r = lq * 32 + lane;              // TMEM row: key (scores) or value dim (output)
@@ -268,8 +409,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     constexpr int QD = HD / 8;                 // query dims per thread (8 threads per query)
     const int qj = et >> 3, qd0 = (et & 7) * QD;
     uint32_t np = 0;
-    // this thread's slice of pass (i, p)'s queries, fp32 (prefetched one pass ahead)
+    int n_req = 0;                             // merge requests posted
+    // posts one merge request (item, KV head), or the end marker (item -1); et == 0 only
+    auto post = [&](int item, int kvh) {
+      const int k = n_req % kMergeSlots;
+      if (n_req >= kMergeSlots)
+        mbar_wait(&m_empty[k], static_cast<uint32_t>((n_req / kMergeSlots) - 1) & 1u, a.err, DEV_TIMEOUT_EMPTY);
+      mreq[2 * k] = item;
+      mreq[2 * k + 1] = kvh;
+      mbar_arrive(&m_full[k]);
+      ++n_req;
+    };
+    // this thread's slice of pass (i, p)'s queries (fp32) and, for et < 16, the query's
+    // position and committed extent -- loaded one pass ahead
     float qv[QD];
+    int qpos = -1, qcend = 0;
     auto load_q = [&](int i, int p) {
       const UnitRef ur = unit_ref(a, u0 + i);
       const AttnItem it = a.items[ur.item];
@@ -285,6 +439,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           const float4 v = __ldcg(src + e);
           qv[4 * e] = v.x; qv[4 * e + 1] = v.y; qv[4 * e + 2] = v.z; qv[4 * e + 3] = v.w;
         }
+      }
+      qpos = -1;
+      qcend = 0;
+      const int mi = p * kQT + et;
+      if (et < kQT && mi < nq) {
+        const int row = it.row_begin + mi / G;
+        qpos = __ldg(&a.nodes[row].pos);
+        qcend = __ldg(&a.nodes[row].c_end);
       }
     };
     if (n_my > 0) load_q(0, 0);
@@ -309,13 +471,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           *reinterpret_cast<uint4*>(qlo + off) = *reinterpret_cast<const uint4*>(l8);
         }
         if (et < kQT) {
-          int bnd = 0;
-          if (et < nb) {
-            const int row = it.row_begin + (q0 + et) / G;
-            const int pos = __ldg(&a.nodes[row].pos), cend = __ldg(&a.nodes[row].c_end);
-            bnd = bulk_end(pos);
-            if (bnd > cend) atomicExch(a.err, DEV_BAD_INDEX);   // a branch key would be in the bulk
-          }
+          const int bnd = qpos >= 0 ? bulk_end(qpos) : 0;
+          if (bnd > qcend) atomicExch(a.err, DEV_BAD_INDEX);   // a branch key would be in the bulk
           meta[et] = bnd;
         }
         fence_proxy_async_smem();
@@ -375,138 +532,38 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                           __fadd_rn(rsum[2 * kQT + j], rsum[3 * kQT + j])));
           }
         }
-        epi_sync();   // red / meta / tiles free for the next pass
+        epi_sync();   // partial writes done; red / meta / tiles free for the next pass
       }
       if (aborted) break;
-      // the unit that completes an (item, KV head) merges: the barrier orders the team's
-      // partial writes before one thread's gpu-scope release increment; the last arriver's
-      // acquire makes every unit's partials visible
+      // the unit that completes an (item, KV head) hands its merge to the merge warps: the
+      // barrier above orders the team's partial writes before this thread's gpu-scope
+      // release increment; the merge warps start after the acquire that saw the last count
       if (et == 0) {
         int prev;
         asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;"
                      : "=r"(prev)
                      : "l"(a.counters + it.counter * a.KVH + ur.kvh)
                      : "memory");
-        sflag[0] = (prev == it.n_groups - 1) ? 1 : 0;
-      }
-      epi_sync();
-      if (sflag[0]) {
-        const int ew = warp - 2;
-        for (int qi = ew; qi < nq; qi += 4) {
-          const int row = it.row_begin + qi / G, qh = ur.kvh * G + qi % G;
-          const DevNode nd = a.nodes[row];
-          const int bnd = bulk_end(nd.pos);
-          // window keys [bnd, pos] on CUDA cores: lane owns dims lane*DPL .. +DPL-1
-          float qw[DPL];
-          const float* qsrc = a.q + (static_cast<size_t>(row) * a.H + qh) * HD + lane * DPL;
-#pragma unroll
-          for (int d = 0; d < DPL; ++d) qw[d] = __ldcg(qsrc + d);
-          const int nw = nd.pos - bnd + 1;   // 1 .. kAttnWindow
-          float sw[kAttnWindow];
-          const __half* rows[kAttnWindow];
-#pragma unroll
-          for (int t = 0; t < kAttnWindow; ++t) {
-            sw[t] = -INFINITY;
-            rows[t] = nullptr;
-            if (t < nw) {
-              const int kk = bnd + t;
-              if (kk < nd.c_end) {
-                rows[t] = a.kv_commit +
-                          ((((static_cast<size_t>(it.seq) * a.L + it.layer) * 2) * a.KVH + ur.kvh) * a.max_ctx + kk) * HD;
-              } else {
-                const int tt = kk - nd.c_end;
-                int slot = 0;
-                if (tt < nd.n_tail) slot = a.tails[nd.tail_off + tt];
-                else atomicExch(a.err, DEV_BAD_INDEX);
-                rows[t] = a.kv_pool +
-                          ((((static_cast<size_t>(it.seq) * a.n_slots + slot) * a.L + it.layer) * 2) * a.KVH + ur.kvh) * HD;
-              }
-              float kv[DPL];
-              const __half* kr = rows[t] + lane * DPL;
-#pragma unroll
-              for (int d = 0; d < DPL; d += 2) {
-                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(kr + d));
-                kv[d] = f.x;
-                kv[d + 1] = f.y;
-              }
-              float dp = 0.0f;
-#pragma unroll
-              for (int d = 0; d < DPL; ++d) dp = fmaf(qw[d], kv[d], dp);
-              sw[t] = warp_sum(dp) * a.scale_log2;
-            }
-          }
-          float mw = -INFINITY;
-#pragma unroll
-          for (int t = 0; t < kAttnWindow; ++t) mw = fmaxf(mw, sw[t]);
-          float lw = 0.0f, ow[DPL];
-#pragma unroll
-          for (int d = 0; d < DPL; ++d) ow[d] = 0.0f;
-          const size_t voff = static_cast<size_t>(a.KVH) * a.max_ctx * HD;   // V rows of the cache
-          const size_t voff_pool = static_cast<size_t>(a.KVH) * HD;          // V rows of the pool
-#pragma unroll
-          for (int t = 0; t < kAttnWindow; ++t) {
-            if (t < nw) {
-              const float pt = exp2f(sw[t] - mw);
-              lw = __fadd_rn(lw, pt);
-              const int kk = bnd + t;
-              const __half* vr = rows[t] + (kk < nd.c_end ? voff : voff_pool) + lane * DPL;
-#pragma unroll
-              for (int d = 0; d < DPL; d += 2) {
-                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(vr + d));
-                ow[d] = fmaf(pt, f.x, ow[d]);
-                ow[d + 1] = fmaf(pt, f.y, ow[d + 1]);
-              }
-            }
-          }
-          // bulk groups in group order, then the window
-          const float* base = a.part + (static_cast<size_t>(row) * a.H + qh) * a.max_groups * PS;
-          float mg[2] = {-INFINITY, -INFINITY}, lg[2] = {0.0f, 0.0f};
-#pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            const int gg = lane + 32 * h2;
-            if (gg < it.n_groups) {
-              mg[h2] = __ldcg(base + gg * PS + HD);
-              lg[h2] = __ldcg(base + gg * PS + HD + 1);
-            }
-          }
-          const float M = fmaxf(warp_max(fmaxf(mg[0], mg[1])), mw);
-          float wg[2];
-#pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) wg[h2] = (lg[h2] > 0.0f) ? exp2f(mg[h2] - M) : 0.0f;
-          const float ww = exp2f(mw - M);
-          const float L = __fadd_rn(warp_sum(__fadd_rn(lg[0] * wg[0], lg[1] * wg[1])), lw * ww);
-          float O[DPL];
-#pragma unroll
-          for (int d = 0; d < DPL; ++d) O[d] = 0.0f;
-          for (int g4 = 0; g4 < it.n_groups; g4 += 4) {   // four groups' loads ahead of their FMAs
-            float pv[4][DPL], wv[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int gg = g4 + e;
-              wv[e] = __shfl_sync(0xffffffffu, gg < 32 ? wg[0] : wg[1], gg & 31);
-              if (gg >= it.n_groups) wv[e] = 0.0f;
-#pragma unroll
-              for (int d = 0; d < DPL; ++d) pv[e][d] = wv[e] != 0.0f ? __ldcg(base + gg * PS + lane * DPL + d) : 0.0f;
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              if (wv[e] == 0.0f) continue;
-#pragma unroll
-              for (int d = 0; d < DPL; ++d) O[d] = fmaf(wv[e], pv[e][d], O[d]);
-            }
-          }
-          const float invl = 1.0f / L;
-          const size_t lo = static_cast<size_t>(a.plane_rows) * a.H * HD;
-#pragma unroll
-          for (int d = 0; d < DPL; ++d) {
-            const float v = fmaf(ww, ow[d], O[d]) * invl;
-            const size_t oo = static_cast<size_t>(row) * a.H * HD + qh * HD + lane * DPL + d;
-            store_pair(a.out + oo, a.out + lo + oo, v);
-          }
+        if (prev == it.n_groups - 1) {
+          a.counters[it.counter * a.KVH + ur.kvh] = 0;   // ready for the next launch
+          post(ur.item, ur.kvh);
         }
-        if (et == 0) a.counters[it.counter * a.KVH + ur.kvh] = 0;
       }
-      epi_sync();   // sflag[0] consumed
+    }
+    if (et == 0) post(-1, 0);
+  } else {
+    // ---------------- merge warps: final combination of completed (item, KV head)s ----------------
+    const int mw = warp - 6;
+    for (int k = 0;; ++k) {
+      const int slot = k % kMergeSlots;
+      if (!mbar_wait(&m_full[slot], static_cast<uint32_t>(k / kMergeSlots) & 1u, a.err, DEV_TIMEOUT_FULL)) break;
+      const int item = mreq[2 * slot], kvh = mreq[2 * slot + 1];
+      if (item < 0) break;
+      const AttnItem it = a.items[item];
+      const int nq = (it.row_end - it.row_begin) * G;
+      for (int qi = mw; qi < nq; qi += 4) merge_query<HD>(a, it, kvh, qi, lane);
+      named_bar_sync(kMergeBar, 128);
+      if (tid == 6 * 32) mbar_arrive(&m_empty[slot]);
     }
   }
   tc_fence_before();
