@@ -28,9 +28,9 @@
 // CTAs (one per SM) take contiguous ranges of units.  Warp 0 streams the committed K and V
 // tiles of each unit through a ring of shared-memory stages with TMA (128-byte swizzle,
 // 32-row boxes); warp 1 owns TMEM and issues the MMAs; warps 2-5 build the query tiles,
-// run the softmax between the two MMAs and write the group partials; warps 6-9 take the
-// final combinations (window keys + group merge) of completed (item, KV head)s off the
-// critical path.
+// run the softmax between the two MMAs and write the group partials; the last two warps
+// take the window keys and the final combinations of the (item, KV head)s off the critical
+// path.
 #include <cuda_fp16.h>
 
 #include <type_traits>
@@ -41,29 +41,30 @@
 namespace dex {
 
 constexpr int kQT = kAttnPassQueries;                 // queries per pass (MMA N)
-constexpr int kAttnThreads = 320;                     // producer, MMA, four epilogue, four merge warps
+constexpr int kMergeWarps = 2;
+constexpr int kAttnThreads = 32 * (6 + kMergeWarps);  // producer, MMA, four epilogue warps, merge warps
 constexpr int kBoxRows = 32;                          // TMA box height
 constexpr int kEpiBar = 1, kMergeBar = 2;             // named barriers of the epilogue / merge warps
-constexpr int kMergeSlots = 4;                        // merge requests in flight
 static_assert(kAttnGroupPos == 128 && kQT == 16, "128-key groups, 16-query MMA columns");
 
-// Shared-memory plan: K/V ring, query and probability tiles (hi, lo), a zero atom that pads
-// the 64-dim value tiles of head_dim 64 to the MMA's 128 rows, reduction scratch, barriers.
+// Shared-memory plan: K/V ring; the query tile (rows 0-15 hi, 16-31 lo) and the
+// probability tile (same); a zero atom that pads the 64-dim value tiles of head_dim 64 to
+// the MMA's 128 rows; reduction scratch; barriers.
 template <int HD>
 struct AttnSmem {
   static constexpr uint32_t kTile = kAttnGroupPos * HD * 2;   // [128 rows][HD] fp16, HD/64 halves of 16 KB
   static constexpr uint32_t kStage = 2 * kTile;
   static constexpr int kStages = (HD == 128) ? 3 : 5;
   static constexpr uint32_t kRing = kStages * kStage;
-  static constexpr uint32_t kQTile = kQT * HD * 2;            // [16][HD] fp16, HD/64 halves of 2 KB
-  static constexpr uint32_t kPTile = kQT * kAttnGroupPos * 2; // [16][128 keys] fp16, two halves of 2 KB
+  static constexpr uint32_t kQTile = 2 * kQT * HD * 2;          // [32][HD] fp16, HD/64 halves of 4 KB
+  static constexpr uint32_t kPTile = 2 * kQT * kAttnGroupPos * 2;   // [32][128 keys] fp16, two halves of 4 KB
   static constexpr uint32_t kZero = (HD == 128) ? 0 : kAttnGroupPos * 128;
-  static constexpr uint32_t oQhi = kRing, oQlo = oQhi + kQTile, oPhi = oQlo + kQTile, oPlo = oPhi + kPTile;
-  static constexpr uint32_t oZero = oPlo + kPTile;
+  static constexpr uint32_t oQ = kRing, oP = oQ + kQTile;
+  static constexpr uint32_t oZero = oP + kPTile;
   static constexpr uint32_t oRed = oZero + kZero;                  // float [2][4][16] max / sum
   static constexpr uint32_t oMeta = oRed + 2 * 4 * kQT * 4;        // int [16] bulk bounds
   static constexpr uint32_t oBar = oMeta + kQT * 4 + 16;
-  static constexpr uint32_t kTotal = oBar + (2 * kStages + 4 + 2 * 4) * 8 + 4 * 8 + 16 + 1024;   // + alignment slack
+  static constexpr uint32_t kTotal = oBar + (2 * kStages + 4) * 8 + 16 + 1024;   // + alignment slack
 };
 
 // MN-major operand descriptor, 128-byte swizzle: 64 contiguous 16-bit elements of M (or N)
@@ -118,12 +119,28 @@ __device__ __forceinline__ UnitRef unit_ref(const AttnArgs& a, int u) {
 }
 __device__ __forceinline__ int bulk_end(int pos) { return max(0, pos - kAttnWindow + 1); }
 
-// Final combination of one query of an (item, KV head): its window keys on CUDA cores,
-// then the bulk groups' partials in group order, then the window part; the output is
-// written as a hi/lo bf16 pair.  One warp per query; every global load of the query is
-// issued before the arithmetic that needs it.
+// Sum of the four accumulator chains of a product, hi and lo columns: for each query column
+// j, v[j] = sum over chains c in order of (D_c[j] + D_c[j + 16]).
+__device__ __forceinline__ void tmem_chain_sum(uint32_t taddr, float (&v)[kQT]) {
+  uint32_t r[32];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    tmem_ld32_nowait(taddr + static_cast<uint32_t>(c * 2 * kQT), r);
+    tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < kQT; ++j) {
+      const float t = __fadd_rn(__uint_as_float(r[j]), __uint_as_float(r[j + kQT]));
+      v[j] = (c == 0) ? t : __fadd_rn(v[j], t);
+    }
+  }
+}
+
+// Window part of one query of an (item, KV head): keys [b, p] on CUDA cores, from the
+// committed cache or the branch pool, stored as the query's record in the window slot of
+// the partials (O unnormalised, max, sum).  One warp per query; the query's loads are issued
+// before the arithmetic that needs them.
 template <int HD>
-__device__ __forceinline__ void merge_query(const AttnArgs& a, const AttnItem& it, int kvh, int qi, int lane) {
+__device__ __forceinline__ void window_query(const AttnArgs& a, const AttnItem& it, int kvh, int qi, int lane) {
   constexpr int DPL = HD / 32;                   // dims per lane
   constexpr int PS = HD + 2;
   using Raw = typename std::conditional<HD == 128, uint2, uint32_t>::type;   // DPL fp16 values
@@ -155,28 +172,13 @@ __device__ __forceinline__ void merge_query(const AttnArgs& a, const AttnItem& i
   const float* qsrc = a.q + (static_cast<size_t>(row) * a.H + qh) * HD + lane * DPL;
 #pragma unroll
   for (int d = 0; d < DPL; ++d) qw[d] = __ldcg(qsrc + d);
-  Raw kr[kAttnWindow], vr[kAttnWindow];
+  Raw kr[kAttnWindow];
 #pragma unroll
   for (int t = 0; t < kAttnWindow; ++t) {
     const __half* kp = reinterpret_cast<const __half*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(krow), t));
-    const __half* vp = reinterpret_cast<const __half*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(vrow), t));
-    if (t < nw) {
-      kr[t] = *reinterpret_cast<const Raw*>(kp + lane * DPL);
-      vr[t] = *reinterpret_cast<const Raw*>(vp + lane * DPL);
-    }
+    if (t < nw) kr[t] = *reinterpret_cast<const Raw*>(kp + lane * DPL);
   }
-  // the bulk groups' statistics (lane gg holds groups gg and gg + 32)
-  const float* base = a.part + (static_cast<size_t>(row) * a.H + qh) * a.max_groups * PS;
-  float mg[2] = {-INFINITY, -INFINITY}, lg[2] = {0.0f, 0.0f};
-#pragma unroll
-  for (int h2 = 0; h2 < 2; ++h2) {
-    const int gg = lane + 32 * h2;
-    if (gg < it.n_groups) {
-      mg[h2] = __ldcg(base + gg * PS + HD);
-      lg[h2] = __ldcg(base + gg * PS + HD + 1);
-    }
-  }
-  // window scores: per key the lane's products in dim order, then the warp butterfly
+  // scores: per key the lane's products in dim order, then the warp butterfly
   float sw[kAttnWindow];
   float mw = -INFINITY;
 #pragma unroll
@@ -195,6 +197,12 @@ __device__ __forceinline__ void merge_query(const AttnArgs& a, const AttnItem& i
       mw = fmaxf(mw, sw[t]);
     }
   }
+  Raw vr[kAttnWindow];   // value rows after the key rows: fewer registers live at once
+#pragma unroll
+  for (int t = 0; t < kAttnWindow; ++t) {
+    const __half* vp = reinterpret_cast<const __half*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(vrow), t));
+    if (t < nw) vr[t] = *reinterpret_cast<const Raw*>(vp + lane * DPL);
+  }
   float lw = 0.0f, ow[DPL];
 #pragma unroll
   for (int d = 0; d < DPL; ++d) ow[d] = 0.0f;
@@ -212,7 +220,38 @@ __device__ __forceinline__ void merge_query(const AttnArgs& a, const AttnItem& i
       }
     }
   }
-  // bulk groups in group order, then the window
+  float* rec = a.part + ((static_cast<size_t>(row) * a.H + qh) * a.part_slots + (a.part_slots - 1)) * PS;
+#pragma unroll
+  for (int d = 0; d < DPL; ++d) __stcg(rec + lane * DPL + d, ow[d]);
+  if (lane == 0) {
+    __stcg(rec + HD, mw);
+    __stcg(rec + HD + 1, lw);
+  }
+}
+
+// Final combination of one query: the bulk groups' records in group order, then the window
+// record; the output is written as a hi/lo bf16 pair.
+template <int HD>
+__device__ __forceinline__ void combine_query(const AttnArgs& a, const AttnItem& it, int kvh, int qi, int lane) {
+  constexpr int DPL = HD / 32;
+  constexpr int PS = HD + 2;
+  const int G = a.H / a.KVH;
+  const int row = it.row_begin + qi / G, qh = kvh * G + qi % G;
+  const float* base = a.part + (static_cast<size_t>(row) * a.H + qh) * a.part_slots * PS;
+  const float* wrec = base + (a.part_slots - 1) * PS;
+  float mg[2] = {-INFINITY, -INFINITY}, lg[2] = {0.0f, 0.0f};
+#pragma unroll
+  for (int h2 = 0; h2 < 2; ++h2) {
+    const int gg = lane + 32 * h2;
+    if (gg < it.n_groups) {
+      mg[h2] = __ldcg(base + gg * PS + HD);
+      lg[h2] = __ldcg(base + gg * PS + HD + 1);
+    }
+  }
+  const float mw = __ldcg(wrec + HD), lw = __ldcg(wrec + HD + 1);
+  float ow[DPL];
+#pragma unroll
+  for (int d = 0; d < DPL; ++d) ow[d] = __ldcg(wrec + lane * DPL + d);
   const float M = fmaxf(warp_max(fmaxf(mg[0], mg[1])), mw);
   float wg[2];
 #pragma unroll
@@ -254,9 +293,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tmKV, const __grid_constant__ AttnArgs a) {
   using SM = AttnSmem<HD>;
   constexpr int S = SM::kStages;
-  constexpr int KSTEPS = HD / 16;                // QK k-steps (dims)
-  constexpr int PSTEPS = kAttnGroupPos / 16;     // PV k-steps (keys)
   constexpr int PS = HD + 2;                     // partial record: O[HD], m, l
+  constexpr int KS_PER_CHAIN = HD / 16 / 4;      // QK k-steps (16 dims) per accumulator chain
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
@@ -268,10 +306,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* s_full = q_full + 1;  // scores in TMEM (MMA -> epilogue)
   uint64_t* p_full = s_full + 1;  // probability tile written (epilogue -> MMA)
   uint64_t* o_full = p_full + 1;  // group output in TMEM (MMA -> epilogue)
-  uint64_t* m_full = o_full + 1;  // [kMergeSlots] merge request posted (epilogue -> merge warps)
-  uint64_t* m_empty = m_full + kMergeSlots;   // [kMergeSlots] merge request done
-  int* mreq = reinterpret_cast<int*>(m_empty + kMergeSlots);   // [kMergeSlots][2] item, KV head
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mreq + 2 * kMergeSlots);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_full + 1);
   volatile int* sflag = reinterpret_cast<volatile int*>(tmem_slot + 1);   // [1] abort
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -280,6 +315,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int u1 = static_cast<int>((static_cast<long long>(cta + 1) * a.n_units) / C);
   const int n_my = u1 - u0;
   const int G = a.H / a.KVH;
+  unsigned long long* tl = a.timeline ? a.timeline + static_cast<size_t>(cta) * kAttnTimelineSlots : nullptr;
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
@@ -289,10 +325,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     mbar_init(s_full, 1);
     mbar_init(p_full, 128);
     mbar_init(o_full, 1);
-    for (int k = 0; k < kMergeSlots; ++k) {
-      mbar_init(&m_full[k], 1);
-      mbar_init(&m_empty[k], 1);
-    }
     sflag[1] = 0;
     fence_mbar_init();
     tma_prefetch(&tmKV);
@@ -303,7 +335,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     *reinterpret_cast<uint4*>(smem + o) = make_uint4(0u, 0u, 0u, 0u);
   fence_proxy_async_smem();
   if (warp == 1) {
-    tmem_alloc(tmem_slot, 32);
+    tmem_alloc(tmem_slot, 256);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -352,12 +384,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
+    // S = K [Qhi|Qlo]^T and O^T = V^T [Phi|Plo]^T with N = 32 (hi columns 0-15, lo 16-31),
+    // each over four independent accumulator chains (a quarter of the dims / keys each) so
+    // the chains' MMAs overlap; the epilogue sums chains and halves in a fixed order.
     if (lane == 0) {
-      const uint32_t id_qk = idesc_f16_f32(128, kQT, false);
-      const uint32_t id_pv = idesc_f16_f32(128, kQT, true);
-      const uint32_t d_s = tmem_base, d_o = tmem_base + kQT;
-      const uint32_t qhi = smem_u32(smem + SM::oQhi), qlo = smem_u32(smem + SM::oQlo);
-      const uint32_t phi = smem_u32(smem + SM::oPhi), plo = smem_u32(smem + SM::oPlo);
+      const uint32_t id_qk = idesc_f16_f32(128, 2 * kQT, false);
+      const uint32_t id_pv = idesc_f16_f32(128, 2 * kQT, true);
+      const uint32_t d_s = tmem_base, d_o = tmem_base + 4 * 2 * kQT;
+      const uint32_t qt = smem_u32(smem + SM::oQ), pt = smem_u32(smem + SM::oP);
       uint32_t np = 0;   // passes so far (barrier phases)
       bool ok = true;
       for (int i = 0; i < n_my && ok; ++i) {
@@ -373,22 +407,28 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (!mbar_wait(q_full, np & 1u, a.err, DEV_TIMEOUT_FULL)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
-          for (int ks = 0; ks < KSTEPS; ++ks) {   // S = K Q^T over 16-dim steps, hi then lo
-            const uint32_t off_a = static_cast<uint32_t>((ks >> 2) * kAttnGroupPos * 128 + (ks & 3) * 32);
-            const uint32_t off_b = static_cast<uint32_t>((ks >> 2) * kQT * 128 + (ks & 3) * 32);
-            const uint64_t ad = sw128_kmajor_desc(kt + off_a);
-            umma_bf16(d_s, ad, sw128_kmajor_desc(qhi + off_b), id_qk, ks > 0 ? 1u : 0u);
-            umma_bf16(d_s, ad, sw128_kmajor_desc(qlo + off_b), id_qk, 1u);
+          for (int e = 0; e < KS_PER_CHAIN; ++e) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {        // chain c: dims [c HD/4, (c+1) HD/4)
+              const int ks = c * KS_PER_CHAIN + e;
+              const uint32_t off_a = static_cast<uint32_t>((ks >> 2) * kAttnGroupPos * 128 + (ks & 3) * 32);
+              const uint32_t off_b = static_cast<uint32_t>((ks >> 2) * 2 * kQT * 128 + (ks & 3) * 32);
+              umma_bf16(d_s + c * 2 * kQT, sw128_kmajor_desc(kt + off_a), sw128_kmajor_desc(qt + off_b), id_qk,
+                        e > 0 ? 1u : 0u);
+            }
           }
           umma_commit(s_full);
           if (!mbar_wait(p_full, np & 1u, a.err, DEV_TIMEOUT_FULL)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
-          for (int ks = 0; ks < PSTEPS; ++ks) {   // O^T = V^T P^T over 16-key steps, hi then lo
-            const uint64_t ad = sw128_mnmajor_desc(vt + ks * 16 * 128, lbo_v, 1024);
-            const uint32_t off_b = static_cast<uint32_t>((ks >> 2) * kQT * 128 + (ks & 3) * 32);
-            umma_bf16(d_o, ad, sw128_kmajor_desc(phi + off_b), id_pv, ks > 0 ? 1u : 0u);
-            umma_bf16(d_o, ad, sw128_kmajor_desc(plo + off_b), id_pv, 1u);
+          for (int e = 0; e < 2; ++e) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {        // chain c: keys [32c, 32c + 32)
+              const int ks = 2 * c + e;
+              const uint64_t ad = sw128_mnmajor_desc(vt + ks * 16 * 128, lbo_v, 1024);
+              const uint32_t off_b = static_cast<uint32_t>((ks >> 2) * 2 * kQT * 128 + (ks & 3) * 32);
+              umma_bf16(d_o + c * 2 * kQT, ad, sw128_kmajor_desc(pt + off_b), id_pv, e > 0 ? 1u : 0u);
+            }
           }
           umma_commit(o_full);
           if (p == n_pass - 1) umma_commit(&empty[st]);   // the stage is free once these MMAs complete
@@ -401,25 +441,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int lq = warp & 3;                   // TMEM lane quarter of this warp
     const int r = lq * 32 + lane;              // TMEM row: key (scores) or value dim (output)
     const uint32_t t_row = static_cast<uint32_t>(lq * 32) << 16;
-    uint8_t* qhi = smem + SM::oQhi;
-    uint8_t* qlo = smem + SM::oQlo;
-    uint8_t* phi = smem + SM::oPhi;
-    uint8_t* plo = smem + SM::oPlo;
+    uint8_t* qtile = smem + SM::oQ;
+    uint8_t* ptile = smem + SM::oP;
     auto epi_sync = [] { named_bar_sync(kEpiBar, 128); };
     constexpr int QD = HD / 8;                 // query dims per thread (8 threads per query)
     const int qj = et >> 3, qd0 = (et & 7) * QD;
     uint32_t np = 0;
-    int n_req = 0;                             // merge requests posted
-    // posts one merge request (item, KV head), or the end marker (item -1); et == 0 only
-    auto post = [&](int item, int kvh) {
-      const int k = n_req % kMergeSlots;
-      if (n_req >= kMergeSlots)
-        mbar_wait(&m_empty[k], static_cast<uint32_t>((n_req / kMergeSlots) - 1) & 1u, a.err, DEV_TIMEOUT_EMPTY);
-      mreq[2 * k] = item;
-      mreq[2 * k + 1] = kvh;
-      mbar_arrive(&m_full[k]);
-      ++n_req;
-    };
+    unsigned long long* etl = (tl && et == 0) ? tl : nullptr;
     // this thread's slice of pass (i, p)'s queries (fp32) and, for et < 16, the query's
     // position and committed extent -- loaded one pass ahead
     float qv[QD];
@@ -449,6 +477,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         qcend = __ldg(&a.nodes[row].c_end);
       }
     };
+    if (etl) {
+      etl[0] = global_timer_ns();
+      etl[2] = static_cast<unsigned long long>(n_my);
+    }
     if (n_my > 0) load_q(0, 0);
     bool aborted = false;
     for (int i = 0; i < n_my && !aborted; ++i) {
@@ -457,18 +489,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const int g0 = ur.g * kAttnGroupPos;
       const int nq = (it.row_end - it.row_begin) * G;
       const int n_pass = (nq + kQT - 1) / kQT;
+      unsigned long long* ut = (etl && i < kAttnTimelineUnits) ? etl + 3 + 4 * i : nullptr;
       for (int p = 0; p < n_pass; ++p, ++np) {
         const int q0 = p * kQT;
         const int nb = min(kQT, nq - q0);
-        // (1) query tile: hi/lo fp16 in the MMA's K-major swizzled layout; bulk bounds
+        // (1) query tile: hi rows 0-15, lo rows 16-31, K-major swizzled; bulk bounds
 #pragma unroll
         for (int e = 0; e < QD; e += 8) {
           __align__(16) __half h8[8], l8[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k) split_f16(qv[e + k], h8[k], l8[k]);
-          const uint32_t off = sw_elem_off(qj, qd0 + e, kQT);
-          *reinterpret_cast<uint4*>(qhi + off) = *reinterpret_cast<const uint4*>(h8);
-          *reinterpret_cast<uint4*>(qlo + off) = *reinterpret_cast<const uint4*>(l8);
+          *reinterpret_cast<uint4*>(qtile + sw_elem_off(qj, qd0 + e, 2 * kQT)) = *reinterpret_cast<const uint4*>(h8);
+          *reinterpret_cast<uint4*>(qtile + sw_elem_off(kQT + qj, qd0 + e, 2 * kQT)) =
+              *reinterpret_cast<const uint4*>(l8);
         }
         if (et < kQT) {
           const int bnd = qpos >= 0 ? bulk_end(qpos) : 0;
@@ -477,6 +510,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         fence_proxy_async_smem();
         mbar_arrive(q_full);
+        if (ut && p == 0) ut[0] = global_timer_ns();
         // the next pass's queries, while this one runs
         if (p + 1 < n_pass) load_q(i, p + 1);
         else if (i + 1 < n_my) load_q(i + 1, 0);
@@ -484,9 +518,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (!mbar_wait(s_full, np & 1u, a.err, DEV_TIMEOUT_ACC)) sflag[1] = 1;
         epi_sync();   // meta visible; abort visible
         if (sflag[1]) { aborted = true; break; }
+        if (ut && p == 0) ut[1] = global_timer_ns();
         tc_fence_after();
         float s[kQT];
-        tmem_ld16(tmem_base + t_row, s);
+        tmem_chain_sum(tmem_base + t_row, s);
         const int key = g0 + r;
         float* rmax = red;
         float* rsum = red + 4 * kQT;
@@ -504,27 +539,28 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           const float pj = (s[j] == -INFINITY) ? 0.0f : exp2f(s[j] - gm[j]);
           __half h, l;
           split_f16(pj, h, l);
-          const uint32_t off = sw_elem_off(j, r, kQT);
-          *reinterpret_cast<__half*>(phi + off) = h;
-          *reinterpret_cast<__half*>(plo + off) = l;
+          *reinterpret_cast<__half*>(ptile + sw_elem_off(j, r, 2 * kQT)) = h;
+          *reinterpret_cast<__half*>(ptile + sw_elem_off(kQT + j, r, 2 * kQT)) = l;
           const float ps = warp_sum(pj);
           if (lane == 0) rsum[lq * kQT + j] = ps;
         }
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(p_full);
+        if (ut && p == 0) ut[2] = global_timer_ns();
         // (3) group output -> partial records (O, m, l) of the pass's queries
         if (!mbar_wait(o_full, np & 1u, a.err, DEV_TIMEOUT_ACC)) sflag[1] = 1;
         epi_sync();   // sums visible; abort visible
         if (sflag[1]) { aborted = true; break; }
+        if (ut && p == n_pass - 1) ut[3] = global_timer_ns();
         tc_fence_after();
         float o[kQT];
-        tmem_ld16(tmem_base + kQT + t_row, o);
+        tmem_chain_sum(tmem_base + 4 * 2 * kQT + t_row, o);
         tc_fence_before();
         for (int j = 0; j < nb; ++j) {
           const int qi = q0 + j;
           const int row = it.row_begin + qi / G, qh = ur.kvh * G + qi % G;
-          float* pp = a.part + ((static_cast<size_t>(row) * a.H + qh) * a.max_groups + ur.g) * PS;
+          float* pp = a.part + ((static_cast<size_t>(row) * a.H + qh) * a.part_slots + ur.g) * PS;
           if (r < HD) __stcg(pp + r, o[j]);
           if (r == HD - 1) {   // the sum in key-quarter order
             __stcg(pp + HD, gm[j]);
@@ -535,42 +571,64 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         epi_sync();   // partial writes done; red / meta / tiles free for the next pass
       }
       if (aborted) break;
-      // the unit that completes an (item, KV head) hands its merge to the merge warps: the
-      // barrier above orders the team's partial writes before this thread's gpu-scope
-      // release increment; the merge warps start after the acquire that saw the last count
-      if (et == 0) {
-        int prev;
-        asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;"
-                     : "=r"(prev)
-                     : "l"(a.counters + it.counter * a.KVH + ur.kvh)
+      // one more unit of this (item, KV head) is done: the barrier above orders the team's
+      // partial writes before this thread's gpu-scope release increment
+      if (et == 0)
+        asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(a.counters + it.counter * a.KVH + ur.kvh)
                      : "memory");
-        if (prev == it.n_groups - 1) {
-          a.counters[it.counter * a.KVH + ur.kvh] = 0;   // ready for the next launch
-          post(ur.item, ur.kvh);
-        }
-      }
     }
-    if (et == 0) post(-1, 0);
+    if (etl) etl[1] = global_timer_ns();
   } else {
-    // ---------------- merge warps: final combination of completed (item, KV head)s ----------------
+    // ---------------- merge warps: window parts and final combinations ----------------
+    // The CTA that owns the last group of an (item, KV head) combines it.  Its window part
+    // needs nothing from the other units, so it is computed first, while the units run;
+    // the combination waits until all of the pair's units have counted themselves done.
     const int mw = warp - 6;
-    for (int k = 0;; ++k) {
-      const int slot = k % kMergeSlots;
-      if (!mbar_wait(&m_full[slot], static_cast<uint32_t>(k / kMergeSlots) & 1u, a.err, DEV_TIMEOUT_FULL)) break;
-      const int item = mreq[2 * slot], kvh = mreq[2 * slot + 1];
-      if (item < 0) break;
-      const AttnItem it = a.items[item];
+    for (int i = 0; i < n_my; ++i) {
+      const UnitRef ur = unit_ref(a, u0 + i);
+      const AttnItem it = a.items[ur.item];
+      if (ur.g != it.n_groups - 1) continue;
       const int nq = (it.row_end - it.row_begin) * G;
-      for (int qi = mw; qi < nq; qi += 4) merge_query<HD>(a, it, kvh, qi, lane);
-      named_bar_sync(kMergeBar, 128);
-      if (tid == 6 * 32) mbar_arrive(&m_empty[slot]);
+      for (int qi = mw; qi < nq; qi += kMergeWarps) window_query<HD>(a, it, ur.kvh, qi, lane);
+    }
+    int n_merge = 0;
+    for (int i = 0; i < n_my; ++i) {
+      const UnitRef ur = unit_ref(a, u0 + i);
+      const AttnItem it = a.items[ur.item];
+      if (ur.g != it.n_groups - 1) continue;
+      int* cnt = a.counters + it.counter * a.KVH + ur.kvh;
+      unsigned long long* mt = (tl && tid == 6 * 32 && n_merge < 4) ? tl + 3 + 4 * kAttnTimelineUnits + 2 * n_merge
+                                                                     : nullptr;
+      if (tid == 6 * 32) {   // every unit of the pair has published its partials
+        const uint64_t t0 = global_timer_ns();
+        for (uint32_t spin = 0;; ++spin) {
+          int v;
+          asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+          if (v >= it.n_groups) break;
+          if ((spin & 63u) == 63u && global_timer_ns() - t0 > kWaitLimitNs) {
+            atomicExch(a.err, DEV_TIMEOUT_ACC);
+            break;
+          }
+          __nanosleep(64);
+        }
+        if (mt) mt[0] = global_timer_ns();
+      }
+      named_bar_sync(kMergeBar, 32 * kMergeWarps);
+      const int nq = (it.row_end - it.row_begin) * G;
+      for (int qi = mw; qi < nq; qi += kMergeWarps) combine_query<HD>(a, it, ur.kvh, qi, lane);
+      named_bar_sync(kMergeBar, 32 * kMergeWarps);
+      if (tid == 6 * 32) {
+        *cnt = 0;   // ready for the next launch
+        if (mt) mt[1] = global_timer_ns();
+      }
+      ++n_merge;
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, 32);
+    tmem_dealloc(tmem_base, 256);
   }
 }
 
@@ -591,7 +649,7 @@ static cudaError_t launch_attn_hd(cudaLaunchConfig_t cfg, const CUtensorMap& tm,
 cudaError_t launch_attention(const CUtensorMap& tm, const AttnArgs& a, int n_ctas, cudaStream_t st, bool pdl) {
   if (a.n_items <= 0 || a.n_units <= 0) return cudaSuccess;
   if (!a.nodes || !a.items || !a.tails || !a.q || !a.kv_commit || !a.kv_pool || !a.out || !a.part || !a.counters ||
-      !a.err || a.plane_rows < 1 || a.max_groups < 1 || a.max_groups > kAttnMaxGroups || n_ctas < 1 ||
+      !a.err || a.plane_rows < 1 || a.part_slots < 2 || a.part_slots > kAttnMaxGroups + 1 || n_ctas < 1 ||
       (a.hd != 64 && a.hd != 128))
     return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};

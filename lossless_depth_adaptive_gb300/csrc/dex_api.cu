@@ -18,6 +18,7 @@
 #include <memory>
 #include <mutex>
 #include <new>
+#include <string>
 #include <vector>
 
 #include "../../include/dex.h"
@@ -134,6 +135,9 @@ struct dex_handle {
   unsigned long long* timeline = nullptr;
   int tl_cap = 0, tl_used = 0;
   std::vector<int32_t> tl_meta;   // per launch: epi, n_groups, nt, n_tiles, n_segs, kblocks, n_ctas, rows
+  unsigned long long* atl = nullptr;   // attention records (same level and file, suffix ".attn")
+  int atl_cap = 0, atl_used = 0;
+  std::vector<int32_t> atl_meta;       // per launch: n_items, n_units, grid
   // host-side allocation-failure injection (DEX_FAIL_ALLOC_AT=k: the k-th allocation of
   // dex_init fails), for tests of the DEX_ENOMEM path
   int alloc_fail_at = 0, alloc_count = 0;
@@ -414,7 +418,7 @@ int run_layers(dex_handle* h, const Uploaded& u, const std::vector<Batch>& batch
     at.L = h->L;
     at.max_ctx = h->cfg.max_ctx;
     at.n_slots = h->n_slots;
-    at.max_groups = h->max_groups;
+    at.part_slots = h->max_groups + 1;
     at.plane_rows = h->rows_cap;
     at.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(h->hd)));
     cudaEvent_t ae0 = nullptr, ae1 = nullptr;
@@ -422,6 +426,11 @@ int run_layers(dex_handle* h, const Uploaded& u, const std::vector<Batch>& batch
       ae0 = next_event(h);
       ae1 = next_event(h);
       cudaEventRecord(ae0, h->st);
+    }
+    if (h->timing == 3 && h->atl && h->atl_used < h->atl_cap) {
+      at.timeline = h->atl + static_cast<size_t>(h->atl_used++) * h->n_sm * dex::kAttnTimelineSlots;
+      const int32_t meta[3] = {sl.n_items, sl.n_units, std::min(h->n_sm, sl.n_units)};
+      h->atl_meta.insert(h->atl_meta.end(), meta, meta + 3);
     }
     cudaError_t ce = dex::launch_attention(h->tm_kv, at, h->n_sm, h->st, true);
     if (ce != cudaSuccess) return cuda_fail(h, ce);
@@ -776,8 +785,24 @@ const char* dex_strerror(int code) {
 
 // Diagnostics file of timing level 3: int64 header {launches, n_ctas, slots}, then int32
 // metadata [launches][8], then the uint64 records [launches][n_ctas][slots].
+static void write_attn_timeline(dex_handle* h, const char* path) {
+  if (!h->atl || h->atl_used == 0) return;
+  const size_t words = static_cast<size_t>(h->atl_used) * h->n_sm * dex::kAttnTimelineSlots;
+  std::vector<unsigned long long> buf(words);
+  if (cudaMemcpy(buf.data(), h->atl, words * 8, cudaMemcpyDeviceToHost) != cudaSuccess) return;
+  const std::string p = std::string(path) + ".attn";
+  FILE* f = fopen(p.c_str(), "wb");
+  if (!f) return;
+  const int64_t hdr[3] = {h->atl_used, h->n_sm, dex::kAttnTimelineSlots};
+  fwrite(hdr, sizeof(hdr), 1, f);
+  fwrite(h->atl_meta.data(), 4, h->atl_meta.size(), f);
+  fwrite(buf.data(), 8, words, f);
+  fclose(f);
+}
+
 static void write_timeline(dex_handle* h) {
   const char* path = getenv("DEX_TIMELINE");
+  if (path) write_attn_timeline(h, path);
   if (!path || !h->timeline || h->tl_used == 0) return;
   const size_t words = static_cast<size_t>(h->tl_used) * h->gemm_ctas * dex::kTimelineSlots;
   std::vector<unsigned long long> buf(words);
@@ -894,7 +919,7 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
   rc |= dalloc(h, &h->ssq, R * (h->d / 128) * 4);
   rc |= dalloc(h, &h->exit_ssq, R * (h->d / 128) * 4);
   rc |= dalloc(h, &h->q, R * qd * 4);
-  rc |= dalloc(h, &h->attn_part, R * h->H * h->max_groups * (hd + 2) * 4);
+  rc |= dalloc(h, &h->attn_part, R * h->H * (h->max_groups + 1) * (hd + 2) * 4);
   rc |= dalloc(h, &h->attn_counters, (static_cast<size_t>(B) * h->N + R) * KVH * 4);
   rc |= dalloc(h, &h->rope, ctx * (hd / 2) * sizeof(float2));
   rc |= dalloc(h, &h->best, (R + 1) * 8);
@@ -1201,6 +1226,9 @@ int dex_set_timing(dex_handle* h, int32_t level) {
     h->tl_cap = n ? std::max(1, atoi(n)) : 512;
     const size_t bytes = static_cast<size_t>(h->tl_cap) * h->gemm_ctas * dex::kTimelineSlots * 8;
     if (dalloc(h, &h->timeline, bytes) || cudaMemset(h->timeline, 0, bytes) != cudaSuccess) return DEX_ENOMEM;
+    h->atl_cap = h->tl_cap;
+    const size_t abytes = static_cast<size_t>(h->atl_cap) * h->n_sm * dex::kAttnTimelineSlots * 8;
+    if (dalloc(h, &h->atl, abytes) || cudaMemset(h->atl, 0, abytes) != cudaSuccess) return DEX_ENOMEM;
   }
   h->timing = level;
   return DEX_OK;

@@ -142,12 +142,19 @@ struct AttnArgs {
   const __half* kv_pool;       // fp16 pool (layout as in GemmArgs)
   __nv_bfloat16* out;          // [2][plane_rows][H*hd] hi/lo pair
   int32_t plane_rows;
-  float* part;                 // [rows][H][max_groups][hd + 2]
+  float* part;                 // [rows][H][part_slots][hd + 2]: group records, then the window record
   int32_t* counters;           // [items * KVH]
   int32_t* err;
-  int32_t H, KVH, hd, L, max_ctx, n_slots, max_groups;
+  int32_t H, KVH, hd, L, max_ctx, n_slots, part_slots;   // part_slots = key groups of max_ctx + 1
   float scale_log2;            // log2(e) / sqrt(hd)
+  // diagnostics: per-CTA records of kAttnTimelineSlots words (globaltimer ns), or null:
+  // [0] epilogue start, [1] epilogue end, [2] units, then per unit (first kAttnTimelineUnits)
+  // query tile posted, scores seen, probabilities posted, output seen; then up to four
+  // combinations (start, end)
+  unsigned long long* timeline;
 };
+constexpr int kAttnTimelineUnits = 24;
+constexpr int kAttnTimelineSlots = 3 + 4 * kAttnTimelineUnits + 8;
 
 struct AssembleArgs {
   const DevNode* nodes;
