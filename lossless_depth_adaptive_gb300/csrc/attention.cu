@@ -62,8 +62,8 @@ struct AttnSmem {
   static constexpr uint32_t oQ = kRing, oP = oQ + kQTile;
   static constexpr uint32_t oZero = oP + kPTile;
   static constexpr uint32_t oRed = oZero + kZero;                  // float [2][4][16] max / sum
-  static constexpr uint32_t oMeta = oRed + 2 * 4 * kQT * 4;        // int [16] bulk bounds
-  static constexpr uint32_t oBar = oMeta + kQT * 4 + 16;
+  static constexpr uint32_t oMeta = oRed + 2 * 4 * kQT * 4;        // int [16] bulk bounds, int [16] record rows
+  static constexpr uint32_t oBar = oMeta + 2 * kQT * 4 + 16;
   static constexpr uint32_t kTotal = oBar + (2 * kStages + 4) * 8 + 16 + 1024;   // + alignment slack
 };
 
@@ -119,18 +119,52 @@ __device__ __forceinline__ UnitRef unit_ref(const AttnArgs& a, int u) {
 }
 __device__ __forceinline__ int bulk_end(int pos) { return max(0, pos - kAttnWindow + 1); }
 
+// Transposed butterfly over a warp for 16 values per lane: on return, lanes 2j and 2j+1 hold
+// the reduction over all 32 lanes of v[j] (16 shuffles instead of 16 separate 5-step
+// butterflies).  The combination tree is fixed by lane numbers, so sums are reproducible.
+template <bool kMax>
+__device__ __forceinline__ float warp_reduce16_transposed(const float (&v)[16], int lane) {
+  auto op = [](float x, float y) { return kMax ? fmaxf(x, y) : __fadd_rn(x, y); };
+  float a8[8], a4[4], a2[2];
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float send = b4 ? v[k] : v[k + 8];
+    const float keep = b4 ? v[k + 8] : v[k];
+    a8[k] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float send = b3 ? a8[k] : a8[k + 4];
+    const float keep = b3 ? a8[k + 4] : a8[k];
+    a4[k] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+  }
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const float send = b2 ? a4[k] : a4[k + 2];
+    const float keep = b2 ? a4[k + 2] : a4[k];
+    a2[k] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+  }
+  const float send = b1 ? a2[0] : a2[1];
+  const float keep = b1 ? a2[1] : a2[0];
+  const float a1 = op(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+  return op(a1, __shfl_xor_sync(0xffffffffu, a1, 1));
+}
+
 // Sum of the four accumulator chains of a product, hi and lo columns: for each query column
 // j, v[j] = sum over chains c in order of (D_c[j] + D_c[j + 16]).
 __device__ __forceinline__ void tmem_chain_sum(uint32_t taddr, float (&v)[kQT]) {
-  uint32_t r[32];
+  uint32_t r0[32], r1[32];
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    tmem_ld32_nowait(taddr + static_cast<uint32_t>(c * 2 * kQT), r);
+  for (int c = 0; c < 4; c += 2) {
+    tmem_ld32_nowait(taddr + static_cast<uint32_t>(c * 2 * kQT), r0);
+    tmem_ld32_nowait(taddr + static_cast<uint32_t>((c + 1) * 2 * kQT), r1);
     tmem_wait_ld();
 #pragma unroll
     for (int j = 0; j < kQT; ++j) {
-      const float t = __fadd_rn(__uint_as_float(r[j]), __uint_as_float(r[j + kQT]));
-      v[j] = (c == 0) ? t : __fadd_rn(v[j], t);
+      const float t0 = __fadd_rn(__uint_as_float(r0[j]), __uint_as_float(r0[j + kQT]));
+      const float t1 = __fadd_rn(__uint_as_float(r1[j]), __uint_as_float(r1[j + kQT]));
+      v[j] = (c == 0) ? __fadd_rn(t0, t1) : __fadd_rn(v[j], __fadd_rn(t0, t1));
     }
   }
 }
@@ -300,6 +334,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* ring = smem;
   float* red = reinterpret_cast<float*>(smem + SM::oRed);     // [0]: max [4][16], [1]: sum [4][16]
   int* meta = reinterpret_cast<int*>(smem + SM::oMeta);       // bulk bound per pass-local query
+  int* qrec = meta + kQT;                                     // row * H + head of each pass-local query
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::oBar);
   uint64_t* empty = full + S;
   uint64_t* q_full = empty + S;   // query tile written (epilogue -> MMA)
@@ -507,6 +542,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           const int bnd = qpos >= 0 ? bulk_end(qpos) : 0;
           if (bnd > qcend) atomicExch(a.err, DEV_BAD_INDEX);   // a branch key would be in the bulk
           meta[et] = bnd;
+          const int qi = q0 + et;
+          qrec[et] = (it.row_begin + qi / G) * a.H + ur.kvh * G + qi % G;
         }
         fence_proxy_async_smem();
         mbar_arrive(q_full);
@@ -526,23 +563,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         float* rmax = red;
         float* rsum = red + 4 * kQT;
 #pragma unroll
-        for (int j = 0; j < kQT; ++j) {
-          s[j] = (j < nb && key < meta[j]) ? s[j] * a.scale_log2 : -INFINITY;
-          const float m = warp_max(s[j]);
-          if (lane == 0) rmax[lq * kQT + j] = m;
+        for (int j = 0; j < kQT; ++j) s[j] = (j < nb && key < meta[j]) ? s[j] * a.scale_log2 : -INFINITY;
+        {
+          const float m = warp_reduce16_transposed<true>(s, lane);   // query lane / 2
+          if ((lane & 1) == 0) rmax[lq * kQT + (lane >> 1)] = m;
         }
         epi_sync();
-        float gm[kQT];
+        float gm[kQT], pr[kQT];
 #pragma unroll
         for (int j = 0; j < kQT; ++j) {
           gm[j] = fmaxf(fmaxf(rmax[0 * kQT + j], rmax[1 * kQT + j]), fmaxf(rmax[2 * kQT + j], rmax[3 * kQT + j]));
-          const float pj = (s[j] == -INFINITY) ? 0.0f : exp2f(s[j] - gm[j]);
+          pr[j] = (s[j] == -INFINITY) ? 0.0f : exp2f(s[j] - gm[j]);
           __half h, l;
-          split_f16(pj, h, l);
+          split_f16(pr[j], h, l);
           *reinterpret_cast<__half*>(ptile + sw_elem_off(j, r, 2 * kQT)) = h;
           *reinterpret_cast<__half*>(ptile + sw_elem_off(kQT + j, r, 2 * kQT)) = l;
-          const float ps = warp_sum(pj);
-          if (lane == 0) rsum[lq * kQT + j] = ps;
+        }
+        {
+          const float ps = warp_reduce16_transposed<false>(pr, lane);
+          if ((lane & 1) == 0) rsum[lq * kQT + (lane >> 1)] = ps;
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -557,16 +596,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         float o[kQT];
         tmem_chain_sum(tmem_base + 4 * 2 * kQT + t_row, o);
         tc_fence_before();
-        for (int j = 0; j < nb; ++j) {
-          const int qi = q0 + j;
-          const int row = it.row_begin + qi / G, qh = ur.kvh * G + qi % G;
-          float* pp = a.part + ((static_cast<size_t>(row) * a.H + qh) * a.part_slots + ur.g) * PS;
-          if (r < HD) __stcg(pp + r, o[j]);
-          if (r == HD - 1) {   // the sum in key-quarter order
-            __stcg(pp + HD, gm[j]);
-            __stcg(pp + HD + 1, __fadd_rn(__fadd_rn(rsum[0 * kQT + j], rsum[1 * kQT + j]),
-                                          __fadd_rn(rsum[2 * kQT + j], rsum[3 * kQT + j])));
-          }
+        if (r < HD) {
+#pragma unroll
+          for (int j = 0; j < kQT; ++j)
+            if (j < nb) __stcg(a.part + (static_cast<size_t>(qrec[j]) * a.part_slots + ur.g) * PS + r, o[j]);
+        }
+        if (et < nb) {   // the query's max and its sum in key-quarter order
+          float* pp = a.part + (static_cast<size_t>(qrec[et]) * a.part_slots + ur.g) * PS;
+          __stcg(pp + HD, gm[et]);
+          __stcg(pp + HD + 1, __fadd_rn(__fadd_rn(rsum[0 * kQT + et], rsum[1 * kQT + et]),
+                                        __fadd_rn(rsum[2 * kQT + et], rsum[3 * kQT + et])));
         }
         epi_sync();   // partial writes done; red / meta / tiles free for the next pass
       }
