@@ -62,8 +62,8 @@ struct AttnSmem {
   static constexpr uint32_t oQ = kRing, oP = oQ + kQTile;
   static constexpr uint32_t oZero = oP + kPTile;
   static constexpr uint32_t oRed = oZero + kZero;                  // float [2][4][16] max / sum
-  static constexpr uint32_t oMeta = oRed + 2 * 4 * kQT * 4;        // int [16] bulk bounds, int [16] record rows
-  static constexpr uint32_t oBar = oMeta + 2 * kQT * 4 + 16;
+  static constexpr uint32_t oMeta = oRed + 2 * 4 * kQT * 4;        // int [2][16] bulk bounds, int [2][16] record rows
+  static constexpr uint32_t oBar = oMeta + 4 * kQT * 4 + 16;
   static constexpr uint32_t kTotal = oBar + (2 * kStages + 4) * 8 + 16 + 1024;   // + alignment slack
 };
 
@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* ring = smem;
   float* red = reinterpret_cast<float*>(smem + SM::oRed);     // [0]: max [4][16], [1]: sum [4][16]
   int* meta = reinterpret_cast<int*>(smem + SM::oMeta);       // bulk bound per pass-local query
-  int* qrec = meta + kQT;                                     // row * H + head of each pass-local query
+  int* qrec = meta + 2 * kQT;                                 // row * H + head of each pass-local query
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::oBar);
   uint64_t* empty = full + S;
   uint64_t* q_full = empty + S;   // query tile written (epilogue -> MMA)
@@ -422,12 +422,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // S = K [Qhi|Qlo]^T and O^T = V^T [Phi|Plo]^T with N = 32 (hi columns 0-15, lo 16-31),
     // each over four independent accumulator chains (a quarter of the dims / keys each) so
     // the chains' MMAs overlap; the epilogue sums chains and halves in a fixed order.
+    // This warp also publishes each finished unit to the combining CTA (a gpu-scope release
+    // increment of the pair's counter), off the epilogue's path: the epilogue wrote the
+    // unit's partials before it posted the next probability tile, which this warp waited for.
     if (lane == 0) {
       const uint32_t id_qk = idesc_f16_f32(128, 2 * kQT, false);
       const uint32_t id_pv = idesc_f16_f32(128, 2 * kQT, true);
       const uint32_t d_s = tmem_base, d_o = tmem_base + 4 * 2 * kQT;
       const uint32_t qt = smem_u32(smem + SM::oQ), pt = smem_u32(smem + SM::oP);
       uint32_t np = 0;   // passes so far (barrier phases)
+      int* pending = nullptr;   // counter of the unit whose partials the next p_full wait covers
       bool ok = true;
       for (int i = 0; i < n_my && ok; ++i) {
         const UnitRef ur = unit_ref(a, u0 + i);
@@ -467,11 +471,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
           umma_commit(o_full);
           if (p == n_pass - 1) umma_commit(&empty[st]);   // the stage is free once these MMAs complete
+          if (pending) {
+            asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(pending) : "memory");
+            pending = nullptr;
+          }
+          if (p == n_pass - 1) pending = a.counters + it.counter * a.KVH + ur.kvh;
         }
       }
     }
   } else if (warp < 6) {
     // ---------------- epilogue: query tiles, softmax, partials ----------------
+    // Per pass n: scores -> probability tile (post) -> the next pass's query tile (post) ->
+    // output -> partial records.  Building the next query tile before the partial stores
+    // lets the next QK^T run while the stores drain, and keeps those stores out of the
+    // proxy fences.
     const int et = tid - 64;                   // 0..127
     const int lq = warp & 3;                   // TMEM lane quarter of this warp
     const int r = lq * 32 + lane;              // TMEM row: key (scores) or value dim (output)
@@ -481,17 +494,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     auto epi_sync = [] { named_bar_sync(kEpiBar, 128); };
     constexpr int QD = HD / 8;                 // query dims per thread (8 threads per query)
     const int qj = et >> 3, qd0 = (et & 7) * QD;
-    uint32_t np = 0;
     unsigned long long* etl = (tl && et == 0) ? tl : nullptr;
-    // this thread's slice of pass (i, p)'s queries (fp32) and, for et < 16, the query's
+    // the CTA's pass sequence (unit i, pass p) in order
+    struct PassRef {
+      int i, p;
+    };
+    auto next_pass = [&](PassRef x) -> PassRef {
+      const UnitRef ur = unit_ref(a, u0 + x.i);
+      const AttnItem it = a.items[ur.item];
+      const int n_pass = ((it.row_end - it.row_begin) * G + kQT - 1) / kQT;
+      return (x.p + 1 < n_pass) ? PassRef{x.i, x.p + 1} : PassRef{x.i + 1, 0};
+    };
+    // this thread's slice of a pass's queries (fp32) and, for et < 16, the query's
     // position and committed extent -- loaded one pass ahead
     float qv[QD];
     int qpos = -1, qcend = 0;
-    auto load_q = [&](int i, int p) {
-      const UnitRef ur = unit_ref(a, u0 + i);
+    auto load_q = [&](PassRef x) {
+      const UnitRef ur = unit_ref(a, u0 + x.i);
       const AttnItem it = a.items[ur.item];
       const int nq = (it.row_end - it.row_begin) * G;
-      const int qi = p * kQT + qj;
+      const int qi = x.p * kQT + qj;
 #pragma unroll
       for (int e = 0; e < QD; ++e) qv[e] = 0.0f;
       if (qi < nq) {
@@ -505,116 +527,134 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       qpos = -1;
       qcend = 0;
-      const int mi = p * kQT + et;
+      const int mi = x.p * kQT + et;
       if (et < kQT && mi < nq) {
         const int row = it.row_begin + mi / G;
         qpos = __ldg(&a.nodes[row].pos);
         qcend = __ldg(&a.nodes[row].c_end);
       }
     };
+    // query tile (hi rows 0-15, lo rows 16-31), bulk bounds and record rows of pass x (buffer b)
+    auto post_q = [&](PassRef x, int b) {
+      const UnitRef ur = unit_ref(a, u0 + x.i);
+      const AttnItem it = a.items[ur.item];
+#pragma unroll
+      for (int e = 0; e < QD; e += 8) {
+        __align__(16) __half h8[8], l8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) split_f16(qv[e + k], h8[k], l8[k]);
+        *reinterpret_cast<uint4*>(qtile + sw_elem_off(qj, qd0 + e, 2 * kQT)) = *reinterpret_cast<const uint4*>(h8);
+        *reinterpret_cast<uint4*>(qtile + sw_elem_off(kQT + qj, qd0 + e, 2 * kQT)) = *reinterpret_cast<const uint4*>(l8);
+      }
+      if (et < kQT) {
+        const int bnd = qpos >= 0 ? bulk_end(qpos) : 0;
+        if (bnd > qcend) atomicExch(a.err, DEV_BAD_INDEX);   // a branch key would be in the bulk
+        meta[b * kQT + et] = bnd;
+        const int qi = x.p * kQT + et;
+        qrec[b * kQT + et] = (it.row_begin + qi / G) * a.H + ur.kvh * G + qi % G;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(q_full);
+    };
     if (etl) {
       etl[0] = global_timer_ns();
       etl[2] = static_cast<unsigned long long>(n_my);
     }
-    if (n_my > 0) load_q(0, 0);
+    uint32_t np = 0;
+    PassRef cur{0, 0};
     bool aborted = false;
-    for (int i = 0; i < n_my && !aborted; ++i) {
+    if (n_my > 0) {
+      load_q(cur);
+      post_q(cur, 0);
+      const PassRef nx = next_pass(cur);
+      if (nx.i < n_my) load_q(nx);
+    }
+    while (cur.i < n_my && !aborted) {
+      const int i = cur.i, p = cur.p;
       const UnitRef ur = unit_ref(a, u0 + i);
       const AttnItem it = a.items[ur.item];
       const int g0 = ur.g * kAttnGroupPos;
       const int nq = (it.row_end - it.row_begin) * G;
       const int n_pass = (nq + kQT - 1) / kQT;
-      unsigned long long* ut = (etl && i < kAttnTimelineUnits) ? etl + 3 + 4 * i : nullptr;
-      for (int p = 0; p < n_pass; ++p, ++np) {
-        const int q0 = p * kQT;
-        const int nb = min(kQT, nq - q0);
-        // (1) query tile: hi rows 0-15, lo rows 16-31, K-major swizzled; bulk bounds
+      const int nb = min(kQT, nq - p * kQT);
+      const int b = np & 1;                    // meta / record-row buffer of this pass
+      unsigned long long* ut = (etl && i < kAttnTimelineUnits && p == 0) ? etl + 3 + 8 * i : nullptr;
+      // (1) scores -> masked exp2 -> probability tile; group max and sum per query
+      if (!mbar_wait(s_full, np & 1u, a.err, DEV_TIMEOUT_ACC)) sflag[1] = 1;
+      epi_sync();   // this pass's bounds visible; abort visible
+      if (sflag[1]) { aborted = true; break; }
+      if (ut) ut[1] = global_timer_ns();
+      tc_fence_after();
+      float s[kQT];
+      tmem_chain_sum(tmem_base + t_row, s);
+      const int key = g0 + r;
+      float* rmax = red;
+      float* rsum = red + 4 * kQT;
 #pragma unroll
-        for (int e = 0; e < QD; e += 8) {
-          __align__(16) __half h8[8], l8[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) split_f16(qv[e + k], h8[k], l8[k]);
-          *reinterpret_cast<uint4*>(qtile + sw_elem_off(qj, qd0 + e, 2 * kQT)) = *reinterpret_cast<const uint4*>(h8);
-          *reinterpret_cast<uint4*>(qtile + sw_elem_off(kQT + qj, qd0 + e, 2 * kQT)) =
-              *reinterpret_cast<const uint4*>(l8);
-        }
-        if (et < kQT) {
-          const int bnd = qpos >= 0 ? bulk_end(qpos) : 0;
-          if (bnd > qcend) atomicExch(a.err, DEV_BAD_INDEX);   // a branch key would be in the bulk
-          meta[et] = bnd;
-          const int qi = q0 + et;
-          qrec[et] = (it.row_begin + qi / G) * a.H + ur.kvh * G + qi % G;
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(q_full);
-        if (ut && p == 0) ut[0] = global_timer_ns();
-        // the next pass's queries, while this one runs
-        if (p + 1 < n_pass) load_q(i, p + 1);
-        else if (i + 1 < n_my) load_q(i + 1, 0);
-        // (2) scores -> masked exp2 -> probability tile; group max and sum per query
-        if (!mbar_wait(s_full, np & 1u, a.err, DEV_TIMEOUT_ACC)) sflag[1] = 1;
-        epi_sync();   // meta visible; abort visible
-        if (sflag[1]) { aborted = true; break; }
-        if (ut && p == 0) ut[1] = global_timer_ns();
-        tc_fence_after();
-        float s[kQT];
-        tmem_chain_sum(tmem_base + t_row, s);
-        const int key = g0 + r;
-        float* rmax = red;
-        float* rsum = red + 4 * kQT;
-#pragma unroll
-        for (int j = 0; j < kQT; ++j) s[j] = (j < nb && key < meta[j]) ? s[j] * a.scale_log2 : -INFINITY;
-        {
-          const float m = warp_reduce16_transposed<true>(s, lane);   // query lane / 2
-          if ((lane & 1) == 0) rmax[lq * kQT + (lane >> 1)] = m;
-        }
-        epi_sync();
-        float gm[kQT], pr[kQT];
-#pragma unroll
-        for (int j = 0; j < kQT; ++j) {
-          gm[j] = fmaxf(fmaxf(rmax[0 * kQT + j], rmax[1 * kQT + j]), fmaxf(rmax[2 * kQT + j], rmax[3 * kQT + j]));
-          pr[j] = (s[j] == -INFINITY) ? 0.0f : exp2f(s[j] - gm[j]);
-          __half h, l;
-          split_f16(pr[j], h, l);
-          *reinterpret_cast<__half*>(ptile + sw_elem_off(j, r, 2 * kQT)) = h;
-          *reinterpret_cast<__half*>(ptile + sw_elem_off(kQT + j, r, 2 * kQT)) = l;
-        }
-        {
-          const float ps = warp_reduce16_transposed<false>(pr, lane);
-          if ((lane & 1) == 0) rsum[lq * kQT + (lane >> 1)] = ps;
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(p_full);
-        if (ut && p == 0) ut[2] = global_timer_ns();
-        // (3) group output -> partial records (O, m, l) of the pass's queries
-        if (!mbar_wait(o_full, np & 1u, a.err, DEV_TIMEOUT_ACC)) sflag[1] = 1;
-        epi_sync();   // sums visible; abort visible
-        if (sflag[1]) { aborted = true; break; }
-        if (ut && p == n_pass - 1) ut[3] = global_timer_ns();
-        tc_fence_after();
-        float o[kQT];
-        tmem_chain_sum(tmem_base + 4 * 2 * kQT + t_row, o);
-        tc_fence_before();
-        if (r < HD) {
-#pragma unroll
-          for (int j = 0; j < kQT; ++j)
-            if (j < nb) __stcg(a.part + (static_cast<size_t>(qrec[j]) * a.part_slots + ur.g) * PS + r, o[j]);
-        }
-        if (et < nb) {   // the query's max and its sum in key-quarter order
-          float* pp = a.part + (static_cast<size_t>(qrec[et]) * a.part_slots + ur.g) * PS;
-          __stcg(pp + HD, gm[et]);
-          __stcg(pp + HD + 1, __fadd_rn(__fadd_rn(rsum[0 * kQT + et], rsum[1 * kQT + et]),
-                                        __fadd_rn(rsum[2 * kQT + et], rsum[3 * kQT + et])));
-        }
-        epi_sync();   // partial writes done; red / meta / tiles free for the next pass
+      for (int j = 0; j < kQT; ++j) s[j] = (j < nb && key < meta[b * kQT + j]) ? s[j] * a.scale_log2 : -INFINITY;
+      {
+        const float m = warp_reduce16_transposed<true>(s, lane);   // query lane / 2
+        if ((lane & 1) == 0) rmax[lq * kQT + (lane >> 1)] = m;
       }
-      if (aborted) break;
-      // one more unit of this (item, KV head) is done: the barrier above orders the team's
-      // partial writes before this thread's gpu-scope release increment
-      if (et == 0)
-        asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(a.counters + it.counter * a.KVH + ur.kvh)
-                     : "memory");
+      epi_sync();
+      float gm[kQT];
+#pragma unroll
+      for (int j = 0; j < kQT; ++j) {
+        gm[j] = fmaxf(fmaxf(rmax[0 * kQT + j], rmax[1 * kQT + j]), fmaxf(rmax[2 * kQT + j], rmax[3 * kQT + j]));
+        s[j] = (s[j] == -INFINITY) ? 0.0f : exp2f(s[j] - gm[j]);
+        __half h, l;
+        split_f16(s[j], h, l);
+        *reinterpret_cast<__half*>(ptile + sw_elem_off(j, r, 2 * kQT)) = h;
+        *reinterpret_cast<__half*>(ptile + sw_elem_off(kQT + j, r, 2 * kQT)) = l;
+      }
+      {
+        const float ps = warp_reduce16_transposed<false>(s, lane);
+        if ((lane & 1) == 0) rsum[lq * kQT + (lane >> 1)] = ps;
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(p_full);
+      if (ut) ut[2] = global_timer_ns();
+      // (2) the next pass's query tile (its queries were loaded one pass ahead), and the
+      // loads of the pass after it
+      const PassRef nx = next_pass(cur);
+      if (nx.i < n_my) {
+        post_q(nx, b ^ 1);
+        const PassRef nn = next_pass(nx);
+        if (nn.i < n_my) load_q(nn);
+      }
+      if (ut) ut[3] = global_timer_ns();
+      // (3) group output -> partial records (O, m, l) of the pass's queries
+      if (!mbar_wait(o_full, np & 1u, a.err, DEV_TIMEOUT_ACC)) sflag[1] = 1;
+      epi_sync();   // sums visible; abort visible
+      if (sflag[1]) { aborted = true; break; }
+      if (ut) ut[4] = global_timer_ns();
+      tc_fence_after();
+      float o[kQT];
+      tmem_chain_sum(tmem_base + 4 * 2 * kQT + t_row, o);
+      tc_fence_before();
+      if (r < HD) {
+#pragma unroll
+        for (int j = 0; j < kQT; ++j)
+          if (j < nb) __stcg(a.part + (static_cast<size_t>(qrec[b * kQT + j]) * a.part_slots + ur.g) * PS + r, o[j]);
+      }
+      if (et < nb) {   // the query's max and its sum in key-quarter order
+        float* pp = a.part + (static_cast<size_t>(qrec[b * kQT + et]) * a.part_slots + ur.g) * PS;
+        __stcg(pp + HD, gm[et]);
+        __stcg(pp + HD + 1, __fadd_rn(__fadd_rn(rsum[0 * kQT + et], rsum[1 * kQT + et]),
+                                      __fadd_rn(rsum[2 * kQT + et], rsum[3 * kQT + et])));
+      }
+      if (ut) ut[5] = global_timer_ns();
+      ++np;
+      cur = nx;
+    }
+    // the last unit's partials are published here (the MMA warp publishes the others)
+    epi_sync();
+    if (et == 0 && !aborted && n_my > 0) {
+      const UnitRef ur = unit_ref(a, u0 + n_my - 1);
+      const AttnItem it = a.items[ur.item];
+      asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(a.counters + it.counter * a.KVH + ur.kvh)
+                   : "memory");
     }
     if (etl) etl[1] = global_timer_ns();
   } else {
@@ -636,7 +676,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const AttnItem it = a.items[ur.item];
       if (ur.g != it.n_groups - 1) continue;
       int* cnt = a.counters + it.counter * a.KVH + ur.kvh;
-      unsigned long long* mt = (tl && tid == 6 * 32 && n_merge < 4) ? tl + 3 + 4 * kAttnTimelineUnits + 2 * n_merge
+      unsigned long long* mt = (tl && tid == 6 * 32 && n_merge < 4) ? tl + 3 + 8 * kAttnTimelineUnits + 2 * n_merge
                                                                      : nullptr;
       if (tid == 6 * 32) {   // every unit of the pair has published its partials
         const uint64_t t0 = global_timer_ns();

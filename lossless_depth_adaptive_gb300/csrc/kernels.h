@@ -149,12 +149,12 @@ struct AttnArgs {
   float scale_log2;            // log2(e) / sqrt(hd)
   // diagnostics: per-CTA records of kAttnTimelineSlots words (globaltimer ns), or null:
   // [0] epilogue start, [1] epilogue end, [2] units, then per unit (first kAttnTimelineUnits)
-  // query tile posted, scores seen, probabilities posted, output seen; then up to four
-  // combinations (start, end)
+  // query tile posted, scores seen, scores reduced, maxima shared, probabilities posted,
+  // output seen, partials written, unit counted; then up to four combinations (start, end)
   unsigned long long* timeline;
 };
-constexpr int kAttnTimelineUnits = 24;
-constexpr int kAttnTimelineSlots = 3 + 4 * kAttnTimelineUnits + 8;
+constexpr int kAttnTimelineUnits = 12;
+constexpr int kAttnTimelineSlots = 3 + 8 * kAttnTimelineUnits + 8;
 
 struct AssembleArgs {
   const DevNode* nodes;
