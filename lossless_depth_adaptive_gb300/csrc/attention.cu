@@ -119,6 +119,46 @@ __device__ __forceinline__ UnitRef unit_ref(const AttnArgs& a, int u) {
 }
 __device__ __forceinline__ int bulk_end(int pos) { return max(0, pos - kAttnWindow + 1); }
 
+// Walks a CTA's contiguous units in order without searching: the item record is reloaded
+// only when the walk enters the next item.
+struct UnitCursor {
+  int item, kvh, g;
+  AttnItem it;
+  __device__ __forceinline__ void init(const AttnArgs& a, int u) {
+    const UnitRef r = unit_ref(a, u);
+    item = r.item;
+    kvh = r.kvh;
+    g = r.g;
+    it = a.items[item];
+  }
+  __device__ __forceinline__ void next(const AttnArgs& a) {
+    if (++g < it.n_groups) return;
+    g = 0;
+    if (++kvh < a.KVH) return;
+    kvh = 0;
+    if (++item < a.n_items) it = a.items[item];
+  }
+  __device__ __forceinline__ int n_queries(int G) const { return (it.row_end - it.row_begin) * G; }
+};
+// A cursor over the CTA's query passes (unit, pass within the unit).
+struct PassCursor {
+  UnitCursor c;
+  int i, p;   // unit index within the CTA, pass within the unit
+  __device__ __forceinline__ void init(const AttnArgs& a, int u0) {
+    c.init(a, u0);
+    i = 0;
+    p = 0;
+  }
+  __device__ __forceinline__ void next(const AttnArgs& a, int G, int n_my) {
+    if ((p + 1) * kQT < c.n_queries(G)) {
+      ++p;
+      return;
+    }
+    p = 0;
+    if (++i < n_my) c.next(a);
+  }
+};
+
 // Transposed butterfly over a warp for 16 values per lane: on return, lanes 2j and 2j+1 hold
 // the reduction over all 32 lanes of v[j] (16 shuffles instead of 16 separate 5-step
 // butterflies).  The combination tree is fixed by lane numbers, so sums are reproducible.
@@ -385,14 +425,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (lane == 0) {
       int issued = 0;
       bool ok = true;
-      for (int i = 0; i < n_my; ++i) {
+      UnitCursor cu;
+      cu.init(a, u0);
+      for (int i = 0; i < n_my; ++i, cu.next(a)) {
         const int st = i % S;
         if (i >= S && !mbar_wait(&empty[st], static_cast<uint32_t>((i / S) - 1) & 1u, a.err, DEV_TIMEOUT_EMPTY)) {
           ok = false;
           break;
         }
-        const UnitRef ur = unit_ref(a, u0 + i);
-        const AttnItem it = a.items[ur.item];
+        const UnitCursor& ur = cu;
+        const AttnItem& it = cu.it;
         const int g0 = ur.g * kAttnGroupPos;
         const int n_com = max(0, min(kAttnGroupPos, bulk_end(it.max_pos) - g0));
         const int nbox = (n_com + kBoxRows - 1) / kBoxRows;
@@ -433,9 +475,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       uint32_t np = 0;   // passes so far (barrier phases)
       int* pending = nullptr;   // counter of the unit whose partials the next p_full wait covers
       bool ok = true;
-      for (int i = 0; i < n_my && ok; ++i) {
-        const UnitRef ur = unit_ref(a, u0 + i);
-        const AttnItem it = a.items[ur.item];
+      UnitCursor cu;
+      cu.init(a, u0);
+      for (int i = 0; i < n_my && ok; ++i, cu.next(a)) {
+        const UnitCursor& ur = cu;
+        const AttnItem& it = cu.it;
         const int st = i % S;
         const int n_pass = ((it.row_end - it.row_begin) * G + kQT - 1) / kQT;
         const uint32_t kt = smem_u32(ring + static_cast<size_t>(st) * SM::kStage);
@@ -495,29 +539,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     constexpr int QD = HD / 8;                 // query dims per thread (8 threads per query)
     const int qj = et >> 3, qd0 = (et & 7) * QD;
     unsigned long long* etl = (tl && et == 0) ? tl : nullptr;
-    // the CTA's pass sequence (unit i, pass p) in order
-    struct PassRef {
-      int i, p;
-    };
-    auto next_pass = [&](PassRef x) -> PassRef {
-      const UnitRef ur = unit_ref(a, u0 + x.i);
-      const AttnItem it = a.items[ur.item];
-      const int n_pass = ((it.row_end - it.row_begin) * G + kQT - 1) / kQT;
-      return (x.p + 1 < n_pass) ? PassRef{x.i, x.p + 1} : PassRef{x.i + 1, 0};
-    };
     // this thread's slice of a pass's queries (fp32) and, for et < 16, the query's
     // position and committed extent -- loaded one pass ahead
     float qv[QD];
     int qpos = -1, qcend = 0;
-    auto load_q = [&](PassRef x) {
-      const UnitRef ur = unit_ref(a, u0 + x.i);
-      const AttnItem it = a.items[ur.item];
-      const int nq = (it.row_end - it.row_begin) * G;
+    auto load_q = [&](const PassCursor& x) {
+      const int nq = x.c.n_queries(G);
       const int qi = x.p * kQT + qj;
 #pragma unroll
       for (int e = 0; e < QD; ++e) qv[e] = 0.0f;
       if (qi < nq) {
-        const int row = it.row_begin + qi / G, qh = ur.kvh * G + qi % G;
+        const int row = x.c.it.row_begin + qi / G, qh = x.c.kvh * G + qi % G;
         const float4* src = reinterpret_cast<const float4*>(a.q + (static_cast<size_t>(row) * a.H + qh) * HD + qd0);
 #pragma unroll
         for (int e = 0; e < QD / 4; ++e) {
@@ -529,15 +561,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       qcend = 0;
       const int mi = x.p * kQT + et;
       if (et < kQT && mi < nq) {
-        const int row = it.row_begin + mi / G;
+        const int row = x.c.it.row_begin + mi / G;
         qpos = __ldg(&a.nodes[row].pos);
         qcend = __ldg(&a.nodes[row].c_end);
       }
     };
     // query tile (hi rows 0-15, lo rows 16-31), bulk bounds and record rows of pass x (buffer b)
-    auto post_q = [&](PassRef x, int b) {
-      const UnitRef ur = unit_ref(a, u0 + x.i);
-      const AttnItem it = a.items[ur.item];
+    auto post_q = [&](const PassCursor& x, int b) {
 #pragma unroll
       for (int e = 0; e < QD; e += 8) {
         __align__(16) __half h8[8], l8[8];
@@ -551,7 +581,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (bnd > qcend) atomicExch(a.err, DEV_BAD_INDEX);   // a branch key would be in the bulk
         meta[b * kQT + et] = bnd;
         const int qi = x.p * kQT + et;
-        qrec[b * kQT + et] = (it.row_begin + qi / G) * a.H + ur.kvh * G + qi % G;
+        qrec[b * kQT + et] = (x.c.it.row_begin + qi / G) * a.H + x.c.kvh * G + qi % G;
       }
       fence_proxy_async_smem();
       mbar_arrive(q_full);
@@ -561,21 +591,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       etl[2] = static_cast<unsigned long long>(n_my);
     }
     uint32_t np = 0;
-    PassRef cur{0, 0};
+    // cur: the pass being computed; nx: the next (its queries are in registers); nn: the one after
+    PassCursor cur, nx, nn;
     bool aborted = false;
     if (n_my > 0) {
+      cur.init(a, u0);
+      nx = cur;
+      nx.next(a, G, n_my);
+      nn = nx;
+      if (nn.i < n_my) nn.next(a, G, n_my);
       load_q(cur);
       post_q(cur, 0);
-      const PassRef nx = next_pass(cur);
       if (nx.i < n_my) load_q(nx);
     }
-    while (cur.i < n_my && !aborted) {
+    while (n_my > 0 && cur.i < n_my && !aborted) {
       const int i = cur.i, p = cur.p;
-      const UnitRef ur = unit_ref(a, u0 + i);
-      const AttnItem it = a.items[ur.item];
+      const UnitCursor& ur = cur.c;
+      const AttnItem& it = cur.c.it;
       const int g0 = ur.g * kAttnGroupPos;
-      const int nq = (it.row_end - it.row_begin) * G;
-      const int n_pass = (nq + kQT - 1) / kQT;
+      const int nq = cur.c.n_queries(G);
       const int nb = min(kQT, nq - p * kQT);
       const int b = np & 1;                    // meta / record-row buffer of this pass
       unsigned long long* ut = (etl && i < kAttnTimelineUnits && p == 0) ? etl + 3 + 8 * i : nullptr;
@@ -617,10 +651,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (ut) ut[2] = global_timer_ns();
       // (2) the next pass's query tile (its queries were loaded one pass ahead), and the
       // loads of the pass after it
-      const PassRef nx = next_pass(cur);
       if (nx.i < n_my) {
         post_q(nx, b ^ 1);
-        const PassRef nn = next_pass(nx);
         if (nn.i < n_my) load_q(nn);
       }
       if (ut) ut[3] = global_timer_ns();
@@ -647,6 +679,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (ut) ut[5] = global_timer_ns();
       ++np;
       cur = nx;
+      nx = nn;
+      if (nn.i < n_my) nn.next(a, G, n_my);
     }
     // the last unit's partials are published here (the MMA warp publishes the others)
     epi_sync();
@@ -663,17 +697,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // needs nothing from the other units, so it is computed first, while the units run;
     // the combination waits until all of the pair's units have counted themselves done.
     const int mw = warp - 6;
-    for (int i = 0; i < n_my; ++i) {
-      const UnitRef ur = unit_ref(a, u0 + i);
-      const AttnItem it = a.items[ur.item];
+    UnitCursor cu;
+    if (n_my > 0) cu.init(a, u0);
+    for (int i = 0; i < n_my; ++i, cu.next(a)) {
+      const UnitCursor& ur = cu;
+      const AttnItem& it = cu.it;
       if (ur.g != it.n_groups - 1) continue;
       const int nq = (it.row_end - it.row_begin) * G;
       for (int qi = mw; qi < nq; qi += kMergeWarps) window_query<HD>(a, it, ur.kvh, qi, lane);
     }
     int n_merge = 0;
-    for (int i = 0; i < n_my; ++i) {
-      const UnitRef ur = unit_ref(a, u0 + i);
-      const AttnItem it = a.items[ur.item];
+    if (n_my > 0) cu.init(a, u0);
+    for (int i = 0; i < n_my; ++i, cu.next(a)) {
+      const UnitCursor& ur = cu;
+      const AttnItem& it = cu.it;
       if (ur.g != it.n_groups - 1) continue;
       int* cnt = a.counters + it.counter * a.KVH + ur.kvh;
       unsigned long long* mt = (tl && tid == 6 * 32 && n_merge < 4) ? tl + 3 + 8 * kAttnTimelineUnits + 2 * n_merge
