@@ -61,7 +61,7 @@ struct AttnSmem {
   static constexpr uint32_t kZero = (HD == 128) ? 0 : kAttnGroupPos * 128;
   static constexpr uint32_t oQ = kRing, oP = oQ + kQTile;
   static constexpr uint32_t oZero = oP + kPTile;
-  static constexpr uint32_t oRed = oZero + kZero;                  // float [2][4][16] max / sum
+  static constexpr uint32_t oRed = oZero + kZero;                  // float [2][16][4] max / sum
   static constexpr uint32_t oMeta = oRed + 2 * 4 * kQT * 4;        // int [2][16] bulk bounds, int [2][16] record rows
   static constexpr uint32_t oBar = oMeta + 4 * kQT * 4 + 16;
   static constexpr uint32_t kTotal = oBar + (2 * kStages + 4) * 8 + 16 + 1024;   // + alignment slack
@@ -372,7 +372,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
-  float* red = reinterpret_cast<float*>(smem + SM::oRed);     // [0]: max [4][16], [1]: sum [4][16]
+  float* red = reinterpret_cast<float*>(smem + SM::oRed);     // [0]: max [16][4], [1]: sum [16][4]
   int* meta = reinterpret_cast<int*>(smem + SM::oMeta);       // bulk bound per pass-local query
   int* qrec = meta + 2 * kQT;                                 // row * H + head of each pass-local query
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::oBar);
@@ -466,7 +466,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // the chains' MMAs overlap; the epilogue sums chains and halves in a fixed order.
     // This warp also publishes each finished unit to the combining CTA (a gpu-scope release
     // increment of the pair's counter), off the epilogue's path: the epilogue wrote the
-    // unit's partials before it posted the next probability tile, which this warp waited for.
+    // unit's partials before it posted the next query tile, which this warp waited for; the
+    // release is issued after the next pass's QK^T so that MMA does not wait for it.
     if (lane == 0) {
       const uint32_t id_qk = idesc_f16_f32(128, 2 * kQT, false);
       const uint32_t id_pv = idesc_f16_f32(128, 2 * kQT, true);
@@ -501,6 +502,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
           }
           umma_commit(s_full);
+          if (pending) {   // publish the previous unit while this pass's QK^T runs
+            asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(pending) : "memory");
+            pending = nullptr;
+          }
           if (!mbar_wait(p_full, np & 1u, a.err, DEV_TIMEOUT_FULL)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
@@ -514,12 +519,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
           }
           umma_commit(o_full);
-          if (p == n_pass - 1) umma_commit(&empty[st]);   // the stage is free once these MMAs complete
-          if (pending) {
-            asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(pending) : "memory");
-            pending = nullptr;
+          if (p == n_pass - 1) {
+            umma_commit(&empty[st]);   // the stage is free once these MMAs complete
+            pending = a.counters + it.counter * a.KVH + ur.kvh;
           }
-          if (p == n_pass - 1) pending = a.counters + it.counter * a.KVH + ur.kvh;
         }
       }
     }
@@ -628,13 +631,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       for (int j = 0; j < kQT; ++j) s[j] = (j < nb && key < meta[b * kQT + j]) ? s[j] * a.scale_log2 : -INFINITY;
       {
         const float m = warp_reduce16_transposed<true>(s, lane);   // query lane / 2
-        if ((lane & 1) == 0) rmax[lq * kQT + (lane >> 1)] = m;
+        if ((lane & 1) == 0) rmax[(lane >> 1) * 4 + lq] = m;        // [query][key quarter]
       }
       epi_sync();
       float gm[kQT];
 #pragma unroll
       for (int j = 0; j < kQT; ++j) {
-        gm[j] = fmaxf(fmaxf(rmax[0 * kQT + j], rmax[1 * kQT + j]), fmaxf(rmax[2 * kQT + j], rmax[3 * kQT + j]));
+        const float4 m4 = *reinterpret_cast<const float4*>(rmax + j * 4);
+        gm[j] = fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w));
         s[j] = (s[j] == -INFINITY) ? 0.0f : exp2f(s[j] - gm[j]);
         __half h, l;
         split_f16(s[j], h, l);
@@ -643,7 +647,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       {
         const float ps = warp_reduce16_transposed<false>(s, lane);
-        if ((lane & 1) == 0) rsum[lq * kQT + (lane >> 1)] = ps;
+        if ((lane & 1) == 0) rsum[(lane >> 1) * 4 + lq] = ps;
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -673,8 +677,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (et < nb) {   // the query's max and its sum in key-quarter order
         float* pp = a.part + (static_cast<size_t>(qrec[b * kQT + et]) * a.part_slots + ur.g) * PS;
         __stcg(pp + HD, gm[et]);
-        __stcg(pp + HD + 1, __fadd_rn(__fadd_rn(rsum[0 * kQT + et], rsum[1 * kQT + et]),
-                                      __fadd_rn(rsum[2 * kQT + et], rsum[3 * kQT + et])));
+        const float4 s4 = *reinterpret_cast<const float4*>(rsum + et * 4);
+        __stcg(pp + HD + 1, __fadd_rn(__fadd_rn(s4.x, s4.y), __fadd_rn(s4.z, s4.w)));
       }
       if (ut) ut[5] = global_timer_ns();
       ++np;
