@@ -64,7 +64,7 @@ struct AttnSmem {
   static constexpr uint32_t oRed = oZero + kZero;                  // float [2][16][4] max / sum
   static constexpr uint32_t oMeta = oRed + 2 * 4 * kQT * 4;        // int [2][16] bulk bounds, int [2][16] record rows
   static constexpr uint32_t oBar = oMeta + 4 * kQT * 4 + 16;
-  static constexpr uint32_t kTotal = oBar + (2 * kStages + 4) * 8 + 16 + 1024;   // + alignment slack
+  static constexpr uint32_t kTotal = oBar + (2 * kStages + 4) * 8 + 32 + 1024;   // + alignment slack
 };
 
 // MN-major operand descriptor, 128-byte swizzle: 64 contiguous 16-bit elements of M (or N)
@@ -304,7 +304,8 @@ __device__ __forceinline__ void window_query(const AttnArgs& a, const AttnItem& 
 }
 
 // Final combination of one query: the bulk groups' records in group order, then the window
-// record; the output is written as a hi/lo bf16 pair.
+// record; the output is written as a hi/lo bf16 pair.  The loads of up to 16 groups are
+// issued together, before the arithmetic.
 template <int HD>
 __device__ __forceinline__ void combine_query(const AttnArgs& a, const AttnItem& it, int kvh, int qi, int lane) {
   constexpr int DPL = HD / 32;
@@ -323,9 +324,13 @@ __device__ __forceinline__ void combine_query(const AttnArgs& a, const AttnItem&
     }
   }
   const float mw = __ldcg(wrec + HD), lw = __ldcg(wrec + HD + 1);
-  float ow[DPL];
+  float ow[DPL], pv[16][DPL];
 #pragma unroll
   for (int d = 0; d < DPL; ++d) ow[d] = __ldcg(wrec + lane * DPL + d);
+#pragma unroll
+  for (int e = 0; e < 16; ++e)
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) pv[e][d] = e < it.n_groups ? __ldcg(base + e * PS + lane * DPL + d) : 0.0f;
   const float M = fmaxf(warp_max(fmaxf(mg[0], mg[1])), mw);
   float wg[2];
 #pragma unroll
@@ -335,21 +340,21 @@ __device__ __forceinline__ void combine_query(const AttnArgs& a, const AttnItem&
   float O[DPL];
 #pragma unroll
   for (int d = 0; d < DPL; ++d) O[d] = 0.0f;
-  for (int g8 = 0; g8 < it.n_groups; g8 += 8) {   // eight groups' loads ahead of their FMAs
-    float pv[8][DPL], wv[8];
+  for (int g16 = 0; g16 < it.n_groups; g16 += 16) {   // groups in order
+    if (g16 > 0) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int gg = g8 + e;
-      wv[e] = __shfl_sync(0xffffffffu, gg < 32 ? wg[0] : wg[1], gg & 31);
-      if (gg >= it.n_groups) wv[e] = 0.0f;
+      for (int e = 0; e < 16; ++e)
 #pragma unroll
-      for (int d = 0; d < DPL; ++d) pv[e][d] = wv[e] != 0.0f ? __ldcg(base + gg * PS + lane * DPL + d) : 0.0f;
+        for (int d = 0; d < DPL; ++d)
+          pv[e][d] = g16 + e < it.n_groups ? __ldcg(base + (g16 + e) * PS + lane * DPL + d) : 0.0f;
     }
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      if (wv[e] == 0.0f) continue;
+    for (int e = 0; e < 16; ++e) {
+      const int gg = g16 + e;
+      const float wv = __shfl_sync(0xffffffffu, gg < 32 ? wg[0] : wg[1], gg & 31);
+      if (gg >= it.n_groups || wv == 0.0f) continue;
 #pragma unroll
-      for (int d = 0; d < DPL; ++d) O[d] = fmaf(wv[e], pv[e][d], O[d]);
+      for (int d = 0; d < DPL; ++d) O[d] = fmaf(wv, pv[e][d], O[d]);
     }
   }
   const float invl = 1.0f / L;
@@ -382,7 +387,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* p_full = s_full + 1;  // probability tile written (epilogue -> MMA)
   uint64_t* o_full = p_full + 1;  // group output in TMEM (MMA -> epilogue)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_full + 1);
-  volatile int* sflag = reinterpret_cast<volatile int*>(tmem_slot + 1);   // [1] abort
+  volatile int* sflag = reinterpret_cast<volatile int*>(tmem_slot + 1);   // [1] abort, [2] next combination
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int C = gridDim.x, cta = blockIdx.x;
@@ -401,6 +406,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     mbar_init(p_full, 128);
     mbar_init(o_full, 1);
     sflag[1] = 0;
+    sflag[2] = -1;
     fence_mbar_init();
     tma_prefetch(&tmKV);
   }
@@ -710,38 +716,56 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const int nq = (it.row_end - it.row_begin) * G;
       for (int qi = mw; qi < nq; qi += kMergeWarps) window_query<HD>(a, it, ur.kvh, qi, lane);
     }
+    // the combinations, in the order the pairs complete: sweep the owned pairs, combine
+    // every one whose units have all counted themselves done
+    // (a combined pair's counter is reset to 0, so a later sweep never picks it again)
     int n_merge = 0;
+    int remaining = 0;
     if (n_my > 0) cu.init(a, u0);
-    for (int i = 0; i < n_my; ++i, cu.next(a)) {
-      const UnitCursor& ur = cu;
-      const AttnItem& it = cu.it;
-      if (ur.g != it.n_groups - 1) continue;
-      int* cnt = a.counters + it.counter * a.KVH + ur.kvh;
-      unsigned long long* mt = (tl && tid == 6 * 32 && n_merge < 4) ? tl + 3 + 8 * kAttnTimelineUnits + 2 * n_merge
-                                                                     : nullptr;
-      if (tid == 6 * 32) {   // every unit of the pair has published its partials
-        const uint64_t t0 = global_timer_ns();
-        for (uint32_t spin = 0;; ++spin) {
+    for (int i = 0; i < n_my; ++i, cu.next(a))
+      if (cu.g == cu.it.n_groups - 1) ++remaining;
+    const uint64_t t_start = global_timer_ns();
+    volatile int* flag = sflag + 2;   // [2]: index of the next pair to combine (-1: none ready)
+    while (remaining > 0) {
+      if (tid == 6 * 32) {
+        int pick = -1;
+        UnitCursor c2;
+        c2.init(a, u0);
+        for (int i = 0; i < n_my && pick < 0; ++i, c2.next(a)) {
+          if (c2.g != c2.it.n_groups - 1) continue;
           int v;
-          asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
-          if (v >= it.n_groups) break;
-          if ((spin & 63u) == 63u && global_timer_ns() - t0 > kWaitLimitNs) {
-            atomicExch(a.err, DEV_TIMEOUT_ACC);
-            break;
-          }
-          __nanosleep(64);
+          asm volatile("ld.acquire.gpu.global.s32 %0, [%1];"
+                       : "=r"(v)
+                       : "l"(a.counters + c2.it.counter * a.KVH + c2.kvh)
+                       : "memory");
+          if (v >= c2.it.n_groups) pick = i;
         }
-        if (mt) mt[0] = global_timer_ns();
+        if (pick < 0 && global_timer_ns() - t_start > kWaitLimitNs) {
+          atomicExch(a.err, DEV_TIMEOUT_ACC);
+          pick = -2;
+        }
+        *flag = pick;
+        if (pick == -1) __nanosleep(128);
       }
       named_bar_sync(kMergeBar, 32 * kMergeWarps);
-      const int nq = (it.row_end - it.row_begin) * G;
-      for (int qi = mw; qi < nq; qi += kMergeWarps) combine_query<HD>(a, it, ur.kvh, qi, lane);
+      const int pick = *flag;
+      named_bar_sync(kMergeBar, 32 * kMergeWarps);   // everyone read the pick before it changes
+      if (pick == -2) break;
+      if (pick < 0) continue;
+      UnitCursor c3;
+      c3.init(a, u0 + pick);
+      unsigned long long* mt = (tl && tid == 6 * 32 && n_merge < 4) ? tl + 3 + 8 * kAttnTimelineUnits + 2 * n_merge
+                                                                     : nullptr;
+      if (mt) mt[0] = global_timer_ns();
+      const int nq = (c3.it.row_end - c3.it.row_begin) * G;
+      for (int qi = mw; qi < nq; qi += kMergeWarps) combine_query<HD>(a, c3.it, c3.kvh, qi, lane);
       named_bar_sync(kMergeBar, 32 * kMergeWarps);
       if (tid == 6 * 32) {
-        *cnt = 0;   // ready for the next launch
+        a.counters[c3.it.counter * a.KVH + c3.kvh] = 0;   // ready for the next launch
         if (mt) mt[1] = global_timer_ns();
       }
       ++n_merge;
+      --remaining;
     }
   }
   tc_fence_before();
