@@ -260,14 +260,38 @@ __device__ __forceinline__ U4 philox4x32_10(U4 c, uint32_t k0, uint32_t k1) {
   }
   return c;
 }
-// Gumbel(0,1) for vocabulary entry v of the row keyed by (seed, seq, target position):
-// counter (v >> 2, pos, seq, 0x44455843), word v & 3, U = ((x >> 9) + 1/2) 2^-23.
+// Gumbel(0,1) from one Philox word x: U = ((x >> 9) + 1/2) 2^-23, G = -log(-log U).  The
+// word of vocabulary entry v in the row keyed by (seed, seq, target position) is word v & 3
+// of the block with counter (v >> 2, pos, seq, 0x44455843).
+__device__ __forceinline__ float gumbel_from_bits(uint32_t w) {
+  const float u = (static_cast<float>(w >> 9) + 0.5f) * 1.1920928955078125e-07f;   // 2^-23
+  return -logf(-logf(u));
+}
 __device__ __forceinline__ float gumbel_noise(uint64_t seed, int seq, int pos, uint32_t v) {
   const U4 o = philox4x32_10(U4{v >> 2, static_cast<uint32_t>(pos), static_cast<uint32_t>(seq), 0x44455843u},
                              static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
-  const uint32_t w = (v & 3u) == 0 ? o.x : (v & 3u) == 1 ? o.y : (v & 3u) == 2 ? o.z : o.w;
-  const float u = (static_cast<float>(w >> 9) + 0.5f) * 1.1920928955078125e-07f;   // 2^-23
-  return -logf(-logf(u));
+  return gumbel_from_bits((v & 3u) == 0 ? o.x : (v & 3u) == 1 ? o.y : (v & 3u) == 2 ? o.z : o.w);
+}
+
+// Transposed butterfly argmax over a warp for 16 packed (score, ~index) keys per lane: on
+// return lanes 2j and 2j+1 hold the maximum key of column j over all 32 lanes.
+__device__ __forceinline__ unsigned long long warp_argmax16_transposed(const unsigned long long (&v)[16], int lane) {
+  auto mx = [](unsigned long long x, unsigned long long y) { return x > y ? x : y; };
+  auto sh = [](unsigned long long x, int m) {
+    const uint32_t lo = __shfl_xor_sync(0xffffffffu, static_cast<uint32_t>(x), m);
+    const uint32_t hi = __shfl_xor_sync(0xffffffffu, static_cast<uint32_t>(x >> 32), m);
+    return (static_cast<unsigned long long>(hi) << 32) | lo;
+  };
+  unsigned long long a8[8], a4[4], a2[2];
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) a8[k] = mx(b4 ? v[k + 8] : v[k], sh(b4 ? v[k] : v[k + 8], 16));
+#pragma unroll
+  for (int k = 0; k < 4; ++k) a4[k] = mx(b3 ? a8[k + 4] : a8[k], sh(b3 ? a8[k] : a8[k + 4], 8));
+#pragma unroll
+  for (int k = 0; k < 2; ++k) a2[k] = mx(b2 ? a4[k + 2] : a4[k], sh(b2 ? a4[k] : a4[k + 2], 4));
+  const unsigned long long a1 = mx(b1 ? a2[1] : a2[0], sh(b1 ? a2[0] : a2[1], 2));
+  return mx(a1, sh(a1, 1));
 }
 
 }  // namespace dex

@@ -134,8 +134,10 @@ int gemm_segments(int n_tiles, int kblocks, int C) {
   return best;
 }
 
+// Two CTAs per SM must stay resident (the persistent grid is 2 x SMs): at most 170
+// registers per thread.
 template <int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ GemmArgs a) {
@@ -478,29 +480,71 @@ __global__ void __launch_bounds__(kThreads, 1)
               __fadd_rn(__fadd_rn(qsum[0 * 16 + ep], qsum[1 * 16 + ep]), __fadd_rn(qsum[2 * 16 + ep], qsum[3 * 16 + ep]));
         named_bar_sync(1, 128);
       } else {   // EPI_EXIT
+        // The chunk's 16 nodes: sequence, target position and the DECS mask restricted to this
+        // tile's 128 vocabulary rows (a bitmap), staged in shared memory by 16 threads.
+        int* cm = reinterpret_cast<int*>(xch);   // [0,16) seq, [16,32) target pos, [32,96) mask words
+        if (ep < 16) {
+          const int c = c0 + ep;
+          uint32_t mw[4] = {0u, 0u, 0u, 0u};
+          int seq = 0, tpos = 0;
+          if (c < n) {
+            const DevNode* nd = a.nodes + b_row0 + c;
+            seq = nd->seq;
+            tpos = nd->target_pos;
+            if (!nd->unmasked) {
+              for (int p = 0; p < nd->n_prior; ++p) {
+                const int t = a.priors[nd->prior_off + p] - lt * kBM;
+                if (t >= 0 && t < kBM) mw[t >> 5] |= 1u << (t & 31);
+              }
+            }
+          }
+          cm[ep] = seq;
+          cm[16 + ep] = tpos;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) cm[32 + 4 * ep + k] = static_cast<int>(mw[k]);
+        }
+        named_bar_sync(1, 128);
         const uint32_t vid = static_cast<uint32_t>(lt * kBM + r);
-#pragma unroll 1
+        const bool v_ok = vid < static_cast<uint32_t>(a.vocab);
+        float noise[16];
+        if (a.sample) {
+          // Gumbel rows: one Philox4x32-10 block covers four consecutive vocabulary entries, so
+          // lane 4k+m computes the block of node 4g+m for its quad's entries, and a 4x4 transpose
+          // within the quad gives every lane its own entry's word for the four nodes
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const int jn = 4 * g + (lane & 3);
+            const U4 w4 = philox4x32_10(U4{vid >> 2, static_cast<uint32_t>(cm[16 + jn]), static_cast<uint32_t>(cm[jn]),
+                                           0x44455843u},
+                                        static_cast<uint32_t>(a.seed), static_cast<uint32_t>(a.seed >> 32));
+            const bool b1 = lane & 2, b0 = lane & 1;
+            // round 1 (lanes m, m^2): keep the half of the row the lane's column pair needs
+            const uint32_t r0 = __shfl_xor_sync(0xffffffffu, b1 ? w4.x : w4.z, 2);
+            const uint32_t r1 = __shfl_xor_sync(0xffffffffu, b1 ? w4.y : w4.w, 2);
+            const uint32_t B0 = b1 ? r0 : w4.x, B1 = b1 ? r1 : w4.y, B2 = b1 ? w4.z : r0, B3 = b1 ? w4.w : r1;
+            // round 2 (lanes m, m^1)
+            const uint32_t t0 = __shfl_xor_sync(0xffffffffu, b0 ? B0 : B1, 1);
+            const uint32_t t1 = __shfl_xor_sync(0xffffffffu, b0 ? B2 : B3, 1);
+            const uint32_t C[4] = {b0 ? t0 : B0, b0 ? B1 : t0, b0 ? t1 : B2, b0 ? B3 : t1};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) noise[4 * g + e] = gumbel_from_bits(C[e]);
+          }
+        }
+        unsigned long long key[16];
+#pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int c = c0 + j;
           float score = -INFINITY;
-          if (c < n && vid < static_cast<uint32_t>(a.vocab)) {
+          if (c < n && v_ok) {
             const float logit = v[j] * inv[c];
             if (a.logits_dbg) a.logits_dbg[static_cast<size_t>(b_row0 + c) * a.vocab + vid] = logit;
-            const DevNode* nd = a.nodes + b_row0 + c;
-            bool masked = false;
-            if (!nd->unmasked) {
-              for (int p = 0; p < nd->n_prior; ++p) masked |= (a.priors[nd->prior_off + p] == static_cast<int>(vid));
-            }
-            if (!masked) score = a.sample ? logit / a.tau + gumbel_noise(a.seed, nd->seq, nd->target_pos, vid) : logit;
+            const bool masked = (static_cast<uint32_t>(cm[32 + 4 * j + (r >> 5)]) >> (r & 31)) & 1u;
+            if (!masked) score = a.sample ? logit / a.tau + noise[j] : logit;
           }
-          unsigned long long key = argmax_key(score, vid);
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
-            key = other > key ? other : key;
-          }
-          if (lane == 0) qkey[wq * 16 + j] = key;
+          key[j] = argmax_key(score, vid);
         }
+        const unsigned long long best_key = warp_argmax16_transposed(key, lane);   // node lane / 2
+        if ((lane & 1) == 0) qkey[wq * 16 + (lane >> 1)] = best_key;
         named_bar_sync(1, 128);
         if (ep < 16 && c0 + ep < n) {
           unsigned long long k = qkey[ep];
