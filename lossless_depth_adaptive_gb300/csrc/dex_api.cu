@@ -313,7 +313,7 @@ int gemm(dex_handle* h, int epi, const CUtensorMap& a0, const CUtensorMap& a1, c
       dex::gemm_partial_bytes(a.nt, static_cast<size_t>(a.n_groups) * a.n_tiles * a.n_segs) > h->partial_bytes)
     return DEX_ECAPACITY;
   a.tmem_cols = pow2_at_least(a.nt);
-  a.stages = dex::gemm_stages_for(a.nt, h->gemm_smem);
+  a.stages = dex::gemm_stages_for(a.nt, epi, h->gemm_smem);
   cudaEvent_t e0 = nullptr, e1 = nullptr;
   if (h->timing == 2) {
     e0 = next_event(h);
@@ -1357,7 +1357,7 @@ int dex_exit_head_decs(const void* hidden, int32_t n, int32_t d, const void* fin
     a.groups[0].b_row0 = 0;
     a.nt = nt;
     a.kblocks = kb;
-    a.stages = dex::gemm_stages_for(nt);
+    a.stages = dex::gemm_stages_for(nt, dex::EPI_EXIT);
     a.n_tiles = n_tiles;
     a.src_tiles0 = n_tiles;
     a.tmem_cols = pow2_at_least(nt);
@@ -1494,7 +1494,7 @@ extern "C" int dex_exit_head_decs_noalloc(const void* hidden, int32_t n, int32_t
   a.groups[0].b_row0 = 0;
   a.nt = nt;
   a.kblocks = kb;
-  a.stages = dex::gemm_stages_for(nt, 200 * 1024);   // one CTA per SM: a deeper ring
+  a.stages = dex::gemm_stages_for(nt, dex::EPI_EXIT, 200 * 1024);   // one CTA per SM: a deeper ring
   a.n_tiles = n_tiles;
   a.src_tiles0 = n_tiles;
   a.tmem_cols = pow2_at_least(nt);

@@ -56,30 +56,35 @@ constexpr int kNtMax = 256;
 struct SmemMap {
   size_t a, b, bar, misc, xch, inv, qsum, qkey, total;
 };
-__host__ __device__ inline SmemMap smem_map(int nt, int stages) {
+// Exchange area of the epilogue: 16 accumulator columns x 128 rows for the epilogues that
+// read across rows (QKV: RoPE partners; SWIGLU: gate/up halves), a small node table otherwise.
+__host__ __device__ constexpr size_t xch_bytes(int epi) {
+  return (epi == EPI_QKV || epi == EPI_SWIGLU) ? static_cast<size_t>(16) * kBM * 4 : 512;
+}
+__host__ __device__ inline SmemMap smem_map(int nt, int stages, int epi) {
   SmemMap m;
   m.a = 0;
   m.b = m.a + static_cast<size_t>(stages) * kABytes;
   m.bar = m.b + static_cast<size_t>(stages) * 2 * nt * kBK * 2;   // hi and lo boxes per stage
   m.misc = m.bar + static_cast<size_t>(2 * stages + 4) * 8;       // full, empty, accf[2], tfree[2]
   m.xch = (m.misc + 32 + 15) & ~static_cast<size_t>(15);        // tmem slot + flags
-  m.inv = m.xch + 16 * kBM * 4;                                    // 16 columns x 128 rows
+  m.inv = m.xch + xch_bytes(epi);
   m.qsum = m.inv + kNtMax * 4;
   m.qkey = m.qsum + 4 * 16 * 4;
   m.total = m.qkey + 4 * 16 * 8;
   return m;
 }
 
-size_t gemm_smem_bytes(int nt, int stages) { return smem_map(nt, stages).total + 1024; }
+size_t gemm_smem_bytes(int nt, int stages, int epi) { return smem_map(nt, stages, epi).total + 1024; }
 
 constexpr size_t kSmemOptin = 227 * 1024;   // largest dynamic shared memory a CTA may opt into
 
 // Pipeline depth: the most stages (2..8) whose whole footprint fits the given budget for
 // small node tiles, or the opt-in limit for the wide tiles of prefill.
-int gemm_stages_for(int nt, size_t small_budget) {
+int gemm_stages_for(int nt, int epi, size_t small_budget) {
   const size_t budget = nt <= 64 ? small_budget : kSmemOptin;
   int s = 8;
-  while (s > 2 && gemm_smem_bytes(nt, s) > budget) --s;
+  while (s > 2 && gemm_smem_bytes(nt, s, epi) > budget) --s;
   return s;
 }
 
@@ -155,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const SmemMap sm = smem_map(a.nt, a.stages);
+  const SmemMap sm = smem_map(a.nt, a.stages, EPI);
   uint8_t* sA = smem + sm.a;
   uint8_t* sB = smem + sm.b;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + sm.bar);
@@ -656,7 +661,7 @@ template <int EPI>
 static cudaError_t launch_one(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& a2,
                               const CUtensorMap& b, const GemmArgs& args, cudaStream_t st, bool pdl) {
   static bool attr_set = false;
-  const size_t smem = gemm_smem_bytes(args.nt, args.stages);
+  const size_t smem = gemm_smem_bytes(args.nt, args.stages, EPI);
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemOptin));
@@ -714,7 +719,7 @@ cudaError_t launch_gemm(int epi, const CUtensorMap& a0, const CUtensorMap& a1, c
   if (args.tmem_cols < args.nt || args.tmem_cols < 32 || args.tmem_cols > 256 ||
       (args.tmem_cols & (args.tmem_cols - 1)))
     return cudaErrorInvalidValue;
-  if (args.stages < 2 || args.stages > 8 || gemm_smem_bytes(args.nt, args.stages) > kSmemOptin)
+  if (args.stages < 2 || args.stages > 8 || gemm_smem_bytes(args.nt, args.stages, epi) > kSmemOptin)
     return cudaErrorInvalidValue;
   switch (epi) {
     case EPI_QKV: return launch_one<EPI_QKV>(a0, a1, a2, b, args, st, pdl);

@@ -193,8 +193,10 @@ struct CollapseArgs {
 // into one contiguous range per CTA; stages chosen from the node tile.
 cudaError_t launch_gemm(int epi, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& a2,
                         const CUtensorMap& b, const GemmArgs& args, cudaStream_t st, bool pdl);
-size_t gemm_smem_bytes(int nt, int stages);
-int gemm_stages_for(int nt, size_t small_budget = 104 * 1024);
+size_t gemm_smem_bytes(int nt, int stages, int epi);
+// Ring depth for node tile nt and epilogue epi: the most stages (2..8) that fit the budget
+// (small node tiles) or the opt-in limit (the wide tiles of prefill).
+int gemm_stages_for(int nt, int epi, size_t small_budget = 104 * 1024);
 // k segments per 128-row tile for a weight of n_tiles tiles and kblocks k-blocks on a grid
 // of n_ctas CTAs (depends on nothing else, so results never depend on the batch).
 int gemm_segments(int n_tiles, int kblocks, int n_ctas);
