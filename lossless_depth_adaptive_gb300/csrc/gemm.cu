@@ -56,10 +56,12 @@ constexpr int kNtMax = 256;
 struct SmemMap {
   size_t a, b, bar, misc, xch, inv, qsum, qkey, total;
 };
-// Exchange area of the epilogue: 16 accumulator columns x 128 rows for the epilogues that
-// read across rows (QKV: RoPE partners; SWIGLU: gate/up halves), a small node table otherwise.
+// Exchange area of the epilogue: 16 accumulator columns x 128 rows (QKV: RoPE partners;
+// SWIGLU: gate/up halves; kept for the residual epilogues too, whose launches measured
+// slower with the extra ring stage a smaller area allows), a small node table for the exit
+// head (which gains a third ring stage at 64-node tiles).
 __host__ __device__ constexpr size_t xch_bytes(int epi) {
-  return (epi == EPI_QKV || epi == EPI_SWIGLU) ? static_cast<size_t>(16) * kBM * 4 : 512;
+  return epi == EPI_EXIT ? 512 : static_cast<size_t>(16) * kBM * 4;
 }
 __host__ __device__ inline SmemMap smem_map(int nt, int stages, int epi) {
   SmemMap m;
