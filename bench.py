@@ -249,6 +249,19 @@ def run_gpu(args):
     barrier()
     stats = dec.stats()
     launches = stats["kernel_launches"]
+    # ---- prefill alone (support path, not the timed metric): device time of the prompts ----
+    pe0, pe1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pe0.record(st)
+    prefill_all()
+    pe1.record(st)
+    pe1.synchronize()
+    prefill_ms = pe0.elapsed_time(pe1)
+    prefill_tok = B * (wl.prompt_len - 1)
+    qd, kvd = shape.n_heads * shape.head_dim, shape.n_kv_heads * shape.head_dim
+    layer_params = (qd + 2 * kvd) * shape.d_model + qd * shape.d_model + 3 * shape.d_ff * shape.d_model
+    # linear layers 2 * params per token, attention 4 * hd * H per (query, visible key)
+    P = wl.prompt_len - 1
+    prefill_flop = B * (2.0 * shape.n_layers * layer_params * P + 4.0 * shape.n_layers * qd * P * (P + 1) / 2)
     value = replica_throughput(args.steps * B * T, ms / 1000.0, world, dev)
     ms = max_over_ranks(ms)
     ms_per_step = ms / args.steps
@@ -323,6 +336,13 @@ def run_gpu(args):
                      "launches": inst["gemm_launches"], "bytes_per_launch": int(bytes_per_launch),
                      "ms_per_launch": inst["ms_gemm"] / max(1, inst["gemm_launches"])},
         "e2e": e2e,
+        "prefill": {"tokens": prefill_tok, "ms": round(prefill_ms, 2),
+                    "tokens_per_s": round(prefill_tok / (prefill_ms / 1e3), 1) if prefill_ms > 0 else None,
+                    "tflops": round(prefill_flop / (prefill_ms / 1e3) / 1e12, 1) if prefill_ms > 0 else None,
+                    "frac_of_bf16_peak": round(prefill_flop / (prefill_ms / 1e3) / 1e12 / bf16, 4)
+                    if prefill_ms > 0 else None,
+                    "note": "support path (not the metric): prompt positions 0..P-2 of every sequence, "
+                            "linear layers at 2 FLOP per weight and token plus causal attention"},
         "gpu_launches": launches,
         "clocks": clk.summary(),
     }

@@ -48,7 +48,10 @@ typedef enum dex_status {
   DEX_ECAPACITY = -4,  /* a sequence would exceed max_ctx or max_new */
   DEX_ETIMEOUT = -5,   /* a bounded device wait gave up (kernel reported a stalled pipeline) */
   DEX_ESTATE = -6,     /* call out of order (e.g. dex_step before dex_prefill) */
-  DEX_ENODEV = -7      /* no usable sm_103 device */
+  DEX_ENODEV = -7,     /* no usable sm_103 device */
+  DEX_ERANGE = -8      /* a linear layer's split-K partial sum was not finite or reached 2^30 in
+                          magnitude (the range of the exact fixed-point segment sum); the
+                          round's results are void, the handle stays usable */
 } dex_status;
 
 /* Model description (Llama-style pre-norm decoder, no biases, SwiGLU FFN, RoPE).

@@ -19,8 +19,8 @@ LIB_PATH = os.path.join(HERE, "_build", "libdex.so")
 
 LAYER_TENSORS = ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "wg", "wu", "wd")
 
-DEX_OK, DEX_EINVAL, DEX_ENOMEM, DEX_ECUDA, DEX_ECAPACITY, DEX_ETIMEOUT, DEX_ESTATE, DEX_ENODEV = \
-    0, -1, -2, -3, -4, -5, -6, -7
+DEX_OK, DEX_EINVAL, DEX_ENOMEM, DEX_ECUDA, DEX_ECAPACITY, DEX_ETIMEOUT, DEX_ESTATE, DEX_ENODEV, DEX_ERANGE = \
+    0, -1, -2, -3, -4, -5, -6, -7, -8
 
 
 class DexLibraryMissing(ImportError):

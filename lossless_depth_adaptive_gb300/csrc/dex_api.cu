@@ -15,6 +15,7 @@
 
 #include <algorithm>
 #include <chrono>
+#include <map>
 #include <memory>
 #include <mutex>
 #include <new>
@@ -105,6 +106,9 @@ struct dex_handle {
   float *hidden = nullptr, *ssq = nullptr, *exit_ssq = nullptr, *q = nullptr, *partial = nullptr,
         *attn_part = nullptr, *logits_dbg = nullptr;
   int32_t *counters = nullptr, *attn_counters = nullptr, *err = nullptr;
+  long long* acc64 = nullptr;   // fixed-point split-K tile sums (zero at rest)
+  bool red_sum = false;          // layer GEMMs of decode rounds sum k segments at L2 in fixed point
+  size_t acc_bytes = 0, counter_bytes = 0, attn_counter_bytes = 0;
   float2* rope = nullptr;
   unsigned long long* best = nullptr;
   const bf16** d_attn_norms = nullptr;
@@ -141,6 +145,9 @@ struct dex_handle {
   // host-side allocation-failure injection (DEX_FAIL_ALLOC_AT=k: the k-th allocation of
   // dex_init fails), for tests of the DEX_ENOMEM path
   int alloc_fail_at = 0, alloc_count = 0;
+  int prefill_rows = 256;        // prompt positions per prefill pass
+  int prefill_group_rows = 64;   // node rows per GEMM group of a prefill pass (the node tile)
+  std::map<std::pair<int, int>, int> prefill_segs;   // (tiles of a launch, k-blocks) -> segments
 
   // Releases everything the handle owns; runs on dex_free and on every failing dex_init.
   ~dex_handle() {
@@ -305,7 +312,8 @@ dex::GemmArgs base_args(dex_handle* h) {
 
 // Launch one grouped GEMM.  Every group has at most 256 node rows; nmax is the largest.
 int gemm(dex_handle* h, int epi, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& a2,
-         const CUtensorMap* bmaps, dex::GemmArgs a, int nmax, int64_t weight_bytes, int64_t act_bytes_per_row) {
+         const CUtensorMap* bmaps, dex::GemmArgs a, int nmax, int64_t weight_bytes, int64_t act_bytes_per_row,
+         bool layer_gemm = false) {
   if (nmax < 1 || nmax > 256) return DEX_ECAPACITY;
   a.nt = (nmax + 15) & ~15;
   a.n_ctas = h->gemm_ctas;
@@ -314,6 +322,16 @@ int gemm(dex_handle* h, int epi, const CUtensorMap& a0, const CUtensorMap& a1, c
     return DEX_ECAPACITY;
   a.tmem_cols = pow2_at_least(a.nt);
   a.stages = dex::gemm_stages_for(a.nt, epi, h->gemm_smem);
+  // A decoder whose lattice gives a sequence at most 16 nodes per round sums the k segments
+  // of its layer GEMMs at L2 in fixed point (no partial tiles to read back at the end of a
+  // launch); one with a wider lattice, the exit head, the adapters and prefill passes sum
+  // fp32 partial tiles in segment order.  The choice depends on the exploration set only,
+  // so a node's result is the same whatever its round, batch or launch.
+  a.acc = h->acc64;
+  a.sum_mode = (layer_gemm && h->red_sum) ? dex::SUM_FIXED_RED : dex::SUM_FP32;
+  if (a.sum_mode == dex::SUM_FIXED_RED &&
+      static_cast<size_t>(a.n_groups) * a.n_tiles * a.nt * 128 * sizeof(long long) > h->acc_bytes)
+    return DEX_ECAPACITY;   // cannot happen: acc covers N groups of the widest round
   cudaEvent_t e0 = nullptr, e1 = nullptr;
   if (h->timing == 2) {
     e0 = next_event(h);
@@ -343,10 +361,24 @@ int gemm(dex_handle* h, int epi, const CUtensorMap& a0, const CUtensorMap& a1, c
 
 // The decoder layers of every slot: per slot, grouped QKV+RoPE+KV write, lattice
 // attention, O + residual, gate/up + SwiGLU, down + residual over the slot's batches.
+// Prefill passes (prefill = true) carry several node groups of the same layer per launch;
+// their k segments follow the launch's own tile count (a prompt position's K/V may then
+// differ in the last bits from what a decode round would write for it; DEX and plain AR
+// decode from the same prefill, so their equality is unaffected), and the weights stay in
+// L2 for the groups that read them after the first.
 int run_layers(dex_handle* h, const Uploaded& u, const std::vector<Batch>& batches, const std::vector<Slot>& slots,
-               bool with_exit) {
+               bool with_exit, bool prefill = false) {
   const int qd = h->H * h->hd, kvd = h->KVH * h->hd;
   const int64_t d = h->d;
+  auto segments = [&](int decode_segs, int n_tiles, int kblocks, int ng) {
+    if (!prefill) return decode_segs;
+    const std::pair<int, int> key(n_tiles * ng, kblocks);
+    auto it = h->prefill_segs.find(key);
+    if (it != h->prefill_segs.end()) return it->second;
+    const int sg = dex::gemm_segments(n_tiles * ng, kblocks, h->gemm_ctas);
+    h->prefill_segs[key] = sg;
+    return sg;
+  };
   for (size_t j = 0; j < slots.size(); ++j) {
     const Slot& sl = slots[j];
     const int ng = static_cast<int>(sl.batch.size());
@@ -389,14 +421,15 @@ int run_layers(dex_handle* h, const Uploaded& u, const std::vector<Batch>& batch
     a.src_tiles0 = qd / 128;
     a.src_tiles1 = kvd / 128;
     a.n_tiles = (qd + 2 * kvd) / 128;
-    a.n_segs = h->seg_qkv;
+    a.n_segs = segments(h->seg_qkv, a.n_tiles, a.kblocks, ng);
+    a.evict_first = prefill ? 0 : 1;
     a.ssq_in = h->ssq;
     a.q_out = h->q;
     a.kv_commit = h->kv_commit;
     a.kv_pool = h->kv_pool;
     a.rope = h->rope;
     int rc = gemm(h, dex::EPI_QKV, h->tm_q[l_first], h->tm_k[l_first], h->tm_v[l_first], h->tm_hb, a, nmax,
-                  static_cast<int64_t>(qd + 2 * kvd) * d * 2, d * 4 + qd * 4 + 2 * kvd * 4);
+                  static_cast<int64_t>(qd + 2 * kvd) * d * 2, d * 4 + qd * 4 + 2 * kvd * 4, !prefill);
     if (rc) return rc;
     // lattice attention over every batch of the slot
     dex::AttnArgs at = {};
@@ -445,32 +478,35 @@ int run_layers(dex_handle* h, const Uploaded& u, const std::vector<Batch>& batch
     fill_groups(a, 1);
     a.kblocks = (qd + 63) / 64;
     a.n_tiles = h->d / 128;
-    a.n_segs = h->seg_o;
+    a.n_segs = segments(h->seg_o, a.n_tiles, a.kblocks, ng);
+    a.evict_first = prefill ? 0 : 1;
     a.src_tiles0 = a.n_tiles;
     a.hidden = h->hidden;
     a.hb_out = h->hb;
     a.ssq_out = h->ssq;
     rc = gemm(h, dex::EPI_RESID, h->tm_o[l_first], h->tm_o[l_first], h->tm_o[l_first], h->tm_attn, a, nmax,
-              static_cast<int64_t>(qd) * d * 2, qd * 4 + d * 8 + d * 4);
+              static_cast<int64_t>(qd) * d * 2, qd * 4 + d * 8 + d * 4, !prefill);
     if (rc) return rc;
     // gate/up + SwiGLU
     a = base_args(h);
     fill_groups(a, 2);
     a.kblocks = (h->d + 63) / 64;
     a.n_tiles = (h->dff + 63) / 64;
-    a.n_segs = h->seg_gu;
+    a.n_segs = segments(h->seg_gu, a.n_tiles, a.kblocks, ng);
+    a.evict_first = prefill ? 0 : 1;
     a.src_tiles0 = a.n_tiles;
     a.ssq_in = h->ssq;
     a.act_out = h->act;
     rc = gemm(h, dex::EPI_SWIGLU, h->tm_g[l_first], h->tm_u[l_first], h->tm_u[l_first], h->tm_hb, a, nmax,
-              static_cast<int64_t>(2) * h->dff * d * 2, d * 4 + h->dff * 4);
+              static_cast<int64_t>(2) * h->dff * d * 2, d * 4 + h->dff * 4, !prefill);
     if (rc) return rc;
     // down + residual (+ exit-head input at the stage boundary)
     a = base_args(h);
     fill_groups(a, 3);
     a.kblocks = (h->dff + 63) / 64;
     a.n_tiles = h->d / 128;
-    a.n_segs = h->seg_d;
+    a.n_segs = segments(h->seg_d, a.n_tiles, a.kblocks, ng);
+    a.evict_first = prefill ? 0 : 1;
     a.src_tiles0 = a.n_tiles;
     a.hidden = h->hidden;
     a.hb_out = h->hb;
@@ -479,7 +515,7 @@ int run_layers(dex_handle* h, const Uploaded& u, const std::vector<Batch>& batch
     a.g_final = h->final_norm;
     a.exit_ssq = h->exit_ssq;
     rc = gemm(h, dex::EPI_RESID, h->tm_d[l_first], h->tm_d[l_first], h->tm_d[l_first], h->tm_act, a, nmax,
-              static_cast<int64_t>(h->dff) * d * 2, h->dff * 4 + d * 8 + d * 8);
+              static_cast<int64_t>(h->dff) * d * 2, h->dff * 4 + d * 8 + d * 8, !prefill);
     if (rc) return rc;
   }
   return DEX_OK;
@@ -489,6 +525,11 @@ int check_device_error(dex_handle* h, int32_t flag) {
   if (flag == 0) return DEX_OK;
   if (debug_enabled()) fprintf(stderr, "dex: device error flag %d\n", flag);
   cudaMemsetAsync(h->err, 0, sizeof(int32_t), h->st);
+  // a launch that gave up may leave arrival counters and tile sums away from zero
+  cudaMemsetAsync(h->counters, 0, h->counter_bytes, h->st);
+  cudaMemsetAsync(h->attn_counters, 0, h->attn_counter_bytes, h->st);
+  cudaMemsetAsync(h->acc64, 0, h->acc_bytes, h->st);
+  if (flag == dex::DEV_RANGE) return DEX_ERANGE;
   return flag == dex::DEV_BAD_INDEX ? DEX_ECUDA : DEX_ETIMEOUT;
 }
 
@@ -893,6 +934,13 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
     if (cps < 1 || cps > 4 || kb < 32 || kb > 227) return DEX_EINVAL;
     h->gemm_ctas = h->n_sm * cps;
     h->gemm_smem = static_cast<size_t>(kb) * 1024;
+    // prompt positions per prefill pass and node rows per GEMM group of a pass: multiples of
+    // 16 in [16, 256], at most kMaxGroups groups per pass
+    if (const char* pr = getenv("DEX_PREFILL_ROWS")) h->prefill_rows = atoi(pr);
+    if (const char* pg = getenv("DEX_PREFILL_GROUP_ROWS")) h->prefill_group_rows = atoi(pg);
+    for (int v : {h->prefill_rows, h->prefill_group_rows})
+      if (v < 16 || v > 256 || (v & 15)) return DEX_EINVAL;
+    if ((h->prefill_rows + h->prefill_group_rows - 1) / h->prefill_group_rows > dex::kMaxGroups) return DEX_EINVAL;
   }
   h->lat.reset(new dex::Lattice(X, n_X, cfg->batch, cfg->decs != 0, cfg->max_branch));
   const int32_t XL[1] = {h->L};
@@ -951,22 +999,46 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
                                             static_cast<size_t>(2 * h->d / 128) * h->seg_ad1,
                                             static_cast<size_t>(t_o) * h->seg_ad2});
     const int nt_round = std::min(256, (std::max(1, h->lat->max_round_nodes()) + 15) & ~15);
-    h->partial_bytes = std::max({dex::gemm_partial_bytes(256, u_layer),
-                                 dex::gemm_partial_bytes(nt_round, u_layer * std::max(1, h->N)),
+    h->partial_bytes = std::max({dex::gemm_partial_bytes(nt_round, u_layer * std::max(1, h->N)),
                                  dex::gemm_partial_bytes(256, static_cast<size_t>(t_lm) * h->seg_lm)});
+    // prefill passes: 1..ng_max groups of prefill_group_rows rows, their own segment counts
+    const int ng_max = (h->prefill_rows + h->prefill_group_rows - 1) / h->prefill_group_rows;
+    const std::pair<int, int> ops[4] = {{t_qkv, kb_d}, {t_o, kb_q}, {t_gu, kb_d}, {t_o, kb_f}};
+    for (int ng = 1; ng <= ng_max; ++ng)
+      for (const auto& op : ops) {
+        const int sg = dex::gemm_segments(op.first * ng, op.second, h->gemm_ctas);
+        h->prefill_segs[std::make_pair(op.first * ng, op.second)] = sg;
+        h->partial_bytes = std::max(h->partial_bytes,
+                                    dex::gemm_partial_bytes(h->prefill_group_rows, static_cast<size_t>(op.first) * ng * sg));
+      }
+    // fixed-point tile sums of the layer launches (at most N groups of the widest round) when
+    // a sequence's round holds at most 16 nodes (2^(N-1) <= 16); DEX_SUM_FP32=1 keeps fp32
+    // partial tiles for every decoder
+    const char* fp32_only = getenv("DEX_SUM_FP32");
+    h->red_sum = h->N <= 5 && !(fp32_only && atoi(fp32_only) != 0);
+    const size_t t_layer = std::max<size_t>({static_cast<size_t>(t_qkv), static_cast<size_t>(t_o),
+                                             static_cast<size_t>(t_gu)});
+    h->acc_bytes = h->red_sum ? static_cast<size_t>(std::max(1, h->N)) * t_layer * nt_round * 128 * sizeof(long long)
+                              : 16;
     if (debug_enabled())
-      fprintf(stderr, "dex: segments qkv %d o %d gu %d down %d lm %d, partial workspace %.1f MB\n", h->seg_qkv,
-              h->seg_o, h->seg_gu, h->seg_d, h->seg_lm, h->partial_bytes / 1e6);
+      fprintf(stderr, "dex: segments qkv %d o %d gu %d down %d lm %d, partial workspace %.1f MB, %s layer sums\n",
+              h->seg_qkv, h->seg_o, h->seg_gu, h->seg_d, h->seg_lm, h->partial_bytes / 1e6,
+              h->red_sum ? "fixed-point (L2)" : "fp32 partial");
   }
-  if (dalloc(h, &h->partial, h->partial_bytes) || dalloc(h, &h->counters, ntiles_max * 4 * std::max(1, h->N)))
+  // arrival counters: one per (group, tile) of a launch, up to kMaxGroups groups
+  h->counter_bytes = ntiles_max * 4 * std::max(dex::kMaxGroups, h->N);
+  h->attn_counter_bytes = (static_cast<size_t>(B) * h->N + R) * KVH * 4;
+  if (dalloc(h, &h->partial, h->partial_bytes) || dalloc(h, &h->counters, h->counter_bytes) ||
+      dalloc(h, &h->acc64, h->acc_bytes))
     return DEX_ENOMEM;
   h->plan_cap = (R * sizeof(dex::DevNode) + R * 16 * 8 +
                  static_cast<size_t>(L) * (B * h->N + R + 8) * sizeof(dex::AttnItem) + 64 * 16 + 8192);
   if (dalloc(h, &h->d_plan, h->plan_cap)) return DEX_ENOMEM;
   if (halloc(h, &h->h_plan, h->plan_cap) || halloc(h, &h->h_best, (R + 1) * 8)) return DEX_ENOMEM;
   // zero-initialised state
-  cudaMemsetAsync(h->counters, 0, ntiles_max * 4 * std::max(1, h->N), h->st);
-  cudaMemsetAsync(h->attn_counters, 0, (static_cast<size_t>(B) * h->N + R) * KVH * 4, h->st);
+  cudaMemsetAsync(h->counters, 0, h->counter_bytes, h->st);
+  cudaMemsetAsync(h->attn_counters, 0, h->attn_counter_bytes, h->st);
+  cudaMemsetAsync(h->acc64, 0, h->acc_bytes, h->st);
   cudaMemsetAsync(h->err, 0, 16, h->st);
   cudaMemsetAsync(h->kv_commit, 0, B * L * 2 * KVH * ctx * hd * 2, h->st);
   cudaMemsetAsync(h->kv_pool, 0, B * h->n_slots * L * 2 * KVH * hd * 2, h->st);
@@ -1103,8 +1175,9 @@ int dex_prefill(dex_handle* h, int32_t seq, const int32_t* tokens, int32_t n_tok
   drop(h->pending_jobs);
   drop(h->pending_jobs_ar);
   const int P = n_tokens - 1;   // committed positions 0..P-1 get their KV here
-  for (int c0 = 0; c0 < P; c0 += 256) {
-    const int n = std::min(256, P - c0);
+  const int chunk = h->prefill_rows;
+  for (int c0 = 0; c0 < P; c0 += chunk) {
+    const int n = std::min(chunk, P - c0);
     RoundTables t;
     for (int i = 0; i < n; ++i) {
       dex::DevNode dn = {};
@@ -1119,19 +1192,30 @@ int dex_prefill(dex_handle* h, int32_t seq, const int32_t* tokens, int32_t n_tok
       dn.unmasked = 1;
       t.nodes.push_back(dn);
     }
-    std::vector<Batch> batches(1);
-    batches[0].off = 0;
-    batches[0].n = n;
-    batches[0].l0 = 0;
-    batches[0].l1 = h->L;
-    dex::AttnItem it = {};
-    it.seq = seq;
-    it.row_begin = 0;
-    it.row_end = n;
-    it.max_pos = c0 + n - 1;
-    it.max_cend = c0 + n;
-    it.n_groups = std::max(1, (dex::attn_bulk_end(it.max_pos) + dex::kAttnGroupPos - 1) / dex::kAttnGroupPos);
-    batches[0].items.push_back(it);
+    // GEMM groups of prefill_group_rows rows (the same layer's weights, read once from HBM
+    // and by the later groups from L2), attention items of one MMA pass each (rows x query
+    // heads per KV head <= 16): the (item, KV head) combinations spread over the grid, and
+    // early rows skip late key groups
+    const int rows_per_item = std::max(1, dex::kAttnPassQueries / (h->H / h->KVH));
+    std::vector<Batch> batches;
+    for (int g0 = 0; g0 < n; g0 += h->prefill_group_rows) {
+      Batch b;
+      b.off = g0;
+      b.n = std::min(h->prefill_group_rows, n - g0);
+      b.l0 = 0;
+      b.l1 = h->L;
+      for (int r0 = g0; r0 < g0 + b.n; r0 += rows_per_item) {
+        dex::AttnItem it = {};
+        it.seq = seq;
+        it.row_begin = r0;
+        it.row_end = std::min(g0 + b.n, r0 + rows_per_item);
+        it.max_pos = c0 + it.row_end - 1;
+        it.max_cend = c0 + it.row_end;
+        it.n_groups = std::max(1, (dex::attn_bulk_end(it.max_pos) + dex::kAttnGroupPos - 1) / dex::kAttnGroupPos);
+        b.items.push_back(it);
+      }
+      batches.push_back(std::move(b));
+    }
     const std::vector<Slot> slots = build_slots(batches, h->KVH, &t);
     Uploaded u;
     int rc = upload(h, t, &u);
@@ -1149,7 +1233,7 @@ int dex_prefill(dex_handle* h, int32_t seq, const int32_t* tokens, int32_t n_tok
     aa.best = nullptr;
     cudaError_t ce = dex::launch_assemble(aa, h->st, false);
     if (ce != cudaSuccess) return cuda_fail(h, ce);
-    rc = run_layers(h, u, batches, slots, false);
+    rc = run_layers(h, u, batches, slots, false, true);
     if (rc) return rc;
     // the upload buffer is reused by the next chunk: wait for this chunk
     if (cudaMemcpyAsync(h->h_best + h->rows_cap, h->err, 4, cudaMemcpyDeviceToHost, h->st) != cudaSuccess ||

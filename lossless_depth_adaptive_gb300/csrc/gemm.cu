@@ -53,15 +53,46 @@ constexpr int kBK = 64;
 constexpr uint32_t kABytes = kBM * kBK * 2;   // 16 KB weight tile per stage
 constexpr int kNtMax = 256;
 
+constexpr int kSumDepth = 2;   // partial tiles whose loads are in flight together in a segment sum
+
+// Split-K segment sums in 2^-32 fixed point: an fp32 partial p with |p| < 2^30 becomes the
+// integer nearest p * 2^32 (exact for |p| >= 2^-9, within 2^-33 absolute below), the
+// segments' integers add exactly in any order, and the total rounds once to fp32.  A
+// partial outside the range (or not finite) adds 0 and raises DEV_RANGE.
+constexpr float kFixScale = 4294967296.0f;            // 2^32
+constexpr float kFixInv = 2.3283064365386963e-10f;    // 2^-32
+constexpr float kFixLimit = 1073741824.0f;            // 2^30
+__device__ __forceinline__ long long to_fixed(float p, int32_t* err) {
+  if (!(fabsf(p) < kFixLimit)) {
+    atomicExch(err, DEV_RANGE);
+    return 0;
+  }
+  return __float2ll_rn(p * kFixScale);
+}
+__device__ __forceinline__ float from_fixed(long long q) { return __ll2float_rn(q) * kFixInv; }
+// fire-and-forget 64-bit add at L2 (two's complement: the unsigned add is the signed one)
+__device__ __forceinline__ void red_add_fixed(long long* p, long long v) {
+  asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(static_cast<unsigned long long>(v))
+               : "memory");
+}
+
 struct SmemMap {
   size_t a, b, bar, misc, xch, inv, qsum, qkey, total;
 };
-// Exchange area of the epilogue: 16 accumulator columns x 128 rows (QKV: RoPE partners;
-// SWIGLU: gate/up halves; kept for the residual epilogues too, whose launches measured
-// slower with the extra ring stage a smaller area allows), a small node table for the exit
-// head (which gains a third ring stage at 64-node tiles).
+// Exchange area of the epilogue: 16 accumulator columns x 128 rows (QKV: RoPE partners,
+// followed by the group's node table of positions and K/V destinations; SWIGLU: gate/up
+// halves; kept for the residual epilogues too, whose launches measured slower with the
+// extra ring stage a smaller area allows), a small node table for the exit head (which
+// gains a third ring stage at 64-node tiles).
+struct QkvNode {
+  long long base;   // element offset of the node's (K, head 0, dim 0) entry in its cache
+  int pos;          // input position (RoPE row)
+  int commit;       // 1: committed cache, 0: branch pool
+};
+static_assert(sizeof(QkvNode) == 16, "16-byte node table entries");
 __host__ __device__ constexpr size_t xch_bytes(int epi) {
-  return epi == EPI_EXIT ? 512 : static_cast<size_t>(16) * kBM * 4;
+  return epi == EPI_EXIT ? 512
+                         : static_cast<size_t>(16) * kBM * 4 + (epi == EPI_QKV ? kNtMax * sizeof(QkvNode) : 0);
 }
 __host__ __device__ inline SmemMap smem_map(int nt, int stages, int epi) {
   SmemMap m;
@@ -143,11 +174,19 @@ int gemm_segments(int n_tiles, int kblocks, int C) {
 
 // Two CTAs per SM must stay resident (the persistent grid is 2 x SMs): at most 170
 // registers per thread.
+// Epilogues that may take their k segments' sum from the fixed-point tile sums (the
+// decoder layers); the exit head and the adapters always sum fp32 partials.
+template <int EPI>
+__host__ __device__ constexpr bool red_sum_epi() {
+  return EPI == EPI_QKV || EPI == EPI_RESID || EPI == EPI_SWIGLU;
+}
+
 template <int EPI>
 __global__ void __launch_bounds__(kThreads, 2)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ GemmArgs a) {
+  constexpr bool kRedOk = red_sum_epi<EPI>();
   const int C = gridDim.x, cta = blockIdx.x;
   const int kb = a.kblocks, S = a.n_segs, nT = a.n_tiles;
   const int U = a.n_groups * nT * S;
@@ -362,58 +401,64 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (EPI == EPI_QKV) {
         const int f = lt * kBM + r;      // feature within the source (q, k or v)
         const int half = a.hd >> 1;
+        const QkvNode* ntab = reinterpret_cast<const QkvNode*>(xch + 16 * kBM);
 #pragma unroll
         for (int j = 0; j < 16; ++j) xch[j * kBM + r] = (c0 + j < n) ? v[j] * inv[c0 + j] : 0.0f;
         named_bar_sync(1, 128);
         const int head = f / a.hd, dim = f - head * a.hd;
+        // the chunk's RoPE factors, all loads issued before the arithmetic
+        float2 cs[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          cs[j] = make_float2(1.0f, 0.0f);
+          if (src != 2 && c0 + j < n)
+            cs[j] = __ldg(a.rope + static_cast<size_t>(ntab[c0 + j].pos) * half + (dim & (half - 1)));
+        }
+        const int kv = src - 1;
+        const size_t off_commit = static_cast<size_t>(kv * a.KVH + head) * a.max_ctx * a.hd + dim;
+        const size_t off_pool = static_cast<size_t>(kv * a.KVH + head) * a.hd + dim;
+#pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int c = c0 + j;
-          if (c >= n) break;
-          const DevNode* nd = a.nodes + b_row0 + c;
-          const float x = xch[j * kBM + r];
-          float out = x;
-          if (src != 2) {
-            const float y = xch[j * kBM + (r ^ half)];
-            const float2 cs = a.rope[static_cast<size_t>(nd->pos) * half + (dim & (half - 1))];
-            out = dim < half ? x * cs.x - y * cs.y : x * cs.x + y * cs.y;
-          }
-          if (src == 0) {
-            a.q_out[static_cast<size_t>(b_row0 + c) * (a.H * a.hd) + f] = out;
-          } else {
-            const int kv = src - 1;
-            __half* dst;
-            if (nd->kv_commit) {
-              dst = a.kv_commit +
-                    ((((static_cast<size_t>(nd->seq) * a.L + grp.layer) * 2 + kv) * a.KVH + head) * a.max_ctx +
-                     nd->pos) * a.hd + dim;
-            } else {
-              dst = a.kv_pool +
-                    ((((static_cast<size_t>(nd->seq) * a.n_slots + nd->slot) * a.L + grp.layer) * 2 + kv) * a.KVH +
-                     head) * a.hd + dim;
+          if (c < n) {
+            const float x = xch[j * kBM + r];
+            float out = x;
+            if (src != 2) {
+              const float y = xch[j * kBM + (r ^ half)];
+              out = dim < half ? x * cs[j].x - y * cs[j].y : x * cs[j].x + y * cs[j].y;
             }
-            *dst = __float2half_rn(out);   // the caches hold fp16 K/V
+            if (src == 0) {
+              a.q_out[static_cast<size_t>(b_row0 + c) * (a.H * a.hd) + f] = out;
+            } else {
+              const QkvNode nd = ntab[c];
+              __half* dst = nd.commit ? a.kv_commit + nd.base + off_commit : a.kv_pool + nd.base + off_pool;
+              *dst = __float2half_rn(out);   // the caches hold fp16 K/V
+            }
           }
         }
         named_bar_sync(1, 128);
       } else if (EPI == EPI_RESID) {
         const int f = lt * kBM + r;
+        const int* hrow = reinterpret_cast<const int*>(inv);
+        // every load of the chunk first: hidden state of the 16 nodes, the two gains
+        float hv[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          hv[j] = (c0 + j < n) ? a.hidden[static_cast<size_t>(hrow[c0 + j]) * a.d + f] : 0.0f;
+        const float gn = grp.has_next ? bf16_to_f32(grp.g_next[f]) : 0.0f;
+        const float ge = grp.stage_end ? bf16_to_f32((grp.g_exit ? grp.g_exit : a.g_final)[f]) : 0.0f;
         float sq[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int c = c0 + j;
           sq[j] = 0.0f;
           if (c < n) {
-            const DevNode* nd = a.nodes + b_row0 + c;
-            float* hp = a.hidden + static_cast<size_t>(nd->hrow) * a.d + f;
-            const float x = __fadd_rn(*hp, v[j]);
-            *hp = x;
+            const float x = __fadd_rn(hv[j], v[j]);
+            a.hidden[static_cast<size_t>(hrow[c]) * a.d + f] = x;
             const size_t o = static_cast<size_t>(b_row0 + c) * a.d + f;
             const size_t lo = static_cast<size_t>(a.plane_rows) * a.d;
-            if (grp.has_next) store_pair(a.hb_out + o, a.hb_out + lo + o, __fmul_rn(x, bf16_to_f32(grp.g_next[f])));
-            if (grp.stage_end) {
-              const __nv_bfloat16* gx = grp.g_exit ? grp.g_exit : a.g_final;
-              store_pair(a.exit_hb + o, a.exit_hb + lo + o, __fmul_rn(x, bf16_to_f32(gx[f])));
-            }
+            if (grp.has_next) store_pair(a.hb_out + o, a.hb_out + lo + o, __fmul_rn(x, gn));
+            if (grp.stage_end) store_pair(a.exit_hb + o, a.exit_hb + lo + o, __fmul_rn(x, ge));
             sq[j] = __fmul_rn(x, x);
           }
         }
@@ -468,8 +513,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           const int c = c0 + j;
           sq[j] = 0.0f;
           if (c < n) {
-            const DevNode* nd = a.nodes + b_row0 + c;
-            const float x = __fadd_rn(a.hidden[static_cast<size_t>(nd->hrow) * a.d + f],
+            const float x = __fadd_rn(a.hidden[static_cast<size_t>(reinterpret_cast<const int*>(inv)[c]) * a.d + f],
                                       __fmul_rn(grp.alpha, __fadd_rn(v[j], b2)));
             const size_t o = static_cast<size_t>(b_row0 + c) * a.d + f;
             store_pair(a.exit_hb + o, a.exit_hb + static_cast<size_t>(a.plane_rows) * a.d + o, __fmul_rn(x, gf));
@@ -569,6 +613,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int buf = ui & 1;
       int src, lt;
       tile_src(x.t, src, lt);
+      if ((EPI == EPI_RESID || EPI == EPI_ADDOWN) && x.g != g_inv) {   // hidden-state rows of the group's nodes
+        named_bar_sync(1, 128);                 // previous readers of the table are done
+        for (int c = ep; c < n; c += 128) reinterpret_cast<int*>(inv)[c] = a.nodes[grp.b_row0 + c].hrow;
+        g_inv = x.g;
+      }
       if (EPI != EPI_RESID && EPI != EPI_ADDOWN && x.g != g_inv) {   // RMSNorm scales of this group's node rows
         named_bar_sync(1, 128);                 // previous readers of inv[] are done
         for (int c = ep; c < n; c += 128) {
@@ -576,6 +625,18 @@ __global__ void __launch_bounds__(kThreads, 2)
           float t = sp[0];
           for (int j = 1; j < ndt; ++j) t = __fadd_rn(t, sp[j]);
           inv[c] = 1.0f / sqrtf(__fadd_rn(__fdiv_rn(t, static_cast<float>(a.d)), a.eps));
+          if (EPI == EPI_QKV) {   // where the node's K and V go, and its RoPE row
+            const DevNode* nd = a.nodes + grp.b_row0 + c;
+            QkvNode e;
+            e.pos = nd->pos;
+            e.commit = nd->kv_commit;
+            e.base = e.commit
+                         ? static_cast<long long>(((static_cast<size_t>(nd->seq) * a.L + grp.layer) * 2 * a.KVH) *
+                                                      a.max_ctx + e.pos) * a.hd
+                         : static_cast<long long>(((static_cast<size_t>(nd->seq) * a.n_slots + nd->slot) * a.L +
+                                                   grp.layer) * 2 * a.KVH) * a.hd;
+            reinterpret_cast<QkvNode*>(xch + 16 * kBM)[c] = e;
+          }
         }
         g_inv = x.g;
       }
@@ -600,38 +661,85 @@ __global__ void __launch_bounds__(kThreads, 2)
                            (static_cast<unsigned long long>(x.t & 0xffff) << 16);
         }
       } else {
-        // segment partial: [unit][row][nt] fp32, a thread's 16 columns are 64 contiguous bytes
-        const size_t tile_unit0 = (static_cast<size_t>(x.g) * nT + x.t) * S;   // unit of segment 0
-        float* part = a.partial + ((tile_unit0 + x.s) * kBM + r) * a.nt;
+        const size_t tile_id = static_cast<size_t>(x.g) * nT + x.t;
+        // tile sums (red path): column c of this thread's row at acc_row[c * kBM]
+        long long* acc_row = (kRedOk && a.sum_mode == SUM_FIXED_RED) ? a.acc + tile_id * a.nt * kBM + r : nullptr;
+        // segment partials: [unit][row][nt] fp32, a thread's 16 columns are 64 contiguous bytes
+        const size_t tile_unit0 = tile_id * S;   // unit of segment 0
         for (int c0 = 0; c0 < n; c0 += 16) {
           float v[16];
           tmem_ld16(taddr + static_cast<uint32_t>(c0), v);
-          float4* dst = reinterpret_cast<float4*>(part + c0);
+          if (kRedOk && acc_row) {
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) __stcg(dst + q4, make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]));
+            for (int j = 0; j < 16; ++j)
+              if (c0 + j < n) red_add_fixed(acc_row + static_cast<size_t>(c0 + j) * kBM, to_fixed(v[j], a.err));
+            if (EPI == EPI_RESID) {   // the residual rows the last arriver reads, while the arrival runs
+              const int* hrow = reinterpret_cast<const int*>(inv);
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (c0 + j < n) prefetch_l1(a.hidden + static_cast<size_t>(hrow[c0 + j]) * a.d + lt * kBM + r);
+            }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(a.partial + ((tile_unit0 + x.s) * kBM + r) * a.nt + c0);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              __stcg(dst + q4, make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]));
+          }
         }
         tc_fence_before();
         mbar_arrive(&tfree[buf]);
         __threadfence();
         named_bar_sync(1, 128);
-        int32_t* counter = a.counters + static_cast<size_t>(x.g) * nT + x.t;
+        int32_t* counter = a.counters + tile_id;
         if (ep == 0) sflag[0] = (atomicAdd(counter, 1) == S - 1) ? 1 : 0;
         named_bar_sync(1, 128);
         const unsigned long long t_arrived = rec ? clock64() : 0ull;
-        if (sflag[0]) {   // last of the tile's segments: sum the partials in segment order
+        if (!acc_row && sflag[0]) {   // last of the tile's segments: fp32 partials in segment order
+          // (the exit head's epilogue leaves registers for one partial tile in flight)
+          constexpr int kDepth = EPI == EPI_EXIT ? 1 : kSumDepth;
           __threadfence();
+          const size_t seg_f4 = static_cast<size_t>(kBM) * a.nt / 4;
+          const float4* prow = reinterpret_cast<const float4*>(a.partial + (tile_unit0 * kBM + r) * a.nt);
           for (int c0 = 0; c0 < n; c0 += 16) {
             float v[16];
-            for (int s2 = 0; s2 < S; ++s2) {
-              const float4* p =
-                  reinterpret_cast<const float4*>(a.partial + ((tile_unit0 + s2) * kBM + r) * a.nt + c0);
-              float4 q[4];
+            const float4* pc = prow + c0 / 4;
+            for (int s0 = 0; s0 < S; s0 += kDepth) {
+              float4 q[kDepth][4];
 #pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4) q[q4] = __ldcg(p + q4);
-              const float* qf = reinterpret_cast<const float*>(q);
+              for (int i = 0; i < kDepth; ++i)
+                if (s0 + i < S) {
 #pragma unroll
-              for (int j = 0; j < 16; ++j) v[j] = (s2 == 0) ? qf[j] : __fadd_rn(v[j], qf[j]);
+                  for (int q4 = 0; q4 < 4; ++q4) q[i][q4] = __ldcg(pc + (s0 + i) * seg_f4 + q4);
+                }
+#pragma unroll
+              for (int i = 0; i < kDepth; ++i)
+                if (s0 + i < S) {
+                  const bool first = (s0 + i == 0);
+#pragma unroll
+                  for (int q4 = 0; q4 < 4; ++q4) {
+                    v[4 * q4 + 0] = first ? q[i][q4].x : __fadd_rn(v[4 * q4 + 0], q[i][q4].x);
+                    v[4 * q4 + 1] = first ? q[i][q4].y : __fadd_rn(v[4 * q4 + 1], q[i][q4].y);
+                    v[4 * q4 + 2] = first ? q[i][q4].z : __fadd_rn(v[4 * q4 + 2], q[i][q4].z);
+                    v[4 * q4 + 3] = first ? q[i][q4].w : __fadd_rn(v[4 * q4 + 3], q[i][q4].w);
+                  }
+                }
             }
+            epilogue_chunk(grp, src, lt, c0, v);
+          }
+          if (ep == 0) *counter = 0;
+        } else if (kRedOk && sflag[0]) {   // last of the tile's segments: the exact fixed-point sum, then the epilogue
+          __threadfence();
+          for (int c0 = 0; c0 < n; c0 += 16) {
+            long long t64[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              t64[j] = (c0 + j < n) ? __ldcg(acc_row + static_cast<size_t>(c0 + j) * kBM) : 0ll;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (c0 + j < n) __stcg(acc_row + static_cast<size_t>(c0 + j) * kBM, 0ll);   // zero at rest
+            float v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = from_fixed(t64[j]);
             epilogue_chunk(grp, src, lt, c0, v);
           }
           if (ep == 0) *counter = 0;
@@ -704,6 +812,9 @@ cudaError_t launch_gemm(int epi, const CUtensorMap& a0, const CUtensorMap& a1, c
     any_end |= gr.stage_end != 0;
   }
   if (!args.err || !args.counters || !args.partial) return cudaErrorInvalidValue;
+  const bool red_ok = epi == EPI_QKV || epi == EPI_RESID || epi == EPI_SWIGLU;
+  if (args.sum_mode != SUM_FP32 && (args.sum_mode != SUM_FIXED_RED || !red_ok || !args.acc))
+    return cudaErrorInvalidValue;
   if (epi != EPI_RESID && epi != EPI_ADDOWN && !args.ssq_in) return cudaErrorInvalidValue;
   if (epi != EPI_SWIGLU && epi != EPI_ADUP && !args.nodes) return cudaErrorInvalidValue;
   if (epi == EPI_ADUP || epi == EPI_ADDOWN)

@@ -12,7 +12,7 @@ namespace dex {
 
 // Error flags written by kernels (read back by the host after each round).
 enum DevErr : int { DEV_OK = 0, DEV_TIMEOUT_FULL = 1, DEV_TIMEOUT_EMPTY = 2, DEV_TIMEOUT_ACC = 3,
-                    DEV_BAD_INDEX = 4 };
+                    DEV_BAD_INDEX = 4, DEV_RANGE = 5 };
 
 // One lattice node of the current round, as the kernels see it.  Node rows are ordered
 // by stage; the rows of stage s form one contiguous batch for that stage's layers, and
@@ -58,6 +58,7 @@ struct AttnItem {
 };
 
 // EPI_ADUP / EPI_ADDOWN: the two layers of an inducing adapter at a non-final exit.
+enum SumMode : int { SUM_FP32 = 0, SUM_FIXED_RED = 2 };
 enum Epi : int { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_EXIT = 3, EPI_ADUP = 4, EPI_ADDOWN = 5 };
 
 // One weight matrix of a grouped launch: a stage's layer and that stage's node rows.  The
@@ -89,6 +90,12 @@ struct GemmArgs {
   int32_t src_tiles0, src_tiles1;   // tiles of source 0 and 1 (source 2 takes the rest)
   int32_t tmem_cols;
   float* partial;       // [n_groups][n_tiles][n_segs][128][nt] fp32 segment partials
+  // How a tile's k segments are summed: SUM_FP32 -- fp32 partial tiles added in segment
+  // order; SUM_FIXED_RED (decoder-layer epilogues) -- each segment adds its
+  // partial at L2 (red.add) into acc in 2^-32 fixed point, where the sum is exact.  A
+  // decoder uses one of the two for every layer launch, so results do not depend on the batch.
+  int32_t sum_mode;
+  long long* acc;       // SUM_FIXED_RED: [n_groups][n_tiles][nt][128] int64, zero at rest
   int32_t* counters;    // [n_groups][n_tiles] arrival counters (left at 0)
   int32_t* err;         // device error flag
   const DevNode* nodes; // node rows (absolute)

@@ -3,11 +3,13 @@
     python -m lossless_depth_adaptive_gb300.profile_case --workload llama7b_x4 --tokens 8
     python -m lossless_depth_adaptive_gb300.profile_case --workload llama7b_x4 --layers 4 --tokens 2
     python -m lossless_depth_adaptive_gb300.profile_case --tokens 8 --adapters 0.001
+    python -m lossless_depth_adaptive_gb300.profile_case --layers 4 --prefill
 
 Builds the workload's seeded weights (optionally only the first ``--layers`` layers, with
 the exploration set rescaled to the same number of stages), prefills the prompt, runs
 ``--warmup`` untimed requests, then opens the CUDA profiler window for exactly one
-request's decode (``--tokens`` committed tokens) and closes it.
+request's decode (``--tokens`` committed tokens) and closes it; with ``--prefill`` the
+window holds the prompts' prefill instead.
 """
 from __future__ import annotations
 
@@ -37,6 +39,7 @@ def main():
                     help="seeded inducing adapters at the non-final exits with scalar gate GATE")
     ap.add_argument("--timeline", action="store_true",
                     help="record per-CTA GEMM clock records of the profiled request (needs DEX_TIMELINE=<file>)")
+    ap.add_argument("--prefill", action="store_true", help="profile the prompts' prefill instead of a decode")
     a = ap.parse_args()
     wl = di.workload(a.workload)
     shape, X = wl.shape, list(wl.X)
@@ -59,6 +62,21 @@ def main():
     for _ in range(a.warmup):
         prefill_all()
         dec.generate(ar=a.ar)
+    if a.prefill:
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.profiler.start()
+        e0.record()
+        prefill_all()
+        e1.record()
+        torch.cuda.synchronize()
+        torch.cuda.profiler.stop()
+        n = sum(len(p) - 1 for p in prompts)
+        ms = e0.elapsed_time(e1)
+        print(f"profiled prefill of {n} positions, layers {shape.n_layers}: {ms:.2f} ms, "
+              f"{n / ms * 1e3:.0f} positions/s")
+        dec.close()
+        return
     prefill_all()
     torch.cuda.synchronize()
     if a.timeline:
