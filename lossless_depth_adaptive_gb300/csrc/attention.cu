@@ -159,36 +159,32 @@ struct PassCursor {
   }
 };
 
-// Transposed butterfly over a warp for 16 values per lane: on return, lanes 2j and 2j+1 hold
-// the reduction over all 32 lanes of v[j] (16 shuffles instead of 16 separate 5-step
-// butterflies).  The combination tree is fixed by lane numbers, so sums are reproducible.
-template <bool kMax>
-__device__ __forceinline__ float warp_reduce16_transposed(const float (&v)[16], int lane) {
+// Transposed butterfly over a warp for K (4, 8 or 16) values per lane: on return, the 32/K
+// lanes 32j/K .. 32(j+1)/K - 1 hold the reduction over all 32 lanes of v[j] (K shuffles
+// plus five minus log2 K, instead of K separate 5-step butterflies).  Whatever K, every
+// lane's value is combined in the same tree -- pairs across lane bit 4, then bit 3, ...,
+// then bit 0 -- so a query's sum is the same bits in a pass of 4, 8 or 16 columns.
+template <int K, bool kMax>
+__device__ __forceinline__ float warp_reduce_transposed(const float (&v)[K], int lane) {
+  static_assert(K == 4 || K == 8 || K == 16, "4, 8 or 16 values per lane");
   auto op = [](float x, float y) { return kMax ? fmaxf(x, y) : __fadd_rn(x, y); };
-  float a8[8], a4[4], a2[2];
-  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+  float cur[K];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const float send = b4 ? v[k] : v[k + 8];
-    const float keep = b4 ? v[k + 8] : v[k];
-    a8[k] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+  for (int k = 0; k < K; ++k) cur[k] = v[k];
+  int bit = 16;
+#pragma unroll
+  for (int w = K; w > 1; w >>= 1, bit >>= 1) {   // halve the values across lane bit `bit`
+    const bool hi = lane & bit;
+#pragma unroll
+    for (int k = 0; k < w / 2; ++k) {
+      const float send = hi ? cur[k] : cur[k + w / 2];
+      const float keep = hi ? cur[k + w / 2] : cur[k];
+      cur[k] = op(keep, __shfl_xor_sync(0xffffffffu, send, bit));
+    }
   }
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float send = b3 ? a8[k] : a8[k + 4];
-    const float keep = b3 ? a8[k + 4] : a8[k];
-    a4[k] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
-  }
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const float send = b2 ? a4[k] : a4[k + 2];
-    const float keep = b2 ? a4[k + 2] : a4[k];
-    a2[k] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
-  }
-  const float send = b1 ? a2[0] : a2[1];
-  const float keep = b1 ? a2[1] : a2[0];
-  const float a1 = op(keep, __shfl_xor_sync(0xffffffffu, send, 2));
-  return op(a1, __shfl_xor_sync(0xffffffffu, a1, 1));
+  for (; bit >= 1; bit >>= 1) cur[0] = op(cur[0], __shfl_xor_sync(0xffffffffu, cur[0], bit));
+  return cur[0];
 }
 
 // Sum of the four accumulator chains of a product, hi and lo columns: for each query column
@@ -628,33 +624,40 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (sflag[1]) { aborted = true; break; }
       if (ut) ut[1] = global_timer_ns();
       tc_fence_after();
-      float s[kQT];
-      tmem_chain_sum(tmem_base + t_row, s);
+      float s16[kQT];
+      tmem_chain_sum(tmem_base + t_row, s16);
       const int key = g0 + r;
       float* rmax = red;
       float* rsum = red + 4 * kQT;
+      // the pass's first K >= nb query columns (the probability tile's other columns keep
+      // finite values from earlier passes; their outputs are never stored)
+      auto softmax = [&](auto kc) {
+        constexpr int K = decltype(kc)::value;
+        constexpr int LPQ = 32 / K;   // lanes holding one query's reduction
+        float s[K];
 #pragma unroll
-      for (int j = 0; j < kQT; ++j) s[j] = (j < nb && key < meta[b * kQT + j]) ? s[j] * a.scale_log2 : -INFINITY;
-      {
-        const float m = warp_reduce16_transposed<true>(s, lane);   // query lane / 2
-        if ((lane & 1) == 0) rmax[(lane >> 1) * 4 + lq] = m;        // [query][key quarter]
-      }
-      epi_sync();
-      float gm[kQT];
+        for (int j = 0; j < K; ++j) s[j] = (j < nb && key < meta[b * kQT + j]) ? s16[j] * a.scale_log2 : -INFINITY;
+        {
+          const float m = warp_reduce_transposed<K, true>(s, lane);
+          if ((lane & (LPQ - 1)) == 0) rmax[(lane / LPQ) * 4 + lq] = m;   // [query][key quarter]
+        }
+        epi_sync();
 #pragma unroll
-      for (int j = 0; j < kQT; ++j) {
-        const float4 m4 = *reinterpret_cast<const float4*>(rmax + j * 4);
-        gm[j] = fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w));
-        s[j] = (s[j] == -INFINITY) ? 0.0f : exp2f(s[j] - gm[j]);
-        __half h, l;
-        split_f16(s[j], h, l);
-        *reinterpret_cast<__half*>(ptile + sw_elem_off(j, r, 2 * kQT)) = h;
-        *reinterpret_cast<__half*>(ptile + sw_elem_off(kQT + j, r, 2 * kQT)) = l;
-      }
-      {
-        const float ps = warp_reduce16_transposed<false>(s, lane);
-        if ((lane & 1) == 0) rsum[(lane >> 1) * 4 + lq] = ps;
-      }
+        for (int j = 0; j < K; ++j) {
+          const float4 m4 = *reinterpret_cast<const float4*>(rmax + j * 4);
+          const float gmax = fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w));
+          s[j] = (s[j] == -INFINITY) ? 0.0f : exp2f(s[j] - gmax);
+          __half h, l;
+          split_f16(s[j], h, l);
+          *reinterpret_cast<__half*>(ptile + sw_elem_off(j, r, 2 * kQT)) = h;
+          *reinterpret_cast<__half*>(ptile + sw_elem_off(kQT + j, r, 2 * kQT)) = l;
+        }
+        const float ps = warp_reduce_transposed<K, false>(s, lane);
+        if ((lane & (LPQ - 1)) == 0) rsum[(lane / LPQ) * 4 + lq] = ps;
+      };
+      if (nb <= 4) softmax(std::integral_constant<int, 4>{});
+      else if (nb <= 8) softmax(std::integral_constant<int, 8>{});
+      else softmax(std::integral_constant<int, 16>{});
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(p_full);
@@ -682,7 +685,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       if (et < nb) {   // the query's max and its sum in key-quarter order
         float* pp = a.part + (static_cast<size_t>(qrec[b * kQT + et]) * a.part_slots + ur.g) * PS;
-        __stcg(pp + HD, gm[et]);
+        const float4 m4 = *reinterpret_cast<const float4*>(rmax + et * 4);
+        __stcg(pp + HD, fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w)));
         const float4 s4 = *reinterpret_cast<const float4*>(rsum + et * 4);
         __stcg(pp + HD + 1, __fadd_rn(__fadd_rn(s4.x, s4.y), __fadd_rn(s4.z, s4.w)));
       }
