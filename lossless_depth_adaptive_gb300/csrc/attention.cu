@@ -419,7 +419,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  griddep_wait();   // q and this round's K/V come from the preceding launch
+  // q and this round's K/V come from the preceding launch; the K/V producer of a decode
+  // round reads only keys committed in earlier rounds and starts without it
+  if (!(warp == 0 && a.early_kv)) griddep_wait();
   griddep_launch_dependents();
 
   if (warp == 0) {

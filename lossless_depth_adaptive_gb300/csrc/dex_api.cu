@@ -454,6 +454,7 @@ int run_layers(dex_handle* h, const Uploaded& u, const std::vector<Batch>& batch
     at.part_slots = h->max_groups + 1;
     at.plane_rows = h->rows_cap;
     at.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(h->hd)));
+    at.early_kv = prefill ? 0 : 1;
     cudaEvent_t ae0 = nullptr, ae1 = nullptr;
     if (h->timing == 2) {
       ae0 = next_event(h);

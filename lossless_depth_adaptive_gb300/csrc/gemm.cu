@@ -688,16 +688,21 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         tc_fence_before();
         mbar_arrive(&tfree[buf]);
-        __threadfence();
+        // arrival: the CTA barrier orders every thread's partial (or red) before one thread's
+        // gpu-scope acq_rel increment, which releases them to the last arriver and, for the
+        // last arriver, acquires the other segments' (the second barrier passes that on)
         named_bar_sync(1, 128);
         int32_t* counter = a.counters + tile_id;
-        if (ep == 0) sflag[0] = (atomicAdd(counter, 1) == S - 1) ? 1 : 0;
+        if (ep == 0) {
+          int prev;
+          asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(prev) : "l"(counter) : "memory");
+          sflag[0] = (prev == S - 1) ? 1 : 0;
+        }
         named_bar_sync(1, 128);
         const unsigned long long t_arrived = rec ? clock64() : 0ull;
         if (!acc_row && sflag[0]) {   // last of the tile's segments: fp32 partials in segment order
           // (the exit head's epilogue leaves registers for one partial tile in flight)
           constexpr int kDepth = EPI == EPI_EXIT ? 1 : kSumDepth;
-          __threadfence();
           const size_t seg_f4 = static_cast<size_t>(kBM) * a.nt / 4;
           const float4* prow = reinterpret_cast<const float4*>(a.partial + (tile_unit0 * kBM + r) * a.nt);
           for (int c0 = 0; c0 < n; c0 += 16) {
@@ -728,7 +733,6 @@ __global__ void __launch_bounds__(kThreads, 2)
           }
           if (ep == 0) *counter = 0;
         } else if (kRedOk && sflag[0]) {   // last of the tile's segments: the exact fixed-point sum, then the epilogue
-          __threadfence();
           for (int c0 = 0; c0 < n; c0 += 16) {
             long long t64[16];
 #pragma unroll

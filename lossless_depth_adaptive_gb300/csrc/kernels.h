@@ -154,6 +154,10 @@ struct AttnArgs {
   int32_t* err;
   int32_t H, KVH, hd, L, max_ctx, n_slots, part_slots;   // part_slots = key groups of max_ctx + 1
   float scale_log2;            // log2(e) / sqrt(hd)
+  // 1: every bulk key was committed before the launch's predecessor ran (a decode round:
+  // bulk keys precede the round's committed extent, and rounds are host-synchronised), so
+  // the K/V producer streams them without waiting for that kernel; 0 (prefill): it waits
+  int32_t early_kv;
   // diagnostics: per-CTA records of kAttnTimelineSlots words (globaltimer ns), or null:
   // [0] epilogue start, [1] epilogue end, [2] units, then per unit (first kAttnTimelineUnits)
   // query tile posted, scores seen, scores reduced, maxima shared, probabilities posted,
