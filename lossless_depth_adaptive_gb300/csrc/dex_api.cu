@@ -821,6 +821,7 @@ const char* dex_strerror(int code) {
     case DEX_ETIMEOUT: return "a bounded device wait timed out";
     case DEX_ESTATE: return "call out of order";
     case DEX_ENODEV: return "no sm_103 device";
+    case DEX_ERANGE: return "a split-K partial sum outside the fixed-point range (not finite or >= 2^30)";
     default: return "unknown error";
   }
 }
