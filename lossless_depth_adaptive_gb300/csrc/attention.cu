@@ -815,4 +815,321 @@ cudaError_t launch_attention(const CUtensorMap& tm, const AttnArgs& a, int n_cta
   return launch_attn_hd<64>(cfg, tm, a);
 }
 
+// ============================================================================================
+// Prefill: causal attention of a pass of consecutive prompt positions, flash-attention style
+// on the tensor cores.  A CTA takes 128 query rows (128 / G positions x the G query heads of
+// one KV head) against every key position up to its last row's, in 128-key tiles streamed
+// by TMA from the committed cache:
+//   S = [Qhi|Qlo] K^T      (M = 128 query rows, N = 128 keys; Q as an fp16 hi/lo pair)
+//   O += P V               (M = 128 query rows, N = head_dim; P fp16, V an MN-major operand)
+// One thread per query row reads its row of S from TMEM, so the softmax needs no exchange
+// between threads.  Two passes: the first takes each row's maximum over all its keys (from
+// Qhi alone -- any value near the maximum keeps the exponentials in range), the second
+// forms P = exp2(s - max) and accumulates O and the row sums, so O never needs rescaling.
+// Prefill numerics are shared by DEX and AR decoding, so they need not match a decode
+// round's bits.
+// ============================================================================================
+namespace {
+constexpr int kPfThreads = 192;   // producer, MMA issuer, four softmax warps
+constexpr int kPfStages = 2;
+
+template <int HD>
+struct PfSmem {
+  static constexpr uint32_t kTile = 128 * HD * 2;            // [128 rows][HD] fp16, HD/64 atoms of 16 KB
+  static constexpr uint32_t oQhi = 0, oQlo = kTile;
+  static constexpr uint32_t oP = 2 * kTile;                  // [128 rows][128 keys] fp16
+  static constexpr uint32_t oRing = oP + 128 * 128 * 2;      // stages of K then V
+  static constexpr uint32_t kStage = 2 * kTile;
+  static constexpr uint32_t oBar = oRing + kPfStages * kStage;
+  static constexpr uint32_t kTotal = oBar + (2 * kPfStages + 8) * 8 + 16 + 1024;
+};
+static_assert(PfSmem<128>::kTotal <= 227 * 1024, "prefill attention shared memory");
+
+__host__ __device__ constexpr uint32_t idesc_f16_f32_bmn(int M, int N) {   // A K-major, B MN-major
+  return (1u << 4) | (1u << 16) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+}  // namespace
+
+template <int HD>
+__global__ void __launch_bounds__(kPfThreads, 1)
+    attn_prefill_kernel(const __grid_constant__ CUtensorMap tmKV, const __grid_constant__ PrefillAttnArgs a) {
+  using SM = PfSmem<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::oBar);
+  uint64_t* empty = full + kPfStages;
+  uint64_t* s_full = empty + kPfStages;   // [2] scores of a tile in S[b]
+  uint64_t* s_free = s_full + 2;          // [2] S[b] read by every row
+  uint64_t* q_full = s_free + 2;          // query tiles written
+  uint64_t* p_full = q_full + 1;          // probability tile written
+  uint64_t* p_free = p_full + 1;          // probability tile consumed by its PV
+  uint64_t* o_full = p_free + 1;          // every PV complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_full + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = a.H / a.KVH, QP = 128 / G;   // query heads per KV head, positions per block
+  const int kvh = blockIdx.y;
+  const int p0 = blockIdx.x * QP;            // first node row (position index) of the block
+  const int np = min(QP, a.n_rows - p0);     // positions in the block
+  if (np <= 0) return;
+  const int max_pos = __ldg(&a.nodes[p0 + np - 1].pos);
+  const int nkt = max_pos / 128 + 1;         // key tiles 0 .. nkt-1
+
+  if (tid == 0) {
+    for (int s = 0; s < kPfStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&s_free[b], 128);
+    }
+    mbar_init(q_full, 128);
+    mbar_init(p_full, 128);
+    mbar_init(p_free, 1);
+    mbar_init(o_full, 1);
+    fence_mbar_init();
+    tma_prefetch(&tmKV);
+  }
+  // key rows past a tile's last loaded row keep finite values: zero the ring once
+  for (uint32_t o = SM::oRing + tid * 16; o < SM::oBar; o += kPfThreads * 16)
+    *reinterpret_cast<uint4*>(smem + o) = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);   // S[0], S[1]: 128 columns each; O: HD columns
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t t_s0 = tmem_base, t_o = tmem_base + 256;
+  griddep_wait();   // q and the pass's K/V come from the preceding launches
+  griddep_launch_dependents();
+
+  constexpr int KS = HD / 16;   // 16-dim k steps of QK^T
+  if (warp == 0) {
+    // ---------------- producer: K tiles (pass 1), then K and V tiles (pass 2) ----------------
+    if (lane == 0) {
+      const int row_k = (((a.seq * a.L + a.layer) * 2 + 0) * a.KVH + kvh) * a.max_ctx;
+      const int row_v = row_k + a.KVH * a.max_ctx;
+      bool ok = true;
+      int issued = 0;
+      for (int j = 0; j < 2 * nkt && ok; ++j) {
+        const int kt = j < nkt ? j : j - nkt;
+        const bool with_v = j >= nkt;
+        const int st = j % kPfStages;
+        if (j >= kPfStages &&
+            !mbar_wait(&empty[st], static_cast<uint32_t>((j / kPfStages) - 1) & 1u, a.err, DEV_TIMEOUT_EMPTY)) {
+          ok = false;
+          break;
+        }
+        const int nk = min(128, max_pos + 1 - kt * 128);   // keys of the tile any row can see
+        const int nbox = (nk + 31) / 32;
+        constexpr int halves = HD / 64;
+        mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>((with_v ? 2 : 1) * nbox * halves * 32 * 128));
+        uint8_t* sk = smem + SM::oRing + static_cast<size_t>(st) * SM::kStage;
+        for (int bx = 0; bx < nbox; ++bx) {
+#pragma unroll
+          for (int h = 0; h < halves; ++h) {
+            const uint32_t off = static_cast<uint32_t>(h * 128 * 128 + bx * 32 * 128);
+            tma_load_2d(sk + off, &tmKV, &full[st], h * 64, row_k + kt * 128 + bx * 32);
+            if (with_v) tma_load_2d(sk + SM::kTile + off, &tmKV, &full[st], h * 64, row_v + kt * 128 + bx * 32);
+          }
+        }
+        issued = j + 1;
+      }
+      if (!ok) {
+        for (int j = (issued > kPfStages ? issued - kPfStages : 0); j < issued; ++j)
+          mbar_wait(&full[j % kPfStages], static_cast<uint32_t>(j / kPfStages) & 1u, nullptr, 0);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      const uint32_t id_qk = idesc_f16_f32(128, 128, false);
+      const uint32_t id_pv = idesc_f16_f32_bmn(128, HD);
+      const uint32_t qhi = smem_u32(smem + SM::oQhi), qlo = smem_u32(smem + SM::oQlo);
+      const uint32_t pt = smem_u32(smem + SM::oP);
+      bool ok = mbar_wait(q_full, 0u, a.err, DEV_TIMEOUT_FULL);
+      for (int j = 0; j < 2 * nkt && ok; ++j) {
+        const bool pass2 = j >= nkt;
+        const int kt = pass2 ? j - nkt : j;
+        const int st = j % kPfStages, b = j & 1;
+        if (!mbar_wait(&full[st], static_cast<uint32_t>(j / kPfStages) & 1u, a.err, DEV_TIMEOUT_FULL)) break;
+        if (j >= 2 && !mbar_wait(&s_free[b], static_cast<uint32_t>((j >> 1) - 1) & 1u, a.err, DEV_TIMEOUT_ACC)) break;
+        tc_fence_after();
+        const uint32_t kt_s = smem_u32(smem + SM::oRing + static_cast<size_t>(st) * SM::kStage);
+        const uint32_t d_s = t_s0 + static_cast<uint32_t>(b) * 128;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          const uint32_t off = static_cast<uint32_t>((ks >> 2) * 128 * 128 + (ks & 3) * 32);
+          const uint64_t kdesc = sw128_kmajor_desc(kt_s + off);
+          umma_bf16(d_s, sw128_kmajor_desc(qhi + off), kdesc, id_qk, ks > 0 ? 1u : 0u);
+          if (pass2) umma_bf16(d_s, sw128_kmajor_desc(qlo + off), kdesc, id_qk, 1u);
+        }
+        umma_commit(&s_full[b]);
+        if (!pass2) {
+          umma_commit(&empty[st]);
+          continue;
+        }
+        if (!mbar_wait(p_full, static_cast<uint32_t>(kt) & 1u, a.err, DEV_TIMEOUT_FULL)) break;
+        tc_fence_after();
+        const uint32_t vt = kt_s + SM::kTile;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {   // 16 keys per step
+          const uint32_t off_p = static_cast<uint32_t>((ks >> 2) * 128 * 128 + (ks & 3) * 32);
+          umma_bf16(t_o, sw128_kmajor_desc(pt + off_p), sw128_mnmajor_desc(vt + ks * 16 * 128, 128 * 128, 1024),
+                    id_pv, (kt > 0 || ks > 0) ? 1u : 0u);
+        }
+        umma_commit(p_free);
+        umma_commit(&empty[st]);
+      }
+      umma_commit(o_full);
+    }
+  } else {
+    // ---------------- softmax: one query row per thread ----------------
+    const int lq = warp & 3;
+    const int r = lq * 32 + lane;                        // query row = TMEM lane
+    const uint32_t t_row = static_cast<uint32_t>(lq * 32) << 16;
+    const int pj = r / G, hq = kvh * G + r % G;          // position index in the block, query head
+    const bool valid = pj < np;
+    const int node = p0 + pj;
+    const int pos = valid ? __ldg(&a.nodes[node].pos) : -1;
+    // query tiles: fp16 hi/lo pair of the row's query
+    {
+      const float* qs = a.q + (static_cast<size_t>(node) * a.H + hq) * HD;
+#pragma unroll
+      for (int e = 0; e < HD; e += 8) {
+        __align__(16) __half h8[8], l8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float x = valid ? __ldcg(qs + e + k) : 0.0f;
+          split_f16(x, h8[k], l8[k]);
+        }
+        *reinterpret_cast<uint4*>(smem + SM::oQhi + sw_elem_off(r, e, 128)) = *reinterpret_cast<const uint4*>(h8);
+        *reinterpret_cast<uint4*>(smem + SM::oQlo + sw_elem_off(r, e, 128)) = *reinterpret_cast<const uint4*>(l8);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(q_full);
+    }
+    float m = -INFINITY, l = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < 2 * nkt && ok; ++j) {
+      const bool pass2 = j >= nkt;
+      const int kt = pass2 ? j - nkt : j;
+      const int b = j & 1;
+      if (!mbar_wait(&s_full[b], static_cast<uint32_t>(j >> 1) & 1u, a.err, DEV_TIMEOUT_ACC)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t taddr = t_s0 + static_cast<uint32_t>(b) * 128 + t_row;
+      const int k0 = kt * 128;
+      if (!pass2) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32_nowait(taddr + static_cast<uint32_t>(c * 32), v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (k0 + c * 32 + i <= pos) m = fmaxf(m, __uint_as_float(v[i]) * a.scale_log2);
+        }
+        tc_fence_before();
+        mbar_arrive(&s_free[b]);
+        continue;
+      }
+      // pass 2: P = exp2(s - m) for this tile's keys, the row sum over the fp16 values used
+      if (kt > 0 && !mbar_wait(p_free, static_cast<uint32_t>(kt - 1) & 1u, a.err, DEV_TIMEOUT_ACC)) {
+        ok = false;
+        break;
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32_nowait(taddr + static_cast<uint32_t>(c * 32), v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          __align__(16) __half p8[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int key = k0 + c * 32 + e + k;
+            const float pf = (key <= pos) ? exp2f(__uint_as_float(v[e + k]) * a.scale_log2 - m) : 0.0f;
+            p8[k] = __float2half_rn(pf);
+            l = __fadd_rn(l, __half2float(p8[k]));
+          }
+          *reinterpret_cast<uint4*>(smem + SM::oP + sw_elem_off(r, c * 32 + e, 128)) =
+              *reinterpret_cast<const uint4*>(p8);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&s_free[b]);
+      fence_proxy_async_smem();
+      mbar_arrive(p_full);
+    }
+    // output row: O / l as a bf16 hi/lo pair
+    if (ok && mbar_wait(o_full, 0u, a.err, DEV_TIMEOUT_ACC)) {
+      tc_fence_after();
+      const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;
+      const size_t lo = static_cast<size_t>(a.plane_rows) * a.H * HD;
+      const size_t o0 = (static_cast<size_t>(node) * a.H + hq) * HD;
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32_nowait(t_o + t_row + static_cast<uint32_t>(c * 32), v);
+        tmem_wait_ld();
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) store_pair(a.out + o0 + c * 32 + i, a.out + lo + o0 + c * 32 + i,
+                                                   __uint_as_float(v[i]) * inv);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+bool prefill_attention_supported(int H, int KVH, int hd) {
+  return (hd == 64 || hd == 128) && KVH > 0 && H % KVH == 0 && 128 % (H / KVH) == 0;
+}
+
+template <int HD>
+static cudaError_t launch_prefill_hd(cudaLaunchConfig_t cfg, const CUtensorMap& tm, const PrefillAttnArgs& a) {
+  static bool set = false;
+  cfg.dynamicSmemBytes = PfSmem<HD>::kTotal;
+  if (!set) {
+    cudaError_t e = cudaFuncSetAttribute(attn_prefill_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(cfg.dynamicSmemBytes));
+    if (e == cudaSuccess) e = apply_carveout(attn_prefill_kernel<HD>);
+    if (e != cudaSuccess) return e;
+    set = true;
+  }
+  return cudaLaunchKernelEx(&cfg, attn_prefill_kernel<HD>, tm, a);
+}
+
+cudaError_t launch_prefill_attention(const CUtensorMap& tm, const PrefillAttnArgs& a, cudaStream_t st, bool pdl) {
+  if (a.n_rows <= 0) return cudaSuccess;
+  if (!a.nodes || !a.q || !a.out || !a.err || a.plane_rows < a.n_rows || !prefill_attention_supported(a.H, a.KVH, a.hd))
+    return cudaErrorInvalidValue;
+  const int QP = 128 / (a.H / a.KVH);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((a.n_rows + QP - 1) / QP), static_cast<unsigned>(a.KVH));
+  cfg.blockDim = dim3(kPfThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (a.hd == 128) return launch_prefill_hd<128>(cfg, tm, a);
+  return launch_prefill_hd<64>(cfg, tm, a);
+}
+
 }  // namespace dex

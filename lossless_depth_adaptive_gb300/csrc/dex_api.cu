@@ -466,7 +466,28 @@ int run_layers(dex_handle* h, const Uploaded& u, const std::vector<Batch>& batch
       const int32_t meta[3] = {sl.n_items, sl.n_units, std::min(h->n_sm, sl.n_units)};
       h->atl_meta.insert(h->atl_meta.end(), meta, meta + 3);
     }
-    cudaError_t ce = dex::launch_attention(h->tm_kv, at, h->n_sm, h->st, true);
+    cudaError_t ce;
+    if (prefill && dex::prefill_attention_supported(h->H, h->KVH, h->hd)) {
+      // a prefill pass: consecutive positions of one sequence, rows 0 .. n-1 of the pass
+      dex::PrefillAttnArgs pa = {};
+      pa.nodes = u.nodes;
+      for (int bi : sl.batch) pa.n_rows = std::max(pa.n_rows, batches[bi].off + batches[bi].n);
+      pa.seq = batches[sl.batch[0]].items.empty() ? 0 : batches[sl.batch[0]].items[0].seq;
+      pa.layer = batches[sl.batch[0]].l0 + static_cast<int>(j);
+      pa.q = h->q;
+      pa.out = h->attn_out;
+      pa.plane_rows = h->rows_cap;
+      pa.err = h->err;
+      pa.H = h->H;
+      pa.KVH = h->KVH;
+      pa.hd = h->hd;
+      pa.L = h->L;
+      pa.max_ctx = h->cfg.max_ctx;
+      pa.scale_log2 = at.scale_log2;
+      ce = dex::launch_prefill_attention(h->tm_kv, pa, h->st, true);
+    } else {
+      ce = dex::launch_attention(h->tm_kv, at, h->n_sm, h->st, true);
+    }
     if (ce != cudaSuccess) return cuda_fail(h, ce);
     if (h->timing == 2) {
       cudaEventRecord(ae1, h->st);

@@ -164,6 +164,20 @@ struct AttnArgs {
   // output seen, partials written, unit counted; then up to four combinations (start, end)
   unsigned long long* timeline;
 };
+// Causal attention of one prefill pass: the pass's node rows are consecutive prompt
+// positions of one sequence whose K/V (every position up to the row's own) are in the
+// committed cache.  One CTA per (block of 128 query rows, KV head): rows are position-major,
+// 128 / G positions x the G query heads of the KV head.
+struct PrefillAttnArgs {
+  const DevNode* nodes;        // the pass's node rows 0 .. n_rows-1 (positions in .pos)
+  int32_t n_rows, seq, layer;
+  const float* q;              // [rows][H*hd]
+  __nv_bfloat16* out;          // [2][plane_rows][H*hd] hi/lo pair
+  int32_t plane_rows;
+  int32_t* err;
+  int32_t H, KVH, hd, L, max_ctx;
+  float scale_log2;            // log2(e) / sqrt(hd)
+};
 constexpr int kAttnTimelineUnits = 12;
 constexpr int kAttnTimelineSlots = 3 + 8 * kAttnTimelineUnits + 8;
 
@@ -228,6 +242,10 @@ inline cudaError_t apply_carveout(F* func) {
 // Persistent launch over min(n_units, n_ctas) CTAs (one per SM); items with more than
 // kAttnPassQueries queries take several passes.
 cudaError_t launch_attention(const CUtensorMap& tm_kv, const AttnArgs& a, int n_ctas, cudaStream_t st, bool pdl);
+// false when the shape has no prefill kernel (head_dim not 64/128, or 128 not a multiple of
+// the query heads per KV head): prefill passes then use launch_attention.
+bool prefill_attention_supported(int H, int KVH, int hd);
+cudaError_t launch_prefill_attention(const CUtensorMap& tm_kv, const PrefillAttnArgs& a, cudaStream_t st, bool pdl);
 cudaError_t launch_assemble(const AssembleArgs& a, cudaStream_t st, bool pdl);
 cudaError_t launch_collapse(const CollapseArgs& a, cudaStream_t st, bool pdl);
 // bf16 [n][d] rows -> hi/lo pair of h * g ([2][plane_rows][d]) and partial sums of squares
