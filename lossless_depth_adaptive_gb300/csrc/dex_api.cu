@@ -313,7 +313,7 @@ dex::GemmArgs base_args(dex_handle* h) {
 // Launch one grouped GEMM.  Every group has at most 256 node rows; nmax is the largest.
 int gemm(dex_handle* h, int epi, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& a2,
          const CUtensorMap* bmaps, dex::GemmArgs a, int nmax, int64_t weight_bytes, int64_t act_bytes_per_row,
-         bool layer_gemm = false) {
+         bool layer_gemm = false, size_t smem_budget = 0) {
   if (nmax < 1 || nmax > 256) return DEX_ECAPACITY;
   a.nt = (nmax + 15) & ~15;
   a.n_ctas = h->gemm_ctas;
@@ -321,7 +321,7 @@ int gemm(dex_handle* h, int epi, const CUtensorMap& a0, const CUtensorMap& a1, c
       dex::gemm_partial_bytes(a.nt, static_cast<size_t>(a.n_groups) * a.n_tiles * a.n_segs) > h->partial_bytes)
     return DEX_ECAPACITY;
   a.tmem_cols = pow2_at_least(a.nt);
-  a.stages = dex::gemm_stages_for(a.nt, epi, h->gemm_smem);
+  a.stages = dex::gemm_stages_for(a.nt, epi, smem_budget ? smem_budget : h->gemm_smem);
   // A decoder whose lattice gives a sequence at most 16 nodes per round sums the k segments
   // of its layer GEMMs at L2 in fixed point (no partial tiles to read back at the end of a
   // launch); one with a wider lattice, the exit head, the adapters and prefill passes sum
@@ -358,6 +358,10 @@ int gemm(dex_handle* h, int epi, const CUtensorMap& a0, const CUtensorMap& a1, c
   h->stats.gemm_bytes += weight_bytes * a.n_groups + act_bytes_per_row * rows;
   return DEX_OK;
 }
+
+// Prefill passes (node tile 64) give each GEMM CTA a third ring stage: 113 KB keeps two CTAs
+// per SM (228 KB per SM, 1 KB reserved per CTA).
+constexpr size_t kPrefillGemmSmem = 113 * 1024;
 
 // The decoder layers of every slot: per slot, grouped QKV+RoPE+KV write, lattice
 // attention, O + residual, gate/up + SwiGLU, down + residual over the slot's batches.
@@ -429,7 +433,8 @@ int run_layers(dex_handle* h, const Uploaded& u, const std::vector<Batch>& batch
     a.kv_pool = h->kv_pool;
     a.rope = h->rope;
     int rc = gemm(h, dex::EPI_QKV, h->tm_q[l_first], h->tm_k[l_first], h->tm_v[l_first], h->tm_hb, a, nmax,
-                  static_cast<int64_t>(qd + 2 * kvd) * d * 2, d * 4 + qd * 4 + 2 * kvd * 4, !prefill);
+                  static_cast<int64_t>(qd + 2 * kvd) * d * 2, d * 4 + qd * 4 + 2 * kvd * 4, !prefill,
+              prefill ? kPrefillGemmSmem : 0);
     if (rc) return rc;
     // lattice attention over every batch of the slot
     dex::AttnArgs at = {};
@@ -507,7 +512,8 @@ int run_layers(dex_handle* h, const Uploaded& u, const std::vector<Batch>& batch
     a.hb_out = h->hb;
     a.ssq_out = h->ssq;
     rc = gemm(h, dex::EPI_RESID, h->tm_o[l_first], h->tm_o[l_first], h->tm_o[l_first], h->tm_attn, a, nmax,
-              static_cast<int64_t>(qd) * d * 2, qd * 4 + d * 8 + d * 4, !prefill);
+              static_cast<int64_t>(qd) * d * 2, qd * 4 + d * 8 + d * 4, !prefill,
+              prefill ? kPrefillGemmSmem : 0);
     if (rc) return rc;
     // gate/up + SwiGLU
     a = base_args(h);
@@ -520,7 +526,8 @@ int run_layers(dex_handle* h, const Uploaded& u, const std::vector<Batch>& batch
     a.ssq_in = h->ssq;
     a.act_out = h->act;
     rc = gemm(h, dex::EPI_SWIGLU, h->tm_g[l_first], h->tm_u[l_first], h->tm_u[l_first], h->tm_hb, a, nmax,
-              static_cast<int64_t>(2) * h->dff * d * 2, d * 4 + h->dff * 4, !prefill);
+              static_cast<int64_t>(2) * h->dff * d * 2, d * 4 + h->dff * 4, !prefill,
+              prefill ? kPrefillGemmSmem : 0);
     if (rc) return rc;
     // down + residual (+ exit-head input at the stage boundary)
     a = base_args(h);
@@ -537,7 +544,8 @@ int run_layers(dex_handle* h, const Uploaded& u, const std::vector<Batch>& batch
     a.g_final = h->final_norm;
     a.exit_ssq = h->exit_ssq;
     rc = gemm(h, dex::EPI_RESID, h->tm_d[l_first], h->tm_d[l_first], h->tm_d[l_first], h->tm_act, a, nmax,
-              static_cast<int64_t>(h->dff) * d * 2, h->dff * 4 + d * 8 + d * 8, !prefill);
+              static_cast<int64_t>(h->dff) * d * 2, h->dff * 4 + d * 8 + d * 8, !prefill,
+              prefill ? kPrefillGemmSmem : 0);
     if (rc) return rc;
   }
   return DEX_OK;
