@@ -116,7 +116,8 @@ struct dex_handle {
   size_t plan_cap = 0;
   // pinned host
   uint8_t* h_plan = nullptr;
-  unsigned long long* h_best = nullptr;   // rows_cap + 1 (last = error flag)
+  // pinned copy of the device flag + best keys: [0..1] the error flag, [2 ..] best keys
+  unsigned long long* h_best = nullptr;
   // packed GEMM weights (one swizzled 16 KB box per (tile, k-block), tile-major)
   std::vector<const uint8_t*> pk_qkv, pk_o, pk_gu, pk_d;
   const uint8_t* pk_lm = nullptr;
@@ -676,7 +677,7 @@ int run_round(dex_handle* h, dex::Lattice* lat, std::vector<dex_copy_job>* pendi
   aa.plane_rows = h->rows_cap;
   aa.ssq = h->ssq;
   aa.best = h->best;
-  cudaError_t ce = dex::launch_assemble(aa, h->st, false);
+  cudaError_t ce = dex::launch_assemble(aa, h->st, !t.jobs.empty());   // overlaps the collapse's tail
   if (ce != cudaSuccess) return cuda_fail(h, ce);
   h->stats.kernel_launches++;
   rc = run_layers(h, u, batches, slots, true);
@@ -756,18 +757,16 @@ int run_round(dex_handle* h, dex::Lattice* lat, std::vector<dex_copy_job>* pendi
   }
   if (ev[3]) cudaEventRecord(ev[3], h->st);
   // tokens (and the device error flag) back to the host: the round's only sync
-  if (cudaMemcpyAsync(h->h_best, h->best, n * sizeof(unsigned long long), cudaMemcpyDeviceToHost, h->st) !=
-          cudaSuccess ||
-      cudaMemcpyAsync(h->h_best + h->rows_cap, h->err, sizeof(int32_t), cudaMemcpyDeviceToHost, h->st) !=
-          cudaSuccess)
+  if (cudaMemcpyAsync(h->h_best, h->err, (n + 2) * sizeof(unsigned long long), cudaMemcpyDeviceToHost, h->st) !=
+      cudaSuccess)
     return cuda_fail(h, cudaGetLastError());
   if (cudaStreamSynchronize(h->st) != cudaSuccess) return cuda_fail(h, cudaGetLastError());
-  h->stats.d2h_bytes += n * 8 + 4;
-  const int32_t dev_err = static_cast<int32_t>(h->h_best[h->rows_cap] & 0xffffffffull);
+  h->stats.d2h_bytes += (n + 2) * 8;
+  const int32_t dev_err = static_cast<int32_t>(h->h_best[0] & 0xffffffffull);
   if (dev_err) return check_device_error(h, dev_err);
   auto t_host1 = std::chrono::steady_clock::now();
   std::vector<int32_t> tokens(n);
-  for (int k = 0; k < n; ++k) tokens[k] = static_cast<int32_t>(~static_cast<uint32_t>(h->h_best[k] & 0xffffffffull));
+  for (int k = 0; k < n; ++k) tokens[k] = static_cast<int32_t>(~static_cast<uint32_t>(h->h_best[2 + k] & 0xffffffffull));
   std::vector<int32_t> committed(lat->batch()), kstar(lat->batch());
   lat->update(plan, tokens.data(), committed.data(), kstar.data(), pending);
   // statistics
@@ -1001,8 +1000,16 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
   rc |= dalloc(h, &h->attn_part, R * h->H * (h->max_groups + 1) * (hd + 2) * 4);
   rc |= dalloc(h, &h->attn_counters, (static_cast<size_t>(B) * h->N + R) * KVH * 4);
   rc |= dalloc(h, &h->rope, ctx * (hd / 2) * sizeof(float2));
-  rc |= dalloc(h, &h->best, (R + 1) * 8);
-  rc |= dalloc(h, &h->err, 16);
+  // the device error flag (16 bytes), then the best keys [R]: one copy of the first n + 2
+  // words per round brings the flag and the round's tokens back together
+  {
+    unsigned long long* base = nullptr;
+    rc |= dalloc(h, &base, (R + 2) * 8);
+    if (base) {
+      h->err = reinterpret_cast<int32_t*>(base);
+      h->best = base + 2;
+    }
+  }
   rc |= dalloc(h, &h->d_attn_norms, L * sizeof(void*));
   if (cfg->debug_logits) rc |= dalloc(h, &h->logits_dbg, R * static_cast<size_t>(h->V) * 4);
   if (rc) return DEX_ENOMEM;
@@ -1065,7 +1072,7 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
   h->plan_cap = (R * sizeof(dex::DevNode) + R * 16 * 8 +
                  static_cast<size_t>(L) * (B * h->N + R + 8) * sizeof(dex::AttnItem) + 64 * 16 + 8192);
   if (dalloc(h, &h->d_plan, h->plan_cap)) return DEX_ENOMEM;
-  if (halloc(h, &h->h_plan, h->plan_cap) || halloc(h, &h->h_best, (R + 1) * 8)) return DEX_ENOMEM;
+  if (halloc(h, &h->h_plan, h->plan_cap) || halloc(h, &h->h_best, (R + 2) * 8)) return DEX_ENOMEM;
   // zero-initialised state
   cudaMemsetAsync(h->counters, 0, h->counter_bytes, h->st);
   cudaMemsetAsync(h->attn_counters, 0, h->attn_counter_bytes, h->st);
@@ -1267,10 +1274,10 @@ int dex_prefill(dex_handle* h, int32_t seq, const int32_t* tokens, int32_t n_tok
     rc = run_layers(h, u, batches, slots, false, true);
     if (rc) return rc;
     // the upload buffer is reused by the next chunk: wait for this chunk
-    if (cudaMemcpyAsync(h->h_best + h->rows_cap, h->err, 4, cudaMemcpyDeviceToHost, h->st) != cudaSuccess ||
+    if (cudaMemcpyAsync(h->h_best, h->err, 4, cudaMemcpyDeviceToHost, h->st) != cudaSuccess ||
         cudaStreamSynchronize(h->st) != cudaSuccess)
       return cuda_fail(h, cudaGetLastError());
-    const int32_t dev_err = static_cast<int32_t>(h->h_best[h->rows_cap] & 0xffffffffull);
+    const int32_t dev_err = static_cast<int32_t>(h->h_best[0] & 0xffffffffull);
     if (dev_err) return check_device_error(h, dev_err);
     // per-launch timings cover decode rounds only: drop the prefill's events
     h->gemm_events.clear();
@@ -1411,11 +1418,11 @@ int dex_selftest_stall(dex_handle* h, int32_t limit_us) {
   if (cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(stall_probe_kernel), args) != cudaSuccess)
     return cuda_fail(h, cudaGetLastError());
   // the same read-back and check as the end of a decode round
-  if (cudaMemcpyAsync(h->h_best + h->rows_cap, h->err, sizeof(int32_t), cudaMemcpyDeviceToHost, h->st) !=
+  if (cudaMemcpyAsync(h->h_best, h->err, sizeof(int32_t), cudaMemcpyDeviceToHost, h->st) !=
           cudaSuccess ||
       cudaStreamSynchronize(h->st) != cudaSuccess)
     return cuda_fail(h, cudaGetLastError());
-  const int32_t flag = static_cast<int32_t>(h->h_best[h->rows_cap] & 0xffffffffull);
+  const int32_t flag = static_cast<int32_t>(h->h_best[0] & 0xffffffffull);
   return check_device_error(h, flag);
 }
 
