@@ -322,7 +322,12 @@ int gemm(dex_handle* h, int epi, const CUtensorMap& a0, const CUtensorMap& a1, c
       dex::gemm_partial_bytes(a.nt, static_cast<size_t>(a.n_groups) * a.n_tiles * a.n_segs) > h->partial_bytes)
     return DEX_ECAPACITY;
   a.tmem_cols = pow2_at_least(a.nt);
-  a.stages = dex::gemm_stages_for(a.nt, epi, smem_budget ? smem_budget : h->gemm_smem);
+  a.stages = dex::gemm_stages_for(a.nt, epi, h->gemm_smem);
+  if (smem_budget) {   // a fixed budget for every node tile (two CTAs per SM), when two stages fit it
+    int st = 8;
+    while (st > 2 && dex::gemm_smem_bytes(a.nt, st, epi) > smem_budget) --st;
+    if (dex::gemm_smem_bytes(a.nt, st, epi) <= smem_budget) a.stages = st;
+  }
   // A decoder whose lattice gives a sequence at most 16 nodes per round sums the k segments
   // of its layer GEMMs at L2 in fixed point (no partial tiles to read back at the end of a
   // launch); one with a wider lattice, the exit head, the adapters and prefill passes sum
@@ -360,8 +365,8 @@ int gemm(dex_handle* h, int epi, const CUtensorMap& a0, const CUtensorMap& a1, c
   return DEX_OK;
 }
 
-// Prefill passes (node tile 64) give each GEMM CTA a third ring stage: 113 KB keeps two CTAs
-// per SM (228 KB per SM, 1 KB reserved per CTA).
+// Shared-memory budget of a prefill pass's GEMM CTAs: 113 KB keeps two CTAs per SM (228 KB
+// per SM, 1 KB reserved per CTA) -- three ring stages at node tile 64, two at 128.
 constexpr size_t kPrefillGemmSmem = 113 * 1024;
 
 // The decoder layers of every slot: per slot, grouped QKV+RoPE+KV write, lattice
