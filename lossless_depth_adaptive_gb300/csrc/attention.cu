@@ -998,15 +998,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int pos = valid ? __ldg(&a.nodes[node].pos) : -1;
     // query tiles: fp16 hi/lo pair of the row's query
     {
-      const float* qs = a.q + (static_cast<size_t>(node) * a.H + hq) * HD;
-#pragma unroll
+      const float4* qs = reinterpret_cast<const float4*>(a.q + (static_cast<size_t>(node) * a.H + hq) * HD);
+#pragma unroll 4
       for (int e = 0; e < HD; e += 8) {
         __align__(16) __half h8[8], l8[8];
+        const float4 x0 = valid ? __ldcg(qs + e / 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 x1 = valid ? __ldcg(qs + e / 4 + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float x = valid ? __ldcg(qs + e + k) : 0.0f;
-          split_f16(x, h8[k], l8[k]);
-        }
+        for (int k = 0; k < 8; ++k) split_f16(xs[k], h8[k], l8[k]);
         *reinterpret_cast<uint4*>(smem + SM::oQhi + sw_elem_off(r, e, 128)) = *reinterpret_cast<const uint4*>(h8);
         *reinterpret_cast<uint4*>(smem + SM::oQlo + sw_elem_off(r, e, 128)) = *reinterpret_cast<const uint4*>(l8);
       }
@@ -1080,10 +1080,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         uint32_t v[32];
         tmem_ld32_nowait(t_o + t_row + static_cast<uint32_t>(c * 32), v);
         tmem_wait_ld();
-        if (valid) {
+        if (valid) {   // the row's bf16 hi/lo pairs, eight values per 16-byte store
 #pragma unroll
-          for (int i = 0; i < 32; ++i) store_pair(a.out + o0 + c * 32 + i, a.out + lo + o0 + c * 32 + i,
-                                                   __uint_as_float(v[i]) * inv);
+          for (int i = 0; i < 32; i += 8) {
+            __align__(16) __nv_bfloat16 h8[8], l8[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const float x = __uint_as_float(v[i + k]) * inv;
+              h8[k] = __float2bfloat16_rn(x);
+              l8[k] = __float2bfloat16_rn(__fsub_rn(x, __bfloat162float(h8[k])));
+            }
+            *reinterpret_cast<uint4*>(a.out + o0 + c * 32 + i) = *reinterpret_cast<const uint4*>(h8);
+            *reinterpret_cast<uint4*>(a.out + lo + o0 + c * 32 + i) = *reinterpret_cast<const uint4*>(l8);
+          }
         }
       }
     }

@@ -67,6 +67,8 @@ int pow2_at_least(int x) {
 
 }  // namespace
 
+constexpr int kPrefillRowsMax = 512;   // most prompt positions per prefill pass (rows of the scratch planes)
+
 struct dex_handle {
   // model
   int L = 0, d = 0, H = 0, KVH = 0, hd = 0, dff = 0, V = 0;
@@ -146,7 +148,7 @@ struct dex_handle {
   // host-side allocation-failure injection (DEX_FAIL_ALLOC_AT=k: the k-th allocation of
   // dex_init fails), for tests of the DEX_ENOMEM path
   int alloc_fail_at = 0, alloc_count = 0;
-  int prefill_rows = 256;        // prompt positions per prefill pass
+  int prefill_rows = kPrefillRowsMax;   // prompt positions per prefill pass
   int prefill_group_rows = 64;   // node rows per GEMM group of a prefill pass (the node tile)
   std::map<std::pair<int, int>, int> prefill_segs;   // (tiles of a launch, k-blocks) -> segments
 
@@ -969,12 +971,13 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
     if (cps < 1 || cps > 4 || kb < 32 || kb > 227) return DEX_EINVAL;
     h->gemm_ctas = h->n_sm * cps;
     h->gemm_smem = static_cast<size_t>(kb) * 1024;
-    // prompt positions per prefill pass and node rows per GEMM group of a pass: multiples of
-    // 16 in [16, 256], at most kMaxGroups groups per pass
+    // prompt positions per prefill pass (a multiple of 16 in [16, kPrefillRowsMax]) and node
+    // rows per GEMM group of a pass (a multiple of 16 in [16, 256]), at most kMaxGroups groups
     if (const char* pr = getenv("DEX_PREFILL_ROWS")) h->prefill_rows = atoi(pr);
     if (const char* pg = getenv("DEX_PREFILL_GROUP_ROWS")) h->prefill_group_rows = atoi(pg);
-    for (int v : {h->prefill_rows, h->prefill_group_rows})
-      if (v < 16 || v > 256 || (v & 15)) return DEX_EINVAL;
+    if (h->prefill_rows < 16 || h->prefill_rows > kPrefillRowsMax || (h->prefill_rows & 15) ||
+        h->prefill_group_rows < 16 || h->prefill_group_rows > 256 || (h->prefill_group_rows & 15))
+      return DEX_EINVAL;
     if ((h->prefill_rows + h->prefill_group_rows - 1) / h->prefill_group_rows > dex::kMaxGroups) return DEX_EINVAL;
   }
   h->lat.reset(new dex::Lattice(X, n_X, cfg->batch, cfg->decs != 0, cfg->max_branch));
@@ -983,9 +986,9 @@ int dex_init(const dex_model* m, const int32_t* X, int32_t n_X, const dex_decode
   h->mode.assign(cfg->batch, 0);
   h->n_done.assign(cfg->batch, 0);
   h->n_slots = h->lat->n_slots();
-  h->rows_cap = std::max(h->lat->max_round_nodes(), 256);
+  h->rows_cap = std::max(h->lat->max_round_nodes(), kPrefillRowsMax);
   h->max_groups = (cfg->max_ctx + dex::kAttnGroupPos - 1) / dex::kAttnGroupPos;
-  h->hrows = cfg->batch * h->n_slots + 256;
+  h->hrows = cfg->batch * h->n_slots + kPrefillRowsMax;
 
   const size_t B = cfg->batch, L = h->L, KVH = h->KVH, hd = h->hd, ctx = cfg->max_ctx, R = h->rows_cap;
   if (B * L * 2 * KVH * ctx >= (size_t(1) << 31)) return DEX_ECAPACITY;   // committed rows: 32-bit TMA rows
