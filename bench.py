@@ -158,6 +158,17 @@ def _gemm_traffic_ratio():
 MODEL_NAMES = {di.LLAMA7B: "llama2-7b-shaped", di.QWEN8B: "qwen3-8b-shaped", di.TINY: "tiny"}
 
 
+def prefill_flop(shape, batch, positions):
+    """FLOP of prefilling `positions` prompt positions of `batch` sequences: every linear
+    layer at 2 FLOP per weight and position (QKV, O, gate, up, down), plus causal attention
+    at 4 * head_dim FLOP per (query head, query, visible key) pair -- QK^T and PV, each
+    query seeing itself and every earlier position."""
+    qd, kvd = shape.n_heads * shape.head_dim, shape.n_kv_heads * shape.head_dim
+    layer_params = (qd + 2 * kvd) * shape.d_model + qd * shape.d_model + 3 * shape.d_ff * shape.d_model
+    pairs = positions * (positions + 1) / 2
+    return batch * shape.n_layers * (2.0 * layer_params * positions + 4.0 * qd * pairs)
+
+
 def _weight_gb(shape):
     qd, kvd = shape.n_heads * shape.head_dim, shape.n_kv_heads * shape.head_dim
     per_layer = (qd + 2 * kvd) * shape.d_model + qd * shape.d_model + 3 * shape.d_ff * shape.d_model
@@ -257,11 +268,7 @@ def run_gpu(args):
     pe1.synchronize()
     prefill_ms = pe0.elapsed_time(pe1)
     prefill_tok = B * (wl.prompt_len - 1)
-    qd, kvd = shape.n_heads * shape.head_dim, shape.n_kv_heads * shape.head_dim
-    layer_params = (qd + 2 * kvd) * shape.d_model + qd * shape.d_model + 3 * shape.d_ff * shape.d_model
-    # linear layers 2 * params per token, attention 4 * hd * H per (query, visible key)
-    P = wl.prompt_len - 1
-    prefill_flop = B * (2.0 * shape.n_layers * layer_params * P + 4.0 * shape.n_layers * qd * P * (P + 1) / 2)
+    pf_flop = prefill_flop(shape, B, wl.prompt_len - 1)
     value = replica_throughput(args.steps * B * T, ms / 1000.0, world, dev)
     ms = max_over_ranks(ms)
     ms_per_step = ms / args.steps
@@ -338,8 +345,8 @@ def run_gpu(args):
         "e2e": e2e,
         "prefill": {"tokens": prefill_tok, "ms": round(prefill_ms, 2),
                     "tokens_per_s": round(prefill_tok / (prefill_ms / 1e3), 1) if prefill_ms > 0 else None,
-                    "tflops": round(prefill_flop / (prefill_ms / 1e3) / 1e12, 1) if prefill_ms > 0 else None,
-                    "frac_of_bf16_peak": round(prefill_flop / (prefill_ms / 1e3) / 1e12 / bf16, 4)
+                    "tflops": round(pf_flop / (prefill_ms / 1e3) / 1e12, 1) if prefill_ms > 0 else None,
+                    "frac_of_bf16_peak": round(pf_flop / (prefill_ms / 1e3) / 1e12 / bf16, 4)
                     if prefill_ms > 0 else None,
                     "note": "support path (not the metric): prompt positions 0..P-2 of every sequence, "
                             "linear layers at 2 FLOP per weight and token plus causal attention"},

@@ -106,3 +106,21 @@ def test_one_core_block_restores_affinity():
     with bench._OneCore():
         assert len(os.sched_getaffinity(0)) == 1
     assert os.sched_getaffinity(0) == before
+
+
+def test_prefill_flop_count():
+    """The bench's prefill FLOP count, checked by brute force on a tiny shape: every linear
+    layer's 2 FLOP per weight and position, and 4 * head_dim FLOP per (query head, query,
+    visible key) pair counted one pair at a time."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import dex_inputs as di
+    shape = di.ModelShape(n_layers=3, d_model=256, n_heads=4, n_kv_heads=2, head_dim=64, d_ff=512,
+                          vocab=1000, tied_head=False)
+    B, P = 2, 7
+    weights = (4 * 64 + 2 * 2 * 64) * 256 + 4 * 64 * 256 + 3 * 512 * 256   # QKV, O, gate/up/down
+    linear = 2 * weights * P
+    attn = sum(4 * 64 * 4 for q in range(P) for k in range(q + 1))
+    assert bench.prefill_flop(shape, B, P) == B * 3 * (linear + attn)
+    # the 7B-shaped prompt of the benchmark: about 6.9 TFLOP (the weights dominate)
+    assert 6.5e12 < bench.prefill_flop(di.LLAMA7B, 1, 511) < 7.2e12
