@@ -142,3 +142,18 @@ def test_out_of_range_partial_reports_erange():
         assert dec.generate()[0] == want
     finally:
         dec.close()
+
+
+def test_prefill_fallback_for_three_query_heads_per_kv_head():
+    """Twelve query heads on four KV heads: 128 is not a multiple of 3, so prefill passes
+    take the lattice attention kernel (items of five rows, fifteen queries per pass); the
+    decode is lossless and matches the oracle."""
+    dexlib = require_gpu()
+    shape = di.ModelShape(n_layers=4, d_model=768, n_heads=12, n_kv_heads=4, head_dim=64, d_ff=2048,
+                          vocab=4096, tied_head=False)
+    X, T = [1, 2, 3, 4], 10
+    w = di.gen_weights(shape, 0.3, seed=0, device="cuda")
+    prompt = di.gen_prompts(shape, 1, 150)[0].tolist()
+    y, z = _dex_and_ar(dexlib, shape, w, X, prompt, T)
+    ref = odex.ar_generate(oracle_model(shape, w), prompt, T, force=y)
+    check_logits_and_tokens(z, y, ref)
