@@ -16,9 +16,10 @@
 // Persistent, fixed-segment split-K: every 128-row output tile's k range is cut into a
 // fixed number of segments S that depends only on the weight shape (and the handle's
 // grid), never on the nodes or on how many weight matrices share the launch.  Each
-// segment is accumulated from zero; a tile's segments are summed in segment order by
-// the last CTA to finish one of them.  A node's result is therefore bit-identical in any
-// batch and in any grouped launch.  The (group, tile, segment) units of a launch are
+// segment is accumulated from zero; the last CTA to finish one of a tile's segments sums
+// them -- fp32 partial tiles in segment order, or (decoder layers of small lattices) the
+// exact 2^-32 fixed-point tile sum every segment added at L2 -- and runs the epilogue.  A
+// node's result is therefore bit-identical in any batch and in any grouped launch.  The (group, tile, segment) units of a launch are
 // dealt out as contiguous ranges over a fixed grid of resident CTAs, so a launch with
 // several weight matrices still runs in one wave; each CTA streams its units' k-blocks
 // through a deep TMA ring without pausing.  Two TMEM accumulators alternate between
