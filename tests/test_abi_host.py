@@ -149,3 +149,19 @@ def test_lattice_batch_of_sequences_is_independent():
                                                                  (1, 0, 1), (1, 1, 1), (1, 2, 1)]
     # the position child of the root takes the root's candidate as input token
     assert [p["token"] for p in plan if p["stage"] == 0] == [1, 2, 3]
+
+
+def test_error_codes_match_the_header():
+    """The binding's DEX_* constants equal include/dex.h's enum, and every code has its own
+    message from dex_strerror."""
+    src = open(os.path.join(ROOT, "include", "dex.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    codes = {name: int(val) for name, val in re.findall(r"\b(DEX_[A-Z]+)\s*=\s*(-?\d+)", src)}
+    assert {"DEX_OK", "DEX_EINVAL", "DEX_ENOMEM", "DEX_ECUDA", "DEX_ECAPACITY", "DEX_ETIMEOUT", "DEX_ESTATE",
+            "DEX_ENODEV", "DEX_ERANGE"} <= set(codes)
+    for name, val in codes.items():
+        assert getattr(dexlib, name) == val, name
+    L = _lib()
+    msgs = {L.dex_strerror(v) for v in codes.values()}
+    assert len(msgs) == len(codes) and b"unknown error" not in msgs
+    assert L.dex_strerror(-99) == b"unknown error"
